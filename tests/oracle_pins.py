@@ -1,0 +1,258 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+Every ``pin_*`` function takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
+oracle disagrees with the fact it checks.  ``tests/test_oracle_pins.py`` runs them on the real
+oracle; ``tests/test_oracle_mutations.py`` runs them on deliberately broken copies of the
+oracle to show that each plausible mistake is caught by at least one pin.
+
+Sources of the facts (page titles and sections):
+  * Paper-Notes "ZeroS: Zero-Sum Linear Attention for Efficient Transformers":
+      - "current pain points": two tokens, v_1 - v_2 unreachable with convex weights;
+      - method details / key design: zero-sum weights (sum_i w_{t,i} = 0), radial-angular
+        decoupling with cos(theta) = q_hat k_hat^T and its RoPE form q_hat R_{t-i} k_hat^T,
+        deviation logits with the prior-smoothed cumulative mean, linear-time prefix scan;
+      - highlights: Lemma 3.4 norm bound.
+  * ai.info AI summary, "Main Findings": Lemma 3.4, ||sum_i w_{t,i} v_i|| <= B t max_i|w_{t,i}|.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+from scipy.special import softmax
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "two_token.json")
+
+
+def rand_problem(seed, B=1, H=2, N=48, d=8, tau_range=1.0, gate_std=1.0):
+    rng = np.random.default_rng(seed)
+    q, k, v, u = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    g1 = rng.standard_normal((B, H, N)) * gate_std
+    gh = rng.standard_normal((B, H, N)) * gate_std
+    mu = rng.standard_normal((H, d))
+    tau = rng.uniform(-tau_range, tau_range, H)
+    return dict(q=q, k=k, v=v, u=u, g1=g1, gh=gh, mu=mu, tau=tau)
+
+
+def relerr(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+def _args(p):
+    return (p["q"], p["k"], p["v"], p["u"], p["g1"], p["gh"], p["mu"], p["tau"])
+
+
+# ---------------------------------------------------------------------------------------------
+def pin_golden_two_token(orc):
+    """Hand-derived two-token cases (logits and outputs) from tests/golden/two_token.json."""
+    with open(GOLDEN) as f:
+        doc = json.load(f)
+    for c in doc["cases"]:
+        d = c["d"]
+        shape4 = (1, 1, 2, d)
+        p = dict(q=np.array(c["q"]).reshape(shape4), k=np.array(c["k"]).reshape(shape4),
+                 v=np.array(c["v"]).reshape(shape4), u=np.array(c["u"]).reshape(shape4),
+                 g1=np.array(c["g1"]).reshape(1, 1, 2), gh=np.array(c["gh"]).reshape(1, 1, 2),
+                 mu=np.array(c["mu"]).reshape(1, d), tau=np.array([c["tau"]]))
+        exp_o = np.array(c["expected_o"]).reshape(shape4)
+        out, s, _, _ = orc.forward(*_args(p), causal=True, rope=c["rope"], debug=True)
+        assert np.allclose(s.reshape(-1), c["expected_s"], rtol=0, atol=1e-14), c["name"]
+        assert np.allclose(out, exp_o, rtol=0, atol=1e-14), c["name"]
+        ob, _, wm = orc.brute(*_args(p), causal=True, rope=c["rope"])
+        assert np.allclose(ob, exp_o, rtol=0, atol=1e-14), c["name"]
+        assert abs(wm.reshape(-1)[1] - abs(c["expected_w21"])) < 1e-14, c["name"]
+
+
+def pin_brute_vs_recurrent(orc):
+    """The five-state recurrence equals the O(N^2) definition (exact algebra, fp64 rounding)."""
+    for seed, (N, d) in enumerate([(1, 4), (2, 6), (33, 8), (64, 16)]):
+        p = rand_problem(100 + seed, N=N, d=d)
+        for causal in (True, False):
+            for rope in (False, True):
+                o = orc.forward(*_args(p), causal=causal, rope=rope)
+                ob, _, _ = orc.brute(*_args(p), causal=causal, rope=rope)
+                err = np.abs(o - ob).max() / max(np.abs(ob).max(), 1.0)
+                assert err < 1e-12, (N, d, causal, rope, err)
+
+
+def pin_zero_sum(orc):
+    """sum_i w_{t,i} = 0 for every t, to 1e-12 (zero-order removal), causal and encoder."""
+    p = rand_problem(7, N=256, d=32, H=1)
+    for causal in (True, False):
+        _, ws, wm = orc.brute(*_args(p), causal=causal)
+        assert np.abs(ws).max() < 1e-12, np.abs(ws).max()
+        assert wm.max() > 1e-6  # weights are not trivially zero
+
+
+def pin_first_output_zero(orc):
+    """o_1 = 0: one token has delta = 0 and softmax = 1 = 1/t, so w_{1,1} = 0."""
+    p = rand_problem(8, N=16, d=8)
+    ob, _, _ = orc.brute(*_args(p), causal=True)
+    assert np.abs(ob[:, :, 0]).max() == 0.0
+    o = orc.forward(*_args(p), causal=True)
+    assert np.abs(o[:, :, 0]).max() <= 1e-12 * np.abs(o).max()
+
+
+def pin_lemma_3_4(orc):
+    """||o_t|| <= max_i ||v_i|| * t * max_i |w_{t,i}| (Lemma 3.4; |cos theta| <= 1)."""
+    p = rand_problem(9, N=96, d=8, H=2)
+    for causal in (True, False):
+        o = orc.forward(*_args(p), causal=causal, rope=True)
+        _, _, wm = orc.brute(*_args(p), causal=causal, rope=True)
+        N = o.shape[2]
+        vnorm = np.linalg.norm(p["v"], axis=-1)
+        for b in range(o.shape[0]):
+            for h in range(o.shape[1]):
+                for t in range(N):
+                    last = t if causal else N - 1
+                    bound = vnorm[b, h, : last + 1].max() * (last + 1) * wm[b, h, t]
+                    assert np.linalg.norm(o[b, h, t]) <= bound * (1 + 1e-12) + 1e-15
+
+
+def pin_two_token_collinear(orc):
+    """With k_2 = lambda k_1 (no rope), o_2 is a signed multiple of v_1 - v_2."""
+    rng = np.random.default_rng(10)
+    for _ in range(5):
+        p = rand_problem(int(rng.integers(1 << 30)), N=2, d=6, H=1)
+        p["k"][:, :, 1] = p["k"][:, :, 0] * rng.uniform(0.1, 3.0)
+        o = orc.forward(*_args(p), causal=True)
+        dv = (p["v"][0, 0, 0] - p["v"][0, 0, 1])
+        o2 = o[0, 0, 1]
+        resid = o2 - (o2 @ dv) / (dv @ dv) * dv
+        assert np.linalg.norm(resid) <= 1e-13 * max(np.linalg.norm(o2), 1e-300)
+        assert np.linalg.norm(o2) > 0
+
+
+def pin_constant_logits(orc):
+    """All u_j = mu = c 1: every logit is equal, delta = eps = 0, so o = 0."""
+    p = rand_problem(11, N=40, d=8)
+    c = 0.37
+    p["u"][:] = c
+    p["mu"][:] = c
+    for causal in (True, False):
+        o = orc.forward(*_args(p), causal=causal, rope=True)
+        assert np.abs(o).max() < 1e-13
+
+
+def _cos_matrix(p, b, h):
+    qn = p["q"][b, h] / np.linalg.norm(p["q"][b, h], axis=-1, keepdims=True)
+    kn = p["k"][b, h] / np.linalg.norm(p["k"][b, h], axis=-1, keepdims=True)
+    return qn @ kn.T
+
+
+def pin_equal_gates_softmax(orc):
+    """sig1 = sigh = sig: w = sig (softmax - 1/t), i.e. softmax attention over the logits
+    (scipy's textbook softmax) minus the uniform average, times cos(theta)."""
+    p = rand_problem(12, N=50, d=8, H=2)
+    p["gh"] = p["g1"].copy()
+    for causal in (True, False):
+        o, s, _, _ = orc.forward(*_args(p), causal=causal, debug=True)
+        N = o.shape[2]
+        for b in range(o.shape[0]):
+            for h in range(o.shape[1]):
+                C = _cos_matrix(p, b, h)
+                for t in range(N):
+                    last = t if causal else N - 1
+                    sm = softmax(s[b, h, : last + 1])
+                    w = (sm - 1.0 / (last + 1)) / (1 + np.exp(-p["g1"][b, h, t]))
+                    ref = (w * C[t, : last + 1]) @ p["v"][b, h, : last + 1]
+                    assert np.allclose(o[b, h, t], ref, rtol=0, atol=1e-13)
+
+
+def _rope_rows(x, base):
+    """Standard rotary embedding (Su et al., half-split pairs), row n at position n."""
+    n, d = x.shape
+    half = d // 2
+    theta = base ** (-2.0 * np.arange(half) / d)
+    ang = np.arange(n)[:, None] * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    return np.concatenate([x[:, :half] * c - x[:, half:] * s, x[:, :half] * s + x[:, half:] * c],
+                          axis=1)
+
+
+def pin_equal_gates_softmax_rope(orc):
+    """As pin_equal_gates_softmax, with cos(theta') = q_hat R_{t-i} k_hat^T from a textbook
+    rotary embedding applied to the unit vectors at absolute positions."""
+    p = rand_problem(19, N=40, d=16, H=1)
+    p["gh"] = p["g1"].copy()
+    base = 500.0
+    o, s, _, _ = orc.forward(*_args(p), causal=True, rope=True, rope_base=base, debug=True)
+    qn = p["q"][0, 0] / np.linalg.norm(p["q"][0, 0], axis=-1, keepdims=True)
+    kn = p["k"][0, 0] / np.linalg.norm(p["k"][0, 0], axis=-1, keepdims=True)
+    C = _rope_rows(qn, base) @ _rope_rows(kn, base).T
+    for t in range(o.shape[2]):
+        w = (softmax(s[0, 0, : t + 1]) - 1.0 / (t + 1)) / (1 + np.exp(-p["g1"][0, 0, t]))
+        ref = (w * C[t, : t + 1]) @ p["v"][0, 0, : t + 1]
+        assert np.allclose(o[0, 0, t], ref, rtol=0, atol=1e-13)
+
+
+def pin_linear_gate_limit(orc):
+    """sigh -> 0 (gh = -40): o_t = (sig1/t) sum_i (s_i - mean s) cos(theta) v_i."""
+    p = rand_problem(13, N=40, d=8, H=1)
+    p["gh"][:] = -40.0
+    o, s, _, _ = orc.forward(*_args(p), causal=True, debug=True)
+    C = _cos_matrix(p, 0, 0)
+    for t in range(o.shape[2]):
+        st = s[0, 0, : t + 1]
+        w = (st - st.mean()) / (t + 1) / (1 + np.exp(-p["g1"][0, 0, t]))
+        ref = (w * C[t, : t + 1]) @ p["v"][0, 0, : t + 1]
+        assert np.allclose(o[0, 0, t], ref, rtol=0, atol=1e-13)
+
+
+def pin_rope_relative(orc):
+    """Only relative positions matter: shifting every rotary position leaves o unchanged."""
+    p = rand_problem(14, N=30, d=8)
+    for causal in (True, False):
+        a = orc.forward(*_args(p), causal=causal, rope=True, pos0=0.0)
+        b = orc.forward(*_args(p), causal=causal, rope=True, pos0=1234.0)
+        assert relerr(a, b) < 1e-10
+
+
+def pin_scale_and_linearity(orc):
+    """q and k enter only through their directions; o is linear in v."""
+    p = rand_problem(15, N=24, d=8)
+    base = orc.forward(*_args(p), causal=True, rope=True)
+    p2 = dict(p)
+    p2["q"] = p["q"] * 3.5
+    p2["k"] = p["k"] * np.linspace(0.2, 4.0, p["k"].shape[2])[None, None, :, None]
+    assert relerr(orc.forward(*_args(p2), causal=True, rope=True), base) < 1e-12
+    rng = np.random.default_rng(16)
+    v2 = rng.standard_normal(p["v"].shape)
+    p3 = dict(p)
+    p3["v"] = 2.0 * p["v"] - v2
+    p4 = dict(p)
+    p4["v"] = v2
+    comb = orc.forward(*_args(p3), causal=True, rope=True)
+    ref = 2.0 * base - orc.forward(*_args(p4), causal=True, rope=True)
+    assert relerr(comb, ref) < 1e-12
+
+
+def pin_prior_limits(orc):
+    """tau -> +inf gives ubar_i = mu; tau -> -inf gives the plain cumulative mean."""
+    p = rand_problem(17, N=20, d=8, H=1)
+    d = p["u"].shape[-1]
+    u = p["u"][0, 0]
+    p["tau"][:] = 40.0
+    _, s, _, _ = orc.forward(*_args(p), causal=True, debug=True)
+    ref = -(u @ p["mu"][0]) / np.sqrt(d)
+    assert np.allclose(s[0, 0], ref, rtol=1e-12, atol=1e-12)
+    p["tau"][:] = -40.0
+    _, s, _, _ = orc.forward(*_args(p), causal=True, debug=True)
+    cmean = np.cumsum(u, axis=0) / np.arange(1, u.shape[0] + 1)[:, None]
+    ref = -np.einsum("ia,ia->i", u, cmean) / np.sqrt(d)
+    assert np.allclose(s[0, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_prefix_sums(orc):
+    """E_t and P_t reported by the recurrence are the prefix sums of e^{s_i} and s_i."""
+    p = rand_problem(18, N=30, d=8)
+    _, s, E, P = orc.forward(*_args(p), causal=True, debug=True)
+    assert np.allclose(E, np.cumsum(np.exp(s), axis=-1), rtol=1e-13)
+    assert np.allclose(P, np.cumsum(s, axis=-1), rtol=1e-13, atol=1e-13)
+
+
+ALL_PINS = [pin_golden_two_token, pin_brute_vs_recurrent, pin_zero_sum, pin_first_output_zero,
+            pin_lemma_3_4, pin_two_token_collinear, pin_constant_logits, pin_equal_gates_softmax,
+            pin_equal_gates_softmax_rope, pin_linear_gate_limit, pin_rope_relative, pin_scale_and_linearity, pin_prior_limits,
+            pin_prefix_sums]

@@ -1,0 +1,59 @@
+"""Planted mistakes in the oracle must each be caught by at least one pin.
+
+Each case copies the oracle's C++ source, applies one textual mutation (a dropped term, a wrong
+sign or index, a transposed operand ...), compiles the copy on the CPU and runs the pin suite on
+it.  The real oracle is never modified.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "zeros_oracle.cpp")
+
+MUTATIONS = [
+    ("sigmoid sign", "1.0 / (1.0 + std::exp(-x))", "1.0 / (1.0 + std::exp(x))"),
+    ("no normalisation", "y[a] = x[a] / n;", "y[a] = x[a];"),
+    ("rotation sign", "x[a + half] = xa * s + xb * c;", "x[a + half] = -xa * s + xb * c;"),
+    ("rotary frequency", "std::pow(base, -2.0 * a / d)", "std::pow(base, -1.0 * a / d)"),
+    ("prior mean excludes token i",
+     "        S[a] += ui[a];\n        ubar[a] = (et * mu[a] + S[a]) / (et + (i + 1));",
+     "        ubar[a] = (et * mu[a] + S[a]) / (et + (i + 1));\n        S[a] += ui[a];"),
+    ("prior weight", "ubar[a] = (et * mu[a] + S[a]) / (et + (i + 1));",
+     "ubar[a] = (mu[a] + S[a]) / (et + (i + 1));"),
+    ("logit scale", "s[i] = -dot / std::sqrt((double)d);\n  }\n}", "s[i] = -dot / d;\n  }\n}"),
+    ("gamma drops sig_h/t",
+     "const double gamma = -(sig1 - sigh) * P / (tcount * tcount) - sigh / tcount;",
+     "const double gamma = -(sig1 - sigh) * P / (tcount * tcount);"),
+    ("beta sign", "const double beta = (sig1 - sigh) / tcount;",
+     "const double beta = (sigh - sig1) / tcount;"),
+    ("transposed F update", "F[(size_t)a * d + j] += es * kv;", "F[(size_t)j * d + a] += es * kv;"),
+    ("brute eps drops delta", "const double eps = soft - 1.0 / tc - delta / tc;",
+     "const double eps = soft - 1.0 / tc;"),
+    ("brute delta sign", "const double delta = s[i] - P / tc;",
+     "const double delta = P / tc - s[i];"),
+    ("encoder prior uses N+1", "ubar[a] = (et * mu[a] + S[a]) / (et + N);",
+     "ubar[a] = (et * mu[a] + S[a]) / (et + N + 1);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutation_is_caught(name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    mutated = src.replace(old, new, 1)
+    with tempfile.TemporaryDirectory() as tmp:
+        cpp = os.path.join(tmp, "mut.cpp")
+        with open(cpp, "w") as f:
+            f.write(mutated)
+        orc = oracle.Oracle(oracle.build(force=True, src=cpp, so=os.path.join(tmp, "mut.so")))
+        caught = []
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin(orc)
+            except AssertionError:
+                caught.append(pin.__name__)
+        assert caught, f"no pin catches the planted mistake: {name}"
