@@ -1,0 +1,417 @@
+"""Benchmark of the ZeroS causal forward: B8 H8 N4096 d64, bf16, RoPE, one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload causal|encoder|long|decode] [--path auto|simt|chunk]
+
+One step = one pass of the whole hot path (logits, prefix scans, zero-sum weights, angular
+factor, state scan and readout: one zeros_fwd call) over one batch of device-resident
+synthetic inputs.  Each step is timed with CUDA events on the launching stream; L2 is flushed
+(a 256 MB write) before every step, outside the timed events.  Prints ONE JSON line (rank 0).
+
+N > 1 (torchrun): every rank runs its own copy of the workload on its own GPU (the B x H
+sequences are independent: weak scaling, no data-path collective); value = tokens of all
+ranks / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import zeros_inputs as zi  # noqa: E402
+
+METRIC = "ZeroS fwd tokens/s (B8·H8·N4096·d64 bf16) and % of roofline on 1 GB300"
+WORKLOADS = {
+    "causal": zi.CAUSAL_ROPE_B8H8N4096D64,
+    "encoder": zi.ENCODER_VIT_B256H3N197D64,
+    "long": zi.LONG_ROPE_B2H16N65536D128,
+    "decode": zi.DECODE_B256H32D128,
+}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def algorithmic_bytes(w: zi.Workload) -> int:
+    """Bytes the method must move per forward: read q, k, v, u and the two gate logits, write
+    out (per token-head 4 d b_in + 8 + d b_out)."""
+    b = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * w.N * (4 * w.d * b + 8 + w.d * b)
+
+
+def decode_bytes(w: zi.Workload) -> int:
+    """Bytes one decode step must move: every sequence's three fp32 d x d states read and
+    written, plus its running sum and scalars, plus the token (q, k, v, u, gates) and out."""
+    b = 2 if w.dtype == "bf16" else 4
+    per = 2 * (12 * w.d * w.d + 4 * w.d + 16) + 4 * w.d * b + 8 + w.d * b
+    return w.B * w.H * per
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+def oracle_rate(w: zi.Workload, inp_cpu: dict, seqs: int, tokens: int, nthreads: int):
+    """Run the fp64 oracle on `seqs` sequences x `tokens` tokens; return (tokens/s, seconds,
+    threads).  Throughput is counted in the metric's token unit (one (b, n) position carries
+    H heads, so seqs*tokens token-heads count as seqs*tokens/H tokens)."""
+    import oracle
+    pick = [(i // w.H, i % w.H) for i in range(seqs)]
+    sel = lambda t: torch.stack([t[b, h, :tokens] for b, h in pick])[None]  # noqa: E731
+    q, k, v, u = (sel(inp_cpu[n]) for n in ("q", "k", "v", "u"))
+    g1, gh = sel(inp_cpu["g1"]), sel(inp_cpu["gh"])
+    # one head's prior for the whole sample (the cost does not depend on which head)
+    mu = inp_cpu["mu"][:1].repeat(seqs, 1)
+    tau = inp_cpu["tau"][:1].repeat(seqs)
+    args = [x.double().numpy() for x in (q[0][None], k[0][None], v[0][None], u[0][None])]
+    q64, k64, v64, u64 = (a.reshape(1, seqs, tokens, w.d) for a in args)
+    g164 = g1.double().numpy().reshape(1, seqs, tokens)
+    gh64 = gh.double().numpy().reshape(1, seqs, tokens)
+    t0 = time.perf_counter()
+    oracle.forward(q64, k64, v64, u64, g164, gh64, mu.double().numpy(), tau.double().numpy(),
+                   causal=w.causal, rope=w.rope, rope_base=w.rope_base, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    token_heads = seqs * tokens
+    return token_heads / w.H / dt, dt, min(nthreads, seqs)
+
+
+def reference_arm(args, w: zi.Workload):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cores = oracle.threads()
+    seqs = min(cores, w.B * w.H)
+    tokens = min(w.N, 512)
+    inp = zi.make(w, "cpu", N=tokens)
+    for _ in range(args.warmup):
+        oracle_rate(w, inp, seqs, tokens, cores)
+    times = []
+    for _ in range(args.steps):
+        _, dt, used = oracle_rate(w, inp, seqs, tokens, cores)
+        times.append(dt)
+    sec = sum(times) / len(times)
+    value = seqs * tokens / w.H / sec
+    sample = (f"{seqs} of the {w.B * w.H} (b,h) sequences x first {tokens} tokens of "
+              f"{w.name}, fp64 recurrent oracle, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------------------------
+def ours_forward(args, w: zi.Workload):
+    world, rank, local = dist_setup()
+    import zero_sum_prefix_gb300 as zs
+    zs.load()
+    dev = torch.device("cuda", local)
+    inp = zi.make(w, dev)
+    out = torch.empty_like(inp["q"])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        zs.fwd(inp["q"], inp["k"], inp["v"], inp["u"], inp["g1"], inp["gh"], inp["mu"],
+               inp["tau"], causal=w.causal, rope=w.rope, rope_base=w.rope_base, out=out,
+               path=args.path)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = zs.kernel_launches()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = zs.kernel_launches() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(sum(per) / len(per), world)
+    tokens = w.B * w.N
+    value = tokens * world / (ms / 1e3)
+
+    hbm, peak_kind = peaks()
+    alg = algorithmic_bytes(w)
+    achieved = alg / (ms / 1e3) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    names = ("q", "k", "v", "u", "g1", "gh", "mu", "tau")
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(inp[n]) for n in names}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n in names:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        o = zs.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["u"], dev_in["g1"],
+                   dev_in["gh"], dev_in["mu"], dev_in["tau"], causal=w.causal, rope=w.rope,
+                   rope_base=w.rope_base, out=out, path=args.path)
+        host_out.copy_(o, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = oracle.threads()
+        inp_cpu = {n: t.cpu() for n, t in inp.items()}
+        seqs = min(w.B * w.H, max(cores, 1) * 4)
+        tokens = w.N
+        rate, dt, used = oracle_rate(w, inp_cpu, seqs, tokens, cores)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": used, "kind": "oracle",
+               "sample": f"{seqs} of {w.B * w.H} (b,h) sequences x all {tokens} tokens, fp64 "
+                         f"recurrent oracle ({dt:.1f} s wall)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "rope": w.rope, "rope_base": w.rope_base,
+                       "path": args.path, "parallelism": f"replicas x{world}",
+                       "l2": "flushed before every step (256 MB write, outside the events)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": alg},
+            "cpu_baseline": cpu,
+            "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+
+
+def ours_decode(args, w: zi.Workload):
+    """Recurrent decode: prefill 8192 tokens (zeros_fwd_ex final_state), then time decode
+    steps; one step advances all B x H sequences by one token."""
+    world, rank, local = dist_setup()
+    import zero_sum_prefix_gb300 as zs
+    zs.load()
+    dev = torch.device("cuda", local)
+    st = torch.empty(zs.state_bytes(w.B, w.H, w.d), dtype=torch.uint8, device=dev)
+    # prefill in batch slices to bound the memory held by inputs
+    slice_b = 16
+    mu = tau = None
+    for b0 in range(0, w.B, slice_b):
+        part = zi.make(w.with_(seed=w.seed * 131 + b0), dev, B=min(slice_b, w.B - b0))
+        if mu is None:
+            mu, tau = part["mu"], part["tau"]
+        nb = part["q"].shape[0]
+        sub = torch.empty(zs.state_bytes(nb, w.H, w.d), dtype=torch.uint8, device=dev)
+        zs.fwd(part["q"], part["k"], part["v"], part["u"], part["g1"], part["gh"], mu, tau,
+               causal=True, rope=w.rope, rope_base=w.rope_base, final_state=sub)
+        rb = zs.record_bytes(w.d)
+        st[256 + b0 * w.H * rb: 256 + (b0 + nb) * w.H * rb].copy_(sub[256:])
+        if b0 == 0:
+            st[:256].copy_(sub[:256])
+        del part, sub
+    # the header records B; rewrite it for the full batch
+    hdr = st[:256].view(torch.int32)
+    hdr[2] = w.B
+    steps_tok = [zi.decode_tokens(w, i, dev) for i in range(8)]
+    out = torch.empty((w.B, w.H, w.d), dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        tk = steps_tok[i % len(steps_tok)]
+        zs.decode_step(st, tk["q"], tk["k"], tk["v"], tk["u"], tk["g1"], tk["gh"], out=out)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    l0 = zs.kernel_launches()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = zs.kernel_launches() - l0
+    clk = clocks.stop()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after decode")
+    per = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms = max_over_ranks(statistics.median(per), world)
+    hbm, kind = peaks()
+    alg = decode_bytes(w)
+    achieved = alg / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "ZeroS decode step tokens/s (B256 H32 d128, fp32 state, after 8192-token "
+                      "prefill)", "value": w.B * world / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d,
+                       "l2": "state (3.2 GB) larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None, "peak_source": kind,
+                         "algorithmic_bytes_per_launch": alg},
+            "gpu_launches": launches, "clocks": clk}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "chunk"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+    elif args.workload == "decode":
+        ours_decode(args, w)
+    else:
+        ours_forward(args, w)
+
+
+if __name__ == "__main__":
+    main()

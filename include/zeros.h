@@ -1,0 +1,150 @@
+/*
+ * zeros.h - C ABI of the GB300 (sm_103a) hot path of ZeroS, zero-sum linear attention.
+ *
+ * What is computed (Paper-Notes "ZeroS: Zero-Sum Linear Attention for Efficient Transformers",
+ * method details):
+ *   deviation logits   s_i = -(1/sqrt d) u_i . ubar_i,
+ *                      ubar_i = (e^tau mu + sum_{j<=i} u_j) / (e^tau + i)   ("deviation logits")
+ *   zero-sum weights   w_{t,i} = sig1_t delta_{t,i}/t + sigh_t eps_{t,i}, sig = sigmoid(gate logit)
+ *                      ("zero-order removal and zero-sum weights")
+ *   angular factor     cos theta_{t,i} = q_hat_t R_{t-i} k_hat_i^T         ("radial-angular
+ *                      decoupling", with RoPE)
+ *   output             o_t = sum_i w_{t,i} cos theta_{t,i} v_i
+ *                          = q_hat_t (alpha_t F_t + beta_t G_t + gamma_t H_t)  ("linear-time
+ *                      prefix scan": E = sum e^s, P = sum s, F = sum e^s k_hat^T v,
+ *                      G = sum s k_hat^T v, H = sum k_hat^T v)
+ * with delta_{t,i} = s_i - P_t/t, eps_{t,i} = e^{s_i}/E_t - 1/t - delta_{t,i}/t, hence
+ * alpha_t = sigh_t/E_t, beta_t = (sig1_t - sigh_t)/t, gamma_t = -(sig1_t - sigh_t) P_t/t^2 - sigh_t/t.
+ * Causal (decoder) mode sums over i <= t; encoder mode sums over every token with t := N and
+ * the full-sequence prior mean (page section "training strategy": both modes exist).
+ * RoPE: half-split pairs (a, a + d/2), theta_a = base^(-2a/d), token t at position t - 1.
+ *
+ * Layouts (row-major, contiguous, all pointers are DEVICE pointers owned by the caller):
+ *   q, k, v, u, out : [B, H, N, d]  bf16 (zeros_fwd) or the dtype given to zeros_fwd_ex
+ *   g1, gh          : [B, H, N]     fp32 gate logits (sig1 = sigmoid(g1), sigh = sigmoid(gh))
+ *   mu              : [H, d]        fp32 per-head prior mean
+ *   tau             : [H]           fp32 per-head prior log-weight
+ * Supported head dimensions: d in {32, 64, 128}.  Every pointer must be 16-byte aligned.
+ *
+ * Errors.  Argument checks run on the host before anything is launched and return a nonzero
+ * zeros_status without touching the GPU.  Conditions found on the device (a non-finite logit,
+ * an exponent out of fp32 range, a bounded wait that gave up) are recorded in a per-device
+ * status word; zeros_get_status() synchronises the stream and returns and clears it.  Outputs
+ * are unspecified when a call or the status word reports an error.  All launches are
+ * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ * Memory.  The library allocates nothing per call once warm: it keeps one lazily created,
+ * per-device workspace (rotary tables) that only grows; it is released at process exit.
+ */
+#ifndef ZEROS_H
+#define ZEROS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZEROS_OK = 0,
+  ZEROS_ERR_INVALID = 1,     /* bad argument: null pointer, negative size, misalignment     */
+  ZEROS_ERR_UNSUPPORTED = 2, /* well-formed but not supported (d not in {32,64,128}, ...)   */
+  ZEROS_ERR_RANGE = 3,       /* device: non-finite logit or exponent outside fp32 range     */
+  ZEROS_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up                              */
+  ZEROS_ERR_CUDA = 5         /* a CUDA runtime call failed (see zeros_last_error_message)   */
+} zeros_status;
+
+typedef enum { ZEROS_BF16 = 0, ZEROS_F32 = 1 } zeros_dtype;
+
+/* Implementation selector for zeros_fwd_ex (all produce the same result up to rounding). */
+typedef enum {
+  ZEROS_PATH_AUTO = 0,  /* chunked tensor-core scan where available, else the SIMT scan      */
+  ZEROS_PATH_SIMT = 1,  /* token-sequential CUDA-core scan (fp32 and bf16 inputs)            */
+  ZEROS_PATH_CHUNK = 2  /* chunked tcgen05/TMEM scan (bf16 inputs, causal)                   */
+} zeros_path;
+
+/*
+ * Forward pass over [B, H, N, d] bf16 inputs, bf16 output, rotary base 10000.
+ * causal = 1: decoder mode (prefix sums); causal = 0: encoder mode (full-sequence sums).
+ * rope   = 1: rotary positions in the angular factor.
+ * B, H or N equal to 0 is a valid empty call (returns ZEROS_OK, launches nothing).
+ */
+int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
+              const float* gh, const float* mu, const float* tau, void* out, int B, int H, int N,
+              int d, int causal, int rope, void* stream);
+
+/*
+ * zeros_fwd with every option.
+ *   dtype       : ZEROS_BF16 or ZEROS_F32 for q, k, v, u and out.
+ *   rope_base   : rotary base (> 0) when rope = 1.
+ *   path        : a zeros_path value.
+ *   final_state : nullable; causal only.  A state blob of zeros_state_bytes(B, H, d) bytes that
+ *                 receives the recurrent state after the N tokens (prefill for
+ *                 zeros_decode_step).  It records dtype, rope and rope_base.
+ *   dbg_s, dbg_E, dbg_P, dbg_m : nullable fp32 [B, H, N].  Per token: the logit s_t, the
+ *                 scaled prefix sum E_t e^{-m_t}, the prefix sum P_t and the running maximum
+ *                 m_t = max_{i<=t} s_i (encoder: the full-sequence values).  These four are
+ *                 bit-identical to those zeros_decode_step_ex reports for the same tokens.
+ */
+int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* mu, const float* tau, void* out, int B, int H,
+                 int N, int d, int causal, int rope, int dtype, float rope_base, int path,
+                 void* final_state, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
+                 void* stream);
+
+/*
+ * Recurrent state ("the state is the checkpoint").  Size in bytes of the blob for B x H
+ * sequences of head dimension d (0 for unsupported d).  Layout: a 256-byte header
+ * {magic "ZSP1", version, B, H, d, dtype, rope, rope_base} followed by B*H records of
+ * zeros_state_record_bytes(d) bytes; record (b, h) at index b*H + h holds
+ *   int32 t (tokens seen), fp32 m (running max of s), fp32 Et (E_t e^{-m}), fp32 P,
+ *   fp32 e^tau, 12 bytes padding, fp32 S_u[d] (running sum of u), fp32 mu[d],
+ *   fp32 F~[d][d] (= F e^{-m}), fp32 G[d][d], fp32 H[d][d]   (row a = key dim, col j = value dim)
+ * padded to a multiple of 256 bytes.  The blob may be copied, saved and restored byte-wise.
+ */
+size_t zeros_state_bytes(int B, int H, int d);
+size_t zeros_state_record_bytes(int d);
+
+/* Empty state (t = 0) for B x H sequences with prior mu [H, d] and tau [H] (device fp32). */
+int zeros_state_init(void* state, const float* mu, const float* tau, int B, int H, int d,
+                     int dtype, int rope, float rope_base, void* stream);
+
+/*
+ * One recurrent-inference step (the linear-time prefix scan applied to one new token) for
+ * every sequence in the state: q, k, v, u [B, H, d] and out [B, H, d] in the state's dtype,
+ * g1, gh [B, H] fp32.  Advances t by one; the token's rotary position is the old t.
+ * The state must come from zeros_state_init or zeros_fwd_ex(final_state) in this process;
+ * otherwise its 256-byte header is read once from the device (a synchronous copy).
+ */
+int zeros_decode_step(void* state, const void* q, const void* k, const void* v, const void* u,
+                      const float* g1, const float* gh, void* out, void* stream);
+
+/* As zeros_decode_step with explicit dimensions (no header lookup) and per-token debug
+ * outputs dbg_s, dbg_E, dbg_P, dbg_m (nullable fp32 [B, H]) as in zeros_fwd_ex. */
+int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const void* k,
+                         const void* v, const void* u, const float* g1, const float* gh,
+                         void* out, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
+                         void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status word. */
+int zeros_get_status(void* stream);
+
+/* Static description of a status code. */
+const char* zeros_status_string(int status);
+
+/* Detail of the last host-side error on this thread ("" if none). */
+const char* zeros_last_error_message(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int zeros_version(void);
+
+/* Number of CUDA kernels this process has launched through the library so far (all devices,
+ * all entry points).  Used by benchmarks to count device work; never reset. */
+unsigned long long zeros_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZEROS_H */

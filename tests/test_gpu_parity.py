@@ -1,0 +1,237 @@
+"""CUDA path vs the fp64 oracle on identical seeded inputs (GPU only).
+
+Tolerance metric (the same everywhere): for every compared (b, h) sequence,
+    err = max_t,j |o - o_ref| / max_t,j |o_ref|
+and the test asserts the worst sequence is within 1e-5 for fp32 inputs and 1e-2 for bf16
+inputs (fp32 accumulation).  The logit s, the prefix sum P, the running maximum m and the
+scaled prefix sum Et = E e^{-m} must be bit-identical between the forward pass and the
+token-by-token decode step.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zeros_inputs as zi
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+
+@pytest.fixture(scope="module")
+def zs():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import zero_sum_prefix_gb300 as m
+    m.load()
+    return m
+
+
+def seq_err(o, ref):
+    """Worst per-sequence max-abs error over max-abs reference (o, ref: [S, N, d])."""
+    o = np.asarray(o, np.float64)
+    ref = np.asarray(ref, np.float64)
+    worst = 0.0
+    for i in range(ref.shape[0]):
+        den = np.abs(ref[i]).max()
+        num = np.abs(o[i] - ref[i]).max()
+        worst = max(worst, num / den if den > 0 else num)
+    return worst
+
+
+def run(zs, inp, w, **kw):
+    return zs.fwd(inp["q"], inp["k"], inp["v"], inp["u"], inp["g1"], inp["gh"], inp["mu"],
+                  inp["tau"], causal=w.causal, rope=w.rope, rope_base=w.rope_base, **kw)
+
+
+def oracle_subset(inp, w, heads, N=None):
+    """fp64 oracle outputs for the listed (b, h) sequences: [len(heads), N, d]."""
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]  # noqa: E731
+    hs = [h for _, h in heads]
+    q, k, v, u = (sel(inp[n]).cpu() for n in ("q", "k", "v", "u"))
+    g1, gh = sel(inp["g1"]).cpu(), sel(inp["gh"]).cpu()
+    # every sampled sequence keeps its own head's prior: run heads one at a time
+    outs = []
+    for i, h in enumerate(hs):
+        o = oracle.forward(q[:, i:i + 1], k[:, i:i + 1], v[:, i:i + 1], u[:, i:i + 1],
+                           g1[:, i:i + 1], gh[:, i:i + 1], inp["mu"][h:h + 1].cpu(),
+                           inp["tau"][h:h + 1].cpu(), causal=w.causal, rope=w.rope,
+                           rope_base=w.rope_base)
+        outs.append(o[0, 0])
+    return np.stack(outs)
+
+
+def gpu_subset(o, heads):
+    return torch.stack([o[b, h] for b, h in heads]).float().cpu().numpy()
+
+
+# ---------------------------------------------------------------------------------------------
+def test_causal_f32_small_workload(zs):
+    w = zi.CAUSAL_F32_SMALL
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert zs.get_status() == 0
+    ref = oracle.forward(*(inp[n].cpu() for n in ("q", "k", "v", "u", "g1", "gh", "mu", "tau")),
+                         causal=True)
+    assert seq_err(o[0].cpu().numpy(), ref[0]) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("N", [1, 2, 37, 300])
+@pytest.mark.parametrize("causal,rope", [(True, False), (True, True), (False, False),
+                                         (False, True)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_small_shapes(zs, d, N, causal, rope, dtype):
+    w = zi.Workload("small", 2, 3, N, d, dtype=dtype, causal=causal, rope=rope, rope_base=500.0,
+                    seed=1000 + N + d)
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert zs.get_status() == 0
+    heads = [(b, h) for b in range(2) for h in range(3)]
+    ref = oracle_subset(inp, w, heads)
+    assert seq_err(gpu_subset(o, heads), ref) <= TOL[dtype]
+
+
+def test_causal_rope_b8h8n4096d64_full(zs):
+    w = zi.CAUSAL_ROPE_B8H8N4096D64
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert zs.get_status() == 0
+    assert torch.isfinite(o.float()).all()
+    heads = zi.sample_heads(w, 6)
+    assert seq_err(gpu_subset(o, heads), oracle_subset(inp, w, heads)) <= TOL["bf16"]
+
+
+def test_encoder_b256h3n197d64_full(zs):
+    w = zi.ENCODER_VIT_B256H3N197D64
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert zs.get_status() == 0
+    assert torch.isfinite(o.float()).all()
+    heads = zi.sample_heads(w, 24)
+    assert seq_err(gpu_subset(o, heads), oracle_subset(inp, w, heads)) <= TOL["bf16"]
+
+
+def test_long_rope_b2h16n65536d128_full(zs):
+    w = zi.LONG_ROPE_B2H16N65536D128
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert zs.get_status() == 0
+    assert torch.isfinite(o.float()).all()
+    heads = zi.sample_heads(w, 3)
+    assert seq_err(gpu_subset(o, heads), oracle_subset(inp, w, heads)) <= TOL["bf16"]
+
+
+# ---------------------------------------------------------------------------------------------
+def _decode_run(zs, w, inp_prefill, steps, device="cuda"):
+    """Prefill with the forward pass, then `steps` decode steps.  Returns the decode outputs
+    [steps, B, H, d], the debug scalars of every step and the per-step token inputs."""
+    st = torch.empty(zs.state_bytes(w.B, w.H, w.d), dtype=torch.uint8, device=device)
+    if inp_prefill is not None:
+        zs.fwd(inp_prefill["q"], inp_prefill["k"], inp_prefill["v"], inp_prefill["u"],
+               inp_prefill["g1"], inp_prefill["gh"], inp_prefill["mu"], inp_prefill["tau"],
+               causal=True, rope=w.rope, rope_base=w.rope_base, final_state=st)
+    else:
+        raise AssertionError("use new_state for an empty prefill")
+    outs, dbgs, toks = [], [], []
+    for i in range(steps):
+        tk = zi.decode_tokens(w, i, device)
+        o, dbg = zs.decode_step(st, tk["q"], tk["k"], tk["v"], tk["u"], tk["g1"], tk["gh"],
+                                debug=True)
+        outs.append(o)
+        dbgs.append(dbg)
+        toks.append(tk)
+    return st, outs, dbgs, toks
+
+
+@pytest.mark.parametrize("d,rope,dtype", [(32, False, "f32"), (64, True, "bf16"),
+                                          (128, True, "bf16"), (128, False, "bf16")])
+def test_decode_matches_forward_bitexact(zs, d, rope, dtype):
+    """Prefill N0 tokens, decode the rest: s, P, m, Et bit-identical to a forward pass over
+    the whole sequence; outputs within tolerance of the oracle."""
+    B, H, N0, steps = 2, 3, 45, 20
+    w = zi.Workload("dec", B, H, N0, d, dtype=dtype, rope=rope, rope_base=10000.0, seed=77 + d)
+    pre = zi.make(w, "cuda")
+    st, outs, dbgs, toks = _decode_run(zs, w, pre, steps)
+    assert zs.get_status() == 0
+    # full sequence = prefill tokens followed by the decoded tokens
+    full = {n: torch.cat([pre[n]] + [t[n].unsqueeze(2) for t in toks], dim=2)
+            for n in ("q", "k", "v", "u", "g1", "gh")}
+    full["mu"], full["tau"] = pre["mu"], pre["tau"]
+    wf = w.with_(N=N0 + steps)
+    o_full, dbg_full = run(zs, full, wf, debug=True)
+    for key in ("s", "E", "P", "m"):
+        dec = torch.stack([dg[key] for dg in dbgs], dim=2)  # [B, H, steps]
+        fwd = dbg_full[key][:, :, N0:]
+        assert torch.equal(dec.view(torch.int32), fwd.contiguous().view(torch.int32)), key
+    dec_o = torch.stack(outs, dim=2)  # [B, H, steps, d]
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    ref = oracle_subset(full, wf, heads)[:, N0:]
+    assert seq_err(gpu_subset(dec_o, heads), ref) <= TOL[dtype]
+    assert seq_err(gpu_subset(o_full[:, :, N0:], heads), ref) <= TOL[dtype]
+    # the state records the token count
+    view = zs.state_view(st, B, H, d)
+    assert (view["t"] == N0 + steps).all()
+
+
+def test_decode_from_empty_state(zs):
+    B, H, d, steps = 3, 2, 64, 24
+    w = zi.Workload("dec0", B, H, steps, d, rope=True, seed=91)
+    inp = zi.make(w, "cuda")
+    st = zs.new_state(inp["mu"], inp["tau"], B, rope=True, rope_base=w.rope_base)
+    outs, dbgs = [], []
+    for t in range(steps):
+        o, dbg = zs.decode_step(st, *(inp[n][:, :, t].contiguous() for n in
+                                      ("q", "k", "v", "u", "g1", "gh")), debug=True)
+        outs.append(o)
+        dbgs.append(dbg)
+    o_f, dbg_f = run(zs, inp, w, debug=True)
+    for key in ("s", "E", "P", "m"):
+        dec = torch.stack([dg[key] for dg in dbgs], dim=2)
+        assert torch.equal(dec.view(torch.int32), dbg_f[key].view(torch.int32)), key
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    ref = oracle_subset(inp, w, heads)
+    assert seq_err(gpu_subset(torch.stack(outs, dim=2), heads), ref) <= TOL["bf16"]
+
+
+def test_decode_header_lookup(zs):
+    """zeros_decode_step on a state blob restored into fresh memory reads its header."""
+    B, H, d = 2, 2, 32
+    w = zi.Workload("hdr", B, H, 10, d, seed=5)
+    inp = zi.make(w, "cuda")
+    st = torch.empty(zs.state_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+    run(zs, inp, w, final_state=st)
+    saved = st.cpu()
+    restored = saved.cuda()  # a new allocation the library has never seen
+    tk = zi.decode_tokens(w, 0, "cuda")
+    o1 = zs.decode_step(restored, tk["q"], tk["k"], tk["v"], tk["u"], tk["g1"], tk["gh"])
+    o2 = zs.decode_step(st, tk["q"], tk["k"], tk["v"], tk["u"], tk["g1"], tk["gh"])
+    assert torch.equal(o1, o2)
+    assert torch.equal(restored, st)
+
+
+def test_device_range_error_is_reported(zs):
+    w = zi.Workload("range", 1, 1, 8, 32, dtype="f32", seed=3)
+    inp = zi.make(w, "cuda")
+    inp["u"][0, 0, 3] = 3.0e38  # the prior-mean numerator overflows -> non-finite logit
+    run(zs, inp, w)
+    assert zs.get_status() == zs.ZEROS_ERR_RANGE
+    assert zs.get_status() == 0  # reading clears it
+    inp = zi.make(w, "cuda")
+    run(zs, inp, w)
+    assert zs.get_status() == 0
+
+
+def test_empty_and_invalid_calls(zs):
+    w = zi.Workload("e", 1, 2, 0, 64, seed=1)
+    inp = zi.make(w, "cuda")
+    o = run(zs, inp, w)
+    assert o.numel() == 0
+    q = torch.zeros((1, 1, 4, 48), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros((1, 1, 4), dtype=torch.float32, device="cuda")
+    mu = torch.zeros((1, 48), dtype=torch.float32, device="cuda")
+    tau = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    with pytest.raises(zs.ZerosError) as e:
+        zs.fwd(q, q, q, q, g, g, mu, tau)
+    assert e.value.code == zs.ZEROS_ERR_UNSUPPORTED

@@ -1,0 +1,384 @@
+// Host side of the ZeroS C ABI (include/zeros.h): argument validation, the per-device
+// workspace (status word, rotary tables), the state registry and the stream-ordered launches.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+
+#include "../../include/zeros.h"
+#include "zs_common.cuh"
+#include "zs_internal.h"
+
+namespace zs {
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<unsigned long long> g_launches{0};
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ZEROS_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceWorkspace {
+  int* status = nullptr;
+  float2* rope = nullptr;
+  size_t rope_entries = 0;  // capacity in float2
+  int rope_N = 0, rope_d = 0;
+  float rope_base = 0.0f;
+};
+
+std::mutex g_mutex;
+std::unordered_map<int, DeviceWorkspace> g_ws;
+
+struct StateInfo {
+  int B, H, d, dtype, rope;
+  float rope_base;
+};
+std::unordered_map<const void*, StateInfo> g_states;
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  return ZEROS_OK;
+}
+
+// Per-device workspace with the status word (allocated once, zeroed).
+int workspace(DeviceWorkspace** out) {
+  int dev;
+  if (int rc = current_device(&dev)) return rc;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceWorkspace& ws = g_ws[dev];
+  if (!ws.status) {
+    cudaError_t e = cudaMalloc(&ws.status, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+    e = cudaMemset(ws.status, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  }
+  *out = &ws;
+  return ZEROS_OK;
+}
+
+// Rotary (cos, sin) table for positions [0, N) and head dimension d, built on `stream`.
+int rope_table(DeviceWorkspace* ws, int N, int d, float base, cudaStream_t stream,
+               const float2** table) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (ws->rope && ws->rope_d == d && ws->rope_base == base && ws->rope_N >= N) {
+    *table = ws->rope;
+    return ZEROS_OK;
+  }
+  const int n_new = N > 0 ? N : 1;
+  const size_t need = (size_t)n_new * (size_t)(d / 2);
+  if (ws->rope) {
+    // Work already queued (on any stream) may still read the current table.
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  }
+  if (need > ws->rope_entries) {
+    if (ws->rope) cudaFree(ws->rope);
+    ws->rope = nullptr;
+    ws->rope_entries = 0;
+    cudaError_t e = cudaMalloc(&ws->rope, need * sizeof(float2));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
+    ws->rope_entries = need;
+  }
+  cudaError_t e = launch_rope_table(ws->rope, n_new, d, (double)base, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  ws->rope_N = n_new;
+  ws->rope_d = d;
+  ws->rope_base = base;
+  *table = ws->rope;
+  return ZEROS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) return fail(ZEROS_ERR_INVALID, std::string(name) + " is null");
+  if (!aligned16(p)) return fail(ZEROS_ERR_INVALID, std::string(name) + " is not 16-byte aligned");
+  return ZEROS_OK;
+}
+
+int check_opt_ptr(const void* p, const char* name) {
+  if (p && !aligned16(p))
+    return fail(ZEROS_ERR_INVALID, std::string(name) + " is not 16-byte aligned");
+  return ZEROS_OK;
+}
+
+int check_dims(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0) return fail(ZEROS_ERR_INVALID, "negative B, H or N");
+  if (d != 32 && d != 64 && d != 128)
+    return fail(ZEROS_ERR_UNSUPPORTED, "head dimension d must be 32, 64 or 128");
+  const unsigned long long bh = (unsigned long long)B * (unsigned long long)H;
+  if (bh > 0x7fffffffull) return fail(ZEROS_ERR_INVALID, "B*H exceeds 2^31-1");
+  if (bh * (unsigned long long)N * (unsigned long long)d > (1ull << 50))
+    return fail(ZEROS_ERR_INVALID, "B*H*N*d exceeds 2^50 elements");
+  if ((unsigned long long)N >= (1ull << 24))
+    return fail(ZEROS_ERR_UNSUPPORTED, "N must be below 2^24 (token counts are exact in fp32)");
+  return ZEROS_OK;
+}
+
+int check_dtype(int dtype) {
+  if (dtype != ZEROS_BF16 && dtype != ZEROS_F32) return fail(ZEROS_ERR_INVALID, "unknown dtype");
+  return ZEROS_OK;
+}
+
+}  // namespace
+
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace zs
+
+using namespace zs;
+
+extern "C" {
+
+int zeros_version(void) { return 100; }
+
+unsigned long long zeros_kernel_launches(void) { return g_launches.load(); }
+
+const char* zeros_status_string(int status) {
+  switch (status) {
+    case ZEROS_OK: return "ok";
+    case ZEROS_ERR_INVALID: return "invalid argument";
+    case ZEROS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ZEROS_ERR_RANGE: return "value out of range on the device";
+    case ZEROS_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case ZEROS_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+const char* zeros_last_error_message(void) { return g_last_error.c_str(); }
+
+size_t zeros_state_record_bytes(int d) {
+  if (d != 32 && d != 64 && d != 128) return 0;
+  return record_bytes(d);
+}
+
+size_t zeros_state_bytes(int B, int H, int d) {
+  if (B < 0 || H < 0 || (d != 32 && d != 64 && d != 128)) return 0;
+  return state_bytes(B, H, d);
+}
+
+int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* mu, const float* tau, void* out, int B, int H,
+                 int N, int d, int causal, int rope, int dtype, float rope_base, int path,
+                 void* final_state, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
+                 void* stream) {
+  g_last_error.clear();
+  if (int rc = check_dims(B, H, N, d)) return rc;
+  if (int rc = check_dtype(dtype)) return rc;
+  if (causal != 0 && causal != 1) return fail(ZEROS_ERR_INVALID, "causal must be 0 or 1");
+  if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
+  if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
+  if (path != ZEROS_PATH_AUTO && path != ZEROS_PATH_SIMT && path != ZEROS_PATH_CHUNK)
+    return fail(ZEROS_ERR_INVALID, "unknown path");
+  if (final_state && !causal)
+    return fail(ZEROS_ERR_INVALID, "final_state is only defined for the causal mode");
+  const char* names[] = {"q", "k", "v", "u", "g1", "gh", "mu", "tau", "out"};
+  const void* ptrs[] = {q, k, v, u, g1, gh, mu, tau, out};
+  const bool empty = (long long)B * H * N == 0;
+  if (!empty)
+    for (int i = 0; i < 9; ++i)
+      if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (int rc = check_opt_ptr(final_state, "final_state")) return rc;
+  if (int rc = check_opt_ptr(dbg_s, "dbg_s")) return rc;
+  if (int rc = check_opt_ptr(dbg_E, "dbg_E")) return rc;
+  if (int rc = check_opt_ptr(dbg_P, "dbg_P")) return rc;
+  if (int rc = check_opt_ptr(dbg_m, "dbg_m")) return rc;
+  if (path == ZEROS_PATH_CHUNK)
+    return fail(ZEROS_ERR_UNSUPPORTED, "the chunked tensor-core path is not available");
+  if (B == 0 || H == 0 || (N == 0 && !final_state)) return ZEROS_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+
+  if (final_state) {
+    if (!mu || !tau) return fail(ZEROS_ERR_INVALID, "mu/tau are null");
+    cudaError_t e = launch_state_init(final_state, mu, tau, B, H, d, dtype, rope, rope_base, st);
+    if (e != cudaSuccess) return cuda_fail(e, "state init launch");
+    std::lock_guard<std::mutex> lk(g_mutex);
+    g_states[final_state] = StateInfo{B, H, d, dtype, rope, rope_base};
+  }
+  if (N == 0) return ZEROS_OK;
+
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.u = u;
+  a.g1 = g1;
+  a.gh = gh;
+  a.mu = mu;
+  a.tau = tau;
+  a.out = out;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.rope = rope;
+  a.dtype = dtype;
+  a.rope_base = rope_base;
+  a.final_state = final_state;
+  a.dbg_s = dbg_s;
+  a.dbg_E = dbg_E;
+  a.dbg_P = dbg_P;
+  a.dbg_m = dbg_m;
+  a.status = ws->status;
+  if (rope) {
+    if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
+  }
+  cudaError_t e = launch_fwd_simt(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ZEROS_OK;
+}
+
+int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
+              const float* gh, const float* mu, const float* tau, void* out, int B, int H, int N,
+              int d, int causal, int rope, void* stream) {
+  return zeros_fwd_ex(q, k, v, u, g1, gh, mu, tau, out, B, H, N, d, causal, rope, ZEROS_BF16,
+                      10000.0f, ZEROS_PATH_AUTO, nullptr, nullptr, nullptr, nullptr, nullptr,
+                      stream);
+}
+
+int zeros_state_init(void* state, const float* mu, const float* tau, int B, int H, int d,
+                     int dtype, int rope, float rope_base, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_dims(B, H, 0, d)) return rc;
+  if (int rc = check_dtype(dtype)) return rc;
+  if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
+  if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
+  if (int rc = check_ptr(state, "state")) return rc;
+  if ((long long)B * H > 0) {
+    if (int rc = check_ptr(mu, "mu")) return rc;
+    if (int rc = check_ptr(tau, "tau")) return rc;
+  }
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+  cudaError_t e = launch_state_init(state, mu, tau, B, H, d, dtype, rope, rope_base,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "state init launch");
+  std::lock_guard<std::mutex> lk(g_mutex);
+  g_states[state] = StateInfo{B, H, d, dtype, rope, rope_base};
+  return ZEROS_OK;
+}
+
+static int decode_impl(void* state, const StateInfo& si, const void* q, const void* k,
+                       const void* v, const void* u, const float* g1, const float* gh, void* out,
+                       float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m, void* stream) {
+  if (int rc = check_dims(si.B, si.H, 1, si.d)) return rc;
+  if (int rc = check_ptr(state, "state")) return rc;
+  if ((long long)si.B * si.H == 0) return ZEROS_OK;
+  const char* names[] = {"q", "k", "v", "u", "g1", "gh", "out"};
+  const void* ptrs[] = {q, k, v, u, g1, gh, out};
+  for (int i = 0; i < 7; ++i)
+    if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (int rc = check_opt_ptr(dbg_s, "dbg_s")) return rc;
+  if (int rc = check_opt_ptr(dbg_E, "dbg_E")) return rc;
+  if (int rc = check_opt_ptr(dbg_P, "dbg_P")) return rc;
+  if (int rc = check_opt_ptr(dbg_m, "dbg_m")) return rc;
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+  DecodeArgs a{};
+  a.state = state;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.u = u;
+  a.g1 = g1;
+  a.gh = gh;
+  a.out = out;
+  a.B = si.B;
+  a.H = si.H;
+  a.d = si.d;
+  a.dtype = si.dtype;
+  a.rope = si.rope;
+  a.rope_base = si.rope_base;
+  a.dbg_s = dbg_s;
+  a.dbg_E = dbg_E;
+  a.dbg_P = dbg_P;
+  a.dbg_m = dbg_m;
+  a.status = ws->status;
+  cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return ZEROS_OK;
+}
+
+int zeros_decode_step(void* state, const void* q, const void* k, const void* v, const void* u,
+                      const float* g1, const float* gh, void* out, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_ptr(state, "state")) return rc;
+  StateInfo si{};
+  bool known = false;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    auto it = g_states.find(state);
+    if (it != g_states.end()) {
+      si = it->second;
+      known = true;
+    }
+  }
+  if (!known) {
+    StateHeader hdr;
+    cudaError_t e = cudaMemcpy(&hdr, state, sizeof(hdr), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the state header");
+    if (std::memcmp(hdr.magic, "ZSP1", 4) != 0 || hdr.version != 1)
+      return fail(ZEROS_ERR_INVALID, "state header not recognised");
+    si = StateInfo{hdr.B, hdr.H, hdr.d, hdr.dtype, hdr.rope, hdr.rope_base};
+    std::lock_guard<std::mutex> lk(g_mutex);
+    g_states[state] = si;
+  }
+  return decode_impl(state, si, q, k, v, u, g1, gh, out, nullptr, nullptr, nullptr, nullptr,
+                     stream);
+}
+
+int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const void* k,
+                         const void* v, const void* u, const float* g1, const float* gh,
+                         void* out, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
+                         void* stream) {
+  g_last_error.clear();
+  StateInfo si{B, H, d, ZEROS_BF16, 0, 10000.0f};
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    auto it = g_states.find(state);
+    if (it != g_states.end()) {
+      if (it->second.B != B || it->second.H != H || it->second.d != d)
+        return fail(ZEROS_ERR_INVALID, "dimensions differ from the state's");
+      si = it->second;
+    } else {
+      return fail(ZEROS_ERR_INVALID,
+                  "state unknown to this process: create it with zeros_state_init or "
+                  "zeros_fwd_ex, or call zeros_decode_step once");
+    }
+  }
+  return decode_impl(state, si, q, k, v, u, g1, gh, out, dbg_s, dbg_E, dbg_P, dbg_m, stream);
+}
+
+int zeros_get_status(void* stream) {
+  g_last_error.clear();
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int st = 0;
+  e = cudaMemcpy(&st, ws->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (st != 0) {
+    e = cudaMemset(ws->status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  }
+  return st;
+}
+
+}  // extern "C"

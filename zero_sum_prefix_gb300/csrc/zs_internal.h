@@ -1,0 +1,49 @@
+// Host-side declarations shared by the translation units of the ZeroS library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace zs {
+
+// Everything a forward launch needs; pointers are device pointers.
+struct FwdArgs {
+  const void *q, *k, *v, *u;
+  const float *g1, *gh, *mu, *tau;
+  void* out;
+  int B, H, N, d;
+  int causal, rope, dtype;
+  float rope_base;
+  const float2* rope_table;  // [N][d/2] (cos, sin) when rope, else null
+  void* final_state;         // nullable (causal only)
+  float *dbg_s, *dbg_E, *dbg_P, *dbg_m;
+  int* status;               // device status word
+};
+
+struct DecodeArgs {
+  void* state;
+  const void *q, *k, *v, *u;
+  const float *g1, *gh;
+  void* out;
+  int B, H, d, dtype, rope;
+  float rope_base;
+  float *dbg_s, *dbg_E, *dbg_P, *dbg_m;
+  int* status;
+};
+
+// Counts every kernel launch the library issues (zs_api.cu).
+void count_launches(unsigned n);
+
+// zs_simt.cu
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_state_init(void* state, const float* mu, const float* tau, int B, int H, int d,
+                              int dtype, int rope, float rope_base, cudaStream_t stream);
+cudaError_t launch_state_header(void* state, int B, int H, int d, int dtype, int rope,
+                                float rope_base, cudaStream_t stream);
+cudaError_t launch_rope_table(float2* table, int N, int d, double base, cudaStream_t stream);
+
+// zs_decode.cu
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace zs

@@ -1,0 +1,346 @@
+// Token-sequential CUDA-core forward of the ZeroS layer (causal and encoder modes), plus the
+// small utility kernels (state init / header, rotary tables).
+//
+// Method: Paper-Notes "ZeroS: Zero-Sum Linear Attention for Efficient Transformers", method
+// details, "linear-time prefix scan": the five prefix states E, P, F, G, H are updated once per
+// token and read out as o_t = q_hat_t (alpha_t F_t + beta_t G_t + gamma_t H_t).  This kernel
+// does exactly that, one token after the other, with the fp32 states in registers.  It is the
+// fp32-input path and the reference CUDA path against which the chunked tensor-core kernel is
+// checked; it is not the bf16 fast path.
+//
+// Grid: one CTA per (b, h, 32-wide slice of the value columns); 256 threads = 8 warps.  Warp w,
+// lane l own state rows a = w + 8 r and value column j0 + l of F~ (= F e^{-m}), G and H.
+// Warp 0 also runs the canonical token update of zs_common.cuh (logit, m, Et, P); warps 1..3
+// normalise / rotate q_t and k_t and stage v_t in shared memory.
+#include <math.h>
+
+#include "zs_common.cuh"
+#include "zs_internal.h"
+
+namespace zs {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct TokenCoefs {
+  float s, f, g, alpha, beta, gamma;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
+  constexpr int R = D / 32;  // columns per lane in a warp-owned row
+  constexpr int RA = D / 8;  // state rows per thread
+  const int bh = blockIdx.x;
+  const int h = bh % a.H;
+  const int j0 = blockIdx.y * 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const size_t row0 = (size_t)bh * N;
+  const T* __restrict__ q = static_cast<const T*>(a.q) + row0 * D;
+  const T* __restrict__ k = static_cast<const T*>(a.k) + row0 * D;
+  const T* __restrict__ v = static_cast<const T*>(a.v) + row0 * D;
+  const T* __restrict__ u = static_cast<const T*>(a.u) + row0 * D;
+  T* __restrict__ out = static_cast<T*>(a.out) + row0 * D;
+  const float* __restrict__ g1 = a.g1 + row0;
+  const float* __restrict__ gh = a.gh + row0;
+
+  __shared__ float qs[D], ks[D], vs[32];
+  __shared__ float red[8][32];
+  __shared__ TokenCoefs tc;
+
+  float F[RA], G[RA], Hs[RA];
+#pragma unroll
+  for (int r = 0; r < RA; ++r) F[r] = G[r] = Hs[r] = 0.0f;
+
+  // Warp-0 scalar state (canonical order of zs_common.cuh).
+  float S[R], mu[R], nfix[R];
+  Scalars sc{-INFINITY, 0.0f, 0.0f};
+  const float etau = expf(a.tau[h]);
+  float den_fix = 0.0f;
+  if (warp == 0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      S[r] = 0.0f;
+      mu[r] = a.mu[(size_t)h * D + lane + 32 * r];
+    }
+    if (!a.causal) {
+      // Encoder: full-sequence prior mean, numerator e^tau mu + sum_j u_j.
+      for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) S[r] = __fadd_rn(S[r], ld(u, (size_t)i * D + lane + 32 * r));
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) nfix[r] = __fmaf_rn(etau, mu[r], S[r]);
+      den_fix = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)D));
+    }
+  }
+
+  auto load_unit_row = [&](const T* src, int t, float* dst) {
+    float x[R];
+    float2 cs[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      x[r] = ld(src, (size_t)t * D + lane + 32 * r);
+      cs[r] = make_float2(1.0f, 0.0f);
+    }
+    if (a.rope) {
+      const float2* tab = a.rope_table + (size_t)t * (D / 2);
+      if (R == 1) {
+        cs[0] = tab[pair_index<R>(lane, 0)];
+      } else {
+#pragma unroll
+        for (int r = 0; r < R / 2; ++r) cs[r] = tab[pair_index<R>(lane, r)];
+      }
+    }
+    unit_rotate<R>(x, a.rope != 0, cs);
+#pragma unroll
+    for (int r = 0; r < R; ++r) dst[lane + 32 * r] = x[r];
+  };
+
+  // ---- pass over the tokens: state update (+ readout in causal mode) ----
+  for (int t = 0; t < N; ++t) {
+    if (warp == 0) {
+      float uu[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) uu[r] = ld(u, (size_t)t * D + lane + 32 * r);
+      float f, g, s;
+      if (a.causal) {
+        s = token_update<R>(uu, S, mu, etau, t + 1, sc, &f, &g);
+      } else {
+        s = fixed_logit<R>(uu, nfix, den_fix);
+        const float m_new = fmaxf(sc.m, s);
+        f = expf(__fsub_rn(sc.m, m_new));
+        g = expf(__fsub_rn(s, m_new));
+        sc.Et = __fmaf_rn(sc.Et, f, g);
+        sc.P = __fadd_rn(sc.P, s);
+        sc.m = m_new;
+      }
+      if (lane == 0) {
+        if (!isfinite(s)) report(a.status, kErrRange);
+        tc.s = s;
+        tc.f = f;
+        tc.g = g;
+        if (a.causal) {
+          const float sig1 = sigmoid(g1[t]), sigh = sigmoid(gh[t]);
+          const float rt = __fdiv_rn(1.0f, (float)(t + 1));
+          const float beta = __fmul_rn(__fsub_rn(sig1, sigh), rt);
+          tc.alpha = __fdiv_rn(sigh, sc.Et);
+          tc.beta = beta;
+          tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, sc.P), rt), __fmul_rn(sigh, rt));
+          if (blockIdx.y == 0) {
+            if (a.dbg_s) a.dbg_s[row0 + t] = s;
+            if (a.dbg_E) a.dbg_E[row0 + t] = sc.Et;
+            if (a.dbg_P) a.dbg_P[row0 + t] = sc.P;
+            if (a.dbg_m) a.dbg_m[row0 + t] = sc.m;
+          }
+        } else if (blockIdx.y == 0 && a.dbg_s) {
+          a.dbg_s[row0 + t] = s;
+        }
+      }
+    } else if (warp == 1) {
+      if (a.causal) load_unit_row(q, t, qs);
+    } else if (warp == 2) {
+      load_unit_row(k, t, ks);
+    } else if (warp == 3) {
+      vs[lane] = ld(v, (size_t)t * D + j0 + lane);
+    }
+    __syncthreads();
+    const float s = tc.s, f = tc.f, g = tc.g;
+    const float vj = vs[lane];
+    float acc = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RA; ++r) {
+      const int ai = warp + 8 * r;
+      const float kv = __fmul_rn(ks[ai], vj);
+      F[r] = __fmaf_rn(F[r], f, __fmul_rn(g, kv));
+      G[r] = __fmaf_rn(s, kv, G[r]);
+      Hs[r] = __fadd_rn(Hs[r], kv);
+      if (a.causal) {
+        const float comb = __fmaf_rn(tc.alpha, F[r], __fmaf_rn(tc.beta, G[r], __fmul_rn(tc.gamma, Hs[r])));
+        acc = __fmaf_rn(qs[ai], comb, acc);
+      }
+    }
+    if (a.causal) red[warp][lane] = acc;
+    __syncthreads();
+    if (a.causal && warp == 7) {
+      float o = red[0][lane];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) o = __fadd_rn(o, red[w][lane]);
+      st(out, (size_t)t * D + j0 + lane, o);
+    }
+  }
+
+  if (a.causal) {
+    // ---- optional final state (prefill for recurrent decoding) ----
+    if (a.final_state) {
+      float* rec = record_ptr(a.final_state, bh, D);
+#pragma unroll
+      for (int r = 0; r < RA; ++r) {
+        const int ai = warp + 8 * r;
+        rec[rec_F(D) + ai * D + j0 + lane] = F[r];
+        rec[rec_G(D) + ai * D + j0 + lane] = G[r];
+        rec[rec_H(D) + ai * D + j0 + lane] = Hs[r];
+      }
+      if (blockIdx.y == 0 && warp == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          rec[rec_S(D) + lane + 32 * r] = S[r];
+          rec[rec_mu(D) + lane + 32 * r] = mu[r];
+        }
+        if (lane == 0) {
+          RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
+          hd->t = N;
+          hd->m = sc.m;
+          hd->Et = sc.Et;
+          hd->P = sc.P;
+          hd->etau = etau;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- encoder readout: every token against the full-sequence state ----
+  __shared__ float fullsc[3];  // Et_N, P_N, m_N
+  if (warp == 0 && lane == 0) {
+    fullsc[0] = sc.Et;
+    fullsc[1] = sc.P;
+    fullsc[2] = sc.m;
+  }
+  const float rN = __fdiv_rn(1.0f, (float)N);
+  for (int t = 0; t < N; ++t) {
+    __syncthreads();  // previous readout finished with qs / tc
+    if (warp == 1) load_unit_row(q, t, qs);
+    if (warp == 0 && lane == 0) {
+      const float sig1 = sigmoid(g1[t]), sigh = sigmoid(gh[t]);
+      const float beta = __fmul_rn(__fsub_rn(sig1, sigh), rN);
+      tc.alpha = __fdiv_rn(sigh, fullsc[0]);
+      tc.beta = beta;
+      tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, fullsc[1]), rN), __fmul_rn(sigh, rN));
+      if (blockIdx.y == 0) {
+        if (a.dbg_E) a.dbg_E[row0 + t] = fullsc[0];
+        if (a.dbg_P) a.dbg_P[row0 + t] = fullsc[1];
+        if (a.dbg_m) a.dbg_m[row0 + t] = fullsc[2];
+      }
+    }
+    __syncthreads();
+    float acc = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RA; ++r) {
+      const int ai = warp + 8 * r;
+      const float comb = __fmaf_rn(tc.alpha, F[r], __fmaf_rn(tc.beta, G[r], __fmul_rn(tc.gamma, Hs[r])));
+      acc = __fmaf_rn(qs[ai], comb, acc);
+    }
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 7) {
+      float o = red[0][lane];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) o = __fadd_rn(o, red[w][lane]);
+      st(out, (size_t)t * D + j0 + lane, o);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_simt_typed(const FwdArgs& a, cudaStream_t stream) {
+  dim3 grid(a.B * a.H, a.d / 32);
+  switch (a.d) {
+    case 32: fwd_simt_kernel<T, 32><<<grid, kThreads, 0, stream>>>(a); break;
+    case 64: fwd_simt_kernel<T, 64><<<grid, kThreads, 0, stream>>>(a); break;
+    case 128: fwd_simt_kernel<T, 128><<<grid, kThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+__global__ void state_init_kernel(void* state, const float* __restrict__ mu,
+                                  const float* __restrict__ tau, int B, int H, int d) {
+  const int bh = blockIdx.x;
+  const int h = bh % H;
+  float* rec = record_ptr(state, bh, d);
+  const size_t nfl = record_bytes(d) / 4;
+  for (size_t i = 8 + threadIdx.x; i < nfl; i += blockDim.x) rec[i] = 0.0f;
+  __syncthreads();
+  for (int i = threadIdx.x; i < d; i += blockDim.x) rec[rec_mu(d) + i] = mu[(size_t)h * d + i];
+  if (threadIdx.x == 0) {
+    RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
+    hd->t = 0;
+    hd->m = -INFINITY;
+    hd->Et = 0.0f;
+    hd->P = 0.0f;
+    hd->etau = expf(tau[h]);
+    hd->pad[0] = hd->pad[1] = hd->pad[2] = 0.0f;
+  }
+}
+
+__global__ void state_header_kernel(void* state, int B, int H, int d, int dtype, int rope,
+                                    float rope_base) {
+  StateHeader* hdr = static_cast<StateHeader*>(state);
+  int* w = reinterpret_cast<int*>(hdr);
+  for (int i = threadIdx.x; i < 64; i += blockDim.x) w[i] = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    hdr->magic[0] = 'Z';
+    hdr->magic[1] = 'S';
+    hdr->magic[2] = 'P';
+    hdr->magic[3] = '1';
+    hdr->version = 1;
+    hdr->B = B;
+    hdr->H = H;
+    hdr->d = d;
+    hdr->dtype = dtype;
+    hdr->rope = rope;
+    hdr->rope_base = rope_base;
+  }
+}
+
+// Rotary table [N][d/2] of (cos, sin) of pos * base^(-2a/d), computed in fp64.
+__global__ void rope_table_kernel(float2* table, int N, int d, double base) {
+  const int half = d / 2;
+  const size_t total = (size_t)N * half;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int pos = (int)(i / half), pa = (int)(i % half);
+    const double ang = (double)pos * pow(base, -2.0 * (double)pa / (double)d);
+    double s, c;
+    sincos(ang, &s, &c);
+    table[i] = make_float2((float)c, (float)s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream) {
+  return a.dtype == 1 ? launch_simt_typed<float>(a, stream)
+                      : launch_simt_typed<__nv_bfloat16>(a, stream);
+}
+
+cudaError_t launch_state_init(void* state, const float* mu, const float* tau, int B, int H, int d,
+                              int dtype, int rope, float rope_base, cudaStream_t stream) {
+  cudaError_t e = launch_state_header(state, B, H, d, dtype, rope, rope_base, stream);
+  if (e != cudaSuccess) return e;
+  if (B * H == 0) return cudaSuccess;
+  state_init_kernel<<<B * H, 256, 0, stream>>>(state, mu, tau, B, H, d);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_state_header(void* state, int B, int H, int d, int dtype, int rope,
+                                float rope_base, cudaStream_t stream) {
+  state_header_kernel<<<1, 64, 0, stream>>>(state, B, H, d, dtype, rope, rope_base);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* table, int N, int d, double base, cudaStream_t stream) {
+  const size_t total = (size_t)N * (d / 2);
+  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  rope_table_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(table, N, d, base);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace zs
