@@ -3,7 +3,9 @@
 Tolerance metric (the same everywhere): for every compared (b, h) sequence,
     err = max_t,j |o - o_ref| / max_t,j |o_ref|
 and the test asserts the worst sequence is within 1e-5 for fp32 inputs and 1e-2 for bf16
-inputs (fp32 accumulation).  The logit s, the prefix sum P, the running maximum m and the
+inputs (fp32 accumulation).  The denominator has a floor of 0.1 (the scale of the outputs for
+N(0, 1) values): a sequence whose exact output is identically zero (N = 1: w_{1,1} = 0) is then
+held to an absolute error of 0.1 x tolerance instead of a meaningless relative one.  The logit s, the prefix sum P, the running maximum m and the
 scaled prefix sum Et = E e^{-m} must be bit-identical between the forward pass and the
 token-by-token decode step.
 """
@@ -17,6 +19,7 @@ import zeros_inputs as zi
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-5, "bf16": 1e-2}
+DEN_FLOOR = 0.1
 
 
 @pytest.fixture(scope="module")
@@ -34,9 +37,9 @@ def seq_err(o, ref):
     ref = np.asarray(ref, np.float64)
     worst = 0.0
     for i in range(ref.shape[0]):
-        den = np.abs(ref[i]).max()
+        den = max(np.abs(ref[i]).max(), DEN_FLOOR)
         num = np.abs(o[i] - ref[i]).max()
-        worst = max(worst, num / den if den > 0 else num)
+        worst = max(worst, num / den)
     return worst
 
 
@@ -235,3 +238,42 @@ def test_empty_and_invalid_calls(zs):
     with pytest.raises(zs.ZerosError) as e:
         zs.fwd(q, q, q, q, g, g, mu, tau)
     assert e.value.code == zs.ZEROS_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 300, 1000])
+@pytest.mark.parametrize("rope", [False, True])
+def test_chunk_path_small_shapes(zs, d, N, rope):
+    """The tcgen05 chunked scan against the oracle (ragged tails, single chunks, many chunks)
+    and its logits / prefix sums against the token-sequential path, bit for bit."""
+    w = zi.Workload("chunk", 2, 2, N, d, rope=rope, seed=3000 + N + d)
+    inp = zi.make(w, "cuda")
+    o_c, dbg_c = run(zs, inp, w, path="chunk", debug=True)
+    assert zs.get_status() == 0
+    o_s, dbg_s = run(zs, inp, w, path="simt", debug=True)
+    for key in ("s", "E", "P", "m"):
+        assert torch.equal(dbg_c[key].view(torch.int32), dbg_s[key].view(torch.int32)), key
+    heads = [(b, h) for b in range(2) for h in range(2)]
+    ref = oracle_subset(inp, w, heads)
+    assert seq_err(gpu_subset(o_c, heads), ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_chunk_final_state_matches_simt(zs, d):
+    """The prefill state written by the chunked path equals the token-sequential one (scalars
+    bit-exact, matrices within bf16-operand rounding)."""
+    B, H, N = 2, 3, 333
+    w = zi.Workload("chunkstate", B, H, N, d, rope=True, seed=4242 + d)
+    inp = zi.make(w, "cuda")
+    st_c = torch.empty(zs.state_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+    st_s = torch.empty_like(st_c)
+    run(zs, inp, w, path="chunk", final_state=st_c)
+    run(zs, inp, w, path="simt", final_state=st_s)
+    assert zs.get_status() == 0
+    vc, vs = zs.state_view(st_c, B, H, d), zs.state_view(st_s, B, H, d)
+    for key in ("t", "m", "Et", "P", "etau", "S", "mu"):
+        assert torch.equal(vc[key], vs[key]), key
+    for key in ("F", "G", "H"):
+        err = (vc[key] - vs[key]).abs().max() / vs[key].abs().max()
+        assert err < 2e-2, (key, float(err))

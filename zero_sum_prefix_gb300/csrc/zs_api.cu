@@ -195,8 +195,11 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
   if (int rc = check_opt_ptr(dbg_E, "dbg_E")) return rc;
   if (int rc = check_opt_ptr(dbg_P, "dbg_P")) return rc;
   if (int rc = check_opt_ptr(dbg_m, "dbg_m")) return rc;
-  if (path == ZEROS_PATH_CHUNK)
-    return fail(ZEROS_ERR_UNSUPPORTED, "the chunked tensor-core path is not available");
+  const bool chunk_ok = chunk_supported(d, dtype, causal);
+  if (path == ZEROS_PATH_CHUNK && !chunk_ok)
+    return fail(ZEROS_ERR_UNSUPPORTED,
+                "the chunked tensor-core path needs bf16, causal mode and d in {64, 128}");
+  const bool use_chunk = chunk_ok && path != ZEROS_PATH_SIMT;
   if (B == 0 || H == 0 || (N == 0 && !final_state)) return ZEROS_OK;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -239,7 +242,7 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
   if (rope) {
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
-  cudaError_t e = launch_fwd_simt(a, st);
+  cudaError_t e = use_chunk ? launch_fwd_chunk(a, st) : launch_fwd_simt(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ZEROS_OK;
 }

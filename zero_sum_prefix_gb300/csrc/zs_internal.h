@@ -43,6 +43,10 @@ cudaError_t launch_state_header(void* state, int B, int H, int d, int dtype, int
                                 float rope_base, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* table, int N, int d, double base, cudaStream_t stream);
 
+// zs_chunk.cu
+bool chunk_supported(int d, int dtype, int causal);
+cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);
+
 // zs_decode.cu
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
