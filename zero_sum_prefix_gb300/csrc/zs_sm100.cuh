@@ -13,6 +13,7 @@
 //     16 rows = 2048 bytes per 16 K-values.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,11 +24,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -53,18 +49,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up (returns false) after
-// `limit_ns` nanoseconds or as soon as *abort is set; never spins unbounded.
+// `limit_cycles` SM clock cycles (default 2^32, about two seconds) or as soon as *abort is set;
+// never spins unbounded.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          long long limit_cycles = 4294967296ll) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+    if ((it & 15) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
+      if (clock64() - t0 > limit_cycles) return false;
     }
   }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------------- TMA
+// 3-D tiled bulk copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // mbar_wait for roles whose next step is warp-collective (tcgen05.ld/st, shuffles): every lane
@@ -186,6 +204,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled atom tile.
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Byte offset of 16-byte chunk `c` (0..3) of row `r` in a tile of 64-byte rows written by TMA
+// with the 64-byte swizzle (chunk bits 4-5 XOR address bits 7-8).
+__device__ __forceinline__ uint32_t sw64_off(int r, int c) {
+  return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
