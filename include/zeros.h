@@ -98,8 +98,11 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
  * sequences of head dimension d (0 for unsupported d).  Layout: a 256-byte header
  * {magic "ZSP1", version, B, H, d, dtype, rope, rope_base} followed by B*H records of
  * zeros_state_record_bytes(d) bytes; record (b, h) at index b*H + h holds
- *   int32 t (tokens seen), fp32 m (running max of s), fp32 Et (E_t e^{-m}), fp32 P,
- *   fp32 e^tau, 12 bytes padding, fp32 S_u[d] (running sum of u), fp32 mu[d],
+ *   int32 t (tokens seen), then the running scalars in the library's blocked order (tokens in
+ *   blocks of 32: a carry at the end of the last completed block plus a local value for the
+ *   current block): fp32 mC, EC, CP (carries of the running max m, of E e^{-m} and of P),
+ *   fp32 e^tau, fp32 ml, El, LP (block-local running max, scaled exp-sum and logit sum),
+ *   fp32 C[d] (carry of the running sum of u), fp32 L[d] (block-local sum of u), fp32 mu[d],
  *   fp32 F~[d][d] (= F e^{-m}), fp32 G[d][d], fp32 H[d][d]   (row a = key dim, col j = value dim)
  * padded to a multiple of 256 bytes.  The blob may be copied, saved and restored byte-wise.
  */

@@ -218,14 +218,15 @@ def check_status(where="device", stream=None):
 
 
 def state_view(state: torch.Tensor, B: int, H: int, d: int) -> dict:
-    """Named views into a state blob (for tests and checkpoint tooling)."""
+    """Named views into a state blob (for tests and checkpoint tooling); layout in zeros.h."""
     rb = record_bytes(d)
     recs = state[256:256 + B * H * rb].view(B * H, rb)
     f = recs.view(torch.float32).view(B * H, rb // 4)
     i = recs.view(torch.int32).view(B * H, rb // 4)
     o = 8
-    return dict(t=i[:, 0], m=f[:, 1], Et=f[:, 2], P=f[:, 3], etau=f[:, 4],
-                S=f[:, o:o + d], mu=f[:, o + d:o + 2 * d],
-                F=f[:, o + 2 * d:o + 2 * d + d * d].view(B * H, d, d),
-                G=f[:, o + 2 * d + d * d:o + 2 * d + 2 * d * d].view(B * H, d, d),
-                H=f[:, o + 2 * d + 2 * d * d:o + 2 * d + 3 * d * d].view(B * H, d, d))
+    return dict(t=i[:, 0], mC=f[:, 1], EC=f[:, 2], CP=f[:, 3], etau=f[:, 4], ml=f[:, 5],
+                El=f[:, 6], LP=f[:, 7], C=f[:, o:o + d], L=f[:, o + d:o + 2 * d],
+                mu=f[:, o + 2 * d:o + 3 * d],
+                F=f[:, o + 3 * d:o + 3 * d + d * d].view(B * H, d, d),
+                G=f[:, o + 3 * d + d * d:o + 3 * d + 2 * d * d].view(B * H, d, d),
+                H=f[:, o + 3 * d + 2 * d * d:o + 3 * d + 3 * d * d].view(B * H, d, d))

@@ -9,7 +9,7 @@
 #include <string>
 #include <unordered_map>
 
-#include "../../include/zeros.h"
+#include "zeros.h"
 #include "zs_common.cuh"
 #include "zs_internal.h"
 
@@ -239,7 +239,7 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
   a.dbg_P = dbg_P;
   a.dbg_m = dbg_m;
   a.status = ws->status;
-  if (rope) {
+  if (rope && !use_chunk) {  // the chunked kernel computes its rotary factors itself
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
   cudaError_t e = use_chunk ? launch_fwd_chunk(a, st) : launch_fwd_simt(a, st);

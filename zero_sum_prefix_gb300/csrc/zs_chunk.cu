@@ -20,19 +20,20 @@
 //     e^{M_{c-1} - M_c} before each chunk's update.
 //   The weight is formed in fp32 before it is rounded: the three terms of w nearly cancel (the
 //   weights sum to zero), so rounding them separately would amplify bf16 rounding errors.
-//   The scalars s, m, Et = E e^{-m}, P follow the canonical fp32 token order of zs_common.cuh
+//   The scalars s, m, Et = E e^{-m}, P follow the canonical blocked fp32 order of zs_common.cuh
 //   (bit-identical to the decode step).
 //
-// Warp roles (352 threads, one CTA per (b, h, value slice), one CTA per SM):
-//   warp 10    (T) : TMA producer: q and k chunks land 128B-swizzled directly in the operand
-//                    tiles, the value slice in a 64B-swizzled staging tile (two stages at d=64).
-//   warps 0-3  (P) : per token row: rotate q/k in place (RoPE), norms, gates, row coefficients,
-//                    column scalars and the scaled value tile Vsc.
+// Warp roles (320 threads, one CTA per (b, h, value slice), one CTA per SM):
+//   warp 9     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
+//                    the operand tiles and the value slice into a 64B-swizzled staging tile (two
+//                    stages at d = 64); lane 1 streams each chunk's u rows (one buffer).
+//   warps 0-3  (P) : warp w owns the 32-token block w of the chunk: the block's column sums,
+//                    logits and local scalar chains (carries of earlier blocks through shared
+//                    memory); then per token row: rotate q/k in place (RoPE), norms, gates, row
+//                    coefficients, column scalars and the scaled value tile Vsc.
 //   warps 4-7  (E) : TMEM -> registers: masked Q K^T -> bf16 tile; state -> bf16 tile (and the
 //                    F~ rescale); X -> output rows.
-//   warp 8     (S) : the sequential scalar chain (prior-mean sums, logits, m, Et, P), 32 tokens
-//                    per batch, running ahead of the other roles through a 2-slot ring.
-//   warp 9     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
+//   warp 8     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
 // TMEM (512 columns): [0,128) Q K^T, [128,256) X, [256, 256 + d) state^T.
 // Every mbarrier wait is bounded in time; a timeout records ZEROS_ERR_TIMEOUT, raises a CTA
 // abort flag and every role leaves its loop; TMEM is released after the last MMA completes.
@@ -51,7 +52,7 @@ using namespace sm100;
 
 constexpr int kC = 128;       // tokens per chunk
 constexpr int kDV = 32;       // value columns per CTA
-constexpr int kThreads = 352;
+constexpr int kThreads = 320;
 constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] bf16 atom tile
 
 template <int D>
@@ -66,8 +67,13 @@ struct Cfg {
   static constexpr uint32_t SST_OFF = AM_OFF + 2 * kTile;
   static constexpr uint32_t COEF_OFF = SST_OFF + KA * kTile;     // float4 [NS][128] row coefs
   static constexpr uint32_t COLS_OFF = COEF_OFF + NS * kC * 16;  // float [NS][3][128] columns
-  static constexpr uint32_t SCAL_OFF = COLS_OFF + NS * 3 * kC * 4;  // float [2][4][128]
-  static constexpr uint32_t MISC_OFF = SCAL_OFF + 2 * 4 * kC * 4;
+  static constexpr uint32_t U_OFF = COLS_OFF + NS * 3 * kC * 4;     // bf16 [128][D] u rows
+  static constexpr uint32_t PHI_OFF = U_OFF + kC * D * 2;             // float [2][D/2] base angles
+  static constexpr uint32_t THETA_OFF = PHI_OFF + 2 * (D / 2) * 4;    // float [D/2] frequencies
+  static constexpr uint32_t LEND_OFF = THETA_OFF + (D / 2) * 4;       // float [4][D]
+  static constexpr uint32_t BPUB_OFF = LEND_OFF + 4 * D * 4;         // float [4][4] + [2][4]
+  static constexpr uint32_t CHAIN_OFF = BPUB_OFF + 128;               // float4 [4][32]
+  static constexpr uint32_t MISC_OFF = CHAIN_OFF + 4 * 32 * 16;
   static constexpr uint32_t BYTES = MISC_OFF + 512;
   static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
   static constexpr uint32_t TM_A = 0, TM_X = 128, TM_ST = 256;
@@ -75,10 +81,10 @@ struct Cfg {
 
 struct Misc {
   uint64_t tma_full[2];
-  uint64_t scal_full[2], scal_empty[2];
+  uint64_t u_full, u_empty;
   uint64_t op_full[2], op_empty[2];
   uint64_t a_full, a_free, am_full, sst_full, x_full, x_free, st_done, fin;
-  float Mslot[2];
+  uint64_t pbar;  // reusable barrier of the four operand warps (bounded waits)
   float Mop[2];
   uint32_t tmem;
   int abort;
@@ -87,145 +93,13 @@ struct Misc {
 
 struct ChunkParams {
   CUtensorMap tq, tk, tv;  // q, k: box {64, 128, 1} 128B swizzle; v: box {32, 128, 1} 64B swizzle
+  CUtensorMap tu;          // u: box {d, 128, 1}, no swizzle (dense 2d-byte rows)
   FwdArgs a;
 };
 
 __device__ __forceinline__ void fail_wait(Misc* ms, int* status) {
   report(status, kErrTimeout);
   ms->abort = 1;
-}
-
-// ============================================================================ S: scalar chain
-template <int D>
-__device__ void role_scalar(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
-                            size_t row0, int nch) {
-  constexpr int R = D / 32;
-  const int lane = threadIdx.x & 31;
-  const __nv_bfloat16* __restrict__ u = static_cast<const __nv_bfloat16*>(a.u) + row0 * D;
-  float* ring = reinterpret_cast<float*>(smem + Cfg<D>::SCAL_OFF);
-  const int N = a.N;
-  const bool dbg = blockIdx.y == 0;
-  const float etau = expf(a.tau[h]);
-  const float sqrtd = __fsqrt_rn((float)D);
-  float S[R], mu[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    S[r] = 0.0f;
-    mu[r] = a.mu[(size_t)h * D + lane + 32 * r];
-  }
-  float m_c = -INFINITY, E_c = 0.0f, P_c = 0.0f;
-
-  for (int c = 0; c < nch; ++c) {
-    const int slot = c & 1;
-    if (c >= 2 && !mbar_wait_warp(&ms->scal_empty[slot], ((c >> 1) - 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
-      return;
-    }
-    float* rs = ring + slot * 4 * kC;
-    for (int b = 0; b < kC / 32; ++b) {
-      const int i0 = c * kC + b * 32;
-      // column chains: lane owns columns lane + 32 r; partial dot of every token of the batch
-      float pp[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int i = i0 + j;
-        // unconditional (clamped) loads so the whole batch can be in flight at once
-        const int ic = i < N ? i : N - 1;
-        float uu[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) uu[r] = __bfloat162float(u[(size_t)ic * D + lane + 32 * r]);
-        if (i < N) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) S[r] = __fadd_rn(S[r], uu[r]);
-        } else {
-#pragma unroll
-          for (int r = 0; r < R; ++r) uu[r] = 0.0f;
-        }
-        float p = __fmul_rn(uu[0], __fmaf_rn(etau, mu[0], S[0]));
-#pragma unroll
-        for (int r = 1; r < R; ++r) p = __fmaf_rn(uu[r], __fmaf_rn(etau, mu[r], S[r]), p);
-        pp[j] = p;
-      }
-      // transpose-reduce: the butterfly tree of zs_common.cuh for 32 tokens at once;
-      // afterwards lane l holds the full dot of token i0 + l.
-#pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
-#pragma unroll
-        for (int k = 0; k < w; ++k) {
-          const float send = up ? pp[k] : pp[k + w];
-          const float keep = up ? pp[k + w] : pp[k];
-          const float recv = __shfl_xor_sync(0xffffffffu, send, w);
-          pp[k] = __fadd_rn(keep, recv);
-        }
-      }
-      const int i = i0 + lane;
-      const bool valid = i < N;
-      const float den = __fmul_rn(__fadd_rn(etau, (float)(i + 1)), sqrtd);
-      const float s = -__fdiv_rn(pp[0], den);
-      if (valid && !isfinite(s)) report(a.status, kErrRange);
-      // running maximum (exact under any order), then f = e^{m_prev - m}, g = e^{s - m}
-      float mm = valid ? s : -INFINITY;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float x = __shfl_up_sync(0xffffffffu, mm, o);
-        if (lane >= o) mm = fmaxf(mm, x);
-      }
-      mm = fmaxf(mm, m_c);
-      float mprev = __shfl_up_sync(0xffffffffu, mm, 1);
-      if (lane == 0) mprev = m_c;
-      const float f = expf(__fsub_rn(mprev, mm));
-      const float g = expf(__fsub_rn(s, mm));
-      // the two sequential chains, in token order, evaluated redundantly by every lane
-      float myE = 0.0f, myP = 0.0f;
-      const int nvalid = min(32, N - i0);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float sj = __shfl_sync(0xffffffffu, s, j);
-        const float fj = __shfl_sync(0xffffffffu, f, j);
-        const float gj = __shfl_sync(0xffffffffu, g, j);
-        if (j < nvalid) {
-          P_c = __fadd_rn(P_c, sj);
-          E_c = __fmaf_rn(E_c, fj, gj);
-        }
-        if (lane == j) {
-          myE = E_c;
-          myP = P_c;
-        }
-      }
-      m_c = __shfl_sync(0xffffffffu, mm, 31);
-      const int r = b * 32 + lane;
-      rs[0 * kC + r] = s;
-      rs[1 * kC + r] = mm;
-      rs[2 * kC + r] = myE;
-      rs[3 * kC + r] = myP;
-      if (dbg && valid) {
-        if (a.dbg_s) a.dbg_s[row0 + i] = s;
-        if (a.dbg_E) a.dbg_E[row0 + i] = myE;
-        if (a.dbg_P) a.dbg_P[row0 + i] = myP;
-        if (a.dbg_m) a.dbg_m[row0 + i] = mm;
-      }
-    }
-    if (lane == 0) ms->Mslot[slot] = m_c;
-    mbar_arrive(&ms->scal_full[slot]);  // 32 arrivals: every lane releases its own writes
-  }
-
-  if (a.final_state && blockIdx.y == 0) {
-    float* rec = record_ptr(a.final_state, bh, D);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      rec[rec_S(D) + lane + 32 * r] = S[r];
-      rec[rec_mu(D) + lane + 32 * r] = mu[r];
-    }
-    if (lane == 0) {
-      RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
-      hd->t = N;
-      hd->m = m_c;
-      hd->Et = E_c;
-      hd->P = P_c;
-      hd->etau = etau;
-    }
-  }
 }
 
 // ============================================================================ T: TMA producer
@@ -256,131 +130,386 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
   }
 }
 
-// ============================================================================ P: operands
-// Rotates (RoPE) row r of a 128B-swizzled bf16 tile in place and returns its squared norm.
-// Pairs are (a, a + D/2); cs holds (cos, sin) of the D/2 pairs of this row's position.
+// u rows of each chunk (single buffer, released by the operand warps after their logits); a
+// separate producer thread so that this stream never waits behind the operand stages.
 template <int D>
-__device__ __forceinline__ float rotate_inplace(uint8_t* tile, int r, bool rope,
-                                                const float4 (&cs)[D / 4]) {
+__device__ void role_tma_u(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch) {
+  using CF = Cfg<D>;
+  const uint32_t base = smem_u32(smem);
+  tma_prefetch_desc(&p.tu);
+  for (int c = 0; c < nch; ++c) {
+    if (c >= 1 && !mbar_wait(&ms->u_empty, (c - 1) & 1, &ms->abort)) {
+      fail_wait(ms, p.a.status);
+      return;
+    }
+    mbar_arrive_expect_tx(&ms->u_full, kC * D * 2);
+    tma_load_3d(base + CF::U_OFF, &p.tu, 0, c * kC, bh, &ms->u_full);
+  }
+}
+
+// ============================================================================ P: operands
+// Rotates (RoPE) pair group g (pairs 8g .. 8g+7 with partners + D/2) of row r of a
+// 128B-swizzled bf16 tile in place and accumulates the row's squared norm into ss (two
+// partial sums).  cs[k] = (cos, sin) of pair 8g + k.
+template <int D>
+__device__ __forceinline__ void rotate_group(uint8_t* tile, int r, int g, bool rope,
+                                             const float2 (&cs)[8], float2& ss) {
   constexpr int HALF = D / 2;
-  float ss = 0.0f;
+  const int ca = 8 * g, cb = 8 * g + HALF;
+  uint4* pa = reinterpret_cast<uint4*>(tile + (ca / 64) * kTile + sw128_off(r, (ca % 64) / 8));
+  uint4* pb = reinterpret_cast<uint4*>(tile + (cb / 64) * kTile + sw128_off(r, (cb % 64) / 8));
+  const uint4 lo = *pa, hi = *pb;
+  const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t oa[4], ob[4];
 #pragma unroll
-  for (int g = 0; g < HALF / 8; ++g) {
-    const int ca = 8 * g, cb = 8 * g + HALF;
-    uint4* pa = reinterpret_cast<uint4*>(tile + (ca / 64) * kTile + sw128_off(r, (ca % 64) / 8));
-    uint4* pb = reinterpret_cast<uint4*>(tile + (cb / 64) * kTile + sw128_off(r, (cb % 64) / 8));
-    const uint4 lo = *pa, hi = *pb;
-    float xa[8], xb[8];
-    const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      unpack_bf16x2(wl[k], xa[2 * k], xa[2 * k + 1]);
-      unpack_bf16x2(wh[k], xb[2 * k], xb[2 * k + 1]);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      ss = __fmaf_rn(xa[k], xa[k], ss);
-      ss = __fmaf_rn(xb[k], xb[k], ss);
-    }
+  for (int k = 0; k < 4; ++k) {
+    float2 xa, xb;  // elements (2k, 2k+1) of the two halves
+    unpack_bf16x2(wl[k], xa.x, xa.y);
+    unpack_bf16x2(wh[k], xb.x, xb.y);
+    ss = __ffma2_rn(xa, xa, ss);
+    ss = __ffma2_rn(xb, xb, ss);
     if (rope) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 t = cs[4 * g + k];  // (cos, sin) of pairs 8g+2k and 8g+2k+1
-        const float a0 = xa[2 * k], b0 = xb[2 * k], a1 = xa[2 * k + 1], b1 = xb[2 * k + 1];
-        xa[2 * k] = __fsub_rn(__fmul_rn(a0, t.x), __fmul_rn(b0, t.y));
-        xb[2 * k] = __fadd_rn(__fmul_rn(a0, t.y), __fmul_rn(b0, t.x));
-        xa[2 * k + 1] = __fsub_rn(__fmul_rn(a1, t.z), __fmul_rn(b1, t.w));
-        xb[2 * k + 1] = __fadd_rn(__fmul_rn(a1, t.w), __fmul_rn(b1, t.z));
-      }
-      uint4 oa, ob;
-      oa.x = pack_bf16x2(xa[0], xa[1]);
-      oa.y = pack_bf16x2(xa[2], xa[3]);
-      oa.z = pack_bf16x2(xa[4], xa[5]);
-      oa.w = pack_bf16x2(xa[6], xa[7]);
-      ob.x = pack_bf16x2(xb[0], xb[1]);
-      ob.y = pack_bf16x2(xb[2], xb[3]);
-      ob.z = pack_bf16x2(xb[4], xb[5]);
-      ob.w = pack_bf16x2(xb[6], xb[7]);
-      *pa = oa;
-      *pb = ob;
+      // pair (a, b) -> (a c - b s, a s + b c), one pair per component of the f32x2 ops
+      const float2 c2 = make_float2(cs[2 * k].x, cs[2 * k + 1].x);
+      const float2 s2 = make_float2(cs[2 * k].y, cs[2 * k + 1].y);
+      const float2 na = __ffma2_rn(xa, c2, __fmul2_rn(make_float2(-xb.x, -xb.y), s2));
+      const float2 nb = __ffma2_rn(xa, s2, __fmul2_rn(xb, c2));
+      oa[k] = pack_bf16x2(na.x, na.y);
+      ob[k] = pack_bf16x2(nb.x, nb.y);
     }
   }
-  return ss;
+  if (rope) {
+    *pa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *pb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
+// The per-token scalars of one 32-token block, by the warp that owns the block (the canonical
+// blocked order of zs_common.cuh).  Lane l owns columns R l + r while the column sums run; after
+// the reduction lane j owns token j of the block.  Carries of the previous blocks arrive through
+// shared memory (two bounded barriers among the four operand warps per chunk).
+struct BlockCarry {
+  float mC, EC, CP;
+};
+
+__device__ __forceinline__ void fold_block(BlockCarry& k, float LP, float ml, float El) {
+  const float P = __fadd_rn(k.CP, LP);
+  const float m = fmaxf(k.mC, ml);
+  const float Et = __fmaf_rn(k.EC, expf(__fsub_rn(k.mC, m)), __fmul_rn(El, expf(__fsub_rn(ml, m))));
+  k.CP = P;
+  k.mC = m;
+  k.EC = Et;
+}
+
+// Column values (R per lane) of token j of a 32-token block in the staged u tile.
+template <int R>
+struct UCols {
+  float2 v[(R + 1) / 2];
+};
+
+template <int D>
+__device__ __forceinline__ UCols<D / 32> load_ucols(const uint8_t* us, int j) {
+  constexpr int R = D / 32;
+  UCols<R> o;
+  if (R == 1) {
+    const uint16_t hv = *reinterpret_cast<const uint16_t*>(us + (size_t)j * D * 2);
+    o.v[0] = make_float2(__uint_as_float((uint32_t)hv << 16), 0.0f);
+  } else if (R == 2) {
+    const uint32_t wv = *reinterpret_cast<const uint32_t*>(us + (size_t)j * D * 2);
+    unpack_bf16x2(wv, o.v[0].x, o.v[0].y);
+  } else {
+    const uint2 wv = *reinterpret_cast<const uint2*>(us + (size_t)j * D * 2);
+    unpack_bf16x2(wv.x, o.v[0].x, o.v[0].y);
+    unpack_bf16x2(wv.y, o.v[(R + 1) / 2 - 1].x, o.v[(R + 1) / 2 - 1].y);
+  }
+  return o;
 }
 
 template <int D>
-__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t row0, int nch) {
+__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
+                              size_t row0, int nch) {
   using CF = Cfg<D>;
+  constexpr int R = D / 32;
+  constexpr int RP = (R + 1) / 2;  // column pairs per lane (R = 1 uses the .x half only)
   const int r = threadIdx.x;  // token row inside the chunk, 0..127
+  const int w = r >> 5, lane = r & 31;
   const int N = a.N;
-  const float* ring = reinterpret_cast<const float*>(smem + CF::SCAL_OFF);
   float4* coef = reinterpret_cast<float4*>(smem + CF::COEF_OFF);
   float* colsc = reinterpret_cast<float*>(smem + CF::COLS_OFF);
+  float* lend = reinterpret_cast<float*>(smem + CF::LEND_OFF);    // [4][D]
+  float* bpub = reinterpret_cast<float*>(smem + CF::BPUB_OFF);    // [4][4] + kc [2][4]
+  float4* chain = reinterpret_cast<float4*>(smem + CF::CHAIN_OFF);  // [4][32] (s, f, g, -)
+  float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
+  float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
+  const bool dbg = blockIdx.y == 0;
+  const float etau = expf(a.tau[h]);
+  const float sqrtd = __fsqrt_rn((float)D);
+  const float2 etau2 = make_float2(etau, etau);
+  float2 mu2[RP], Cc[RP];
+#pragma unroll
+  for (int x = 0; x < RP; ++x) {
+    mu2[x] = make_float2(a.mu[(size_t)h * D + R * lane + 2 * x],
+                         R > 1 ? a.mu[(size_t)h * D + R * lane + 2 * x + 1] : 0.0f);
+    Cc[x] = make_float2(0.0f, 0.0f);
+  }
+  if (r == 0) {
+    bpub[16 + 0] = -INFINITY;  // chunk-start carries (mC, EC, CP) for chunk 0
+    bpub[16 + 1] = 0.0f;
+    bpub[16 + 2] = 0.0f;
+  }
+  const double two_pi = 6.283185307179586476925286766559;
+  constexpr int PPW = (D / 2 + 3) / 4;  // rotary pairs per warp
+  const int pj = w * PPW + lane;
+  const bool owns_pair = a.rope && lane < PPW && pj < D / 2;
+  double theta_d = 0.0;
+  if (owns_pair) {
+    theta_d = pow((double)a.rope_base, -2.0 * (double)pj / (double)D);
+    theta[pj] = (float)theta_d;
+  }
 
   for (int c = 0; c < nch; ++c) {
     const int st = c % CF::NS;
     const int i = c * kC + r;
     const bool valid = i < N;
-    // loads that do not depend on the TMA tiles go out first
-    float4 cs[D / 4];
-    if (a.rope) {
-      const float4* tab = reinterpret_cast<const float4*>(a.rope_table + (size_t)min(i, N - 1) * (D / 2));
-#pragma unroll
-      for (int x = 0; x < D / 4; ++x) cs[x] = __ldg(tab + x);
-    }
+    const int b0 = c * kC + 32 * w;  // first token of this warp's block
+    const int nvalid = max(0, min(32, N - b0));
     float g1 = 0.0f, gh = 0.0f;
     if (valid) {
       g1 = __ldg(a.g1 + row0 + i);
       gh = __ldg(a.gh + row0 + i);
     }
-    if (!mbar_wait(&ms->tma_full[st], (c / CF::NS) & 1, &ms->abort)) {
+    // rotary base angle of this chunk per pair, reduced modulo 2 pi in fp64; token r of the
+    // chunk then uses phi_j + r theta_j (read after the first exchange below)
+    if (owns_pair) {
+      const double ang = (double)(c * kC) * theta_d;
+      phi[(c & 1) * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
+    }
+    // ---- u of the block from the staged tile: lane owns columns R lane .. R lane + R - 1 ----
+    if (!mbar_wait_warp(&ms->u_full, c & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    const uint8_t* us = smem + CF::U_OFF + (size_t)(32 * w) * D * 2 + R * lane * 2;
+    // ---- phase 1: local column sums of the block -> its end value ----
+    float2 L[RP];
+#pragma unroll
+    for (int x = 0; x < RP; ++x) L[x] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const UCols<R> uj = load_ucols<D>(us, j);
+#pragma unroll
+      for (int x = 0; x < RP; ++x) L[x] = __fadd2_rn(L[x], uj.v[x]);
+    }
+#pragma unroll
+    for (int x = 0; x < RP; ++x) {
+      lend[w * D + R * lane + 2 * x] = L[x].x;
+      if (R > 1) lend[w * D + R * lane + 2 * x + 1] = L[x].y;
+    }
+    mbar_arrive(&ms->pbar);
+    if (!mbar_wait_warp(&ms->pbar, (2 * c) & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    // ---- column carry at this block's start (and at the next chunk's start) ----
+    float2 Cw[RP];
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) {
+      if (ww == w) {
+#pragma unroll
+        for (int x = 0; x < RP; ++x) Cw[x] = Cc[x];
+      }
+#pragma unroll
+      for (int x = 0; x < RP; ++x) {
+        const float2 le = make_float2(lend[ww * D + R * lane + 2 * x],
+                                      R > 1 ? lend[ww * D + R * lane + 2 * x + 1] : 0.0f);
+        Cc[x] = __fadd2_rn(Cc[x], le);
+      }
+    }
+    // ---- phase 2: S = C + L per token, logit partial products (two tokens per f32x2) ----
+    float pp[32];
+#pragma unroll
+    for (int x = 0; x < RP; ++x) L[x] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const UCols<R> u0 = load_ucols<D>(us, j), u1 = load_ucols<D>(us, j + 1);
+      float2 n0[RP], n1[RP];
+#pragma unroll
+      for (int x = 0; x < RP; ++x) {
+        L[x] = __fadd2_rn(L[x], u0.v[x]);
+        n0[x] = __ffma2_rn(etau2, mu2[x], __fadd2_rn(Cw[x], L[x]));
+        L[x] = __fadd2_rn(L[x], u1.v[x]);
+        n1[x] = __ffma2_rn(etau2, mu2[x], __fadd2_rn(Cw[x], L[x]));
+      }
+      // p = u[R l] n[R l], then fma over the lane's remaining columns, for tokens j and j + 1
+      float2 p = __fmul2_rn(make_float2(u0.v[0].x, u1.v[0].x), make_float2(n0[0].x, n1[0].x));
+#pragma unroll
+      for (int col = 1; col < R; ++col) {
+        const int x = col >> 1;
+        const float a0 = (col & 1) ? u0.v[x].y : u0.v[x].x, a1 = (col & 1) ? u1.v[x].y : u1.v[x].x;
+        const float m0 = (col & 1) ? n0[x].y : n0[x].x, m1 = (col & 1) ? n1[x].y : n1[x].x;
+        p = __ffma2_rn(make_float2(a0, a1), make_float2(m0, m1), p);
+      }
+      pp[j] = p.x;
+      pp[j + 1] = p.y;
+    }
+    mbar_arrive(&ms->u_empty);  // this thread is done with the staged u rows
+    // transpose-reduce: the butterfly tree of the contract for 32 tokens at once; afterwards
+    // lane j holds the full dot of token b0 + j (= this thread's own token row).
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < o; ++k) {
+        const float send = up ? pp[k] : pp[k + o];
+        const float keep = up ? pp[k + o] : pp[k];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+        pp[k] = __fadd_rn(keep, recv);
+      }
+    }
+    const float den = __fmul_rn(__fadd_rn(etau, (float)(i + 1)), sqrtd);
+    const float s = -__fdiv_rn(pp[0], den);
+    if (valid && !isfinite(s)) report(a.status, kErrRange);
+    // ---- block-local running max, scaled exp-sum and logit sum (token order) ----
+    float ml = valid ? s : -INFINITY;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float x = __shfl_up_sync(0xffffffffu, ml, o);
+      if (lane >= o) ml = fmaxf(ml, x);
+    }
+    float mlp = __shfl_up_sync(0xffffffffu, ml, 1);
+    if (lane == 0) mlp = -INFINITY;
+    chain[w * 32 + lane] = make_float4(s, expf(__fsub_rn(mlp, ml)), expf(__fsub_rn(s, ml)), 0.0f);
+    __syncwarp();
+    float LP = 0.0f, El = 0.0f;
+    const int kend = min(nvalid, lane + 1);  // this lane accumulates tokens 0 .. lane
+    for (int k = 0; k < kend; ++k) {
+      const float4 e = chain[w * 32 + k];
+      LP = __fadd_rn(LP, e.x);
+      El = __fmaf_rn(El, e.y, e.z);
+    }
+    if (lane == 31) {  // block end values: tokens 0 .. nvalid-1
+      bpub[w * 4 + 0] = LP;
+      bpub[w * 4 + 1] = ml;
+      bpub[w * 4 + 2] = El;
+    }
+    mbar_arrive(&ms->pbar);
+    if (!mbar_wait_warp(&ms->pbar, (2 * c + 1) & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    // carries at this block's start: chunk-start carries folded over the earlier blocks
+    const float* kcb = bpub + 16 + (c & 1) * 4;
+    BlockCarry kw{kcb[0], kcb[1], kcb[2]};
+    for (int ww = 0; ww < w; ++ww) fold_block(kw, bpub[ww * 4 + 0], bpub[ww * 4 + 1], bpub[ww * 4 + 2]);
+    float M = kw.mC;  // running max at the chunk's last valid token (max is exact)
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, bpub[ww * 4 + 1]);
+    if (w == 3 && lane == 0) {  // chunk-start carries of the next chunk
+      BlockCarry kn = kw;
+      fold_block(kn, bpub[12 + 0], bpub[12 + 1], bpub[12 + 2]);
+      float* kcn = bpub + 16 + ((c + 1) & 1) * 4;
+      kcn[0] = kn.mC;
+      kcn[1] = kn.EC;
+      kcn[2] = kn.CP;
+    }
+    // this token's scalars
+    const float P = __fadd_rn(kw.CP, LP);
+    const float m = fmaxf(kw.mC, ml);
+    const float Et = __fmaf_rn(kw.EC, expf(__fsub_rn(kw.mC, m)), __fmul_rn(El, expf(__fsub_rn(ml, m))));
+    if (dbg && valid) {
+      if (a.dbg_s) a.dbg_s[row0 + i] = s;
+      if (a.dbg_E) a.dbg_E[row0 + i] = Et;
+      if (a.dbg_P) a.dbg_P[row0 + i] = P;
+      if (a.dbg_m) a.dbg_m[row0 + i] = m;
+    }
+    // ---- recurrent state after the last token (prefill), by the warp owning that token ----
+    if (a.final_state && dbg && c == nch - 1 && nvalid > 0 && b0 + nvalid == N) {
+      float* rec = record_ptr(a.final_state, bh, D);
+      const bool closed = nvalid == 32;  // the block is complete: fold it as the decode step does
+      const float LPe = __shfl_sync(0xffffffffu, LP, 31);
+      const float mle = __shfl_sync(0xffffffffu, ml, 31);
+      const float Ele = __shfl_sync(0xffffffffu, El, 31);
+      BlockCarry kf = kw;
+      if (closed) fold_block(kf, LPe, mle, Ele);
+#pragma unroll
+      for (int x = 0; x < RP; ++x) {
+#pragma unroll
+        for (int y = 0; y < 2 && 2 * x + y < R; ++y) {
+          const float cw = y ? Cw[x].y : Cw[x].x, le = y ? L[x].y : L[x].x;
+          rec[rec_C(D) + R * lane + 2 * x + y] = closed ? __fadd_rn(cw, le) : cw;
+          rec[rec_L(D) + R * lane + 2 * x + y] = closed ? 0.0f : le;
+          rec[rec_mu(D) + R * lane + 2 * x + y] = y ? mu2[x].y : mu2[x].x;
+        }
+      }
+      if (lane == 0) {
+        RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
+        hd->t = N;
+        hd->mC = kf.mC;
+        hd->EC = kf.EC;
+        hd->CP = kf.CP;
+        hd->etau = etau;
+        hd->ml = closed ? -INFINITY : mle;
+        hd->El = closed ? 0.0f : Ele;
+        hd->LP = closed ? 0.0f : LPe;
+      }
+    }
+    // ---- operands: rotate q, k in place (TMA tiles), norms ----
+    if (!mbar_wait_warp(&ms->tma_full[st], (c / CF::NS) & 1, &ms->abort)) {
       fail_wait(ms, a.status);
       return;
     }
     uint8_t* qt = smem + CF::Q_OFF + st * CF::KA * kTile;
     uint8_t* kt = smem + CF::K_OFF + st * CF::KA * kTile;
     const bool rot = a.rope != 0 && valid;
-    const float qq = rotate_inplace<D>(qt, r, rot, cs);
-    const float kk = rotate_inplace<D>(kt, r, rot, cs);
+    float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
+    const float* ph = phi + (c & 1) * (D / 2);
+    const float rf = (float)r;
+#pragma unroll
+    for (int g = 0; g < D / 16; ++g) {
+      float2 cs[8];
+      if (rot) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float sn, cn;
+          __sincosf(__fmaf_rn(rf, theta[8 * g + k], ph[8 * g + k]), &sn, &cn);
+          cs[k] = make_float2(cn, sn);
+        }
+      }
+      rotate_group<D>(qt, r, g, rot, cs, qq2);
+      rotate_group<D>(kt, r, g, rot, cs, kk2);
+    }
+    const float qq = __fadd_rn(qq2.x, qq2.y), kk = __fadd_rn(kk2.x, kk2.y);
     // value slice of this token from the staging tile
-    float vv[kDV];
+    float2 vv[kDV / 2];
     {
       const uint8_t* vst = smem + CF::VST_OFF + st * 128 * 64;
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const uint4 w = *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
-        unpack_bf16x2(w.x, vv[8 * x + 0], vv[8 * x + 1]);
-        unpack_bf16x2(w.y, vv[8 * x + 2], vv[8 * x + 3]);
-        unpack_bf16x2(w.z, vv[8 * x + 4], vv[8 * x + 5]);
-        unpack_bf16x2(w.w, vv[8 * x + 6], vv[8 * x + 7]);
+        const uint4 wv = *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
+        unpack_bf16x2(wv.x, vv[4 * x + 0].x, vv[4 * x + 0].y);
+        unpack_bf16x2(wv.y, vv[4 * x + 1].x, vv[4 * x + 1].y);
+        unpack_bf16x2(wv.z, vv[4 * x + 2].x, vv[4 * x + 2].y);
+        unpack_bf16x2(wv.w, vv[4 * x + 3].x, vv[4 * x + 3].y);
       }
     }
-    // scalars of this chunk from the S ring
-    const int slot = c & 1;
-    if (!mbar_wait(&ms->scal_full[slot], (c >> 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
-      return;
-    }
-    const float* rs = ring + slot * 4 * kC;
-    const float s = rs[0 * kC + r], m = rs[1 * kC + r], Et = rs[2 * kC + r], P = rs[3 * kC + r];
-    const float M = ms->Mslot[slot];
-    mbar_arrive(&ms->scal_empty[slot]);
-
-    const float kap = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(kk), 1e-12f));
-    const float rho = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(qq), 1e-12f));
+    // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
+    // contract: fast exp, reciprocal square root and division are accurate enough here)
+    const float kap = rsqrtf(fmaxf(kk, 1e-24f));
+    const float rho = rsqrtf(fmaxf(qq, 1e-24f));
     float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
     float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
-      ce = __fmul_rn(expf(__fsub_rn(s, M)), kap);
+      ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
       cs1 = __fmul_rn(s, kap);
       ck = kap;
-      const float sig1 = sigmoid(g1), sigh = sigmoid(gh);
-      const float rt = __fdiv_rn(1.0f, (float)(i + 1));
-      const float b0 = __fmul_rn(__fsub_rn(sig1, sigh), rt);
-      const float ahat = __fmul_rn(__fdiv_rn(sigh, Et), expf(__fsub_rn(M, m)));
-      cf.x = __fmul_rn(rho, ahat);
-      cf.y = __fmul_rn(rho, b0);
-      cf.z = -__fmul_rn(rho, __fadd_rn(__fmul_rn(__fmul_rn(b0, P), rt), __fmul_rn(sigh, rt)));
+      const float sig1 = __fdividef(1.0f, 1.0f + __expf(-g1));
+      const float sigh = __fdividef(1.0f, 1.0f + __expf(-gh));
+      const float rt = __fdividef(1.0f, (float)(i + 1));
+      const float b0c = (sig1 - sigh) * rt;
+      const float ahat = __fdividef(sigh, Et) * __expf(M - m);
+      cf.x = rho * ahat;
+      cf.y = rho * b0c;
+      cf.z = -rho * (b0c * P * rt + sigh * rt);
       if (!isfinite(cf.x) || !isfinite(ce)) report(a.status, kErrRange);
     }
     coef[st * kC + r] = cf;
@@ -390,29 +519,23 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
     if (r == 0) ms->Mop[st] = M;
     // Vsc row: atom 0 = [v | e v], atom 1 = [s' v | k v]
     uint8_t* vt = smem + CF::V_OFF + st * 2 * kTile;
+    const float2 ce2 = make_float2(ce, ce), cs2 = make_float2(cs1, cs1), ck2 = make_float2(ck, ck);
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      uint4 pv, pe, ps, pk;
-      pv.x = pack_bf16x2(vv[8 * x + 0], vv[8 * x + 1]);
-      pv.y = pack_bf16x2(vv[8 * x + 2], vv[8 * x + 3]);
-      pv.z = pack_bf16x2(vv[8 * x + 4], vv[8 * x + 5]);
-      pv.w = pack_bf16x2(vv[8 * x + 6], vv[8 * x + 7]);
-      pe.x = pack_bf16x2(__fmul_rn(ce, vv[8 * x + 0]), __fmul_rn(ce, vv[8 * x + 1]));
-      pe.y = pack_bf16x2(__fmul_rn(ce, vv[8 * x + 2]), __fmul_rn(ce, vv[8 * x + 3]));
-      pe.z = pack_bf16x2(__fmul_rn(ce, vv[8 * x + 4]), __fmul_rn(ce, vv[8 * x + 5]));
-      pe.w = pack_bf16x2(__fmul_rn(ce, vv[8 * x + 6]), __fmul_rn(ce, vv[8 * x + 7]));
-      ps.x = pack_bf16x2(__fmul_rn(cs1, vv[8 * x + 0]), __fmul_rn(cs1, vv[8 * x + 1]));
-      ps.y = pack_bf16x2(__fmul_rn(cs1, vv[8 * x + 2]), __fmul_rn(cs1, vv[8 * x + 3]));
-      ps.z = pack_bf16x2(__fmul_rn(cs1, vv[8 * x + 4]), __fmul_rn(cs1, vv[8 * x + 5]));
-      ps.w = pack_bf16x2(__fmul_rn(cs1, vv[8 * x + 6]), __fmul_rn(cs1, vv[8 * x + 7]));
-      pk.x = pack_bf16x2(__fmul_rn(ck, vv[8 * x + 0]), __fmul_rn(ck, vv[8 * x + 1]));
-      pk.y = pack_bf16x2(__fmul_rn(ck, vv[8 * x + 2]), __fmul_rn(ck, vv[8 * x + 3]));
-      pk.z = pack_bf16x2(__fmul_rn(ck, vv[8 * x + 4]), __fmul_rn(ck, vv[8 * x + 5]));
-      pk.w = pack_bf16x2(__fmul_rn(ck, vv[8 * x + 6]), __fmul_rn(ck, vv[8 * x + 7]));
-      *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = pv;
-      *reinterpret_cast<uint4*>(vt + sw128_off(r, 4 + x)) = pe;
-      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, x)) = ps;
-      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, 4 + x)) = pk;
+      uint32_t pv[4], pe[4], ps[4], pk[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const float2 v2 = vv[4 * x + y];
+        const float2 e2 = __fmul2_rn(ce2, v2), s2 = __fmul2_rn(cs2, v2), k2 = __fmul2_rn(ck2, v2);
+        pv[y] = pack_bf16x2(v2.x, v2.y);
+        pe[y] = pack_bf16x2(e2.x, e2.y);
+        ps[y] = pack_bf16x2(s2.x, s2.y);
+        pk[y] = pack_bf16x2(k2.x, k2.y);
+      }
+      *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+      *reinterpret_cast<uint4*>(vt + sw128_off(r, 4 + x)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
+      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, x)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, 4 + x)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     fence_proxy_async_smem();
     mbar_arrive(&ms->op_full[st]);
@@ -509,6 +632,8 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     ok = mbar_wait_warp(&ms->op_full[st], (c / CF::NS) & 1, &ms->abort);
     if (!ok) break;
     const float4 cf = coef[st * kC + t];  // (a, b, g) of row t
+    const float2 ra2 = make_float2(cf.x, cf.x), rb2 = make_float2(cf.y, cf.y),
+                 rg2 = make_float2(cf.z, cf.z);
     const float M_cur = ms->Mop[st];
     const float* ce = colsc + (st * 3 + 0) * kC;
     const float* cs = colsc + (st * 3 + 1) * kC;
@@ -539,21 +664,24 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         const float4 s1 = *reinterpret_cast<const float4*>(cs + col0 + 4);
         const float4 k0 = *reinterpret_cast<const float4*>(ck + col0);
         const float4 k1 = *reinterpret_cast<const float4*>(ck + col0 + 4);
-        const float ee[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        float e[8];
-#pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const float w = __fmaf_rn(cf.x, ee[y], __fmaf_rn(cf.y, ss[y], __fmul_rn(cf.z, kk[y])));
-          const float val = __fmul_rn(v[x * 8 + y], w);
-          e[y] = (cb < wq || col0 + y <= t) ? val : 0.0f;
-        }
+        const float2 ee[4] = {make_float2(e0.x, e0.y), make_float2(e0.z, e0.w),
+                              make_float2(e1.x, e1.y), make_float2(e1.z, e1.w)};
+        const float2 ss[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
+                              make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
+        const float2 kk[4] = {make_float2(k0.x, k0.y), make_float2(k0.z, k0.w),
+                              make_float2(k1.x, k1.y), make_float2(k1.z, k1.w)};
         uint4 p;
-        p.x = pack_bf16x2(e[0], e[1]);
-        p.y = pack_bf16x2(e[2], e[3]);
-        p.z = pack_bf16x2(e[4], e[5]);
-        p.w = pack_bf16x2(e[6], e[7]);
+        uint32_t* pw = reinterpret_cast<uint32_t*>(&p);
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float2 wgt = __ffma2_rn(ra2, ee[y], __ffma2_rn(rb2, ss[y], __fmul2_rn(rg2, kk[y])));
+          float2 val = __fmul2_rn(make_float2(v[x * 8 + 2 * y], v[x * 8 + 2 * y + 1]), wgt);
+          if (cb == wq) {  // diagonal block: keep i <= t only
+            if (col0 + 2 * y > t) val.x = 0.0f;
+            if (col0 + 2 * y + 1 > t) val.y = 0.0f;
+          }
+          pw[y] = pack_bf16x2(val.x, val.y);
+        }
         sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
       }
     }
@@ -599,15 +727,20 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     ok = mbar_wait_warp(&ms->x_full, c & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
-    float xf[32], xg[32], xh[32], xs[32];
-    tmem_ld32(tm + CF::TM_X + 96, xs);
+    // o = X_SV + a X_F + b X_G + g X_H, accumulated one 32-column block at a time
+    float o[32];
+    tmem_ld32(tm + CF::TM_X + 96, o);
     if (c >= 1) {
-      tmem_ld32(tm + CF::TM_X + 0, xf);
-      tmem_ld32(tm + CF::TM_X + 32, xg);
-      tmem_ld32(tm + CF::TM_X + 64, xh);
-    } else {
+      float xb[32];
+      tmem_ld32(tm + CF::TM_X + 0, xb);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) xf[j] = xg[j] = xh[j] = 0.0f;
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.x, xb[j], o[j]);
+      tmem_ld32(tm + CF::TM_X + 32, xb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.y, xb[j], o[j]);
+      tmem_ld32(tm + CF::TM_X + 64, xb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.z, xb[j], o[j]);
     }
     tc_fence_before();
     mbar_arrive(&ms->x_free);
@@ -616,18 +749,11 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        float o[8];
-#pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const int j = 8 * x + y;
-          o[y] = __fadd_rn(__fmaf_rn(cf.x, xf[j], __fmaf_rn(cf.y, xg[j], __fmul_rn(cf.z, xh[j]))),
-                           xs[j]);
-        }
         uint4 p;
-        p.x = pack_bf16x2(o[0], o[1]);
-        p.y = pack_bf16x2(o[2], o[3]);
-        p.z = pack_bf16x2(o[4], o[5]);
-        p.w = pack_bf16x2(o[6], o[7]);
+        p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
+        p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
+        p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
+        p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
         dst[x] = p;
       }
     }
@@ -676,8 +802,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tma_full[i], 1);
-      mbar_init(&ms->scal_full[i], 32);
-      mbar_init(&ms->scal_empty[i], 128);
       mbar_init(&ms->op_full[i], 128);
       mbar_init(&ms->op_empty[i], 1);
     }
@@ -689,10 +813,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->x_free, 128);
     mbar_init(&ms->st_done, 1);
     mbar_init(&ms->fin, 1);
+    mbar_init(&ms->pbar, 128);
+    mbar_init(&ms->u_full, 1);
+    mbar_init(&ms->u_empty, 128);
     ms->abort = 0;
     ms->never = 0;
   }
-  if (warp == 9) {
+  if (warp == 8) {
     tmem_alloc(&ms->tmem, 512);
     tmem_relinquish();
   }
@@ -701,20 +828,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   tc_fence_after();
 
   if (warp < 4) {
-    role_operands<D>(a, smem, ms, row0, nch);
+    role_operands<D>(a, smem, ms, bh, h, row0, nch);
   } else if (warp < 8) {
     role_epilogue<D>(a, smem, ms, bh, row0, nch);
   } else if (warp == 8) {
-    role_scalar<D>(a, smem, ms, bh, h, row0, nch);
-  } else if (warp == 9) {
     if ((threadIdx.x & 31) == 0) role_mma<D>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
     role_tma<D>(p, smem, ms, bh, nch);
+  } else if ((threadIdx.x & 31) == 1) {
+    role_tma_u<D>(p, smem, ms, bh, nch);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 8) {
     // every MMA has completed once `fin` fires (it is committed after the last one)
     if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
     tc_fence_after();
@@ -776,7 +903,8 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   if (!make_map(&p.tq, a.q, D, a.N, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&p.tk, a.k, D, a.N, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&p.tv, a.v, D, a.N, BH, kDV, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&p.tv, a.v, D, a.N, BH, kDV, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&p.tu, a.u, D, a.N, BH, D, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorNotSupported;
   dim3 grid(BH, D / kDV);
   chunk_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(p);

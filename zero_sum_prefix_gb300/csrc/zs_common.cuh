@@ -2,24 +2,30 @@
 //
 // The one numerics contract every kernel obeys (so that the logit s_t, the prefix sum P_t,
 // the running maximum m_t and the scaled prefix sum Et_t = E_t e^{-m_t} come out bit-identical
-// whether a sequence is processed by a forward kernel or token by token by the decode kernel):
+// whether a sequence is processed by a forward kernel or token by token by the decode step):
 //
-//   for each new token t (1-based count), with d = 32 R and lane l of a warp owning the columns
-//   a = l + 32 r (r = 0..R-1):
-//     S[a]   <- S[a] + u_t[a]                          fp32, one add per column, token order
-//     n[a]    = fma(e^tau, mu[a], S[a])                numerator of the prior mean times (e^tau+t)
-//     p_l     = u[l]*n[l], then p_l = fma(u[l+32r], n[l+32r], p_l) for r = 1..R-1
-//     dot     = butterfly sum of p_l over the lanes (xor offsets 16, 8, 4, 2, 1; own + partner)
-//     s_t     = -dot / ((e^tau + t) * sqrt(d))
-//     m_t     = max(m_{t-1}, s_t)                      (m_0 = -inf)
-//     Et_t    = fma(Et_{t-1}, exp(m_{t-1} - m_t), exp(s_t - m_t))     (Et_0 = 0)
-//     P_t     = P_{t-1} + s_t
-//   every operation is an explicit round-to-nearest intrinsic (no contraction, no fast math),
-//   and exp is CUDA's expf.  This is the deviation-logit definition of the Paper-Notes page
-//   "ZeroS: Zero-Sum Linear Attention for Efficient Transformers" (method details, "deviation
-//   logits": s_i = -(1/sqrt d) u_i ubar_i^T with ubar_i = (e^tau mu + sum_{j<=i} u_j)/(e^tau + i))
-//   and its prefix sums E_t = sum e^{s_i}, P_t = sum s_i ("linear-time prefix scan"), evaluated
-//   in one fixed fp32 order.  The running maximum keeps every exponential <= 1.
+// Tokens are grouped in blocks of 32 (block b holds tokens 32b+1 .. 32b+32, t 1-based).  Every
+// running quantity is a carry (its value at the end of the previous block) plus a local value
+// accumulated inside the current block, so that the blocks of a chunk can be processed in
+// parallel and then chained by one operation per block.  With d = 32 R and lane l of a warp
+// owning the R contiguous columns a = R l + r:
+//     L[a] <- L[a] + u_t[a]                 (local column sum, reset at each block start)
+//     S[a]  = C[a] + L[a]                   (C = S at the end of the previous block)
+//     n[a]  = fma(e^tau, mu[a], S[a])       (numerator of the prior mean times e^tau + t)
+//     p_l   = u[Rl] n[Rl], then p_l = fma(u[Rl+r], n[Rl+r], p_l) for r = 1..R-1
+//     dot   = butterfly sum of p_l over the lanes (xor offsets 16, 8, 4, 2, 1; own + partner)
+//     s_t   = -dot / ((e^tau + t) sqrt(d))
+//     LP   <- LP + s_t,        P_t = CP + LP
+//     ml'   = max(ml, s_t),    El <- fma(El, exp(ml - ml'), exp(s_t - ml')),  ml <- ml'
+//     m_t   = max(mC, ml),     Et_t = fma(EC, exp(mC - m_t), El exp(ml - m_t))
+//     at a block's last token: C = S, CP = P_t, mC = m_t, EC = Et_t; L = 0, LP = 0,
+//     ml = -inf, El = 0.
+// Every operation is an explicit round-to-nearest intrinsic (no contraction, no fast math) and
+// exp is CUDA's expf.  This evaluates the deviation logits of the Paper-Notes page "ZeroS:
+// Zero-Sum Linear Attention for Efficient Transformers" (method details, "deviation logits":
+// s_i = -(1/sqrt d) u_i ubar_i^T, ubar_i = (e^tau mu + sum_{j<=i} u_j)/(e^tau + i)) and the
+// prefix sums E_t = sum e^{s_i}, P_t = sum s_i of its "linear-time prefix scan" in one fixed
+// fp32 order; the running maximum keeps every exponential <= 1.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -55,26 +61,25 @@ static_assert(sizeof(StateHeader) == 256, "state header is 256 bytes");
 
 struct RecordHead {  // first 32 bytes of every (b, h) record
   int t;
-  float m;
-  float Et;
-  float P;
+  float mC, EC, CP;  // carries at the end of the last completed block
   float etau;
-  float pad[3];
+  float ml, El, LP;  // local values of the current block
 };
 static_assert(sizeof(RecordHead) == 32, "record head is 32 bytes");
 
 __host__ __device__ constexpr size_t record_bytes(int d) {
-  return ((32 + 8 * (size_t)d + 12 * (size_t)d * d) + 255) / 256 * 256;
+  return ((32 + 12 * (size_t)d + 12 * (size_t)d * d) + 255) / 256 * 256;
 }
 __host__ __device__ constexpr size_t state_bytes(int B, int H, int d) {
   return 256 + (size_t)B * H * record_bytes(d);
 }
-// Float offsets inside a record.
-__host__ __device__ constexpr int rec_S(int) { return 8; }
-__host__ __device__ constexpr int rec_mu(int d) { return 8 + d; }
-__host__ __device__ constexpr int rec_F(int d) { return 8 + 2 * d; }
-__host__ __device__ constexpr int rec_G(int d) { return 8 + 2 * d + d * d; }
-__host__ __device__ constexpr int rec_H(int d) { return 8 + 2 * d + 2 * d * d; }
+// Float offsets inside a record: C (column-sum carry), L (local column sums), mu, F~, G, H.
+__host__ __device__ constexpr int rec_C(int) { return 8; }
+__host__ __device__ constexpr int rec_L(int d) { return 8 + d; }
+__host__ __device__ constexpr int rec_mu(int d) { return 8 + 2 * d; }
+__host__ __device__ constexpr int rec_F(int d) { return 8 + 3 * d; }
+__host__ __device__ constexpr int rec_G(int d) { return 8 + 3 * d + d * d; }
+__host__ __device__ constexpr int rec_H(int d) { return 8 + 3 * d + 2 * d * d; }
 
 __device__ __forceinline__ float* record_ptr(void* state, int bh, int d) {
   return reinterpret_cast<float*>(reinterpret_cast<char*>(state) + 256 + (size_t)bh * record_bytes(d));
@@ -98,50 +103,86 @@ __device__ __forceinline__ float sigmoid(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
 }
 
-// Per-token scalar state carried by every path.
+constexpr int kBlk = 32;  // block length of the numerics contract
+
+// Running scalars of one sequence (identical in every lane of the owning warp).
 struct Scalars {
-  float m;   // running maximum of s
-  float Et;  // E_t * exp(-m_t)
-  float P;   // sum of s
+  float mC, EC, CP;  // carries: m, Et and P at the end of the previous block
+  float ml, El, LP;  // block-local running max, scaled exp-sum and logit sum
 };
 
-// The canonical token update above, executed by one full warp.  u, S, mu hold the lane's
-// columns a = lane + 32 r.  Returns s_t (identical in every lane); updates S and sc in place
-// (identical in every lane).  `t` is the 1-based token count including this token.
+__device__ __forceinline__ Scalars scalars_init() {
+  return Scalars{-INFINITY, 0.0f, 0.0f, -INFINITY, 0.0f, 0.0f};
+}
+
+// Logit dot product of one token, canonical lane/tree order (lane owns columns R l + r).
 template <int R>
-__device__ __forceinline__ float token_update(const float (&u)[R], float (&S)[R], const float (&mu)[R],
-                                              float etau, int t, Scalars& sc, float* f_out,
-                                              float* g_out) {
+__device__ __forceinline__ float logit_dot(const float (&u)[R], const float (&n)[R]) {
+  float p = __fmul_rn(u[0], n[0]);
 #pragma unroll
-  for (int r = 0; r < R; ++r) S[r] = __fadd_rn(S[r], u[r]);
-  float p = __fmul_rn(u[0], __fmaf_rn(etau, mu[0], S[0]));
-#pragma unroll
-  for (int r = 1; r < R; ++r) p = __fmaf_rn(u[r], __fmaf_rn(etau, mu[r], S[r]), p);
+  for (int r = 1; r < R; ++r) p = __fmaf_rn(u[r], n[r], p);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
+  return p;
+}
+
+// Per-token outputs of the contract.
+struct TokenOut {
+  float s, P, m, Et;
+  float m_prev;  // m_{t-1} (running max before this token; -inf for the first token)
+};
+
+// The canonical token update, executed by one full warp.  u, C, L, mu hold the lane's columns
+// R l + r.  `t` is the 1-based count including this token.  Updates C, L and sc in place.
+template <int R>
+__device__ __forceinline__ TokenOut token_update(const float (&u)[R], float (&C)[R], float (&L)[R],
+                                                 const float (&mu)[R], float etau, int t,
+                                                 Scalars& sc) {
+  TokenOut o;
+  o.m_prev = fmaxf(sc.mC, sc.ml);
+  float S[R], n[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    L[r] = __fadd_rn(L[r], u[r]);
+    S[r] = __fadd_rn(C[r], L[r]);
+    n[r] = __fmaf_rn(etau, mu[r], S[r]);
+  }
+  const float dot = logit_dot<R>(u, n);
   const float den = __fmul_rn(__fadd_rn(etau, (float)t), __fsqrt_rn((float)(32 * R)));
-  const float s = -__fdiv_rn(p, den);
-  const float m_new = fmaxf(sc.m, s);
-  const float f = expf(__fsub_rn(sc.m, m_new));
-  const float g = expf(__fsub_rn(s, m_new));
-  sc.Et = __fmaf_rn(sc.Et, f, g);
-  sc.P = __fadd_rn(sc.P, s);
-  sc.m = m_new;
-  *f_out = f;
-  *g_out = g;
-  return s;
+  const float s = -__fdiv_rn(dot, den);
+  sc.LP = __fadd_rn(sc.LP, s);
+  const float P = __fadd_rn(sc.CP, sc.LP);
+  const float ml = fmaxf(sc.ml, s);
+  sc.El = __fmaf_rn(sc.El, expf(__fsub_rn(sc.ml, ml)), expf(__fsub_rn(s, ml)));
+  sc.ml = ml;
+  const float m = fmaxf(sc.mC, ml);
+  const float Et = __fmaf_rn(sc.EC, expf(__fsub_rn(sc.mC, m)),
+                             __fmul_rn(sc.El, expf(__fsub_rn(ml, m))));
+  if ((t - 1) % kBlk == kBlk - 1) {  // block end: fold the local values into the carries
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      C[r] = S[r];
+      L[r] = 0.0f;
+    }
+    sc.CP = P;
+    sc.mC = m;
+    sc.EC = Et;
+    sc.LP = 0.0f;
+    sc.ml = -INFINITY;
+    sc.El = 0.0f;
+  }
+  o.s = s;
+  o.P = P;
+  o.m = m;
+  o.Et = Et;
+  return o;
 }
 
 // Logit of one token against a fixed prior numerator n[a] (encoder mode: the full-sequence
 // mean), same lane/tree order as token_update.
 template <int R>
 __device__ __forceinline__ float fixed_logit(const float (&u)[R], const float (&n)[R], float den) {
-  float p = __fmul_rn(u[0], n[0]);
-#pragma unroll
-  for (int r = 1; r < R; ++r) p = __fmaf_rn(u[r], n[r], p);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
-  return -__fdiv_rn(p, den);
+  return -__fdiv_rn(logit_dot<R>(u, n), den);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -44,22 +44,28 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
   const T* __restrict__ v = static_cast<const T*>(a.v) + tok;
   const T* __restrict__ u = static_cast<const T*>(a.u) + tok;
 
-  float S[R];
+  float C[R], L[R];
   Scalars sc;
   if (warp == 0) {
     float uu[R], mu[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      uu[r] = ld(u, lane + 32 * r);
-      S[r] = rec[rec_S(D) + lane + 32 * r];
-      mu[r] = rec[rec_mu(D) + lane + 32 * r];
+      uu[r] = ld(u, R * lane + r);
+      C[r] = rec[rec_C(D) + R * lane + r];
+      L[r] = rec[rec_L(D) + R * lane + r];
+      mu[r] = rec[rec_mu(D) + R * lane + r];
     }
-    sc.m = hd->m;
-    sc.Et = hd->Et;
-    sc.P = hd->P;
+    sc.mC = hd->mC;
+    sc.EC = hd->EC;
+    sc.CP = hd->CP;
+    sc.ml = hd->ml;
+    sc.El = hd->El;
+    sc.LP = hd->LP;
     const float etau = hd->etau;
-    float f, g;
-    const float s = token_update<R>(uu, S, mu, etau, t_old + 1, sc, &f, &g);
+    const TokenOut o = token_update<R>(uu, C, L, mu, etau, t_old + 1, sc);
+    const float s = o.s;
+    const float f = expf(__fsub_rn(o.m_prev, o.m));
+    const float g = expf(__fsub_rn(s, o.m));
     if (lane == 0) {
       if (!isfinite(s)) report(a.status, kErrRange);
       const float sig1 = sigmoid(a.g1[bh]), sigh = sigmoid(a.gh[bh]);
@@ -68,13 +74,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
       coef[0] = s;
       coef[1] = f;
       coef[2] = g;
-      coef[3] = __fdiv_rn(sigh, sc.Et);
+      coef[3] = __fdiv_rn(sigh, o.Et);
       coef[4] = beta;
-      coef[5] = -__fadd_rn(__fmul_rn(__fmul_rn(beta, sc.P), rt), __fmul_rn(sigh, rt));
+      coef[5] = -__fadd_rn(__fmul_rn(__fmul_rn(beta, o.P), rt), __fmul_rn(sigh, rt));
       if (a.dbg_s) a.dbg_s[bh] = s;
-      if (a.dbg_E) a.dbg_E[bh] = sc.Et;
-      if (a.dbg_P) a.dbg_P[bh] = sc.P;
-      if (a.dbg_m) a.dbg_m[bh] = sc.m;
+      if (a.dbg_E) a.dbg_E[bh] = o.Et;
+      if (a.dbg_P) a.dbg_P[bh] = o.P;
+      if (a.dbg_m) a.dbg_m[bh] = o.m;
     }
   } else if (warp == 1 || warp == 2) {
     const T* src = warp == 1 ? q : k;
@@ -165,12 +171,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
   }
   if (warp == 0) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) rec[rec_S(D) + lane + 32 * r] = S[r];
+    for (int r = 0; r < R; ++r) {
+      rec[rec_C(D) + R * lane + r] = C[r];
+      rec[rec_L(D) + R * lane + r] = L[r];
+    }
     if (lane == 0) {
       hd->t = t_old + 1;
-      hd->m = sc.m;
-      hd->Et = sc.Et;
-      hd->P = sc.P;
+      hd->mC = sc.mC;
+      hd->EC = sc.EC;
+      hd->CP = sc.CP;
+      hd->ml = sc.ml;
+      hd->El = sc.El;
+      hd->LP = sc.LP;
     }
   }
 }

@@ -52,25 +52,30 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 #pragma unroll
   for (int r = 0; r < RA; ++r) F[r] = G[r] = Hs[r] = 0.0f;
 
-  // Warp-0 scalar state (canonical order of zs_common.cuh).
-  float S[R], mu[R], nfix[R];
-  Scalars sc{-INFINITY, 0.0f, 0.0f};
+  // Warp-0 scalar state (canonical order of zs_common.cuh; lane owns columns R lane + r).
+  float C[R], L[R], mu[R], nfix[R];
+  Scalars sc = scalars_init();
+  float m_run = -INFINITY, Et_run = 0.0f, P_run = 0.0f;  // encoder chains
   const float etau = expf(a.tau[h]);
   float den_fix = 0.0f;
   if (warp == 0) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      S[r] = 0.0f;
-      mu[r] = a.mu[(size_t)h * D + lane + 32 * r];
+      C[r] = 0.0f;
+      L[r] = 0.0f;
+      mu[r] = a.mu[(size_t)h * D + R * lane + r];
     }
     if (!a.causal) {
       // Encoder: full-sequence prior mean, numerator e^tau mu + sum_j u_j.
+      float Su[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) Su[r] = 0.0f;
       for (int i = 0; i < N; ++i) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) S[r] = __fadd_rn(S[r], ld(u, (size_t)i * D + lane + 32 * r));
+        for (int r = 0; r < R; ++r) Su[r] = __fadd_rn(Su[r], ld(u, (size_t)i * D + R * lane + r));
       }
 #pragma unroll
-      for (int r = 0; r < R; ++r) nfix[r] = __fmaf_rn(etau, mu[r], S[r]);
+      for (int r = 0; r < R; ++r) nfix[r] = __fmaf_rn(etau, mu[r], Su[r]);
       den_fix = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)D));
     }
   }
@@ -102,18 +107,27 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     if (warp == 0) {
       float uu[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) uu[r] = ld(u, (size_t)t * D + lane + 32 * r);
-      float f, g, s;
+      for (int r = 0; r < R; ++r) uu[r] = ld(u, (size_t)t * D + R * lane + r);
+      float f, g, s, Et, P, m;
       if (a.causal) {
-        s = token_update<R>(uu, S, mu, etau, t + 1, sc, &f, &g);
+        const TokenOut o = token_update<R>(uu, C, L, mu, etau, t + 1, sc);
+        s = o.s;
+        Et = o.Et;
+        P = o.P;
+        m = o.m;
+        f = expf(__fsub_rn(o.m_prev, m));
+        g = expf(__fsub_rn(s, m));
       } else {
         s = fixed_logit<R>(uu, nfix, den_fix);
-        const float m_new = fmaxf(sc.m, s);
-        f = expf(__fsub_rn(sc.m, m_new));
+        const float m_new = fmaxf(m_run, s);
+        f = expf(__fsub_rn(m_run, m_new));
         g = expf(__fsub_rn(s, m_new));
-        sc.Et = __fmaf_rn(sc.Et, f, g);
-        sc.P = __fadd_rn(sc.P, s);
-        sc.m = m_new;
+        Et_run = __fmaf_rn(Et_run, f, g);
+        P_run = __fadd_rn(P_run, s);
+        m_run = m_new;
+        Et = Et_run;
+        P = P_run;
+        m = m_run;
       }
       if (lane == 0) {
         if (!isfinite(s)) report(a.status, kErrRange);
@@ -124,14 +138,14 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
           const float sig1 = sigmoid(g1[t]), sigh = sigmoid(gh[t]);
           const float rt = __fdiv_rn(1.0f, (float)(t + 1));
           const float beta = __fmul_rn(__fsub_rn(sig1, sigh), rt);
-          tc.alpha = __fdiv_rn(sigh, sc.Et);
+          tc.alpha = __fdiv_rn(sigh, Et);
           tc.beta = beta;
-          tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, sc.P), rt), __fmul_rn(sigh, rt));
+          tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, P), rt), __fmul_rn(sigh, rt));
           if (blockIdx.y == 0) {
             if (a.dbg_s) a.dbg_s[row0 + t] = s;
-            if (a.dbg_E) a.dbg_E[row0 + t] = sc.Et;
-            if (a.dbg_P) a.dbg_P[row0 + t] = sc.P;
-            if (a.dbg_m) a.dbg_m[row0 + t] = sc.m;
+            if (a.dbg_E) a.dbg_E[row0 + t] = Et;
+            if (a.dbg_P) a.dbg_P[row0 + t] = P;
+            if (a.dbg_m) a.dbg_m[row0 + t] = m;
           }
         } else if (blockIdx.y == 0 && a.dbg_s) {
           a.dbg_s[row0 + t] = s;
@@ -184,16 +198,20 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
       if (blockIdx.y == 0 && warp == 0) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          rec[rec_S(D) + lane + 32 * r] = S[r];
-          rec[rec_mu(D) + lane + 32 * r] = mu[r];
+          rec[rec_C(D) + R * lane + r] = C[r];
+          rec[rec_L(D) + R * lane + r] = L[r];
+          rec[rec_mu(D) + R * lane + r] = mu[r];
         }
         if (lane == 0) {
           RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
           hd->t = N;
-          hd->m = sc.m;
-          hd->Et = sc.Et;
-          hd->P = sc.P;
+          hd->mC = sc.mC;
+          hd->EC = sc.EC;
+          hd->CP = sc.CP;
           hd->etau = etau;
+          hd->ml = sc.ml;
+          hd->El = sc.El;
+          hd->LP = sc.LP;
         }
       }
     }
@@ -203,9 +221,9 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
   // ---- encoder readout: every token against the full-sequence state ----
   __shared__ float fullsc[3];  // Et_N, P_N, m_N
   if (warp == 0 && lane == 0) {
-    fullsc[0] = sc.Et;
-    fullsc[1] = sc.P;
-    fullsc[2] = sc.m;
+    fullsc[0] = Et_run;
+    fullsc[1] = P_run;
+    fullsc[2] = m_run;
   }
   const float rN = __fdiv_rn(1.0f, (float)N);
   for (int t = 0; t < N; ++t) {
@@ -268,11 +286,13 @@ __global__ void state_init_kernel(void* state, const float* __restrict__ mu,
   if (threadIdx.x == 0) {
     RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
     hd->t = 0;
-    hd->m = -INFINITY;
-    hd->Et = 0.0f;
-    hd->P = 0.0f;
+    hd->mC = -INFINITY;
+    hd->EC = 0.0f;
+    hd->CP = 0.0f;
     hd->etau = expf(tau[h]);
-    hd->pad[0] = hd->pad[1] = hd->pad[2] = 0.0f;
+    hd->ml = -INFINITY;
+    hd->El = 0.0f;
+    hd->LP = 0.0f;
   }
 }
 
