@@ -23,17 +23,19 @@
 //   The scalars s, m, Et = E e^{-m}, P follow the canonical blocked fp32 order of zs_common.cuh
 //   (bit-identical to the decode step).
 //
-// Warp roles (320 threads, one CTA per (b, h, value slice), one CTA per SM):
-//   warp 9     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
-//                    the operand tiles and the value slice into a 64B-swizzled staging tile (two
-//                    stages at d = 64); lane 1 streams each chunk's u rows (one buffer).
-//   warps 0-3  (P) : warp w owns the 32-token block w of the chunk: the block's column sums,
-//                    logits and local scalar chains (carries of earlier blocks through shared
-//                    memory); then per token row: rotate q/k in place (RoPE), norms, gates, row
-//                    coefficients, column scalars and the scaled value tile Vsc.
-//   warps 4-7  (E) : TMEM -> registers: masked Q K^T -> bf16 tile; state -> bf16 tile (and the
-//                    F~ rescale); X -> output rows.
-//   warp 8     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
+// Warp roles (448 threads, one CTA per (b, h, value slice), one CTA per SM):
+//   warps 0-3   (PS): warp w owns the 32-token block w of the chunk: the block's column sums,
+//                     logits and local scalar chains (carries of earlier blocks through shared
+//                     memory, two bounded barriers per chunk); hands (s, m, Et, P) per token and
+//                     the chunk reference to PO through a two-slot ring.
+//   warps 4-7   (PO): per token row: rotary factors, rotate q/k in place (RoPE), norms, gates,
+//                     row coefficients, column scalars and the scaled value tile Vsc.
+//   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) x weights -> bf16 tile; state ->
+//                     bf16 tile (and the F~ rescale); X -> output rows.
+//   warp 12     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
+//   warp 13     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
+//                     the operand tiles and the value slice into a 64B-swizzled staging tile (two
+//                     stages at d = 64); lane 1 streams each chunk's u rows (one buffer).
 // TMEM (512 columns): [0,128) Q K^T, [128,256) X, [256, 256 + d) state^T.
 // Every mbarrier wait is bounded in time; a timeout records ZEROS_ERR_TIMEOUT, raises a CTA
 // abort flag and every role leaves its loop; TMEM is released after the last MMA completes.
@@ -52,7 +54,7 @@ using namespace sm100;
 
 constexpr int kC = 128;       // tokens per chunk
 constexpr int kDV = 32;       // value columns per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] bf16 atom tile
 
 template <int D>
@@ -73,7 +75,8 @@ struct Cfg {
   static constexpr uint32_t LEND_OFF = THETA_OFF + (D / 2) * 4;       // float [4][D]
   static constexpr uint32_t BPUB_OFF = LEND_OFF + 4 * D * 4;         // float [4][4] + [2][4]
   static constexpr uint32_t CHAIN_OFF = BPUB_OFF + 128;               // float4 [4][32]
-  static constexpr uint32_t MISC_OFF = CHAIN_OFF + 4 * 32 * 16;
+  static constexpr uint32_t SCAL_OFF = CHAIN_OFF + 4 * 32 * 16;     // float4 [2][128]
+  static constexpr uint32_t MISC_OFF = SCAL_OFF + 2 * kC * 16;
   static constexpr uint32_t BYTES = MISC_OFF + 512;
   static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
   static constexpr uint32_t TM_A = 0, TM_X = 128, TM_ST = 256;
@@ -84,8 +87,11 @@ struct Misc {
   uint64_t u_full, u_empty;
   uint64_t op_full[2], op_empty[2];
   uint64_t a_full, a_free, am_full, sst_full, x_full, x_free, st_done, fin;
-  uint64_t pbar;  // reusable barrier of the four operand warps (bounded waits)
+  uint64_t pbar;   // reusable barrier of the four scalar warps (bounded waits)
+  uint64_t pobar;  // reusable barrier of the four operand warps
+  uint64_t scal_full[2], scal_empty[2];
   float Mop[2];
+  float Mslot[2];
   uint32_t tmem;
   int abort;
   int never;  // stays 0: lets the final TMEM-release wait ignore the abort flag
@@ -225,22 +231,20 @@ __device__ __forceinline__ UCols<D / 32> load_ucols(const uint8_t* us, int j) {
   return o;
 }
 
+// ---------------------------------------------------------------- PS: scalars of the blocks
 template <int D>
-__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
-                              size_t row0, int nch) {
+__device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
+                             size_t row0, int nch) {
   using CF = Cfg<D>;
   constexpr int R = D / 32;
   constexpr int RP = (R + 1) / 2;  // column pairs per lane (R = 1 uses the .x half only)
-  const int r = threadIdx.x;  // token row inside the chunk, 0..127
+  const int r = threadIdx.x;       // token row inside the chunk, 0..127
   const int w = r >> 5, lane = r & 31;
   const int N = a.N;
-  float4* coef = reinterpret_cast<float4*>(smem + CF::COEF_OFF);
-  float* colsc = reinterpret_cast<float*>(smem + CF::COLS_OFF);
-  float* lend = reinterpret_cast<float*>(smem + CF::LEND_OFF);    // [4][D]
-  float* bpub = reinterpret_cast<float*>(smem + CF::BPUB_OFF);    // [4][4] + kc [2][4]
+  float* lend = reinterpret_cast<float*>(smem + CF::LEND_OFF);      // [4][D]
+  float* bpub = reinterpret_cast<float*>(smem + CF::BPUB_OFF);      // [4][4] + kc [2][4]
   float4* chain = reinterpret_cast<float4*>(smem + CF::CHAIN_OFF);  // [4][32] (s, f, g, -)
-  float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
-  float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
+  float4* scal = reinterpret_cast<float4*>(smem + CF::SCAL_OFF);    // [2][128] (s, m, Et, P)
   const bool dbg = blockIdx.y == 0;
   const float etau = expf(a.tau[h]);
   const float sqrtd = __fsqrt_rn((float)D);
@@ -257,33 +261,13 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     bpub[16 + 1] = 0.0f;
     bpub[16 + 2] = 0.0f;
   }
-  const double two_pi = 6.283185307179586476925286766559;
-  constexpr int PPW = (D / 2 + 3) / 4;  // rotary pairs per warp
-  const int pj = w * PPW + lane;
-  const bool owns_pair = a.rope && lane < PPW && pj < D / 2;
-  double theta_d = 0.0;
-  if (owns_pair) {
-    theta_d = pow((double)a.rope_base, -2.0 * (double)pj / (double)D);
-    theta[pj] = (float)theta_d;
-  }
 
   for (int c = 0; c < nch; ++c) {
-    const int st = c % CF::NS;
+    const int slot = c & 1;
     const int i = c * kC + r;
     const bool valid = i < N;
     const int b0 = c * kC + 32 * w;  // first token of this warp's block
     const int nvalid = max(0, min(32, N - b0));
-    float g1 = 0.0f, gh = 0.0f;
-    if (valid) {
-      g1 = __ldg(a.g1 + row0 + i);
-      gh = __ldg(a.gh + row0 + i);
-    }
-    // rotary base angle of this chunk per pair, reduced modulo 2 pi in fp64; token r of the
-    // chunk then uses phi_j + r theta_j (read after the first exchange below)
-    if (owns_pair) {
-      const double ang = (double)(c * kC) * theta_d;
-      phi[(c & 1) * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
-    }
     // ---- u of the block from the staged tile: lane owns columns R lane .. R lane + R - 1 ----
     if (!mbar_wait_warp(&ms->u_full, c & 1, &ms->abort)) {
       fail_wait(ms, a.status);
@@ -294,7 +278,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     float2 L[RP];
 #pragma unroll
     for (int x = 0; x < RP; ++x) L[x] = make_float2(0.0f, 0.0f);
-#pragma unroll
+#pragma unroll 8
     for (int j = 0; j < 32; ++j) {
       const UCols<R> uj = load_ucols<D>(us, j);
 #pragma unroll
@@ -354,7 +338,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     }
     mbar_arrive(&ms->u_empty);  // this thread is done with the staged u rows
     // transpose-reduce: the butterfly tree of the contract for 32 tokens at once; afterwards
-    // lane j holds the full dot of token b0 + j (= this thread's own token row).
+    // lane j holds the full dot of token b0 + j.
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       const bool up = (lane & o) != 0;
@@ -382,10 +366,13 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     __syncwarp();
     float LP = 0.0f, El = 0.0f;
     const int kend = min(nvalid, lane + 1);  // this lane accumulates tokens 0 .. lane
-    for (int k = 0; k < kend; ++k) {
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
       const float4 e = chain[w * 32 + k];
-      LP = __fadd_rn(LP, e.x);
-      El = __fmaf_rn(El, e.y, e.z);
+      if (k < kend) {
+        LP = __fadd_rn(LP, e.x);
+        El = __fmaf_rn(El, e.y, e.z);
+      }
     }
     if (lane == 31) {  // block end values: tokens 0 .. nvalid-1
       bpub[w * 4 + 0] = LP;
@@ -422,6 +409,14 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       if (a.dbg_P) a.dbg_P[row0 + i] = P;
       if (a.dbg_m) a.dbg_m[row0 + i] = m;
     }
+    // hand the scalars to the operand warps (two-slot ring)
+    if (c >= 2 && !mbar_wait_warp(&ms->scal_empty[slot], ((c >> 1) - 1) & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    scal[slot * kC + r] = make_float4(s, m, Et, P);
+    if (r == 0) ms->Mslot[slot] = M;
+    mbar_arrive(&ms->scal_full[slot]);
     // ---- recurrent state after the last token (prefill), by the warp owning that token ----
     if (a.final_state && dbg && c == nch - 1 && nvalid > 0 && b0 + nvalid == N) {
       float* rec = record_ptr(a.final_state, bh, D);
@@ -453,7 +448,54 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         hd->LP = closed ? 0.0f : LPe;
       }
     }
-    // ---- operands: rotate q, k in place (TMA tiles), norms ----
+  }
+}
+
+// ---------------------------------------------------------------- PO: tensor-core operands
+template <int D>
+__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, size_t row0,
+                              int nch) {
+  using CF = Cfg<D>;
+  const int r = threadIdx.x - 128;  // token row inside the chunk, 0..127
+  const int w = r >> 5, lane = r & 31;
+  const int N = a.N;
+  float4* coef = reinterpret_cast<float4*>(smem + CF::COEF_OFF);
+  float* colsc = reinterpret_cast<float*>(smem + CF::COLS_OFF);
+  const float4* scal = reinterpret_cast<const float4*>(smem + CF::SCAL_OFF);
+  float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
+  float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
+  const double two_pi = 6.283185307179586476925286766559;
+  constexpr int PPW = (D / 2 + 3) / 4;  // rotary pairs per warp
+  const int pj = w * PPW + lane;
+  const bool owns_pair = a.rope && lane < PPW && pj < D / 2;
+  double theta_d = 0.0;
+  if (owns_pair) {
+    theta_d = pow((double)a.rope_base, -2.0 * (double)pj / (double)D);
+    theta[pj] = (float)theta_d;
+  }
+
+  for (int c = 0; c < nch; ++c) {
+    const int st = c % CF::NS;
+    const int slot = c & 1;
+    const int i = c * kC + r;
+    const bool valid = i < N;
+    float g1 = 0.0f, gh = 0.0f;
+    if (valid) {
+      g1 = __ldg(a.g1 + row0 + i);
+      gh = __ldg(a.gh + row0 + i);
+    }
+    // rotary base angle of this chunk per pair, reduced modulo 2 pi in fp64; token r of the
+    // chunk then uses phi_j + r theta_j
+    if (owns_pair) {
+      const double ang = (double)(c * kC) * theta_d;
+      phi[(c & 1) * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
+    }
+    mbar_arrive(&ms->pobar);
+    if (!mbar_wait_warp(&ms->pobar, c & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    // ---- rotate q, k in place (TMA tiles), norms ----
     if (!mbar_wait_warp(&ms->tma_full[st], (c / CF::NS) & 1, &ms->abort)) {
       fail_wait(ms, a.status);
       return;
@@ -464,7 +506,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
     const float* ph = phi + (c & 1) * (D / 2);
     const float rf = (float)r;
-#pragma unroll
+#pragma unroll 1
     for (int g = 0; g < D / 16; ++g) {
       float2 cs[8];
       if (rot) {
@@ -492,6 +534,15 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         unpack_bf16x2(wv.w, vv[4 * x + 3].x, vv[4 * x + 3].y);
       }
     }
+    // ---- scalars of this token from the scalar warps ----
+    if (!mbar_wait_warp(&ms->scal_full[slot], (c >> 1) & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    const float4 sc = scal[slot * kC + r];
+    const float M = ms->Mslot[slot];
+    mbar_arrive(&ms->scal_empty[slot]);
+    const float s = sc.x, m = sc.y, Et = sc.z, P = sc.w;
     // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
     // contract: fast exp, reciprocal square root and division are accurate enough here)
     const float kap = rsqrtf(fmaxf(kk, 1e-24f));
@@ -643,7 +694,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     if (!ok) break;
     tc_fence_after();
     const uint32_t sm = base + CF::AM_OFF;
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
       if (cb > wq) {  // every column of this block is after every row of this warp
 #pragma unroll
@@ -670,8 +721,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
                               make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
         const float2 kk[4] = {make_float2(k0.x, k0.y), make_float2(k0.z, k0.w),
                               make_float2(k1.x, k1.y), make_float2(k1.z, k1.w)};
-        uint4 p;
-        uint32_t* pw = reinterpret_cast<uint32_t*>(&p);
+        uint32_t pw[4];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
           const float2 wgt = __ffma2_rn(ra2, ee[y], __ffma2_rn(rb2, ss[y], __fmul2_rn(rg2, kk[y])));
@@ -682,6 +732,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
           }
           pw[y] = pack_bf16x2(val.x, val.y);
         }
+        const uint4 p = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
       }
     }
@@ -698,7 +749,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         const bool rescale = (wq == 1) && (M_cur > M_prev);
         const float fac = rescale ? expf(__fsub_rn(M_prev, M_cur)) : 1.0f;
         const uint32_t sst = base + CF::SST_OFF;
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           float v[32];
           tmem_ld32(tm + CF::TM_ST + cb * 32, v);
@@ -814,12 +865,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->st_done, 1);
     mbar_init(&ms->fin, 1);
     mbar_init(&ms->pbar, 128);
+    mbar_init(&ms->pobar, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->scal_full[i], 128);
+      mbar_init(&ms->scal_empty[i], 128);
+    }
     mbar_init(&ms->u_full, 1);
     mbar_init(&ms->u_empty, 128);
     ms->abort = 0;
     ms->never = 0;
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(&ms->tmem, 512);
     tmem_relinquish();
   }
@@ -828,10 +884,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   tc_fence_after();
 
   if (warp < 4) {
-    role_operands<D>(a, smem, ms, bh, h, row0, nch);
+    role_scalars<D>(a, smem, ms, bh, h, row0, nch);
   } else if (warp < 8) {
+    role_operands<D>(a, smem, ms, h, row0, nch);
+  } else if (warp < 12) {
     role_epilogue<D>(a, smem, ms, bh, row0, nch);
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     if ((threadIdx.x & 31) == 0) role_mma<D>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
     role_tma<D>(p, smem, ms, bh, nch);
@@ -841,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     // every MMA has completed once `fin` fires (it is committed after the last one)
     if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
     tc_fence_after();
