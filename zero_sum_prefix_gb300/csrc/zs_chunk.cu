@@ -36,7 +36,8 @@
 //   warp 13     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
 //                     the operand tiles and the value slice into a 64B-swizzled staging tile (two
 //                     stages at d = 64); lane 1 streams each chunk's u rows (one buffer).
-// TMEM (512 columns): [0,128) Q K^T, [128,256) X, [256, 256 + d) state^T.
+// TMEM (512 columns): [0,128) Q K^T, [128,384) X (two buffers, chunk parity), [384, 384 + d)
+// state^T.
 // Every mbarrier wait is bounded in time; a timeout records ZEROS_ERR_TIMEOUT, raises a CTA
 // abort flag and every role leaves its loop; TMEM is released after the last MMA completes.
 #include <math.h>
@@ -79,14 +80,15 @@ struct Cfg {
   static constexpr uint32_t MISC_OFF = SCAL_OFF + 2 * kC * 16;
   static constexpr uint32_t BYTES = MISC_OFF + 512;
   static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
-  static constexpr uint32_t TM_A = 0, TM_X = 128, TM_ST = 256;
+  static constexpr uint32_t TM_A = 0, TM_X = 128, TM_ST = 384;  // X: two buffers of 128
 };
 
 struct Misc {
   uint64_t tma_full[2];
   uint64_t u_full, u_empty;
   uint64_t op_full[2], op_empty[2];
-  uint64_t a_full, a_free, am_full, sst_full, x_full, x_free, st_done, fin;
+  uint64_t a_full, a_free, am_full, sst_full, st_done, fin;
+  uint64_t x_full[2], x_free[2];
   uint64_t pbar;   // reusable barrier of the four scalar warps (bounded waits)
   uint64_t pobar;  // reusable barrier of the four operand warps
   uint64_t scal_full[2], scal_empty[2];
@@ -624,16 +626,17 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
     mma_commit(&ms->a_full);
     ok = mbar_wait(&ms->am_full, c & 1, &ms->abort);
     if (ok && c >= 1) ok = mbar_wait(&ms->sst_full, (c - 1) & 1, &ms->abort);
-    if (ok && c >= 1) ok = mbar_wait(&ms->x_free, (c - 1) & 1, &ms->abort);
+    if (ok && c >= 2) ok = mbar_wait(&ms->x_free[c & 1], ((c >> 1) - 1) & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
+    const uint32_t tXc = tX + (uint32_t)(c & 1) * 128;
     // ---- X[:, 0:96] = Q [F~ | G | H] (previous chunks); X[:, 96:128] = S V ----
     if (c >= 1) {
       const uint32_t sst = base + CF::SST_OFF + 32 * 128;  // state rows 32..127
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
-        mma_bf16(tX, sw128_desc(qt + off, 16, 1024), sw128_desc(sst + off, 16, 1024), id_qs,
+        mma_bf16(tXc, sw128_desc(qt + off, 16, 1024), sw128_desc(sst + off, 16, 1024), id_qs,
                  kk > 0);
       }
     }
@@ -642,10 +645,10 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
     for (int kk = 0; kk < kC / 16; ++kk) {
       const uint32_t aoff = (kk / 4) * kTile + (kk % 4) * 32;  // K-major, K = token i
       const uint32_t boff = kk * 2048;                          // MN-major, 16 rows per step
-      mma_bf16(tX + 96, sw128_desc(sm + aoff, 16, 1024), sw128_desc(vt + boff, kTile, 1024),
+      mma_bf16(tXc + 96, sw128_desc(sm + aoff, 16, 1024), sw128_desc(vt + boff, kTile, 1024),
                id_sv, kk > 0);
     }
-    mma_commit(&ms->x_full);
+    mma_commit(&ms->x_full[c & 1]);
     // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
@@ -677,6 +680,44 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out) + row0 * D;
   float M_prev = 0.0f;
   bool ok = true;
+  float4 cf_prev = make_float4(0.f, 0.f, 0.f, 0.f);
+  // o = X_SV + a X_F + b X_G + g X_H for chunk cc, one 32-column block at a time
+  auto xstep = [&](int cc, const float4 cfc) -> bool {
+    const int xb_par = cc & 1;
+    if (!mbar_wait_warp(&ms->x_full[xb_par], (cc >> 1) & 1, &ms->abort)) return false;
+    tc_fence_after();
+    const uint32_t tx = tm + CF::TM_X + (uint32_t)xb_par * 128;
+    float o[32];
+    tmem_ld32(tx + 96, o);
+    if (cc >= 1) {
+      float xb[32];
+      tmem_ld32(tx + 0, xb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.x, xb[j], o[j]);
+      tmem_ld32(tx + 32, xb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.y, xb[j], o[j]);
+      tmem_ld32(tx + 64, xb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.z, xb[j], o[j]);
+    }
+    tc_fence_before();
+    mbar_arrive(&ms->x_free[xb_par]);
+    const int i = cc * kC + t;
+    if (i < N) {
+      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        uint4 p;
+        p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
+        p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
+        p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
+        p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
+        dst[x] = p;
+      }
+    }
+    return true;
+  };
 
   for (int c = 0; c < nch && ok; ++c) {
     const int st = c % CF::NS;
@@ -774,42 +815,16 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       fence_proxy_async_smem();
       mbar_arrive(&ms->sst_full);
     }
-    // ---- X -> output row t ----
-    ok = mbar_wait_warp(&ms->x_full, c & 1, &ms->abort);
-    if (!ok) break;
-    tc_fence_after();
-    // o = X_SV + a X_F + b X_G + g X_H, accumulated one 32-column block at a time
-    float o[32];
-    tmem_ld32(tm + CF::TM_X + 96, o);
+    // ---- output rows of the previous chunk (its X was computed while this chunk's S and
+    // state tiles were being formed) ----
     if (c >= 1) {
-      float xb[32];
-      tmem_ld32(tm + CF::TM_X + 0, xb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.x, xb[j], o[j]);
-      tmem_ld32(tm + CF::TM_X + 32, xb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.y, xb[j], o[j]);
-      tmem_ld32(tm + CF::TM_X + 64, xb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cf.z, xb[j], o[j]);
+      ok = xstep(c - 1, cf_prev);
+      if (!ok) break;
     }
-    tc_fence_before();
-    mbar_arrive(&ms->x_free);
-    const int i = c * kC + t;
-    if (i < N) {
-      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        uint4 p;
-        p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
-        p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
-        p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
-        p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
-        dst[x] = p;
-      }
-    }
+    cf_prev = cf;
     M_prev = M_cur;
   }
+  if (ok && nch > 0) ok = xstep(nch - 1, cf_prev);
   if (!ok) {
     fail_wait(ms, a.status);
     return;
@@ -860,8 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->a_free, 128);
     mbar_init(&ms->am_full, 128);
     mbar_init(&ms->sst_full, 128);
-    mbar_init(&ms->x_full, 1);
-    mbar_init(&ms->x_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->x_full[i], 1);
+      mbar_init(&ms->x_free[i], 128);
+    }
     mbar_init(&ms->st_done, 1);
     mbar_init(&ms->fin, 1);
     mbar_init(&ms->pbar, 128);
