@@ -94,6 +94,29 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
                  void* stream);
 
 /*
+ * Allocation-free forward (the pages have no counterpart: this entry point exists for callers
+ * that must not allocate device memory themselves or through this library, for example code
+ * whose device memory is all handed out up front by its own allocator, or a runtime that forbids
+ * cudaMalloc once it is serving).  Same computation and layouts as zeros_fwd_ex on the
+ * token-sequential path (ZEROS_PATH_SIMT), without final state or debug outputs.
+ *   - It calls no cudaMalloc / cudaFree and no allocating routine.  Its only scratch, the rotary
+ *     (cos, sin) table, lives in a fixed 1 MiB device array compiled into the library, which every
+ *     device that loads the library holds until the process exits; with rope = 1 it needs
+ *     N * d / 2 <= 131072 and returns ZEROS_ERR_UNSUPPORTED beyond that.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - Every call rewrites the shared table, so calls that overlap on the GPU (different streams
+ *     at the same time) race; serialise them.
+ *   - status: nullable device int, caller-owned.  It is zeroed on `stream` at the start of the
+ *     call and receives the first device-side error (ZEROS_ERR_RANGE ...); read it after the
+ *     stream has finished.  The library's own status word (zeros_get_status) is not used.
+ */
+int zeros_fwd_noalloc(const void* q, const void* k, const void* v, const void* u,
+                      const float* g1, const float* gh, const float* mu, const float* tau,
+                      void* out, int B, int H, int N, int d, int causal, int rope, int dtype,
+                      float rope_base, int* status, void* stream);
+
+/*
  * Recurrent state ("the state is the checkpoint").  Size in bytes of the blob for B x H
  * sequences of head dimension d (0 for unsupported d).  Layout: a 256-byte header
  * {magic "ZSP1", version, B, H, d, dtype, rope, rope_base} followed by B*H records of

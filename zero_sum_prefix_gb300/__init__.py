@@ -28,7 +28,7 @@ PATHS = {"auto": 0, "simt": 1, "chunk": 2}
 EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record_bytes",
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
-           "zeros_kernel_launches"]
+           "zeros_kernel_launches", "zeros_fwd_noalloc"]
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def load():
         lib.zeros_last_error_message.restype = ctypes.c_char_p
         lib.zeros_version.restype = i
         lib.zeros_kernel_launches.restype = ctypes.c_ulonglong
+        lib.zeros_fwd_noalloc.argtypes = [vp] * 9 + [i] * 7 + [f, vp, vp]
+        lib.zeros_fwd_noalloc.restype = i
         _lib = lib
         return lib
 

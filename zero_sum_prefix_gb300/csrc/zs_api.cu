@@ -255,6 +255,65 @@ int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const 
                       stream);
 }
 
+int zeros_fwd_noalloc(const void* q, const void* k, const void* v, const void* u,
+                      const float* g1, const float* gh, const float* mu, const float* tau,
+                      void* out, int B, int H, int N, int d, int causal, int rope, int dtype,
+                      float rope_base, int* status, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_dims(B, H, N, d)) return rc;
+  if (int rc = check_dtype(dtype)) return rc;
+  if (causal != 0 && causal != 1) return fail(ZEROS_ERR_INVALID, "causal must be 0 or 1");
+  if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
+  if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
+  const bool empty = (long long)B * H * N == 0;
+  const char* names[] = {"q", "k", "v", "u", "g1", "gh", "mu", "tau", "out"};
+  const void* ptrs[] = {q, k, v, u, g1, gh, mu, tau, out};
+  if (!empty)
+    for (int i = 0; i < 9; ++i)
+      if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u))
+    return fail(ZEROS_ERR_INVALID, "status is not 4-byte aligned");
+  if (rope && (size_t)N * (size_t)(d / 2) > kNoAllocRopeEntries)
+    return fail(ZEROS_ERR_UNSUPPORTED,
+                "zeros_fwd_noalloc: N * d / 2 exceeds its fixed rotary scratch of 131072 entries");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (status) {
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  }
+  if (empty) return ZEROS_OK;
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.u = u;
+  a.g1 = g1;
+  a.gh = gh;
+  a.mu = mu;
+  a.tau = tau;
+  a.out = out;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.rope = rope;
+  a.dtype = dtype;
+  a.rope_base = rope_base;
+  a.status = status;
+  if (rope) {
+    float2* table = nullptr;
+    cudaError_t e = noalloc_rope_table(&table);
+    if (e != cudaSuccess) return cuda_fail(e, "looking up the fixed rotary scratch");
+    e = launch_rope_table(table, N, d, (double)rope_base, st);  // rewritten on every call
+    if (e != cudaSuccess) return cuda_fail(e, "rotary table launch");
+    a.rope_table = table;
+  }
+  cudaError_t e = launch_fwd_simt(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ZEROS_OK;
+}
+
 int zeros_state_init(void* state, const float* mu, const float* tau, int B, int H, int d,
                      int dtype, int rope, float rope_base, void* stream) {
   g_last_error.clear();

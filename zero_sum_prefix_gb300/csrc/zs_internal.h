@@ -43,6 +43,11 @@ cudaError_t launch_state_header(void* state, int B, int H, int d, int dtype, int
                                 float rope_base, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* table, int N, int d, double base, cudaStream_t stream);
 
+// Fixed scratch of the allocation-free forward: (cos, sin) entries for N * d/2 <= this bound.
+constexpr size_t kNoAllocRopeEntries = size_t(1) << 17;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t noalloc_rope_table(float2** table);
+
 // zs_chunk.cu
 bool chunk_supported(int d, int dtype, int causal);
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);

@@ -14,6 +14,8 @@
 // normalise / rotate q_t and k_t and stage v_t in shared memory.
 #include <math.h>
 
+#include <mutex>
+
 #include "zs_common.cuh"
 #include "zs_internal.h"
 
@@ -332,6 +334,32 @@ __global__ void rope_table_kernel(float2* table, int N, int d, double base) {
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------------------------------
+// Scratch of the allocation-free forward (zeros_fwd_noalloc): the rotary table lives in this
+// fixed device array instead of the library workspace.  Every device that loads the library
+// holds it (1 MiB) until the process exits.
+static __device__ __align__(256) float2 g_noalloc_rope[kNoAllocRopeEntries];
+
+cudaError_t noalloc_rope_table(float2** table) {
+  // Host code cannot use the array's name as a device address: ask the runtime for it (once
+  // per device, with that device current).
+  static std::mutex mtx;
+  static float2* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mtx);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_rope);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float2*>(p);
+  }
+  *table = addr[dev];
+  return cudaSuccess;
+}
 
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream) {
   return a.dtype == 1 ? launch_simt_typed<float>(a, stream)
