@@ -11,33 +11,42 @@
 //   and rho_t = 1/|q_t|, kappa_i = 1/|k_i|, row coefficients (a, b, g)_t = rho_t (alphâ_t,
 //   beta_t, gamma_t) with alphâ_t = sigh_t e^{M_c - m_t} / Et_t and column scalars
 //   (e, s', k)_i = (e^{s_i - M_c} kappa_i, s_i kappa_i, kappa_i):
-//     intra  S_{t,i} = [i <= t] (Q_t . K_i) (a_t e_i + b_t s'_i + g_t k_i)   (fp32, rounded once)
+//     W_{t,i} = a_t e_i + b_t s'_i + g_t k_i        (tensor core, hi/lo bf16 split, fp32 sum)
+//     intra  S_{t,i} = [i <= t] (Q_t . K_i) W_{t,i} (fp32 product, rounded once to bf16)
 //     Vsc_i = [ v_i | e_i v_i | s'_i v_i | k_i v_i ]                          (C x 128, bf16)
 //     X[:, 0:96]   = Q [F~ | G | H]   (state of the previous chunks)
 //     X[:, 96:128] = S V
 //     o_t = a_t X_F + b_t X_G + g_t X_H + X_SV
 //     state^T (128 x d; rows [unused | F~ | G | H]) += Vsc^T K, F~ rescaled by
 //     e^{M_{c-1} - M_c} before each chunk's update.
-//   The weight is formed in fp32 before it is rounded: the three terms of w nearly cancel (the
-//   weights sum to zero), so rounding them separately would amplify bf16 rounding errors.
-//   The scalars s, m, Et = E e^{-m}, P follow the canonical blocked fp32 order of zs_common.cuh
-//   (bit-identical to the decode step).
+//   The weight is formed to fp32 accuracy before the product is rounded: the three terms of w
+//   nearly cancel (the weights sum to zero), so rounding them separately would amplify bf16
+//   rounding errors.  The scalars s, m, Et = E e^{-m}, P follow the canonical blocked fp32 order
+//   of zs_common.cuh (bit-identical to the decode step).
+//
+// Cluster pairs: the two CTAs of a cluster hold two value slices of the same (b, h).  Chunk c is
+// owned by CTA c % 2: only the owner streams the chunk's q, k and u, computes its scalars
+// (carries of the previous chunk arrive from the other CTA through distributed shared memory),
+// rotates q and k and forms the weight operands and coefficients, then bulk-copies the rotated
+// tiles, the weight operands and the coefficients into the other CTA's stage.  Each CTA builds
+// its own scaled value tile, issues its own MMAs and writes its own output columns.  Stage
+// releases and the weight-operand release are multicast to both CTAs.
 //
 // Warp roles (448 threads, one CTA per (b, h, value slice), one CTA per SM):
-//   warps 0-3   (PS): warp w owns the 32-token block w of the chunk: the block's column sums,
+//   warps 0,1,4,5 (PS): warp w owns the 32-token block w of the chunk: the block's column sums,
 //                     logits and local scalar chains (carries of earlier blocks through shared
 //                     memory, two bounded barriers per chunk); hands (s, m, Et, P) per token and
 //                     the chunk reference to PO through a two-slot ring.
-//   warps 4-7   (PO): per token row: rotary factors, rotate q/k in place (RoPE), norms, gates,
-//                     row coefficients, column scalars and the scaled value tile Vsc.
-//   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) x weights -> bf16 tile; state ->
-//                     bf16 tile (and the F~ rescale); X -> output rows.
+//   warps 2,3,6,7 (PO): per token row: rotary factors, rotate q/k in place (RoPE), norms, gates,
+//                     row coefficients, the hi/lo weight operands and the scaled value tile Vsc.
+//   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> bf16 tile; state -> bf16
+//                     tile (and the F~ rescale); X -> output rows.
 //   warp 12     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
 //   warp 13     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
-//                     the operand tiles and the value slice into a 64B-swizzled staging tile (two
-//                     stages at d = 64); lane 1 streams each chunk's u rows (one buffer).
-// TMEM (512 columns): [0,128) Q K^T, [128,384) X (two buffers, chunk parity), [384, 384 + d)
-// state^T.
+//                     the operand tiles (two stages at d = 64) and the value slice into a
+//                     64B-swizzled staging tile, with an L2 prefetch of each chunk issued before
+//                     its stage frees; lane 1 streams each chunk's u rows (one buffer).
+// TMEM (512 columns): [0,128) Q K^T, [128,256) W, [256,384) X, [384, 384 + d) state^T.
 // Every mbarrier wait is bounded in time; a timeout records ZEROS_ERR_TIMEOUT, raises a CTA
 // abort flag and every role leaves its loop; TMEM is released after the last MMA completes.
 #include <math.h>
@@ -55,8 +64,23 @@ using namespace sm100;
 
 constexpr int kC = 128;       // tokens per chunk
 constexpr int kDV = 32;       // value columns per CTA
+constexpr int kCL = 1;  // CTAs per cluster (value slices sharing one (b, h)); 1 or 2
 constexpr int kThreads = 448;
 constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] bf16 atom tile
+
+__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
+  return (x + a - 1) / a * a;
+}
+
+// Per-stage coefficients of a chunk: row coefficients (a, b, g), column scalars (e, s', k) and
+// the chunk reference M_c; copied by the chunk's owner into the other CTA of the cluster.
+struct Xch {
+  float4 coef[kC];
+  float cols[3][kC];
+  float M;
+  float pad[3];
+};
+static_assert(sizeof(Xch) == 3600, "Xch is moved by one bulk copy (multiple of 16 bytes)");
 
 template <int D>
 struct Cfg {
@@ -65,38 +89,49 @@ struct Cfg {
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NS * KA * kTile;
   static constexpr uint32_t V_OFF = K_OFF + NS * KA * kTile;
-  static constexpr uint32_t VST_OFF = V_OFF + NS * 2 * kTile;    // raw v slices [NS][128 x 32]
-  static constexpr uint32_t AM_OFF = VST_OFF + NS * 128 * 64;
+  static constexpr uint32_t VST_OFF = V_OFF + NS * 2 * kTile;    // raw v slice [128 x 32]
+  static constexpr uint32_t AM_OFF = VST_OFF + 128 * 64;
   static constexpr uint32_t SST_OFF = AM_OFF + 2 * kTile;
-  static constexpr uint32_t COEF_OFF = SST_OFF + KA * kTile;     // float4 [NS][128] row coefs
-  static constexpr uint32_t COLS_OFF = COEF_OFF + NS * kC * 16;  // float [NS][3][128] columns
-  static constexpr uint32_t U_OFF = COLS_OFF + NS * 3 * kC * 4;     // bf16 [128][D] u rows
+  static constexpr uint32_t RW_OFF = SST_OFF + KA * kTile;       // weight MMA A: [128 x 16] bf16
+  static constexpr uint32_t CW_OFF = RW_OFF + kC * 32;           // weight MMA B: [128 x 16] bf16
+  static constexpr uint32_t XCH_OFF = CW_OFF + kC * 32;          // Xch [NS]
+  static constexpr uint32_t U_OFF = align_up(XCH_OFF + NS * (uint32_t)sizeof(Xch), 1024);
   static constexpr uint32_t PHI_OFF = U_OFF + kC * D * 2;             // float [2][D/2] base angles
   static constexpr uint32_t THETA_OFF = PHI_OFF + 2 * (D / 2) * 4;    // float [D/2] frequencies
   static constexpr uint32_t LEND_OFF = THETA_OFF + (D / 2) * 4;       // float [4][D]
   static constexpr uint32_t BPUB_OFF = LEND_OFF + 4 * D * 4;         // float [4][4] + [2][4]
   static constexpr uint32_t CHAIN_OFF = BPUB_OFF + 128;               // float4 [4][32]
   static constexpr uint32_t SCAL_OFF = CHAIN_OFF + 4 * 32 * 16;     // float4 [2][128]
-  static constexpr uint32_t MISC_OFF = SCAL_OFF + 2 * kC * 16;
+  static constexpr uint32_t CIN_OFF = SCAL_OFF + 2 * kC * 16;       // float [2][D] column carries
+  static constexpr uint32_t KCIN_OFF = CIN_OFF + 2 * D * 4;         // float [2][4] scalar carries
+  static constexpr uint32_t MISC_OFF = KCIN_OFF + 32;
   static constexpr uint32_t BYTES = MISC_OFF + 512;
   static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
-  static constexpr uint32_t TM_A = 0, TM_X = 128, TM_ST = 384;  // X: two buffers of 128
+  static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
+  // bytes a non-owner receives per chunk: rotated Q and K, the weight operands, the Xch block
+  static constexpr uint32_t PEER_BYTES = 2 * KA * kTile + 2 * kC * 32 + (uint32_t)sizeof(Xch);
+  static_assert(SMEM <= 232448, "shared memory budget of one CTA");
 };
 
 struct Misc {
   uint64_t tma_full[2];
-  uint64_t u_full, u_empty;
-  uint64_t op_full[2], op_empty[2];
-  uint64_t a_full, a_free, am_full, sst_full, st_done, fin;
-  uint64_t x_full[2], x_free[2];
-  uint64_t pbar;   // reusable barrier of the four scalar warps (bounded waits)
-  uint64_t pobar;  // reusable barrier of the four operand warps
+  uint64_t u_full, u_empty, vst_empty;
+  uint64_t op_full, vsc_full;        // Vsc of an owned / other-owned chunk written
+  uint64_t qk_empty[2];  // Q, K and Xch of a stage released by every CTA of the cluster
+  uint64_t vsc_free[2];  // Vsc of the last chunk of this parity consumed (S V completed)
+  uint64_t a_full, a_free, am_full, sst_full, sst_free, st_done, fin;
+  uint64_t w_done;                   // both CTAs' weight MMAs have read R and C
+  uint64_t x_full, x_free;
+  uint64_t pbar;     // reusable barrier of the four scalar warps (bounded waits)
+  uint64_t pobar;    // reusable barrier of the four operand warps
+  uint64_t po_sync;  // Q, K, R, C and Xch of an owned chunk written
   uint64_t scal_full[2], scal_empty[2];
-  float Mop[2];
+  uint64_t peer_full;            // tiles of a chunk owned by the other CTA have landed
+  uint64_t ccar_full, kcar_full;  // carries from the other CTA's previous chunk
   float Mslot[2];
   uint32_t tmem;
   int abort;
-  int never;  // stays 0: lets the final TMEM-release wait ignore the abort flag
+  int never;  // stays 0: lets the final waits ignore the abort flag
 };
 
 struct ChunkParams {
@@ -105,50 +140,150 @@ struct ChunkParams {
   FwdArgs a;
 };
 
+template <int CL>
 __device__ __forceinline__ void fail_wait(Misc* ms, int* status) {
   report(status, kErrTimeout);
   ms->abort = 1;
+  if (CL > 1) st_cluster_s32(mapa(smem_u32(&ms->abort), cluster_rank() ^ 1u), 1);
+}
+
+__device__ __forceinline__ Xch* xch(uint8_t* smem, uint32_t off, int st) {
+  return reinterpret_cast<Xch*>(smem + off) + st;
+}
+
+// Load barrier of chunk c and the parity of its phase.  Without a cluster, one barrier per
+// stage; with a cluster, one per owner, so that the operand warps (chunks of this CTA) and the
+// epilogue warps (chunks of the other CTA) each wait for consecutive phases of their own barrier
+// (a parity wait names its phase only when the previous phase has completed and the next one
+// cannot have).
+template <int D, int CL>
+__device__ __forceinline__ int tf_index(int c) {
+  return CL > 1 ? c % CL : c % Cfg<D>::NS;
+}
+template <int D, int CL>
+__device__ __forceinline__ uint32_t tf_phase(int c) {
+  return (uint32_t)(CL > 1 ? c / CL : c / Cfg<D>::NS) & 1u;
+}
+
+// Before the Vsc tile of chunk c is written: the S V product of chunk c - NS (same stage) has
+// completed.  One barrier per chunk parity, so that each builder role (operand warps for this
+// CTA's chunks, epilogue warps for the other CTA's) waits for consecutive phases of its own.
+template <int D, int CL>
+__device__ __forceinline__ bool vsc_wait(Misc* ms, int c) {
+  constexpr int NS = Cfg<D>::NS;
+  if (c < NS) return true;
+  return mbar_wait_warp(&ms->vsc_free[(c - NS) & 1], (uint32_t)((c - NS) >> 1) & 1u, &ms->abort);
+}
+
+// Raw value row r (64B-swizzled staging tile) -> columns 0..31 of the Vsc tile (bf16 words).
+__device__ __forceinline__ void copy_v_row(uint8_t* vt, const uint8_t* vst, int r) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) =
+        *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
+}
+
+// Vsc row r: atom 0 = [v | e v], atom 1 = [s' v | k v] from the row's v (already in columns
+// 0..31) and its column scalars (e, s', k).
+__device__ __forceinline__ void build_vsc_row(uint8_t* vt, int r, float ce, float cs1, float ck) {
+  const float2 ce2 = make_float2(ce, ce), cs2 = make_float2(cs1, cs1), ck2 = make_float2(ck, ck);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(vt + sw128_off(r, x));
+    const uint32_t pv[4] = {wv.x, wv.y, wv.z, wv.w};
+    uint32_t pe[4], ps[4], pk[4];
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      float2 v2;
+      unpack_bf16x2(pv[y], v2.x, v2.y);
+      const float2 e2 = __fmul2_rn(ce2, v2), s2 = __fmul2_rn(cs2, v2), k2 = __fmul2_rn(ck2, v2);
+      pe[y] = pack_bf16x2(e2.x, e2.y);
+      ps[y] = pack_bf16x2(s2.x, s2.y);
+      pk[y] = pack_bf16x2(k2.x, k2.y);
+    }
+    *reinterpret_cast<uint4*>(vt + sw128_off(r, 4 + x)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
+    *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, x)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+    *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, 4 + x)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// Warps 0, 1, 4, 5 are the scalar warps and 2, 3, 6, 7 the operand warps (warp w runs on
+// sub-partition w % 4, so each of these sub-partitions interleaves one role's code with the
+// epilogue's); both roles number their warps 0..3 in this order.
+__device__ __forceinline__ int group_index() {
+  const int warp = threadIdx.x >> 5;
+  return (warp & 1) | ((warp >> 2) << 1);
 }
 
 // ============================================================================ T: TMA producer
-template <int D>
-__device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch) {
+// Every CTA streams its value slice for every chunk; q and k only for the chunks it owns.
+template <int D, int CL>
+__device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
+                         int rank) {
   using CF = Cfg<D>;
   const uint32_t base = smem_u32(smem);
   const int j0 = blockIdx.y * kDV;
-  constexpr uint32_t bytes = 2 * CF::KA * kTile + 128 * 64;
+  constexpr uint32_t qk_bytes = 2 * CF::KA * kTile, v_bytes = 128 * 64;
   tma_prefetch_desc(&p.tq);
   tma_prefetch_desc(&p.tk);
   tma_prefetch_desc(&p.tv);
   for (int c = 0; c < nch; ++c) {
     const int st = c % CF::NS;
-    if (c >= CF::NS && !mbar_wait(&ms->op_empty[st], ((c / CF::NS) - 1) & 1, &ms->abort)) {
-      fail_wait(ms, p.a.status);
+    const bool owned = (c % CL) == rank;
+    if (c >= CF::NS) {
+      // the chunk's tiles start towards L2 while the stage is still in use
+      if (owned) {
+#pragma unroll
+        for (int at = 0; at < CF::KA; ++at) {
+          tma_prefetch_3d(&p.tq, 64 * at, c * kC, bh);
+          tma_prefetch_3d(&p.tk, 64 * at, c * kC, bh);
+        }
+      }
+      tma_prefetch_3d(&p.tv, j0, c * kC, bh);
+      // both CTAs of the cluster have released the stage's Q, K and Xch
+      if (!mbar_wait_cl(&ms->qk_empty[st], ((c / CF::NS) - 1) & 1, &ms->abort)) {
+        fail_wait<CL>(ms, p.a.status);
+        return;
+      }
+    }
+    // a chunk owned by the other CTA: its tiles arrive by bulk copy (the previous phase of
+    // peer_full completed before this chunk's stage was released)
+    if (CL > 1 && !owned) mbar_arrive_expect_tx(&ms->peer_full, CF::PEER_BYTES);
+    uint64_t* tf = &ms->tma_full[tf_index<D, CL>(c)];
+    mbar_arrive_expect_tx(tf, (owned ? qk_bytes : 0u) + v_bytes);
+    if (owned) {
+      const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
+      const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
+#pragma unroll
+      for (int at = 0; at < CF::KA; ++at) {
+        tma_load_3d(qt + at * kTile, &p.tq, 64 * at, c * kC, bh, tf);
+        tma_load_3d(kt + at * kTile, &p.tk, 64 * at, c * kC, bh, tf);
+      }
+    }
+    // the raw value slice has one buffer, released by the operand warps once copied
+    if (c >= 1 && !mbar_wait(&ms->vst_empty, (c - 1) & 1, &ms->abort)) {
+      fail_wait<CL>(ms, p.a.status);
       return;
     }
-    mbar_arrive_expect_tx(&ms->tma_full[st], bytes);
-    const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
-    const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
-#pragma unroll
-    for (int at = 0; at < CF::KA; ++at) {
-      tma_load_3d(qt + at * kTile, &p.tq, 64 * at, c * kC, bh, &ms->tma_full[st]);
-      tma_load_3d(kt + at * kTile, &p.tk, 64 * at, c * kC, bh, &ms->tma_full[st]);
-    }
-    tma_load_3d(base + CF::VST_OFF + st * 128 * 64, &p.tv, j0, c * kC, bh, &ms->tma_full[st]);
+    tma_load_3d(base + CF::VST_OFF, &p.tv, j0, c * kC, bh, tf);
   }
 }
 
-// u rows of each chunk (single buffer, released by the operand warps after their logits); a
-// separate producer thread so that this stream never waits behind the operand stages.
-template <int D>
-__device__ void role_tma_u(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch) {
+// u rows of each owned chunk (single buffer, released by the scalar warps after their logits);
+// a separate producer thread so that this stream never waits behind the operand stages.
+template <int D, int CL>
+__device__ void role_tma_u(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
+                           int rank) {
   using CF = Cfg<D>;
   const uint32_t base = smem_u32(smem);
   tma_prefetch_desc(&p.tu);
-  for (int c = 0; c < nch; ++c) {
-    if (c >= 1 && !mbar_wait(&ms->u_empty, (c - 1) & 1, &ms->abort)) {
-      fail_wait(ms, p.a.status);
-      return;
+  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
+    if (kk >= 1) {
+      tma_prefetch_3d(&p.tu, 0, c * kC, bh);
+      if (!mbar_wait(&ms->u_empty, (kk - 1) & 1, &ms->abort)) {
+        fail_wait<CL>(ms, p.a.status);
+        return;
+      }
     }
     mbar_arrive_expect_tx(&ms->u_full, kC * D * 2);
     tma_load_3d(base + CF::U_OFF, &p.tu, 0, c * kC, bh, &ms->u_full);
@@ -234,20 +369,27 @@ __device__ __forceinline__ UCols<D / 32> load_ucols(const uint8_t* us, int j) {
 }
 
 // ---------------------------------------------------------------- PS: scalars of the blocks
-template <int D>
+// Runs the chunks this CTA owns.  With a cluster, the column carry at a chunk's start and the
+// chunk-start scalar carries (mC, EC, CP) come from the other CTA, which processed the previous
+// chunk; the carries of the next chunk are sent the same way.  Slots are indexed by the number
+// of carries received so far: a slot is rewritten only two owned chunks later.
+template <int D, int CL>
 __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
-                             size_t row0, int nch) {
+                             size_t row0, int nch, int rank) {
   using CF = Cfg<D>;
   constexpr int R = D / 32;
   constexpr int RP = (R + 1) / 2;  // column pairs per lane (R = 1 uses the .x half only)
-  const int r = threadIdx.x;       // token row inside the chunk, 0..127
-  const int w = r >> 5, lane = r & 31;
+  const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-token block
+  const int r = 32 * w + lane;     // token row inside the chunk, 0..127
   const int N = a.N;
   float* lend = reinterpret_cast<float*>(smem + CF::LEND_OFF);      // [4][D]
   float* bpub = reinterpret_cast<float*>(smem + CF::BPUB_OFF);      // [4][4] + kc [2][4]
   float4* chain = reinterpret_cast<float4*>(smem + CF::CHAIN_OFF);  // [4][32] (s, f, g, -)
   float4* scal = reinterpret_cast<float4*>(smem + CF::SCAL_OFF);    // [2][128] (s, m, Et, P)
-  const bool dbg = blockIdx.y == 0;
+  const float* cin = reinterpret_cast<const float*>(smem + CF::CIN_OFF);    // [2][D]
+  const float* kcin = reinterpret_cast<const float*>(smem + CF::KCIN_OFF);  // [2][4]
+  const uint32_t peer = (uint32_t)rank ^ 1u;
+  const bool dbg = blockIdx.y < CL;  // the first cluster of value slices writes the scalars
   const float etau = expf(a.tau[h]);
   const float sqrtd = __fsqrt_rn((float)D);
   const float2 etau2 = make_float2(etau, etau);
@@ -258,21 +400,22 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
                          R > 1 ? a.mu[(size_t)h * D + R * lane + 2 * x + 1] : 0.0f);
     Cc[x] = make_float2(0.0f, 0.0f);
   }
-  if (r == 0) {
+  if (CL == 1 && r == 0) {
     bpub[16 + 0] = -INFINITY;  // chunk-start carries (mC, EC, CP) for chunk 0
     bpub[16 + 1] = 0.0f;
     bpub[16 + 2] = 0.0f;
   }
 
-  for (int c = 0; c < nch; ++c) {
-    const int slot = c & 1;
+  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
+    const int slot = kk & 1;
     const int i = c * kC + r;
     const bool valid = i < N;
     const int b0 = c * kC + 32 * w;  // first token of this warp's block
     const int nvalid = max(0, min(32, N - b0));
+    const int rslot = ((c - 1) / 2) & 1;  // carry slot of this chunk (cluster of two)
     // ---- u of the block from the staged tile: lane owns columns R lane .. R lane + R - 1 ----
-    if (!mbar_wait_warp(&ms->u_full, c & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (!mbar_wait_warp(&ms->u_full, kk & 1, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
     const uint8_t* us = smem + CF::U_OFF + (size_t)(32 * w) * D * 2 + R * lane * 2;
@@ -292,11 +435,21 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
       if (R > 1) lend[w * D + R * lane + 2 * x + 1] = L[x].y;
     }
     mbar_arrive(&ms->pbar);
-    if (!mbar_wait_warp(&ms->pbar, (2 * c) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (!mbar_wait_warp(&ms->pbar, (2 * kk) & 1, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
     // ---- column carry at this block's start (and at the next chunk's start) ----
+    if (CL > 1 && c > 0) {
+      if (!mbar_wait_cl_warp(&ms->ccar_full, rslot, &ms->abort)) {
+        fail_wait<CL>(ms, a.status);
+        return;
+      }
+#pragma unroll
+      for (int x = 0; x < RP; ++x)
+        Cc[x] = make_float2(cin[rslot * D + R * lane + 2 * x],
+                            R > 1 ? cin[rslot * D + R * lane + 2 * x + 1] : 0.0f);
+    }
     float2 Cw[RP];
 #pragma unroll
     for (int ww = 0; ww < 4; ++ww) {
@@ -310,6 +463,16 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
                                       R > 1 ? lend[ww * D + R * lane + 2 * x + 1] : 0.0f);
         Cc[x] = __fadd2_rn(Cc[x], le);
       }
+    }
+    if (CL > 1 && w == 0 && c + 1 < nch) {  // the next chunk's column carry -> other CTA
+      const uint32_t dst = mapa(smem_u32(smem + CF::CIN_OFF) + (uint32_t)(((c / 2) & 1) * D * 4),
+                                peer);
+#pragma unroll
+      for (int x = 0; x < RP; ++x) {
+        st_cluster_f32(dst + (uint32_t)(R * lane + 2 * x) * 4, Cc[x].x);
+        if (R > 1) st_cluster_f32(dst + (uint32_t)(R * lane + 2 * x + 1) * 4, Cc[x].y);
+      }
+      mbar_arrive_remote(mapa(smem_u32(&ms->ccar_full), peer));
     }
     // ---- phase 2: S = C + L per token, logit partial products (two tokens per f32x2) ----
     float pp[32];
@@ -382,13 +545,22 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
       bpub[w * 4 + 2] = El;
     }
     mbar_arrive(&ms->pbar);
-    if (!mbar_wait_warp(&ms->pbar, (2 * c + 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (!mbar_wait_warp(&ms->pbar, (2 * kk + 1) & 1, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
     // carries at this block's start: chunk-start carries folded over the earlier blocks
-    const float* kcb = bpub + 16 + (c & 1) * 4;
-    BlockCarry kw{kcb[0], kcb[1], kcb[2]};
+    BlockCarry kw{-INFINITY, 0.0f, 0.0f};
+    if (CL == 1) {
+      const float* kcb = bpub + 16 + (c & 1) * 4;
+      kw = BlockCarry{kcb[0], kcb[1], kcb[2]};
+    } else if (c > 0) {
+      if (!mbar_wait_cl_warp(&ms->kcar_full, rslot, &ms->abort)) {
+        fail_wait<CL>(ms, a.status);
+        return;
+      }
+      kw = BlockCarry{kcin[rslot * 4 + 0], kcin[rslot * 4 + 1], kcin[rslot * 4 + 2]};
+    }
     for (int ww = 0; ww < w; ++ww) fold_block(kw, bpub[ww * 4 + 0], bpub[ww * 4 + 1], bpub[ww * 4 + 2]);
     float M = kw.mC;  // running max at the chunk's last valid token (max is exact)
 #pragma unroll
@@ -396,10 +568,19 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
     if (w == 3 && lane == 0) {  // chunk-start carries of the next chunk
       BlockCarry kn = kw;
       fold_block(kn, bpub[12 + 0], bpub[12 + 1], bpub[12 + 2]);
-      float* kcn = bpub + 16 + ((c + 1) & 1) * 4;
-      kcn[0] = kn.mC;
-      kcn[1] = kn.EC;
-      kcn[2] = kn.CP;
+      if (CL == 1) {
+        float* kcn = bpub + 16 + ((c + 1) & 1) * 4;
+        kcn[0] = kn.mC;
+        kcn[1] = kn.EC;
+        kcn[2] = kn.CP;
+      } else if (c + 1 < nch) {
+        const uint32_t dst =
+            mapa(smem_u32(smem + CF::KCIN_OFF) + (uint32_t)(((c / 2) & 1) * 16), peer);
+        st_cluster_f32(dst + 0, kn.mC);
+        st_cluster_f32(dst + 4, kn.EC);
+        st_cluster_f32(dst + 8, kn.CP);
+        mbar_arrive_remote(mapa(smem_u32(&ms->kcar_full), peer));
+      }
     }
     // this token's scalars
     const float P = __fadd_rn(kw.CP, LP);
@@ -412,8 +593,8 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
       if (a.dbg_m) a.dbg_m[row0 + i] = m;
     }
     // hand the scalars to the operand warps (two-slot ring)
-    if (c >= 2 && !mbar_wait_warp(&ms->scal_empty[slot], ((c >> 1) - 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (kk >= 2 && !mbar_wait_warp(&ms->scal_empty[slot], ((kk >> 1) - 1) & 1, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
     scal[slot * kC + r] = make_float4(s, m, Et, P);
@@ -454,18 +635,20 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
 }
 
 // ---------------------------------------------------------------- PO: tensor-core operands
-template <int D>
+// Chunks this CTA owns: rotate q/k, coefficients, weight operands and the Xch block (bulk-copied
+// to the other CTA of the cluster), then this CTA's scaled value tile Vsc.  The value tiles of
+// the chunks of the other CTA are built by the epilogue warps.
+template <int D, int CL>
 __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, size_t row0,
-                              int nch) {
+                              int nch, int rank) {
   using CF = Cfg<D>;
-  const int r = threadIdx.x - 128;  // token row inside the chunk, 0..127
-  const int w = r >> 5, lane = r & 31;
+  const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-row group
+  const int r = 32 * w + lane;      // token row inside the chunk, 0..127
   const int N = a.N;
-  float4* coef = reinterpret_cast<float4*>(smem + CF::COEF_OFF);
-  float* colsc = reinterpret_cast<float*>(smem + CF::COLS_OFF);
   const float4* scal = reinterpret_cast<const float4*>(smem + CF::SCAL_OFF);
   float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
   float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
+  const uint32_t peer = (uint32_t)rank ^ 1u;
   const double two_pi = 6.283185307179586476925286766559;
   constexpr int PPW = (D / 2 + 3) / 4;  // rotary pairs per warp
   const int pj = w * PPW + lane;
@@ -476,180 +659,227 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
     theta[pj] = (float)theta_d;
   }
 
-  for (int c = 0; c < nch; ++c) {
+  // rotary base angle of chunk cc per pair, reduced modulo 2 pi in fp64; token r of the chunk
+  // then uses phi_j + r theta_j.  Written one chunk ahead (double buffer, pobar orders it).
+  auto put_phi = [&](int cc, int slot) {
+    if (owns_pair) {
+      const double ang = (double)(cc * kC) * theta_d;
+      phi[slot * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
+    }
+  };
+  // gate logits of chunk cc (loaded one chunk ahead so that their latency is hidden)
+  auto load_gates = [&](int cc, float& x1, float& xh) {
+    x1 = 0.0f;
+    xh = 0.0f;
+    if (cc < nch && cc * kC + r < N) {
+      x1 = __ldg(a.g1 + row0 + cc * kC + r);
+      xh = __ldg(a.gh + row0 + cc * kC + r);
+    }
+  };
+  float g1, gh;
+  load_gates(rank, g1, gh);
+  put_phi(rank, 0);
+
+  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
     const int st = c % CF::NS;
-    const int slot = c & 1;
     const int i = c * kC + r;
     const bool valid = i < N;
-    float g1 = 0.0f, gh = 0.0f;
-    if (valid) {
-      g1 = __ldg(a.g1 + row0 + i);
-      gh = __ldg(a.gh + row0 + i);
-    }
-    // rotary base angle of this chunk per pair, reduced modulo 2 pi in fp64; token r of the
-    // chunk then uses phi_j + r theta_j
-    if (owns_pair) {
-      const double ang = (double)(c * kC) * theta_d;
-      phi[(c & 1) * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
-    }
+    Xch* xc = xch(smem, CF::XCH_OFF, st);
     mbar_arrive(&ms->pobar);
-    if (!mbar_wait_warp(&ms->pobar, c & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (!mbar_wait_warp(&ms->pobar, kk & 1, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
-    // ---- rotate q, k in place (TMA tiles), norms ----
-    if (!mbar_wait_warp(&ms->tma_full[st], (c / CF::NS) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    if (!mbar_wait_warp(&ms->tma_full[tf_index<D, CL>(c)], tf_phase<D, CL>(c), &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
     uint8_t* qt = smem + CF::Q_OFF + st * CF::KA * kTile;
     uint8_t* kt = smem + CF::K_OFF + st * CF::KA * kTile;
-    const bool rot = a.rope != 0 && valid;
-    float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
-    const float* ph = phi + (c & 1) * (D / 2);
-    const float rf = (float)r;
-#pragma unroll 1
-    for (int g = 0; g < D / 16; ++g) {
-      float2 cs[8];
-      if (rot) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float sn, cn;
-          __sincosf(__fmaf_rn(rf, theta[8 * g + k], ph[8 * g + k]), &sn, &cn);
-          cs[k] = make_float2(cn, sn);
-        }
-      }
-      rotate_group<D>(qt, r, g, rot, cs, qq2);
-      rotate_group<D>(kt, r, g, rot, cs, kk2);
-    }
-    const float qq = __fadd_rn(qq2.x, qq2.y), kk = __fadd_rn(kk2.x, kk2.y);
-    // value slice of this token from the staging tile
-    float2 vv[kDV / 2];
+    uint8_t* vt = smem + CF::V_OFF + st * 2 * kTile;
+    float g1n, ghn;
+    load_gates(c + CL, g1n, ghn);
+    float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
     {
-      const uint8_t* vst = smem + CF::VST_OFF + st * 128 * 64;
+      // ---- rotate q, k in place (TMA tiles), norms ----
+      const bool rot = a.rope != 0 && valid;
+      float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
+      const float* ph = phi + (kk & 1) * (D / 2);
+      const float rf = (float)r;
+#pragma unroll 1
+      for (int g = 0; g < D / 16; ++g) {
+        float2 cs[8];
+        if (rot) {
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
-        unpack_bf16x2(wv.x, vv[4 * x + 0].x, vv[4 * x + 0].y);
-        unpack_bf16x2(wv.y, vv[4 * x + 1].x, vv[4 * x + 1].y);
-        unpack_bf16x2(wv.z, vv[4 * x + 2].x, vv[4 * x + 2].y);
-        unpack_bf16x2(wv.w, vv[4 * x + 3].x, vv[4 * x + 3].y);
+          for (int k = 0; k < 8; ++k) {
+            float sn, cn;
+            __sincosf(__fmaf_rn(rf, theta[8 * g + k], ph[8 * g + k]), &sn, &cn);
+            cs[k] = make_float2(cn, sn);
+          }
+        }
+        rotate_group<D>(qt, r, g, rot, cs, qq2);
+        rotate_group<D>(kt, r, g, rot, cs, kk2);
+      }
+      const float qq = __fadd_rn(qq2.x, qq2.y), kq = __fadd_rn(kk2.x, kk2.y);
+      // ---- scalars of this token from the scalar warps ----
+      const int slot = kk & 1;
+      if (!mbar_wait_warp(&ms->scal_full[slot], (kk >> 1) & 1, &ms->abort)) {
+        fail_wait<CL>(ms, a.status);
+        return;
+      }
+      const float4 sc = scal[slot * kC + r];
+      const float M = ms->Mslot[slot];
+      mbar_arrive(&ms->scal_empty[slot]);
+      const float s = sc.x, m = sc.y, Et = sc.z, P = sc.w;
+      // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
+      // contract: fast exp, reciprocal square root and division are accurate enough here)
+      const float kap = rsqrtf(fmaxf(kq, 1e-24f));
+      const float rho = rsqrtf(fmaxf(qq, 1e-24f));
+      float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (valid) {
+        ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
+        cs1 = __fmul_rn(s, kap);
+        ck = kap;
+        const float sig1 = __fdividef(1.0f, 1.0f + __expf(-g1));
+        const float sigh = __fdividef(1.0f, 1.0f + __expf(-gh));
+        const float rt = __fdividef(1.0f, (float)(i + 1));
+        const float b0c = (sig1 - sigh) * rt;
+        const float ahat = __fdividef(sigh, Et) * __expf(M - m);
+        cf.x = rho * ahat;
+        cf.y = rho * b0c;
+        cf.z = -rho * (b0c * P * rt + sigh * rt);
+        if (!isfinite(cf.x) || !isfinite(ce)) report(a.status, kErrRange);
+      }
+      xc->coef[r] = cf;
+      xc->cols[0][r] = ce;
+      xc->cols[1][r] = cs1;
+      xc->cols[2][r] = ck;
+      if (r == 0) xc->M = M;
+      // Weight operands: W_{t,i} = a_t e_i + b_t s'_i + g_t k_i is formed by one K = 16 MMA of
+      // the row vector [a a' a a' b b' b b' g g' g g' 0 0 0 0] (hi and lo bf16 parts,
+      // x = x + x') and the column vector [e e' e e' s s' s s' k k' k k' 0 0 0 0] paired as
+      // (hi hi, hi lo, lo hi, lo lo): every product is exact in fp32, the representation error
+      // is about 2^-17 of each term, so the nearly cancelling sum keeps fp32-level accuracy.
+      // The buffer is single: both CTAs' weight MMAs of the previous chunk must have completed.
+      // (Phase c-2 of w_done is complete here: the stage of this chunk was released after both
+      // CTAs' MMAs of an earlier chunk, whose weight commits precede their stage commits.)
+      if (c >= 1 && !mbar_wait_cl_warp(&ms->w_done, (c - 1) & 1, &ms->abort)) {
+        fail_wait<CL>(ms, a.status);
+        return;
+      }
+      {
+        float xh[6], xl[6];
+        const float xs[6] = {cf.x, cf.y, cf.z, ce, cs1, ck};
+#pragma unroll
+        for (int k = 0; k < 6; ++k) {
+          xh[k] = __bfloat162float(__float2bfloat16_rn(xs[k]));
+          xl[k] = __fsub_rn(xs[k], xh[k]);
+        }
+        uint8_t* rw = smem + CF::RW_OFF;
+        uint8_t* cw = smem + CF::CW_OFF;
+        *reinterpret_cast<uint4*>(rw + sw32_off(r, 0)) =
+            make_uint4(pack_bf16x2(xh[0], xh[0]), pack_bf16x2(xl[0], xl[0]),
+                       pack_bf16x2(xh[1], xh[1]), pack_bf16x2(xl[1], xl[1]));
+        *reinterpret_cast<uint4*>(rw + sw32_off(r, 1)) =
+            make_uint4(pack_bf16x2(xh[2], xh[2]), pack_bf16x2(xl[2], xl[2]), 0u, 0u);
+        *reinterpret_cast<uint4*>(cw + sw32_off(r, 0)) =
+            make_uint4(pack_bf16x2(xh[3], xl[3]), pack_bf16x2(xh[3], xl[3]),
+                       pack_bf16x2(xh[4], xl[4]), pack_bf16x2(xh[4], xl[4]));
+        *reinterpret_cast<uint4*>(cw + sw32_off(r, 1)) =
+            make_uint4(pack_bf16x2(xh[5], xl[5]), pack_bf16x2(xh[5], xl[5]), 0u, 0u);
+      }
+      // Q, K, R, C and Xch are complete: the MMA may start, and with a cluster one thread
+      // bulk-copies them to the other CTA once every operand thread's writes are visible to the
+      // copy engine
+      fence_proxy_async_smem();
+      mbar_arrive(&ms->po_sync);
+      if (CL > 1 && r == 0) {
+        if (!mbar_wait(&ms->po_sync, kk & 1, &ms->abort)) {
+          fail_wait<CL>(ms, a.status);
+          return;
+        }
+        const uint32_t bar = mapa(smem_u32(&ms->peer_full), peer);
+        const uint32_t lq = smem_u32(qt), lk = smem_u32(kt);
+        const uint32_t lw = smem_u32(smem + CF::RW_OFF), lx = smem_u32(xc);
+        bulk_copy_to_cta(mapa(lq, peer), lq, CF::KA * kTile, bar);
+        bulk_copy_to_cta(mapa(lk, peer), lk, CF::KA * kTile, bar);
+        bulk_copy_to_cta(mapa(lw, peer), lw, 2 * kC * 32, bar);
+        bulk_copy_to_cta(mapa(lx, peer), lx, (uint32_t)sizeof(Xch), bar);
       }
     }
-    // ---- scalars of this token from the scalar warps ----
-    if (!mbar_wait_warp(&ms->scal_full[slot], (c >> 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+    // value slice of this token: raw bf16 words copied to columns 0..31 of the Vsc tile (once the
+    // stage's previous Vsc was consumed), the staging buffer handed back, then the scaled parts
+    if (!vsc_wait<D, CL>(ms, c)) {
+      fail_wait<CL>(ms, a.status);
       return;
     }
-    const float4 sc = scal[slot * kC + r];
-    const float M = ms->Mslot[slot];
-    mbar_arrive(&ms->scal_empty[slot]);
-    const float s = sc.x, m = sc.y, Et = sc.z, P = sc.w;
-    // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
-    // contract: fast exp, reciprocal square root and division are accurate enough here)
-    const float kap = rsqrtf(fmaxf(kk, 1e-24f));
-    const float rho = rsqrtf(fmaxf(qq, 1e-24f));
-    float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
-    float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) {
-      ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
-      cs1 = __fmul_rn(s, kap);
-      ck = kap;
-      const float sig1 = __fdividef(1.0f, 1.0f + __expf(-g1));
-      const float sigh = __fdividef(1.0f, 1.0f + __expf(-gh));
-      const float rt = __fdividef(1.0f, (float)(i + 1));
-      const float b0c = (sig1 - sigh) * rt;
-      const float ahat = __fdividef(sigh, Et) * __expf(M - m);
-      cf.x = rho * ahat;
-      cf.y = rho * b0c;
-      cf.z = -rho * (b0c * P * rt + sigh * rt);
-      if (!isfinite(cf.x) || !isfinite(ce)) report(a.status, kErrRange);
-    }
-    coef[st * kC + r] = cf;
-    colsc[(st * 3 + 0) * kC + r] = ce;
-    colsc[(st * 3 + 1) * kC + r] = cs1;
-    colsc[(st * 3 + 2) * kC + r] = ck;
-    if (r == 0) ms->Mop[st] = M;
-    // Vsc row: atom 0 = [v | e v], atom 1 = [s' v | k v]
-    uint8_t* vt = smem + CF::V_OFF + st * 2 * kTile;
-    const float2 ce2 = make_float2(ce, ce), cs2 = make_float2(cs1, cs1), ck2 = make_float2(ck, ck);
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      uint32_t pv[4], pe[4], ps[4], pk[4];
-#pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        const float2 v2 = vv[4 * x + y];
-        const float2 e2 = __fmul2_rn(ce2, v2), s2 = __fmul2_rn(cs2, v2), k2 = __fmul2_rn(ck2, v2);
-        pv[y] = pack_bf16x2(v2.x, v2.y);
-        pe[y] = pack_bf16x2(e2.x, e2.y);
-        ps[y] = pack_bf16x2(s2.x, s2.y);
-        pk[y] = pack_bf16x2(k2.x, k2.y);
-      }
-      *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-      *reinterpret_cast<uint4*>(vt + sw128_off(r, 4 + x)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
-      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, x)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
-      *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, 4 + x)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
+    copy_v_row(vt, smem + CF::VST_OFF, r);
+    mbar_arrive(&ms->vst_empty);
+    build_vsc_row(vt, r, ce, cs1, ck);
     fence_proxy_async_smem();
-    mbar_arrive(&ms->op_full[st]);
+    mbar_arrive(&ms->op_full);
+    if (c + CL < nch) put_phi(c + CL, (kk + 1) & 1);
+    g1 = g1n;
+    gh = ghn;
   }
 }
 
 // ============================================================================ M: MMA issue
-template <int D>
+// Per chunk c, in issue order (each group waits only for what it reads or overwrites):
+//   A = Q K^T and W = R C^T                 (Q, K, R, C written; previous S tile formed)
+//                                                                         -> a_full, w_done
+//   state += Vsc^T K                        (state copied to the B tile, F~ rescaled)  -> st_done
+//   X[:, 0:96] = Q [F~ | G | H] (c >= 1)    (previous outputs read from X)
+//                                                                      -> sst_free, qk_empty
+//   X[:, 96:128] = S V                      (this chunk's S tile formed)   -> x_full, vsc_free
+// qk_empty follows the Q [F|G|H] product (the S V product for the first chunk).  w_done and
+// qk_empty are delivered to both CTAs of a cluster (the owner of a later chunk writes into the
+// other CTA's buffers).  The epilogue reads a chunk's Xch block before it frees X of the
+// previous chunk, which the Q [F|G|H] product waits for.
+template <int D, int CL>
 __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
+  constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1u);  // every CTA of the cluster
   using CF = Cfg<D>;
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
-  const uint32_t tA = tm + CF::TM_A, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
-  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);   // Q K^T
+  const uint32_t tA = tm + CF::TM_A, tW = tm + CF::TM_W, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
+  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);   // Q K^T, R C^T
   constexpr uint32_t id_qs = idesc_bf16_f32(128, 96, false, false);    // Q [F|G|H]
   constexpr uint32_t id_sv = idesc_bf16_f32(128, 32, false, true);     // S V
   constexpr uint32_t id_st = idesc_bf16_f32(128, D, true, true);       // Vsc^T K
+  const uint64_t d_rw = sw32_desc(base + CF::RW_OFF), d_cw = sw32_desc(base + CF::CW_OFF);
   bool ok = true;
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
   for (int c = 0; c < nch && ok; ++c) {
     const int st = c % CF::NS;
+    const bool owned = (c % CL) == rank;
+    const uint32_t ph = (uint32_t)(c / CL) & 1u;  // phase of the owned / other-owned barriers
     const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
     const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
     const uint32_t vt = base + CF::V_OFF + st * 2 * kTile;
-    ok = mbar_wait(&ms->op_full[st], (c / CF::NS) & 1, &ms->abort);
+    ok = owned ? mbar_wait(&ms->po_sync, ph, &ms->abort)
+               : mbar_wait_cl(&ms->peer_full, ph, &ms->abort);
     if (ok && c >= 1) ok = mbar_wait(&ms->a_free, (c - 1) & 1, &ms->abort);
+    // every phase of w_done is observed in order (the end-of-kernel wait relies on it)
+    if (ok && c >= 1) ok = mbar_wait_cl(&ms->w_done, (c - 1) & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
-    // ---- A = Q K^T (K = d) ----
+    // ---- A = Q K^T (K = d); W = R C^T (K = 16) ----
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
       mma_bf16(tA, sw128_desc(qt + off, 16, 1024), sw128_desc(kt + off, 16, 1024), id_qk,
                kk > 0);
     }
+    mma_bf16(tW, d_rw, d_cw, id_qk, 0u);
     mma_commit(&ms->a_full);
-    ok = mbar_wait(&ms->am_full, c & 1, &ms->abort);
-    if (ok && c >= 1) ok = mbar_wait(&ms->sst_full, (c - 1) & 1, &ms->abort);
-    if (ok && c >= 2) ok = mbar_wait(&ms->x_free[c & 1], ((c >> 1) - 1) & 1, &ms->abort);
+    if (CL > 1) mma_commit_mc(&ms->w_done, kAll);
+    else mma_commit(&ms->w_done);
+    // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
+    if (c >= 1 && !mbar_wait(&ms->sst_full, (c - 1) & 1, &ms->abort)) { ok = false; break; }
+    ok = owned ? mbar_wait(&ms->op_full, ph, &ms->abort) : mbar_wait(&ms->vsc_full, ph, &ms->abort);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t tXc = tX + (uint32_t)(c & 1) * 128;
-    // ---- X[:, 0:96] = Q [F~ | G | H] (previous chunks); X[:, 96:128] = S V ----
-    if (c >= 1) {
-      const uint32_t sst = base + CF::SST_OFF + 32 * 128;  // state rows 32..127
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
-        mma_bf16(tXc, sw128_desc(qt + off, 16, 1024), sw128_desc(sst + off, 16, 1024), id_qs,
-                 kk > 0);
-      }
-    }
-    const uint32_t sm = base + CF::AM_OFF;
-#pragma unroll
-    for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint32_t aoff = (kk / 4) * kTile + (kk % 4) * 32;  // K-major, K = token i
-      const uint32_t boff = kk * 2048;                          // MN-major, 16 rows per step
-      mma_bf16(tXc + 96, sw128_desc(sm + aoff, 16, 1024), sw128_desc(vt + boff, kTile, 1024),
-               id_sv, kk > 0);
-    }
-    mma_commit(&ms->x_full[c & 1]);
-    // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       const uint32_t off = kk * 2048;
@@ -657,14 +887,49 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
                (c > 0 || kk > 0) ? 1u : 0u);
     }
     mma_commit(&ms->st_done);
-    mma_commit(&ms->op_empty[st]);
+    // ---- X[:, 0:96] = Q [F~ | G | H] (state of the previous chunks, B tile rows 32..127) ----
+    if (c >= 1) {
+      if (!mbar_wait(&ms->x_free, (c - 1) & 1, &ms->abort)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sst = base + CF::SST_OFF + 32 * 128;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
+        mma_bf16(tX, sw128_desc(qt + off, 16, 1024), sw128_desc(sst + off, 16, 1024), id_qs,
+                 kk > 0);
+      }
+      mma_commit(&ms->sst_free);
+      // Q, K (and, through the epilogue's order, Xch) of this chunk are no longer read
+      if (CL > 1) mma_commit_mc(&ms->qk_empty[st], kAll);
+      else mma_commit(&ms->qk_empty[st]);
+    }
+    // ---- X[:, 96:128] = S V ----
+    if (!mbar_wait(&ms->am_full, c & 1, &ms->abort)) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t sm = base + CF::AM_OFF;
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) {
+      const uint32_t aoff = (kk / 4) * kTile + (kk % 4) * 32;  // K-major, K = token i
+      const uint32_t boff = kk * 2048;                          // MN-major, 16 rows per step
+      mma_bf16(tX + 96, sw128_desc(sm + aoff, 16, 1024), sw128_desc(vt + boff, kTile, 1024),
+               id_sv, kk > 0);
+    }
+    mma_commit(&ms->x_full);
+    if (c == 0) {  // the first chunk has no Q [F|G|H] product: release after the S tile was read
+      if (CL > 1) mma_commit_mc(&ms->qk_empty[st], kAll);
+      else mma_commit(&ms->qk_empty[st]);
+    }
+    mma_commit(&ms->vsc_free[c & 1]);
   }
-  if (!ok) fail_wait(ms, a.status);
+  if (!ok) fail_wait<CL>(ms, a.status);
   mma_commit(&ms->fin);
 }
 
 // ============================================================================ E: epilogue
-template <int D>
+// Per chunk c: the S tile (A o W, masked, bf16), the scaled value tile of chunk c+1 when the
+// other CTA of the cluster owns it, the state after chunk c as the bf16 B tile of chunk c+1 (F~
+// rescaled to M_{c+1}), then the output rows of chunk c.
+template <int D, int CL>
 __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, size_t row0,
                               int nch) {
   using CF = Cfg<D>;
@@ -673,122 +938,104 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tm = ms->tmem + lane_off;
   const uint32_t base = smem_u32(smem);
-  const float4* coef = reinterpret_cast<const float4*>(smem + CF::COEF_OFF);
-  const float* colsc = reinterpret_cast<const float*>(smem + CF::COLS_OFF);
   const int j0 = blockIdx.y * kDV;
   const int N = a.N;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out) + row0 * D;
-  float M_prev = 0.0f;
-  bool ok = true;
-  float4 cf_prev = make_float4(0.f, 0.f, 0.f, 0.f);
-  // o = X_SV + a X_F + b X_G + g X_H for chunk cc, one 32-column block at a time
-  auto xstep = [&](int cc, const float4 cfc) -> bool {
-    const int xb_par = cc & 1;
-    if (!mbar_wait_warp(&ms->x_full[xb_par], (cc >> 1) & 1, &ms->abort)) return false;
-    tc_fence_after();
-    const uint32_t tx = tm + CF::TM_X + (uint32_t)xb_par * 128;
-    float o[32];
-    tmem_ld32(tx + 96, o);
-    if (cc >= 1) {
-      float xb[32];
-      tmem_ld32(tx + 0, xb);
+  const uint32_t sm = base + CF::AM_OFF;
+  // Columns after every row of this warp (blocks cb > wq) are zero in every chunk: written once.
+  for (int cb = wq + 1; cb < 4; ++cb) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.x, xb[j], o[j]);
-      tmem_ld32(tx + 32, xb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.y, xb[j], o[j]);
-      tmem_ld32(tx + 64, xb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __fmaf_rn(cfc.z, xb[j], o[j]);
+    for (int x = 0; x < 4; ++x) {
+      const int col0 = cb * 32 + x * 8;
+      sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), make_uint4(0, 0, 0, 0));
     }
-    tc_fence_before();
-    mbar_arrive(&ms->x_free[xb_par]);
-    const int i = cc * kC + t;
-    if (i < N) {
-      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        uint4 p;
-        p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
-        p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
-        p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
-        p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
-        dst[x] = p;
-      }
-    }
+  }
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
+  auto owned = [&](int cc) { return (cc % CL) == rank; };
+  // coefficients and M of chunk cc are in this CTA's Xch block
+  auto wait_xch = [&](int cc) -> bool {
+    const uint32_t ph = (uint32_t)(cc / CL) & 1u;
+    return owned(cc) ? mbar_wait_warp(&ms->po_sync, ph, &ms->abort)
+                     : mbar_wait_cl_warp(&ms->peer_full, ph, &ms->abort);
+  };
+  // value tile of a chunk owned by the other CTA (row t)
+  auto vsc_other = [&](int cc) -> bool {
+    const int sv = cc % CF::NS;
+    if (!mbar_wait_warp(&ms->tma_full[tf_index<D, CL>(cc)], tf_phase<D, CL>(cc), &ms->abort))
+      return false;
+    if (!vsc_wait<D, CL>(ms, cc)) return false;
+    uint8_t* vt = smem + CF::V_OFF + sv * 2 * kTile;
+    copy_v_row(vt, smem + CF::VST_OFF, t);
+    mbar_arrive(&ms->vst_empty);
+    if (!mbar_wait_cl_warp(&ms->peer_full, (uint32_t)(cc / CL) & 1u, &ms->abort)) return false;
+    const Xch* xv = xch(smem, CF::XCH_OFF, sv);
+    build_vsc_row(vt, t, xv->cols[0][t], xv->cols[1][t], xv->cols[2][t]);
+    fence_proxy_async_smem();
+    mbar_arrive(&ms->vsc_full);
     return true;
   };
-
+  bool ok = true;
+  if (CL > 1 && nch > 0 && !owned(0)) ok = vsc_other(0);
+  // (a, b, g) of row t and M of the current chunk: read while the previous chunk is in flight
+  // (before X of that chunk is freed), since the chunk's Xch block is released with its Q, K
+  float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+  float M_cur = 0.0f;
+  if (ok && nch > 0) {
+    ok = wait_xch(0);
+    cf = xch(smem, CF::XCH_OFF, 0)->coef[t];
+    M_cur = xch(smem, CF::XCH_OFF, 0)->M;
+  }
   for (int c = 0; c < nch && ok; ++c) {
-    const int st = c % CF::NS;
-    ok = mbar_wait_warp(&ms->op_full[st], (c / CF::NS) & 1, &ms->abort);
-    if (!ok) break;
-    const float4 cf = coef[st * kC + t];  // (a, b, g) of row t
-    const float2 ra2 = make_float2(cf.x, cf.x), rb2 = make_float2(cf.y, cf.y),
-                 rg2 = make_float2(cf.z, cf.z);
-    const float M_cur = ms->Mop[st];
-    const float* ce = colsc + (st * 3 + 0) * kC;
-    const float* cs = colsc + (st * 3 + 1) * kC;
-    const float* ck = colsc + (st * 3 + 2) * kC;
-    // ---- S = [i <= t] (Q K^T) (a e + b s' + g k), fp32 then bf16 (rows t, K = token i) ----
+    float4 cf_next = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M_next = 0.0f;
+    // ---- S = [i <= t] (Q K^T) o W, fp32 product then bf16 (rows t, K = token i) ----
     ok = mbar_wait_warp(&ms->a_full, c & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t sm = base + CF::AM_OFF;
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-      if (cb > wq) {  // every column of this block is after every row of this warp
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int col0 = cb * 32 + x * 8;
-          sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), make_uint4(0, 0, 0, 0));
-        }
-        continue;
-      }
-      float v[32];
-      tmem_ld32(tm + CF::TM_A + cb * 32, v);
+    for (int cb = 0; cb <= wq; ++cb) {
+      float v[32], wv[32];
+      tmem_ld32x2(tm + CF::TM_A + cb * 32, tm + CF::TM_W + cb * 32, v, wv);
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const int col0 = cb * 32 + x * 8;
-        const float4 e0 = *reinterpret_cast<const float4*>(ce + col0);
-        const float4 e1 = *reinterpret_cast<const float4*>(ce + col0 + 4);
-        const float4 s0 = *reinterpret_cast<const float4*>(cs + col0);
-        const float4 s1 = *reinterpret_cast<const float4*>(cs + col0 + 4);
-        const float4 k0 = *reinterpret_cast<const float4*>(ck + col0);
-        const float4 k1 = *reinterpret_cast<const float4*>(ck + col0 + 4);
-        const float2 ee[4] = {make_float2(e0.x, e0.y), make_float2(e0.z, e0.w),
-                              make_float2(e1.x, e1.y), make_float2(e1.z, e1.w)};
-        const float2 ss[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
-                              make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
-        const float2 kk[4] = {make_float2(k0.x, k0.y), make_float2(k0.z, k0.w),
-                              make_float2(k1.x, k1.y), make_float2(k1.z, k1.w)};
         uint32_t pw[4];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          const float2 wgt = __ffma2_rn(ra2, ee[y], __ffma2_rn(rb2, ss[y], __fmul2_rn(rg2, kk[y])));
-          float2 val = __fmul2_rn(make_float2(v[x * 8 + 2 * y], v[x * 8 + 2 * y + 1]), wgt);
+          const int e0 = x * 8 + 2 * y;
+          float2 val = __fmul2_rn(make_float2(v[e0], v[e0 + 1]), make_float2(wv[e0], wv[e0 + 1]));
           if (cb == wq) {  // diagonal block: keep i <= t only
             if (col0 + 2 * y > t) val.x = 0.0f;
             if (col0 + 2 * y + 1 > t) val.y = 0.0f;
           }
           pw[y] = pack_bf16x2(val.x, val.y);
         }
-        const uint4 p = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
+        sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8),
+               make_uint4(pw[0], pw[1], pw[2], pw[3]));
       }
     }
     tc_fence_before();
     mbar_arrive(&ms->a_free);
     fence_proxy_async_smem();
     mbar_arrive(&ms->am_full);
-    // ---- state (after chunk c-1) -> bf16 B operand rows 32..127, F~ rescaled to M_c ----
-    if (c >= 1) {
-      ok = mbar_wait_warp(&ms->st_done, (c - 1) & 1, &ms->abort);
+    if (CL > 1 && c + 1 < nch && !owned(c + 1)) {
+      ok = vsc_other(c + 1);
       if (!ok) break;
+    }
+    // ---- state after chunk c -> bf16 B operand rows 32..127 of chunk c+1, F~ rescaled ----
+    if (c + 1 < nch) {
+      const int st1 = (c + 1) % CF::NS;
+      ok = wait_xch(c + 1);
+      if (ok) ok = mbar_wait_warp(&ms->st_done, c & 1, &ms->abort);
+      if (ok && c >= 1) ok = mbar_wait_warp(&ms->sst_free, (c - 1) & 1, &ms->abort);
+      if (!ok) break;
+      const Xch* xn = xch(smem, CF::XCH_OFF, st1);
+      cf_next = xn->coef[t];
+      M_next = xn->M;
       tc_fence_after();
       if (wq >= 1) {
-        const bool rescale = (wq == 1) && (M_cur > M_prev);
-        const float fac = rescale ? expf(__fsub_rn(M_prev, M_cur)) : 1.0f;
+        const bool rescale = (wq == 1) && (M_next > M_cur);
+        const float fac = rescale ? expf(__fsub_rn(M_cur, M_next)) : 1.0f;
         const uint32_t sst = base + CF::SST_OFF;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -815,24 +1062,52 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       fence_proxy_async_smem();
       mbar_arrive(&ms->sst_full);
     }
-    // ---- output rows of the previous chunk (its X was computed while this chunk's S and
-    // state tiles were being formed) ----
-    if (c >= 1) {
-      ok = xstep(c - 1, cf_prev);
-      if (!ok) break;
+    // ---- o = X_SV + a X_F + b X_G + g X_H for the rows of chunk c (two 16-column halves) ----
+    ok = mbar_wait_warp(&ms->x_full, c & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const int i = c * kC + t;
+    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t tx = tm + CF::TM_X + hf * 16;
+      float o[16], xb[16];
+      tmem_ld16x2(tx + 96, tx + 0, o, xb);
+      if (c >= 1) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = __fmaf_rn(cf.x, xb[j], o[j]);
+        float xc[16];
+        tmem_ld16x2(tx + 32, tx + 64, xb, xc);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = __fmaf_rn(cf.z, xc[j], __fmaf_rn(cf.y, xb[j], o[j]));
+      }
+      if (hf == 1) {
+        tc_fence_before();
+        mbar_arrive(&ms->x_free);
+      }
+      if (i < N) {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          uint4 p;
+          p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
+          p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
+          p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
+          p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
+          dst[2 * hf + x] = p;
+        }
+      }
     }
-    cf_prev = cf;
-    M_prev = M_cur;
+    cf = cf_next;
+    M_cur = M_next;
   }
-  if (ok && nch > 0) ok = xstep(nch - 1, cf_prev);
   if (!ok) {
-    fail_wait(ms, a.status);
+    fail_wait<CL>(ms, a.status);
     return;
   }
   // ---- final state (prefill): columns j0.. of F~, G, H (state rows 32..127) ----
   if (a.final_state && nch > 0) {
     if (!mbar_wait_warp(&ms->st_done, (nch - 1) & 1, &ms->abort)) {
-      fail_wait(ms, a.status);
+      fail_wait<CL>(ms, a.status);
       return;
     }
     tc_fence_after();
@@ -852,7 +1127,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
 }
 
 // ============================================================================ kernel
-template <int D>
+template <int D, int CL>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ ChunkParams p) {
   using CF = Cfg<D>;
   const FwdArgs& a = p.a;
@@ -864,33 +1139,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   const int bh = blockIdx.x, h = bh % a.H;
   const size_t row0 = (size_t)bh * a.N;
   const int nch = (a.N + kC - 1) / kC;
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tma_full[i], 1);
-      mbar_init(&ms->op_full[i], 128);
-      mbar_init(&ms->op_empty[i], 1);
+      mbar_init(&ms->qk_empty[i], CL);
+      mbar_init(&ms->vsc_free[i], 1);
     }
+    mbar_init(&ms->op_full, 128);
+    mbar_init(&ms->vsc_full, 128);
     mbar_init(&ms->a_full, 1);
     mbar_init(&ms->a_free, 128);
     mbar_init(&ms->am_full, 128);
     mbar_init(&ms->sst_full, 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->x_full[i], 1);
-      mbar_init(&ms->x_free[i], 128);
-    }
+    mbar_init(&ms->sst_free, 1);
+    mbar_init(&ms->x_full, 1);
+    mbar_init(&ms->x_free, 128);
     mbar_init(&ms->st_done, 1);
     mbar_init(&ms->fin, 1);
+    mbar_init(&ms->w_done, CL);
     mbar_init(&ms->pbar, 128);
     mbar_init(&ms->pobar, 128);
+    mbar_init(&ms->po_sync, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->scal_full[i], 128);
       mbar_init(&ms->scal_empty[i], 128);
     }
     mbar_init(&ms->u_full, 1);
     mbar_init(&ms->u_empty, 128);
+    mbar_init(&ms->vst_empty, 128);
+    mbar_init(&ms->peer_full, 1);
+    mbar_init(&ms->ccar_full, 32);
+    mbar_init(&ms->kcar_full, 1);
     ms->abort = 0;
     ms->never = 0;
+    if (CL > 1) fence_mbarrier_init_cluster();
   }
   if (warp == 12) {
     tmem_alloc(&ms->tmem, 512);
@@ -899,19 +1183,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CL > 1) cluster_sync_all();  // the other CTA's barriers exist before any remote access
 
-  if (warp < 4) {
-    role_scalars<D>(a, smem, ms, bh, h, row0, nch);
+  if (warp < 8 && (warp & 2) == 0) {
+    role_scalars<D, CL>(a, smem, ms, bh, h, row0, nch, rank);
   } else if (warp < 8) {
-    role_operands<D>(a, smem, ms, h, row0, nch);
+    role_operands<D, CL>(a, smem, ms, h, row0, nch, rank);
   } else if (warp < 12) {
-    role_epilogue<D>(a, smem, ms, bh, row0, nch);
+    role_epilogue<D, CL>(a, smem, ms, bh, row0, nch);
   } else if (warp == 12) {
-    if ((threadIdx.x & 31) == 0) role_mma<D>(a, smem, ms, nch);
+    if ((threadIdx.x & 31) == 0) role_mma<D, CL>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
-    role_tma<D>(p, smem, ms, bh, nch);
+    role_tma<D, CL>(p, smem, ms, bh, nch, rank);
   } else if ((threadIdx.x & 31) == 1) {
-    role_tma_u<D>(p, smem, ms, bh, nch);
+    role_tma_u<D, CL>(p, smem, ms, bh, nch, rank);
   }
 
   tc_fence_before();
@@ -921,6 +1206,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
     tc_fence_after();
     tmem_dealloc(ms->tmem, 512);
+  }
+  if (CL > 1 && threadIdx.x == 0 && nch > 0) {
+    // The other CTA's last stage and weight releases land in this CTA's barriers: wait for
+    // them (bounded) so that no arrival targets this CTA after it exits.  Every earlier phase
+    // of these barriers was waited for in order, so the parity identifies the phase.
+    for (int st = 0; st < CF::NS && st < nch; ++st) {
+      const int c_last = st + ((nch - 1 - st) / CF::NS) * CF::NS;
+      if (!mbar_wait_cl(&ms->qk_empty[st], (c_last / CF::NS) & 1, &ms->never, 1ll << 31))
+        report(a.status, kErrTimeout);
+    }
+    if (!mbar_wait_cl(&ms->w_done, (nch - 1) & 1, &ms->never, 1ll << 31))
+      report(a.status, kErrTimeout);
   }
 }
 
@@ -968,7 +1265,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chunk_kernel<D, kCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
@@ -981,9 +1278,22 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
       !make_map(&p.tv, a.v, D, a.N, BH, kDV, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tu, a.u, D, a.N, BH, D, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorNotSupported;
-  dim3 grid(BH, D / kDV);
-  chunk_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(p);
+  static_assert((D / kDV) % kCL == 0, "value slices pair up into clusters");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(BH, D / kDV, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = kCL;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kCL > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, chunk_kernel<D, kCL>, p);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
