@@ -46,7 +46,7 @@ L2_FLUSH_BYTES = 256 << 20
 # sources it was measured on; reported as null once the sources change.
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
                  "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"7c0695904cabb32f": 136547328 + 20113408}
+MEASURED_TRAFFIC = {"e27b41c13baaaded": 136448768 + 20346624}
 
 
 def kernel_fingerprint() -> str:
@@ -160,10 +160,12 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------------------------
-def oracle_rate(w: zi.Workload, inp_cpu: dict, seqs: int, tokens: int, nthreads: int):
-    """Run the fp64 oracle on `seqs` sequences x `tokens` tokens; return (tokens/s, seconds,
-    threads).  Throughput is counted in the metric's token unit (one (b, n) position carries
-    H heads, so seqs*tokens token-heads count as seqs*tokens/H tokens)."""
+def oracle_rate(w: zi.Workload, inp_cpu: dict, seqs: int, tokens: int, nthreads: int,
+                min_seconds: float = 0.0):
+    """Run the fp64 oracle on `seqs` sequences x `tokens` tokens, repeated until `min_seconds`
+    of wall time have passed; return (tokens/s, seconds, threads, passes).  Throughput is
+    counted in the metric's token unit (one (b, n) position carries H heads, so seqs*tokens
+    token-heads count as seqs*tokens/H tokens)."""
     import oracle
     pick = [(i // w.H, i % w.H) for i in range(seqs)]
     sel = lambda t: torch.stack([t[b, h, :tokens] for b, h in pick])[None]  # noqa: E731
@@ -176,12 +178,18 @@ def oracle_rate(w: zi.Workload, inp_cpu: dict, seqs: int, tokens: int, nthreads:
     q64, k64, v64, u64 = (a.reshape(1, seqs, tokens, w.d) for a in args)
     g164 = g1.double().numpy().reshape(1, seqs, tokens)
     gh64 = gh.double().numpy().reshape(1, seqs, tokens)
+    mu64, tau64 = mu.double().numpy(), tau.double().numpy()
     t0 = time.perf_counter()
-    oracle.forward(q64, k64, v64, u64, g164, gh64, mu.double().numpy(), tau.double().numpy(),
-                   causal=w.causal, rope=w.rope, rope_base=w.rope_base, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    token_heads = seqs * tokens
-    return token_heads / w.H / dt, dt, min(nthreads, seqs)
+    passes = 0
+    while True:
+        oracle.forward(q64, k64, v64, u64, g164, gh64, mu64, tau64, causal=w.causal,
+                       rope=w.rope, rope_base=w.rope_base, nthreads=nthreads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= 50:
+            break
+    token_heads = seqs * tokens * passes
+    return token_heads / w.H / dt, dt, min(nthreads, seqs), passes
 
 
 def reference_arm(args, w: zi.Workload):
@@ -199,7 +207,7 @@ def reference_arm(args, w: zi.Workload):
         oracle_rate(w, inp, seqs, tokens, cores)
     times = []
     for _ in range(args.steps):
-        _, dt, used = oracle_rate(w, inp, seqs, tokens, cores)
+        _, dt, used, _ = oracle_rate(w, inp, seqs, tokens, cores)
         times.append(dt)
     sec = sum(times) / len(times)
     value = seqs * tokens / w.H / sec
@@ -306,11 +314,10 @@ def ours_forward(args, w: zi.Workload):
         cores = oracle.threads()
         inp_cpu = {n: t.cpu() for n, t in inp.items()}
         seqs = min(w.B * w.H, max(cores, 1) * 4)
-        tokens = w.N
-        rate, dt, used = oracle_rate(w, inp_cpu, seqs, tokens, cores)
+        rate, dt, used, reps = oracle_rate(w, inp_cpu, seqs, w.N, cores, min_seconds=1.5)
         cpu = {"value": rate, "unit": "tokens/s", "cores": used, "kind": "oracle",
-               "sample": f"{seqs} of {w.B * w.H} (b,h) sequences x all {tokens} tokens, fp64 "
-                         f"recurrent oracle ({dt:.1f} s wall)"}
+               "sample": f"{seqs} of {w.B * w.H} (b,h) sequences x all {w.N} tokens, fp64 "
+                         f"recurrent oracle, {reps} passes ({dt:.1f} s wall)"}
 
     if rank == 0:
         line = {
