@@ -90,8 +90,7 @@ struct Cfg {
   static constexpr uint32_t K_OFF = Q_OFF + NS * KA * kTile;
   static constexpr uint32_t V_OFF = K_OFF + NS * KA * kTile;
   static constexpr uint32_t VST_OFF = V_OFF + NS * 2 * kTile;    // raw v slice [128 x 32]
-  static constexpr uint32_t AM_OFF = VST_OFF + 128 * 64;
-  static constexpr uint32_t SST_OFF = AM_OFF + 2 * kTile;
+  static constexpr uint32_t SST_OFF = VST_OFF + 128 * 64;
   static constexpr uint32_t RW_OFF = SST_OFF + KA * kTile;       // weight MMA A: [128 x 16] bf16
   static constexpr uint32_t CW_OFF = RW_OFF + kC * 32;           // weight MMA B: [128 x 16] bf16
   static constexpr uint32_t XCH_OFF = CW_OFF + kC * 32;          // Xch [NS]
@@ -108,6 +107,9 @@ struct Cfg {
   static constexpr uint32_t BYTES = MISC_OFF + 512;
   static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
   static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
+  // S tile (bf16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
+  // Q K^T columns (then the next Q K^T waits for the S V product)
+  static constexpr uint32_t TM_S = (D == 64) ? 448 : 0;
   // bytes a non-owner receives per chunk: rotated Q and K, the weight operands, the Xch block
   static constexpr uint32_t PEER_BYTES = 2 * KA * kTile + 2 * kC * 32 + (uint32_t)sizeof(Xch);
   static_assert(SMEM <= 232448, "shared memory budget of one CTA");
@@ -860,6 +862,8 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
     ok = owned ? mbar_wait(&ms->po_sync, ph, &ms->abort)
                : mbar_wait_cl(&ms->peer_full, ph, &ms->abort);
     if (ok && c >= 1) ok = mbar_wait(&ms->a_free, (c - 1) & 1, &ms->abort);
+    // the S tile shares the Q K^T columns: the previous S V product must have read it
+    if (CF::TM_S == CF::TM_A && ok && c >= 1) ok = mbar_wait(&ms->x_full, (c - 1) & 1, &ms->abort);
     // every phase of w_done is observed in order (the end-of-kernel wait relies on it)
     if (ok && c >= 1) ok = mbar_wait_cl(&ms->w_done, (c - 1) & 1, &ms->abort);
     if (!ok) break;
@@ -906,13 +910,11 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
     // ---- X[:, 96:128] = S V ----
     if (!mbar_wait(&ms->am_full, c & 1, &ms->abort)) { ok = false; break; }
     tc_fence_after();
-    const uint32_t sm = base + CF::AM_OFF;
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint32_t aoff = (kk / 4) * kTile + (kk % 4) * 32;  // K-major, K = token i
-      const uint32_t boff = kk * 2048;                          // MN-major, 16 rows per step
-      mma_bf16(tX + 96, sw128_desc(sm + aoff, 16, 1024), sw128_desc(vt + boff, kTile, 1024),
-               id_sv, kk > 0);
+      const uint32_t boff = kk * 2048;  // MN-major B, 16 token rows per step
+      mma_bf16_ts(tX + 96, tm + CF::TM_S + kk * 8, sw128_desc(vt + boff, kTile, 1024), id_sv,
+                  kk > 0);
     }
     mma_commit(&ms->x_full);
     if (c == 0) {  // the first chunk has no Q [F|G|H] product: release after the S tile was read
@@ -941,15 +943,6 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   const int j0 = blockIdx.y * kDV;
   const int N = a.N;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out) + row0 * D;
-  const uint32_t sm = base + CF::AM_OFF;
-  // Columns after every row of this warp (blocks cb > wq) are zero in every chunk: written once.
-  for (int cb = wq + 1; cb < 4; ++cb) {
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int col0 = cb * 32 + x * 8;
-      sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), make_uint4(0, 0, 0, 0));
-    }
-  }
   const int rank = CL > 1 ? (int)cluster_rank() : 0;
   auto owned = [&](int cc) { return (cc % CL) == rank; };
   // coefficients and M of chunk cc are in this CTA's Xch block
@@ -992,31 +985,36 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     ok = mbar_wait_warp(&ms->a_full, c & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
+    // block cb of S (columns 32cb..32cb+31) goes to the 16 packed columns 16cb.. of the S tile;
+    // with the S tile on the Q K^T columns these were read before (blocks run in order)
 #pragma unroll 1
     for (int cb = 0; cb <= wq; ++cb) {
       float v[32], wv[32];
       tmem_ld32x2(tm + CF::TM_A + cb * 32, tm + CF::TM_W + cb * 32, v, wv);
+      uint32_t pw[16];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int col0 = cb * 32 + x * 8;
-        uint32_t pw[4];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const int e0 = x * 8 + 2 * y;
-          float2 val = __fmul2_rn(make_float2(v[e0], v[e0 + 1]), make_float2(wv[e0], wv[e0 + 1]));
-          if (cb == wq) {  // diagonal block: keep i <= t only
-            if (col0 + 2 * y > t) val.x = 0.0f;
-            if (col0 + 2 * y + 1 > t) val.y = 0.0f;
-          }
-          pw[y] = pack_bf16x2(val.x, val.y);
+      for (int y = 0; y < 16; ++y) {
+        float2 val = __fmul2_rn(make_float2(v[2 * y], v[2 * y + 1]),
+                                make_float2(wv[2 * y], wv[2 * y + 1]));
+        if (cb == wq) {  // diagonal block: keep i <= t only
+          if (cb * 32 + 2 * y > t) val.x = 0.0f;
+          if (cb * 32 + 2 * y + 1 > t) val.y = 0.0f;
         }
-        sts128(sm + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8),
-               make_uint4(pw[0], pw[1], pw[2], pw[3]));
+        pw[y] = pack_bf16x2(val.x, val.y);
       }
+      tmem_st16_nowait(tm + CF::TM_S + cb * 16, pw);
     }
+    {
+      // blocks after every row of this warp are zero
+      uint32_t zw[16];
+#pragma unroll
+      for (int y = 0; y < 16; ++y) zw[y] = 0u;
+#pragma unroll 1
+      for (int cb = wq + 1; cb < 4; ++cb) tmem_st16_nowait(tm + CF::TM_S + cb * 16, zw);
+    }
+    tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&ms->a_free);
-    fence_proxy_async_smem();
     mbar_arrive(&ms->am_full);
     if (CL > 1 && c + 1 < nch && !owned(c + 1)) {
       ok = vsc_other(c + 1);

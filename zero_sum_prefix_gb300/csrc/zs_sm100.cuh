@@ -63,12 +63,10 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity)
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up (returns false) after
-// `limit_cycles` SM clock cycles (default 2^32, about two seconds) or as soon as *abort is set;
-// never spins unbounded.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          long long limit_cycles = 4294967296ll) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Polling loop of mbar_wait, kept out of line so that the many wait sites stay small (the
+// first probe is inline).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            long long limit_cycles) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -77,6 +75,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       if (clock64() - t0 > limit_cycles) return false;
     }
   }
+}
+
+// Waits for the phase with the given parity to complete.  Gives up (returns false) after
+// `limit_cycles` SM clock cycles (default 2^32, about two seconds) or as soon as *abort is set;
+// never spins unbounded.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long limit_cycles = 4294967296ll) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, limit_cycles);
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -116,9 +123,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // mbar_wait with cluster-scope acquire (see mbar_try_wait_cl).
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                             long long limit_cycles = 4294967296ll) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_cl_slow(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, long long limit_cycles) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cl(bar, parity)) return true;
@@ -127,6 +133,11 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, vol
       if (clock64() - t0 > limit_cycles) return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             long long limit_cycles = 4294967296ll) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  return mbar_wait_cl_slow(bar, parity, abort, limit_cycles);
 }
 
 __device__ __forceinline__ bool mbar_wait_cl_warp(uint64_t* bar, uint32_t parity,
@@ -230,6 +241,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] = (accumulate ? D : 0) + A * B with A (bf16, K-major) in tensor memory: lane m holds
+// row m, each 32-bit column two consecutive K elements (the lower K index in the low half);
+// B bf16 from shared memory, D fp32.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The mbarrier receives one arrival once every MMA issued so far by this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -317,6 +340,20 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va
     va[i] = __uint_as_float(r[i]);
     vb[i] = __uint_as_float(q[i]);
   }
+}
+
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (no wait: see tmem_wait_st).
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Store 32 consecutive fp32 columns of this thread's TMEM lane; includes the wait.
