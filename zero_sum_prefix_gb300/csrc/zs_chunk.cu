@@ -36,7 +36,7 @@
 //   warps 0,1,4,5 (PS): warp w owns the 32-token block w of the chunk: the block's column sums,
 //                     logits and local scalar chains (carries of earlier blocks through shared
 //                     memory, two bounded barriers per chunk); hands (s, m, Et, P) per token and
-//                     the chunk reference to PO through a two-slot ring.
+//                     the chunk reference to PO through a ring (two slots, one with a cluster).
 //   warps 2,3,6,7 (PO): per token row: rotary factors, rotate q/k in place (RoPE), norms, gates,
 //                     row coefficients, the hi/lo weight operands and the scaled value tile Vsc.
 //   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> bf16 tile; state -> bf16
@@ -82,30 +82,35 @@ struct Xch {
 };
 static_assert(sizeof(Xch) == 3600, "Xch is moved by one bulk copy (multiple of 16 bytes)");
 
-template <int D>
+template <int D, int CL>
 struct Cfg {
   static constexpr int KA = D / 64;               // atom tiles along d
-  static constexpr int NS = (D == 64) ? 2 : 1;    // operand stages
+  // Operand stages: NSV for the scaled value tile, NSQ for q, k and the Xch block.  With a
+  // cluster at d = 64 the chunks of one owner are two apart; a third q/k stage lets an owner's
+  // next chunk load while its previous chunk and the other CTA's chunk are in flight.
+  static constexpr int NSV = (D == 64) ? 2 : 1;
+  static constexpr int NSQ = (CL > 1 && D == 64) ? 3 : NSV;
+  static constexpr int SCALS = (CL > 1) ? 1 : 2;  // slots of the scalar ring
   static constexpr uint32_t Q_OFF = 0;
-  static constexpr uint32_t K_OFF = Q_OFF + NS * KA * kTile;
-  static constexpr uint32_t V_OFF = K_OFF + NS * KA * kTile;
-  static constexpr uint32_t VST_OFF = V_OFF + NS * 2 * kTile;    // raw v slice [128 x 32]
+  static constexpr uint32_t K_OFF = Q_OFF + NSQ * KA * kTile;
+  static constexpr uint32_t V_OFF = K_OFF + NSQ * KA * kTile;
+  static constexpr uint32_t VST_OFF = V_OFF + NSV * 2 * kTile;   // raw v slice [128 x 32]
   static constexpr uint32_t SST_OFF = VST_OFF + 128 * 64;
   static constexpr uint32_t RW_OFF = SST_OFF + KA * kTile;       // weight MMA A: [128 x 16] bf16
   static constexpr uint32_t CW_OFF = RW_OFF + kC * 32;           // weight MMA B: [128 x 16] bf16
-  static constexpr uint32_t XCH_OFF = CW_OFF + kC * 32;          // Xch [NS]
-  static constexpr uint32_t U_OFF = align_up(XCH_OFF + NS * (uint32_t)sizeof(Xch), 1024);
+  static constexpr uint32_t XCH_OFF = CW_OFF + kC * 32;          // Xch [NSQ]
+  static constexpr uint32_t U_OFF = align_up(XCH_OFF + NSQ * (uint32_t)sizeof(Xch), 1024);
   static constexpr uint32_t PHI_OFF = U_OFF + kC * D * 2;             // float [2][D/2] base angles
   static constexpr uint32_t THETA_OFF = PHI_OFF + 2 * (D / 2) * 4;    // float [D/2] frequencies
   static constexpr uint32_t LEND_OFF = THETA_OFF + (D / 2) * 4;       // float [4][D]
   static constexpr uint32_t BPUB_OFF = LEND_OFF + 4 * D * 4;         // float [4][4] + [2][4]
   static constexpr uint32_t CHAIN_OFF = BPUB_OFF + 128;               // float4 [4][32]
-  static constexpr uint32_t SCAL_OFF = CHAIN_OFF + 4 * 32 * 16;     // float4 [2][128]
-  static constexpr uint32_t CIN_OFF = SCAL_OFF + 2 * kC * 16;       // float [2][D] column carries
+  static constexpr uint32_t SCAL_OFF = CHAIN_OFF + 4 * 32 * 16;     // float4 [SCALS][128]
+  static constexpr uint32_t CIN_OFF = SCAL_OFF + SCALS * kC * 16;   // float [2][D] column carries
   static constexpr uint32_t KCIN_OFF = CIN_OFF + 2 * D * 4;         // float [2][4] scalar carries
   static constexpr uint32_t MISC_OFF = KCIN_OFF + 32;
   static constexpr uint32_t BYTES = MISC_OFF + 512;
-  static constexpr uint32_t SMEM = BYTES + 1024;                 // + alignment slack
+  static constexpr uint32_t SMEM = BYTES;  // the base is 1024-byte aligned (checked at entry)
   static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
   // S tile (bf16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
   // Q K^T columns (then the next Q K^T waits for the S V product)
@@ -119,7 +124,7 @@ struct Misc {
   uint64_t tma_full[2];
   uint64_t u_full, u_empty, vst_empty;
   uint64_t op_full, vsc_full;        // Vsc of an owned / other-owned chunk written
-  uint64_t qk_empty[2];  // Q, K and Xch of a stage released by every CTA of the cluster
+  uint64_t qk_empty[3];  // Q, K and Xch of a stage released by every CTA of the cluster
   uint64_t vsc_free[2];  // Vsc of the last chunk of this parity consumed (S V completed)
   uint64_t a_full, a_free, am_full, sst_full, sst_free, st_done, fin;
   uint64_t w_done;                   // both CTAs' weight MMAs have read R and C
@@ -131,10 +136,16 @@ struct Misc {
   uint64_t peer_full;            // tiles of a chunk owned by the other CTA have landed
   uint64_t ccar_full, kcar_full;  // carries from the other CTA's previous chunk
   float Mslot[2];
+  int w_seen;  // with a cluster: number of w_done phases observed (monotonic)
   uint32_t tmem;
   int abort;
   int never;  // stays 0: lets the final waits ignore the abort flag
 };
+
+static_assert(sizeof(Misc) <= 512, "Misc fits its shared-memory slot");
+static_assert(Cfg<64, 2>::NSQ <= 3 && Cfg<64, 1>::NSQ <= 3 && Cfg<128, 2>::NSQ <= 3,
+              "qk_empty has one barrier per q/k stage");
+static_assert(Cfg<64, 1>::SCALS <= 2 && Cfg<64, 2>::SCALS <= 2, "scal ring barriers");
 
 struct ChunkParams {
   CUtensorMap tq, tk, tv;  // q, k: box {64, 128, 1} 128B swizzle; v: box {32, 128, 1} 64B swizzle
@@ -160,11 +171,11 @@ __device__ __forceinline__ Xch* xch(uint8_t* smem, uint32_t off, int st) {
 // cannot have).
 template <int D, int CL>
 __device__ __forceinline__ int tf_index(int c) {
-  return CL > 1 ? c % CL : c % Cfg<D>::NS;
+  return CL > 1 ? c % CL : c % Cfg<D, CL>::NSQ;
 }
 template <int D, int CL>
 __device__ __forceinline__ uint32_t tf_phase(int c) {
-  return (uint32_t)(CL > 1 ? c / CL : c / Cfg<D>::NS) & 1u;
+  return (uint32_t)(CL > 1 ? c / CL : c / Cfg<D, CL>::NSQ) & 1u;
 }
 
 // Before the Vsc tile of chunk c is written: the S V product of chunk c - NS (same stage) has
@@ -172,7 +183,7 @@ __device__ __forceinline__ uint32_t tf_phase(int c) {
 // CTA's chunks, epilogue warps for the other CTA's) waits for consecutive phases of its own.
 template <int D, int CL>
 __device__ __forceinline__ bool vsc_wait(Misc* ms, int c) {
-  constexpr int NS = Cfg<D>::NS;
+  constexpr int NS = Cfg<D, CL>::NSV;
   if (c < NS) return true;
   return mbar_wait_warp(&ms->vsc_free[(c - NS) & 1], (uint32_t)((c - NS) >> 1) & 1u, &ms->abort);
 }
@@ -222,7 +233,7 @@ __device__ __forceinline__ int group_index() {
 template <int D, int CL>
 __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
                          int rank) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const uint32_t base = smem_u32(smem);
   const int j0 = blockIdx.y * kDV;
   constexpr uint32_t qk_bytes = 2 * CF::KA * kTile, v_bytes = 128 * 64;
@@ -230,9 +241,9 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
   tma_prefetch_desc(&p.tk);
   tma_prefetch_desc(&p.tv);
   for (int c = 0; c < nch; ++c) {
-    const int st = c % CF::NS;
+    const int st = c % CF::NSQ;
     const bool owned = (c % CL) == rank;
-    if (c >= CF::NS) {
+    if (c >= CF::NSQ) {
       // the chunk's tiles start towards L2 while the stage is still in use
       if (owned) {
 #pragma unroll
@@ -243,14 +254,20 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
       }
       tma_prefetch_3d(&p.tv, j0, c * kC, bh);
       // both CTAs of the cluster have released the stage's Q, K and Xch
-      if (!mbar_wait_cl(&ms->qk_empty[st], ((c / CF::NS) - 1) & 1, &ms->abort)) {
+      if (!mbar_wait_cl(&ms->qk_empty[st], ((c / CF::NSQ) - 1) & 1, &ms->abort)) {
         fail_wait<CL>(ms, p.a.status);
         return;
       }
     }
-    // a chunk owned by the other CTA: its tiles arrive by bulk copy (the previous phase of
-    // peer_full completed before this chunk's stage was released)
-    if (CL > 1 && !owned) mbar_arrive_expect_tx(&ms->peer_full, CF::PEER_BYTES);
+    // a chunk owned by the other CTA: its tiles arrive by bulk copy; the barrier's previous
+    // phase (the other CTA's previous chunk) must have completed before this arrival
+    if (CL > 1 && !owned) {
+      if (c >= CL && !mbar_wait_cl(&ms->peer_full, (uint32_t)((c - CL) / CL) & 1u, &ms->abort)) {
+        fail_wait<CL>(ms, p.a.status);
+        return;
+      }
+      mbar_arrive_expect_tx(&ms->peer_full, CF::PEER_BYTES);
+    }
     uint64_t* tf = &ms->tma_full[tf_index<D, CL>(c)];
     mbar_arrive_expect_tx(tf, (owned ? qk_bytes : 0u) + v_bytes);
     if (owned) {
@@ -271,12 +288,26 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
   }
 }
 
+// With a cluster: observes every phase of w_done in order and publishes the count, for the
+// operand warps, which only handle every other chunk (a parity wait names its phase only when
+// the waiter has seen the previous one).
+template <int CL>
+__device__ void role_wdone_observer(const FwdArgs& a, Misc* ms, int nch) {
+  for (int c = 0; c < nch; ++c) {
+    if (!mbar_wait_cl(&ms->w_done, (uint32_t)c & 1u, &ms->abort)) {
+      fail_wait<CL>(ms, a.status);
+      return;
+    }
+    st_release_s32(&ms->w_seen, c + 1);
+  }
+}
+
 // u rows of each owned chunk (single buffer, released by the scalar warps after their logits);
 // a separate producer thread so that this stream never waits behind the operand stages.
 template <int D, int CL>
 __device__ void role_tma_u(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
                            int rank) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const uint32_t base = smem_u32(smem);
   tma_prefetch_desc(&p.tu);
   for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
@@ -378,7 +409,7 @@ __device__ __forceinline__ UCols<D / 32> load_ucols(const uint8_t* us, int j) {
 template <int D, int CL>
 __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
                              size_t row0, int nch, int rank) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   constexpr int R = D / 32;
   constexpr int RP = (R + 1) / 2;  // column pairs per lane (R = 1 uses the .x half only)
   const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-token block
@@ -409,7 +440,7 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
   }
 
   for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
-    const int slot = kk & 1;
+    const int slot = kk % CF::SCALS;
     const int i = c * kC + r;
     const bool valid = i < N;
     const int b0 = c * kC + 32 * w;  // first token of this warp's block
@@ -594,8 +625,9 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
       if (a.dbg_P) a.dbg_P[row0 + i] = P;
       if (a.dbg_m) a.dbg_m[row0 + i] = m;
     }
-    // hand the scalars to the operand warps (two-slot ring)
-    if (kk >= 2 && !mbar_wait_warp(&ms->scal_empty[slot], ((kk >> 1) - 1) & 1, &ms->abort)) {
+    // hand the scalars to the operand warps (ring of SCALS slots)
+    if (kk >= CF::SCALS &&
+        !mbar_wait_warp(&ms->scal_empty[slot], ((kk / CF::SCALS) - 1) & 1, &ms->abort)) {
       fail_wait<CL>(ms, a.status);
       return;
     }
@@ -643,7 +675,7 @@ __device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, 
 template <int D, int CL>
 __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, size_t row0,
                               int nch, int rank) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-row group
   const int r = 32 * w + lane;      // token row inside the chunk, 0..127
   const int N = a.N;
@@ -683,7 +715,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
   put_phi(rank, 0);
 
   for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
-    const int st = c % CF::NS;
+    const int st = c % CF::NSQ;
     const int i = c * kC + r;
     const bool valid = i < N;
     Xch* xc = xch(smem, CF::XCH_OFF, st);
@@ -698,7 +730,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
     }
     uint8_t* qt = smem + CF::Q_OFF + st * CF::KA * kTile;
     uint8_t* kt = smem + CF::K_OFF + st * CF::KA * kTile;
-    uint8_t* vt = smem + CF::V_OFF + st * 2 * kTile;
+    uint8_t* vt = smem + CF::V_OFF + (c % CF::NSV) * 2 * kTile;
     float g1n, ghn;
     load_gates(c + CL, g1n, ghn);
     float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
@@ -724,8 +756,8 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
       }
       const float qq = __fadd_rn(qq2.x, qq2.y), kq = __fadd_rn(kk2.x, kk2.y);
       // ---- scalars of this token from the scalar warps ----
-      const int slot = kk & 1;
-      if (!mbar_wait_warp(&ms->scal_full[slot], (kk >> 1) & 1, &ms->abort)) {
+      const int slot = kk % CF::SCALS;
+      if (!mbar_wait_warp(&ms->scal_full[slot], (kk / CF::SCALS) & 1, &ms->abort)) {
         fail_wait<CL>(ms, a.status);
         return;
       }
@@ -762,10 +794,15 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
       // x = x + x') and the column vector [e e' e e' s s' s s' k k' k k' 0 0 0 0] paired as
       // (hi hi, hi lo, lo hi, lo lo): every product is exact in fp32, the representation error
       // is about 2^-17 of each term, so the nearly cancelling sum keeps fp32-level accuracy.
-      // The buffer is single: both CTAs' weight MMAs of the previous chunk must have completed.
-      // (Phase c-2 of w_done is complete here: the stage of this chunk was released after both
-      // CTAs' MMAs of an earlier chunk, whose weight commits precede their stage commits.)
-      if (c >= 1 && !mbar_wait_cl_warp(&ms->w_done, (c - 1) & 1, &ms->abort)) {
+      // The buffer is single: both CTAs' weight MMAs of the previous chunk must have completed
+      // (without a cluster these warps wait for every phase of w_done in order; with one, the
+      // observer thread's count says how many phases completed).
+      bool wok = true;
+      if (c >= 1) {
+        wok = CL > 1 ? counter_wait(&ms->w_seen, c, &ms->abort)
+                     : mbar_wait(&ms->w_done, (c - 1) & 1, &ms->abort);
+      }
+      if (!__all_sync(0xffffffffu, wok)) {
         fail_wait<CL>(ms, a.status);
         return;
       }
@@ -841,7 +878,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
 template <int D, int CL>
 __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
   constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1u);  // every CTA of the cluster
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const uint32_t tA = tm + CF::TM_A, tW = tm + CF::TM_W, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
@@ -853,12 +890,12 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
   bool ok = true;
   const int rank = CL > 1 ? (int)cluster_rank() : 0;
   for (int c = 0; c < nch && ok; ++c) {
-    const int st = c % CF::NS;
+    const int st = c % CF::NSQ;
     const bool owned = (c % CL) == rank;
     const uint32_t ph = (uint32_t)(c / CL) & 1u;  // phase of the owned / other-owned barriers
     const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
     const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
-    const uint32_t vt = base + CF::V_OFF + st * 2 * kTile;
+    const uint32_t vt = base + CF::V_OFF + (c % CF::NSV) * 2 * kTile;
     ok = owned ? mbar_wait(&ms->po_sync, ph, &ms->abort)
                : mbar_wait_cl(&ms->peer_full, ph, &ms->abort);
     if (ok && c >= 1) ok = mbar_wait(&ms->a_free, (c - 1) & 1, &ms->abort);
@@ -934,7 +971,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 template <int D, int CL>
 __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, size_t row0,
                               int nch) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const int wq = (threadIdx.x >> 5) & 3;          // TMEM lane quadrant of this warp
   const int t = wq * 32 + (threadIdx.x & 31);     // TMEM lane = token row / state row
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -953,7 +990,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   };
   // value tile of a chunk owned by the other CTA (row t)
   auto vsc_other = [&](int cc) -> bool {
-    const int sv = cc % CF::NS;
+    const int sv = cc % CF::NSV;
     if (!mbar_wait_warp(&ms->tma_full[tf_index<D, CL>(cc)], tf_phase<D, CL>(cc), &ms->abort))
       return false;
     if (!vsc_wait<D, CL>(ms, cc)) return false;
@@ -961,7 +998,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     copy_v_row(vt, smem + CF::VST_OFF, t);
     mbar_arrive(&ms->vst_empty);
     if (!mbar_wait_cl_warp(&ms->peer_full, (uint32_t)(cc / CL) & 1u, &ms->abort)) return false;
-    const Xch* xv = xch(smem, CF::XCH_OFF, sv);
+    const Xch* xv = xch(smem, CF::XCH_OFF, cc % CF::NSQ);
     build_vsc_row(vt, t, xv->cols[0][t], xv->cols[1][t], xv->cols[2][t]);
     fence_proxy_async_smem();
     mbar_arrive(&ms->vsc_full);
@@ -985,24 +1022,46 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     ok = mbar_wait_warp(&ms->a_full, c & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
-    // block cb of S (columns 32cb..32cb+31) goes to the 16 packed columns 16cb.. of the S tile;
-    // with the S tile on the Q K^T columns these were read before (blocks run in order)
-#pragma unroll 1
-    for (int cb = 0; cb <= wq; ++cb) {
-      float v[32], wv[32];
-      tmem_ld32x2(tm + CF::TM_A + cb * 32, tm + CF::TM_W + cb * 32, v, wv);
-      uint32_t pw[16];
+    // 16-column piece h of S (columns 16h..16h+15) goes to the 8 packed columns 8h.. of the S
+    // tile; pieces are double-buffered (the load of piece h+1 is in flight while piece h is
+    // formed).  With the S tile on the Q K^T columns, every column written was read before.
+    {
+      const int npiece = 2 * (wq + 1);  // pieces holding entries i <= t for some row of the warp
+      uint32_t ra0[16], rw0[16], ra1[16], rw1[16];
+      auto piece = [&](int h, uint32_t (&ra)[16], uint32_t (&rw)[16]) {
+        uint32_t pw[8];
 #pragma unroll
-      for (int y = 0; y < 16; ++y) {
-        float2 val = __fmul2_rn(make_float2(v[2 * y], v[2 * y + 1]),
-                                make_float2(wv[2 * y], wv[2 * y + 1]));
-        if (cb == wq) {  // diagonal block: keep i <= t only
-          if (cb * 32 + 2 * y > t) val.x = 0.0f;
-          if (cb * 32 + 2 * y + 1 > t) val.y = 0.0f;
+        for (int y = 0; y < 8; ++y) {
+          float2 val = __fmul2_rn(make_float2(__uint_as_float(ra[2 * y]), __uint_as_float(ra[2 * y + 1])),
+                                  make_float2(__uint_as_float(rw[2 * y]), __uint_as_float(rw[2 * y + 1])));
+          const int col = 16 * h + 2 * y;
+          if ((h >> 1) == wq) {  // diagonal block: keep i <= t only
+            if (col > t) val.x = 0.0f;
+            if (col + 1 > t) val.y = 0.0f;
+          }
+          pw[y] = pack_bf16x2(val.x, val.y);
         }
-        pw[y] = pack_bf16x2(val.x, val.y);
+        tmem_st8_nowait(tm + CF::TM_S + 8 * h, pw);
+      };
+      tmem_ld16_nowait(tm + CF::TM_A, ra0);
+      tmem_ld16_nowait(tm + CF::TM_W, rw0);
+#pragma unroll 1
+      for (int h = 0; h < npiece; h += 2) {
+        tmem_wait_ld();
+        reg_fence(ra0);
+        reg_fence(rw0);
+        tmem_ld16_nowait(tm + CF::TM_A + 16 * (h + 1), ra1);
+        tmem_ld16_nowait(tm + CF::TM_W + 16 * (h + 1), rw1);
+        piece(h, ra0, rw0);
+        tmem_wait_ld();
+        reg_fence(ra1);
+        reg_fence(rw1);
+        if (h + 2 < npiece) {
+          tmem_ld16_nowait(tm + CF::TM_A + 16 * (h + 2), ra0);
+          tmem_ld16_nowait(tm + CF::TM_W + 16 * (h + 2), rw0);
+        }
+        piece(h + 1, ra1, rw1);
       }
-      tmem_st16_nowait(tm + CF::TM_S + cb * 16, pw);
     }
     {
       // blocks after every row of this warp are zero
@@ -1022,7 +1081,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     }
     // ---- state after chunk c -> bf16 B operand rows 32..127 of chunk c+1, F~ rescaled ----
     if (c + 1 < nch) {
-      const int st1 = (c + 1) % CF::NS;
+      const int st1 = (c + 1) % CF::NSQ;
       ok = wait_xch(c + 1);
       if (ok) ok = mbar_wait_warp(&ms->st_done, c & 1, &ms->abort);
       if (ok && c >= 1) ok = mbar_wait_warp(&ms->sst_free, (c - 1) & 1, &ms->abort);
@@ -1035,24 +1094,38 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         const bool rescale = (wq == 1) && (M_next > M_cur);
         const float fac = rescale ? expf(__fsub_rn(M_cur, M_next)) : 1.0f;
         const uint32_t sst = base + CF::SST_OFF;
+        // 32 state columns per round: two 16-column loads, one wait
 #pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float v[32];
-          tmem_ld32(tm + CF::TM_ST + cb * 32, v);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[2][16];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) tmem_ld16_nowait(tm + CF::TM_ST + c0 + 16 * q, rr[q]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) reg_fence(rr[q]);
           if (rescale) {
 #pragma unroll
-            for (int y = 0; y < 32; ++y) v[y] = __fmul_rn(v[y], fac);
-            tmem_st32(tm + CF::TM_ST + cb * 32, v);
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+              for (int y = 0; y < 16; ++y)
+                rr[q][y] = __float_as_uint(__fmul_rn(__uint_as_float(rr[q][y]), fac));
+              tmem_st16_nowait(tm + CF::TM_ST + c0 + 16 * q, rr[q]);
+            }
+            tmem_wait_st();
           }
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            uint4 p;
-            p.x = pack_bf16x2(v[8 * x + 0], v[8 * x + 1]);
-            p.y = pack_bf16x2(v[8 * x + 2], v[8 * x + 3]);
-            p.z = pack_bf16x2(v[8 * x + 4], v[8 * x + 5]);
-            p.w = pack_bf16x2(v[8 * x + 6], v[8 * x + 7]);
-            const int col0 = cb * 32 + x * 8;
-            sts128(sst + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
+          for (int q = 0; q < 2; ++q) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              const uint32_t* w8 = rr[q] + 8 * x;
+              uint4 p;
+              p.x = pack_bf16x2(__uint_as_float(w8[0]), __uint_as_float(w8[1]));
+              p.y = pack_bf16x2(__uint_as_float(w8[2]), __uint_as_float(w8[3]));
+              p.z = pack_bf16x2(__uint_as_float(w8[4]), __uint_as_float(w8[5]));
+              p.w = pack_bf16x2(__uint_as_float(w8[6]), __uint_as_float(w8[7]));
+              const int col0 = c0 + 16 * q + 8 * x;
+              sts128(sst + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
+            }
           }
         }
       }
@@ -1069,30 +1142,39 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       const uint32_t tx = tm + CF::TM_X + hf * 16;
-      float o[16], xb[16];
-      tmem_ld16x2(tx + 96, tx + 0, o, xb);
+      uint32_t rsv[16], rx[16];
+      tmem_ld16_nowait(tx + 96, rsv);
+      if (c >= 1) tmem_ld16_nowait(tx + 0, rx);
+      tmem_wait_ld();
+      reg_fence(rsv);
       if (c >= 1) {
+        reg_fence(rx);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = __fmaf_rn(cf.x, xb[j], o[j]);
-        float xc[16];
-        tmem_ld16x2(tx + 32, tx + 64, xb, xc);
+        for (int j = 0; j < 16; ++j)
+          rsv[j] = __float_as_uint(__fmaf_rn(cf.x, __uint_as_float(rx[j]), __uint_as_float(rsv[j])));
+        uint32_t ry[16];
+        tmem_ld16_nowait(tx + 32, rx);
+        tmem_ld16_nowait(tx + 64, ry);
+        tmem_wait_ld();
+        reg_fence(rx);
+        reg_fence(ry);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = __fmaf_rn(cf.z, xc[j], __fmaf_rn(cf.y, xb[j], o[j]));
+        for (int j = 0; j < 16; ++j)
+          rsv[j] = __float_as_uint(__fmaf_rn(cf.z, __uint_as_float(ry[j]),
+                                             __fmaf_rn(cf.y, __uint_as_float(rx[j]),
+                                                       __uint_as_float(rsv[j]))));
       }
+      uint32_t ob[8];  // the half's 16 outputs as bf16 pairs
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ob[j] = pack_bf16x2(__uint_as_float(rsv[2 * j]), __uint_as_float(rsv[2 * j + 1]));
       if (hf == 1) {
         tc_fence_before();
         mbar_arrive(&ms->x_free);
       }
       if (i < N) {
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          uint4 p;
-          p.x = pack_bf16x2(o[8 * x + 0], o[8 * x + 1]);
-          p.y = pack_bf16x2(o[8 * x + 2], o[8 * x + 3]);
-          p.z = pack_bf16x2(o[8 * x + 4], o[8 * x + 5]);
-          p.w = pack_bf16x2(o[8 * x + 6], o[8 * x + 7]);
-          dst[2 * hf + x] = p;
-        }
+        dst[2 * hf + 0] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        dst[2 * hf + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
       }
     }
     cf = cf_next;
@@ -1127,11 +1209,14 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
 // ============================================================================ kernel
 template <int D, int CL>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ ChunkParams p) {
-  using CF = Cfg<D>;
+  using CF = Cfg<D, CL>;
   const FwdArgs& a = p.a;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) report(a.status, kErrUnsupported);
+    return;
+  }
   Misc* ms = reinterpret_cast<Misc*>(smem + CF::MISC_OFF);
   const int warp = threadIdx.x >> 5;
   const int bh = blockIdx.x, h = bh % a.H;
@@ -1142,9 +1227,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tma_full[i], 1);
-      mbar_init(&ms->qk_empty[i], CL);
       mbar_init(&ms->vsc_free[i], 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&ms->qk_empty[i], CL);
     mbar_init(&ms->op_full, 128);
     mbar_init(&ms->vsc_full, 128);
     mbar_init(&ms->a_full, 1);
@@ -1172,6 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->kcar_full, 1);
     ms->abort = 0;
     ms->never = 0;
+    ms->w_seen = 0;
     if (CL > 1) fence_mbarrier_init_cluster();
   }
   if (warp == 12) {
@@ -1195,6 +1281,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     role_tma<D, CL>(p, smem, ms, bh, nch, rank);
   } else if ((threadIdx.x & 31) == 1) {
     role_tma_u<D, CL>(p, smem, ms, bh, nch, rank);
+  } else if (CL > 1 && (threadIdx.x & 31) == 2) {
+    role_wdone_observer<CL>(a, ms, nch);
   }
 
   tc_fence_before();
@@ -1209,13 +1297,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     // The other CTA's last stage and weight releases land in this CTA's barriers: wait for
     // them (bounded) so that no arrival targets this CTA after it exits.  Every earlier phase
     // of these barriers was waited for in order, so the parity identifies the phase.
-    for (int st = 0; st < CF::NS && st < nch; ++st) {
-      const int c_last = st + ((nch - 1 - st) / CF::NS) * CF::NS;
-      if (!mbar_wait_cl(&ms->qk_empty[st], (c_last / CF::NS) & 1, &ms->never, 1ll << 31))
+    for (int st = 0; st < CF::NSQ && st < nch; ++st) {
+      const int c_last = st + ((nch - 1 - st) / CF::NSQ) * CF::NSQ;
+      if (!mbar_wait_cl(&ms->qk_empty[st], (c_last / CF::NSQ) & 1, &ms->never, 1ll << 31))
         report(a.status, kErrTimeout);
     }
-    if (!mbar_wait_cl(&ms->w_done, (nch - 1) & 1, &ms->never, 1ll << 31))
-      report(a.status, kErrTimeout);
+    // (every phase of w_done was waited for by the observer thread before the final barrier)
   }
 }
 
@@ -1264,7 +1351,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
     e = cudaFuncSetAttribute(chunk_kernel<D, kCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Cfg<D>::SMEM);
+                             (int)Cfg<D, kCL>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
@@ -1280,7 +1367,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(BH, D / kDV, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<D, kCL>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -194,6 +194,29 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// Monotonic counters in shared memory (for a waiter that does not see every phase of a barrier).
+__device__ __forceinline__ void st_release_s32(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Waits until *p >= target; bounded like mbar_wait.
+__device__ __noinline__ bool counter_wait(const int* p, int target, volatile int* abort,
+                                          long long limit_cycles = 4294967296ll) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_s32(p) >= target) return true;
+    __nanosleep(64);
+    if ((it & 15) == 15) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit_cycles) return false;
+    }
+  }
+}
+
 // mbar_wait for roles whose next step is warp-collective (tcgen05.ld/st, shuffles): every lane
 // waits and the outcome is made identical across the warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
@@ -287,6 +310,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Issue a load of 16 consecutive 32-bit columns of this thread's TMEM lane without waiting.
+// The registers may only be read after tmem_wait_ld() followed by reg_fence() on them.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Ties the registers to this point (after a wait): no read of them is moved above it.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+// Store 8 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
 }
 
 // Two blocks of 16 consecutive fp32 columns of this thread's TMEM lane, one wait for both.
