@@ -46,7 +46,7 @@ L2_FLUSH_BYTES = 256 << 20
 # sources it was measured on; reported as null once the sources change.
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
                  "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"e27b41c13baaaded": 136448768 + 20346624}
+MEASURED_TRAFFIC = {"d9a00efde17d4d9b": 136402432 + 19879424}
 
 
 def kernel_fingerprint() -> str:
@@ -132,14 +132,20 @@ class ClockSampler:
 
 
 def dist_setup():
+    """Rank / world from the torchrun environment.  One process per GPU over NCCL; on a host
+    without CUDA (the multi-process tests) the same code runs over gloo."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    cuda = torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if cuda:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    elif cuda:
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -154,9 +160,16 @@ def max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, ms_per_rank: float, world: int) -> tuple:
+    """Whole-job throughput: the units every rank processed / the slowest rank's time."""
+    ms = max_over_ranks(ms_per_rank, world)
+    return units_per_rank * world / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------------------------------------
@@ -270,9 +283,8 @@ def ours_forward(args, w: zi.Workload):
     if zs.get_status() != 0:
         raise RuntimeError("device status after the timed region")
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = max_over_ranks(sum(per) / len(per), world)
     tokens = w.B * w.N
-    value = tokens * world / (ms / 1e3)
+    value, ms = aggregate_rate(tokens, sum(per) / len(per), world)
 
     hbm, peak_kind = peaks()
     alg = algorithmic_bytes(w)
