@@ -59,6 +59,14 @@ def _unpack(q, k, v, u, g1, gh, mu, tau):
     return q, k, v, u, g1, gh, mu, tau, (B, H, N, d)
 
 
+def _gate(g, shape):
+    if g is None:
+        return None
+    g = _f64(g)
+    assert g.shape == shape
+    return g
+
+
 class Oracle:
     """ctypes front end of one compiled oracle library."""
 
@@ -67,9 +75,9 @@ class Oracle:
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
         lib.zs_oracle_fwd.argtypes = [dp] * 9 + [i] * 6 + [ctypes.c_double, ctypes.c_double,
-                                                         i, dp, dp, dp]
+                                                         i, dp, dp, dp, dp]
         lib.zs_oracle_fwd.restype = i
-        lib.zs_oracle_brute.argtypes = [dp] * 9 + [i] * 6 + [ctypes.c_double, i, dp, dp]
+        lib.zs_oracle_brute.argtypes = [dp] * 9 + [i] * 6 + [ctypes.c_double, i, dp, dp, dp]
         lib.zs_oracle_brute.restype = i
         lib.zs_oracle_threads.restype = i
         self.lib = lib
@@ -79,13 +87,15 @@ class Oracle:
         return self.lib.zs_oracle_threads()
 
     def forward(self, q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False,
-                rope_base=10000.0, pos0=0.0, nthreads=0, debug=False):
+                rope_base=10000.0, pos0=0.0, nthreads=0, debug=False, g0=None):
         """Recurrent fp64 forward (five prefix states).  Layouts: q,k,v,u [B,H,N,d],
-        g1,gh [B,H,N], mu [H,d], tau [H] (numpy arrays or CPU/GPU torch tensors).
+        g1,gh [B,H,N], mu [H,d], tau [H] (numpy arrays or CPU/GPU torch tensors); g0 [B,H,N]
+        (optional) are the zero-order gate logits of a first layer.
 
         Returns ``out`` [B,H,N,d] float64, or ``(out, s, E, P)`` when ``debug`` is true
         (each [B,H,N]: the logit s_t and the prefix sums E_t, P_t at every step)."""
         q, k, v, u, g1, gh, mu, tau, (B, H, N, d) = _unpack(q, k, v, u, g1, gh, mu, tau)
+        g0 = _gate(g0, (B, H, N))
         out = np.zeros((B, H, N, d), np.float64)
         s = E = P = None
         if debug:
@@ -93,23 +103,24 @@ class Oracle:
         rc = self.lib.zs_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh),
                                     _ptr(mu), _ptr(tau), _ptr(out), B, H, N, d, int(causal),
                                     int(rope), float(rope_base), float(pos0), int(nthreads),
-                                    _ptr(s), _ptr(E), _ptr(P))
+                                    _ptr(s), _ptr(E), _ptr(P), _ptr(g0))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return (out, s, E, P) if debug else out
 
     def brute(self, q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False,
-              rope_base=10000.0, nthreads=0):
+              rope_base=10000.0, nthreads=0, g0=None):
         """O(N^2 d) fp64 evaluation of the definition.  Returns ``(out, wsum, wabsmax)`` with
         ``wsum[b,h,t] = sum_i w_{t,i}`` and ``wabsmax[b,h,t] = max_i |w_{t,i}|``."""
         q, k, v, u, g1, gh, mu, tau, (B, H, N, d) = _unpack(q, k, v, u, g1, gh, mu, tau)
+        g0 = _gate(g0, (B, H, N))
         out = np.zeros((B, H, N, d), np.float64)
         ws = np.zeros((B, H, N), np.float64)
         wm = np.zeros((B, H, N), np.float64)
         rc = self.lib.zs_oracle_brute(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh),
                                       _ptr(mu), _ptr(tau), _ptr(out), B, H, N, d, int(causal),
                                       int(rope), float(rope_base), int(nthreads), _ptr(ws),
-                                      _ptr(wm))
+                                      _ptr(wm), _ptr(g0))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return out, ws, wm

@@ -31,6 +31,10 @@
 //   * Encoder (non-causal) mode: every sum runs over all N tokens and t := N in delta, eps and
 //     the coefficients; the prior mean is the full-sequence mean for every token.  Gates stay
 //     per token.
+//   * Zero-order gate (optional, first layer; [PN] zero-order removal: "the first layer may keep
+//     the zero-order term"; [AI] "optionally sigma^0_t in the first layer"): the weight gains
+//     the zero-order term itself, w_{t,i} += sig^0_t / t with sig^0_t = sigmoid(g0_t), so the
+//     weights sum to sig^0_t; in the five-state form gamma_t gains sig^0_t / t.
 //
 // Parity pins for everything here live in tests/test_oracle_pins.py.
 
@@ -44,6 +48,7 @@ namespace {
 
 struct Problem {
   const double *q, *k, *v, *u, *g1, *gh, *mu, *tau;
+  const double* g0;  // nullable: zero-order gate logits [B,H,N]
   int B, H, N, d;
   int causal, rope;
   double rope_base;
@@ -142,6 +147,7 @@ void recurrent_one(const Problem& pr, int b, int h, double* out, double* dbg_s, 
     const double alpha = sigh / E;
     const double beta = (sig1 - sigh) / tcount;
     const double gamma = -(sig1 - sigh) * P / (tcount * tcount) - sigh / tcount;
+    const double zero_order = pr.g0 ? sigmoid(pr.g0[base + t_idx]) / tcount : 0.0;
     unit_vector(q + (size_t)t_idx * d, d, qh.data());
     if (pr.rope) rotate(qh.data(), d, pr.pos0 + t_idx, pr.rope_base);
     double* ot = o + (size_t)t_idx * d;
@@ -149,7 +155,7 @@ void recurrent_one(const Problem& pr, int b, int h, double* out, double* dbg_s, 
       double acc = 0.0;
       for (int a = 0; a < d; ++a) {
         const size_t e = (size_t)a * d + j;
-        acc += qh[a] * (alpha * F[e] + beta * G[e] + gamma * Hs[e]);
+        acc += qh[a] * (alpha * F[e] + beta * G[e] + (gamma + zero_order) * Hs[e]);
       }
       ot[j] = acc;
     }
@@ -173,6 +179,7 @@ void recurrent_one(const Problem& pr, int b, int h, double* out, double* dbg_s, 
 //   softmax_{t,i} = e^{s_i} / E_t, delta_{t,i} = s_i - P_t/t,
 //   eps_{t,i} = softmax_{t,i} - 1/t - delta_{t,i}/t,
 //   w_{t,i} = sig^1_t delta_{t,i}/t + sig^h_t eps_{t,i}          ([PN] zero-sum weights)
+//             (+ sig^0_t / t with the optional zero-order gate)
 //   c_{t,i} = q_hat_t R_{t-i} k_hat_i^T                            ([PN] radial-angular + RoPE)
 //   o_t = sum_i w_{t,i} c_{t,i} v_i.
 // Logits are recomputed from the definition of ubar_i with an explicit inner sum per i.
@@ -209,6 +216,7 @@ void brute_one(const Problem& pr, int b, int h, double* out, double* wsum, doubl
       P += s[i];
     }
     const double sig1 = sigmoid(pr.g1[base + t]), sigh = sigmoid(pr.gh[base + t]);
+    const double sig0 = pr.g0 ? sigmoid(pr.g0[base + t]) : 0.0;
     unit_vector(q + (size_t)t * d, d, qh.data());
     double* ot = out + (base + t) * d;
     for (int j = 0; j < d; ++j) ot[j] = 0.0;
@@ -217,7 +225,8 @@ void brute_one(const Problem& pr, int b, int h, double* out, double* wsum, doubl
       const double soft = std::exp(s[i]) / E;
       const double delta = s[i] - P / tc;
       const double eps = soft - 1.0 / tc - delta / tc;
-      const double w = sig1 * delta / tc + sigh * eps;
+      const double w_zs = sig1 * delta / tc + sigh * eps;
+      const double w = w_zs + sig0 / tc;  // zero-order term (0 unless the gate is given)
       unit_vector(k + (size_t)i * d, d, kh.data());
       std::copy(qh.begin(), qh.end(), qr.begin());
       if (pr.rope) rotate(qr.data(), d, (double)(t - i), pr.rope_base);
@@ -257,12 +266,14 @@ extern "C" {
 
 // Recurrent fp64 forward.  Layouts: q,k,v,u,out [B,H,N,d]; g1,gh [B,H,N]; mu [H,d]; tau [H].
 // dbg_s/dbg_E/dbg_P ([B,H,N], nullable) receive s_t, E_t and P_t (causal) or s_t, E_N, P_N
-// (encoder).  nthreads <= 0 uses every hardware thread.  Returns 0, or 1 on bad arguments.
+// (encoder).  g0 ([B,H,N], nullable) are the zero-order gate logits.  nthreads <= 0 uses every
+// hardware thread.  Returns 0, or 1 on bad arguments.
 int zs_oracle_fwd(const double* q, const double* k, const double* v, const double* u,
                   const double* g1, const double* gh, const double* mu, const double* tau,
                   double* out, int B, int H, int N, int d, int causal, int rope, double rope_base,
-                  double pos0, int nthreads, double* dbg_s, double* dbg_E, double* dbg_P) {
-  Problem pr{q, k, v, u, g1, gh, mu, tau, B, H, N, d, causal, rope, rope_base, pos0};
+                  double pos0, int nthreads, double* dbg_s, double* dbg_E, double* dbg_P,
+                  const double* g0) {
+  Problem pr{q, k, v, u, g1, gh, mu, tau, g0, B, H, N, d, causal, rope, rope_base, pos0};
   if (!valid(pr) || !out) return 1;
   parallel_over_heads(pr, nthreads,
                       [&](int b, int h) { recurrent_one(pr, b, h, out, dbg_s, dbg_E, dbg_P); });
@@ -270,12 +281,13 @@ int zs_oracle_fwd(const double* q, const double* k, const double* v, const doubl
 }
 
 // Brute-force O(N^2 d) fp64 forward of the definition.  wsum [B,H,N] receives sum_i w_{t,i}
-// and wabsmax [B,H,N] receives max_i |w_{t,i}| (both nullable).
+// and wabsmax [B,H,N] receives max_i |w_{t,i}| (both nullable); g0 as in zs_oracle_fwd.
 int zs_oracle_brute(const double* q, const double* k, const double* v, const double* u,
                     const double* g1, const double* gh, const double* mu, const double* tau,
                     double* out, int B, int H, int N, int d, int causal, int rope,
-                    double rope_base, int nthreads, double* wsum, double* wabsmax) {
-  Problem pr{q, k, v, u, g1, gh, mu, tau, B, H, N, d, causal, rope, rope_base, 0.0};
+                    double rope_base, int nthreads, double* wsum, double* wabsmax,
+                    const double* g0) {
+  Problem pr{q, k, v, u, g1, gh, mu, tau, g0, B, H, N, d, causal, rope, rope_base, 0.0};
   if (!valid(pr) || !out) return 1;
   parallel_over_heads(pr, nthreads,
                       [&](int b, int h) { brute_one(pr, b, h, out, wsum, wabsmax); });

@@ -252,7 +252,74 @@ def pin_prefix_sums(orc):
     assert np.allclose(P, np.cumsum(s, axis=-1), rtol=1e-13, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------------------------
+# Zero-order gate of a first layer (Paper-Notes, zero-order removal: "the first layer may keep
+# the zero-order term"; ai.info: "optionally sigma^0_t in the first layer"): w_{t,i} gains
+# sig^0_t / t.
+
+def _sig(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def _uniform_angular(p, b, h, t, last, rope, base, g0):
+    """sig^0_t/(last+1) * sum_{i<=last} cos(theta_{t,i}) v_i, with a textbook rotary map."""
+    qn = p["q"][b, h] / np.linalg.norm(p["q"][b, h], axis=-1, keepdims=True)
+    kn = p["k"][b, h] / np.linalg.norm(p["k"][b, h], axis=-1, keepdims=True)
+    if rope:
+        qn, kn = _rope_rows(qn, base), _rope_rows(kn, base)
+    c = qn[t] @ kn[: last + 1].T
+    return _sig(g0[b, h, t]) / (last + 1) * (c @ p["v"][b, h, : last + 1])
+
+
+def pin_zero_order_sum(orc):
+    """With the zero-order gate the weights sum to sig^0_t (not 0), and the five-state form
+    still equals the definition."""
+    p = rand_problem(21, N=64, d=8, H=2)
+    g0 = np.random.default_rng(22).standard_normal(p["g1"].shape) * 2.0
+    for causal in (True, False):
+        for rope in (False, True):
+            o = orc.forward(*_args(p), causal=causal, rope=rope, g0=g0)
+            ob, ws, _ = orc.brute(*_args(p), causal=causal, rope=rope, g0=g0)
+            assert np.abs(ws - _sig(g0)).max() < 1e-12
+            assert np.abs(o - ob).max() / max(np.abs(ob).max(), 1.0) < 1e-12
+
+
+def pin_zero_order_uniform(orc):
+    """sig^1 = sig^h = 0 (gate logits -1000): only the zero-order term is left, the uniform
+    average of the angular-weighted values: o_t = (sig^0_t / t) sum_{i<=t} cos(theta) v_i."""
+    p = rand_problem(23, N=30, d=8, H=2)
+    p["g1"][:] = -1000.0
+    p["gh"][:] = -1000.0
+    g0 = np.random.default_rng(24).standard_normal(p["g1"].shape)
+    base = 300.0
+    for causal in (True, False):
+        for rope in (False, True):
+            o = orc.forward(*_args(p), causal=causal, rope=rope, rope_base=base, g0=g0)
+            N = o.shape[2]
+            for b in range(o.shape[0]):
+                for h in range(o.shape[1]):
+                    for t in range(N):
+                        last = t if causal else N - 1
+                        ref = _uniform_angular(p, b, h, t, last, rope, base, g0)
+                        assert np.allclose(o[b, h, t], ref, rtol=0, atol=1e-13)
+
+
+def pin_zero_order_linearity(orc):
+    """The zero-order term adds (sig^0_t / t) sum_{i<=t} cos(theta) v_i to the zero-sum output."""
+    p = rand_problem(25, N=24, d=8, H=1)
+    g0 = np.random.default_rng(26).standard_normal(p["g1"].shape)
+    for causal in (True, False):
+        o0 = orc.forward(*_args(p), causal=causal, rope=True)
+        o1 = orc.forward(*_args(p), causal=causal, rope=True, g0=g0)
+        N = o0.shape[2]
+        for t in range(N):
+            last = t if causal else N - 1
+            ref = _uniform_angular(p, 0, 0, t, last, True, 10000.0, g0)
+            assert np.allclose(o1[0, 0, t] - o0[0, 0, t], ref, rtol=0, atol=1e-13)
+
+
 ALL_PINS = [pin_golden_two_token, pin_brute_vs_recurrent, pin_zero_sum, pin_first_output_zero,
             pin_lemma_3_4, pin_two_token_collinear, pin_constant_logits, pin_equal_gates_softmax,
             pin_equal_gates_softmax_rope, pin_linear_gate_limit, pin_rope_relative, pin_scale_and_linearity, pin_prior_limits,
-            pin_prefix_sums]
+            pin_prefix_sums,
+            pin_zero_order_sum, pin_zero_order_uniform, pin_zero_order_linearity]

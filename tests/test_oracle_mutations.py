@@ -37,6 +37,10 @@ MUTATIONS = [
      "const double delta = P / tc - s[i];"),
     ("encoder prior uses N+1", "ubar[a] = (et * mu[a] + S[a]) / (et + N);",
      "ubar[a] = (et * mu[a] + S[a]) / (et + N + 1);"),
+    ("zero-order term dropped", "(gamma + zero_order) * Hs[e]", "gamma * Hs[e]"),
+    ("zero-order over t+1", "sigmoid(pr.g0[base + t_idx]) / tcount",
+     "sigmoid(pr.g0[base + t_idx]) / (tcount + 1)"),
+    ("brute zero-order dropped", "const double w = w_zs + sig0 / tc;", "const double w = w_zs;"),
 ]
 
 
