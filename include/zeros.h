@@ -76,6 +76,11 @@ int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const 
 
 /*
  * zeros_fwd with every option.
+ *   g0          : nullable fp32 [B, H, N]: zero-order gate logits of a first layer (Paper-Notes
+ *                 "ZeroS", zero-order removal: the first layer may keep the zero-order term).
+ *                 Every weight gains sigmoid(g0_t) / t (encoder: / N), so the weights of
+ *                 query t sum to sigmoid(g0_t) instead of 0.  NULL: no zero-order term (the
+ *                 pages' default).
  *   dtype       : ZEROS_BF16 or ZEROS_F32 for q, k, v, u and out.
  *   rope_base   : rotary base (> 0) when rope = 1.
  *   path        : a zeros_path value.
@@ -88,7 +93,8 @@ int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const 
  *                 bit-identical to those zeros_decode_step_ex reports for the same tokens.
  */
 int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
-                 const float* gh, const float* mu, const float* tau, void* out, int B, int H,
+                 const float* gh, const float* g0, const float* mu, const float* tau, void* out,
+                 int B, int H,
                  int N, int d, int causal, int rope, int dtype, float rope_base, int path,
                  void* final_state, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
                  void* stream);
@@ -146,10 +152,12 @@ int zeros_state_init(void* state, const float* mu, const float* tau, int B, int 
 int zeros_decode_step(void* state, const void* q, const void* k, const void* v, const void* u,
                       const float* g1, const float* gh, void* out, void* stream);
 
-/* As zeros_decode_step with explicit dimensions (no header lookup) and per-token debug
- * outputs dbg_s, dbg_E, dbg_P, dbg_m (nullable fp32 [B, H]) as in zeros_fwd_ex. */
+/* As zeros_decode_step with explicit dimensions (no header lookup), the zero-order gate g0
+ * (nullable fp32 [B, H], as in zeros_fwd_ex) and per-token debug outputs dbg_s, dbg_E, dbg_P,
+ * dbg_m (nullable fp32 [B, H]) as in zeros_fwd_ex. */
 int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const void* k,
                          const void* v, const void* u, const float* g1, const float* gh,
+                         const float* g0,
                          void* out, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
                          void* stream);
 

@@ -48,9 +48,11 @@ def test_state_sizes(lib):
     assert lib.zeros_state_record_bytes(16) == 0
 
 
-def _fwd(lib, ptr=16, B=1, H=1, N=8, d=64, causal=1, rope=0, dtype=0, base=1e4, path=0):
+def _fwd(lib, ptr=16, B=1, H=1, N=8, d=64, causal=1, rope=0, dtype=0, base=1e4, path=0,
+         g0=None):
     p = ctypes.c_void_p(ptr) if ptr is not None else None
-    return lib.zeros_fwd_ex(p, p, p, p, p, p, p, p, p, B, H, N, d, causal, rope, dtype, base,
+    g = ctypes.c_void_p(g0) if g0 is not None else None
+    return lib.zeros_fwd_ex(p, p, p, p, p, p, g, p, p, p, B, H, N, d, causal, rope, dtype, base,
                             path, None, None, None, None, None, None)
 
 
@@ -65,15 +67,16 @@ def test_host_validation_without_gpu(lib):
     assert _fwd(lib, causal=2) == zs.ZEROS_ERR_INVALID
     assert _fwd(lib, rope=1, base=0.0) == zs.ZEROS_ERR_INVALID
     assert _fwd(lib, path=9) == zs.ZEROS_ERR_INVALID
+    assert _fwd(lib, g0=20) == zs.ZEROS_ERR_INVALID  # optional zero-order gate misaligned
     assert _fwd(lib, N=1 << 24) == zs.ZEROS_ERR_UNSUPPORTED
     # empty problems are valid no-ops and touch nothing
     assert _fwd(lib, ptr=None, B=0) == zs.ZEROS_OK
     assert _fwd(lib, ptr=None, N=0, H=3) == zs.ZEROS_OK
     # a final state is a causal-mode concept
     p = ctypes.c_void_p(16)
-    assert lib.zeros_fwd_ex(p, p, p, p, p, p, p, p, p, 1, 1, 4, 64, 0, 0, 0, 1e4, 0, p, None,
-                            None, None, None, None) == zs.ZEROS_ERR_INVALID
+    assert lib.zeros_fwd_ex(p, p, p, p, p, p, None, p, p, p, 1, 1, 4, 64, 0, 0, 0, 1e4, 0, p,
+                            None, None, None, None, None) == zs.ZEROS_ERR_INVALID
     # decode on a state this process never created is rejected by the explicit-shape entry
-    assert lib.zeros_decode_step_ex(p, 1, 1, 64, *([p] * 7), None, None, None, None,
+    assert lib.zeros_decode_step_ex(p, 1, 1, 64, *([p] * 6), None, p, None, None, None, None,
                                     None) == zs.ZEROS_ERR_INVALID
     assert lib.zeros_state_init(None, p, p, 1, 1, 64, 0, 0, 1e4, None) == zs.ZEROS_ERR_INVALID

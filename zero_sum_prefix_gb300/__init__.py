@@ -56,7 +56,7 @@ def load():
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.zeros_fwd.argtypes = [vp] * 9 + [i] * 6 + [vp]
         lib.zeros_fwd.restype = i
-        lib.zeros_fwd_ex.argtypes = [vp] * 9 + [i] * 7 + [f, i, vp, vp, vp, vp, vp, vp]
+        lib.zeros_fwd_ex.argtypes = [vp] * 10 + [i] * 7 + [f, i, vp, vp, vp, vp, vp, vp]
         lib.zeros_fwd_ex.restype = i
         lib.zeros_state_bytes.argtypes = [i, i, i]
         lib.zeros_state_bytes.restype = sz
@@ -66,7 +66,7 @@ def load():
         lib.zeros_state_init.restype = i
         lib.zeros_decode_step.argtypes = [vp] * 9
         lib.zeros_decode_step.restype = i
-        lib.zeros_decode_step_ex.argtypes = [vp, i, i, i] + [vp] * 12
+        lib.zeros_decode_step_ex.argtypes = [vp, i, i, i] + [vp] * 13
         lib.zeros_decode_step_ex.restype = i
         lib.zeros_get_status.argtypes = [vp]
         lib.zeros_get_status.restype = i
@@ -125,16 +125,19 @@ def _need(t, name, shape, dtype=None):
 
 
 def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000.0, out=None,
-        final_state=None, debug=False, path="auto", stream=None):
+        final_state=None, debug=False, path="auto", stream=None, g0=None):
     """ZeroS forward.  q, k, v, u: [B, H, N, d] bf16 or fp32 (same dtype); g1, gh: [B, H, N]
-    fp32 gate logits; mu: [H, d] fp32; tau: [H] fp32.  Returns ``out`` (same dtype as q), or
-    ``(out, dbg)`` with ``dbg = dict(s, E, P, m)`` ([B, H, N] fp32) when ``debug``."""
+    fp32 gate logits; mu: [H, d] fp32; tau: [H] fp32; g0: optional [B, H, N] fp32 zero-order
+    gate logits of a first layer.  Returns ``out`` (same dtype as q), or ``(out, dbg)`` with
+    ``dbg = dict(s, E, P, m)`` ([B, H, N] fp32) when ``debug``."""
     B, H, N, d = q.shape
     dt = q.dtype
     for name, t in (("q", q), ("k", k), ("v", v), ("u", u)):
         _need(t, name, (B, H, N, d), dt)
     _need(g1, "g1", (B, H, N), torch.float32)
     _need(gh, "gh", (B, H, N), torch.float32)
+    if g0 is not None:
+        _need(g0, "g0", (B, H, N), torch.float32)
     _need(mu, "mu", (H, d), torch.float32)
     _need(tau, "tau", (H,), torch.float32)
     if out is None:
@@ -147,8 +150,9 @@ def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000
         dbg = {n: torch.empty((B, H, N), device=q.device, dtype=torch.float32)
                for n in ("s", "E", "P", "m")}
     lib = load()
-    rc = lib.zeros_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(mu),
-                          _ptr(tau), _ptr(out), B, H, N, d, int(bool(causal)), int(bool(rope)),
+    rc = lib.zeros_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(g0),
+                          _ptr(mu), _ptr(tau), _ptr(out), B, H, N, d, int(bool(causal)),
+                          int(bool(rope)),
                           _dtype_code(q), float(rope_base), PATHS[path], _ptr(final_state),
                           *(None if dbg is None else _ptr(dbg[n]) for n in ("s", "E", "P", "m")),
                           _stream(stream))
@@ -181,27 +185,33 @@ def new_state(mu, tau, B: int, *, dtype=torch.bfloat16, rope=False, rope_base=10
     return st
 
 
-def decode_step(state, q, k, v, u, g1, gh, *, out=None, debug=False, stream=None):
-    """One recurrent step for every sequence: q, k, v, u [B, H, d]; g1, gh [B, H]."""
+def decode_step(state, q, k, v, u, g1, gh, *, out=None, debug=False, stream=None, g0=None):
+    """One recurrent step for every sequence: q, k, v, u [B, H, d]; g1, gh [B, H]; g0
+    optional [B, H] zero-order gate logits."""
     B, H, d = q.shape
     dt = q.dtype
     for name, t in (("q", q), ("k", k), ("v", v), ("u", u)):
         _need(t, name, (B, H, d), dt)
     _need(g1, "g1", (B, H), torch.float32)
     _need(gh, "gh", (B, H), torch.float32)
+    if g0 is not None:
+        _need(g0, "g0", (B, H), torch.float32)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", (B, H, d), dt)
     lib = load()
-    if debug:
-        dbg = {n: torch.empty((B, H), device=q.device, dtype=torch.float32)
-               for n in ("s", "E", "P", "m")}
+    if debug or g0 is not None:
+        dbg = None
+        if debug:
+            dbg = {n: torch.empty((B, H), device=q.device, dtype=torch.float32)
+                   for n in ("s", "E", "P", "m")}
         rc = lib.zeros_decode_step_ex(_ptr(state), B, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(u),
-                                      _ptr(g1), _ptr(gh), _ptr(out),
-                                      *(_ptr(dbg[n]) for n in ("s", "E", "P", "m")),
+                                      _ptr(g1), _ptr(gh), _ptr(g0), _ptr(out),
+                                      *(None if dbg is None else _ptr(dbg[n])
+                                        for n in ("s", "E", "P", "m")),
                                       _stream(stream))
         _check(rc, "zeros_decode_step_ex")
-        return out, dbg
+        return (out, dbg) if debug else out
     rc = lib.zeros_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1),
                                _ptr(gh), _ptr(out), _stream(stream))
     _check(rc, "zeros_decode_step")

@@ -170,8 +170,9 @@ size_t zeros_state_bytes(int B, int H, int d) {
 }
 
 int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
-                 const float* gh, const float* mu, const float* tau, void* out, int B, int H,
-                 int N, int d, int causal, int rope, int dtype, float rope_base, int path,
+                 const float* gh, const float* g0, const float* mu, const float* tau, void* out,
+                 int B, int H, int N, int d, int causal, int rope, int dtype, float rope_base,
+                 int path,
                  void* final_state, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
                  void* stream) {
   g_last_error.clear();
@@ -191,6 +192,7 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
     for (int i = 0; i < 9; ++i)
       if (int rc = check_ptr(ptrs[i], names[i])) return rc;
   if (int rc = check_opt_ptr(final_state, "final_state")) return rc;
+  if (int rc = check_opt_ptr(g0, "g0")) return rc;
   if (int rc = check_opt_ptr(dbg_s, "dbg_s")) return rc;
   if (int rc = check_opt_ptr(dbg_E, "dbg_E")) return rc;
   if (int rc = check_opt_ptr(dbg_P, "dbg_P")) return rc;
@@ -222,6 +224,7 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
   a.u = u;
   a.g1 = g1;
   a.gh = gh;
+  a.g0 = g0;
   a.mu = mu;
   a.tau = tau;
   a.out = out;
@@ -250,7 +253,8 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
 int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
               const float* gh, const float* mu, const float* tau, void* out, int B, int H, int N,
               int d, int causal, int rope, void* stream) {
-  return zeros_fwd_ex(q, k, v, u, g1, gh, mu, tau, out, B, H, N, d, causal, rope, ZEROS_BF16,
+  return zeros_fwd_ex(q, k, v, u, g1, gh, nullptr, mu, tau, out, B, H, N, d, causal, rope,
+                      ZEROS_BF16,
                       10000.0f, ZEROS_PATH_AUTO, nullptr, nullptr, nullptr, nullptr, nullptr,
                       stream);
 }
@@ -337,8 +341,9 @@ int zeros_state_init(void* state, const float* mu, const float* tau, int B, int 
 }
 
 static int decode_impl(void* state, const StateInfo& si, const void* q, const void* k,
-                       const void* v, const void* u, const float* g1, const float* gh, void* out,
-                       float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m, void* stream) {
+                       const void* v, const void* u, const float* g1, const float* gh,
+                       const float* g0, void* out, float* dbg_s, float* dbg_E, float* dbg_P,
+                       float* dbg_m, void* stream) {
   if (int rc = check_dims(si.B, si.H, 1, si.d)) return rc;
   if (int rc = check_ptr(state, "state")) return rc;
   if ((long long)si.B * si.H == 0) return ZEROS_OK;
@@ -346,6 +351,7 @@ static int decode_impl(void* state, const StateInfo& si, const void* q, const vo
   const void* ptrs[] = {q, k, v, u, g1, gh, out};
   for (int i = 0; i < 7; ++i)
     if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (int rc = check_opt_ptr(g0, "g0")) return rc;
   if (int rc = check_opt_ptr(dbg_s, "dbg_s")) return rc;
   if (int rc = check_opt_ptr(dbg_E, "dbg_E")) return rc;
   if (int rc = check_opt_ptr(dbg_P, "dbg_P")) return rc;
@@ -360,6 +366,7 @@ static int decode_impl(void* state, const StateInfo& si, const void* q, const vo
   a.u = u;
   a.g1 = g1;
   a.gh = gh;
+  a.g0 = g0;
   a.out = out;
   a.B = si.B;
   a.H = si.H;
@@ -401,14 +408,14 @@ int zeros_decode_step(void* state, const void* q, const void* k, const void* v, 
     std::lock_guard<std::mutex> lk(g_mutex);
     g_states[state] = si;
   }
-  return decode_impl(state, si, q, k, v, u, g1, gh, out, nullptr, nullptr, nullptr, nullptr,
-                     stream);
+  return decode_impl(state, si, q, k, v, u, g1, gh, nullptr, out, nullptr, nullptr, nullptr,
+                     nullptr, stream);
 }
 
 int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const void* k,
                          const void* v, const void* u, const float* g1, const float* gh,
-                         void* out, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
-                         void* stream) {
+                         const float* g0, void* out, float* dbg_s, float* dbg_E, float* dbg_P,
+                         float* dbg_m, void* stream) {
   g_last_error.clear();
   StateInfo si{B, H, d, ZEROS_BF16, 0, 10000.0f};
   {
@@ -424,7 +431,8 @@ int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const 
                   "zeros_fwd_ex, or call zeros_decode_step once");
     }
   }
-  return decode_impl(state, si, q, k, v, u, g1, gh, out, dbg_s, dbg_E, dbg_P, dbg_m, stream);
+  return decode_impl(state, si, q, k, v, u, g1, gh, g0, out, dbg_s, dbg_E, dbg_P, dbg_m,
+                     stream);
 }
 
 int zeros_get_status(void* stream) {

@@ -701,17 +701,20 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
       phi[slot * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
     }
   };
-  // gate logits of chunk cc (loaded one chunk ahead so that their latency is hidden)
-  auto load_gates = [&](int cc, float& x1, float& xh) {
+  // gate logits of chunk cc (loaded one chunk ahead so that their latency is hidden); x0 is the
+  // optional zero-order gate (-inf when absent, so that its sigmoid is 0)
+  auto load_gates = [&](int cc, float& x1, float& xh, float& x0) {
     x1 = 0.0f;
     xh = 0.0f;
+    x0 = -INFINITY;
     if (cc < nch && cc * kC + r < N) {
       x1 = __ldg(a.g1 + row0 + cc * kC + r);
       xh = __ldg(a.gh + row0 + cc * kC + r);
+      if (a.g0) x0 = __ldg(a.g0 + row0 + cc * kC + r);
     }
   };
-  float g1, gh;
-  load_gates(rank, g1, gh);
+  float g1, gh, g0;
+  load_gates(rank, g1, gh, g0);
   put_phi(rank, 0);
 
   for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
@@ -731,8 +734,8 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
     uint8_t* qt = smem + CF::Q_OFF + st * CF::KA * kTile;
     uint8_t* kt = smem + CF::K_OFF + st * CF::KA * kTile;
     uint8_t* vt = smem + CF::V_OFF + (c % CF::NSV) * 2 * kTile;
-    float g1n, ghn;
-    load_gates(c + CL, g1n, ghn);
+    float g1n, ghn, g0n;
+    load_gates(c + CL, g1n, ghn, g0n);
     float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
     {
       // ---- rotate q, k in place (TMA tiles), norms ----
@@ -782,6 +785,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
         cf.x = rho * ahat;
         cf.y = rho * b0c;
         cf.z = -rho * (b0c * P * rt + sigh * rt);
+        if (a.g0) cf.z += rho * __fdividef(1.0f, 1.0f + __expf(-g0)) * rt;  // zero-order term
         if (!isfinite(cf.x) || !isfinite(ce)) report(a.status, kErrRange);
       }
       xc->coef[r] = cf;
@@ -860,6 +864,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
     if (c + CL < nch) put_phi(c + CL, (kk + 1) & 1);
     g1 = g1n;
     gh = ghn;
+    g0 = g0n;
   }
 }
 

@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
       coef[3] = __fdiv_rn(sigh, o.Et);
       coef[4] = beta;
       coef[5] = -__fadd_rn(__fmul_rn(__fmul_rn(beta, o.P), rt), __fmul_rn(sigh, rt));
+      // optional zero-order term of a first layer: every weight gains sig0 / t
+      if (a.g0) coef[5] = __fadd_rn(coef[5], __fmul_rn(sigmoid(a.g0[bh]), rt));
       if (a.dbg_s) a.dbg_s[bh] = s;
       if (a.dbg_E) a.dbg_E[bh] = o.Et;
       if (a.dbg_P) a.dbg_P[bh] = o.P;

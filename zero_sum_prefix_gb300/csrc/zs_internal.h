@@ -11,6 +11,7 @@ namespace zs {
 struct FwdArgs {
   const void *q, *k, *v, *u;
   const float *g1, *gh, *mu, *tau;
+  const float* g0;  // nullable: zero-order gate logits [B,H,N]
   void* out;
   int B, H, N, d;
   int causal, rope, dtype;
@@ -25,6 +26,7 @@ struct DecodeArgs {
   void* state;
   const void *q, *k, *v, *u;
   const float *g1, *gh;
+  const float* g0;  // nullable: zero-order gate logits [B,H]
   void* out;
   int B, H, d, dtype, rope;
   float rope_base;

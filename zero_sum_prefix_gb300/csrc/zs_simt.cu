@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
           tc.alpha = __fdiv_rn(sigh, Et);
           tc.beta = beta;
           tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, P), rt), __fmul_rn(sigh, rt));
+          // optional zero-order term of a first layer: every weight gains sig0 / t
+          if (a.g0) tc.gamma = __fadd_rn(tc.gamma, __fmul_rn(sigmoid(a.g0[row0 + t]), rt));
           if (blockIdx.y == 0) {
             if (a.dbg_s) a.dbg_s[row0 + t] = s;
             if (a.dbg_E) a.dbg_E[row0 + t] = Et;
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
       tc.alpha = __fdiv_rn(sigh, fullsc[0]);
       tc.beta = beta;
       tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, fullsc[1]), rN), __fmul_rn(sigh, rN));
+      if (a.g0) tc.gamma = __fadd_rn(tc.gamma, __fmul_rn(sigmoid(a.g0[row0 + t]), rN));
       if (blockIdx.y == 0) {
         if (a.dbg_E) a.dbg_E[row0 + t] = fullsc[0];
         if (a.dbg_P) a.dbg_P[row0 + t] = fullsc[1];
