@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload causal|encoder|long|decode] [--path auto|simt|chunk]
+                    [--pass fwd|bwd]
 
 One step = one pass of the whole hot path (logits, prefix scans, zero-sum weights, angular
 factor, state scan and readout: one zeros_fwd call) over one batch of device-resident
@@ -71,6 +72,13 @@ def decode_bytes(w: zi.Workload) -> int:
     b = 2 if w.dtype == "bf16" else 4
     per = 2 * (12 * w.d * w.d + 4 * w.d + 16) + 4 * w.d * b + 8 + w.d * b
     return w.B * w.H * per
+
+
+def backward_bytes(w: zi.Workload) -> int:
+    """Bytes the backward must move: read q, k, v, u, dout and the two gate logits, write the
+    fp32 gradients dq, dk, dv, du, dg1, dgh (per token-head 5 d b_in + 8 + 16 d + 8)."""
+    b = 2 if w.dtype == "bf16" else 4
+    return w.B * w.H * w.N * (5 * w.d * b + 8 + 16 * w.d + 8)
 
 
 def peaks():
@@ -357,6 +365,125 @@ def ours_forward(args, w: zi.Workload):
         print(json.dumps(line))
 
 
+def ours_backward(args, w: zi.Workload):
+    """Backward of the causal layer (zeros_bwd): one step = the gradients of sum(out * dout)
+    with respect to every input, for the whole batch."""
+    if not w.causal:
+        raise SystemExit("the backward pass is defined for the causal workloads")
+    world, rank, local = dist_setup()
+    import zero_sum_prefix_gb300 as zs
+    zs.load()
+    dev = torch.device("cuda", local)
+    inp = zi.make(w, dev)
+    gen = torch.Generator(device="cpu").manual_seed(w.seed * 7 + 3)
+    dout = torch.randn(inp["q"].shape, generator=gen).to(dev, inp["q"].dtype)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    names = ("q", "k", "v", "u", "g1", "gh", "mu", "tau")
+
+    def step(src, do):
+        return zs.bwd(*(src[n] for n in names), do, rope=w.rope, rope_base=w.rope_base)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step(inp, dout)
+    torch.cuda.synchronize()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    l0 = zs.kernel_launches()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step(inp, dout)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = zs.kernel_launches() - l0
+    barrier(world)
+    clk = clocks.stop()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    tokens = w.B * w.N
+    value, ms = aggregate_rate(tokens, sum(per) / len(per), world)
+    hbm, kind = peaks()
+    alg = backward_bytes(w)
+
+    # end to end with host buffers: inputs and dout in, every gradient out
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    host_do = dout.cpu().pin_memory()
+    dev_in = {n: torch.empty_like(inp[n]) for n in names}
+    dev_do = torch.empty_like(dout)
+    grads = step(inp, dout)
+    host_g = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in grads.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_do.numel() * host_do.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_g.values())
+
+    def e2e_step():
+        for n in names:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        dev_do.copy_(host_do, non_blocking=True)
+        g = step(dev_in, dev_do)
+        for n, t in g.items():
+            host_g[n].copy_(t, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import grad as ograd
+        toks = min(w.N, 1024)
+        c = {n: inp[n].cpu() for n in names}
+        sl = lambda t: t[:1, :, :toks]  # noqa: E731
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            ograd.backward(sl(c["q"]), sl(c["k"]), sl(c["v"]), sl(c["u"]), sl(c["g1"]),
+                           sl(c["gh"]), c["mu"], c["tau"], sl(dout.cpu()), rope=w.rope,
+                           rope_base=w.rope_base)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 1.5 or reps >= 20:
+                break
+        cpu = {"value": toks * reps / (dt), "unit": "tokens/s", "cores": torch.get_num_threads(),
+               "kind": "oracle",
+               "sample": f"batch 1 (all {w.H} heads) x first {toks} tokens, fp64 autograd of "
+                         f"the O(N^2) definition, {reps} passes ({dt:.1f} s wall)"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": f"ZeroS backward tokens/s ({w.name})", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "rope": w.rope, "pass": "backward",
+                       "l2": "flushed before every step (256 MB write, outside the events)"},
+            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": alg / (ms / 1e3) / 1e9 / hbm, "traffic": None,
+                         "peak_source": kind, "algorithmic_bytes_per_launch": alg},
+            "cpu_baseline": cpu,
+            "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clk}))
+
+
 def ours_decode(args, w: zi.Workload):
     """Recurrent decode: prefill 8192 tokens (zeros_fwd_ex final_state), then time decode
     steps; one step advances all B x H sequences by one token."""
@@ -440,11 +567,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "chunk"])
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, w)
+    elif args.pass_ == "bwd":
+        ours_backward(args, w)
     elif args.workload == "decode":
         ours_decode(args, w)
     else:

@@ -123,6 +123,26 @@ int zeros_fwd_noalloc(const void* q, const void* k, const void* v, const void* u
                       float rope_base, int* status, void* stream);
 
 /*
+ * Backward pass of the causal forward (training): gradients of L = sum(out * dout) with respect
+ * to every input.  Differentiates the pages' five-state scan (Paper-Notes "ZeroS", method
+ * details: deviation logits, zero-sum weights, radial-angular decoupling, linear-time prefix
+ * scan); the pages give no backward, this is the derivative of that definition.
+ *   q, k, v, u, dout          : [B, H, N, d] in `dtype` (ZEROS_BF16 or ZEROS_F32)
+ *   g1, gh, mu, tau, g0       : as in zeros_fwd_ex (g0 nullable)
+ *   dq, dk, dv, du            : [B, H, N, d] fp32, written
+ *   dg1, dgh                  : [B, H, N] fp32, written;  dg0: nullable, needs g0
+ *   dmu [H, d], dtau [H]      : fp32, overwritten with the sums over the batch
+ * Causal mode only.  The library keeps a per-device scratch of B*H*N*(8+d)*4 bytes for the
+ * pass (grown on demand; growing it waits for the device).  Gradients are reduced in fp32;
+ * dmu and dtau are summed over the batch with atomic adds (order not fixed).
+ */
+int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
+              const float* gh, const float* g0, const float* mu, const float* tau,
+              const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
+              float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
+              int rope, int dtype, float rope_base, void* stream);
+
+/*
  * Recurrent state ("the state is the checkpoint").  Size in bytes of the blob for B x H
  * sequences of head dimension d (0 for unsupported d).  Layout: a 256-byte header
  * {magic "ZSP1", version, B, H, d, dtype, rope, rope_base} followed by B*H records of

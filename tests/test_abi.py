@@ -80,3 +80,15 @@ def test_host_validation_without_gpu(lib):
     assert lib.zeros_decode_step_ex(p, 1, 1, 64, *([p] * 6), None, p, None, None, None, None,
                                     None) == zs.ZEROS_ERR_INVALID
     assert lib.zeros_state_init(None, p, p, 1, 1, 64, 0, 0, 1e4, None) == zs.ZEROS_ERR_INVALID
+    # backward: rejected arguments never reach the GPU
+    def bwd(ptr=16, d=64, g0=None, dg0=None, rope=0, base=1e4):
+        x = ctypes.c_void_p(ptr) if ptr is not None else None
+        g = ctypes.c_void_p(g0) if g0 is not None else None
+        dg = ctypes.c_void_p(dg0) if dg0 is not None else None
+        return lib.zeros_bwd(x, x, x, x, x, x, g, x, x, x, x, x, x, x, x, x, dg, x, x,
+                             1, 1, 8, d, rope, 0, base, None)
+    assert bwd(d=48) == zs.ZEROS_ERR_UNSUPPORTED
+    assert bwd(ptr=None) == zs.ZEROS_ERR_INVALID
+    assert bwd(ptr=24) == zs.ZEROS_ERR_INVALID
+    assert bwd(dg0=16) == zs.ZEROS_ERR_INVALID       # dg0 without the gate
+    assert bwd(rope=1, base=-1.0) == zs.ZEROS_ERR_INVALID

@@ -28,7 +28,7 @@ PATHS = {"auto": 0, "simt": 1, "chunk": 2}
 EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record_bytes",
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
-           "zeros_kernel_launches", "zeros_fwd_noalloc"]
+           "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd"]
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,8 @@ def load():
         lib.zeros_version.restype = i
         lib.zeros_kernel_launches.restype = ctypes.c_ulonglong
         lib.zeros_fwd_noalloc.argtypes = [vp] * 9 + [i] * 7 + [f, vp, vp]
+        lib.zeros_bwd.argtypes = [vp] * 19 + [i] * 6 + [f, vp]
+        lib.zeros_bwd.restype = i
         lib.zeros_fwd_noalloc.restype = i
         _lib = lib
         return lib
@@ -158,6 +160,39 @@ def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000
                           _stream(stream))
     _check(rc, "zeros_fwd_ex")
     return (out, dbg) if debug else out
+
+
+def bwd(q, k, v, u, g1, gh, mu, tau, dout, *, rope=False, rope_base=10000.0, g0=None,
+        stream=None):
+    """Backward of the causal forward: gradients of sum(out * dout).  Inputs as in ``fwd``
+    (causal mode); ``dout`` has the shape and dtype of q.  Returns a dict of fp32 tensors
+    dq, dk, dv, du [B, H, N, d], dg1, dgh [B, H, N], dmu [H, d], dtau [H] (and dg0 when
+    ``g0`` is given)."""
+    B, H, N, d = q.shape
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("u", u), ("dout", dout)):
+        _need(t, name, (B, H, N, d), dt)
+    _need(g1, "g1", (B, H, N), torch.float32)
+    _need(gh, "gh", (B, H, N), torch.float32)
+    if g0 is not None:
+        _need(g0, "g0", (B, H, N), torch.float32)
+    _need(mu, "mu", (H, d), torch.float32)
+    _need(tau, "tau", (H,), torch.float32)
+    f32 = dict(device=q.device, dtype=torch.float32)
+    g = {n: torch.empty((B, H, N, d), **f32) for n in ("dq", "dk", "dv", "du")}
+    g["dg1"] = torch.empty((B, H, N), **f32)
+    g["dgh"] = torch.empty((B, H, N), **f32)
+    g["dmu"] = torch.empty((H, d), **f32)
+    g["dtau"] = torch.empty((H,), **f32)
+    if g0 is not None:
+        g["dg0"] = torch.empty((B, H, N), **f32)
+    rc = load().zeros_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(g0),
+                          _ptr(mu), _ptr(tau), _ptr(dout), _ptr(g["dq"]), _ptr(g["dk"]),
+                          _ptr(g["dv"]), _ptr(g["du"]), _ptr(g["dg1"]), _ptr(g["dgh"]),
+                          _ptr(g.get("dg0")), _ptr(g["dmu"]), _ptr(g["dtau"]), B, H, N, d,
+                          int(bool(rope)), _dtype_code(q), float(rope_base), _stream(stream))
+    _check(rc, "zeros_bwd")
+    return g
 
 
 def state_bytes(B: int, H: int, d: int) -> int:

@@ -30,6 +30,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 struct DeviceWorkspace {
   int* status = nullptr;
+  float* bwd = nullptr;  // backward scratch (per-token scalars and prior means)
+  size_t bwd_bytes = 0;
   float2* rope = nullptr;
   size_t rope_entries = 0;  // capacity in float2
   int rope_N = 0, rope_d = 0;
@@ -96,6 +98,26 @@ int rope_table(DeviceWorkspace* ws, int N, int d, float base, cudaStream_t strea
   ws->rope_d = d;
   ws->rope_base = base;
   *table = ws->rope;
+  return ZEROS_OK;
+}
+
+// Backward scratch of at least `bytes`, grown on demand (after the device has drained: queued
+// work may still use the old buffer).
+int bwd_scratch(DeviceWorkspace* ws, size_t bytes, float** out) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (bytes > ws->bwd_bytes) {
+    if (ws->bwd) {
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+      cudaFree(ws->bwd);
+    }
+    ws->bwd = nullptr;
+    ws->bwd_bytes = 0;
+    cudaError_t e = cudaMalloc(&ws->bwd, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(backward scratch)");
+    ws->bwd_bytes = bytes;
+  }
+  *out = ws->bwd;
   return ZEROS_OK;
 }
 
@@ -433,6 +455,77 @@ int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const 
   }
   return decode_impl(state, si, q, k, v, u, g1, gh, g0, out, dbg_s, dbg_E, dbg_P, dbg_m,
                      stream);
+}
+
+int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
+              const float* gh, const float* g0, const float* mu, const float* tau,
+              const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
+              float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
+              int rope, int dtype, float rope_base, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_dims(B, H, N, d)) return rc;
+  if (int rc = check_dtype(dtype)) return rc;
+  if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
+  if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
+  if (dg0 && !g0) return fail(ZEROS_ERR_INVALID, "dg0 needs the zero-order gate g0");
+  const char* names[] = {"q", "k", "v", "u", "g1", "gh", "dout", "dq", "dk", "dv", "du",
+                         "dg1", "dgh"};
+  const void* ptrs[] = {q, k, v, u, g1, gh, dout, dq, dk, dv, du, dg1, dgh};
+  const bool empty = (long long)B * H * N == 0;
+  if (!empty)
+    for (int i = 0; i < 13; ++i)
+      if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (H > 0) {
+    const char* n2[] = {"mu", "tau", "dmu", "dtau"};
+    const void* p2[] = {mu, tau, dmu, dtau};
+    for (int i = 0; i < 4; ++i)
+      if (int rc = check_ptr(p2[i], n2[i])) return rc;
+  }
+  if (int rc = check_opt_ptr(g0, "g0")) return rc;
+  if (int rc = check_opt_ptr(dg0, "dg0")) return rc;
+  if (H == 0) return ZEROS_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // mu and tau gradients are sums over the batch: start from zero
+  cudaError_t e = cudaMemsetAsync(dmu, 0, (size_t)H * d * sizeof(float), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dtau, 0, (size_t)H * sizeof(float), st);
+  if (e != cudaSuccess) return cuda_fail(e, "zeroing dmu / dtau");
+  if (empty) return ZEROS_OK;
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+  BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.u = u;
+  a.dout = dout;
+  a.g1 = g1;
+  a.gh = gh;
+  a.g0 = g0;
+  a.mu = mu;
+  a.tau = tau;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.du = du;
+  a.dg1 = dg1;
+  a.dgh = dgh;
+  a.dg0 = dg0;
+  a.dmu = dmu;
+  a.dtau = dtau;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.rope = rope;
+  a.dtype = dtype;
+  a.status = ws->status;
+  if (int rc = bwd_scratch(ws, bwd_scratch_bytes(B, H, N, d), &a.scratch)) return rc;
+  if (rope) {
+    if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
+  }
+  e = launch_bwd(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ZEROS_OK;
 }
 
 int zeros_get_status(void* stream) {

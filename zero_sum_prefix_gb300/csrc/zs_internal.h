@@ -34,6 +34,19 @@ struct DecodeArgs {
   int* status;
 };
 
+struct BwdArgs {
+  const void *q, *k, *v, *u, *dout;  // [B,H,N,d] input dtype
+  const float *g1, *gh, *g0;         // [B,H,N] (g0 nullable)
+  const float *mu, *tau;             // [H,d], [H]
+  float *dq, *dk, *dv, *du;          // [B,H,N,d] fp32
+  float *dg1, *dgh, *dg0;            // [B,H,N] fp32 (dg0 nullable)
+  float *dmu, *dtau;                 // [H,d], [H] fp32, accumulated (zeroed by the host)
+  float* scratch;                    // bwd_scratch_bytes
+  const float2* rope_table;          // [N][d/2] when rope
+  int B, H, N, d, rope, dtype;
+  int* status;
+};
+
 // Counts every kernel launch the library issues (zs_api.cu).
 void count_launches(unsigned n);
 
@@ -53,6 +66,10 @@ cudaError_t noalloc_rope_table(float2** table);
 // zs_chunk.cu
 bool chunk_supported(int d, int dtype, int causal);
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);
+
+// zs_backward.cu
+size_t bwd_scratch_bytes(int B, int H, int N, int d);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // zs_decode.cu
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
