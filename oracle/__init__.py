@@ -80,6 +80,8 @@ class Oracle:
         lib.zs_oracle_brute.argtypes = [dp] * 9 + [i] * 6 + [ctypes.c_double, i, dp, dp, dp]
         lib.zs_oracle_brute.restype = i
         lib.zs_oracle_threads.restype = i
+        lib.zs_oracle_layer_norm.argtypes = [dp] * 3 + [ctypes.c_double, dp] + [i] * 4
+        lib.zs_oracle_layer_norm.restype = i
         self.lib = lib
 
     def threads(self) -> int:
@@ -126,6 +128,19 @@ class Oracle:
         return out, ws, wm
 
 
+    def layer_norm(self, o, w=None, b=None, eps=1e-5):
+        """Output LayerNorm of every head's row over its d channels: o [B,H,N,d]; w, b [H,d]
+        (None: gain 1, bias 0).  Returns a new float64 array."""
+        o = _f64(o)
+        B, H, N, d = o.shape
+        w, b = _gate(w, (H, d)), _gate(b, (H, d))
+        y = np.zeros_like(o)
+        if self.lib.zs_oracle_layer_norm(_ptr(o), _ptr(w), _ptr(b), float(eps), _ptr(y),
+                                         B, H, N, d) != 0:
+            raise ValueError("oracle rejected its arguments")
+        return y
+
+
 def default() -> Oracle:
     global _lib
     with _lock:
@@ -144,3 +159,7 @@ def forward(*args, **kw):
 
 def brute(*args, **kw):
     return default().brute(*args, **kw)
+
+
+def layer_norm(*args, **kw):
+    return default().layer_norm(*args, **kw)

@@ -35,6 +35,11 @@
 //     the zero-order term"; [AI] "optionally sigma^0_t in the first layer"): the weight gains
 //     the zero-order term itself, w_{t,i} += sig^0_t / t with sig^0_t = sigmoid(g0_t), so the
 //     weights sum to sig^0_t; in the five-state form gamma_t gains sig^0_t / t.
+//   * Output LayerNorm (optional; [PN] ablation table "without LayerNorm" and the Lipschitz
+//     discussion of the highlights section name a LayerNorm on the layer's output but not its
+//     placement): applied to each head's output row o_t over its d channels,
+//     y = (o_t - mean) / sqrt(var + eps) * w + b with the biased variance, w and b per head
+//     [H,d] (absent: 1 and 0).
 //
 // Parity pins for everything here live in tests/test_oracle_pins.py.
 
@@ -291,6 +296,30 @@ int zs_oracle_brute(const double* q, const double* k, const double* v, const dou
   if (!valid(pr) || !out) return 1;
   parallel_over_heads(pr, nthreads,
                       [&](int b, int h) { brute_one(pr, b, h, out, wsum, wabsmax); });
+  return 0;
+}
+
+// LayerNorm of every output row: o, y [B,H,N,d]; w, b [H,d] (nullable: 1 and 0).  y may alias
+// o.  Returns 0, or 1 on bad arguments.
+int zs_oracle_layer_norm(const double* o, const double* w, const double* b, double eps, double* y,
+                         int B, int H, int N, int d) {
+  if (!o || !y || B < 0 || H < 0 || N < 0 || d <= 0 || !(eps >= 0.0)) return 1;
+  for (long long r = 0; r < (long long)B * H * N; ++r) {
+    const int h = (int)((r / N) % H);
+    const double* x = o + r * d;
+    double mean = 0.0;
+    for (int j = 0; j < d; ++j) mean += x[j];
+    mean /= d;
+    double var = 0.0;
+    for (int j = 0; j < d; ++j) var += (x[j] - mean) * (x[j] - mean);
+    var /= d;
+    const double inv = 1.0 / std::sqrt(var + eps);
+    for (int j = 0; j < d; ++j) {
+      const double gain = w ? w[(size_t)h * d + j] : 1.0;
+      const double bias = b ? b[(size_t)h * d + j] : 0.0;
+      y[r * d + j] = (x[j] - mean) * inv * gain + bias;
+    }
+  }
   return 0;
 }
 

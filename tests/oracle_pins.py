@@ -318,8 +318,55 @@ def pin_zero_order_linearity(orc):
             assert np.allclose(o1[0, 0, t] - o0[0, 0, t], ref, rtol=0, atol=1e-13)
 
 
+# ---------------------------------------------------------------------------------------------
+# Output LayerNorm (Paper-Notes, ablation table "without LayerNorm" and the highlights' remark that
+# LayerNorm supersedes the 1/sqrt(t) Lipschitz decay; placement read as each head's output row).
+def _ln_params(seed, H, d):
+    rng = np.random.default_rng(seed)
+    return 1.0 + 0.5 * rng.standard_normal((H, d)), 0.3 * rng.standard_normal((H, d))
+
+
+def pin_layer_norm_moments(orc):
+    """Without gain and bias every normalised row has mean 0 and population variance
+    var / (var + eps), var being the row's own population variance (numpy)."""
+    p = rand_problem(31, B=2, H=3, N=20, d=16)
+    o = orc.forward(*_args(p), causal=True, rope=True)
+    for eps in (1e-5, 0.25):
+        y = orc.layer_norm(o, eps=eps)
+        var = np.var(o, axis=-1)
+        assert np.abs(y.mean(-1)).max() < 1e-13
+        rows = var > 0
+        assert np.allclose(np.var(y, axis=-1)[rows], (var / (var + eps))[rows], rtol=1e-12, atol=0)
+
+
+def pin_layer_norm_library(orc):
+    """Gain and bias per head: every head's rows equal torch.nn.functional.layer_norm (fp64)."""
+    import torch
+    p = rand_problem(32, B=2, H=3, N=17, d=8)
+    w, b = _ln_params(33, 3, 8)
+    for causal in (True, False):
+        o = orc.forward(*_args(p), causal=causal, rope=False)
+        y = orc.layer_norm(o, w, b, eps=1e-5)
+        for h in range(3):
+            ref = torch.nn.functional.layer_norm(torch.from_numpy(o[:, h]), (8,),
+                                                 torch.from_numpy(w[h]), torch.from_numpy(b[h]),
+                                                 eps=1e-5).numpy()
+            assert np.allclose(y[:, h], ref, rtol=0, atol=1e-12)
+
+
+def pin_layer_norm_first_row(orc):
+    """The first causal output is zero (the one weight of a single token is zero; the recurrence
+    leaves rounding residue near 1e-16), so its normalised row is the head's bias."""
+    p = rand_problem(34, B=1, H=2, N=5, d=8)
+    w, b = _ln_params(35, 2, 8)
+    y = orc.layer_norm(orc.forward(*_args(p), causal=True), w, b, eps=1e-5)
+    assert np.allclose(y[:, :, 0], np.broadcast_to(b, y[:, :, 0].shape), rtol=0, atol=1e-9)
+    assert not np.allclose(y[:, :, 1], np.broadcast_to(b, y[:, :, 1].shape), rtol=0, atol=1e-3)
+
+
 ALL_PINS = [pin_golden_two_token, pin_brute_vs_recurrent, pin_zero_sum, pin_first_output_zero,
             pin_lemma_3_4, pin_two_token_collinear, pin_constant_logits, pin_equal_gates_softmax,
             pin_equal_gates_softmax_rope, pin_linear_gate_limit, pin_rope_relative, pin_scale_and_linearity, pin_prior_limits,
             pin_prefix_sums,
-            pin_zero_order_sum, pin_zero_order_uniform, pin_zero_order_linearity]
+            pin_zero_order_sum, pin_zero_order_uniform, pin_zero_order_linearity,
+            pin_layer_norm_moments, pin_layer_norm_library, pin_layer_norm_first_row]

@@ -41,6 +41,10 @@ MUTATIONS = [
     ("zero-order over t+1", "sigmoid(pr.g0[base + t_idx]) / tcount",
      "sigmoid(pr.g0[base + t_idx]) / (tcount + 1)"),
     ("brute zero-order dropped", "const double w = w_zs + sig0 / tc;", "const double w = w_zs;"),
+    ("layer norm unbiased variance", "    var /= d;", "    var /= (d - 1);"),
+    ("layer norm eps outside sqrt", "1.0 / std::sqrt(var + eps)", "1.0 / (std::sqrt(var) + eps)"),
+    ("layer norm head index", "const int h = (int)((r / N) % H);", "const int h = (int)(r % H);"),
+    ("layer norm bias dropped", "* inv * gain + bias;", "* inv * gain;"),
 ]
 
 
