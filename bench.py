@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload causal|encoder|long|decode] [--path auto|simt|chunk]
-                    [--pass fwd|bwd]
+                    [--pass fwd|bwd] [--ln]
 
 One step = one pass of the whole hot path (logits, prefix scans, zero-sum weights, angular
 factor, state scan and readout: one zeros_fwd call) over one batch of device-resident
@@ -259,10 +259,16 @@ def ours_forward(args, w: zi.Workload):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    ln = {}
+    if args.ln:  # fused output LayerNorm with a per-head gain and bias
+        gen = torch.Generator(device="cpu").manual_seed(w.seed + 17)
+        ln = dict(ln=True, ln_w=(1.0 + 0.1 * torch.randn((w.H, w.d), generator=gen)).to(dev),
+                  ln_b=(0.1 * torch.randn((w.H, w.d), generator=gen)).to(dev))
+
     def step():
         zs.fwd(inp["q"], inp["k"], inp["v"], inp["u"], inp["g1"], inp["gh"], inp["mu"],
                inp["tau"], causal=w.causal, rope=w.rope, rope_base=w.rope_base, out=out,
-               path=args.path)
+               path=args.path, **ln)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1.0)
@@ -311,7 +317,7 @@ def ours_forward(args, w: zi.Workload):
             dev_in[n].copy_(host[n], non_blocking=True)
         o = zs.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["u"], dev_in["g1"],
                    dev_in["gh"], dev_in["mu"], dev_in["tau"], causal=w.causal, rope=w.rope,
-                   rope_base=w.rope_base, out=out, path=args.path)
+                   rope_base=w.rope_base, out=out, path=args.path, **ln)
         host_out.copy_(o, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 20))
@@ -348,12 +354,13 @@ def ours_forward(args, w: zi.Workload):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "causal": w.causal, "rope": w.rope, "rope_base": w.rope_base,
                        "path": args.path, "parallelism": f"replicas x{world}",
+                       "output_layernorm": bool(args.ln),
                        "l2": "flushed before every step (256 MB write, outside the events)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm,
                          "traffic": (MEASURED_TRAFFIC.get(kernel_fingerprint())
                                      if w is zi.CAUSAL_ROPE_B8H8N4096D64 and args.path != "simt"
-                                     else None),
+                                     and not args.ln else None),
                          "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": alg},
             "cpu_baseline": cpu,
@@ -568,6 +575,7 @@ def main():
     ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "chunk"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--ln", action="store_true", help="fuse the output LayerNorm (forward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]

@@ -100,6 +100,25 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
                  void* stream);
 
 /*
+ * Forward with a fused output LayerNorm (Paper-Notes "ZeroS", ablation table: removing the
+ * LayerNorm costs accuracy; highlights: LayerNorm supersedes the 1/sqrt(t) Lipschitz decay.
+ * The pages do not place it; read here as the normalisation of each head's output row):
+ *   y_t = (o_t - mean(o_t)) / sqrt(var(o_t) + ln_eps) * ln_w[h] + ln_b[h]
+ * over the d columns of o_t, var the population variance, before the output is rounded to
+ * its dtype.  Same computation, layouts and other arguments as zeros_fwd_ex (without debug
+ * outputs); final_state (prefill) holds the un-normalised scan state as there.
+ *   ln_w, ln_b : nullable fp32 [H, d] gain and bias (NULL: 1 and 0), 16-byte aligned
+ *   ln_eps     : finite, >= 0
+ * On the GPU the d / 32 value slices of a head run as one thread-block cluster and exchange
+ * their rows' statistics through distributed shared memory.
+ */
+int zeros_fwd_ln(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* g0, const float* mu, const float* tau,
+                 const float* ln_w, const float* ln_b, float ln_eps, void* out, int B, int H,
+                 int N, int d, int causal, int rope, int dtype, float rope_base, int path,
+                 void* final_state, void* stream);
+
+/*
  * Allocation-free forward (the pages have no counterpart: this entry point exists for callers
  * that must not allocate device memory themselves or through this library, for example code
  * whose device memory is all handed out up front by its own allocator, or a runtime that forbids
@@ -180,6 +199,13 @@ int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const 
                          const float* g0,
                          void* out, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
                          void* stream);
+
+/* zeros_decode_step_ex with the fused output LayerNorm of zeros_fwd_ln (ln_w, ln_b nullable
+ * fp32 [H, d]; ln_eps finite, >= 0) and no debug outputs.  The state is not affected by it. */
+int zeros_decode_step_ln(void* state, int B, int H, int d, const void* q, const void* k,
+                         const void* v, const void* u, const float* g1, const float* gh,
+                         const float* g0, const float* ln_w, const float* ln_b, float ln_eps,
+                         void* out, void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's status word. */
 int zeros_get_status(void* stream);

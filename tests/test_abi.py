@@ -92,3 +92,17 @@ def test_host_validation_without_gpu(lib):
     assert bwd(ptr=24) == zs.ZEROS_ERR_INVALID
     assert bwd(dg0=16) == zs.ZEROS_ERR_INVALID       # dg0 without the gate
     assert bwd(rope=1, base=-1.0) == zs.ZEROS_ERR_INVALID
+    # output LayerNorm: epsilon and gain/bias pointers are checked before any CUDA call
+    def fwd_ln(eps=1e-5, w=None, b=None, d=64):
+        wp = ctypes.c_void_p(w) if w is not None else None
+        bp = ctypes.c_void_p(b) if b is not None else None
+        return lib.zeros_fwd_ln(p, p, p, p, p, p, None, p, p, wp, bp, eps, p, 1, 1, 4, d, 1, 0,
+                                0, 1e4, 0, None, None)
+    assert fwd_ln(eps=-1.0) == zs.ZEROS_ERR_INVALID
+    assert fwd_ln(eps=float("inf")) == zs.ZEROS_ERR_INVALID
+    assert fwd_ln(eps=float("nan")) == zs.ZEROS_ERR_INVALID
+    assert fwd_ln(w=20) == zs.ZEROS_ERR_INVALID
+    assert fwd_ln(b=36) == zs.ZEROS_ERR_INVALID
+    assert fwd_ln(d=48) == zs.ZEROS_ERR_UNSUPPORTED
+    assert lib.zeros_decode_step_ln(p, 1, 1, 64, *([p] * 6), None, None, None, 1e-5, p,
+                                    None) == zs.ZEROS_ERR_INVALID

@@ -28,7 +28,8 @@ PATHS = {"auto": 0, "simt": 1, "chunk": 2}
 EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record_bytes",
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
-           "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd"]
+           "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd", "zeros_fwd_ln",
+           "zeros_decode_step_ln"]
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +79,10 @@ def load():
         lib.zeros_fwd_noalloc.argtypes = [vp] * 9 + [i] * 7 + [f, vp, vp]
         lib.zeros_bwd.argtypes = [vp] * 19 + [i] * 6 + [f, vp]
         lib.zeros_bwd.restype = i
+        lib.zeros_fwd_ln.argtypes = [vp] * 11 + [f, vp] + [i] * 7 + [f, i, vp, vp]
+        lib.zeros_fwd_ln.restype = i
+        lib.zeros_decode_step_ln.argtypes = [vp, i, i, i] + [vp] * 9 + [f, vp, vp]
+        lib.zeros_decode_step_ln.restype = i
         lib.zeros_fwd_noalloc.restype = i
         _lib = lib
         return lib
@@ -126,12 +131,22 @@ def _need(t, name, shape, dtype=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _ln_args(ln, ln_w, ln_b, H, d):
+    if ln_w is not None:
+        _need(ln_w, "ln_w", (H, d), torch.float32)
+    if ln_b is not None:
+        _need(ln_b, "ln_b", (H, d), torch.float32)
+    return bool(ln) or ln_w is not None or ln_b is not None
+
+
 def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000.0, out=None,
-        final_state=None, debug=False, path="auto", stream=None, g0=None):
+        final_state=None, debug=False, path="auto", stream=None, g0=None, ln=False, ln_w=None,
+        ln_b=None, ln_eps=1e-5):
     """ZeroS forward.  q, k, v, u: [B, H, N, d] bf16 or fp32 (same dtype); g1, gh: [B, H, N]
     fp32 gate logits; mu: [H, d] fp32; tau: [H] fp32; g0: optional [B, H, N] fp32 zero-order
-    gate logits of a first layer.  Returns ``out`` (same dtype as q), or ``(out, dbg)`` with
-    ``dbg = dict(s, E, P, m)`` ([B, H, N] fp32) when ``debug``."""
+    gate logits of a first layer.  ``ln`` (implied by ``ln_w`` / ``ln_b``, [H, d] fp32) fuses
+    the output LayerNorm of each head's rows.  Returns ``out`` (same dtype as q), or
+    ``(out, dbg)`` with ``dbg = dict(s, E, P, m)`` ([B, H, N] fp32) when ``debug``."""
     B, H, N, d = q.shape
     dt = q.dtype
     for name, t in (("q", q), ("k", k), ("v", v), ("u", u)):
@@ -147,11 +162,21 @@ def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000
     _need(out, "out", (B, H, N, d), dt)
     if final_state is not None:
         _need(final_state, "final_state", (state_bytes(B, H, d),), torch.uint8)
+    lib = load()
+    if _ln_args(ln, ln_w, ln_b, H, d):
+        if debug:
+            raise ValueError("debug outputs are not available with the output LayerNorm")
+        rc = lib.zeros_fwd_ln(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(g0),
+                              _ptr(mu), _ptr(tau), _ptr(ln_w), _ptr(ln_b), float(ln_eps),
+                              _ptr(out), B, H, N, d, int(bool(causal)), int(bool(rope)),
+                              _dtype_code(q), float(rope_base), PATHS[path], _ptr(final_state),
+                              _stream(stream))
+        _check(rc, "zeros_fwd_ln")
+        return out
     dbg = None
     if debug:
         dbg = {n: torch.empty((B, H, N), device=q.device, dtype=torch.float32)
                for n in ("s", "E", "P", "m")}
-    lib = load()
     rc = lib.zeros_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(g0),
                           _ptr(mu), _ptr(tau), _ptr(out), B, H, N, d, int(bool(causal)),
                           int(bool(rope)),
@@ -220,9 +245,10 @@ def new_state(mu, tau, B: int, *, dtype=torch.bfloat16, rope=False, rope_base=10
     return st
 
 
-def decode_step(state, q, k, v, u, g1, gh, *, out=None, debug=False, stream=None, g0=None):
+def decode_step(state, q, k, v, u, g1, gh, *, out=None, debug=False, stream=None, g0=None,
+                ln=False, ln_w=None, ln_b=None, ln_eps=1e-5):
     """One recurrent step for every sequence: q, k, v, u [B, H, d]; g1, gh [B, H]; g0
-    optional [B, H] zero-order gate logits."""
+    optional [B, H] zero-order gate logits; ``ln`` / ``ln_w`` / ``ln_b`` as in ``fwd``."""
     B, H, d = q.shape
     dt = q.dtype
     for name, t in (("q", q), ("k", k), ("v", v), ("u", u)):
@@ -235,6 +261,14 @@ def decode_step(state, q, k, v, u, g1, gh, *, out=None, debug=False, stream=None
         out = torch.empty_like(q)
     _need(out, "out", (B, H, d), dt)
     lib = load()
+    if _ln_args(ln, ln_w, ln_b, H, d):
+        if debug:
+            raise ValueError("debug outputs are not available with the output LayerNorm")
+        rc = lib.zeros_decode_step_ln(_ptr(state), B, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(u),
+                                      _ptr(g1), _ptr(gh), _ptr(g0), _ptr(ln_w), _ptr(ln_b),
+                                      float(ln_eps), _ptr(out), _stream(stream))
+        _check(rc, "zeros_decode_step_ln")
+        return out
     if debug or g0 is not None:
         dbg = None
         if debug:

@@ -191,14 +191,23 @@ size_t zeros_state_bytes(int B, int H, int d) {
   return state_bytes(B, H, d);
 }
 
-int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
-                 const float* gh, const float* g0, const float* mu, const float* tau, void* out,
-                 int B, int H, int N, int d, int causal, int rope, int dtype, float rope_base,
-                 int path,
-                 void* final_state, float* dbg_s, float* dbg_E, float* dbg_P, float* dbg_m,
-                 void* stream) {
+static int check_ln(int ln, const float* ln_w, const float* ln_b, float ln_eps) {
+  if (!ln) return ZEROS_OK;
+  if (!(ln_eps >= 0.0f && ln_eps <= 3.0e38f))
+    return fail(ZEROS_ERR_INVALID, "ln_eps must be finite and >= 0");
+  if (int rc = check_opt_ptr(ln_w, "ln_w")) return rc;
+  return check_opt_ptr(ln_b, "ln_b");
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                    const float* gh, const float* g0, const float* mu, const float* tau,
+                    void* out, int B, int H, int N, int d, int causal, int rope, int dtype,
+                    float rope_base, int path, void* final_state, float* dbg_s, float* dbg_E,
+                    float* dbg_P, float* dbg_m, int ln, const float* ln_w, const float* ln_b,
+                    float ln_eps, void* stream) {
   g_last_error.clear();
   if (int rc = check_dims(B, H, N, d)) return rc;
+  if (int rc = check_ln(ln, ln_w, ln_b, ln_eps)) return rc;
   if (int rc = check_dtype(dtype)) return rc;
   if (causal != 0 && causal != 1) return fail(ZEROS_ERR_INVALID, "causal must be 0 or 1");
   if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
@@ -264,12 +273,36 @@ int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, con
   a.dbg_P = dbg_P;
   a.dbg_m = dbg_m;
   a.status = ws->status;
+  a.ln = ln;
+  a.ln_w = ln_w;
+  a.ln_b = ln_b;
+  a.ln_eps = ln_eps;
   if (rope && !use_chunk) {  // the chunked kernel computes its rotary factors itself
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
   cudaError_t e = use_chunk ? launch_fwd_chunk(a, st) : launch_fwd_simt(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ZEROS_OK;
+}
+
+int zeros_fwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* g0, const float* mu, const float* tau, void* out,
+                 int B, int H, int N, int d, int causal, int rope, int dtype, float rope_base,
+                 int path, void* final_state, float* dbg_s, float* dbg_E, float* dbg_P,
+                 float* dbg_m, void* stream) {
+  return fwd_impl(q, k, v, u, g1, gh, g0, mu, tau, out, B, H, N, d, causal, rope, dtype,
+                  rope_base, path, final_state, dbg_s, dbg_E, dbg_P, dbg_m, 0, nullptr, nullptr,
+                  0.0f, stream);
+}
+
+int zeros_fwd_ln(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* g0, const float* mu, const float* tau,
+                 const float* ln_w, const float* ln_b, float ln_eps, void* out, int B, int H,
+                 int N, int d, int causal, int rope, int dtype, float rope_base, int path,
+                 void* final_state, void* stream) {
+  return fwd_impl(q, k, v, u, g1, gh, g0, mu, tau, out, B, H, N, d, causal, rope, dtype,
+                  rope_base, path, final_state, nullptr, nullptr, nullptr, nullptr, 1, ln_w, ln_b,
+                  ln_eps, stream);
 }
 
 int zeros_fwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
@@ -365,8 +398,10 @@ int zeros_state_init(void* state, const float* mu, const float* tau, int B, int 
 static int decode_impl(void* state, const StateInfo& si, const void* q, const void* k,
                        const void* v, const void* u, const float* g1, const float* gh,
                        const float* g0, void* out, float* dbg_s, float* dbg_E, float* dbg_P,
-                       float* dbg_m, void* stream) {
+                       float* dbg_m, void* stream, int ln = 0, const float* ln_w = nullptr,
+                       const float* ln_b = nullptr, float ln_eps = 0.0f) {
   if (int rc = check_dims(si.B, si.H, 1, si.d)) return rc;
+  if (int rc = check_ln(ln, ln_w, ln_b, ln_eps)) return rc;
   if (int rc = check_ptr(state, "state")) return rc;
   if ((long long)si.B * si.H == 0) return ZEROS_OK;
   const char* names[] = {"q", "k", "v", "u", "g1", "gh", "out"};
@@ -401,6 +436,10 @@ static int decode_impl(void* state, const StateInfo& si, const void* q, const vo
   a.dbg_P = dbg_P;
   a.dbg_m = dbg_m;
   a.status = ws->status;
+  a.ln = ln;
+  a.ln_w = ln_w;
+  a.ln_b = ln_b;
+  a.ln_eps = ln_eps;
   cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return ZEROS_OK;
@@ -432,6 +471,30 @@ int zeros_decode_step(void* state, const void* q, const void* k, const void* v, 
   }
   return decode_impl(state, si, q, k, v, u, g1, gh, nullptr, out, nullptr, nullptr, nullptr,
                      nullptr, stream);
+}
+
+static int known_state(void* state, int B, int H, int d, StateInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  auto it = g_states.find(state);
+  if (it == g_states.end())
+    return fail(ZEROS_ERR_INVALID,
+                "state unknown to this process: create it with zeros_state_init or "
+                "zeros_fwd_ex, or call zeros_decode_step once");
+  if (it->second.B != B || it->second.H != H || it->second.d != d)
+    return fail(ZEROS_ERR_INVALID, "dimensions differ from the state's");
+  *out = it->second;
+  return ZEROS_OK;
+}
+
+int zeros_decode_step_ln(void* state, int B, int H, int d, const void* q, const void* k,
+                         const void* v, const void* u, const float* g1, const float* gh,
+                         const float* g0, const float* ln_w, const float* ln_b, float ln_eps,
+                         void* out, void* stream) {
+  g_last_error.clear();
+  StateInfo si{};
+  if (int rc = known_state(state, B, H, d, &si)) return rc;
+  return decode_impl(state, si, q, k, v, u, g1, gh, g0, out, nullptr, nullptr, nullptr, nullptr,
+                     stream, 1, ln_w, ln_b, ln_eps);
 }
 
 int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const void* k,

@@ -109,7 +109,12 @@ struct Cfg {
   static constexpr uint32_t CIN_OFF = SCAL_OFF + SCALS * kC * 16;   // float [2][D] column carries
   static constexpr uint32_t KCIN_OFF = CIN_OFF + 2 * D * 4;         // float [2][4] scalar carries
   static constexpr uint32_t MISC_OFF = KCIN_OFF + 32;
-  static constexpr uint32_t BYTES = MISC_OFF + 512;
+  // output LayerNorm: per-row (mean, M2) of every value slice of the head, two chunk slots
+  // (float2 [2][D / kDV][128]), then this slice's gain and bias (float [2][32]); only without
+  // the chunk-alternating cluster, which has no room for them
+  static constexpr uint32_t LNX_OFF = MISC_OFF + 512;
+  static constexpr uint32_t LNW_OFF = LNX_OFF + (CL == 1 ? 2 * (D / kDV) * kC * 8 : 0);
+  static constexpr uint32_t BYTES = LNW_OFF + (CL == 1 ? 2 * 32 * 4 : 0);
   static constexpr uint32_t SMEM = BYTES;  // the base is 1024-byte aligned (checked at entry)
   static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
   // S tile (bf16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
@@ -135,6 +140,7 @@ struct Misc {
   uint64_t scal_full[2], scal_empty[2];
   uint64_t peer_full;            // tiles of a chunk owned by the other CTA have landed
   uint64_t ccar_full, kcar_full;  // carries from the other CTA's previous chunk
+  uint64_t ln_full[2];  // output LayerNorm: row statistics of the other value slices landed
   float Mslot[2];
   int w_seen;  // with a cluster: number of w_done phases observed (monotonic)
   uint32_t tmem;
@@ -973,7 +979,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 // Per chunk c: the S tile (A o W, masked, bf16), the scaled value tile of chunk c+1 when the
 // other CTA of the cluster owns it, the state after chunk c as the bf16 B tile of chunk c+1 (F~
 // rescaled to M_{c+1}), then the output rows of chunk c.
-template <int D, int CL>
+template <int D, int CL, bool LN>
 __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, size_t row0,
                               int nch) {
   using CF = Cfg<D, CL>;
@@ -1144,10 +1150,10 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     tc_fence_after();
     const int i = c * kC + t;
     uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * D + j0);
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
+    // the 16 outputs of half hf of row t (fp32 bit patterns)
+    auto out_half = [&](int hf, uint32_t (&rsv)[16]) {
       const uint32_t tx = tm + CF::TM_X + hf * 16;
-      uint32_t rsv[16], rx[16];
+      uint32_t rx[16];
       tmem_ld16_nowait(tx + 96, rsv);
       if (c >= 1) tmem_ld16_nowait(tx + 0, rx);
       tmem_wait_ld();
@@ -1168,6 +1174,63 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
           rsv[j] = __float_as_uint(__fmaf_rn(cf.z, __uint_as_float(ry[j]),
                                              __fmaf_rn(cf.y, __uint_as_float(rx[j]),
                                                        __uint_as_float(rsv[j]))));
+      }
+    };
+    float ln_mean = 0.0f, ln_rstd = 1.0f;
+    if constexpr (LN) {
+      // Output LayerNorm over the head's d columns, split over the D / 32 value-slice CTAs of
+      // the cluster: each publishes its rows' (mean, M2) over its 32 columns (shifted sums),
+      // the statistics are merged (pairwise moment update), and the
+      // outputs are recomputed from TMEM (X stays allocated until x_free) and normalised.
+      constexpr int NSL = D / kDV;
+      float sh = 0.0f, s1 = 0.0f, s2 = 0.0f;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t rsv[16];
+        out_half(hf, rsv);
+        if (hf == 0) sh = __uint_as_float(rsv[0]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float dv = __uint_as_float(rsv[j]) - sh;
+          s1 += dv;
+          s2 = __fmaf_rn(dv, dv, s2);
+        }
+      }
+      const float lmean = sh + s1 * (1.0f / kDV);
+      const float lm2 = fmaxf(s2 - s1 * s1 * (1.0f / kDV), 0.0f);
+      const int me = blockIdx.y;
+      float2* lnx = reinterpret_cast<float2*>(smem + CF::LNX_OFF);
+      const uint32_t slot = smem_u32(&lnx[((c & 1) * NSL + me) * kC + t]);
+#pragma unroll
+      for (int r = 1; r < NSL; ++r) st_cluster_f32x2(mapa(slot, (me + r) % NSL), lmean, lm2);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int r = 1; r < NSL; ++r)
+          mbar_arrive_remote(mapa(smem_u32(&ms->ln_full[c & 1]), (me + r) % NSL));
+      }
+      ok = mbar_wait_cl_warp(&ms->ln_full[c & 1], (uint32_t)(c >> 1) & 1u, &ms->abort);
+      if (!ok) break;
+      float cnt = (float)kDV, mean = lmean, m2 = lm2;  // merged over the slices
+#pragma unroll
+      for (int r = 1; r < NSL; ++r) {
+        const float2 o = lnx[((c & 1) * NSL + (me + r) % NSL) * kC + t];
+        moments_merge(cnt, mean, m2, (float)kDV, o.x, o.y);
+      }
+      ln_mean = mean;
+      ln_rstd = rsqrtf(m2 * (1.0f / D) + a.ln_eps);
+    }
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t rsv[16];
+      out_half(hf, rsv);
+      if constexpr (LN) {
+        const float* lw = reinterpret_cast<const float*>(smem + CF::LNW_OFF);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float y = (__uint_as_float(rsv[j]) - ln_mean) * ln_rstd;
+          rsv[j] = __float_as_uint(__fmaf_rn(y, lw[16 * hf + j], lw[32 + 16 * hf + j]));
+        }
       }
       uint32_t ob[8];  // the half's 16 outputs as bf16 pairs
 #pragma unroll
@@ -1212,7 +1275,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
 }
 
 // ============================================================================ kernel
-template <int D, int CL>
+template <int D, int CL, bool LN>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ ChunkParams p) {
   using CF = Cfg<D, CL>;
   const FwdArgs& a = p.a;
@@ -1260,10 +1323,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->peer_full, 1);
     mbar_init(&ms->ccar_full, 32);
     mbar_init(&ms->kcar_full, 1);
+    // LayerNorm statistics: one arrival per epilogue warp of every other value slice
+    for (int i = 0; i < 2; ++i) mbar_init(&ms->ln_full[i], 4 * (D / kDV - 1));
     ms->abort = 0;
     ms->never = 0;
     ms->w_seen = 0;
-    if (CL > 1) fence_mbarrier_init_cluster();
+    if (CL > 1 || LN) fence_mbarrier_init_cluster();
+  }
+  if (LN && threadIdx.x < 64) {  // this slice's LayerNorm gain (1 when absent) and bias (0)
+    const int j = threadIdx.x & 31;
+    const float* src = threadIdx.x < 32 ? a.ln_w : a.ln_b;
+    reinterpret_cast<float*>(smem + CF::LNW_OFF)[threadIdx.x] =
+        src ? src[(size_t)h * D + blockIdx.y * kDV + j] : (threadIdx.x < 32 ? 1.0f : 0.0f);
   }
   if (warp == 12) {
     tmem_alloc(&ms->tmem, 512);
@@ -1272,14 +1343,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL > 1) cluster_sync_all();  // the other CTA's barriers exist before any remote access
+  if (CL > 1 || LN) cluster_sync_all();  // the other CTAs' barriers exist before any remote access
 
   if (warp < 8 && (warp & 2) == 0) {
     role_scalars<D, CL>(a, smem, ms, bh, h, row0, nch, rank);
   } else if (warp < 8) {
     role_operands<D, CL>(a, smem, ms, h, row0, nch, rank);
   } else if (warp < 12) {
-    role_epilogue<D, CL>(a, smem, ms, bh, row0, nch);
+    role_epilogue<D, CL, LN>(a, smem, ms, bh, row0, nch);
   } else if (warp == 12) {
     if ((threadIdx.x & 31) == 0) role_mma<D, CL>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
@@ -1309,6 +1380,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     }
     // (every phase of w_done was waited for by the observer thread before the final barrier)
   }
+  // LayerNorm: the other slices write statistics into this CTA's shared memory until their
+  // last chunk; no CTA of the cluster exits before all have finished (every wait is bounded,
+  // so every thread arrives here)
+  if (LN) cluster_sync_all();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1347,15 +1422,18 @@ bool make_map(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_x,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool LN>
 cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
+  // with the output LayerNorm the D / 32 value slices of a head form one cluster
+  constexpr int kClY = LN ? D / kDV : kCL;
+  static_assert(!LN || kCL == 1, "the LayerNorm cluster spans the value slices");
   static std::atomic<uint64_t> attr_set{0};  // bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(chunk_kernel<D, kCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chunk_kernel<D, kCL, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Cfg<D, kCL>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
@@ -1377,11 +1455,11 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = kCL;
+  attr[0].val.clusterDim.y = kClY;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = kCL > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, chunk_kernel<D, kCL>, p);
+  cfg.numAttrs = kClY > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, chunk_kernel<D, kCL, LN>, p);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1394,8 +1472,8 @@ bool chunk_supported(int d, int dtype, int causal) {
 }
 
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return launch_d<64>(a, stream);
-  if (a.d == 128) return launch_d<128>(a, stream);
+  if (a.d == 64) return a.ln ? launch_d<64, true>(a, stream) : launch_d<64, false>(a, stream);
+  if (a.d == 128) return a.ln ? launch_d<128, true>(a, stream) : launch_d<128, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 

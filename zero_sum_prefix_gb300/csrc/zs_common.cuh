@@ -238,4 +238,23 @@ __device__ __forceinline__ int pair_index(int lane, int r) {
   return lane + 32 * r;  // valid for r < R/2
 }
 
+// ------------------------------------------------------------------------ output LayerNorm
+// Chan, Golub and LeVeque's pairwise update: merge the moments (count n, mean, M2 = sum of
+// squared deviations) of one part of a row with those of another part (n2, mean2, m22).
+__device__ __forceinline__ void moments_merge(float& n, float& mean, float& m2, float n2,
+                                              float mean2, float m22) {
+  const float nn = n + n2;
+  const float delta = mean2 - mean;
+  mean = __fmaf_rn(delta, n2 / nn, mean);
+  m2 = m2 + m22 + delta * delta * (n * n2 / nn);
+  n = nn;
+}
+
+// Sum over the 32 lanes of a warp (every lane receives it).
+__device__ __forceinline__ float warp_sum32(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 }  // namespace zs

@@ -155,21 +155,47 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
   }
   red[rp][c4] = acc;
   __syncthreads();
-  if (threadIdx.x < C4) {
-    float4 o = red[0][threadIdx.x];
+  if (warp == 0) {  // lanes < C4 reduce and write 4 output columns each
+    const bool mine = threadIdx.x < C4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mine) {
+      o = red[0][threadIdx.x];
 #pragma unroll 4
-    for (int r = 1; r < RPP; ++r) {
-      const float4 x = red[r][threadIdx.x];
-      o.x = __fadd_rn(o.x, x.x);
-      o.y = __fadd_rn(o.y, x.y);
-      o.z = __fadd_rn(o.z, x.z);
-      o.w = __fadd_rn(o.w, x.w);
+      for (int r = 1; r < RPP; ++r) {
+        const float4 x = red[r][threadIdx.x];
+        o.x = __fadd_rn(o.x, x.x);
+        o.y = __fadd_rn(o.y, x.y);
+        o.z = __fadd_rn(o.z, x.z);
+        o.w = __fadd_rn(o.w, x.w);
+      }
     }
-    T* out = static_cast<T*>(a.out) + tok + 4 * threadIdx.x;
-    st(out, 0, o.x);
-    st(out, 1, o.y);
-    st(out, 2, o.z);
-    st(out, 3, o.w);
+    if (a.ln) {  // output LayerNorm over the head's d columns (mean first, then deviations)
+      const float mean = warp_sum32((o.x + o.y) + (o.z + o.w)) * (1.0f / D);
+      float dv = 0.0f;
+      if (mine)
+        dv = (o.x - mean) * (o.x - mean) + (o.y - mean) * (o.y - mean) +
+             (o.z - mean) * (o.z - mean) + (o.w - mean) * (o.w - mean);
+      const float rstd = rsqrtf(warp_sum32(dv) * (1.0f / D) + a.ln_eps);
+      if (mine) {
+        // gain and bias rows are 16-byte aligned (checked by the host)
+        const size_t j4 = ((size_t)(bh % a.H) * D) / 4 + threadIdx.x;
+        const float4 w = a.ln_w ? reinterpret_cast<const float4*>(a.ln_w)[j4]
+                                : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 b = a.ln_b ? reinterpret_cast<const float4*>(a.ln_b)[j4]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        o.x = __fmaf_rn((o.x - mean) * rstd, w.x, b.x);
+        o.y = __fmaf_rn((o.y - mean) * rstd, w.y, b.y);
+        o.z = __fmaf_rn((o.z - mean) * rstd, w.z, b.z);
+        o.w = __fmaf_rn((o.w - mean) * rstd, w.w, b.w);
+      }
+    }
+    if (mine) {
+      T* out = static_cast<T*>(a.out) + tok + 4 * threadIdx.x;
+      st(out, 0, o.x);
+      st(out, 1, o.y);
+      st(out, 2, o.z);
+      st(out, 3, o.w);
+    }
   }
   if (warp == 0) {
 #pragma unroll

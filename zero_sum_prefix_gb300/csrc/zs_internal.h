@@ -20,6 +20,9 @@ struct FwdArgs {
   void* final_state;         // nullable (causal only)
   float *dbg_s, *dbg_E, *dbg_P, *dbg_m;
   int* status;               // device status word
+  int ln;                    // output LayerNorm over each head's d columns
+  const float *ln_w, *ln_b;  // nullable [H,d] gain and bias
+  float ln_eps;
 };
 
 struct DecodeArgs {
@@ -32,6 +35,9 @@ struct DecodeArgs {
   float rope_base;
   float *dbg_s, *dbg_E, *dbg_P, *dbg_m;
   int* status;
+  int ln;                    // output LayerNorm as in FwdArgs
+  const float *ln_w, *ln_b;
+  float ln_eps;
 };
 
 struct BwdArgs {

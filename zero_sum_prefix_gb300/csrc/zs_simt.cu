@@ -18,9 +18,12 @@
 
 #include "zs_common.cuh"
 #include "zs_internal.h"
+#include "zs_sm100.cuh"
 
 namespace zs {
 namespace {
+
+using namespace sm100;
 
 constexpr int kThreads = 256;
 
@@ -49,6 +52,70 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
   __shared__ float qs[D], ks[D], vs[32];
   __shared__ float red[8][32];
   __shared__ TokenCoefs tc;
+
+  // Output LayerNorm over the head's d columns.  The d/32 value slices of a head form one
+  // cluster (launched so when ln is set and d > 32).  Warp 7 writes the outputs: for token t it
+  // publishes (mean, M2) of its 32 columns to the other slices, then normalises token t - 1,
+  // whose statistics have had a token's time to arrive.
+  constexpr int NSL = D / 32;
+  __shared__ float2 lnx[2][NSL];                 // [token parity][slice]
+  __shared__ __align__(8) uint64_t ln_full[2];   // one arrival per other slice
+  __shared__ int ln_abort;
+  const bool clustered = a.ln && NSL > 1;
+  const int me = blockIdx.y;
+  if (clustered) {
+    if (threadIdx.x == 0) {
+      mbar_init(&ln_full[0], NSL - 1);
+      mbar_init(&ln_full[1], NSL - 1);
+      ln_abort = 0;
+      fence_mbarrier_init_cluster();
+    }
+    cluster_sync_all();
+  }
+  float ln_w = 1.0f, ln_b = 0.0f;
+  if (a.ln && warp == 7) {
+    if (a.ln_w) ln_w = a.ln_w[(size_t)h * D + j0 + lane];
+    if (a.ln_b) ln_b = a.ln_b[(size_t)h * D + j0 + lane];
+  }
+  float prev_o = 0.0f, prev_mean = 0.0f, prev_m2 = 0.0f;
+  bool ln_ok = true;
+  // warp 7: normalise and store token tt (its output, mean and M2 held in prev_*)
+  auto ln_finish = [&](int tt) {
+    float n = 32.0f, mean = prev_mean, m2 = prev_m2;
+    if (clustered && ln_ok) {
+      ln_ok = mbar_wait_cl_warp(&ln_full[tt & 1], (uint32_t)(tt >> 1) & 1u, &ln_abort);
+      if (!ln_ok) report(a.status, kErrTimeout);
+#pragma unroll
+      for (int r = 1; r < NSL; ++r) {
+        const float2 o = lnx[tt & 1][(me + r) % NSL];
+        moments_merge(n, mean, m2, 32.0f, o.x, o.y);
+      }
+    }
+    const float rstd = rsqrtf(m2 * (1.0f / D) + a.ln_eps);
+    st(out, (size_t)tt * D + j0 + lane, __fmaf_rn((prev_o - mean) * rstd, ln_w, ln_b));
+  };
+  // warp 7: output o of token tt (lane = column j0 + lane)
+  auto emit = [&](int tt, float o) {
+    if (!a.ln) {
+      st(out, (size_t)tt * D + j0 + lane, o);
+      return;
+    }
+    const float mean = warp_sum32(o) * (1.0f / 32.0f);
+    const float dv = o - mean;
+    const float m2 = warp_sum32(dv * dv);
+    if (tt >= 1) ln_finish(tt - 1);
+    if (clustered && ln_ok && lane == 0) {
+#pragma unroll
+      for (int r = 1; r < NSL; ++r) {
+        const uint32_t peer = (uint32_t)((me + r) % NSL);
+        st_cluster_f32x2(mapa(smem_u32(&lnx[tt & 1][me]), peer), mean, m2);
+        mbar_arrive_remote(mapa(smem_u32(&ln_full[tt & 1]), peer));
+      }
+    }
+    prev_o = o;
+    prev_mean = mean;
+    prev_m2 = m2;
+  };
 
   float F[RA], G[RA], Hs[RA];
 #pragma unroll
@@ -184,9 +251,10 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
       float o = red[0][lane];
 #pragma unroll
       for (int w = 1; w < 8; ++w) o = __fadd_rn(o, red[w][lane]);
-      st(out, (size_t)t * D + j0 + lane, o);
+      emit(t, o);
     }
   }
+  if (a.causal && a.ln && warp == 7 && N > 0) ln_finish(N - 1);
 
   if (a.causal) {
     // ---- optional final state (prefill for recurrent decoding) ----
@@ -219,6 +287,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
         }
       }
     }
+    // no CTA of a LayerNorm cluster exits while another may still write its statistics
+    if (clustered) cluster_sync_all();
     return;
   }
 
@@ -260,21 +330,36 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
       float o = red[0][lane];
 #pragma unroll
       for (int w = 1; w < 8; ++w) o = __fadd_rn(o, red[w][lane]);
-      st(out, (size_t)t * D + j0 + lane, o);
+      emit(t, o);
     }
   }
+  if (a.ln && warp == 7 && N > 0) ln_finish(N - 1);
+  if (clustered) cluster_sync_all();
 }
 
 template <typename T>
 cudaError_t launch_simt_typed(const FwdArgs& a, cudaStream_t stream) {
-  dim3 grid(a.B * a.H, a.d / 32);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.H, a.d / 32, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  // with the output LayerNorm the value slices of a head form one cluster
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.d / 32;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (a.ln && a.d > 32) ? 1 : 0;
+  cudaError_t e;
   switch (a.d) {
-    case 32: fwd_simt_kernel<T, 32><<<grid, kThreads, 0, stream>>>(a); break;
-    case 64: fwd_simt_kernel<T, 64><<<grid, kThreads, 0, stream>>>(a); break;
-    case 128: fwd_simt_kernel<T, 128><<<grid, kThreads, 0, stream>>>(a); break;
+    case 32: e = cudaLaunchKernelEx(&cfg, fwd_simt_kernel<T, 32>, a); break;
+    case 64: e = cudaLaunchKernelEx(&cfg, fwd_simt_kernel<T, 64>, a); break;
+    case 128: e = cudaLaunchKernelEx(&cfg, fwd_simt_kernel<T, 128>, a); break;
     default: return cudaErrorInvalidValue;
   }
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity)
 
 // Polling loop of mbar_wait, kept out of line so that the many wait sites stay small (the
 // first probe is inline).
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
                                             long long limit_cycles) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
@@ -123,7 +123,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // mbar_wait with cluster-scope acquire (see mbar_try_wait_cl).
-__device__ __noinline__ bool mbar_wait_cl_slow(uint64_t* bar, uint32_t parity,
+static __device__ __noinline__ bool mbar_wait_cl_slow(uint64_t* bar, uint32_t parity,
                                                volatile int* abort, long long limit_cycles) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
@@ -162,6 +162,10 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t caddr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(x), "f"(y)
+               : "memory");
 }
 __device__ __forceinline__ void st_cluster_s32(uint32_t caddr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
@@ -204,7 +208,7 @@ __device__ __forceinline__ int ld_acquire_s32(const int* p) {
   return v;
 }
 // Waits until *p >= target; bounded like mbar_wait.
-__device__ __noinline__ bool counter_wait(const int* p, int target, volatile int* abort,
+static __device__ __noinline__ bool counter_wait(const int* p, int target, volatile int* abort,
                                           long long limit_cycles = 4294967296ll) {
   const long long t0 = clock64();
   for (uint32_t it = 0;; ++it) {
