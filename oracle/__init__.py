@@ -80,6 +80,8 @@ class Oracle:
         lib.zs_oracle_brute.argtypes = [dp] * 9 + [i] * 6 + [ctypes.c_double, i, dp, dp, dp]
         lib.zs_oracle_brute.restype = i
         lib.zs_oracle_threads.restype = i
+        lib.zs_oracle_sm.argtypes = [dp] * 7 + [i] * 6 + [ctypes.c_double, i, dp]
+        lib.zs_oracle_sm.restype = i
         lib.zs_oracle_layer_norm.argtypes = [dp] * 3 + [ctypes.c_double, dp] + [i] * 4
         lib.zs_oracle_layer_norm.restype = i
         self.lib = lib
@@ -128,6 +130,22 @@ class Oracle:
         return out, ws, wm
 
 
+    def sm(self, q, k, v, g1, gh, *, causal=True, rope=False, rope_base=10000.0, nthreads=0,
+           g0=None, wsum=False):
+        """ZeroS-SM (the zero-sum reweighting of standard softmax attention), O(N^2 d) fp64.
+        q, k, v [B,H,N,d]; g1, gh, g0 [B,H,N].  Returns ``out``, or ``(out, wsum)``."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, d = q.shape
+        assert k.shape == q.shape and v.shape == q.shape
+        g1, gh, g0 = _gate(g1, (B, H, N)), _gate(gh, (B, H, N)), _gate(g0, (B, H, N))
+        out = np.zeros((B, H, N, d), np.float64)
+        ws = np.zeros((B, H, N), np.float64) if wsum else None
+        if self.lib.zs_oracle_sm(_ptr(q), _ptr(k), _ptr(v), _ptr(g1), _ptr(gh), _ptr(g0),
+                                 _ptr(out), B, H, N, d, int(causal), int(rope),
+                                 float(rope_base), int(nthreads), _ptr(ws)) != 0:
+            raise ValueError("oracle rejected its arguments")
+        return (out, ws) if wsum else out
+
     def layer_norm(self, o, w=None, b=None, eps=1e-5):
         """Output LayerNorm of every head's row over its d channels: o [B,H,N,d]; w, b [H,d]
         (None: gain 1, bias 0).  Returns a new float64 array."""
@@ -163,3 +181,7 @@ def brute(*args, **kw):
 
 def layer_norm(*args, **kw):
     return default().layer_norm(*args, **kw)
+
+
+def sm(*args, **kw):
+    return default().sm(*args, **kw)

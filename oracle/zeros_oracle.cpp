@@ -41,6 +41,8 @@
 //     y = (o_t - mean) / sqrt(var + eps) * w + b with the biased variance, w and b per head
 //     [H,d] (absent: 1 and 0).
 //
+//   * ZeroS-SM (quadratic variant): see sm_one.
+//
 // Parity pins for everything here live in tests/test_oracle_pins.py.
 
 #include <algorithm>
@@ -247,6 +249,55 @@ void brute_one(const Problem& pr, int b, int h, double* out, double* wsum, doubl
   }
 }
 
+// ZeroS-SM, the quadratic variant: the same zero-sum reweighting applied to standard softmax
+// attention ([PN] linear-time prefix scan section: "the same reweighting can be applied to
+// standard softmax attention"; the appendix with its formula is not among the pages).  Reading:
+// the logits are the standard attention logits s_{t,i} = q_t R_{t-i} k_i^T / sqrt d (raw q and
+// k, rotary positions when rope), and every query t has its own softmax, mean logit and
+// zero-sum weights over its keys i:
+//   softmax_{t,i} = e^{s_{t,i}} / sum_j e^{s_{t,j}},  delta_{t,i} = s_{t,i} - (1/t) sum_j s_{t,j},
+//   eps_{t,i} = softmax_{t,i} - 1/t - delta_{t,i}/t,
+//   w_{t,i} = sig^1_t delta_{t,i}/t + sig^h_t eps_{t,i} (+ sig^0_t / t),   o_t = sum_i w_{t,i} v_i
+// (no angular factor: the logits already carry q and k).  Encoder: every key, t := N.
+void sm_one(const Problem& pr, int b, int h, double* out, double* wsum) {
+  const int N = pr.N, d = pr.d;
+  const size_t base = ((size_t)b * pr.H + h) * (size_t)N;
+  const double* q = pr.q + base * d;
+  const double* k = pr.k + base * d;
+  const double* v = pr.v + base * d;
+  std::vector<double> s(N), qr(d);
+  for (int t = 0; t < N; ++t) {
+    const int last = pr.causal ? t : N - 1;
+    const double tc = (double)(last + 1);
+    double m = -INFINITY, P = 0.0;
+    for (int i = 0; i <= last; ++i) {
+      std::copy(q + (size_t)t * d, q + (size_t)(t + 1) * d, qr.begin());
+      if (pr.rope) rotate(qr.data(), d, (double)(t - i), pr.rope_base);
+      double dot = 0.0;
+      for (int a = 0; a < d; ++a) dot += qr[a] * k[(size_t)i * d + a];
+      s[i] = dot / std::sqrt((double)d);
+      m = std::max(m, s[i]);
+      P += s[i];
+    }
+    double E = 0.0;
+    for (int i = 0; i <= last; ++i) E += std::exp(s[i] - m);
+    const double sig1 = sigmoid(pr.g1[base + t]), sigh = sigmoid(pr.gh[base + t]);
+    const double sig0 = pr.g0 ? sigmoid(pr.g0[base + t]) : 0.0;
+    double* ot = out + (base + t) * d;
+    for (int j = 0; j < d; ++j) ot[j] = 0.0;
+    double ws = 0.0;
+    for (int i = 0; i <= last; ++i) {
+      const double soft = std::exp(s[i] - m) / E;
+      const double delta = s[i] - P / tc;
+      const double eps = soft - 1.0 / tc - delta / tc;
+      const double w = sig1 * delta / tc + sigh * eps + sig0 / tc;
+      for (int j = 0; j < d; ++j) ot[j] += w * v[(size_t)i * d + j];
+      ws += w;
+    }
+    if (wsum) wsum[base + t] = ws;
+  }
+}
+
 template <class F>
 void parallel_over_heads(const Problem& pr, int nthreads, F fn) {
   const int total = pr.B * pr.H;
@@ -296,6 +347,20 @@ int zs_oracle_brute(const double* q, const double* k, const double* v, const dou
   if (!valid(pr) || !out) return 1;
   parallel_over_heads(pr, nthreads,
                       [&](int b, int h) { brute_one(pr, b, h, out, wsum, wabsmax); });
+  return 0;
+}
+
+// ZeroS-SM (quadratic variant, see sm_one): q, k, v, out [B,H,N,d]; g1, gh, g0 [B,H,N] (g0
+// nullable); wsum [B,H,N] (nullable) receives sum_i w_{t,i}.  Returns 0, or 1 on bad arguments.
+int zs_oracle_sm(const double* q, const double* k, const double* v, const double* g1,
+                 const double* gh, const double* g0, double* out, int B, int H, int N, int d,
+                 int causal, int rope, double rope_base, int nthreads, double* wsum) {
+  Problem pr{q, k, v, nullptr, g1, gh, nullptr, nullptr, g0, B, H, N, d, causal, rope,
+             rope_base, 0.0};
+  if (!q || !k || !v || !g1 || !gh || !out || B < 0 || H < 0 || N < 0 || d <= 0 ||
+      (rope && d % 2))
+    return 1;
+  parallel_over_heads(pr, nthreads, [&](int b, int h) { sm_one(pr, b, h, out, wsum); });
   return 0;
 }
 

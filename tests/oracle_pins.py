@@ -364,9 +364,89 @@ def pin_layer_norm_first_row(orc):
     assert not np.allclose(y[:, :, 1], np.broadcast_to(b, y[:, :, 1].shape), rtol=0, atol=1e-3)
 
 
+# ---------------------------------------------------------------------------------------------
+# ZeroS-SM: the zero-sum reweighting of standard softmax attention (Paper-Notes, linear-time
+# prefix scan: "the same reweighting can be applied to standard softmax attention"; the
+# two-token contrast v_1 - v_2 of the "current pain points" section).
+def _sm_args(p):
+    return (p["q"], p["k"], p["v"], p["g1"], p["gh"])
+
+
+def _logistic(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def pin_sm_two_token(orc):
+    """Closed form for two tokens: with D = s_{2,1} - s_{2,2}, w_{2,1} = sig1 D/4 +
+    sigh (logistic(D) - 1/2 - D/4) = -w_{2,2}, so o_2 = w_{2,1} (v_1 - v_2); and o_1 = 0."""
+    for seed, rope in ((41, False), (42, True)):
+        p = rand_problem(seed, B=1, H=3, N=2, d=8)
+        o = orc.sm(*_sm_args(p), causal=True, rope=rope, rope_base=100.0)
+        for h in range(3):
+            q, k, v = p["q"][0, h], p["k"][0, h], p["v"][0, h]
+            if rope:
+                q, k = _rope_rows(q, 100.0), _rope_rows(k, 100.0)
+            D = (q[1] @ k[0] - q[1] @ k[1]) / np.sqrt(8)
+            s1, sh = _logistic(p["g1"][0, h, 1]), _logistic(p["gh"][0, h, 1])
+            w21 = s1 * D / 4 + sh * (_logistic(D) - 0.5 - D / 4)
+            assert np.allclose(o[0, h, 1], w21 * (v[0] - v[1]), rtol=0, atol=1e-14)
+            assert np.abs(o[0, h, 0]).max() < 1e-15
+
+
+def pin_sm_equal_gates_softmax(orc):
+    """sig1 = sigh = sig: w = sig (softmax - 1/t): scipy's softmax attention over the masked
+    logits Q K^T / sqrt d (textbook rotary map with rope) minus the mean of the values."""
+    for causal, rope in ((True, False), (False, False), (True, True)):
+        p = rand_problem(43, B=1, H=2, N=30, d=8)
+        p["gh"] = p["g1"].copy()
+        o = orc.sm(*_sm_args(p), causal=causal, rope=rope, rope_base=300.0)
+        N = o.shape[2]
+        for h in range(2):
+            q, k, v = p["q"][0, h], p["k"][0, h], p["v"][0, h]
+            if rope:
+                q, k = _rope_rows(q, 300.0), _rope_rows(k, 300.0)
+            S = q @ k.T / np.sqrt(8)
+            for t in range(N):
+                last = t if causal else N - 1
+                att = softmax(S[t, : last + 1]) @ v[: last + 1]
+                ref = _logistic(p["g1"][0, h, t]) * (att - v[: last + 1].mean(axis=0))
+                assert np.allclose(o[0, h, t], ref, rtol=0, atol=1e-13)
+
+
+def pin_sm_linear_gate_limit(orc):
+    """sigh -> 0: o_t = (sig1/t) sum_i (s_{t,i} - mean_i s_{t,i}) v_i, the centred logits as
+    weights of a linear attention (numpy matrix products)."""
+    p = rand_problem(44, B=1, H=1, N=25, d=8)
+    p["gh"][:] = -40.0
+    o = orc.sm(*_sm_args(p), causal=True)
+    S = p["q"][0, 0] @ p["k"][0, 0].T / np.sqrt(8)
+    for t in range(25):
+        st = S[t, : t + 1]
+        w = _logistic(p["g1"][0, 0, t]) * (st - st.mean()) / (t + 1)
+        assert np.allclose(o[0, 0, t], w @ p["v"][0, 0, : t + 1], rtol=0, atol=1e-13)
+
+
+def pin_sm_zero_sum_and_shift(orc):
+    """The weights of every query sum to zero (plus sig0 with the zero-order gate); adding one
+    vector to every key shifts a query's logits by a constant, which changes nothing."""
+    p = rand_problem(45, B=2, H=2, N=20, d=8)
+    g0 = np.random.default_rng(46).standard_normal(p["g1"].shape)
+    for causal in (True, False):
+        _, ws = orc.sm(*_sm_args(p), causal=causal, wsum=True)
+        assert np.abs(ws).max() < 1e-13
+        _, ws0 = orc.sm(*_sm_args(p), causal=causal, wsum=True, g0=g0)
+        assert np.allclose(ws0, _logistic(g0), rtol=0, atol=1e-13)
+        a = orc.sm(*_sm_args(p), causal=causal)
+        p2 = dict(p, k=p["k"] + np.random.default_rng(47).standard_normal(8))
+        b = orc.sm(*_sm_args(p2), causal=causal)
+        assert relerr(b, a) < 1e-10
+
+
 ALL_PINS = [pin_golden_two_token, pin_brute_vs_recurrent, pin_zero_sum, pin_first_output_zero,
             pin_lemma_3_4, pin_two_token_collinear, pin_constant_logits, pin_equal_gates_softmax,
             pin_equal_gates_softmax_rope, pin_linear_gate_limit, pin_rope_relative, pin_scale_and_linearity, pin_prior_limits,
             pin_prefix_sums,
             pin_zero_order_sum, pin_zero_order_uniform, pin_zero_order_linearity,
-            pin_layer_norm_moments, pin_layer_norm_library, pin_layer_norm_first_row]
+            pin_layer_norm_moments, pin_layer_norm_library, pin_layer_norm_first_row,
+            pin_sm_two_token, pin_sm_equal_gates_softmax, pin_sm_linear_gate_limit,
+            pin_sm_zero_sum_and_shift]

@@ -31,10 +31,13 @@ MUTATIONS = [
     ("beta sign", "const double beta = (sig1 - sigh) / tcount;",
      "const double beta = (sigh - sig1) / tcount;"),
     ("transposed F update", "F[(size_t)a * d + j] += es * kv;", "F[(size_t)j * d + a] += es * kv;"),
-    ("brute eps drops delta", "const double eps = soft - 1.0 / tc - delta / tc;",
-     "const double eps = soft - 1.0 / tc;"),
-    ("brute delta sign", "const double delta = s[i] - P / tc;",
-     "const double delta = P / tc - s[i];"),
+    ("brute eps drops delta", "const double eps = soft - 1.0 / tc - delta / tc;\n      const double w_zs",
+     "const double eps = soft - 1.0 / tc;\n      const double w_zs"),
+    ("brute delta sign",
+     "const double delta = s[i] - P / tc;\n      const double eps = soft - 1.0 / tc - delta / tc;"
+     "\n      const double w_zs",
+     "const double delta = P / tc - s[i];\n      const double eps = soft - 1.0 / tc - delta / tc;"
+     "\n      const double w_zs"),
     ("encoder prior uses N+1", "ubar[a] = (et * mu[a] + S[a]) / (et + N);",
      "ubar[a] = (et * mu[a] + S[a]) / (et + N + 1);"),
     ("zero-order term dropped", "(gamma + zero_order) * Hs[e]", "gamma * Hs[e]"),
@@ -45,13 +48,25 @@ MUTATIONS = [
     ("layer norm eps outside sqrt", "1.0 / std::sqrt(var + eps)", "1.0 / (std::sqrt(var) + eps)"),
     ("layer norm head index", "const int h = (int)((r / N) % H);", "const int h = (int)(r % H);"),
     ("layer norm bias dropped", "* inv * gain + bias;", "* inv * gain;"),
+    ("sm logit scale", "s[i] = dot / std::sqrt((double)d);", "s[i] = dot / d;"),
+    ("sm delta without the mean",
+     "const double delta = s[i] - P / tc;\n      const double eps = soft - 1.0 / tc - delta / tc;"
+     "\n      const double w = sig1",
+     "const double delta = s[i];\n      const double eps = soft - 1.0 / tc - delta / tc;"
+     "\n      const double w = sig1"),
+    ("sm eps drops delta", "const double eps = soft - 1.0 / tc - delta / tc;\n      const double w = sig1",
+     "const double eps = soft - 1.0 / tc;\n      const double w = sig1"),
+    ("sm rotary direction", "rotate(qr.data(), d, (double)(t - i), pr.rope_base);\n      double dot",
+     "rotate(qr.data(), d, (double)(i - t), pr.rope_base);\n      double dot"),
+    ("sm t off by one", "const int last = pr.causal ? t : N - 1;\n    const double tc = (double)(last + 1);\n    double m",
+     "const int last = pr.causal ? t : N - 1;\n    const double tc = (double)(last + 2);\n    double m"),
 ]
 
 
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_mutation_is_caught(name, old, new):
     src = open(SRC).read()
-    assert src.count(old) >= 1, f"mutation anchor not found: {name}"
+    assert src.count(old) == 1, f"mutation anchor not found or not unique: {name}"
     mutated = src.replace(old, new, 1)
     with tempfile.TemporaryDirectory() as tmp:
         cpp = os.path.join(tmp, "mut.cpp")
