@@ -1,7 +1,7 @@
 """Benchmark of the ZeroS causal forward: B8 H8 N4096 d64, bf16, RoPE, one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload causal|encoder|long|decode] [--path auto|simt|chunk]
+                    [--workload causal|encoder|long|decode|sm] [--path auto|simt|chunk]
                     [--pass fwd|bwd] [--ln]
 
 One step = one pass of the whole hot path (logits, prefix scans, zero-sum weights, angular
@@ -39,6 +39,7 @@ WORKLOADS = {
     "encoder": zi.ENCODER_VIT_B256H3N197D64,
     "long": zi.LONG_ROPE_B2H16N65536D128,
     "decode": zi.DECODE_B256H32D128,
+    "sm": zi.CAUSAL_ROPE_B8H8N4096D64,  # ZeroS-SM on the causal RoPE workload's q, k, v, gates
 }
 L2_FLUSH_BYTES = 256 << 20
 
@@ -491,6 +492,131 @@ def ours_backward(args, w: zi.Workload):
             "gpu_launches": launches, "clocks": clk}))
 
 
+def sm_flops(w: zi.Workload) -> float:
+    """Algorithmic flops of ZeroS-SM: the logits Q K^T and the weighted sum W V over the visible
+    (query, key) pairs, 2 d flops per pair each (causal: N (N + 1) / 2 pairs per sequence)."""
+    pairs = w.N * (w.N + 1) / 2 if w.causal else float(w.N) * w.N
+    return w.B * w.H * pairs * 4.0 * w.d
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def ours_sm(args, w: zi.Workload):
+    """ZeroS-SM, the quadratic variant (zeros_sm_fwd): one step = one forward of the batch."""
+    world, rank, local = dist_setup()
+    import zero_sum_prefix_gb300 as zs
+    zs.load()
+    dev = torch.device("cuda", local)
+    inp = zi.make(w, dev)
+    names = ("q", "k", "v", "g1", "gh")
+    out = torch.empty_like(inp["q"])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(src):
+        return zs.sm_fwd(*(src[n] for n in names), causal=w.causal, rope=w.rope,
+                         rope_base=w.rope_base, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1.0)
+        step(inp)
+    torch.cuda.synchronize()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    l0 = zs.kernel_launches()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step(inp)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    launches = zs.kernel_launches() - l0
+    barrier(world)
+    clk = clocks.stop()
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    tokens = w.B * w.N
+    value, ms = aggregate_rate(tokens, sum(per) / len(per), world)
+    peak, kind = bf16_peak()
+    achieved = sm_flops(w) / (ms / 1e3) / 1e12
+
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(inp[n]) for n in names}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n in names:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        host_out.copy_(step(dev_in), non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        toks = min(w.N, 1024)
+        sel = {n: inp[n][:1, :, :toks].cpu() for n in names}
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.sm(*(sel[n] for n in names), causal=w.causal, rope=w.rope,
+                      rope_base=w.rope_base, nthreads=oracle.threads())
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 1.5 or reps >= 20:
+                break
+        cpu = {"value": toks * reps / dt, "unit": "tokens/s",
+               "cores": min(oracle.threads(), w.H), "kind": "oracle",
+               "sample": f"batch 1 (all {w.H} heads) x first {toks} tokens, fp64 O(N^2) "
+                         f"oracle, {reps} passes ({dt:.1f} s wall)"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": f"ZeroS-SM fwd tokens/s ({w.name})", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "rope": w.rope, "variant": "ZeroS-SM",
+                       "l2": "flushed before every step (256 MB write, outside the events)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": kind, "algorithmic_flops_per_launch": sm_flops(w)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clk}))
+
+
 def ours_decode(args, w: zi.Workload):
     """Recurrent decode: prefill 8192 tokens (zeros_fwd_ex final_state), then time decode
     steps; one step advances all B x H sequences by one token."""
@@ -581,6 +707,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, w)
+    elif args.workload == "sm":
+        ours_sm(args, w)
     elif args.pass_ == "bwd":
         ours_backward(args, w)
     elif args.workload == "decode":

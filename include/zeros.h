@@ -119,6 +119,24 @@ int zeros_fwd_ln(const void* q, const void* k, const void* v, const void* u, con
                  void* final_state, void* stream);
 
 /*
+ * ZeroS-SM, the quadratic variant (Paper-Notes "ZeroS", linear-time prefix scan: the same
+ * zero-sum reweighting applied to standard softmax attention; its formula sits in an appendix
+ * the pages do not include).  Reading: logits s_{t,i} = q_t k_i^T / sqrt(d) with raw q, k
+ * (rotated to their positions when rope = 1), and per query t over its keys i (i <= t when
+ * causal = 1, every key with t := N when causal = 0)
+ *   w_{t,i} = sig1_t delta_{t,i}/t + sigh_t eps_{t,i} (+ sig0_t/t),  o_t = sum_i w_{t,i} v_i,
+ *   delta_{t,i} = s_{t,i} - (1/t) sum_j s_{t,j},  eps_{t,i} = softmax_{t,i} - 1/t - delta_{t,i}/t.
+ *   q, k, v, out : [B, H, N, d] bf16 (dtype must be ZEROS_BF16), d in {64, 128}
+ *   g1, gh, g0   : fp32 [B, H, N] gate logits (g0 nullable: the zero-order gate)
+ *   N <= 8388480.  O(N^2 d) work on the tensor cores; with rope = 1 the library rotates q and k
+ *   into a per-device scratch of 4*B*H*N*d bytes (grown on demand; growing it waits for the
+ *   device) and keeps a rotary table as zeros_fwd_ex does.
+ */
+int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, const float* gh,
+                 const float* g0, void* out, int B, int H, int N, int d, int causal, int rope,
+                 int dtype, float rope_base, void* stream);
+
+/*
  * Allocation-free forward (the pages have no counterpart: this entry point exists for callers
  * that must not allocate device memory themselves or through this library, for example code
  * whose device memory is all handed out up front by its own allocator, or a runtime that forbids

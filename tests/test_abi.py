@@ -106,3 +106,16 @@ def test_host_validation_without_gpu(lib):
     assert fwd_ln(d=48) == zs.ZEROS_ERR_UNSUPPORTED
     assert lib.zeros_decode_step_ln(p, 1, 1, 64, *([p] * 6), None, None, None, 1e-5, p,
                                     None) == zs.ZEROS_ERR_INVALID
+    # ZeroS-SM: bf16 and d in {64, 128} only; the usual argument checks
+    def sm(d=64, dtype=0, ptr=16, rope=0, base=1e4, N=8, causal=1):
+        x = ctypes.c_void_p(ptr) if ptr is not None else None
+        return lib.zeros_sm_fwd(x, x, x, x, x, None, x, 1, 1, N, d, causal, rope, dtype, base,
+                                None)
+    assert sm(d=32) == zs.ZEROS_ERR_UNSUPPORTED
+    assert sm(dtype=1) == zs.ZEROS_ERR_UNSUPPORTED
+    assert sm(ptr=None) == zs.ZEROS_ERR_INVALID
+    assert sm(ptr=40) == zs.ZEROS_ERR_INVALID
+    assert sm(rope=1, base=0.0) == zs.ZEROS_ERR_INVALID
+    assert sm(causal=3) == zs.ZEROS_ERR_INVALID
+    assert sm(N=65535 * 128 + 1) == zs.ZEROS_ERR_UNSUPPORTED
+    assert sm(ptr=None, N=0) == zs.ZEROS_OK

@@ -29,7 +29,7 @@ EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
            "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd", "zeros_fwd_ln",
-           "zeros_decode_step_ln"]
+           "zeros_decode_step_ln", "zeros_sm_fwd"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,8 @@ def load():
         lib.zeros_fwd_ln.restype = i
         lib.zeros_decode_step_ln.argtypes = [vp, i, i, i] + [vp] * 9 + [f, vp, vp]
         lib.zeros_decode_step_ln.restype = i
+        lib.zeros_sm_fwd.argtypes = [vp] * 7 + [i] * 7 + [f, vp]
+        lib.zeros_sm_fwd.restype = i
         lib.zeros_fwd_noalloc.restype = i
         _lib = lib
         return lib
@@ -185,6 +187,27 @@ def fwd(q, k, v, u, g1, gh, mu, tau, *, causal=True, rope=False, rope_base=10000
                           _stream(stream))
     _check(rc, "zeros_fwd_ex")
     return (out, dbg) if debug else out
+
+
+def sm_fwd(q, k, v, g1, gh, *, causal=True, rope=False, rope_base=10000.0, g0=None, out=None,
+           stream=None):
+    """ZeroS-SM (the zero-sum reweighting of standard softmax attention): q, k, v [B, H, N, d]
+    bf16, d in {64, 128}; g1, gh (g0 optional) [B, H, N] fp32.  Returns ``out`` (bf16)."""
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, (B, H, N, d), torch.bfloat16)
+    _need(g1, "g1", (B, H, N), torch.float32)
+    _need(gh, "gh", (B, H, N), torch.float32)
+    if g0 is not None:
+        _need(g0, "g0", (B, H, N), torch.float32)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (B, H, N, d), torch.bfloat16)
+    rc = load().zeros_sm_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g1), _ptr(gh), _ptr(g0), _ptr(out),
+                             B, H, N, d, int(bool(causal)), int(bool(rope)), ZEROS_BF16,
+                             float(rope_base), _stream(stream))
+    _check(rc, "zeros_sm_fwd")
+    return out
 
 
 def bwd(q, k, v, u, g1, gh, mu, tau, dout, *, rope=False, rope_base=10000.0, g0=None,

@@ -32,6 +32,8 @@ struct DeviceWorkspace {
   int* status = nullptr;
   float* bwd = nullptr;  // backward scratch (per-token scalars and prior means)
   size_t bwd_bytes = 0;
+  void* sm = nullptr;     // ZeroS-SM scratch (rotated q and k)
+  size_t sm_bytes = 0;
   float2* rope = nullptr;
   size_t rope_entries = 0;  // capacity in float2
   int rope_N = 0, rope_d = 0;
@@ -118,6 +120,25 @@ int bwd_scratch(DeviceWorkspace* ws, size_t bytes, float** out) {
     ws->bwd_bytes = bytes;
   }
   *out = ws->bwd;
+  return ZEROS_OK;
+}
+
+// ZeroS-SM scratch of at least `bytes` (grown like the backward scratch).
+int sm_scratch(DeviceWorkspace* ws, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (bytes > ws->sm_bytes) {
+    if (ws->sm) {
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+      cudaFree(ws->sm);
+    }
+    ws->sm = nullptr;
+    ws->sm_bytes = 0;
+    cudaError_t e = cudaMalloc(&ws->sm, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(ZeroS-SM scratch)");
+    ws->sm_bytes = bytes;
+  }
+  *out = ws->sm;
   return ZEROS_OK;
 }
 
@@ -588,6 +609,62 @@ int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const 
   }
   e = launch_bwd(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ZEROS_OK;
+}
+
+int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, const float* gh,
+                 const float* g0, void* out, int B, int H, int N, int d, int causal, int rope,
+                 int dtype, float rope_base, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_dims(B, H, N, d)) return rc;
+  if (int rc = check_dtype(dtype)) return rc;
+  if (causal != 0 && causal != 1) return fail(ZEROS_ERR_INVALID, "causal must be 0 or 1");
+  if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
+  if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
+  if (!sm_supported(d, dtype))
+    return fail(ZEROS_ERR_UNSUPPORTED, "ZeroS-SM needs bf16 inputs and d in {64, 128}");
+  if (N > 65535 * 128) return fail(ZEROS_ERR_UNSUPPORTED, "ZeroS-SM needs N <= 8388480");
+  const bool empty = (long long)B * H * N == 0;
+  const char* names[] = {"q", "k", "v", "g1", "gh", "out"};
+  const void* ptrs[] = {q, k, v, g1, gh, out};
+  if (!empty)
+    for (int i = 0; i < 6; ++i)
+      if (int rc = check_ptr(ptrs[i], names[i])) return rc;
+  if (int rc = check_opt_ptr(g0, "g0")) return rc;
+  if (empty) return ZEROS_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceWorkspace* ws;
+  if (int rc = workspace(&ws)) return rc;
+  SmArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g1 = g1;
+  a.gh = gh;
+  a.g0 = g0;
+  a.out = out;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.status = ws->status;
+  if (rope) {  // rotate q and k once into the library's scratch
+    const size_t each = (size_t)B * H * N * d * 2;
+    void* buf = nullptr;
+    if (int rc = sm_scratch(ws, 2 * each, &buf)) return rc;
+    const float2* table = nullptr;
+    if (int rc = rope_table(ws, N, d, rope_base, st, &table)) return rc;
+    void* qr = buf;
+    void* kr = static_cast<uint8_t*>(buf) + each;
+    cudaError_t e = launch_sm_rotate(q, qr, table, B * H, N, d, st);
+    if (e == cudaSuccess) e = launch_sm_rotate(k, kr, table, B * H, N, d, st);
+    if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
+    a.q = qr;
+    a.k = kr;
+  }
+  cudaError_t e = launch_sm(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ZeroS-SM launch");
   return ZEROS_OK;
 }
 

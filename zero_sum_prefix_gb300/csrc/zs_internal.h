@@ -53,6 +53,16 @@ struct BwdArgs {
   int* status;
 };
 
+// ZeroS-SM (quadratic variant): bf16 q, k (already rotated when rotary positions are used),
+// v [B,H,N,d]; fp32 gates [B,H,N]; bf16 out.
+struct SmArgs {
+  const void *q, *k, *v;
+  const float *g1, *gh, *g0;  // g0 nullable
+  void* out;
+  int B, H, N, d, causal;
+  int* status;
+};
+
 // Counts every kernel launch the library issues (zs_api.cu).
 void count_launches(unsigned n);
 
@@ -79,5 +89,11 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // zs_decode.cu
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// zs_sm.cu
+bool sm_supported(int d, int dtype);
+cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream);
+cudaError_t launch_sm_rotate(const void* x, void* y, const float2* table, int BH, int N, int d,
+                             cudaStream_t stream);
 
 }  // namespace zs

@@ -1,0 +1,493 @@
+// ZeroS-SM: the zero-sum reweighting applied to standard softmax attention (the quadratic
+// variant).  Paper-Notes "ZeroS: Zero-Sum Linear Attention for Efficient Transformers", method
+// details / linear-time prefix scan ("the same reweighting can be applied to standard softmax
+// attention"), experiments (ZeroS-SM rows of the MAD and WikiText-103 tables).  The pages do not
+// print its formula; the reading implemented here: logits s_{t,i} = q_t k_i^T / sqrt d (rotary
+// positions when asked), and per query t over its keys i (i <= t, or every key in encoder mode,
+// where t := N):
+//   w_{t,i} = sig1_t delta_{t,i}/t + sigh_t eps_{t,i} (+ sig0_t/t),
+//   delta_{t,i} = s_{t,i} - P_t/t,  eps_{t,i} = e^{s_{t,i}}/E_t - 1/t - delta_{t,i}/t,
+// with P_t = sum_i s_{t,i} and E_t = sum_i e^{s_{t,i}}.  Expanding,
+//   w_{t,i} = alpha_t e^{s_{t,i} - m_t} + beta_t s_{t,i} + gamma_t,
+//   alpha_t = sigh_t / (E_t e^{-m_t}),  beta_t = (sig1_t - sigh_t)/t,
+//   gamma_t = -beta_t P_t/t - sigh_t/t (+ sig0_t/t),                 o_t = sum_i w_{t,i} v_i.
+//
+// Kernel (one CTA per 128-query tile of one (b, h), heaviest causal tiles first): two passes
+// over the key tiles.  Pass 1 computes S = Q K^T on the tensor cores (tcgen05.mma, accumulator
+// in TMEM) and, per query row, the running maximum, the scaled exp-sum and the logit sum.  Pass 2
+// recomputes S, forms W in fp32 from the final row statistics (the three terms nearly cancel,
+// since the weights sum to zero, so W is rounded to bf16 only once, as a whole), writes it to
+// TMEM and accumulates O += W V with W as the TMEM A operand.  Two epilogue warpgroups take the
+// even and odd key tiles (two S buffers, two W buffers), so the exponentials of one tile overlap
+// the other's; the row statistics of the two halves are merged between the passes.
+//
+// Warps: 0 = TMA producer (Q once; K per pass-1 tile; K and V per pass-2 tile, through a ring
+// of stages), 1 = TMEM allocation and the single MMA-issuing thread, 4-7 and 8-11 = epilogue
+// warpgroups (TMEM lane quadrant = warp % 4, one query row per thread).  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "zs_common.cuh"
+#include "zs_internal.h"
+#include "zs_sm100.cuh"
+
+namespace zs {
+namespace {
+
+using namespace sm100;
+
+constexpr int kT = 128;                  // query rows per CTA, keys per tile
+constexpr int kSmThreads = 384;          // 12 warps
+constexpr uint32_t kAtom = 128 * 128;    // one [128 x 64] bf16 tile, 128-byte swizzle
+
+template <int D>
+struct SmCfg {
+  static constexpr int KA = D / 64;                        // atom tiles along d
+  static constexpr int NS = (D == 64) ? 4 : 3;             // K/V stages
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t STAGE_OFF = Q_OFF + KA * kAtom;
+  static constexpr uint32_t STAGE = 2 * KA * kAtom;        // K then V
+  static constexpr uint32_t STAT_OFF = STAGE_OFF + NS * STAGE;  // float4 [128] row stats
+  static constexpr uint32_t MISC_OFF = STAT_OFF + kT * 16;
+  static constexpr uint32_t BYTES = MISC_OFF + 256;
+  static_assert(BYTES <= 232448, "shared memory budget of one CTA");
+  // TMEM columns: S buffers, output accumulator, W buffers (bf16 pairs)
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_W0 = 384, TM_W1 = 448;
+};
+
+struct SmMisc {
+  uint64_t q_full;
+  uint64_t kv_full[4], kv_empty[4];
+  uint64_t s_full[2], s_free[2], w_full[2], w_free[2];
+  uint64_t o_full, fin;
+  uint32_t tmem;
+  int abort;
+  int never;
+};
+static_assert(sizeof(SmMisc) <= 256, "SmMisc fits its slot");
+
+struct SmParams {
+  CUtensorMap tq, tk, tv;  // [B*H, N, d] bf16, box {64, 128, 1}, 128-byte swizzle
+  SmArgs a;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Number of key tiles a query tile visits and the key count t of each row.
+__device__ __forceinline__ int key_tiles(const SmArgs& a, int qt) {
+  return a.causal ? qt + 1 : (a.N + kT - 1) / kT;
+}
+
+// Index of pass-2 item g among the pass-2 items of the same buffer (g & 1); J = key tiles.
+__device__ __forceinline__ int p2_index(int g, int J) {
+  const int first = J + ((J ^ g) & 1);
+  return (g - first) >> 1;
+}
+
+// ------------------------------------------------------------------------------ producer
+template <int D>
+__device__ void sm_producer(const SmParams& p, uint8_t* smem, SmMisc* ms, int bh, int qt, int J) {
+  using CF = SmCfg<D>;
+  const uint32_t base = smem_u32(smem);
+  mbar_arrive_expect_tx(&ms->q_full, CF::KA * kAtom);
+#pragma unroll
+  for (int at = 0; at < CF::KA; ++at)
+    tma_load_3d(base + CF::Q_OFF + at * kAtom, &p.tq, 64 * at, qt * kT, bh, &ms->q_full);
+  for (int g = 0; g < 2 * J; ++g) {
+    const int st = g % CF::NS;
+    if (g >= CF::NS && !mbar_wait(&ms->kv_empty[st], ((g / CF::NS) - 1) & 1, &ms->abort)) {
+      report(p.a.status, kErrTimeout);
+      ms->abort = 1;
+      return;
+    }
+    const bool pass2 = g >= J;
+    const int j = pass2 ? g - J : g;
+    const uint32_t kt = base + CF::STAGE_OFF + st * CF::STAGE;
+    mbar_arrive_expect_tx(&ms->kv_full[st], (pass2 ? 2 : 1) * CF::KA * kAtom);
+#pragma unroll
+    for (int at = 0; at < CF::KA; ++at)
+      tma_load_3d(kt + at * kAtom, &p.tk, 64 * at, j * kT, bh, &ms->kv_full[st]);
+    if (pass2) {
+#pragma unroll
+      for (int at = 0; at < CF::KA; ++at)
+        tma_load_3d(kt + (CF::KA + at) * kAtom, &p.tv, 64 * at, j * kT, bh, &ms->kv_full[st]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ void sm_mma(const SmArgs& a, uint8_t* smem, SmMisc* ms, int J) {
+  using CF = SmCfg<D>;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t tm = ms->tmem;
+  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
+  constexpr uint32_t id_ov = idesc_bf16_f32(128, D, false, true);      // O += W V
+  // O += W V for the pass-2 item g (W from TMEM, V MN-major in its stage)
+  auto issue_wv = [&](int g) -> bool {
+    const int b = g & 1, j = g - J;
+    if (!mbar_wait(&ms->w_full[b], p2_index(g, J) & 1, &ms->abort)) return false;
+    tc_fence_after();
+    const uint32_t vt = base + CF::STAGE_OFF + (g % CF::NS) * CF::STAGE + CF::KA * kAtom;
+    const uint32_t tw = tm + (b ? CF::TM_W1 : CF::TM_W0);
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk)
+      mma_bf16_ts(tm + CF::TM_O, tw + kk * 8, sw128_desc(vt + kk * 2048, kAtom, 1024), id_ov,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+    mma_commit(&ms->w_free[b]);
+    mma_commit(&ms->kv_empty[g % CF::NS]);
+    return true;
+  };
+  bool ok = mbar_wait(&ms->q_full, 0, &ms->abort);
+  for (int g = 0; g < 2 * J && ok; ++g) {
+    const int st = g % CF::NS, b = g & 1;
+    ok = mbar_wait(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort);
+    if (ok && g >= 2) ok = mbar_wait(&ms->s_free[b], ((g >> 1) - 1) & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t qs = base + CF::Q_OFF, ks = base + CF::STAGE_OFF + st * CF::STAGE;
+    const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk / 4) * kAtom + (kk % 4) * 32;
+      mma_bf16(ts, sw128_desc(qs + off, 16, 1024), sw128_desc(ks + off, 16, 1024), id_qk,
+               kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&ms->s_full[b]);
+    if (g < J) mma_commit(&ms->kv_empty[st]);  // pass 1 reads K only
+    if (g >= J + 1) ok = issue_wv(g - 1);      // the previous tile's W is due by now
+  }
+  if (ok && J > 0) ok = issue_wv(2 * J - 1);
+  if (ok) mma_commit(&ms->o_full);
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+  }
+  mma_commit(&ms->fin);
+}
+
+// ------------------------------------------------------------------------------ epilogue
+// Warpgroup w (0 or 1) handles the key tiles of parity w in both passes; thread = query row.
+template <int D>
+__device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, int qt, int J,
+                            int w) {
+  using CF = SmCfg<D>;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int r = wq * 32 + (threadIdx.x & 31);
+  const uint32_t tl = ms->tmem + ((uint32_t)(wq * 32) << 16);
+  const uint32_t ts = tl + (w ? CF::TM_S1 : CF::TM_S0);
+  const uint32_t tw = tl + (w ? CF::TM_W1 : CF::TM_W0);
+  const int t = qt * kT + r;                      // query index (0-based)
+  const bool row_ok = t < a.N;
+  const size_t row = (size_t)bh * a.N + t;
+  const int lim = a.causal ? t : a.N - 1;         // last key of this query
+  const float tc = a.causal ? (float)(t + 1) : (float)a.N;
+  const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+  const float c2 = 1.4426950408889634f * inv_sqrt_d;  // log2(e) / sqrt(d): exponent in base 2
+  bool ok = true;
+
+  // ---- pass 1: running maximum (base-2 units), scaled exp-sum and logit sum ----
+  float m2 = -INFINITY, l = 0.0f, P = 0.0f;
+  for (int g = w; g < J && ok; g += 2) {
+    ok = mbar_wait_warp(&ms->s_full[w], (g >> 1) & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const int k0 = g * kT;
+    const bool full = k0 + kT - 1 <= lim;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      float v[32];
+      tmem_ld32(ts + 32 * ch, v);
+      float cm = -INFINITY, cs = 0.0f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const bool valid = full || k0 + 32 * ch + x <= lim;
+        if (valid) {
+          cm = fmaxf(cm, v[x]);
+          cs += v[x];
+        }
+      }
+      if (cm == -INFINITY) continue;  // no key of this chunk is visible to the row
+      const float mn = fmaxf(m2, cm * c2);
+      float acc = 0.0f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const bool valid = full || k0 + 32 * ch + x <= lim;
+        if (valid) acc += ex2(fmaf(v[x], c2, -mn));
+      }
+      l = fmaf(l, ex2(m2 - mn), acc);
+      m2 = mn;
+      P += cs;
+    }
+    tc_fence_before();
+    mbar_arrive(&ms->s_free[w]);
+  }
+  if (!ok) ms->abort = 1;
+  // ---- merge the two halves' statistics: warpgroup 0 publishes its row's, warpgroup 1
+  // merges and publishes the result (both warpgroups reach both barriers) ----
+  float4* stat = reinterpret_cast<float4*>(smem + CF::STAT_OFF);
+  if (w == 0) stat[r] = make_float4(m2, l, P, 0.0f);
+  named_bar_sync(1, 256);
+  if (w == 1) {
+    const float4 o = stat[r];
+    if (o.x != -INFINITY) {
+      const float mn = fmaxf(m2, o.x);
+      l = l * ex2(m2 - mn) + o.y * ex2(o.x - mn);
+      m2 = mn;
+    }
+    P += o.z;
+    stat[r] = make_float4(m2, l, P, 0.0f);
+  }
+  named_bar_sync(1, 256);
+  if (w == 0) {
+    const float4 o = stat[r];
+    m2 = o.x;
+    l = o.y;
+    P = o.z;
+  }
+  if (ms->abort) return;
+
+  // ---- coefficients of the row: w = alpha 2^{c2 raw - m2} + bs raw + gamma ----
+  float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
+  if (row_ok) {
+    sig1 = sigmoid(a.g1[row]);
+    sigh = sigmoid(a.gh[row]);
+    if (a.g0) sig0 = sigmoid(a.g0[row]);
+  }
+  const float rt = 1.0f / tc;
+  const float alpha = sigh / l;
+  const float beta = (sig1 - sigh) * rt;
+  const float bs = beta * inv_sqrt_d;
+  const float gamma = fmaf(-beta * P * inv_sqrt_d, rt, (sig0 - sigh) * rt);
+
+  // ---- pass 2: W tiles (bf16, rounded once) for the O += W V products ----
+  for (int g = J + ((J ^ w) & 1); g < 2 * J && ok; g += 2) {
+    const int n = p2_index(g, J), j = g - J;
+    ok = mbar_wait_warp(&ms->s_full[w], (g >> 1) & 1, &ms->abort);
+    if (ok && n >= 1) ok = mbar_wait_warp(&ms->w_free[w], (n - 1) & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const int k0 = j * kT;
+    const bool full = k0 + kT - 1 <= lim;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      float v[32];
+      tmem_ld32(ts + 32 * ch, v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int y = 0; y < 16; ++y) {
+        float wv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int x = 2 * y + e;
+          const bool valid = full || k0 + 32 * ch + x <= lim;
+          wv[e] = valid ? fmaf(alpha, ex2(fmaf(v[x], c2, -m2)), fmaf(bs, v[x], gamma)) : 0.0f;
+        }
+        pk[y] = pack_bf16x2(wv[0], wv[1]);
+      }
+      tmem_st16_nowait(tw + 16 * ch, pk);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&ms->s_free[w]);
+    mbar_arrive(&ms->w_full[w]);
+  }
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+    return;
+  }
+  // ---- output: warpgroup w writes columns [w D/2, (w + 1) D/2) of its rows ----
+  if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort)) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+    return;
+  }
+  tc_fence_after();
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+  for (int cb = 0; cb < D / 64; ++cb) {
+    const int c0 = w * (D / 2) + 32 * cb;
+    float v[32];
+    tmem_ld32(tl + CF::TM_O + c0, v);
+    if (row_ok) {
+      uint4* dst = reinterpret_cast<uint4*>(out + row * D + c0);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        dst[q4] = make_uint4(pack_bf16x2(v[8 * q4 + 0], v[8 * q4 + 1]),
+                             pack_bf16x2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                             pack_bf16x2(v[8 * q4 + 4], v[8 * q4 + 5]),
+                             pack_bf16x2(v[8 * q4 + 6], v[8 * q4 + 7]));
+    }
+  }
+}
+
+// ============================================================================ kernel
+template <int D>
+__global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant__ SmParams p) {
+  using CF = SmCfg<D>;
+  const SmArgs& a = p.a;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report(a.status, kErrUnsupported);
+    return;
+  }
+  SmMisc* ms = reinterpret_cast<SmMisc*>(smem + CF::MISC_OFF);
+  const int warp = threadIdx.x >> 5;
+  const int nqt = (a.N + kT - 1) / kT;
+  // every sequence's heaviest (last) causal query tile first, then the next lighter ones
+  const int qt = a.causal ? nqt - 1 - (int)blockIdx.y : (int)blockIdx.y;
+  const int bh = blockIdx.x;
+  const int J = key_tiles(a, qt);
+  if (threadIdx.x == 0) {
+    mbar_init(&ms->q_full, 1);
+    for (int i = 0; i < CF::NS; ++i) {
+      mbar_init(&ms->kv_full[i], 1);
+      mbar_init(&ms->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->s_free[i], 128);
+      mbar_init(&ms->w_full[i], 128);
+      mbar_init(&ms->w_free[i], 1);
+    }
+    mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->fin, 1);
+    ms->abort = 0;
+    ms->never = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(&ms->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) sm_producer<D>(p, smem, ms, bh, qt, J);
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) sm_mma<D>(a, smem, ms, J);
+  } else if (warp >= 4) {
+    sm_epilogue<D>(a, smem, ms, bh, qt, J, (warp - 4) >> 2);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    // every MMA has completed once `fin` fires (it is committed after the last one)
+    if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
+    tc_fence_after();
+    tmem_dealloc(ms->tmem, 512);
+  }
+}
+
+// Rotary map of bf16 rows [BH, N, d] (half-split pairs, token n at position n) into `y`, with
+// the fp64-built (cos, sin) table [N][d/2]; the rotated values are rounded to bf16 once.
+__global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                                 const float2* __restrict__ table, int N, int d, size_t pairs) {
+  const int half = d / 2;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < pairs;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int a = (int)(i % half);
+    const size_t rowi = i / half;  // (bh, n)
+    const int n = (int)(rowi % N);
+    const float2 cs = table[(size_t)n * half + a];
+    const size_t o = rowi * d + a;
+    const float xa = __bfloat162float(x[o]), xb = __bfloat162float(x[o + half]);
+    y[o] = __float2bfloat16_rn(__fmaf_rn(xa, cs.x, -xb * cs.y));
+    y[o + half] = __float2bfloat16_rn(__fmaf_rn(xa, cs.y, xb * cs.x));
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn sm_encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (!f) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(ptr);
+      fn.store(f);
+    }
+  }
+  return f;
+}
+
+// [B*H, N, d] bf16 viewed as 3-D (d fastest), boxes {64, 128, 1}, 128-byte swizzle; rows past N
+// read as zeros.
+bool sm_map(CUtensorMap* m, const void* ptr, int d, int N, int BH) {
+  EncodeTiledFn f = sm_encode_fn();
+  if (!f) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kT, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_sm_d(const SmArgs& a, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_set{0};  // bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(sm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SmCfg<D>::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  SmParams p;
+  p.a = a;
+  const int BH = a.B * a.H;
+  if (!sm_map(&p.tq, a.q, D, a.N, BH) || !sm_map(&p.tk, a.k, D, a.N, BH) ||
+      !sm_map(&p.tv, a.v, D, a.N, BH))
+    return cudaErrorNotSupported;
+  const dim3 grid(BH, (a.N + kT - 1) / kT, 1);
+  sm_kernel<D><<<grid, kSmThreads, SmCfg<D>::BYTES, stream>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool sm_supported(int d, int dtype) { return dtype == 0 && (d == 64 || d == 128); }
+
+cudaError_t launch_sm_rotate(const void* x, void* y, const float2* table, int BH, int N, int d,
+                             cudaStream_t stream) {
+  const size_t pairs = (size_t)BH * N * (d / 2);
+  if (pairs == 0) return cudaSuccess;
+  const int blocks = (int)((pairs + 255) / 256 < 152 * 16 ? (pairs + 255) / 256 : 152 * 16);
+  sm_rotate_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                               static_cast<__nv_bfloat16*>(y), table, N, d, pairs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_sm_d<64>(a, stream);
+  if (a.d == 128) return launch_sm_d<128>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace zs
