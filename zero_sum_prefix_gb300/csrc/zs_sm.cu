@@ -189,6 +189,9 @@ __device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, 
   const bool row_ok = t < a.N;
   const size_t row = (size_t)bh * a.N + t;
   const int lim = a.causal ? t : a.N - 1;         // last key of this query
+  // last key visible to every row of this warp: a tile is unmasked for the whole warp when it
+  // ends at or before it (uniform across the warp, as the .sync.aligned TMEM loads require)
+  const int lim_warp = a.causal ? qt * kT + wq * 32 : a.N - 1;
   const float tc = a.causal ? (float)(t + 1) : (float)a.N;
   const float inv_sqrt_d = 1.0f / sqrtf((float)D);
   const float c2 = 1.4426950408889634f * inv_sqrt_d;  // log2(e) / sqrt(d): exponent in base 2
@@ -201,10 +204,55 @@ __device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, 
     if (!ok) break;
     tc_fence_after();
     const int k0 = g * kT;
-    const bool full = k0 + kT - 1 <= lim;
+    const bool full = k0 + kT - 1 <= lim_warp;
+    if (full) {  // every key visible: packed fp32 arithmetic, loads double-buffered
+      uint32_t ra[32], rb[32];
+      auto stat_chunk = [&](uint32_t (&rv)[32]) {
+        float cm = __uint_as_float(rv[0]);
+        float2 ps = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int y = 0; y < 16; ++y) {
+          const float2 xv = make_float2(__uint_as_float(rv[2 * y]), __uint_as_float(rv[2 * y + 1]));
+          cm = fmaxf(cm, fmaxf(xv.x, xv.y));
+          ps = __fadd2_rn(ps, xv);
+        }
+        const float mn = fmaxf(m2, cm * c2);
+        const float2 c2v = make_float2(c2, c2), nm = make_float2(-mn, -mn);
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int y = 0; y < 16; ++y) {
+          const float2 e = __ffma2_rn(
+              make_float2(__uint_as_float(rv[2 * y]), __uint_as_float(rv[2 * y + 1])), c2v, nm);
+          acc = __fadd2_rn(acc, make_float2(ex2(e.x), ex2(e.y)));
+        }
+        l = fmaf(l, ex2(m2 - mn), acc.x + acc.y);
+        m2 = mn;
+        P += ps.x + ps.y;
+      };
+      tmem_ld32_nowait(ts, ra);
+      tmem_wait_ld();
+      reg_fence(ra);
+      tmem_ld32_nowait(ts + 32, rb);
+      stat_chunk(ra);
+      tmem_wait_ld();
+      reg_fence(rb);
+      tmem_ld32_nowait(ts + 64, ra);
+      stat_chunk(rb);
+      tmem_wait_ld();
+      reg_fence(ra);
+      tmem_ld32_nowait(ts + 96, rb);
+      stat_chunk(ra);
+      tmem_wait_ld();
+      reg_fence(rb);
+      stat_chunk(rb);
+      tc_fence_before();
+      mbar_arrive(&ms->s_free[w]);
+      continue;
+    }
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
       float v[32];
+      __syncwarp();  // the rows of a warp diverge below; the TMEM load needs all 32 lanes
       tmem_ld32(ts + 32 * ch, v);
       float cm = -INFINITY, cs = 0.0f;
 #pragma unroll
@@ -276,10 +324,50 @@ __device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, 
     if (!ok) break;
     tc_fence_after();
     const int k0 = j * kT;
-    const bool full = k0 + kT - 1 <= lim;
+    const bool full = k0 + kT - 1 <= lim_warp;
+    if (full) {  // every key visible: packed fp32 arithmetic, loads double-buffered
+      const float2 c2v = make_float2(c2, c2), nm = make_float2(-m2, -m2);
+      const float2 av = make_float2(alpha, alpha), bv = make_float2(bs, bs);
+      const float2 gv = make_float2(gamma, gamma);
+      uint32_t ra[32], rb[32];
+      auto w_chunk = [&](uint32_t (&rv)[32], int ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int y = 0; y < 16; ++y) {
+          const float2 xv = make_float2(__uint_as_float(rv[2 * y]), __uint_as_float(rv[2 * y + 1]));
+          float2 e = __ffma2_rn(xv, c2v, nm);
+          e = make_float2(ex2(e.x), ex2(e.y));
+          const float2 wv = __ffma2_rn(e, av, __ffma2_rn(xv, bv, gv));
+          pk[y] = pack_bf16x2(wv.x, wv.y);
+        }
+        tmem_st16_nowait(tw + 16 * ch, pk);
+      };
+      tmem_ld32_nowait(ts, ra);
+      tmem_wait_ld();
+      reg_fence(ra);
+      tmem_ld32_nowait(ts + 32, rb);
+      w_chunk(ra, 0);
+      tmem_wait_ld();
+      reg_fence(rb);
+      tmem_ld32_nowait(ts + 64, ra);
+      w_chunk(rb, 1);
+      tmem_wait_ld();
+      reg_fence(ra);
+      tmem_ld32_nowait(ts + 96, rb);
+      w_chunk(ra, 2);
+      tmem_wait_ld();
+      reg_fence(rb);
+      w_chunk(rb, 3);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ms->s_free[w]);
+      mbar_arrive(&ms->w_full[w]);
+      continue;
+    }
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
       float v[32];
+      __syncwarp();
       tmem_ld32(ts + 32 * ch, v);
       uint32_t pk[16];
 #pragma unroll
