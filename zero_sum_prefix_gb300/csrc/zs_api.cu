@@ -657,8 +657,7 @@ int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, c
     if (int rc = rope_table(ws, N, d, rope_base, st, &table)) return rc;
     void* qr = buf;
     void* kr = static_cast<uint8_t*>(buf) + each;
-    cudaError_t e = launch_sm_rotate(q, qr, table, B * H, N, d, st);
-    if (e == cudaSuccess) e = launch_sm_rotate(k, kr, table, B * H, N, d, st);
+    cudaError_t e = launch_sm_rotate(q, k, qr, kr, table, B * H, N, d, st);
     if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
     a.q = qr;
     a.k = kr;

@@ -93,7 +93,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // zs_sm.cu
 bool sm_supported(int d, int dtype);
 cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream);
-cudaError_t launch_sm_rotate(const void* x, void* y, const float2* table, int BH, int N, int d,
-                             cudaStream_t stream);
+cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
+                             const float2* table, int BH, int N, int d, cudaStream_t stream);
 
 }  // namespace zs

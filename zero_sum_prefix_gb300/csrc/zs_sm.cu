@@ -479,21 +479,41 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
   }
 }
 
-// Rotary map of bf16 rows [BH, N, d] (half-split pairs, token n at position n) into `y`, with
-// the fp64-built (cos, sin) table [N][d/2]; the rotated values are rounded to bf16 once.
-__global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y,
-                                 const float2* __restrict__ table, int N, int d, size_t pairs) {
-  const int half = d / 2;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < pairs;
+// Rotary map of the bf16 rows [BH, N, d] of q and of k (half-split pairs, token n at position
+// n) into yq and yk, with the fp64-built (cos, sin) table [N][d/2]; the rotated values are
+// rounded to bf16 once.  A thread takes 8 consecutive pairs of one row (16-byte loads and
+// stores of each half); the first half of the threads does q, the second k.
+__global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
+                                 const __nv_bfloat16* __restrict__ xk, __nv_bfloat16* __restrict__ yq,
+                                 __nv_bfloat16* __restrict__ yk, const float2* __restrict__ table,
+                                 int N, int d, size_t groups) {
+  const int half = d / 2, gpr = half / 8;  // groups of 8 pairs per row
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * groups;
        i += (size_t)gridDim.x * blockDim.x) {
-    const int a = (int)(i % half);
-    const size_t rowi = i / half;  // (bh, n)
+    const bool is_k = i >= groups;
+    const size_t gi = is_k ? i - groups : i;
+    const int a0 = (int)(gi % gpr) * 8;
+    const size_t rowi = gi / gpr;  // (bh, n)
     const int n = (int)(rowi % N);
-    const float2 cs = table[(size_t)n * half + a];
-    const size_t o = rowi * d + a;
-    const float xa = __bfloat162float(x[o]), xb = __bfloat162float(x[o + half]);
-    y[o] = __float2bfloat16_rn(__fmaf_rn(xa, cs.x, -xb * cs.y));
-    y[o + half] = __float2bfloat16_rn(__fmaf_rn(xa, cs.y, xb * cs.x));
+    const size_t o = rowi * d + a0;
+    const __nv_bfloat16* x = is_k ? xk : xq;
+    __nv_bfloat16* y = is_k ? yk : yq;
+    const uint4 ua = *reinterpret_cast<const uint4*>(x + o);
+    const uint4 ub = *reinterpret_cast<const uint4*>(x + o + half);
+    const float4* tb = reinterpret_cast<const float4*>(table + (size_t)n * half + a0);
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+    uint32_t ra[4], rb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {  // pairs a0 + 2e and a0 + 2e + 1
+      const float4 cs = tb[e];     // (cos, sin) of both pairs
+      float xa0, xa1, xb0, xb1;
+      unpack_bf16x2(wa[e], xa0, xa1);
+      unpack_bf16x2(wb[e], xb0, xb1);
+      ra[e] = pack_bf16x2(__fmaf_rn(xa0, cs.x, -xb0 * cs.y), __fmaf_rn(xa1, cs.z, -xb1 * cs.w));
+      rb[e] = pack_bf16x2(__fmaf_rn(xa0, cs.y, xb0 * cs.x), __fmaf_rn(xa1, cs.w, xb1 * cs.z));
+    }
+    *reinterpret_cast<uint4*>(y + o) = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+    *reinterpret_cast<uint4*>(y + o + half) = make_uint4(rb[0], rb[1], rb[2], rb[3]);
   }
 }
 
@@ -561,13 +581,15 @@ cudaError_t launch_sm_d(const SmArgs& a, cudaStream_t stream) {
 
 bool sm_supported(int d, int dtype) { return dtype == 0 && (d == 64 || d == 128); }
 
-cudaError_t launch_sm_rotate(const void* x, void* y, const float2* table, int BH, int N, int d,
-                             cudaStream_t stream) {
-  const size_t pairs = (size_t)BH * N * (d / 2);
-  if (pairs == 0) return cudaSuccess;
-  const int blocks = (int)((pairs + 255) / 256 < 152 * 16 ? (pairs + 255) / 256 : 152 * 16);
-  sm_rotate_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
-                                               static_cast<__nv_bfloat16*>(y), table, N, d, pairs);
+cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
+                             const float2* table, int BH, int N, int d, cudaStream_t stream) {
+  const size_t groups = (size_t)BH * N * (d / 16);  // 8 pairs per group, per tensor
+  if (groups == 0) return cudaSuccess;
+  const size_t want = (2 * groups + 255) / 256;
+  const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  sm_rotate_kernel<<<blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<__nv_bfloat16*>(yq), static_cast<__nv_bfloat16*>(yk), table, N, d, groups);
   count_launches(1);
   return cudaGetLastError();
 }
