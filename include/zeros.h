@@ -179,6 +179,18 @@ int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const 
               float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
               int rope, int dtype, float rope_base, void* stream);
 
+/* zeros_bwd with an implementation path (a zeros_path value): ZEROS_PATH_SIMT = the
+ * token-sequential kernel (any d); ZEROS_PATH_CHUNK = the chunk-parallel kernels (d = 64 only,
+ * else ZEROS_ERR_UNSUPPORTED): a forward launch supplies the per-token scalars, then per chunk
+ * of 64 tokens the intra-chunk products and the inter-chunk terms from stored chunk-start and
+ * suffix states (scratch of about B*H*N*(6 d + 8)*4 + 24 B*H*ceil(N/64)*d*d bytes);
+ * ZEROS_PATH_AUTO = the chunked kernels where supported.  Both reduce in fp32. */
+int zeros_bwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* g0, const float* mu, const float* tau,
+                 const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
+                 float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
+                 int rope, int dtype, float rope_base, int path, void* stream);
+
 /*
  * Recurrent state ("the state is the checkpoint").  Size in bytes of the blob for B x H
  * sequences of head dimension d (0 for unsupported d).  Layout: a 256-byte header

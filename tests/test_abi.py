@@ -92,6 +92,12 @@ def test_host_validation_without_gpu(lib):
     assert bwd(ptr=24) == zs.ZEROS_ERR_INVALID
     assert bwd(dg0=16) == zs.ZEROS_ERR_INVALID       # dg0 without the gate
     assert bwd(rope=1, base=-1.0) == zs.ZEROS_ERR_INVALID
+    def bwd_ex(d=64, path=0):
+        x = ctypes.c_void_p(16)
+        return lib.zeros_bwd_ex(x, x, x, x, x, x, None, x, x, x, x, x, x, x, x, x, None, x, x,
+                                1, 1, 8, d, 0, 0, 1e4, path, None)
+    assert bwd_ex(path=7) == zs.ZEROS_ERR_INVALID
+    assert bwd_ex(d=32, path=2) == zs.ZEROS_ERR_UNSUPPORTED  # chunked: d = 64 only
     # output LayerNorm: epsilon and gain/bias pointers are checked before any CUDA call
     def fwd_ln(eps=1e-5, w=None, b=None, d=64):
         wp = ctypes.c_void_p(w) if w is not None else None

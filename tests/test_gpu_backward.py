@@ -35,18 +35,28 @@ def _rel(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
-@pytest.mark.parametrize("d,N,rope,dtype,zero_order", [
-    (32, 37, False, "f32", False), (64, 1, True, "f32", False), (64, 200, True, "f32", False),
-    (128, 77, True, "f32", True), (64, 150, False, "bf16", False), (128, 64, True, "bf16", True),
-    (32, 300, True, "f32", True)])
-def test_backward_matches_autograd(zs, d, N, rope, dtype, zero_order):
+CASES = [(32, 37, False, "f32", False), (64, 1, True, "f32", False), (64, 200, True, "f32", False),
+         (128, 77, True, "f32", True), (64, 150, False, "bf16", False),
+         (128, 64, True, "bf16", True), (32, 300, True, "f32", True),
+         (64, 64, True, "bf16", False), (64, 65, False, "f32", True),
+         (64, 300, True, "bf16", True)]
+
+
+@pytest.mark.parametrize("path", ["simt", "chunk"])
+@pytest.mark.parametrize("d,N,rope,dtype,zero_order", CASES)
+def test_backward_matches_autograd(zs, d, N, rope, dtype, zero_order, path):
+    """Both backward paths: the token-sequential kernel (any d) and the chunk-parallel kernels
+    (d = 64; chunks of 64 tokens, so N = 64, 65, 150, 200, 300 cover one chunk, a ragged second
+    chunk and several chunks)."""
+    if path == "chunk" and d != 64:
+        pytest.skip("the chunked backward is built for d = 64")
     w = zi.Workload("bwd", 2, 2, N, d, dtype=dtype, rope=rope, seed=500 + d + N)
     inp = zi.make(w, "cuda")
     gen = torch.Generator(device="cpu").manual_seed(17 + N)
     dout = torch.randn((w.B, w.H, N, d), generator=gen).to(inp["q"].dtype).cuda()
     g0 = (torch.randn((w.B, w.H, N), generator=gen) * 1.5).cuda() if zero_order else None
     args = [inp[n] for n in KEYS]
-    got = zs.bwd(*args, dout, rope=rope, rope_base=w.rope_base, g0=g0)
+    got = zs.bwd(*args, dout, rope=rope, rope_base=w.rope_base, g0=g0, path=path)
     assert zs.get_status() == 0
     ref = og.backward(*(a.float().cpu() for a in args), dout.float().cpu(), rope=rope,
                       rope_base=w.rope_base, g0=None if g0 is None else g0.cpu())
@@ -56,7 +66,7 @@ def test_backward_matches_autograd(zs, d, N, rope, dtype, zero_order):
             assert got["d" + n].abs().max().item() <= ZERO_ABS, n
         return
     errs = {n: _rel(got["d" + n].cpu().numpy(), ref[n]) for n in ref}
-    print(d, N, rope, dtype, zero_order, {n: f"{e:.1e}" for n, e in errs.items()})
+    print(path, d, N, rope, dtype, zero_order, {n: f"{e:.1e}" for n, e in errs.items()})
     for n, e in errs.items():
         assert e <= TOL_GRAD, (n, e)
 
@@ -69,3 +79,29 @@ def test_backward_empty_and_status(zs):
     g = zs.bwd(*(z[n] for n in KEYS), dout)
     assert zs.get_status() == 0
     assert torch.count_nonzero(g["dmu"]) == 0 and torch.count_nonzero(g["dtau"]) == 0
+
+
+def test_backward_full_size_sampled(zs):
+    """The bench's causal RoPE B8 H8 N4096 d64 bf16 launch through the chunked path: the
+    gradients of two sampled sequences (every per-sequence gradient depends on that sequence
+    only) against the autograd oracle on that whole sequence; d mu and d tau (sums over the
+    batch) against the token-sequential kernel on the same inputs."""
+    w = zi.CAUSAL_ROPE_B8H8N4096D64
+    inp = zi.make(w, "cuda")
+    gen = torch.Generator(device="cpu").manual_seed(4096)
+    dout = torch.randn(inp["q"].shape, generator=gen).to(inp["q"].dtype).cuda()
+    args = [inp[n] for n in KEYS]
+    got = zs.bwd(*args, dout, rope=True, rope_base=w.rope_base, path="chunk")
+    assert zs.get_status() == 0
+    for b, h in ((0, 0), (6, 3)):
+        sel = [x[b:b + 1, h:h + 1].float().cpu() for x in args[:6]]
+        ref = og.backward(*sel, inp["mu"][h:h + 1].cpu(), inp["tau"][h:h + 1].cpu(),
+                          dout[b:b + 1, h:h + 1].float().cpu(), rope=True,
+                          rope_base=w.rope_base)
+        for n in ("q", "k", "v", "u", "g1", "gh"):
+            e = _rel(got["d" + n][b:b + 1, h:h + 1].cpu().numpy(), ref[n])
+            assert e <= 1e-4, (b, h, n, e)
+    seq = zs.bwd(*args, dout, rope=True, rope_base=w.rope_base, path="simt")
+    assert zs.get_status() == 0
+    for n in ("dmu", "dtau"):
+        assert _rel(got[n].cpu().numpy(), seq[n].cpu().numpy()) <= 1e-4, n

@@ -29,7 +29,7 @@ EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
            "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd", "zeros_fwd_ln",
-           "zeros_decode_step_ln", "zeros_sm_fwd"]
+           "zeros_decode_step_ln", "zeros_sm_fwd", "zeros_bwd_ex"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,8 @@ def load():
         lib.zeros_fwd_ln.restype = i
         lib.zeros_decode_step_ln.argtypes = [vp, i, i, i] + [vp] * 9 + [f, vp, vp]
         lib.zeros_decode_step_ln.restype = i
+        lib.zeros_bwd_ex.argtypes = [vp] * 19 + [i] * 6 + [f, i, vp]
+        lib.zeros_bwd_ex.restype = i
         lib.zeros_sm_fwd.argtypes = [vp] * 7 + [i] * 7 + [f, vp]
         lib.zeros_sm_fwd.restype = i
         lib.zeros_fwd_noalloc.restype = i
@@ -211,7 +213,7 @@ def sm_fwd(q, k, v, g1, gh, *, causal=True, rope=False, rope_base=10000.0, g0=No
 
 
 def bwd(q, k, v, u, g1, gh, mu, tau, dout, *, rope=False, rope_base=10000.0, g0=None,
-        stream=None):
+        stream=None, path="auto"):
     """Backward of the causal forward: gradients of sum(out * dout).  Inputs as in ``fwd``
     (causal mode); ``dout`` has the shape and dtype of q.  Returns a dict of fp32 tensors
     dq, dk, dv, du [B, H, N, d], dg1, dgh [B, H, N], dmu [H, d], dtau [H] (and dg0 when
@@ -234,12 +236,13 @@ def bwd(q, k, v, u, g1, gh, mu, tau, dout, *, rope=False, rope_base=10000.0, g0=
     g["dtau"] = torch.empty((H,), **f32)
     if g0 is not None:
         g["dg0"] = torch.empty((B, H, N), **f32)
-    rc = load().zeros_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh), _ptr(g0),
-                          _ptr(mu), _ptr(tau), _ptr(dout), _ptr(g["dq"]), _ptr(g["dk"]),
-                          _ptr(g["dv"]), _ptr(g["du"]), _ptr(g["dg1"]), _ptr(g["dgh"]),
-                          _ptr(g.get("dg0")), _ptr(g["dmu"]), _ptr(g["dtau"]), B, H, N, d,
-                          int(bool(rope)), _dtype_code(q), float(rope_base), _stream(stream))
-    _check(rc, "zeros_bwd")
+    rc = load().zeros_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(g1), _ptr(gh),
+                             _ptr(g0), _ptr(mu), _ptr(tau), _ptr(dout), _ptr(g["dq"]),
+                             _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["du"]), _ptr(g["dg1"]),
+                             _ptr(g["dgh"]), _ptr(g.get("dg0")), _ptr(g["dmu"]),
+                             _ptr(g["dtau"]), B, H, N, d, int(bool(rope)), _dtype_code(q),
+                             float(rope_base), PATHS[path], _stream(stream))
+    _check(rc, "zeros_bwd_ex")
     return g
 
 

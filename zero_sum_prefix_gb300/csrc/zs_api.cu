@@ -541,13 +541,21 @@ int zeros_decode_step_ex(void* state, int B, int H, int d, const void* q, const 
                      stream);
 }
 
-int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
-              const float* gh, const float* g0, const float* mu, const float* tau,
-              const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
-              float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
-              int rope, int dtype, float rope_base, void* stream) {
+int zeros_bwd_ex(const void* q, const void* k, const void* v, const void* u, const float* g1,
+                 const float* gh, const float* g0, const float* mu, const float* tau,
+                 const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
+                 float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
+                 int rope, int dtype, float rope_base, int path, void* stream) {
   g_last_error.clear();
   if (int rc = check_dims(B, H, N, d)) return rc;
+  if (path != ZEROS_PATH_AUTO && path != ZEROS_PATH_SIMT && path != ZEROS_PATH_CHUNK)
+    return fail(ZEROS_ERR_INVALID, "unknown path");
+  const unsigned long long n_chunks =
+      (unsigned long long)B * H * (((unsigned long long)N + 63) / 64);
+  const bool chunk_ok = bwd_chunk_supported(d) && n_chunks <= 0x7fffffffull;
+  if (path == ZEROS_PATH_CHUNK && !chunk_ok)
+    return fail(ZEROS_ERR_UNSUPPORTED, "the chunked backward needs d = 64");
+  const bool use_chunk = chunk_ok && path != ZEROS_PATH_SIMT;
   if (int rc = check_dtype(dtype)) return rc;
   if (rope != 0 && rope != 1) return fail(ZEROS_ERR_INVALID, "rope must be 0 or 1");
   if (rope && !(rope_base > 0.0f)) return fail(ZEROS_ERR_INVALID, "rope_base must be > 0");
@@ -603,13 +611,61 @@ int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const 
   a.rope = rope;
   a.dtype = dtype;
   a.status = ws->status;
-  if (int rc = bwd_scratch(ws, bwd_scratch_bytes(B, H, N, d), &a.scratch)) return rc;
   if (rope) {
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
-  e = launch_bwd(a, st);
+  if (!use_chunk) {
+    if (int rc = bwd_scratch(ws, bwd_scratch_bytes(B, H, N, d), &a.scratch)) return rc;
+    e = launch_bwd(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return ZEROS_OK;
+  }
+  // chunked: a forward launch writes the per-token scalars (its output goes to scratch), then
+  // the state, chunk and scan kernels
+  const size_t BHN = (size_t)B * H * N;
+  const size_t out_bytes = ((BHN * d * (dtype == ZEROS_F32 ? 4 : 2)) + 255) / 256 * 256;
+  float* buf = nullptr;
+  if (int rc = bwd_scratch(ws, out_bytes + bwd_chunk_scratch_bytes(B, H, N, d), &buf)) return rc;
+  float* scal = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(buf) + out_bytes);
+  FwdArgs f{};
+  f.q = q;
+  f.k = k;
+  f.v = v;
+  f.u = u;
+  f.g1 = g1;
+  f.gh = gh;
+  f.g0 = g0;
+  f.mu = mu;
+  f.tau = tau;
+  f.out = buf;
+  f.B = B;
+  f.H = H;
+  f.N = N;
+  f.d = d;
+  f.causal = 1;
+  f.rope = rope;
+  f.dtype = dtype;
+  f.rope_base = rope_base;
+  f.rope_table = a.rope_table;
+  f.dbg_s = scal;
+  f.dbg_E = scal + BHN;
+  f.dbg_P = scal + 2 * BHN;
+  f.dbg_m = scal + 3 * BHN;
+  f.status = ws->status;
+  e = chunk_supported(d, dtype, 1) ? launch_fwd_chunk(f, st) : launch_fwd_simt(f, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch (backward scalars)");
+  e = launch_bwd_chunk(a, scal, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ZEROS_OK;
+}
+
+int zeros_bwd(const void* q, const void* k, const void* v, const void* u, const float* g1,
+              const float* gh, const float* g0, const float* mu, const float* tau,
+              const void* dout, float* dq, float* dk, float* dv, float* du, float* dg1,
+              float* dgh, float* dg0, float* dmu, float* dtau, int B, int H, int N, int d,
+              int rope, int dtype, float rope_base, void* stream) {
+  return zeros_bwd_ex(q, k, v, u, g1, gh, g0, mu, tau, dout, dq, dk, dv, du, dg1, dgh, dg0, dmu,
+                      dtau, B, H, N, d, rope, dtype, rope_base, ZEROS_PATH_AUTO, stream);
 }
 
 int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, const float* gh,

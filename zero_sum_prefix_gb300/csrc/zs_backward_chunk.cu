@@ -1,0 +1,660 @@
+// Chunk-parallel backward of the causal ZeroS layer (d = 64): the same gradients as the
+// token-sequential kernel of zs_backward.cu (Paper-Notes "ZeroS: Zero-Sum Linear Attention for
+// Efficient Transformers", method details: deviation logits, zero-sum weights, radial-angular
+// decoupling, linear-time prefix scan; the derivative of that definition), computed in chunks
+// of C = 64 tokens so that every (b, h, chunk) works in parallel.
+//
+// With W_{t,i} = alpha_t e^{s_i} + beta_t s_i + gamma_t and c_{t,i} = q_hat_t k_hat_i^T, the
+// output is o_t = sum_{i<=t} c_{t,i} W_{t,i} v_i.  For a chunk c (reference M_c = running max at
+// its last token, M_{c-1} at the previous chunk's), in fp32:
+//   intra:  S = Q K^T, dA = dO V^T, W~_{t,i} = ah_t e_i + beta_t s_i + gamma_t (i <= t, inside the
+//           chunk; e_i = e^{s_i - M_c}, ah_t = alpha~_t e^{M_c - m_t}), A = S o W~, dC = dA o W~,
+//           dW = dA o S;  dQ += dC K, dK += dC^T Q, dV += A^T dO;  row sums of dW (e, s, 1)
+//           give the intra parts of d ah, d beta, d gamma; column sums (ah, beta) the direct ds.
+//   inter (the chunk-start states F~_c = sum_{i<chunk} e^{s_i - M_{c-1}} k_i^T v_i, G_c, H_c):
+//           X = dO [F~|G|H]^T; dq_hat += rho X_F + beta X_G + gamma X_H (rho_t = alpha~_t
+//           e^{M_{c-1} - m_t}); d rho, d beta, d gamma += q_hat . X.
+//   suffix (the states of the later chunks D~F_c = sum_{t>chunk} alpha~_t e^{M_c - m_t} q^T do,
+//           D^G_c, D^H_c): Y = V D^T, Z = K D;  dk_hat += e Y_F + s Y_G + Y_H,
+//           dv += e Z_F + s Z_G + Z_H, ds += e v.Z_F + v.Z_G.
+// The chunk-start and suffix states come from bwd_states_kernel (one pass over the chunks in
+// each direction, the value columns split over four CTAs); the E and P terms of ds, the gate
+// gradients' companions and du, d mu, d tau from bwd_final_kernel (scans over the tokens).
+// The per-token s, E e^{-m}, P and m are those of the forward kernels (their debug outputs).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "zs_common.cuh"
+#include "zs_internal.h"
+
+namespace zs {
+namespace {
+
+constexpr int kD = 64;        // head dimension of the chunked path
+constexpr int kCk = 64;       // tokens per chunk
+constexpr int kNT = 256;      // threads per CTA
+constexpr int kLD = kD + 1;   // padded row stride of the fp32 tiles
+constexpr int kSlices = 4;    // value-column slices of the state kernel
+constexpr int kSW = kD / kSlices;
+
+// Scratch layout (fp32), shared with the host: per-token forward scalars, the two state sets,
+// per-token backward scalars, the prior means.
+struct BwdChunkScratch {
+  float *s, *E, *P, *m;   // [BH][N] forward scalars (s, E e^{-m}, P, m)
+  float* fs;              // [BH][NC][3][D][D] chunk-start states F~, G, H
+  float* ds;              // [BH][NC][3][D][D] suffix states D~F, D^G, D^H
+  float* tok;             // [BH][N][4] d alpha~, d gamma, direct ds, ds
+  float* ubar;            // [BH][N][D]
+};
+
+// Token coefficients of the forward (the same expressions as the forward kernels).
+struct TokCoef {
+  float alt, beta, gamma, sig1, sigh;
+};
+__device__ __forceinline__ TokCoef tok_coef(const BwdArgs& a, size_t row, int t, float Et,
+                                            float P) {
+  TokCoef c;
+  c.sig1 = sigmoid(a.g1[row]);
+  c.sigh = sigmoid(a.gh[row]);
+  const float rt = __fdiv_rn(1.0f, (float)(t + 1));
+  c.beta = __fmul_rn(__fsub_rn(c.sig1, c.sigh), rt);
+  c.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(c.beta, P), rt), __fmul_rn(c.sigh, rt));
+  if (a.g0) c.gamma = __fadd_rn(c.gamma, __fmul_rn(sigmoid(a.g0[row]), rt));
+  c.alt = __fdiv_rn(c.sigh, Et);
+  return c;
+}
+
+// Rotated unit vector of row t of src (one warp; lane owns columns lane and lane + 32, which
+// form one rotary pair).  Returns the norm; writes the rotated unit row to dst[0..64).
+template <typename T>
+__device__ __forceinline__ float unit_row(const T* src, const BwdArgs& a, int t, float* dst) {
+  const int lane = threadIdx.x & 31;
+  float x0 = ld(src, lane), x1 = ld(src, lane + 32);
+  float ss = __fmaf_rn(x0, x0, __fmul_rn(x1, x1));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+  const float n = fmaxf(__fsqrt_rn(ss), 1e-12f);
+  const float inv = __fdiv_rn(1.0f, n);
+  x0 = __fmul_rn(x0, inv);
+  x1 = __fmul_rn(x1, inv);
+  if (a.rope) {
+    const float2 cs = a.rope_table[(size_t)t * (kD / 2) + lane];
+    const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+    const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+    x0 = y0;
+    x1 = y1;
+  }
+  dst[lane] = x0;
+  dst[lane + 32] = x1;
+  return n;
+}
+
+// ================================================================== chunk states
+// grid (BH, slices, 2): z = 0 stores the chunk-start forward states F~_c, G_c, H_c (F~ relative
+// to M_{c-1}) going forward; z = 1 stores the suffix states D~F_c (relative to M_c), D^G_c, D^H_c
+// going backward.  Columns j0 .. j0 + 15 of each d x d state; thread (a = tid / 4, 4 columns).
+template <typename T>
+__global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScratch sc) {
+  __shared__ float rows[kCk][kD];      // k_hat (z = 0) or q_hat (z = 1) of the chunk
+  __shared__ float cols[kCk][kSW];     // v or do slice
+  __shared__ float cf[kCk][3];         // per-token weights of the three states
+  __shared__ float fac;                // rescale of the F~ state
+  const int bh = blockIdx.x, j0 = blockIdx.y * kSW, dir = blockIdx.z;
+  const int N = a.N, NC = (N + kCk - 1) / kCk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ar = tid >> 2, cj = (tid & 3) * 4;
+  const size_t row0 = (size_t)bh * N;
+  const T* __restrict__ src = static_cast<const T*>(dir == 0 ? a.k : a.q) + row0 * kD;
+  const T* __restrict__ val = static_cast<const T*>(dir == 0 ? a.v : a.dout) + row0 * kD;
+  float st[3][4];
+#pragma unroll
+  for (int m = 0; m < 3; ++m)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) st[m][x] = 0.0f;
+  float* out = dir == 0 ? sc.fs : sc.ds;
+  for (int it = 0; it < NC; ++it) {
+    const int c = dir == 0 ? it : NC - 1 - it;
+    float* dst = out + (((size_t)bh * NC + c) * 3) * kD * kD;
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+      *reinterpret_cast<float4*>(dst + (size_t)m * kD * kD + ar * kD + j0 + cj) =
+          make_float4(st[m][0], st[m][1], st[m][2], st[m][3]);
+    if (dir == 0 ? c == NC - 1 : c == 0) break;
+    // chunk c's rows and weights
+    const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
+    const float Mc = sc.m[row0 + t0 + tn - 1];
+    const float Mp = c > 0 ? sc.m[row0 + t0 - 1] : 0.0f;
+    for (int r = warp; r < kCk; r += kNT / 32) {
+      if (r < tn) {
+        unit_row<T>(src + (size_t)(t0 + r) * kD, a, t0 + r, rows[r]);
+      } else {
+        rows[r][lane] = 0.0f;
+        rows[r][lane + 32] = 0.0f;
+      }
+    }
+    for (int e = tid; e < kCk * kSW; e += kNT) {
+      const int r = e / kSW, j = e % kSW;
+      cols[r][j] = r < tn ? ld(val, (size_t)(t0 + r) * kD + j0 + j) : 0.0f;
+    }
+    if (tid < kCk) {
+      float w0 = 0.0f, w1 = 0.0f, w2 = 0.0f;
+      if (tid < tn) {
+        const size_t row = row0 + t0 + tid;
+        const float s = sc.s[row];
+        if (dir == 0) {
+          w0 = expf(__fsub_rn(s, Mc));  // e_i relative to M_c
+          w1 = s;
+          w2 = 1.0f;
+        } else {
+          const TokCoef k = tok_coef(a, row, t0 + tid, sc.E[row], sc.P[row]);
+          w0 = __fmul_rn(k.alt, expf(__fsub_rn(Mp, sc.m[row])));  // relative to M_{c-1}
+          w1 = k.beta;
+          w2 = k.gamma;
+        }
+      }
+      cf[tid][0] = w0;
+      cf[tid][1] = w1;
+      cf[tid][2] = w2;
+    }
+    if (tid == 0) fac = dir == 0 ? (c > 0 ? expf(__fsub_rn(Mp, Mc)) : 0.0f) : expf(__fsub_rn(Mp, Mc));
+    __syncthreads();
+#pragma unroll
+    for (int x = 0; x < 4; ++x) st[0][x] = __fmul_rn(st[0][x], fac);
+    for (int r = 0; r < tn; ++r) {
+      const float ka = rows[r][ar];
+      const float4 vv = *reinterpret_cast<const float4*>(&cols[r][cj]);
+      const float kv[4] = {__fmul_rn(ka, vv.x), __fmul_rn(ka, vv.y), __fmul_rn(ka, vv.z),
+                           __fmul_rn(ka, vv.w)};
+#pragma unroll
+      for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) st[m][x] = __fmaf_rn(cf[r][m], kv[x], st[m][x]);
+    }
+    __syncthreads();
+  }
+}
+
+// ================================================================== chunk gradients
+// 64 x 64 fp32 products from shared tiles (row stride kLD): thread (tr = tid / 16, tc = tid % 16)
+// accumulates rows 4 tr .. 4 tr + 3 and columns 4 tc .. 4 tc + 3 of  op(A) op(B)  over k < 64,
+// op(A)(r, k) = TA ? A[k][r] : A[r][k],  op(B)(k, c) = TB ? B[c][k] : B[k][c].
+template <bool TA, bool TB>
+__device__ __forceinline__ void gemm64(const float* A, const float* B, float (&acc)[4][4]) {
+  const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
+#pragma unroll 4
+  for (int k = 0; k < 64; ++k) {
+    float av[4], bv[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      av[x] = TA ? A[k * kLD + 4 * tr + x] : A[(4 * tr + x) * kLD + k];
+      bv[x] = TB ? B[(4 * tc + x) * kLD + k] : B[k * kLD + 4 * tc + x];
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = __fmaf_rn(av[x], bv[y], acc[x][y]);
+  }
+}
+
+__device__ __forceinline__ void zero44(float (&acc)[4][4]) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.0f;
+}
+
+// Sum over the 16 threads of a half warp that share a row group.
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct ChunkSmem {
+  static constexpr uint32_t TILE = kCk * kLD;  // floats
+  static constexpr int NTILE = 6;              // Q, K, V, dO, two product / state tiles
+  static constexpr int NSC = 20;               // per-token scalar arrays
+  static constexpr uint32_t BYTES = (NTILE * TILE + NSC * kCk + 16 * kCk * 2) * 4;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkScratch scr) {
+  extern __shared__ float sm[];
+  float* Qs = sm;                       // q_hat rows (rotated unit vectors)
+  float* Ks = Qs + ChunkSmem::TILE;     // k_hat rows
+  float* Vs = Ks + ChunkSmem::TILE;     // v rows
+  float* Ds = Vs + ChunkSmem::TILE;     // do rows
+  float* P1 = Ds + ChunkSmem::TILE;     // A, then a state matrix, then dq_hat
+  float* P2 = P1 + ChunkSmem::TILE;     // dC, then a state matrix, then dk_hat
+  float* scal = P2 + ChunkSmem::TILE;   // [NSC][kCk]
+  float* colp = scal + ChunkSmem::NSC * kCk;  // [2][16][kCk] column partials
+  float* s_s = scal + 0 * kCk;    // s
+  float* s_e = scal + 1 * kCk;    // e^{s - M_c}
+  float* s_ah = scal + 2 * kCk;   // alpha~ e^{M_c - m}
+  float* s_be = scal + 3 * kCk;   // beta
+  float* s_ga = scal + 4 * kCk;   // gamma
+  float* s_rho = scal + 5 * kCk;  // alpha~ e^{M_{c-1} - m}
+  float* s_nq = scal + 6 * kCk;   // |q|
+  float* s_nk = scal + 7 * kCk;   // |k|
+  float* r_dah = scal + 8 * kCk;  // row sums: d ah (intra), d beta, d gamma
+  float* r_dbe = scal + 9 * kCk;
+  float* r_dga = scal + 10 * kCk;
+  float* r_drho = scal + 11 * kCk;  // inter: d rho, d beta, d gamma
+  float* r_dbe2 = scal + 12 * kCk;
+  float* r_dga2 = scal + 13 * kCk;
+  float* c_ds = scal + 14 * kCk;    // inter ds (e v.Z_F + v.Z_G)
+
+  const int N = a.N, NC = (N + kCk - 1) / kCk;
+  const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tr = tid >> 4, tc = tid & 15;
+  const size_t row0 = (size_t)bh * N;
+  const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
+  const T* __restrict__ q = static_cast<const T*>(a.q) + row0 * kD;
+  const T* __restrict__ k = static_cast<const T*>(a.k) + row0 * kD;
+  const T* __restrict__ v = static_cast<const T*>(a.v) + row0 * kD;
+  const T* __restrict__ dout = static_cast<const T*>(a.dout) + row0 * kD;
+  const float Mc = scr.m[row0 + t0 + tn - 1];
+  const float Mp = c > 0 ? scr.m[row0 + t0 - 1] : 0.0f;
+
+  // ---- rows of the chunk (zero past N) and per-token scalars ----
+  for (int r = warp; r < kCk; r += kNT / 32) {
+    if (r < tn) {
+      const float nq = unit_row<T>(q + (size_t)(t0 + r) * kD, a, t0 + r, Qs + r * kLD);
+      const float nk = unit_row<T>(k + (size_t)(t0 + r) * kD, a, t0 + r, Ks + r * kLD);
+      Vs[r * kLD + lane] = ld(v, (size_t)(t0 + r) * kD + lane);
+      Vs[r * kLD + lane + 32] = ld(v, (size_t)(t0 + r) * kD + lane + 32);
+      Ds[r * kLD + lane] = ld(dout, (size_t)(t0 + r) * kD + lane);
+      Ds[r * kLD + lane + 32] = ld(dout, (size_t)(t0 + r) * kD + lane + 32);
+      if (lane == 0) {
+        s_nq[r] = nq;
+        s_nk[r] = nk;
+      }
+    } else {
+      Qs[r * kLD + lane] = Qs[r * kLD + lane + 32] = 0.0f;
+      Ks[r * kLD + lane] = Ks[r * kLD + lane + 32] = 0.0f;
+      Vs[r * kLD + lane] = Vs[r * kLD + lane + 32] = 0.0f;
+      Ds[r * kLD + lane] = Ds[r * kLD + lane + 32] = 0.0f;
+      if (lane == 0) s_nq[r] = s_nk[r] = 1.0f;
+    }
+  }
+  if (tid < kCk) {
+    float sv = 0.0f, ev = 0.0f, ah = 0.0f, be = 0.0f, ga = 0.0f, rho = 0.0f;
+    if (tid < tn) {
+      const size_t row = row0 + t0 + tid;
+      sv = scr.s[row];
+      const float mt = scr.m[row];
+      const TokCoef kc = tok_coef(a, row, t0 + tid, scr.E[row], scr.P[row]);
+      ev = expf(__fsub_rn(sv, Mc));
+      ah = __fmul_rn(kc.alt, expf(__fsub_rn(Mc, mt)));
+      be = kc.beta;
+      ga = kc.gamma;
+      rho = c > 0 ? __fmul_rn(kc.alt, expf(__fsub_rn(Mp, mt))) : 0.0f;
+    }
+    s_s[tid] = sv;
+    s_e[tid] = ev;
+    s_ah[tid] = ah;
+    s_be[tid] = be;
+    s_ga[tid] = ga;
+    s_rho[tid] = rho;
+  }
+  __syncthreads();
+
+  // ---- intra-chunk products ----
+  float dq[4][4], dk[4][4], dv[4][4];
+  {
+    float sa[4][4], da[4][4];
+    zero44(sa);
+    zero44(da);
+    gemm64<false, true>(Qs, Ks, sa);  // S = Q K^T
+    gemm64<false, true>(Ds, Vs, da);  // dA = dO V^T
+    float rs_e[4], rs_s[4], rs_1[4], cp_a[4], cp_b[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) rs_e[x] = rs_s[x] = rs_1[x] = cp_a[x] = cp_b[x] = 0.0f;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int t = 4 * tr + x;
+      const float ah = s_ah[t], be = s_be[t], ga = s_ga[t];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int i = 4 * tc + y;
+        float av = 0.0f, dc = 0.0f;
+        if (i <= t) {
+          const float w = __fmaf_rn(ah, s_e[i], __fmaf_rn(be, s_s[i], ga));
+          av = __fmul_rn(sa[x][y], w);
+          dc = __fmul_rn(da[x][y], w);
+          const float dw = __fmul_rn(da[x][y], sa[x][y]);
+          rs_e[x] = __fmaf_rn(dw, s_e[i], rs_e[x]);
+          rs_s[x] = __fmaf_rn(dw, s_s[i], rs_s[x]);
+          rs_1[x] = __fadd_rn(rs_1[x], dw);
+          cp_a[y] = __fmaf_rn(dw, ah, cp_a[y]);
+          cp_b[y] = __fmaf_rn(dw, be, cp_b[y]);
+        }
+        P1[t * kLD + i] = av;
+        P2[t * kLD + i] = dc;
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float e = sum16(rs_e[x]), s = sum16(rs_s[x]), o = sum16(rs_1[x]);
+      if (tc == 0) {
+        r_dah[4 * tr + x] = e;
+        r_dbe[4 * tr + x] = s;
+        r_dga[4 * tr + x] = o;
+      }
+    }
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      colp[tr * kCk + 4 * tc + y] = cp_a[y];
+      colp[16 * kCk + tr * kCk + 4 * tc + y] = cp_b[y];
+    }
+  }
+  __syncthreads();
+  zero44(dq);
+  zero44(dk);
+  zero44(dv);
+  gemm64<false, false>(P2, Ks, dq);  // dQ = dC K
+  gemm64<true, false>(P2, Qs, dk);   // dK = dC^T Q
+  gemm64<true, false>(P1, Ds, dv);   // dV = A^T dO
+  float cA = 0.0f, cB = 0.0f;        // column sums of dW ah and dW beta (thread tid < 64)
+  if (tid < kCk) {
+    for (int g = 0; g < 16; ++g) {
+      cA = __fadd_rn(cA, colp[g * kCk + tid]);
+      cB = __fadd_rn(cB, colp[16 * kCk + g * kCk + tid]);
+    }
+  }
+  __syncthreads();
+
+  // ---- inter-chunk: the chunk-start states, X = dO M^T ----
+  const float* fs = scr.fs + (((size_t)bh * NC + c) * 3) * kD * kD;
+  const float* dsu = scr.ds + (((size_t)bh * NC + c) * 3) * kD * kD;
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    float* Ms = (mtx & 1) ? P2 : P1;
+    for (int e = tid; e < kD * kD / 4; e += kNT) {
+      const float4 x4 = reinterpret_cast<const float4*>(fs + (size_t)mtx * kD * kD)[e];
+      const int r = (4 * e) / kD, cc = (4 * e) % kD;
+      Ms[r * kLD + cc] = x4.x;
+      Ms[r * kLD + cc + 1] = x4.y;
+      Ms[r * kLD + cc + 2] = x4.z;
+      Ms[r * kLD + cc + 3] = x4.w;
+    }
+    __syncthreads();
+    float xa[4][4];
+    zero44(xa);
+    gemm64<false, true>(Ds, Ms, xa);  // X[t][a] = sum_j do_t[j] M[a][j]
+    const float* coef = mtx == 0 ? s_rho : mtx == 1 ? s_be : s_ga;
+    float* rdst = mtx == 0 ? r_drho : mtx == 1 ? r_dbe2 : r_dga2;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int t = 4 * tr + x;
+      const float cf = coef[t];
+      float rd = 0.0f;
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        dq[x][y] = __fmaf_rn(cf, xa[x][y], dq[x][y]);
+        rd = __fmaf_rn(xa[x][y], Qs[t * kLD + 4 * tc + y], rd);
+      }
+      rd = sum16(rd);
+      if (tc == 0) rdst[t] = rd;
+    }
+    __syncthreads();
+  }
+
+  // ---- suffix states: Y = V D^T (dk), Z = K D (dv, ds) ----
+  float dsp[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this thread's partial of e v.Z_F + v.Z_G per row
+  for (int mtx = 0; mtx < 3; ++mtx) {
+    float* Ms = (mtx & 1) ? P2 : P1;
+    for (int e = tid; e < kD * kD / 4; e += kNT) {
+      const float4 x4 = reinterpret_cast<const float4*>(dsu + (size_t)mtx * kD * kD)[e];
+      const int r = (4 * e) / kD, cc = (4 * e) % kD;
+      Ms[r * kLD + cc] = x4.x;
+      Ms[r * kLD + cc + 1] = x4.y;
+      Ms[r * kLD + cc + 2] = x4.z;
+      Ms[r * kLD + cc + 3] = x4.w;
+    }
+    __syncthreads();
+    float ya[4][4], za[4][4];
+    zero44(ya);
+    zero44(za);
+    gemm64<false, true>(Vs, Ms, ya);   // Y[i][a] = sum_j v_i[j] D[a][j]
+    gemm64<false, false>(Ks, Ms, za);  // Z[i][j] = sum_a k_i[a] D[a][j]
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int i = 4 * tr + x;
+      const float w = mtx == 0 ? s_e[i] : mtx == 1 ? s_s[i] : 1.0f;
+      float rd = 0.0f;
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        dk[x][y] = __fmaf_rn(w, ya[x][y], dk[x][y]);
+        dv[x][y] = __fmaf_rn(w, za[x][y], dv[x][y]);
+        rd = __fmaf_rn(za[x][y], Vs[i * kLD + 4 * tc + y], rd);
+      }
+      if (mtx == 0) dsp[x] = __fmul_rn(s_e[i], rd);
+      if (mtx == 1) dsp[x] = __fadd_rn(dsp[x], rd);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const float r = sum16(dsp[x]);
+    if (tc == 0) c_ds[4 * tr + x] = r;
+  }
+
+  // ---- outputs: dv directly; dq_hat, dk_hat staged for the unit-vector backward ----
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int t = 4 * tr + x;
+    if (t < tn)
+      *reinterpret_cast<float4*>(a.dv + (row0 + t0 + t) * kD + 4 * tc) =
+          make_float4(dv[x][0], dv[x][1], dv[x][2], dv[x][3]);
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      P1[t * kLD + 4 * tc + y] = dq[x][y];
+      P2[t * kLD + 4 * tc + y] = dk[x][y];
+    }
+  }
+  __syncthreads();
+  // dx = R^T (dy - y_hat (y_hat . dy)) / |x|, one warp per row (lane: the pair lane, lane + 32)
+  for (int r = warp; r < tn; r += kNT / 32) {
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float* dy = (which ? P2 : P1) + r * kLD;
+      const float* yh = (which ? Ks : Qs) + r * kLD;
+      float g0 = dy[lane], g1 = dy[lane + 32];
+      float dot = __fmaf_rn(yh[lane], g0, __fmul_rn(yh[lane + 32], g1));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, o));
+      g0 = __fsub_rn(g0, __fmul_rn(yh[lane], dot));
+      g1 = __fsub_rn(g1, __fmul_rn(yh[lane + 32], dot));
+      if (a.rope) {  // inverse rotation of the pair
+        const float2 cs = a.rope_table[(size_t)(t0 + r) * (kD / 2) + lane];
+        const float x0 = __fmaf_rn(g0, cs.x, __fmul_rn(g1, cs.y));
+        const float x1 = __fmaf_rn(-g0, cs.y, __fmul_rn(g1, cs.x));
+        g0 = x0;
+        g1 = x1;
+      }
+      const float inv = __fdiv_rn(1.0f, which ? s_nk[r] : s_nq[r]);
+      float* dst = (which ? a.dk : a.dq) + (row0 + t0 + r) * kD;
+      dst[lane] = __fmul_rn(g0, inv);
+      dst[lane + 32] = __fmul_rn(g1, inv);
+    }
+  }
+  // ---- per-token scalars: d alpha~, d gamma, direct ds; gate gradients ----
+  if (tid < tn) {
+    const int t = tid;
+    const size_t row = row0 + t0 + t;
+    const float mt = scr.m[row];
+    const float dal = __fadd_rn(__fmul_rn(r_dah[t], expf(__fsub_rn(Mc, mt))),
+                                c > 0 ? __fmul_rn(r_drho[t], expf(__fsub_rn(Mp, mt))) : 0.0f);
+    const float dbe = __fadd_rn(r_dbe[t], r_dbe2[t]);
+    const float dga = __fadd_rn(r_dga[t], r_dga2[t]);
+    const float dsd = __fadd_rn(__fmaf_rn(s_e[t], cA, cB), c_ds[t]);
+    float* tk = scr.tok + row * 4;
+    tk[0] = dal;
+    tk[1] = dga;
+    tk[2] = dsd;
+    const float Et = scr.E[row], P = scr.P[row];
+    const float sig1 = sigmoid(a.g1[row]), sigh = sigmoid(a.gh[row]);
+    const float rt = __fdiv_rn(1.0f, (float)(t0 + t + 1));
+    const float Pt2 = __fmul_rn(__fmul_rn(P, rt), rt);
+    const float dsig1 = __fsub_rn(__fmul_rn(dbe, rt), __fmul_rn(dga, Pt2));
+    const float dsigh = __fadd_rn(__fsub_rn(__fdiv_rn(dal, Et), __fmul_rn(dbe, rt)),
+                                  __fmul_rn(dga, __fsub_rn(Pt2, rt)));
+    a.dg1[row] = __fmul_rn(dsig1, __fmul_rn(sig1, __fsub_rn(1.0f, sig1)));
+    a.dgh[row] = __fmul_rn(dsigh, __fmul_rn(sigh, __fsub_rn(1.0f, sigh)));
+    if (a.g0 && a.dg0) {
+      const float s0 = sigmoid(a.g0[row]);
+      a.dg0[row] = __fmul_rn(__fmul_rn(dga, rt), __fmul_rn(s0, __fsub_rn(1.0f, s0)));
+    }
+  }
+}
+
+// ================================================================== token scans
+// One CTA per (b, h).  (1) ds_t = direct_t + e^{s_t - m_t} EA_t + PA_t with the suffix sums
+// EA_t = e^{m_t - m_{t+1}} EA_{t+1} - alpha~_t d alpha~_t / E~_t and PA_t = PA_{t+1} -
+// (beta_t / t) d gamma_t (the E and P terms of ds, as in the token-sequential kernel), by one
+// thread over tokens staged 256 at a time.  (2) ubar (prefix of u), Z (suffix of ds u / (e^tau + t)),
+// du = -(ds ubar + Z)/sqrt d, the d tau partial sum; four token segments x d columns with the
+// segments' totals combined through shared memory.
+template <typename T>
+__global__ void __launch_bounds__(kNT) bwd_final_kernel(BwdArgs a, BwdChunkScratch scr) {
+  __shared__ float stg[5][kNT];
+  __shared__ float segu[4][kD], segz[4][kD];
+  __shared__ float red[kNT / 32];
+  const int bh = blockIdx.x, h = bh % a.H;
+  const int N = a.N, tid = threadIdx.x;
+  const size_t row0 = (size_t)bh * N;
+  const float etau = expf(a.tau[h]);
+  const float rsd = __fdiv_rn(1.0f, __fsqrt_rn((float)kD));
+  // ---- (1) ds ----
+  float EA = 0.0f, PA = 0.0f;
+  for (int b0 = ((N - 1) / kNT) * kNT; b0 >= 0; b0 -= kNT) {
+    const int t = b0 + tid;
+    if (t < N) {
+      const size_t row = row0 + t;
+      const float* tk = scr.tok + row * 4;
+      const float Et = scr.E[row], m = scr.m[row];
+      const float sig1 = sigmoid(a.g1[row]), sigh = sigmoid(a.gh[row]);
+      const float tf = (float)(t + 1);
+      const float alt = __fdiv_rn(sigh, Et);
+      const float beta = __fmul_rn(__fsub_rn(sig1, sigh), __fdiv_rn(1.0f, tf));
+      stg[0][tid] = -__fdiv_rn(__fmul_rn(alt, tk[0]), Et);
+      stg[1][tid] = -__fmul_rn(__fdiv_rn(beta, tf), tk[1]);
+      stg[2][tid] = t + 1 < N ? expf(__fsub_rn(m, scr.m[row + 1])) : 0.0f;
+      stg[3][tid] = expf(__fsub_rn(scr.s[row], m));
+      stg[4][tid] = tk[2];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int x = min(kNT, N - b0) - 1; x >= 0; --x) {
+        EA = __fmaf_rn(EA, stg[2][x], stg[0][x]);
+        PA = __fadd_rn(PA, stg[1][x]);
+        stg[4][x] = __fadd_rn(stg[4][x], __fmaf_rn(stg[3][x], EA, PA));
+      }
+    }
+    __syncthreads();
+    if (t < N) scr.tok[(row0 + t) * 4 + 3] = stg[4][tid];
+    __syncthreads();
+  }
+  // ---- (2) ubar, Z, du ----
+  const T* __restrict__ u = static_cast<const T*>(a.u) + row0 * kD;
+  const int g = tid / kD, j = tid % kD;  // segment, column
+  const int L = (N + 3) / 4, ta = min(N, g * L), tb = min(N, ta + L);
+  const float mu = a.mu[(size_t)h * kD + j];
+  float su = 0.0f;
+  for (int t = ta; t < tb; ++t) su = __fadd_rn(su, ld(u, (size_t)t * kD + j));
+  segu[g][j] = su;
+  __syncthreads();
+  float S = 0.0f;
+  for (int x = 0; x < g; ++x) S = __fadd_rn(S, segu[x][j]);
+  const float emu = __fmul_rn(etau, mu);
+  float zl = 0.0f;
+#pragma unroll 4
+  for (int t = ta; t < tb; ++t) {
+    const float ut = ld(u, (size_t)t * kD + j);
+    S = __fadd_rn(S, ut);
+    const float wt = __fdiv_rn(1.0f, __fadd_rn(etau, (float)(t + 1)));
+    scr.ubar[(row0 + t) * kD + j] = __fmul_rn(__fadd_rn(emu, S), wt);
+    zl = __fmaf_rn(__fmul_rn(scr.tok[(row0 + t) * 4 + 3], ut), wt, zl);
+  }
+  segz[g][j] = zl;
+  __syncthreads();
+  float z = 0.0f;
+  for (int x = g + 1; x < 4; ++x) z = __fadd_rn(z, segz[x][j]);
+  float tacc = 0.0f;
+#pragma unroll 4
+  for (int t = tb - 1; t >= ta; --t) {
+    const float ut = ld(u, (size_t)t * kD + j);
+    const float ds = scr.tok[(row0 + t) * 4 + 3];
+    const float ub = scr.ubar[(row0 + t) * kD + j];
+    const float wt = __fdiv_rn(1.0f, __fadd_rn(etau, (float)(t + 1)));
+    const float dsu = __fmul_rn(ds, ut);
+    z = __fmaf_rn(dsu, wt, z);
+    tacc = __fmaf_rn(__fmul_rn(dsu, __fsub_rn(mu, ub)), wt, tacc);
+    a.du[(row0 + t) * kD + j] = -__fmul_rn(__fmaf_rn(ds, ub, z), rsd);
+  }
+  // d mu: Z at the first token (segment 0 ends with the total); d tau: all partials
+  if (g == 0) atomicAdd(a.dmu + (size_t)h * kD + j, -__fmul_rn(__fmul_rn(etau, z), rsd));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) tacc = __fadd_rn(tacc, __shfl_xor_sync(0xffffffffu, tacc, o));
+  if ((tid & 31) == 0) red[tid >> 5] = tacc;
+  __syncthreads();
+  if (tid == 0) {
+    float ts = 0.0f;
+    for (int w = 0; w < kNT / 32; ++w) ts = __fadd_rn(ts, red[w]);
+    atomicAdd(a.dtau + h, -__fmul_rn(__fmul_rn(etau, ts), rsd));
+  }
+}
+
+template <typename T>
+cudaError_t launch_chunk_t(const BwdArgs& a, const BwdChunkScratch& sc, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(bwd_chunk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ChunkSmem::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  const int BH = a.B * a.H, NC = (a.N + kCk - 1) / kCk;
+  bwd_states_kernel<T><<<dim3(BH, kSlices, 2), kNT, 0, stream>>>(a, sc);
+  bwd_chunk_kernel<T><<<(unsigned)(BH * NC), kNT, ChunkSmem::BYTES, stream>>>(a, sc);
+  bwd_final_kernel<T><<<BH, kNT, 0, stream>>>(a, sc);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_chunk_supported(int d) { return d == kD; }
+
+// Scratch (bytes) of the chunked backward: forward scalars s, E e^{-m}, P, m [BH][N] each (the
+// forward kernels write them first), chunk-start and suffix states, token scalars, prior means.
+size_t bwd_chunk_scratch_bytes(int B, int H, int N, int d) {
+  const size_t BH = (size_t)B * H, NC = (size_t)(N + kCk - 1) / kCk;
+  return (BH * N * 4 + 2 * BH * NC * 3 * (size_t)d * d + BH * N * 4 + BH * N * (size_t)d) *
+         sizeof(float);
+}
+
+cudaError_t launch_bwd_chunk(const BwdArgs& a, float* scratch, cudaStream_t stream) {
+  const size_t BH = (size_t)a.B * a.H, N = (size_t)a.N, NC = (N + kCk - 1) / kCk;
+  BwdChunkScratch sc;
+  sc.s = scratch;
+  sc.E = sc.s + BH * N;
+  sc.P = sc.E + BH * N;
+  sc.m = sc.P + BH * N;
+  sc.fs = sc.m + BH * N;
+  sc.ds = sc.fs + BH * NC * 3 * kD * kD;
+  sc.tok = sc.ds + BH * NC * 3 * kD * kD;
+  sc.ubar = sc.tok + BH * N * 4;
+  return a.dtype == 1 ? launch_chunk_t<float>(a, sc, stream)
+                      : launch_chunk_t<__nv_bfloat16>(a, sc, stream);
+}
+
+}  // namespace zs

@@ -90,6 +90,13 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // zs_decode.cu
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// zs_backward_chunk.cu: chunk-parallel backward (d = 64).  The scratch starts with the forward
+// scalars s, E e^{-m}, P, m ([B*H*N] each), which the caller fills by a forward launch with
+// those debug outputs.
+bool bwd_chunk_supported(int d);
+size_t bwd_chunk_scratch_bytes(int B, int H, int N, int d);
+cudaError_t launch_bwd_chunk(const BwdArgs& a, float* scratch, cudaStream_t stream);
+
 // zs_sm.cu
 bool sm_supported(int d, int dtype);
 cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream);
