@@ -19,7 +19,8 @@
 //           dv += e Z_F + s Z_G + Z_H, ds += e v.Z_F + v.Z_G.
 // The chunk-start and suffix states come from bwd_states_kernel (one pass over the chunks in
 // each direction, the value columns split over four CTAs); the E and P terms of ds, the gate
-// gradients' companions and du, d mu, d tau from bwd_final_kernel (scans over the tokens).
+// gradients' companions and du, d mu, d tau from bwd_ds_kernel and bwd_du_kernel (scans over
+// the tokens).
 // The per-token s, E e^{-m}, P and m are those of the forward kernels (their debug outputs).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,7 +37,7 @@ namespace {
 constexpr int kD = 64;        // head dimension of the chunked path
 constexpr int kCk = 64;       // tokens per chunk
 constexpr int kNT = 256;      // threads per CTA
-constexpr int kLD = kD + 1;   // padded row stride of the fp32 tiles
+constexpr int kLD = kD + 4;   // padded row stride of the fp32 tiles (16-byte rows, offset banks)
 constexpr int kSlices = 4;    // value-column slices of the state kernel
 constexpr int kSW = kD / kSlices;
 
@@ -48,6 +49,8 @@ struct BwdChunkScratch {
   float* ds;              // [BH][NC][3][D][D] suffix states D~F, D^G, D^H
   float* tok;             // [BH][N][4] d alpha~, d gamma, direct ds, ds
   float* ubar;            // [BH][N][D]
+  float *qhat, *khat;     // [BH][N][D] rotated unit q and k
+  float *nq, *nk;         // [BH][N] their norms
 };
 
 // Token coefficients of the forward (the same expressions as the forward kernels).
@@ -92,22 +95,41 @@ __device__ __forceinline__ float unit_row(const T* src, const BwdArgs& a, int t,
   return n;
 }
 
+// ================================================================== unit rows
+// Rotated unit vectors of every q and k row (one warp per row), with the norms.
+template <typename T>
+__global__ void __launch_bounds__(kNT) bwd_rows_kernel(BwdArgs a, BwdChunkScratch sc) {
+  const size_t rows = (size_t)a.B * a.H * a.N;
+  const int lane = threadIdx.x & 31;
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; w < 2 * rows;
+       w += ((size_t)gridDim.x * blockDim.x) >> 5) {
+    const bool isk = w >= rows;
+    const size_t row = isk ? w - rows : w;
+    const int t = (int)(row % a.N);
+    const T* src = static_cast<const T*>(isk ? a.k : a.q) + row * kD;
+    const float n = unit_row<T>(src, a, t, (isk ? sc.khat : sc.qhat) + row * kD);
+    if (lane == 0) (isk ? sc.nk : sc.nq)[row] = n;
+  }
+}
+
 // ================================================================== chunk states
 // grid (BH, slices, 2): z = 0 stores the chunk-start forward states F~_c, G_c, H_c (F~ relative
 // to M_{c-1}) going forward; z = 1 stores the suffix states D~F_c (relative to M_c), D^G_c, D^H_c
 // going backward.  Columns j0 .. j0 + 15 of each d x d state; thread (a = tid / 4, 4 columns).
+// The next chunk's rows, value slice and scalars are loaded into registers while the current
+// chunk is accumulated.
 template <typename T>
 __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScratch sc) {
-  __shared__ float rows[kCk][kD];      // k_hat (z = 0) or q_hat (z = 1) of the chunk
-  __shared__ float cols[kCk][kSW];     // v or do slice
-  __shared__ float cf[kCk][3];         // per-token weights of the three states
-  __shared__ float fac;                // rescale of the F~ state
+  __shared__ __align__(16) float rows[kCk][kD];  // k_hat (z = 0) or q_hat (z = 1) of the chunk
+  __shared__ __align__(16) float cols[kCk][kSW];  // v or do slice
+  __shared__ float cf[kCk][3];                    // per-token weights of the three states
+  __shared__ float fac;                           // rescale of the F~ state
   const int bh = blockIdx.x, j0 = blockIdx.y * kSW, dir = blockIdx.z;
   const int N = a.N, NC = (N + kCk - 1) / kCk;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int ar = tid >> 2, cj = (tid & 3) * 4;
   const size_t row0 = (size_t)bh * N;
-  const T* __restrict__ src = static_cast<const T*>(dir == 0 ? a.k : a.q) + row0 * kD;
+  const float* __restrict__ hat = (dir == 0 ? sc.khat : sc.qhat) + row0 * kD;
   const T* __restrict__ val = static_cast<const T*>(dir == 0 ? a.v : a.dout) + row0 * kD;
   float st[3][4];
 #pragma unroll
@@ -115,6 +137,39 @@ __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScra
 #pragma unroll
     for (int x = 0; x < 4; ++x) st[m][x] = 0.0f;
   float* out = dir == 0 ? sc.fs : sc.ds;
+  // prefetch registers: 16 row values, 4 values of the slice, the token's weights, M_c, M_{c-1}
+  float4 pr[4];
+  float pv[4], pw[3], pMc = 0.0f, pMp = 0.0f;
+  auto fetch = [&](int c) {
+    const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int e = tid + kNT * x, r = e / (kD / 4);
+      pr[x] = r < tn ? reinterpret_cast<const float4*>(hat + (size_t)t0 * kD)[e]
+                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int y = 0; y < 4; ++y) pv[y] = ar < tn ? ld(val, (size_t)(t0 + ar) * kD + j0 + cj + y) : 0.0f;
+    pMc = sc.m[row0 + t0 + tn - 1];
+    pMp = c > 0 ? sc.m[row0 + t0 - 1] : 0.0f;
+    pw[0] = pw[1] = pw[2] = 0.0f;
+    if (tid < tn) {
+      const size_t row = row0 + t0 + tid;
+      const float s = sc.s[row];
+      if (dir == 0) {
+        pw[0] = expf(__fsub_rn(s, pMc));  // e_i relative to M_c
+        pw[1] = s;
+        pw[2] = 1.0f;
+      } else {
+        const TokCoef k = tok_coef(a, row, t0 + tid, sc.E[row], sc.P[row]);
+        pw[0] = __fmul_rn(k.alt, expf(__fsub_rn(pMp, sc.m[row])));  // relative to M_{c-1}
+        pw[1] = k.beta;
+        pw[2] = k.gamma;
+      }
+    }
+  };
+  const int last = dir == 0 ? NC - 1 : 0;  // the chunk whose state is stored without an update
+  if (NC > 1) fetch(dir == 0 ? 0 : NC - 1);
   for (int it = 0; it < NC; ++it) {
     const int c = dir == 0 ? it : NC - 1 - it;
     float* dst = out + (((size_t)bh * NC + c) * 3) * kD * kD;
@@ -122,56 +177,36 @@ __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScra
     for (int m = 0; m < 3; ++m)
       *reinterpret_cast<float4*>(dst + (size_t)m * kD * kD + ar * kD + j0 + cj) =
           make_float4(st[m][0], st[m][1], st[m][2], st[m][3]);
-    if (dir == 0 ? c == NC - 1 : c == 0) break;
-    // chunk c's rows and weights
-    const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
-    const float Mc = sc.m[row0 + t0 + tn - 1];
-    const float Mp = c > 0 ? sc.m[row0 + t0 - 1] : 0.0f;
-    for (int r = warp; r < kCk; r += kNT / 32) {
-      if (r < tn) {
-        unit_row<T>(src + (size_t)(t0 + r) * kD, a, t0 + r, rows[r]);
-      } else {
-        rows[r][lane] = 0.0f;
-        rows[r][lane + 32] = 0.0f;
-      }
-    }
-    for (int e = tid; e < kCk * kSW; e += kNT) {
-      const int r = e / kSW, j = e % kSW;
-      cols[r][j] = r < tn ? ld(val, (size_t)(t0 + r) * kD + j0 + j) : 0.0f;
-    }
-    if (tid < kCk) {
-      float w0 = 0.0f, w1 = 0.0f, w2 = 0.0f;
-      if (tid < tn) {
-        const size_t row = row0 + t0 + tid;
-        const float s = sc.s[row];
-        if (dir == 0) {
-          w0 = expf(__fsub_rn(s, Mc));  // e_i relative to M_c
-          w1 = s;
-          w2 = 1.0f;
-        } else {
-          const TokCoef k = tok_coef(a, row, t0 + tid, sc.E[row], sc.P[row]);
-          w0 = __fmul_rn(k.alt, expf(__fsub_rn(Mp, sc.m[row])));  // relative to M_{c-1}
-          w1 = k.beta;
-          w2 = k.gamma;
-        }
-      }
-      cf[tid][0] = w0;
-      cf[tid][1] = w1;
-      cf[tid][2] = w2;
-    }
-    if (tid == 0) fac = dir == 0 ? (c > 0 ? expf(__fsub_rn(Mp, Mc)) : 0.0f) : expf(__fsub_rn(Mp, Mc));
-    __syncthreads();
+    if (c == last) break;
+    const int tn = min(N, c * kCk + kCk) - c * kCk;
 #pragma unroll
-    for (int x = 0; x < 4; ++x) st[0][x] = __fmul_rn(st[0][x], fac);
+    for (int x = 0; x < 4; ++x) reinterpret_cast<float4*>(&rows[0][0])[tid + kNT * x] = pr[x];
+    *reinterpret_cast<float4*>(&cols[ar][cj]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+    if (tid < kCk) {
+      cf[tid][0] = pw[0];
+      cf[tid][1] = pw[1];
+      cf[tid][2] = pw[2];
+    }
+    if (tid == 0) fac = (dir == 0 && c == 0) ? 0.0f : expf(__fsub_rn(pMp, pMc));
+    __syncthreads();
+    const int nxt = dir == 0 ? c + 1 : c - 1;
+    if (nxt != last) fetch(nxt);  // in flight while this chunk is accumulated
+    const float f = fac;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) st[0][x] = __fmul_rn(st[0][x], f);
+#pragma unroll 4
     for (int r = 0; r < tn; ++r) {
       const float ka = rows[r][ar];
       const float4 vv = *reinterpret_cast<const float4*>(&cols[r][cj]);
       const float kv[4] = {__fmul_rn(ka, vv.x), __fmul_rn(ka, vv.y), __fmul_rn(ka, vv.z),
                            __fmul_rn(ka, vv.w)};
+      const float w0 = cf[r][0], w1 = cf[r][1], w2 = cf[r][2];
 #pragma unroll
-      for (int m = 0; m < 3; ++m)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) st[m][x] = __fmaf_rn(cf[r][m], kv[x], st[m][x]);
+      for (int x = 0; x < 4; ++x) {
+        st[0][x] = __fmaf_rn(w0, kv[x], st[0][x]);
+        st[1][x] = __fmaf_rn(w1, kv[x], st[1][x]);
+        st[2][x] = __fmaf_rn(w2, kv[x], st[2][x]);
+      }
     }
     __syncthreads();
   }
@@ -180,22 +215,37 @@ __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScra
 // ================================================================== chunk gradients
 // 64 x 64 fp32 products from shared tiles (row stride kLD): thread (tr = tid / 16, tc = tid % 16)
 // accumulates rows 4 tr .. 4 tr + 3 and columns 4 tc .. 4 tc + 3 of  op(A) op(B)  over k < 64,
-// op(A)(r, k) = TA ? A[k][r] : A[r][k],  op(B)(k, c) = TB ? B[c][k] : B[k][c].
+// op(A)(r, k) = TA ? A[k][r] : A[r][k],  op(B)(k, c) = TB ? B[c][k] : B[k][c]; four k at a time
+// with 16-byte loads (eight loads per 64 multiply-adds).
 template <bool TA, bool TB>
 __device__ __forceinline__ void gemm64(const float* A, const float* B, float (&acc)[4][4]) {
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
-#pragma unroll 4
-  for (int k = 0; k < 64; ++k) {
-    float av[4], bv[4];
+#pragma unroll 2
+  for (int k0 = 0; k0 < 64; k0 += 4) {
+    float av[4][4], bv[4][4];  // [k - k0][row or column]
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      av[x] = TA ? A[k * kLD + 4 * tr + x] : A[(4 * tr + x) * kLD + k];
-      bv[x] = TB ? B[(4 * tc + x) * kLD + k] : B[k * kLD + 4 * tc + x];
+      if (TA) {
+        const float4 t = *reinterpret_cast<const float4*>(A + (k0 + x) * kLD + 4 * tr);
+        av[x][0] = t.x; av[x][1] = t.y; av[x][2] = t.z; av[x][3] = t.w;
+      } else {
+        const float4 t = *reinterpret_cast<const float4*>(A + (4 * tr + x) * kLD + k0);
+        av[0][x] = t.x; av[1][x] = t.y; av[2][x] = t.z; av[3][x] = t.w;
+      }
+      if (TB) {
+        const float4 t = *reinterpret_cast<const float4*>(B + (4 * tc + x) * kLD + k0);
+        bv[0][x] = t.x; bv[1][x] = t.y; bv[2][x] = t.z; bv[3][x] = t.w;
+      } else {
+        const float4 t = *reinterpret_cast<const float4*>(B + (k0 + x) * kLD + 4 * tc);
+        bv[x][0] = t.x; bv[x][1] = t.y; bv[x][2] = t.z; bv[x][3] = t.w;
+      }
     }
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int y = 0; y < 4; ++y) acc[x][y] = __fmaf_rn(av[x], bv[y], acc[x][y]);
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = __fmaf_rn(av[kk][x], bv[kk][y], acc[x][y]);
   }
 }
 
@@ -216,13 +266,15 @@ __device__ __forceinline__ float sum16(float v) {
 struct ChunkSmem {
   static constexpr uint32_t TILE = kCk * kLD;  // floats
   static constexpr int NTILE = 6;              // Q, K, V, dO, two product / state tiles
-  static constexpr int NSC = 20;               // per-token scalar arrays
-  static constexpr uint32_t BYTES = (NTILE * TILE + NSC * kCk + 16 * kCk * 2) * 4;
+  static constexpr int NSC = 15;               // per-token scalar arrays
+  // tiles, scalars, column partial sums [2][8 warps][kCk]; two CTAs fit on one SM
+  static constexpr uint32_t BYTES = (NTILE * TILE + NSC * kCk + 8 * kCk * 2) * 4;
+  static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkScratch scr) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* Qs = sm;                       // q_hat rows (rotated unit vectors)
   float* Ks = Qs + ChunkSmem::TILE;     // k_hat rows
   float* Vs = Ks + ChunkSmem::TILE;     // v rows
@@ -230,7 +282,7 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
   float* P1 = Ds + ChunkSmem::TILE;     // A, then a state matrix, then dq_hat
   float* P2 = P1 + ChunkSmem::TILE;     // dC, then a state matrix, then dk_hat
   float* scal = P2 + ChunkSmem::TILE;   // [NSC][kCk]
-  float* colp = scal + ChunkSmem::NSC * kCk;  // [2][16][kCk] column partials
+  float* colp = scal + ChunkSmem::NSC * kCk;  // [2][8][kCk] column partials (one per warp)
   float* s_s = scal + 0 * kCk;    // s
   float* s_e = scal + 1 * kCk;    // e^{s - M_c}
   float* s_ah = scal + 2 * kCk;   // alpha~ e^{M_c - m}
@@ -253,8 +305,6 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
   const int tr = tid >> 4, tc = tid & 15;
   const size_t row0 = (size_t)bh * N;
   const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
-  const T* __restrict__ q = static_cast<const T*>(a.q) + row0 * kD;
-  const T* __restrict__ k = static_cast<const T*>(a.k) + row0 * kD;
   const T* __restrict__ v = static_cast<const T*>(a.v) + row0 * kD;
   const T* __restrict__ dout = static_cast<const T*>(a.dout) + row0 * kD;
   const float Mc = scr.m[row0 + t0 + tn - 1];
@@ -263,8 +313,12 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
   // ---- rows of the chunk (zero past N) and per-token scalars ----
   for (int r = warp; r < kCk; r += kNT / 32) {
     if (r < tn) {
-      const float nq = unit_row<T>(q + (size_t)(t0 + r) * kD, a, t0 + r, Qs + r * kLD);
-      const float nk = unit_row<T>(k + (size_t)(t0 + r) * kD, a, t0 + r, Ks + r * kLD);
+      const size_t rw = row0 + t0 + r;
+      Qs[r * kLD + lane] = scr.qhat[rw * kD + lane];
+      Qs[r * kLD + lane + 32] = scr.qhat[rw * kD + lane + 32];
+      Ks[r * kLD + lane] = scr.khat[rw * kD + lane];
+      Ks[r * kLD + lane + 32] = scr.khat[rw * kD + lane + 32];
+      const float nq = scr.nq[rw], nk = scr.nk[rw];
       Vs[r * kLD + lane] = ld(v, (size_t)(t0 + r) * kD + lane);
       Vs[r * kLD + lane + 32] = ld(v, (size_t)(t0 + r) * kD + lane + 32);
       Ds[r * kLD + lane] = ld(dout, (size_t)(t0 + r) * kD + lane);
@@ -347,9 +401,13 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
       }
     }
 #pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      colp[tr * kCk + 4 * tc + y] = cp_a[y];
-      colp[16 * kCk + tr * kCk + 4 * tc + y] = cp_b[y];
+    for (int y = 0; y < 4; ++y) {  // the warp's two row groups, then one partial per warp
+      const float pa = cp_a[y] + __shfl_xor_sync(0xffffffffu, cp_a[y], 16);
+      const float pb = cp_b[y] + __shfl_xor_sync(0xffffffffu, cp_b[y], 16);
+      if (lane < 16) {
+        colp[warp * kCk + 4 * tc + y] = pa;
+        colp[8 * kCk + warp * kCk + 4 * tc + y] = pb;
+      }
     }
   }
   __syncthreads();
@@ -361,9 +419,9 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
   gemm64<true, false>(P1, Ds, dv);   // dV = A^T dO
   float cA = 0.0f, cB = 0.0f;        // column sums of dW ah and dW beta (thread tid < 64)
   if (tid < kCk) {
-    for (int g = 0; g < 16; ++g) {
+    for (int g = 0; g < 8; ++g) {
       cA = __fadd_rn(cA, colp[g * kCk + tid]);
-      cB = __fadd_rn(cB, colp[16 * kCk + g * kCk + tid]);
+      cB = __fadd_rn(cB, colp[8 * kCk + g * kCk + tid]);
     }
   }
   __syncthreads();
@@ -376,10 +434,7 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     for (int e = tid; e < kD * kD / 4; e += kNT) {
       const float4 x4 = reinterpret_cast<const float4*>(fs + (size_t)mtx * kD * kD)[e];
       const int r = (4 * e) / kD, cc = (4 * e) % kD;
-      Ms[r * kLD + cc] = x4.x;
-      Ms[r * kLD + cc + 1] = x4.y;
-      Ms[r * kLD + cc + 2] = x4.z;
-      Ms[r * kLD + cc + 3] = x4.w;
+      *reinterpret_cast<float4*>(Ms + r * kLD + cc) = x4;
     }
     __syncthreads();
     float xa[4][4];
@@ -410,10 +465,7 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     for (int e = tid; e < kD * kD / 4; e += kNT) {
       const float4 x4 = reinterpret_cast<const float4*>(dsu + (size_t)mtx * kD * kD)[e];
       const int r = (4 * e) / kD, cc = (4 * e) % kD;
-      Ms[r * kLD + cc] = x4.x;
-      Ms[r * kLD + cc + 1] = x4.y;
-      Ms[r * kLD + cc + 2] = x4.z;
-      Ms[r * kLD + cc + 3] = x4.w;
+      *reinterpret_cast<float4*>(Ms + r * kLD + cc) = x4;
     }
     __syncthreads();
     float ya[4][4], za[4][4];
@@ -513,58 +565,84 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
 }
 
 // ================================================================== token scans
-// One CTA per (b, h).  (1) ds_t = direct_t + e^{s_t - m_t} EA_t + PA_t with the suffix sums
+// ds_t = direct_t + e^{s_t - m_t} EA_t + PA_t with the suffix recurrences
 // EA_t = e^{m_t - m_{t+1}} EA_{t+1} - alpha~_t d alpha~_t / E~_t and PA_t = PA_{t+1} -
-// (beta_t / t) d gamma_t (the E and P terms of ds, as in the token-sequential kernel), by one
-// thread over tokens staged 256 at a time.  (2) ubar (prefix of u), Z (suffix of ds u / (e^tau + t)),
-// du = -(ds ubar + Z)/sqrt d, the d tau partial sum; four token segments x d columns with the
-// segments' totals combined through shared memory.
+// (beta_t / t) d gamma_t (the E and P terms of ds, as in the token-sequential kernel).  One CTA
+// per (b, h); thread i takes a segment of consecutive tokens: it composes its segment's affine
+// map EA_in -> EA_out, a single thread chains the segments from the end, then every thread
+// replays its segment from its carry.
+__global__ void __launch_bounds__(kNT) bwd_ds_kernel(BwdArgs a, BwdChunkScratch scr) {
+  __shared__ float segR[kNT], segB[kNT], segP[kNT];  // segment maps, then carries
+  const int bh = blockIdx.x, N = a.N, tid = threadIdx.x;
+  const size_t row0 = (size_t)bh * N;
+  const int L = (N + kNT - 1) / kNT, ta = min(N, tid * L), tb = min(N, ta + L);
+  auto coef = [&](int t, float& r, float& b, float& p, float& ex) {
+    const size_t row = row0 + t;
+    const float* tk = scr.tok + row * 4;
+    const float Et = scr.E[row], m = scr.m[row];
+    const float sig1 = sigmoid(a.g1[row]), sigh = sigmoid(a.gh[row]);
+    const float tf = (float)(t + 1);
+    const float alt = __fdiv_rn(sigh, Et);
+    const float beta = __fmul_rn(__fsub_rn(sig1, sigh), __fdiv_rn(1.0f, tf));
+    b = -__fdiv_rn(__fmul_rn(alt, tk[0]), Et);
+    p = -__fmul_rn(__fdiv_rn(beta, tf), tk[1]);
+    r = t + 1 < N ? expf(__fsub_rn(m, scr.m[row + 1])) : 0.0f;
+    ex = expf(__fsub_rn(scr.s[row], m));
+  };
+  // EA_ta = R EA_tb + B over the segment (tokens tb-1 down to ta)
+  float R = 1.0f, B = 0.0f, PS = 0.0f;
+  for (int t = tb - 1; t >= ta; --t) {
+    float r, b, p, ex;
+    coef(t, r, b, p, ex);
+    B = __fmaf_rn(B, r, b);
+    R = __fmul_rn(R, r);
+    PS = __fadd_rn(PS, p);
+  }
+  segR[tid] = R;
+  segB[tid] = B;
+  segP[tid] = PS;
+  __syncthreads();
+  if (tid == 0) {  // carries: EA and PA entering each segment from the tokens after it
+    float ea = 0.0f, pa = 0.0f;
+    for (int g = kNT - 1; g >= 0; --g) {
+      const float r = segR[g], b = segB[g], p = segP[g];
+      segR[g] = ea;
+      segB[g] = pa;
+      ea = __fmaf_rn(ea, r, b);
+      pa = __fadd_rn(pa, p);
+    }
+  }
+  __syncthreads();
+  float EA = segR[tid], PA = segB[tid];
+  for (int t = tb - 1; t >= ta; --t) {
+    float r, b, p, ex;
+    coef(t, r, b, p, ex);
+    EA = __fmaf_rn(EA, r, b);
+    PA = __fadd_rn(PA, p);
+    float* tk = scr.tok + (row0 + t) * 4;
+    tk[3] = __fadd_rn(tk[2], __fmaf_rn(ex, EA, PA));
+  }
+}
+
+// ubar (prefix of u), Z (suffix of ds u / (e^tau + t)), du = -(ds ubar + Z)/sqrt d and the d tau
+// partial sums.  One CTA per (b, h): 16 token segments x 64 columns, the segments' totals
+// combined through shared memory.
+constexpr int kSeg = 16;
 template <typename T>
-__global__ void __launch_bounds__(kNT) bwd_final_kernel(BwdArgs a, BwdChunkScratch scr) {
-  __shared__ float stg[5][kNT];
-  __shared__ float segu[4][kD], segz[4][kD];
-  __shared__ float red[kNT / 32];
+__global__ void __launch_bounds__(kSeg * kD) bwd_du_kernel(BwdArgs a, BwdChunkScratch scr) {
+  __shared__ float segu[kSeg][kD], segz[kSeg][kD];
+  __shared__ float red[kSeg * kD / 32];
   const int bh = blockIdx.x, h = bh % a.H;
   const int N = a.N, tid = threadIdx.x;
   const size_t row0 = (size_t)bh * N;
   const float etau = expf(a.tau[h]);
   const float rsd = __fdiv_rn(1.0f, __fsqrt_rn((float)kD));
-  // ---- (1) ds ----
-  float EA = 0.0f, PA = 0.0f;
-  for (int b0 = ((N - 1) / kNT) * kNT; b0 >= 0; b0 -= kNT) {
-    const int t = b0 + tid;
-    if (t < N) {
-      const size_t row = row0 + t;
-      const float* tk = scr.tok + row * 4;
-      const float Et = scr.E[row], m = scr.m[row];
-      const float sig1 = sigmoid(a.g1[row]), sigh = sigmoid(a.gh[row]);
-      const float tf = (float)(t + 1);
-      const float alt = __fdiv_rn(sigh, Et);
-      const float beta = __fmul_rn(__fsub_rn(sig1, sigh), __fdiv_rn(1.0f, tf));
-      stg[0][tid] = -__fdiv_rn(__fmul_rn(alt, tk[0]), Et);
-      stg[1][tid] = -__fmul_rn(__fdiv_rn(beta, tf), tk[1]);
-      stg[2][tid] = t + 1 < N ? expf(__fsub_rn(m, scr.m[row + 1])) : 0.0f;
-      stg[3][tid] = expf(__fsub_rn(scr.s[row], m));
-      stg[4][tid] = tk[2];
-    }
-    __syncthreads();
-    if (tid == 0) {
-      for (int x = min(kNT, N - b0) - 1; x >= 0; --x) {
-        EA = __fmaf_rn(EA, stg[2][x], stg[0][x]);
-        PA = __fadd_rn(PA, stg[1][x]);
-        stg[4][x] = __fadd_rn(stg[4][x], __fmaf_rn(stg[3][x], EA, PA));
-      }
-    }
-    __syncthreads();
-    if (t < N) scr.tok[(row0 + t) * 4 + 3] = stg[4][tid];
-    __syncthreads();
-  }
-  // ---- (2) ubar, Z, du ----
   const T* __restrict__ u = static_cast<const T*>(a.u) + row0 * kD;
-  const int g = tid / kD, j = tid % kD;  // segment, column
-  const int L = (N + 3) / 4, ta = min(N, g * L), tb = min(N, ta + L);
+  const int g = tid / kD, j = tid % kD;
+  const int L = (N + kSeg - 1) / kSeg, ta = min(N, g * L), tb = min(N, ta + L);
   const float mu = a.mu[(size_t)h * kD + j];
   float su = 0.0f;
+#pragma unroll 4
   for (int t = ta; t < tb; ++t) su = __fadd_rn(su, ld(u, (size_t)t * kD + j));
   segu[g][j] = su;
   __syncthreads();
@@ -583,7 +661,7 @@ __global__ void __launch_bounds__(kNT) bwd_final_kernel(BwdArgs a, BwdChunkScrat
   segz[g][j] = zl;
   __syncthreads();
   float z = 0.0f;
-  for (int x = g + 1; x < 4; ++x) z = __fadd_rn(z, segz[x][j]);
+  for (int x = g + 1; x < kSeg; ++x) z = __fadd_rn(z, segz[x][j]);
   float tacc = 0.0f;
 #pragma unroll 4
   for (int t = tb - 1; t >= ta; --t) {
@@ -596,7 +674,7 @@ __global__ void __launch_bounds__(kNT) bwd_final_kernel(BwdArgs a, BwdChunkScrat
     tacc = __fmaf_rn(__fmul_rn(dsu, __fsub_rn(mu, ub)), wt, tacc);
     a.du[(row0 + t) * kD + j] = -__fmul_rn(__fmaf_rn(ds, ub, z), rsd);
   }
-  // d mu: Z at the first token (segment 0 ends with the total); d tau: all partials
+  // d mu: Z at the first token (segment 0 ends with the total); d tau: every partial
   if (g == 0) atomicAdd(a.dmu + (size_t)h * kD + j, -__fmul_rn(__fmul_rn(etau, z), rsd));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) tacc = __fadd_rn(tacc, __shfl_xor_sync(0xffffffffu, tacc, o));
@@ -604,7 +682,7 @@ __global__ void __launch_bounds__(kNT) bwd_final_kernel(BwdArgs a, BwdChunkScrat
   __syncthreads();
   if (tid == 0) {
     float ts = 0.0f;
-    for (int w = 0; w < kNT / 32; ++w) ts = __fadd_rn(ts, red[w]);
+    for (int w = 0; w < kSeg * kD / 32; ++w) ts = __fadd_rn(ts, red[w]);
     atomicAdd(a.dtau + h, -__fmul_rn(__fmul_rn(etau, ts), rsd));
   }
 }
@@ -623,10 +701,14 @@ cudaError_t launch_chunk_t(const BwdArgs& a, const BwdChunkScratch& sc, cudaStre
     attr_set.fetch_or(bit);
   }
   const int BH = a.B * a.H, NC = (a.N + kCk - 1) / kCk;
+  const size_t warps = 2 * (size_t)BH * a.N;
+  const size_t rb = (warps * 32 + kNT - 1) / kNT;
+  bwd_rows_kernel<T><<<(unsigned)(rb < 152 * 32 ? rb : 152 * 32), kNT, 0, stream>>>(a, sc);
   bwd_states_kernel<T><<<dim3(BH, kSlices, 2), kNT, 0, stream>>>(a, sc);
   bwd_chunk_kernel<T><<<(unsigned)(BH * NC), kNT, ChunkSmem::BYTES, stream>>>(a, sc);
-  bwd_final_kernel<T><<<BH, kNT, 0, stream>>>(a, sc);
-  count_launches(3);
+  bwd_ds_kernel<<<BH, kNT, 0, stream>>>(a, sc);
+  bwd_du_kernel<T><<<BH, kSeg * kD, 0, stream>>>(a, sc);
+  count_launches(5);
   return cudaGetLastError();
 }
 
@@ -638,7 +720,8 @@ bool bwd_chunk_supported(int d) { return d == kD; }
 // forward kernels write them first), chunk-start and suffix states, token scalars, prior means.
 size_t bwd_chunk_scratch_bytes(int B, int H, int N, int d) {
   const size_t BH = (size_t)B * H, NC = (size_t)(N + kCk - 1) / kCk;
-  return (BH * N * 4 + 2 * BH * NC * 3 * (size_t)d * d + BH * N * 4 + BH * N * (size_t)d) *
+  return (BH * N * 4 + 2 * BH * NC * 3 * (size_t)d * d + BH * N * 4 + BH * N * (size_t)d +
+          BH * N * (2 * (size_t)d + 2)) *
          sizeof(float);
 }
 
@@ -653,6 +736,10 @@ cudaError_t launch_bwd_chunk(const BwdArgs& a, float* scratch, cudaStream_t stre
   sc.ds = sc.fs + BH * NC * 3 * kD * kD;
   sc.tok = sc.ds + BH * NC * 3 * kD * kD;
   sc.ubar = sc.tok + BH * N * 4;
+  sc.qhat = sc.ubar + BH * N * kD;
+  sc.khat = sc.qhat + BH * N * kD;
+  sc.nq = sc.khat + BH * N * kD;
+  sc.nk = sc.nq + BH * N;
   return a.dtype == 1 ? launch_chunk_t<float>(a, sc, stream)
                       : launch_chunk_t<__nv_bfloat16>(a, sc, stream);
 }
