@@ -213,31 +213,32 @@ __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScra
 }
 
 // ================================================================== chunk gradients
-// 64 x 64 fp32 products from shared tiles (row stride kLD): thread (tr = tid / 16, tc = tid % 16)
-// accumulates rows 4 tr .. 4 tr + 3 and columns 4 tc .. 4 tc + 3 of  op(A) op(B)  over k < 64,
-// op(A)(r, k) = TA ? A[k][r] : A[r][k],  op(B)(k, c) = TB ? B[c][k] : B[k][c]; four k at a time
-// with 16-byte loads (eight loads per 64 multiply-adds).
+// 64 x 64 fp32 products from shared tiles (row stride kLD = 68 floats): thread (tr = tid / 16,
+// tc = tid % 16) accumulates rows tr + 16 x and columns tc + 16 y (x, y < 4) of  op(A) op(B)
+// over k < 64, op(A)(r, k) = TA ? A[k][r] : A[r][k],  op(B)(k, c) = TB ? B[c][k] : B[k][c].
+// Four k at a time; operands along k are read as 16-byte vectors.  The eight threads of a
+// 16-byte load phase read eight rows 68 floats apart, i.e. disjoint bank quadruples.
 template <bool TA, bool TB>
 __device__ __forceinline__ void gemm64(const float* A, const float* B, float (&acc)[4][4]) {
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
 #pragma unroll 2
   for (int k0 = 0; k0 < 64; k0 += 4) {
-    float av[4][4], bv[4][4];  // [k - k0][row or column]
+    float av[4][4], bv[4][4];  // [k - k0][row or column index x / y]
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       if (TA) {
-        const float4 t = *reinterpret_cast<const float4*>(A + (k0 + x) * kLD + 4 * tr);
-        av[x][0] = t.x; av[x][1] = t.y; av[x][2] = t.z; av[x][3] = t.w;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) av[kk][x] = A[(k0 + kk) * kLD + tr + 16 * x];
       } else {
-        const float4 t = *reinterpret_cast<const float4*>(A + (4 * tr + x) * kLD + k0);
+        const float4 t = *reinterpret_cast<const float4*>(A + (tr + 16 * x) * kLD + k0);
         av[0][x] = t.x; av[1][x] = t.y; av[2][x] = t.z; av[3][x] = t.w;
       }
       if (TB) {
-        const float4 t = *reinterpret_cast<const float4*>(B + (4 * tc + x) * kLD + k0);
+        const float4 t = *reinterpret_cast<const float4*>(B + (tc + 16 * x) * kLD + k0);
         bv[0][x] = t.x; bv[1][x] = t.y; bv[2][x] = t.z; bv[3][x] = t.w;
       } else {
-        const float4 t = *reinterpret_cast<const float4*>(B + (k0 + x) * kLD + 4 * tc);
-        bv[x][0] = t.x; bv[x][1] = t.y; bv[x][2] = t.z; bv[x][3] = t.w;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) bv[kk][x] = B[(k0 + kk) * kLD + tc + 16 * x];
       }
     }
 #pragma unroll
@@ -370,11 +371,11 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     for (int x = 0; x < 4; ++x) rs_e[x] = rs_s[x] = rs_1[x] = cp_a[x] = cp_b[x] = 0.0f;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      const int t = 4 * tr + x;
+      const int t = tr + 16 * x;
       const float ah = s_ah[t], be = s_be[t], ga = s_ga[t];
 #pragma unroll
       for (int y = 0; y < 4; ++y) {
-        const int i = 4 * tc + y;
+        const int i = tc + 16 * y;
         float av = 0.0f, dc = 0.0f;
         if (i <= t) {
           const float w = __fmaf_rn(ah, s_e[i], __fmaf_rn(be, s_s[i], ga));
@@ -395,9 +396,9 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     for (int x = 0; x < 4; ++x) {
       const float e = sum16(rs_e[x]), s = sum16(rs_s[x]), o = sum16(rs_1[x]);
       if (tc == 0) {
-        r_dah[4 * tr + x] = e;
-        r_dbe[4 * tr + x] = s;
-        r_dga[4 * tr + x] = o;
+        r_dah[tr + 16 * x] = e;
+        r_dbe[tr + 16 * x] = s;
+        r_dga[tr + 16 * x] = o;
       }
     }
 #pragma unroll
@@ -405,8 +406,8 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
       const float pa = cp_a[y] + __shfl_xor_sync(0xffffffffu, cp_a[y], 16);
       const float pb = cp_b[y] + __shfl_xor_sync(0xffffffffu, cp_b[y], 16);
       if (lane < 16) {
-        colp[warp * kCk + 4 * tc + y] = pa;
-        colp[8 * kCk + warp * kCk + 4 * tc + y] = pb;
+        colp[warp * kCk + tc + 16 * y] = pa;
+        colp[8 * kCk + warp * kCk + tc + 16 * y] = pb;
       }
     }
   }
@@ -444,13 +445,13 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     float* rdst = mtx == 0 ? r_drho : mtx == 1 ? r_dbe2 : r_dga2;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      const int t = 4 * tr + x;
+      const int t = tr + 16 * x;
       const float cf = coef[t];
       float rd = 0.0f;
 #pragma unroll
       for (int y = 0; y < 4; ++y) {
         dq[x][y] = __fmaf_rn(cf, xa[x][y], dq[x][y]);
-        rd = __fmaf_rn(xa[x][y], Qs[t * kLD + 4 * tc + y], rd);
+        rd = __fmaf_rn(xa[x][y], Qs[t * kLD + tc + 16 * y], rd);
       }
       rd = sum16(rd);
       if (tc == 0) rdst[t] = rd;
@@ -475,14 +476,14 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
     gemm64<false, false>(Ks, Ms, za);  // Z[i][j] = sum_a k_i[a] D[a][j]
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      const int i = 4 * tr + x;
+      const int i = tr + 16 * x;
       const float w = mtx == 0 ? s_e[i] : mtx == 1 ? s_s[i] : 1.0f;
       float rd = 0.0f;
 #pragma unroll
       for (int y = 0; y < 4; ++y) {
         dk[x][y] = __fmaf_rn(w, ya[x][y], dk[x][y]);
         dv[x][y] = __fmaf_rn(w, za[x][y], dv[x][y]);
-        rd = __fmaf_rn(za[x][y], Vs[i * kLD + 4 * tc + y], rd);
+        rd = __fmaf_rn(za[x][y], Vs[i * kLD + tc + 16 * y], rd);
       }
       if (mtx == 0) dsp[x] = __fmul_rn(s_e[i], rd);
       if (mtx == 1) dsp[x] = __fadd_rn(dsp[x], rd);
@@ -492,20 +493,21 @@ __global__ void __launch_bounds__(kNT, 2) bwd_chunk_kernel(BwdArgs a, BwdChunkSc
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
     const float r = sum16(dsp[x]);
-    if (tc == 0) c_ds[4 * tr + x] = r;
+    if (tc == 0) c_ds[tr + 16 * x] = r;
   }
 
   // ---- outputs: dv directly; dq_hat, dk_hat staged for the unit-vector backward ----
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
-    const int t = 4 * tr + x;
-    if (t < tn)
-      *reinterpret_cast<float4*>(a.dv + (row0 + t0 + t) * kD + 4 * tc) =
-          make_float4(dv[x][0], dv[x][1], dv[x][2], dv[x][3]);
+    const int t = tr + 16 * x;
+    if (t < tn) {
+#pragma unroll
+      for (int y = 0; y < 4; ++y) a.dv[(row0 + t0 + t) * kD + tc + 16 * y] = dv[x][y];
+    }
 #pragma unroll
     for (int y = 0; y < 4; ++y) {
-      P1[t * kLD + 4 * tc + y] = dq[x][y];
-      P2[t * kLD + 4 * tc + y] = dk[x][y];
+      P1[t * kLD + tc + 16 * y] = dq[x][y];
+      P2[t * kLD + tc + 16 * y] = dk[x][y];
     }
   }
   __syncthreads();
