@@ -182,6 +182,59 @@ def aggregate_rate(units_per_rank: float, ms_per_rank: float, world: int) -> tup
 
 
 # ---------------------------------------------------------------------------------------------
+def pipelined_e2e(host_in: dict, step, steps: int, world: int) -> float:
+    """End-to-end time per step through the public API with host buffers: every step copies its
+    inputs from pinned host memory (``host_in``) to the device, runs ``step(dev_inputs)`` (which
+    returns the device result tensors) and copies the results back to pinned host memory.  Three
+    streams and two buffer sets let step i+1's host-to-device copy, step i's kernels and step
+    i-1's device-to-host copy run at the same time (a streaming pipeline; each buffer set is
+    reused only after its previous step's kernels and copy-back finished).  Returns ms per step
+    (max over ranks)."""
+    sets = [{n: torch.empty_like(t, device="cuda") for n, t in host_in.items()} for _ in range(2)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    host_out = [None, None]
+    held = [None, None]  # results of a set's last step, alive until its copy-back is ordered
+
+    def run(n_steps):
+        for i in range(n_steps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[b])
+                for n, t in host_in.items():
+                    sets[b][n].copy_(t, non_blocking=True)
+                ev_in[b].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[b])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[b])
+                res = step(sets[b])
+                held[b] = res
+                ev_cmp[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[b])
+                if host_out[b] is None:
+                    host_out[b] = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in res]
+                for h, r in zip(host_out[b], res):
+                    h.copy_(r, non_blocking=True)
+                ev_out[b].record(s_out)
+
+    run(4)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    run(steps)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) / steps, world)
+
+
 def oracle_rate(w: zi.Workload, inp_cpu: dict, seqs: int, tokens: int, nthreads: int,
                 min_seconds: float = 0.0):
     """Run the fp64 oracle on `seqs` sequences x `tokens` tokens, repeated until `min_seconds`
@@ -305,34 +358,21 @@ def ours_forward(args, w: zi.Workload):
     alg = algorithmic_bytes(w)
     achieved = alg / (ms / 1e3) / 1e9
 
-    # ---- end to end through the public API with host buffers ----
+    # ---- end to end through the public API with host buffers (pipelined over steps) ----
     names = ("q", "k", "v", "u", "g1", "gh", "mu", "tau")
     host = {n: inp[n].cpu().pin_memory() for n in names}
-    dev_in = {n: torch.empty_like(inp[n]) for n in names}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = out.numel() * out.element_size()
+    outs = {}
 
-    def e2e_step():
-        for n in names:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        o = zs.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["u"], dev_in["g1"],
-                   dev_in["gh"], dev_in["mu"], dev_in["tau"], causal=w.causal, rope=w.rope,
-                   rope_base=w.rope_base, out=out, path=args.path, **ln)
-        host_out.copy_(o, non_blocking=True)
+    def e2e_step(src):
+        o = outs.setdefault(src["q"].data_ptr(), torch.empty_like(out))
+        zs.fwd(src["q"], src["k"], src["v"], src["u"], src["g1"], src["gh"], src["mu"],
+               src["tau"], causal=w.causal, rope=w.rope, rope_base=w.rope_base, out=o,
+               path=args.path, **ln)
+        return [o]
 
-    e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_ms = pipelined_e2e(host, e2e_step, max(3, min(args.steps, 20)), world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -423,36 +463,17 @@ def ours_backward(args, w: zi.Workload):
     hbm, kind = peaks()
     alg = backward_bytes(w)
 
-    # end to end with host buffers: inputs and dout in, every gradient out
+    # end to end with host buffers: inputs and dout in, every gradient out (pipelined)
     host = {n: inp[n].cpu().pin_memory() for n in names}
-    host_do = dout.cpu().pin_memory()
-    dev_in = {n: torch.empty_like(inp[n]) for n in names}
-    dev_do = torch.empty_like(dout)
+    host["dout"] = dout.cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     grads = step(inp, dout)
-    host_g = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in grads.items()}
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_do.numel() * host_do.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in host_g.values())
+    d2h = sum(t.numel() * t.element_size() for t in grads.values())
 
-    def e2e_step():
-        for n in names:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        dev_do.copy_(host_do, non_blocking=True)
-        g = step(dev_in, dev_do)
-        for n, t in g.items():
-            host_g[n].copy_(t, non_blocking=True)
+    def e2e_step(src):
+        return list(step(src, src["dout"]).values())
 
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_ms = pipelined_e2e(host, e2e_step, max(3, min(args.steps, 10)), world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -557,28 +578,17 @@ def ours_sm(args, w: zi.Workload):
     achieved = sm_flops(w) / (ms / 1e3) / 1e12
 
     host = {n: inp[n].cpu().pin_memory() for n in names}
-    dev_in = {n: torch.empty_like(inp[n]) for n in names}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = out.numel() * out.element_size()
+    outs = {}
 
-    def e2e_step():
-        for n in names:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        host_out.copy_(step(dev_in), non_blocking=True)
+    def e2e_step(src):
+        o = outs.setdefault(src["q"].data_ptr(), torch.empty_like(out))
+        zs.sm_fwd(*(src[n] for n in names), causal=w.causal, rope=w.rope,
+                  rope_base=w.rope_base, out=o)
+        return [o]
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, min(args.steps, 10))
-    e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+    e2e_ms = pipelined_e2e(host, e2e_step, max(3, min(args.steps, 10)), world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
