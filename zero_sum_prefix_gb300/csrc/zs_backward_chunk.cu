@@ -627,29 +627,29 @@ __global__ void __launch_bounds__(kNT) bwd_ds_kernel(BwdArgs a, BwdChunkScratch 
 }
 
 // ubar (prefix of u), Z (suffix of ds u / (e^tau + t)), du = -(ds ubar + Z)/sqrt d and the d tau
-// partial sums.  One CTA per (b, h): 16 token segments x 64 columns, the segments' totals
-// combined through shared memory.
-constexpr int kSeg = 16;
+// partial sums.  Grid (b h, column groups of 16): 64 token segments x 16 columns per CTA, the
+// segments' totals combined through shared memory.
+constexpr int kSeg = 64, kCols = 16;
 template <typename T>
-__global__ void __launch_bounds__(kSeg * kD) bwd_du_kernel(BwdArgs a, BwdChunkScratch scr) {
-  __shared__ float segu[kSeg][kD], segz[kSeg][kD];
-  __shared__ float red[kSeg * kD / 32];
+__global__ void __launch_bounds__(kSeg * kCols) bwd_du_kernel(BwdArgs a, BwdChunkScratch scr) {
+  __shared__ float segu[kSeg][kCols], segz[kSeg][kCols];
+  __shared__ float red[kSeg * kCols / 32];
   const int bh = blockIdx.x, h = bh % a.H;
   const int N = a.N, tid = threadIdx.x;
   const size_t row0 = (size_t)bh * N;
   const float etau = expf(a.tau[h]);
   const float rsd = __fdiv_rn(1.0f, __fsqrt_rn((float)kD));
   const T* __restrict__ u = static_cast<const T*>(a.u) + row0 * kD;
-  const int g = tid / kD, j = tid % kD;
+  const int g = tid / kCols, jj = tid % kCols, j = blockIdx.y * kCols + jj;
   const int L = (N + kSeg - 1) / kSeg, ta = min(N, g * L), tb = min(N, ta + L);
   const float mu = a.mu[(size_t)h * kD + j];
   float su = 0.0f;
 #pragma unroll 4
   for (int t = ta; t < tb; ++t) su = __fadd_rn(su, ld(u, (size_t)t * kD + j));
-  segu[g][j] = su;
+  segu[g][jj] = su;
   __syncthreads();
   float S = 0.0f;
-  for (int x = 0; x < g; ++x) S = __fadd_rn(S, segu[x][j]);
+  for (int x = 0; x < g; ++x) S = __fadd_rn(S, segu[x][jj]);
   const float emu = __fmul_rn(etau, mu);
   float zl = 0.0f;
 #pragma unroll 4
@@ -660,10 +660,10 @@ __global__ void __launch_bounds__(kSeg * kD) bwd_du_kernel(BwdArgs a, BwdChunkSc
     scr.ubar[(row0 + t) * kD + j] = __fmul_rn(__fadd_rn(emu, S), wt);
     zl = __fmaf_rn(__fmul_rn(scr.tok[(row0 + t) * 4 + 3], ut), wt, zl);
   }
-  segz[g][j] = zl;
+  segz[g][jj] = zl;
   __syncthreads();
   float z = 0.0f;
-  for (int x = g + 1; x < kSeg; ++x) z = __fadd_rn(z, segz[x][j]);
+  for (int x = g + 1; x < kSeg; ++x) z = __fadd_rn(z, segz[x][jj]);
   float tacc = 0.0f;
 #pragma unroll 4
   for (int t = tb - 1; t >= ta; --t) {
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(kSeg * kD) bwd_du_kernel(BwdArgs a, BwdChunkSc
   __syncthreads();
   if (tid == 0) {
     float ts = 0.0f;
-    for (int w = 0; w < kSeg * kD / 32; ++w) ts = __fadd_rn(ts, red[w]);
+    for (int w = 0; w < kSeg * kCols / 32; ++w) ts = __fadd_rn(ts, red[w]);
     atomicAdd(a.dtau + h, -__fmul_rn(__fmul_rn(etau, ts), rsd));
   }
 }
@@ -709,7 +709,7 @@ cudaError_t launch_chunk_t(const BwdArgs& a, const BwdChunkScratch& sc, cudaStre
   bwd_states_kernel<T><<<dim3(BH, kSlices, 2), kNT, 0, stream>>>(a, sc);
   bwd_chunk_kernel<T><<<(unsigned)(BH * NC), kNT, ChunkSmem::BYTES, stream>>>(a, sc);
   bwd_ds_kernel<<<BH, kNT, 0, stream>>>(a, sc);
-  bwd_du_kernel<T><<<BH, kSeg * kD, 0, stream>>>(a, sc);
+  bwd_du_kernel<T><<<dim3(BH, kD / kCols), kSeg * kCols, 0, stream>>>(a, sc);
   count_launches(5);
   return cudaGetLastError();
 }
