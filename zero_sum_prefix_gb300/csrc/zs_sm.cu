@@ -244,9 +244,9 @@ __device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, 
       stat_chunk(ra);
       tmem_wait_ld();
       reg_fence(rb);
-      stat_chunk(rb);
       tc_fence_before();
-      mbar_arrive(&ms->s_free[w]);
+      mbar_arrive(&ms->s_free[w]);  // every column of S is in registers: release the buffer
+      stat_chunk(rb);
       continue;
     }
 #pragma unroll 1
@@ -357,10 +357,11 @@ __device__ void sm_epilogue(const SmArgs& a, uint8_t* smem, SmMisc* ms, int bh, 
       w_chunk(ra, 2);
       tmem_wait_ld();
       reg_fence(rb);
+      tc_fence_before();
+      mbar_arrive(&ms->s_free[w]);  // every column of S is in registers: release the buffer
       w_chunk(rb, 3);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ms->s_free[w]);
       mbar_arrive(&ms->w_full[w]);
       continue;
     }
