@@ -65,7 +65,8 @@ def _run(zs, w, path, gain, eps, seed):
     (64, 129, True, "bf16", "chunk", False, 1e-3), (128, 1, True, "bf16", "chunk", True, 1e-5),
     (64, 129, True, "bf16", "simt", True, 1e-5), (32, 77, True, "f32", "simt", True, 1e-5),
     (64, 77, True, "f32", "simt", True, 1e-5), (128, 40, True, "f32", "simt", False, 1e-5),
-    (64, 50, False, "bf16", "simt", True, 1e-5), (128, 50, False, "f32", "simt", True, 1e-5)])
+    (64, 50, False, "bf16", "simt", True, 1e-5), (128, 50, False, "f32", "simt", True, 1e-5),
+    (64, 130, False, "f32", "auto", True, 1e-5), (64, 200, False, "bf16", "auto", False, 1e-5)])
 def test_forward_layernorm(zs, d, N, causal, dtype, path, gain, eps):
     w = zi.Workload("ln", 2, 3, N, d, dtype=dtype, causal=causal, rope=causal,
                     seed=500 + d + N)

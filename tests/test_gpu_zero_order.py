@@ -36,7 +36,8 @@ def _oracle(inp, w, g0):
 @pytest.mark.parametrize("d,N,causal,dtype,path", [
     (64, 300, True, "bf16", "chunk"), (128, 300, True, "bf16", "chunk"),
     (64, 129, True, "bf16", "simt"), (32, 77, True, "f32", "simt"),
-    (64, 50, False, "bf16", "simt"), (64, 50, False, "f32", "simt")])
+    (64, 50, False, "bf16", "simt"), (64, 50, False, "f32", "simt"),
+    (64, 150, False, "bf16", "auto"), (64, 70, False, "f32", "auto")])
 def test_forward_with_zero_order_gate(zs, d, N, causal, dtype, path):
     w = zi.Workload("g0", 2, 2, N, d, dtype=dtype, causal=causal, rope=causal, seed=300 + d + N)
     inp = zi.make(w, "cuda")

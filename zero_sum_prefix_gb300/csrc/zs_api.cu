@@ -254,6 +254,10 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
     return fail(ZEROS_ERR_UNSUPPORTED,
                 "the chunked tensor-core path needs bf16, causal mode and d in {64, 128}");
   const bool use_chunk = chunk_ok && path != ZEROS_PATH_SIMT;
+  // encoder mode: the tiled kernel, unless the token-sequential path or its debug scalars are
+  // asked for
+  const bool use_enc = !causal && enc_supported(d) && path != ZEROS_PATH_SIMT && !dbg_s &&
+                       !dbg_E && !dbg_P && !dbg_m;
   if (B == 0 || H == 0 || (N == 0 && !final_state)) return ZEROS_OK;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -301,7 +305,9 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
   if (rope && !use_chunk) {  // the chunked kernel computes its rotary factors itself
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
-  cudaError_t e = use_chunk ? launch_fwd_chunk(a, st) : launch_fwd_simt(a, st);
+  cudaError_t e = use_chunk ? launch_fwd_chunk(a, st)
+                  : use_enc ? launch_fwd_encoder(a, st)
+                            : launch_fwd_simt(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ZEROS_OK;
 }

@@ -97,6 +97,10 @@ bool bwd_chunk_supported(int d);
 size_t bwd_chunk_scratch_bytes(int B, int H, int N, int d);
 cudaError_t launch_bwd_chunk(const BwdArgs& a, float* scratch, cudaStream_t stream);
 
+// zs_encoder.cu: encoder-mode forward in 64-token tiles (d = 64; no debug outputs)
+bool enc_supported(int d);
+cudaError_t launch_fwd_encoder(const FwdArgs& a, cudaStream_t stream);
+
 // zs_sm.cu
 bool sm_supported(int d, int dtype);
 cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream);
