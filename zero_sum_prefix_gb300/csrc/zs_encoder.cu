@@ -13,7 +13,7 @@
 // tiles of 64 tokens: a pass over the tokens for sum u, a pass accumulating the states in
 // registers (each thread 3 x 16 state entries; the F state rescaled when the maximum grows), and
 // a pass of 64 x 64 x 64 fp32 tile products Q [F|G|H] for the outputs, with the optional output
-// LayerNorm fused.  All arithmetic fp32 (the token-sequential kernel remains the path that
+// LayerNorm fused.  Tiles are loaded with 16-byte vectors, four lanes per row.  All arithmetic fp32 (the token-sequential kernel remains the path that
 // reports per-token debug scalars).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,28 +41,86 @@ struct EncSmem {
   static constexpr unsigned BYTES = FLOATS * 4;
 };
 
-// Rotated unit vector of row t (one warp; lane owns columns lane and lane + 32 = one rotary
-// pair) into dst; returns nothing (the norm is not needed in encoder mode's outputs: q and k
-// enter only through their directions).
+// Tile helpers: thread (r = tid / 4, quarter qq = tid % 4) owns columns 16 qq .. 16 qq + 15 of
+// row r of a 64 x 64 tile (row stride kLD), so that every global load is a 16-byte vector and
+// every row is handled by four neighbouring lanes.
 template <typename T>
-__device__ __forceinline__ void enc_unit_row(const T* src, const FwdArgs& a, int t, float* dst) {
-  const int lane = threadIdx.x & 31;
-  float x0 = ld(src, lane), x1 = ld(src, lane + 32);
-  float ss = __fmaf_rn(x0, x0, __fmul_rn(x1, x1));
+__device__ __forceinline__ void load16(const T* src, float (&x)[16]);
+template <>
+__device__ __forceinline__ void load16<float>(const float* src, float (&x)[16]) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(ss), 1e-12f));
-  x0 *= inv;
-  x1 *= inv;
-  if (a.rope) {
-    const float2 cs = a.rope_table[(size_t)t * (kD / 2) + lane];
-    const float y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-    const float y1 = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
-    x0 = y0;
-    x1 = y1;
+  for (int i = 0; i < 4; ++i) {
+    const float4 t = reinterpret_cast<const float4*>(src)[i];
+    x[4 * i] = t.x; x[4 * i + 1] = t.y; x[4 * i + 2] = t.z; x[4 * i + 3] = t.w;
   }
-  dst[lane] = x0;
-  dst[lane + 32] = x1;
+}
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* src, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 t = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+      x[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+  }
+}
+
+// Row r of the tile (zero past the sequence) into registers x; returns the row's squared norm
+// (summed over the four lanes of the row).
+template <typename T>
+__device__ __forceinline__ float tile_row(const T* base, int t0, int tn, float (&x)[16]) {
+  const int r = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  if (r < tn) {
+    load16<T>(base + (size_t)(t0 + r) * kD + 16 * qq, x);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  return ss;
+}
+
+__device__ __forceinline__ void store_row(float* dst, const float (&x)[16]) {
+  const int r = threadIdx.x >> 2, qq = threadIdx.x & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(dst + r * kLD + 16 * qq + 4 * i) =
+        make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+}
+
+// Unit rows of a tile (rotated to their positions when rope): loads, normalises and stores; the
+// rotation of the pairs (a, a + 32) runs after a barrier, thread (r, p) taking pairs 8p .. 8p + 7.
+template <typename T>
+__device__ __forceinline__ void unit_tile(const T* base, const FwdArgs& a, int t0, int tn,
+                                          float* dst) {
+  float x[16];
+  const float ss = tile_row<T>(base, t0, tn, x);
+  const float inv = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(ss), 1e-12f));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] *= inv;
+  store_row(dst, x);
+  if (a.rope) {
+    __syncthreads();
+    const int r = threadIdx.x >> 2, p = threadIdx.x & 3;
+    if (r < tn) {
+      const float2* tab = a.rope_table + (size_t)(t0 + r) * (kD / 2) + 8 * p;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c0 = 8 * p + e;
+        const float2 cs = tab[e];
+        const float x0 = dst[r * kLD + c0], x1 = dst[r * kLD + c0 + 32];
+        dst[r * kLD + c0] = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+        dst[r * kLD + c0 + 32] = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+      }
+    }
+  }
 }
 
 template <typename T>
@@ -102,16 +160,13 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
   }
   __syncthreads();
   const float den = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)kD));
-  float n0, n1;  // this lane's two columns of the numerator (lane, lane + 32)
-  {
-    float s0 = 0.0f, s1 = 0.0f;
-    for (int g = 0; g < kNT / kD; ++g) {
-      s0 += red[g * kD + lane];
-      s1 += red[g * kD + lane + 32];
-    }
-    n0 = __fmaf_rn(etau, a.mu[(size_t)h * kD + lane], s0);
-    n1 = __fmaf_rn(etau, a.mu[(size_t)h * kD + lane + 32], s1);
+  __shared__ float nv[kD];  // numerator e^tau mu + sum_j u_j
+  if (tid < kD) {
+    float s0 = 0.0f;
+    for (int g = 0; g < kNT / kD; ++g) s0 += red[g * kD + tid];
+    nv[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], s0);
   }
+  __syncthreads();
 
   // ---- states: thread owns row ar, columns cj .. cj + 15 of F~, G, H ----
   const int ar = tid >> 2, cj = (tid & 3) * 16;
@@ -123,22 +178,19 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
   const int NT = (N + kT - 1) / kT;
   for (int c = 0; c < NT; ++c) {
     const int t0 = c * kT, tn = min(N, t0 + kT) - t0;
-    for (int r = warp; r < kT; r += kNT / 32) {
-      if (r < tn) {
-        const int t = t0 + r;
-        enc_unit_row<T>(k + (size_t)t * kD, a, t, Rt + r * kLD);
-        Vt[r * kLD + lane] = ld(v, (size_t)t * kD + lane);
-        Vt[r * kLD + lane + 32] = ld(v, (size_t)t * kD + lane + 32);
-        float dot = __fmaf_rn(ld(u, (size_t)t * kD + lane), n0,
-                              __fmul_rn(ld(u, (size_t)t * kD + lane + 32), n1));
+    unit_tile<T>(k, a, t0, tn, Rt);
+    {
+      float x[16];
+      tile_row<T>(v, t0, tn, x);
+      store_row(Vt, x);
+      tile_row<T>(u, t0, tn, x);  // logits: s = -(u . n) / ((e^tau + N) sqrt d)
+      const int r = tid >> 2, qq = tid & 3;
+      float dot = 0.0f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) ts[r] = -__fdiv_rn(dot, den);
-      } else {
-        Rt[r * kLD + lane] = Rt[r * kLD + lane + 32] = 0.0f;
-        Vt[r * kLD + lane] = Vt[r * kLD + lane + 32] = 0.0f;
-        if (lane == 0) ts[r] = -INFINITY;
-      }
+      for (int i = 0; i < 16; ++i) dot = __fmaf_rn(x[i], nv[16 * qq + i], dot);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      if (qq == 0) ts[r] = r < tn ? -__fdiv_rn(dot, den) : -INFINITY;
     }
     __syncthreads();
     if (warp == 0) {  // tile maximum, new running maximum, E~ and P
@@ -203,13 +255,7 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
   const int tr = tid >> 4, tc = tid & 15;
   for (int c = 0; c < NT; ++c) {
     const int t0 = c * kT, tn = min(N, t0 + kT) - t0;
-    for (int r = warp; r < kT; r += kNT / 32) {
-      if (r < tn) {
-        enc_unit_row<T>(q + (size_t)(t0 + r) * kD, a, t0 + r, Rt + r * kLD);
-      } else {
-        Rt[r * kLD + lane] = Rt[r * kLD + lane + 32] = 0.0f;
-      }
-    }
+    unit_tile<T>(q, a, t0, tn, Rt);
     if (tid < kT) {
       float al = 0.0f, be = 0.0f, ga = 0.0f;
       if (tid < tn) {
