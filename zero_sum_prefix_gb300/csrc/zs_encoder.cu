@@ -23,6 +23,7 @@
 
 #include "zs_common.cuh"
 #include "zs_internal.h"
+#include "zs_sm100.cuh"
 #include "zs_tiles.cuh"
 
 namespace zs {
@@ -31,6 +32,7 @@ namespace {
 using tiles::gemm64;
 using tiles::sum16;
 using tiles::zero44;
+using namespace sm100;
 
 constexpr int kD = 64, kT = 64, kNT = 256, kLD = tiles::kLD;
 
@@ -312,6 +314,323 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
   }
 }
 
+// ============================================================== tensor-core encoder (bf16)
+// The same computation with both contractions on tcgen05 (bf16 operands, fp32 accumulation in
+// TMEM), one CTA of 128 threads per sequence, thread = token row of a 128-token tile:
+//   states:  D1 = [e o v | s o v]^T K_hat  (M = 128: rows 0..63 = F~^T, 64..127 = G^T),
+//            D2 = [v | e o v]^T K_hat       (rows 0..63 = H^T; the rest unused),
+//            accumulated over the token tiles (A operands MN-major from the swizzled value
+//            atoms, B = the k_hat atom, K = tokens);
+//   outputs: D3 = Q_hat [F~ | G | H] (M = 128 tokens, N = 192, K = d), the states copied to a
+//            K-major bf16 tile first, and o_t = alpha~_t D3_F + beta_t D3_G + gamma_t D3_H.
+// The three terms nearly cancel (the weights sum to zero), so e o v, s o v and the states are
+// each split into bf16 hi and lo parts (two products accumulated into one TMEM tile): only
+// k_hat, q_hat and v, which the three terms share, are rounded to bf16 once.
+// The logits of the whole sequence stay in shared memory (N <= kTcNMax).
+constexpr int kTcThreads = 128, kTcT = 128, kTcNMax = 4096;
+constexpr uint32_t kAtom = 128 * 128;  // [128 rows x 64 bf16], 128-byte swizzle
+
+struct EncTcSmem {
+  // value atoms: v, then the hi and lo bf16 parts of e o v and s o v (the A operand pairs
+  // [EVH | SVH] and [EVL | SVL] are contiguous), the k_hat / q_hat atom
+  static constexpr uint32_t AV = 0, EVH = kAtom, SVH = 2 * kAtom, EVL = 3 * kAtom,
+                            SVL = 4 * kAtom, KQ = 5 * kAtom;
+  static constexpr uint32_t BHI = 6 * kAtom;              // [192 rows][64] K-major states, hi
+  static constexpr uint32_t BLO = BHI + 192 * 128;        // and lo bf16 parts
+  static constexpr uint32_t SARR = BLO + 192 * 128;       // float [kTcNMax] logits
+  static constexpr uint32_t RED = SARR + kTcNMax * 4;     // float [2][kD] + misc
+  static constexpr uint32_t BAR = RED + (2 * kD + 8) * 4; // mbarrier, TMEM address
+  static constexpr uint32_t BYTES = BAR + 64;
+  static_assert(BYTES + 1024 <= 233472, "one CTA per SM");
+};
+
+__device__ __forceinline__ void put_row_bf16(uint8_t* atom, int r, const float (&x)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(atom + sw128_off(r, c)) =
+        make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                   pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+}
+
+// Row r of scale * x as the bf16 pair (hi, lo) with hi + lo = scale * x to about 2^-17: the
+// three state terms nearly cancel (the weights sum to zero), so each is kept to fp32 accuracy.
+__device__ __forceinline__ void put_row_split(uint8_t* hi_atom, uint8_t* lo_atom, int r,
+                                              float scale, const float (&x)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float y0 = scale * x[8 * c + 2 * e], y1 = scale * x[8 * c + 2 * e + 1];
+      const float h0 = __bfloat162float(__float2bfloat16_rn(y0));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(y1));
+      ph[e] = pack_bf16x2(h0, h1);
+      pl[e] = pack_bf16x2(y0 - h0, y1 - h1);
+    }
+    *reinterpret_cast<uint4*>(hi_atom + sw128_off(r, c)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4*>(lo_atom + sw128_off(r, c)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+  }
+}
+
+// Row t of a bf16 tensor (64 values) into x; zero when t is past the sequence.
+__device__ __forceinline__ void get_row_bf16(const __nv_bfloat16* src, bool valid, float (&x)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) w = reinterpret_cast<const uint4*>(src)[c];
+    unpack_bf16x2(w.x, x[8 * c], x[8 * c + 1]);
+    unpack_bf16x2(w.y, x[8 * c + 2], x[8 * c + 3]);
+    unpack_bf16x2(w.z, x[8 * c + 4], x[8 * c + 5]);
+    unpack_bf16x2(w.w, x[8 * c + 6], x[8 * c + 7]);
+  }
+}
+
+// Unit row (rotated to position t with rope; pairs (a, a + 32) are both in this thread).
+__device__ __forceinline__ void unit_rot_row(const FwdArgs& a, int t, bool valid, float (&x)[64]) {
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+  const float inv = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(ss), 1e-12f));
+#pragma unroll
+  for (int i = 0; i < 64; ++i) x[i] *= inv;
+  if (a.rope && valid) {
+    const float2* tab = a.rope_table + (size_t)t * (kD / 2);
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      const float2 cs = tab[p];
+      const float x0 = x[p], x1 = x[p + 32];
+      x[p] = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+      x[p + 32] = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
+  using SM = EncTcSmem;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) report(a.status, kErrUnsupported);
+    return;
+  }
+  float* sarr = reinterpret_cast<float*>(smem + SM::SARR);
+  float* red = reinterpret_cast<float*>(smem + SM::RED);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SM::BAR + 8);
+  int* abort_flag = reinterpret_cast<int*>(smem + SM::BAR + 12);
+  const int bh = blockIdx.x, h = bh % a.H;
+  const int N = a.N, tid = threadIdx.x, warp = tid >> 5;
+  const size_t row0 = (size_t)bh * N;
+  const __nv_bfloat16* __restrict__ q = static_cast<const __nv_bfloat16*>(a.q) + row0 * kD;
+  const __nv_bfloat16* __restrict__ k = static_cast<const __nv_bfloat16*>(a.k) + row0 * kD;
+  const __nv_bfloat16* __restrict__ v = static_cast<const __nv_bfloat16*>(a.v) + row0 * kD;
+  const __nv_bfloat16* __restrict__ u = static_cast<const __nv_bfloat16*>(a.u) + row0 * kD;
+  __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out) + row0 * kD;
+  const float etau = expf(a.tau[h]);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  // ---- prior numerator: column j summed by threads j and j + 64 over alternate tokens ----
+  {
+    const int j = tid & (kD - 1), g = tid >> 6;
+    float su = 0.0f;
+    for (int t = g; t < N; t += 2) su += __bfloat162float(u[(size_t)t * kD + j]);
+    red[g * kD + j] = su;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lane quadrant
+  if (tid < kD) red[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], red[tid] + red[kD + tid]);
+  __syncthreads();
+  const float den = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)kD));
+  // ---- logits of every token (thread per token), maximum, E~ and P ----
+  float lmax = -INFINITY, lsum = 0.0f;
+  for (int t = tid; t < N; t += kTcThreads) {
+    float x[64];
+    get_row_bf16(u + (size_t)t * kD, true, x);
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) dot = __fmaf_rn(x[i], red[i], dot);
+    const float s = -__fdiv_rn(dot, den);
+    sarr[t] = s;
+    lmax = fmaxf(lmax, s);
+    lsum += s;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+  }
+  if ((tid & 31) == 0) {
+    red[2 * kD + warp] = lmax;
+    red[2 * kD + 4 + warp] = lsum;
+  }
+  __syncthreads();
+  const float m = fmaxf(fmaxf(red[2 * kD], red[2 * kD + 1]), fmaxf(red[2 * kD + 2], red[2 * kD + 3]));
+  const float P = (red[2 * kD + 4] + red[2 * kD + 5]) + (red[2 * kD + 6] + red[2 * kD + 7]);
+  if (!isfinite(m)) report(a.status, kErrRange);
+  float esum = 0.0f;
+  for (int t = tid; t < N; t += kTcThreads) esum += expf(__fsub_rn(sarr[t], m));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) esum += __shfl_xor_sync(0xffffffffu, esum, o);
+  __syncthreads();  // everyone has read the maxima and sums above
+  if ((tid & 31) == 0) red[2 * kD + warp] = esum;
+  __syncthreads();
+  const float Et = (red[2 * kD] + red[2 * kD + 1]) + (red[2 * kD + 2] + red[2 * kD + 3]);
+
+  // ---- states over the token tiles ----
+  constexpr uint32_t id_st = idesc_bf16_f32(128, kD, true, true);
+  const uint32_t base = smem_u32(smem);
+  const int NT = (N + kTcT - 1) / kTcT;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int tt = 0; tt < NT && ok; ++tt) {
+    const int t = tt * kTcT + tid;
+    const bool valid = t < N;
+    float x[64];
+    get_row_bf16(k + (size_t)t * kD, valid, x);
+    unit_rot_row(a, t, valid, x);
+    put_row_bf16(smem + SM::KQ, tid, x);
+    get_row_bf16(v + (size_t)t * kD, valid, x);
+    put_row_bf16(smem + SM::AV, tid, x);
+    const float s = valid ? sarr[t] : 0.0f;
+    const float e = valid ? expf(__fsub_rn(s, m)) : 0.0f;
+    put_row_split(smem + SM::EVH, smem + SM::EVL, tid, e, x);
+    put_row_split(smem + SM::SVH, smem + SM::SVL, tid, s, x);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTcT / 16; ++kk) {
+        const uint32_t off = kk * 2048;  // 16 token rows per step
+        const uint32_t acc = (tt > 0 || kk > 0) ? 1u : 0u;
+        const uint64_t bk = sw128_desc(base + SM::KQ + off, kAtom, 1024);
+        mma_bf16(tm, sw128_desc(base + SM::EVH + off, kAtom, 1024), bk, id_st, acc);
+        mma_bf16(tm, sw128_desc(base + SM::EVL + off, kAtom, 1024), bk, id_st, 1u);
+        mma_bf16(tm + 64, sw128_desc(base + SM::AV + off, kAtom, 1024), bk, id_st, acc);
+      }
+      mma_commit(bar);
+    }
+    ok = mbar_wait(bar, phase, abort_flag);
+    phase ^= 1u;
+    tc_fence_after();
+    ok = __syncthreads_and(ok) != 0;  // uniform, and the tiles may be rewritten
+  }
+  if (!ok) report(a.status, kErrTimeout);
+
+  // ---- states -> K-major bf16 hi/lo tiles: rows 0..63 F~, 64..127 G (D1), 128..191 H (D2) ----
+  if (ok) {
+    float x[64];
+    tmem_ld32(tl + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+    tmem_ld32(tl + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+    put_row_split(smem + SM::BHI, smem + SM::BLO, tid, 1.0f, x);
+    tmem_ld32(tl + 64, *reinterpret_cast<float(*)[32]>(&x[0]));
+    tmem_ld32(tl + 96, *reinterpret_cast<float(*)[32]>(&x[32]));
+    if (tid < kD) put_row_split(smem + SM::BHI, smem + SM::BLO, 128 + tid, 1.0f, x);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- outputs per token tile: D3 = Q_hat [F~|G|H], combined with the row coefficients ----
+  constexpr uint32_t id_out = idesc_bf16_f32(128, 3 * kD, false, false);
+  const float rN = __fdiv_rn(1.0f, (float)N);
+  for (int tt = 0; tt < NT && ok; ++tt) {
+    const int t = tt * kTcT + tid;
+    const bool valid = t < N;
+    float x[64];
+    get_row_bf16(q + (size_t)t * kD, valid, x);
+    unit_rot_row(a, t, valid, x);
+    put_row_bf16(smem + SM::KQ, tid, x);
+    float al = 0.0f, be = 0.0f, ga = 0.0f;
+    if (valid) {
+      const size_t row = row0 + t;
+      const float sig1 = sigmoid(a.g1[row]), sigh = sigmoid(a.gh[row]);
+      be = __fmul_rn(__fsub_rn(sig1, sigh), rN);
+      ga = -__fadd_rn(__fmul_rn(__fmul_rn(be, P), rN), __fmul_rn(sigh, rN));
+      if (a.g0) ga = __fadd_rn(ga, __fmul_rn(sigmoid(a.g0[row]), rN));
+      al = __fdiv_rn(sigh, Et);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = kk * 32;  // 16 K values = 32 bytes inside the swizzled row
+        const uint64_t aq = sw128_desc(base + SM::KQ + off, 16, 1024);
+        mma_bf16(tm, aq, sw128_desc(base + SM::BHI + off, 16, 1024), id_out, kk > 0 ? 1u : 0u);
+        mma_bf16(tm, aq, sw128_desc(base + SM::BLO + off, 16, 1024), id_out, 1u);
+      }
+      mma_commit(bar);
+    }
+    ok = mbar_wait(bar, phase, abort_flag);
+    phase ^= 1u;
+    tc_fence_after();
+    ok = __syncthreads_and(ok) != 0;  // uniform before the aligned TMEM loads
+    if (!ok) break;
+    float o[64];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float f[32], g2[32], hh[32];
+      tmem_ld32(tl + 32 * half, f);
+      tmem_ld32(tl + 64 + 32 * half, g2);
+      tmem_ld32(tl + 128 + 32 * half, hh);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        o[32 * half + j] = __fmaf_rn(al, f[j], __fmaf_rn(be, g2[j], __fmul_rn(ga, hh[j])));
+    }
+    if (a.ln) {  // output LayerNorm over the row (the whole row is in this thread)
+      float mean = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) mean += o[j];
+      mean *= (1.0f / kD);
+      float var = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) var = __fmaf_rn(o[j] - mean, o[j] - mean, var);
+      const float rstd = rsqrtf(var * (1.0f / kD) + a.ln_eps);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const float w = a.ln_w ? a.ln_w[(size_t)h * kD + j] : 1.0f;
+        const float b = a.ln_b ? a.ln_b[(size_t)h * kD + j] : 0.0f;
+        o[j] = __fmaf_rn((o[j] - mean) * rstd, w, b);
+      }
+    }
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)t * kD);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
+                            pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
+                            pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+    }
+    tc_fence_before();
+    __syncthreads();  // D3 read and the q tile consumed before the next tile
+  }
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    // the products of the phase that was not observed must finish before TMEM is released
+    if (tid == 0) {
+      int never = 0;
+      mbar_wait(bar, phase ^ 1u, &never, 1ll << 32);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 256);
+  }
+}
+
 }  // namespace
 
 bool enc_supported(int d) { return d == kD; }
@@ -332,10 +651,20 @@ cudaError_t launch_fwd_encoder(const FwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[f32].fetch_or(bit);
   }
-  if (f32)
+  if (!f32 && a.N <= kTcNMax) {  // bf16: both contractions on the tensor cores
+    static std::atomic<uint64_t> tc_set{0};
+    if (!(tc_set.load() & bit)) {
+      e = cudaFuncSetAttribute(enc_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)EncTcSmem::BYTES);
+      if (e != cudaSuccess) return e;
+      tc_set.fetch_or(bit);
+    }
+    enc_tc_kernel<<<a.B * a.H, kTcThreads, EncTcSmem::BYTES, stream>>>(a);
+  } else if (f32) {
     enc_kernel<float><<<a.B * a.H, kNT, EncSmem::BYTES, stream>>>(a);
-  else
+  } else {
     enc_kernel<__nv_bfloat16><<<a.B * a.H, kNT, EncSmem::BYTES, stream>>>(a);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
