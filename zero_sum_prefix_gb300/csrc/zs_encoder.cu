@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
 // The three terms nearly cancel (the weights sum to zero), so e o v, s o v and the states are
 // each split into bf16 hi and lo parts (two products accumulated into one TMEM tile): only
 // k_hat, q_hat and v, which the three terms share, are rounded to bf16 once.
-// The logits of the whole sequence stay in shared memory (N <= kTcNMax).
-constexpr int kTcThreads = 128, kTcT = 128, kTcNMax = 4096;
+// Each token's logit is recomputed where it is needed (three light passes over u).
+constexpr int kTcThreads = 128, kTcT = 128, kTcNMax = 1 << 20;
 constexpr uint32_t kAtom = 128 * 128;  // [128 rows x 64 bf16], 128-byte swizzle
 
 struct EncTcSmem {
@@ -335,13 +335,15 @@ struct EncTcSmem {
   // [EVH | SVH] and [EVL | SVL] are contiguous), the k_hat / q_hat atom
   static constexpr uint32_t AV = 0, EVH = kAtom, SVH = 2 * kAtom, EVL = 3 * kAtom,
                             SVL = 4 * kAtom, KQ = 5 * kAtom;
-  static constexpr uint32_t BHI = 6 * kAtom;              // [192 rows][64] K-major states, hi
-  static constexpr uint32_t BLO = BHI + 192 * 128;        // and lo bf16 parts
-  static constexpr uint32_t SARR = BLO + 192 * 128;       // float [kTcNMax] logits
-  static constexpr uint32_t RED = SARR + kTcNMax * 4;     // float [2][kD] + misc
+  // [192 rows][64] K-major states, hi and lo bf16 parts: written after the last state product,
+  // over the value atoms, which are dead by then (the q_hat atom KQ stays separate)
+  static constexpr uint32_t BHI = 0;
+  static constexpr uint32_t BLO = BHI + 192 * 128;
+  static_assert(BLO + 192 * 128 <= KQ, "the state tiles overlay the value atoms only");
+  static constexpr uint32_t RED = 6 * kAtom;              // float [2][kD] + misc
   static constexpr uint32_t BAR = RED + (2 * kD + 8) * 4; // mbarrier, TMEM address
   static constexpr uint32_t BYTES = BAR + 64;
-  static_assert(BYTES + 1024 <= 233472, "one CTA per SM");
+  static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
 __device__ __forceinline__ void put_row_bf16(uint8_t* atom, int r, const float (&x)[64]) {
@@ -412,7 +414,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     if (threadIdx.x == 0) report(a.status, kErrUnsupported);
     return;
   }
-  float* sarr = reinterpret_cast<float*>(smem + SM::SARR);
   float* red = reinterpret_cast<float*>(smem + SM::RED);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SM::BAR + 8);
@@ -449,16 +450,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
   if (tid < kD) red[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], red[tid] + red[kD + tid]);
   __syncthreads();
   const float den = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)kD));
-  // ---- logits of every token (thread per token), maximum, E~ and P ----
-  float lmax = -INFINITY, lsum = 0.0f;
-  for (int t = tid; t < N; t += kTcThreads) {
+  // logit of token t: s = -(u_t . n) / ((e^tau + N) sqrt d)
+  auto logit = [&](int t) -> float {
     float x[64];
     get_row_bf16(u + (size_t)t * kD, true, x);
     float dot = 0.0f;
 #pragma unroll
     for (int i = 0; i < 64; ++i) dot = __fmaf_rn(x[i], red[i], dot);
-    const float s = -__fdiv_rn(dot, den);
-    sarr[t] = s;
+    return -__fdiv_rn(dot, den);
+  };
+  // ---- maximum logit and P (thread per token), then E~ ----
+  float lmax = -INFINITY, lsum = 0.0f;
+  for (int t = tid; t < N; t += kTcThreads) {
+    const float s = logit(t);
     lmax = fmaxf(lmax, s);
     lsum += s;
   }
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
   const float P = (red[2 * kD + 4] + red[2 * kD + 5]) + (red[2 * kD + 6] + red[2 * kD + 7]);
   if (!isfinite(m)) report(a.status, kErrRange);
   float esum = 0.0f;
-  for (int t = tid; t < N; t += kTcThreads) esum += expf(__fsub_rn(sarr[t], m));
+  for (int t = tid; t < N; t += kTcThreads) esum += expf(__fsub_rn(logit(t), m));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) esum += __shfl_xor_sync(0xffffffffu, esum, o);
   __syncthreads();  // everyone has read the maxima and sums above
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     put_row_bf16(smem + SM::KQ, tid, x);
     get_row_bf16(v + (size_t)t * kD, valid, x);
     put_row_bf16(smem + SM::AV, tid, x);
-    const float s = valid ? sarr[t] : 0.0f;
+    const float s = valid ? logit(t) : 0.0f;
     const float e = valid ? expf(__fsub_rn(s, m)) : 0.0f;
     put_row_split(smem + SM::EVH, smem + SM::EVL, tid, e, x);
     put_row_split(smem + SM::SVH, smem + SM::SVL, tid, s, x);
