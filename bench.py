@@ -687,6 +687,23 @@ def ours_decode(args, w: zi.Workload):
     hbm, kind = peaks()
     alg = decode_bytes(w)
     achieved = alg / (ms / 1e3) / 1e9
+
+    # end to end: each step's token (q, k, v, u, gates) copied in from pinned host memory and its
+    # output copied back; the recurrent state stays resident on the device
+    tk0 = steps_tok[0]
+    host = {n: tk0[n].cpu().pin_memory() for n in ("q", "k", "v", "u", "g1", "gh")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+    outs = {}
+
+    def e2e_step(src):
+        o = outs.setdefault(src["q"].data_ptr(), torch.empty_like(out))
+        zs.decode_step(st, src["q"], src["k"], src["v"], src["u"], src["g1"], src["gh"], out=o)
+        return [o]
+
+    e2e_ms = pipelined_e2e(host, e2e_step, max(3, min(args.steps, 50)), world)
+    if zs.get_status() != 0:
+        raise RuntimeError("device status after the end-to-end decode steps")
     if rank == 0:
         print(json.dumps({
             "metric": "ZeroS decode step tokens/s (B256 H32 d128, fp32 state, after 8192-token "
@@ -699,6 +716,8 @@ def ours_decode(args, w: zi.Workload):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": None, "peak_source": kind,
                          "algorithmic_bytes_per_launch": alg},
+            "e2e": {"value": w.B * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches, "clocks": clk}))
 
 
