@@ -43,12 +43,13 @@ WORKLOADS = {
 }
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture summarised
-# in profiles/chunk_kernel_causal_rope_b8h8n4096d64.md, keyed by a fingerprint of the kernel
-# sources it was measured on; reported as null once the sources change.
-CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
-                 "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"4ac2b6299fa25440": 136403200 + 19902976}
+# DRAM bytes (read + write) of one forward call (the scalar pass and the chunk kernel), from the
+# ncu captures summarised in profiles/chunk_kernel_causal_rope_b8h8n4096d64.md, keyed by a
+# fingerprint of the kernel sources they were measured on; reported as null once the sources
+# change.
+CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
+                 "zero_sum_prefix_gb300/csrc/zs_sm100.cuh", "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
+MEASURED_TRAFFIC = {}
 
 
 def kernel_fingerprint() -> str:
@@ -403,7 +404,9 @@ def ours_forward(args, w: zi.Workload):
                                      if w is zi.CAUSAL_ROPE_B8H8N4096D64 and args.path != "simt"
                                      and not args.ln else None),
                          "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": alg},
+                         "algorithmic_bytes_per_launch": alg,
+                         "timed": ("the whole zeros_fwd call: scalar pass + chunk kernel"
+                                   if args.path != "simt" else "the whole zeros_fwd call")},
             "cpu_baseline": cpu,
             "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

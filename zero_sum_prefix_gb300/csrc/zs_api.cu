@@ -34,6 +34,8 @@ struct DeviceWorkspace {
   size_t bwd_bytes = 0;
   void* sm = nullptr;     // ZeroS-SM scratch (rotated q and k)
   size_t sm_bytes = 0;
+  void* fwd = nullptr;    // chunked forward scratch (per-token scalars)
+  size_t fwd_bytes = 0;
   float2* rope = nullptr;
   size_t rope_entries = 0;  // capacity in float2
   int rope_N = 0, rope_d = 0;
@@ -139,6 +141,25 @@ int sm_scratch(DeviceWorkspace* ws, size_t bytes, void** out) {
     ws->sm_bytes = bytes;
   }
   *out = ws->sm;
+  return ZEROS_OK;
+}
+
+// Chunked forward scratch of at least `bytes` (grown like the backward scratch).
+int fwd_scratch(DeviceWorkspace* ws, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (bytes > ws->fwd_bytes) {
+    if (ws->fwd) {
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+      cudaFree(ws->fwd);
+    }
+    ws->fwd = nullptr;
+    ws->fwd_bytes = 0;
+    cudaError_t e = cudaMalloc(&ws->fwd, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(forward scratch)");
+    ws->fwd_bytes = bytes;
+  }
+  *out = ws->fwd;
   return ZEROS_OK;
 }
 
@@ -305,9 +326,17 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
   if (rope && !use_chunk) {  // the chunked kernel computes its rotary factors itself
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
-  cudaError_t e = use_chunk ? launch_fwd_chunk(a, st)
-                  : use_enc ? launch_fwd_encoder(a, st)
-                            : launch_fwd_simt(a, st);
+  if (use_chunk) {  // the scalar pass, then the chunk kernel
+    void* buf = nullptr;
+    if (int rc = fwd_scratch(ws, (size_t)B * H * N * sizeof(float4), &buf)) return rc;
+    a.scal = static_cast<float4*>(buf);
+    cudaError_t e = launch_fwd_scalars(a, a.scal, st);
+    if (e != cudaSuccess) return cuda_fail(e, "forward scalar launch");
+    e = launch_fwd_chunk(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return ZEROS_OK;
+  }
+  cudaError_t e = use_enc ? launch_fwd_encoder(a, st) : launch_fwd_simt(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ZEROS_OK;
 }
@@ -626,8 +655,8 @@ int zeros_bwd_ex(const void* q, const void* k, const void* v, const void* u, con
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return ZEROS_OK;
   }
-  // chunked: a forward launch writes the per-token scalars (its output goes to scratch), then
-  // the state, chunk and scan kernels
+  // chunked: the forward's per-token scalars (the scalar pass for bf16 inputs, else a forward
+  // launch whose output goes to scratch), then the state, chunk and scan kernels
   const size_t BHN = (size_t)B * H * N;
   const size_t out_bytes = ((BHN * d * (dtype == ZEROS_F32 ? 4 : 2)) + 255) / 256 * 256;
   float* buf = nullptr;
@@ -658,7 +687,12 @@ int zeros_bwd_ex(const void* q, const void* k, const void* v, const void* u, con
   f.dbg_P = scal + 2 * BHN;
   f.dbg_m = scal + 3 * BHN;
   f.status = ws->status;
-  e = chunk_supported(d, dtype, 1) ? launch_fwd_chunk(f, st) : launch_fwd_simt(f, st);
+  if (chunk_supported(d, dtype, 1)) {
+    static_assert(sizeof(float4) <= 64 * 2, "the scalars fit the forward output's scratch");
+    e = launch_fwd_scalars(f, reinterpret_cast<float4*>(buf), st);
+  } else {
+    e = launch_fwd_simt(f, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "forward launch (backward scalars)");
   e = launch_bwd_chunk(a, scal, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");

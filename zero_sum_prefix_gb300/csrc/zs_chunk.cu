@@ -21,31 +21,24 @@
 //     e^{M_{c-1} - M_c} before each chunk's update.
 //   The weight is formed to fp32 accuracy before the product is rounded: the three terms of w
 //   nearly cancel (the weights sum to zero), so rounding them separately would amplify bf16
-//   rounding errors.  The scalars s, m, Et = E e^{-m}, P follow the canonical blocked fp32 order
-//   of zs_common.cuh (bit-identical to the decode step).
-//
-// Cluster pairs: the two CTAs of a cluster hold two value slices of the same (b, h).  Chunk c is
-// owned by CTA c % 2: only the owner streams the chunk's q, k and u, computes its scalars
-// (carries of the previous chunk arrive from the other CTA through distributed shared memory),
-// rotates q and k and forms the weight operands and coefficients, then bulk-copies the rotated
-// tiles, the weight operands and the coefficients into the other CTA's stage.  Each CTA builds
-// its own scaled value tile, issues its own MMAs and writes its own output columns.  Stage
-// releases and the weight-operand release are multicast to both CTAs.
+//   rounding errors.  The scalars s, m, Et = E e^{-m}, P of every token come from the scalar
+//   pass (zs_scalars.cu, the canonical blocked fp32 order of zs_common.cuh), which runs first;
+//   the chunk reference M_c is the m of the chunk's last token.
 //
 // Warp roles (448 threads, one CTA per (b, h, value slice), one CTA per SM):
-//   warps 0,1,4,5 (PS): warp w owns the 32-token block w of the chunk: the block's column sums,
-//                     logits and local scalar chains (carries of earlier blocks through shared
-//                     memory, two bounded barriers per chunk); hands (s, m, Et, P) per token and
-//                     the chunk reference to PO through a ring (two slots, one with a cluster).
-//   warps 2,3,6,7 (PO): per token row: rotary factors, rotate q/k in place (RoPE), norms, gates,
-//                     row coefficients, the hi/lo weight operands and the scaled value tile Vsc.
+//   warps 0-7   (O) : operands; token row r = 32 (w % 4) + lane, half hf = w / 4 of the row's
+//                     work: rotary factors and in-place rotation (RoPE) of the hf-th half of the
+//                     rotary pairs of q and k (TMA-landed tiles), partial norms exchanged through
+//                     shared memory; hf = 0 forms the row coefficients and the row weight
+//                     operand, hf = 1 the column weight operand; each half builds half of the
+//                     row's scaled value tile Vsc.
 //   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> bf16 tile; state -> bf16
 //                     tile (and the F~ rescale); X -> output rows.
 //   warp 12     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
-//   warp 13     (T) : TMA producers: lane 0 streams q and k chunks 128B-swizzled directly into
-//                     the operand tiles (two stages at d = 64) and the value slice into a
-//                     64B-swizzled staging tile, with an L2 prefetch of each chunk issued before
-//                     its stage frees; lane 1 streams each chunk's u rows (one buffer).
+//   warp 13     (T) : TMA producer: q and k chunks 128B-swizzled directly into the operand
+//                     tiles (two stages at d = 64) and the value slice into a 64B-swizzled
+//                     staging tile, with an L2 prefetch of each chunk issued before its stage
+//                     frees.
 // TMEM (512 columns): [0,128) Q K^T, [128,256) W, [256,384) X, [384, 384 + d) state^T.
 // Every mbarrier wait is bounded in time; a timeout records ZEROS_ERR_TIMEOUT, raises a CTA
 // abort flag and every role leaves its loop; TMEM is released after the last MMA completes.
@@ -64,33 +57,19 @@ using namespace sm100;
 
 constexpr int kC = 128;       // tokens per chunk
 constexpr int kDV = 32;       // value columns per CTA
-constexpr int kCL = 1;  // CTAs per cluster (value slices sharing one (b, h)); 1 or 2
 constexpr int kThreads = 448;
 constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] bf16 atom tile
 
-__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) {
-  return (x + a - 1) / a * a;
-}
-
-// Per-stage coefficients of a chunk: row coefficients (a, b, g), column scalars (e, s', k) and
-// the chunk reference M_c; copied by the chunk's owner into the other CTA of the cluster.
-struct Xch {
+// Row coefficients (a, b, g) of a chunk, one block per operand stage.
+struct Coef {
   float4 coef[kC];
-  float cols[3][kC];
-  float M;
-  float pad[3];
 };
-static_assert(sizeof(Xch) == 3600, "Xch is moved by one bulk copy (multiple of 16 bytes)");
 
-template <int D, int CL>
+template <int D>
 struct Cfg {
-  static constexpr int KA = D / 64;               // atom tiles along d
-  // Operand stages: NSV for the scaled value tile, NSQ for q, k and the Xch block.  With a
-  // cluster at d = 64 the chunks of one owner are two apart; a third q/k stage lets an owner's
-  // next chunk load while its previous chunk and the other CTA's chunk are in flight.
-  static constexpr int NSV = (D == 64) ? 2 : 1;
-  static constexpr int NSQ = (CL > 1 && D == 64) ? 3 : NSV;
-  static constexpr int SCALS = (CL > 1) ? 1 : 2;  // slots of the scalar ring
+  static constexpr int KA = D / 64;              // atom tiles along d
+  static constexpr int NSQ = (D == 64) ? 3 : 1;  // q/k stages (with their coefficient blocks)
+  static constexpr int NSV = (D == 64) ? 2 : 1;  // scaled value tile stages
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NSQ * KA * kTile;
   static constexpr uint32_t V_OFF = K_OFF + NSQ * KA * kTile;
@@ -98,117 +77,89 @@ struct Cfg {
   static constexpr uint32_t SST_OFF = VST_OFF + 128 * 64;
   static constexpr uint32_t RW_OFF = SST_OFF + KA * kTile;       // weight MMA A: [128 x 16] bf16
   static constexpr uint32_t CW_OFF = RW_OFF + kC * 32;           // weight MMA B: [128 x 16] bf16
-  static constexpr uint32_t XCH_OFF = CW_OFF + kC * 32;          // Xch [NSQ]
-  static constexpr uint32_t U_OFF = align_up(XCH_OFF + NSQ * (uint32_t)sizeof(Xch), 1024);
-  static constexpr uint32_t PHI_OFF = U_OFF + kC * D * 2;             // float [2][D/2] base angles
-  static constexpr uint32_t THETA_OFF = PHI_OFF + 2 * (D / 2) * 4;    // float [D/2] frequencies
-  static constexpr uint32_t LEND_OFF = THETA_OFF + (D / 2) * 4;       // float [4][D]
-  static constexpr uint32_t BPUB_OFF = LEND_OFF + 4 * D * 4;         // float [4][4] + [2][4]
-  static constexpr uint32_t CHAIN_OFF = BPUB_OFF + 128;               // float4 [4][32]
-  static constexpr uint32_t SCAL_OFF = CHAIN_OFF + 4 * 32 * 16;     // float4 [SCALS][128]
-  static constexpr uint32_t CIN_OFF = SCAL_OFF + SCALS * kC * 16;   // float [2][D] column carries
-  static constexpr uint32_t KCIN_OFF = CIN_OFF + 2 * D * 4;         // float [2][4] scalar carries
-  static constexpr uint32_t MISC_OFF = KCIN_OFF + 32;
+  static constexpr uint32_t COEF_OFF = CW_OFF + kC * 32;         // Coef [NSQ]
+  static constexpr uint32_t PHI_OFF = COEF_OFF + NSQ * (uint32_t)sizeof(Coef);  // float [2][D/2]
+  static constexpr uint32_t THETA_OFF = PHI_OFF + 2 * (D / 2) * 4;             // float [D/2]
+  static constexpr uint32_t NRM_OFF = THETA_OFF + (D / 2) * 4;   // float2 [2][128] half norms
+  static constexpr uint32_t MISC_OFF = NRM_OFF + 2 * kC * 8;
   // output LayerNorm: per-row (mean, M2) of every value slice of the head, two chunk slots
-  // (float2 [2][D / kDV][128]), then this slice's gain and bias (float [2][32]); only without
-  // the chunk-alternating cluster, which has no room for them
+  // (float2 [2][D / kDV][128]), then this slice's gain and bias (float [2][32])
   static constexpr uint32_t LNX_OFF = MISC_OFF + 512;
-  static constexpr uint32_t LNW_OFF = LNX_OFF + (CL == 1 ? 2 * (D / kDV) * kC * 8 : 0);
-  static constexpr uint32_t BYTES = LNW_OFF + (CL == 1 ? 2 * 32 * 4 : 0);
+  static constexpr uint32_t LNW_OFF = LNX_OFF + 2 * (D / kDV) * kC * 8;
+  static constexpr uint32_t BYTES = LNW_OFF + 2 * 32 * 4;
   static constexpr uint32_t SMEM = BYTES;  // the base is 1024-byte aligned (checked at entry)
   static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
   // S tile (bf16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
   // Q K^T columns (then the next Q K^T waits for the S V product)
   static constexpr uint32_t TM_S = (D == 64) ? 448 : 0;
-  // bytes a non-owner receives per chunk: rotated Q and K, the weight operands, the Xch block
-  static constexpr uint32_t PEER_BYTES = 2 * KA * kTile + 2 * kC * 32 + (uint32_t)sizeof(Xch);
   static_assert(SMEM <= 232448, "shared memory budget of one CTA");
 };
 
+constexpr int kMaxNSQ = 3;
+
 struct Misc {
-  uint64_t tma_full[2];
-  uint64_t u_full, u_empty, vst_empty;
-  uint64_t op_full, vsc_full;        // Vsc of an owned / other-owned chunk written
-  uint64_t qk_empty[3];  // Q, K and Xch of a stage released by every CTA of the cluster
+  uint64_t tma_full[kMaxNSQ];
+  uint64_t vst_empty;
+  uint64_t op_full;      // Vsc of a chunk written
+  uint64_t qk_empty[kMaxNSQ];  // Q, K and the coefficients of a stage released
   uint64_t vsc_free[2];  // Vsc of the last chunk of this parity consumed (S V completed)
   uint64_t a_full, a_free, am_full, sst_full, sst_free, st_done, fin;
-  uint64_t w_done;                   // both CTAs' weight MMAs have read R and C
+  uint64_t w_done;       // the weight MMA has read R and C
   uint64_t x_full, x_free;
-  uint64_t pbar;     // reusable barrier of the four scalar warps (bounded waits)
-  uint64_t pobar;    // reusable barrier of the four operand warps
-  uint64_t po_sync;  // Q, K, R, C and Xch of an owned chunk written
-  uint64_t scal_full[2], scal_empty[2];
-  uint64_t peer_full;            // tiles of a chunk owned by the other CTA have landed
-  uint64_t ccar_full, kcar_full;  // carries from the other CTA's previous chunk
-  uint64_t ln_full[2];  // output LayerNorm: row statistics of the other value slices landed
-  float Mslot[2];
-  int w_seen;  // with a cluster: number of w_done phases observed (monotonic)
+  uint64_t pobar;        // the operand warps: start of a chunk (rotary base angles written)
+  uint64_t nbar;         // the operand warps: half norms of a chunk written
+  uint64_t po_sync;      // Q, K, R and C of a chunk written (waited by the MMA thread)
+  // coefficients of a chunk written into its stage (waited by the epilogue: one barrier per
+  // stage, whose next phase needs the stage's release, which follows the epilogue's read)
+  uint64_t cf_full[kMaxNSQ];
+  uint64_t ln_full[2];   // output LayerNorm: row statistics of the other value slices landed
   uint32_t tmem;
   int abort;
   int never;  // stays 0: lets the final waits ignore the abort flag
 };
 
 static_assert(sizeof(Misc) <= 512, "Misc fits its shared-memory slot");
-static_assert(Cfg<64, 2>::NSQ <= 3 && Cfg<64, 1>::NSQ <= 3 && Cfg<128, 2>::NSQ <= 3,
-              "qk_empty has one barrier per q/k stage");
-static_assert(Cfg<64, 1>::SCALS <= 2 && Cfg<64, 2>::SCALS <= 2, "scal ring barriers");
+static_assert(Cfg<64>::NSQ <= kMaxNSQ && Cfg<128>::NSQ <= kMaxNSQ, "one barrier per q/k stage");
+static_assert(Cfg<64>::NSV <= 2 && Cfg<128>::NSV <= 2, "vsc_free has one barrier per parity");
 
 struct ChunkParams {
   CUtensorMap tq, tk, tv;  // q, k: box {64, 128, 1} 128B swizzle; v: box {32, 128, 1} 64B swizzle
-  CUtensorMap tu;          // u: box {d, 128, 1}, no swizzle (dense 2d-byte rows)
   FwdArgs a;
 };
 
-template <int CL>
 __device__ __forceinline__ void fail_wait(Misc* ms, int* status) {
   report(status, kErrTimeout);
   ms->abort = 1;
-  if (CL > 1) st_cluster_s32(mapa(smem_u32(&ms->abort), cluster_rank() ^ 1u), 1);
 }
 
-__device__ __forceinline__ Xch* xch(uint8_t* smem, uint32_t off, int st) {
-  return reinterpret_cast<Xch*>(smem + off) + st;
+__device__ __forceinline__ Coef* coef_block(uint8_t* smem, uint32_t off, int st) {
+  return reinterpret_cast<Coef*>(smem + off) + st;
 }
 
-// Load barrier of chunk c and the parity of its phase.  Without a cluster, one barrier per
-// stage; with a cluster, one per owner, so that the operand warps (chunks of this CTA) and the
-// epilogue warps (chunks of the other CTA) each wait for consecutive phases of their own barrier
-// (a parity wait names its phase only when the previous phase has completed and the next one
-// cannot have).
-template <int D, int CL>
-__device__ __forceinline__ int tf_index(int c) {
-  return CL > 1 ? c % CL : c % Cfg<D, CL>::NSQ;
-}
-template <int D, int CL>
-__device__ __forceinline__ uint32_t tf_phase(int c) {
-  return (uint32_t)(CL > 1 ? c / CL : c / Cfg<D, CL>::NSQ) & 1u;
+// The chunk reference M_c: the running maximum at the chunk's last token.
+__device__ __forceinline__ float chunk_ref(const float4* __restrict__ scal, int c, int N) {
+  return __ldg(&scal[min(N, (c + 1) * kC) - 1].y);
 }
 
 // Before the Vsc tile of chunk c is written: the S V product of chunk c - NS (same stage) has
-// completed.  One barrier per chunk parity, so that each builder role (operand warps for this
-// CTA's chunks, epilogue warps for the other CTA's) waits for consecutive phases of its own.
-template <int D, int CL>
+// completed.  One barrier per chunk parity, waited in consecutive phases.
+template <int D>
 __device__ __forceinline__ bool vsc_wait(Misc* ms, int c) {
-  constexpr int NS = Cfg<D, CL>::NSV;
+  constexpr int NS = Cfg<D>::NSV;
   if (c < NS) return true;
   return mbar_wait_warp(&ms->vsc_free[(c - NS) & 1], (uint32_t)((c - NS) >> 1) & 1u, &ms->abort);
 }
 
-// Raw value row r (64B-swizzled staging tile) -> columns 0..31 of the Vsc tile (bf16 words).
-__device__ __forceinline__ void copy_v_row(uint8_t* vt, const uint8_t* vst, int r) {
-#pragma unroll
-  for (int x = 0; x < 4; ++x)
-    *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) =
-        *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
-}
-
-// Vsc row r: atom 0 = [v | e v], atom 1 = [s' v | k v] from the row's v (already in columns
-// 0..31) and its column scalars (e, s', k).
-__device__ __forceinline__ void build_vsc_row(uint8_t* vt, int r, float ce, float cs1, float ck) {
+// Vsc row r, 16-byte pieces x0, x0 + 1 of the value row: the raw bf16 words are copied from
+// the 64B-swizzled staging tile to columns 8 x .. 8 x + 7 of atom 0, then the scaled parts:
+// atom 0 = [v | e v], atom 1 = [s' v | k v], from the row's column scalars (e, s', k).
+__device__ __forceinline__ void build_vsc_half(uint8_t* vt, const uint8_t* vst, int r, int x0,
+                                               float ce, float cs1, float ck) {
   const float2 ce2 = make_float2(ce, ce), cs2 = make_float2(cs1, cs1), ck2 = make_float2(ck, ck);
 #pragma unroll
-  for (int x = 0; x < 4; ++x) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(vt + sw128_off(r, x));
+  for (int x = x0; x < x0 + 2; ++x) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
+    *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = wv;
     const uint32_t pv[4] = {wv.x, wv.y, wv.z, wv.w};
     uint32_t pe[4], ps[4], pk[4];
 #pragma unroll
@@ -226,20 +177,10 @@ __device__ __forceinline__ void build_vsc_row(uint8_t* vt, int r, float ce, floa
   }
 }
 
-// Warps 0, 1, 4, 5 are the scalar warps and 2, 3, 6, 7 the operand warps (warp w runs on
-// sub-partition w % 4, so each of these sub-partitions interleaves one role's code with the
-// epilogue's); both roles number their warps 0..3 in this order.
-__device__ __forceinline__ int group_index() {
-  const int warp = threadIdx.x >> 5;
-  return (warp & 1) | ((warp >> 2) << 1);
-}
-
 // ============================================================================ T: TMA producer
-// Every CTA streams its value slice for every chunk; q and k only for the chunks it owns.
-template <int D, int CL>
-__device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
-                         int rank) {
-  using CF = Cfg<D, CL>;
+template <int D>
+__device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch) {
+  using CF = Cfg<D>;
   const uint32_t base = smem_u32(smem);
   const int j0 = blockIdx.y * kDV;
   constexpr uint32_t qk_bytes = 2 * CF::KA * kTile, v_bytes = 128 * 64;
@@ -248,88 +189,38 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
   tma_prefetch_desc(&p.tv);
   for (int c = 0; c < nch; ++c) {
     const int st = c % CF::NSQ;
-    const bool owned = (c % CL) == rank;
     if (c >= CF::NSQ) {
       // the chunk's tiles start towards L2 while the stage is still in use
-      if (owned) {
-#pragma unroll
-        for (int at = 0; at < CF::KA; ++at) {
-          tma_prefetch_3d(&p.tq, 64 * at, c * kC, bh);
-          tma_prefetch_3d(&p.tk, 64 * at, c * kC, bh);
-        }
-      }
-      tma_prefetch_3d(&p.tv, j0, c * kC, bh);
-      // both CTAs of the cluster have released the stage's Q, K and Xch
-      if (!mbar_wait_cl(&ms->qk_empty[st], ((c / CF::NSQ) - 1) & 1, &ms->abort)) {
-        fail_wait<CL>(ms, p.a.status);
-        return;
-      }
-    }
-    // a chunk owned by the other CTA: its tiles arrive by bulk copy; the barrier's previous
-    // phase (the other CTA's previous chunk) must have completed before this arrival
-    if (CL > 1 && !owned) {
-      if (c >= CL && !mbar_wait_cl(&ms->peer_full, (uint32_t)((c - CL) / CL) & 1u, &ms->abort)) {
-        fail_wait<CL>(ms, p.a.status);
-        return;
-      }
-      mbar_arrive_expect_tx(&ms->peer_full, CF::PEER_BYTES);
-    }
-    uint64_t* tf = &ms->tma_full[tf_index<D, CL>(c)];
-    mbar_arrive_expect_tx(tf, (owned ? qk_bytes : 0u) + v_bytes);
-    if (owned) {
-      const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
-      const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
 #pragma unroll
       for (int at = 0; at < CF::KA; ++at) {
-        tma_load_3d(qt + at * kTile, &p.tq, 64 * at, c * kC, bh, tf);
-        tma_load_3d(kt + at * kTile, &p.tk, 64 * at, c * kC, bh, tf);
+        tma_prefetch_3d(&p.tq, 64 * at, c * kC, bh);
+        tma_prefetch_3d(&p.tk, 64 * at, c * kC, bh);
       }
+      tma_prefetch_3d(&p.tv, j0, c * kC, bh);
+      if (!mbar_wait(&ms->qk_empty[st], ((c / CF::NSQ) - 1) & 1, &ms->abort)) {
+        fail_wait(ms, p.a.status);
+        return;
+      }
+    }
+    uint64_t* tf = &ms->tma_full[st];
+    mbar_arrive_expect_tx(tf, qk_bytes + v_bytes);
+    const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
+    const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
+#pragma unroll
+    for (int at = 0; at < CF::KA; ++at) {
+      tma_load_3d(qt + at * kTile, &p.tq, 64 * at, c * kC, bh, tf);
+      tma_load_3d(kt + at * kTile, &p.tk, 64 * at, c * kC, bh, tf);
     }
     // the raw value slice has one buffer, released by the operand warps once copied
     if (c >= 1 && !mbar_wait(&ms->vst_empty, (c - 1) & 1, &ms->abort)) {
-      fail_wait<CL>(ms, p.a.status);
+      fail_wait(ms, p.a.status);
       return;
     }
     tma_load_3d(base + CF::VST_OFF, &p.tv, j0, c * kC, bh, tf);
   }
 }
 
-// With a cluster: observes every phase of w_done in order and publishes the count, for the
-// operand warps, which only handle every other chunk (a parity wait names its phase only when
-// the waiter has seen the previous one).
-template <int CL>
-__device__ void role_wdone_observer(const FwdArgs& a, Misc* ms, int nch) {
-  for (int c = 0; c < nch; ++c) {
-    if (!mbar_wait_cl(&ms->w_done, (uint32_t)c & 1u, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
-      return;
-    }
-    st_release_s32(&ms->w_seen, c + 1);
-  }
-}
-
-// u rows of each owned chunk (single buffer, released by the scalar warps after their logits);
-// a separate producer thread so that this stream never waits behind the operand stages.
-template <int D, int CL>
-__device__ void role_tma_u(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, int nch,
-                           int rank) {
-  using CF = Cfg<D, CL>;
-  const uint32_t base = smem_u32(smem);
-  tma_prefetch_desc(&p.tu);
-  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
-    if (kk >= 1) {
-      tma_prefetch_3d(&p.tu, 0, c * kC, bh);
-      if (!mbar_wait(&ms->u_empty, (kk - 1) & 1, &ms->abort)) {
-        fail_wait<CL>(ms, p.a.status);
-        return;
-      }
-    }
-    mbar_arrive_expect_tx(&ms->u_full, kC * D * 2);
-    tma_load_3d(base + CF::U_OFF, &p.tu, 0, c * kC, bh, &ms->u_full);
-  }
-}
-
-// ============================================================================ P: operands
+// ============================================================================ O: operands
 // Rotates (RoPE) pair group g (pairs 8g .. 8g+7 with partners + D/2) of row r of a
 // 128B-swizzled bf16 tile in place and accumulates the row's squared norm into ss (two
 // partial sums).  cs[k] = (cos, sin) of pair 8g + k.
@@ -366,333 +257,23 @@ __device__ __forceinline__ void rotate_group(uint8_t* tile, int r, int g, bool r
   }
 }
 
-// The per-token scalars of one 32-token block, by the warp that owns the block (the canonical
-// blocked order of zs_common.cuh).  Lane l owns columns R l + r while the column sums run; after
-// the reduction lane j owns token j of the block.  Carries of the previous blocks arrive through
-// shared memory (two bounded barriers among the four operand warps per chunk).
-struct BlockCarry {
-  float mC, EC, CP;
-};
-
-__device__ __forceinline__ void fold_block(BlockCarry& k, float LP, float ml, float El) {
-  const float P = __fadd_rn(k.CP, LP);
-  const float m = fmaxf(k.mC, ml);
-  const float Et = __fmaf_rn(k.EC, expf(__fsub_rn(k.mC, m)), __fmul_rn(El, expf(__fsub_rn(ml, m))));
-  k.CP = P;
-  k.mC = m;
-  k.EC = Et;
-}
-
-// Column values (R per lane) of token j of a 32-token block in the staged u tile.
-template <int R>
-struct UCols {
-  float2 v[(R + 1) / 2];
-};
-
+// Per chunk: rotation of this half's rotary pairs of q and k, the row's norms (halves summed
+// through shared memory), then hf = 0: row coefficients (a, b, g) and the row weight operand;
+// hf = 1: the column weight operand; both: half of the row's Vsc.
 template <int D>
-__device__ __forceinline__ UCols<D / 32> load_ucols(const uint8_t* us, int j) {
-  constexpr int R = D / 32;
-  UCols<R> o;
-  if (R == 1) {
-    const uint16_t hv = *reinterpret_cast<const uint16_t*>(us + (size_t)j * D * 2);
-    o.v[0] = make_float2(__uint_as_float((uint32_t)hv << 16), 0.0f);
-  } else if (R == 2) {
-    const uint32_t wv = *reinterpret_cast<const uint32_t*>(us + (size_t)j * D * 2);
-    unpack_bf16x2(wv, o.v[0].x, o.v[0].y);
-  } else {
-    const uint2 wv = *reinterpret_cast<const uint2*>(us + (size_t)j * D * 2);
-    unpack_bf16x2(wv.x, o.v[0].x, o.v[0].y);
-    unpack_bf16x2(wv.y, o.v[(R + 1) / 2 - 1].x, o.v[(R + 1) / 2 - 1].y);
-  }
-  return o;
-}
-
-// ---------------------------------------------------------------- PS: scalars of the blocks
-// Runs the chunks this CTA owns.  With a cluster, the column carry at a chunk's start and the
-// chunk-start scalar carries (mC, EC, CP) come from the other CTA, which processed the previous
-// chunk; the carries of the next chunk are sent the same way.  Slots are indexed by the number
-// of carries received so far: a slot is rewritten only two owned chunks later.
-template <int D, int CL>
-__device__ void role_scalars(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, int h,
-                             size_t row0, int nch, int rank) {
-  using CF = Cfg<D, CL>;
-  constexpr int R = D / 32;
-  constexpr int RP = (R + 1) / 2;  // column pairs per lane (R = 1 uses the .x half only)
-  const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-token block
-  const int r = 32 * w + lane;     // token row inside the chunk, 0..127
+__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t row0, int nch) {
+  using CF = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hf = warp >> 2;         // which half of the row's work
+  const int r = 32 * (warp & 3) + lane;  // token row inside the chunk, 0..127
   const int N = a.N;
-  float* lend = reinterpret_cast<float*>(smem + CF::LEND_OFF);      // [4][D]
-  float* bpub = reinterpret_cast<float*>(smem + CF::BPUB_OFF);      // [4][4] + kc [2][4]
-  float4* chain = reinterpret_cast<float4*>(smem + CF::CHAIN_OFF);  // [4][32] (s, f, g, -)
-  float4* scal = reinterpret_cast<float4*>(smem + CF::SCAL_OFF);    // [2][128] (s, m, Et, P)
-  const float* cin = reinterpret_cast<const float*>(smem + CF::CIN_OFF);    // [2][D]
-  const float* kcin = reinterpret_cast<const float*>(smem + CF::KCIN_OFF);  // [2][4]
-  const uint32_t peer = (uint32_t)rank ^ 1u;
-  const bool dbg = blockIdx.y < CL;  // the first cluster of value slices writes the scalars
-  const float etau = expf(a.tau[h]);
-  const float sqrtd = __fsqrt_rn((float)D);
-  const float2 etau2 = make_float2(etau, etau);
-  float2 mu2[RP], Cc[RP];
-#pragma unroll
-  for (int x = 0; x < RP; ++x) {
-    mu2[x] = make_float2(a.mu[(size_t)h * D + R * lane + 2 * x],
-                         R > 1 ? a.mu[(size_t)h * D + R * lane + 2 * x + 1] : 0.0f);
-    Cc[x] = make_float2(0.0f, 0.0f);
-  }
-  if (CL == 1 && r == 0) {
-    bpub[16 + 0] = -INFINITY;  // chunk-start carries (mC, EC, CP) for chunk 0
-    bpub[16 + 1] = 0.0f;
-    bpub[16 + 2] = 0.0f;
-  }
-
-  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
-    const int slot = kk % CF::SCALS;
-    const int i = c * kC + r;
-    const bool valid = i < N;
-    const int b0 = c * kC + 32 * w;  // first token of this warp's block
-    const int nvalid = max(0, min(32, N - b0));
-    const int rslot = ((c - 1) / 2) & 1;  // carry slot of this chunk (cluster of two)
-    // ---- u of the block from the staged tile: lane owns columns R lane .. R lane + R - 1 ----
-    if (!mbar_wait_warp(&ms->u_full, kk & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
-      return;
-    }
-    const uint8_t* us = smem + CF::U_OFF + (size_t)(32 * w) * D * 2 + R * lane * 2;
-    // ---- phase 1: local column sums of the block -> its end value ----
-    float2 L[RP];
-#pragma unroll
-    for (int x = 0; x < RP; ++x) L[x] = make_float2(0.0f, 0.0f);
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-      const UCols<R> uj = load_ucols<D>(us, j);
-#pragma unroll
-      for (int x = 0; x < RP; ++x) L[x] = __fadd2_rn(L[x], uj.v[x]);
-    }
-#pragma unroll
-    for (int x = 0; x < RP; ++x) {
-      lend[w * D + R * lane + 2 * x] = L[x].x;
-      if (R > 1) lend[w * D + R * lane + 2 * x + 1] = L[x].y;
-    }
-    mbar_arrive(&ms->pbar);
-    if (!mbar_wait_warp(&ms->pbar, (2 * kk) & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
-      return;
-    }
-    // ---- column carry at this block's start (and at the next chunk's start) ----
-    if (CL > 1 && c > 0) {
-      if (!mbar_wait_cl_warp(&ms->ccar_full, rslot, &ms->abort)) {
-        fail_wait<CL>(ms, a.status);
-        return;
-      }
-#pragma unroll
-      for (int x = 0; x < RP; ++x)
-        Cc[x] = make_float2(cin[rslot * D + R * lane + 2 * x],
-                            R > 1 ? cin[rslot * D + R * lane + 2 * x + 1] : 0.0f);
-    }
-    float2 Cw[RP];
-#pragma unroll
-    for (int ww = 0; ww < 4; ++ww) {
-      if (ww == w) {
-#pragma unroll
-        for (int x = 0; x < RP; ++x) Cw[x] = Cc[x];
-      }
-#pragma unroll
-      for (int x = 0; x < RP; ++x) {
-        const float2 le = make_float2(lend[ww * D + R * lane + 2 * x],
-                                      R > 1 ? lend[ww * D + R * lane + 2 * x + 1] : 0.0f);
-        Cc[x] = __fadd2_rn(Cc[x], le);
-      }
-    }
-    if (CL > 1 && w == 0 && c + 1 < nch) {  // the next chunk's column carry -> other CTA
-      const uint32_t dst = mapa(smem_u32(smem + CF::CIN_OFF) + (uint32_t)(((c / 2) & 1) * D * 4),
-                                peer);
-#pragma unroll
-      for (int x = 0; x < RP; ++x) {
-        st_cluster_f32(dst + (uint32_t)(R * lane + 2 * x) * 4, Cc[x].x);
-        if (R > 1) st_cluster_f32(dst + (uint32_t)(R * lane + 2 * x + 1) * 4, Cc[x].y);
-      }
-      mbar_arrive_remote(mapa(smem_u32(&ms->ccar_full), peer));
-    }
-    // ---- phase 2: S = C + L per token, logit partial products (two tokens per f32x2) ----
-    float pp[32];
-#pragma unroll
-    for (int x = 0; x < RP; ++x) L[x] = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const UCols<R> u0 = load_ucols<D>(us, j), u1 = load_ucols<D>(us, j + 1);
-      float2 n0[RP], n1[RP];
-#pragma unroll
-      for (int x = 0; x < RP; ++x) {
-        L[x] = __fadd2_rn(L[x], u0.v[x]);
-        n0[x] = __ffma2_rn(etau2, mu2[x], __fadd2_rn(Cw[x], L[x]));
-        L[x] = __fadd2_rn(L[x], u1.v[x]);
-        n1[x] = __ffma2_rn(etau2, mu2[x], __fadd2_rn(Cw[x], L[x]));
-      }
-      // p = u[R l] n[R l], then fma over the lane's remaining columns, for tokens j and j + 1
-      float2 p = __fmul2_rn(make_float2(u0.v[0].x, u1.v[0].x), make_float2(n0[0].x, n1[0].x));
-#pragma unroll
-      for (int col = 1; col < R; ++col) {
-        const int x = col >> 1;
-        const float a0 = (col & 1) ? u0.v[x].y : u0.v[x].x, a1 = (col & 1) ? u1.v[x].y : u1.v[x].x;
-        const float m0 = (col & 1) ? n0[x].y : n0[x].x, m1 = (col & 1) ? n1[x].y : n1[x].x;
-        p = __ffma2_rn(make_float2(a0, a1), make_float2(m0, m1), p);
-      }
-      pp[j] = p.x;
-      pp[j + 1] = p.y;
-    }
-    mbar_arrive(&ms->u_empty);  // this thread is done with the staged u rows
-    // transpose-reduce: the butterfly tree of the contract for 32 tokens at once; afterwards
-    // lane j holds the full dot of token b0 + j.
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int k = 0; k < o; ++k) {
-        const float send = up ? pp[k] : pp[k + o];
-        const float keep = up ? pp[k + o] : pp[k];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
-        pp[k] = __fadd_rn(keep, recv);
-      }
-    }
-    const float den = __fmul_rn(__fadd_rn(etau, (float)(i + 1)), sqrtd);
-    const float s = -__fdiv_rn(pp[0], den);
-    if (valid && !isfinite(s)) report(a.status, kErrRange);
-    // ---- block-local running max, scaled exp-sum and logit sum (token order) ----
-    float ml = valid ? s : -INFINITY;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float x = __shfl_up_sync(0xffffffffu, ml, o);
-      if (lane >= o) ml = fmaxf(ml, x);
-    }
-    float mlp = __shfl_up_sync(0xffffffffu, ml, 1);
-    if (lane == 0) mlp = -INFINITY;
-    chain[w * 32 + lane] = make_float4(s, expf(__fsub_rn(mlp, ml)), expf(__fsub_rn(s, ml)), 0.0f);
-    __syncwarp();
-    float LP = 0.0f, El = 0.0f;
-    const int kend = min(nvalid, lane + 1);  // this lane accumulates tokens 0 .. lane
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float4 e = chain[w * 32 + k];
-      if (k < kend) {
-        LP = __fadd_rn(LP, e.x);
-        El = __fmaf_rn(El, e.y, e.z);
-      }
-    }
-    if (lane == 31) {  // block end values: tokens 0 .. nvalid-1
-      bpub[w * 4 + 0] = LP;
-      bpub[w * 4 + 1] = ml;
-      bpub[w * 4 + 2] = El;
-    }
-    mbar_arrive(&ms->pbar);
-    if (!mbar_wait_warp(&ms->pbar, (2 * kk + 1) & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
-      return;
-    }
-    // carries at this block's start: chunk-start carries folded over the earlier blocks
-    BlockCarry kw{-INFINITY, 0.0f, 0.0f};
-    if (CL == 1) {
-      const float* kcb = bpub + 16 + (c & 1) * 4;
-      kw = BlockCarry{kcb[0], kcb[1], kcb[2]};
-    } else if (c > 0) {
-      if (!mbar_wait_cl_warp(&ms->kcar_full, rslot, &ms->abort)) {
-        fail_wait<CL>(ms, a.status);
-        return;
-      }
-      kw = BlockCarry{kcin[rslot * 4 + 0], kcin[rslot * 4 + 1], kcin[rslot * 4 + 2]};
-    }
-    for (int ww = 0; ww < w; ++ww) fold_block(kw, bpub[ww * 4 + 0], bpub[ww * 4 + 1], bpub[ww * 4 + 2]);
-    float M = kw.mC;  // running max at the chunk's last valid token (max is exact)
-#pragma unroll
-    for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, bpub[ww * 4 + 1]);
-    if (w == 3 && lane == 0) {  // chunk-start carries of the next chunk
-      BlockCarry kn = kw;
-      fold_block(kn, bpub[12 + 0], bpub[12 + 1], bpub[12 + 2]);
-      if (CL == 1) {
-        float* kcn = bpub + 16 + ((c + 1) & 1) * 4;
-        kcn[0] = kn.mC;
-        kcn[1] = kn.EC;
-        kcn[2] = kn.CP;
-      } else if (c + 1 < nch) {
-        const uint32_t dst =
-            mapa(smem_u32(smem + CF::KCIN_OFF) + (uint32_t)(((c / 2) & 1) * 16), peer);
-        st_cluster_f32(dst + 0, kn.mC);
-        st_cluster_f32(dst + 4, kn.EC);
-        st_cluster_f32(dst + 8, kn.CP);
-        mbar_arrive_remote(mapa(smem_u32(&ms->kcar_full), peer));
-      }
-    }
-    // this token's scalars
-    const float P = __fadd_rn(kw.CP, LP);
-    const float m = fmaxf(kw.mC, ml);
-    const float Et = __fmaf_rn(kw.EC, expf(__fsub_rn(kw.mC, m)), __fmul_rn(El, expf(__fsub_rn(ml, m))));
-    if (dbg && valid) {
-      if (a.dbg_s) a.dbg_s[row0 + i] = s;
-      if (a.dbg_E) a.dbg_E[row0 + i] = Et;
-      if (a.dbg_P) a.dbg_P[row0 + i] = P;
-      if (a.dbg_m) a.dbg_m[row0 + i] = m;
-    }
-    // hand the scalars to the operand warps (ring of SCALS slots)
-    if (kk >= CF::SCALS &&
-        !mbar_wait_warp(&ms->scal_empty[slot], ((kk / CF::SCALS) - 1) & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
-      return;
-    }
-    scal[slot * kC + r] = make_float4(s, m, Et, P);
-    if (r == 0) ms->Mslot[slot] = M;
-    mbar_arrive(&ms->scal_full[slot]);
-    // ---- recurrent state after the last token (prefill), by the warp owning that token ----
-    if (a.final_state && dbg && c == nch - 1 && nvalid > 0 && b0 + nvalid == N) {
-      float* rec = record_ptr(a.final_state, bh, D);
-      const bool closed = nvalid == 32;  // the block is complete: fold it as the decode step does
-      const float LPe = __shfl_sync(0xffffffffu, LP, 31);
-      const float mle = __shfl_sync(0xffffffffu, ml, 31);
-      const float Ele = __shfl_sync(0xffffffffu, El, 31);
-      BlockCarry kf = kw;
-      if (closed) fold_block(kf, LPe, mle, Ele);
-#pragma unroll
-      for (int x = 0; x < RP; ++x) {
-#pragma unroll
-        for (int y = 0; y < 2 && 2 * x + y < R; ++y) {
-          const float cw = y ? Cw[x].y : Cw[x].x, le = y ? L[x].y : L[x].x;
-          rec[rec_C(D) + R * lane + 2 * x + y] = closed ? __fadd_rn(cw, le) : cw;
-          rec[rec_L(D) + R * lane + 2 * x + y] = closed ? 0.0f : le;
-          rec[rec_mu(D) + R * lane + 2 * x + y] = y ? mu2[x].y : mu2[x].x;
-        }
-      }
-      if (lane == 0) {
-        RecordHead* hd = reinterpret_cast<RecordHead*>(rec);
-        hd->t = N;
-        hd->mC = kf.mC;
-        hd->EC = kf.EC;
-        hd->CP = kf.CP;
-        hd->etau = etau;
-        hd->ml = closed ? -INFINITY : mle;
-        hd->El = closed ? 0.0f : Ele;
-        hd->LP = closed ? 0.0f : LPe;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------- PO: tensor-core operands
-// Chunks this CTA owns: rotate q/k, coefficients, weight operands and the Xch block (bulk-copied
-// to the other CTA of the cluster), then this CTA's scaled value tile Vsc.  The value tiles of
-// the chunks of the other CTA are built by the epilogue warps.
-template <int D, int CL>
-__device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, size_t row0,
-                              int nch, int rank) {
-  using CF = Cfg<D, CL>;
-  const int w = group_index(), lane = threadIdx.x & 31;  // w: the warp's 32-row group
-  const int r = 32 * w + lane;      // token row inside the chunk, 0..127
-  const int N = a.N;
-  const float4* scal = reinterpret_cast<const float4*>(smem + CF::SCAL_OFF);
+  const float4* __restrict__ scal = a.scal + row0;
   float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
   float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
-  const uint32_t peer = (uint32_t)rank ^ 1u;
+  float2* nrm = reinterpret_cast<float2*>(smem + CF::NRM_OFF);    // [2][128] (|q|^2, |k|^2)
   const double two_pi = 6.283185307179586476925286766559;
-  constexpr int PPW = (D / 2 + 3) / 4;  // rotary pairs per warp
-  const int pj = w * PPW + lane;
-  const bool owns_pair = a.rope && lane < PPW && pj < D / 2;
+  const int pj = threadIdx.x;  // rotary pair owned for the tables (threads 0 .. D/2 - 1)
+  const bool owns_pair = a.rope && pj < D / 2;
   double theta_d = 0.0;
   if (owns_pair) {
     theta_d = pow((double)a.rope_base, -2.0 * (double)pj / (double)D);
@@ -707,50 +288,59 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
       phi[slot * (D / 2) + pj] = (float)(ang - rint(ang * (1.0 / two_pi)) * two_pi);
     }
   };
-  // gate logits of chunk cc (loaded one chunk ahead so that their latency is hidden); x0 is the
-  // optional zero-order gate (-inf when absent, so that its sigmoid is 0)
-  auto load_gates = [&](int cc, float& x1, float& xh, float& x0) {
-    x1 = 0.0f;
-    xh = 0.0f;
-    x0 = -INFINITY;
-    if (cc < nch && cc * kC + r < N) {
-      x1 = __ldg(a.g1 + row0 + cc * kC + r);
-      xh = __ldg(a.gh + row0 + cc * kC + r);
-      if (a.g0) x0 = __ldg(a.g0 + row0 + cc * kC + r);
-    }
+  // inputs of chunk cc that are loaded one chunk ahead (their latency is hidden): the token's
+  // scalars, the chunk reference and the gate logits (x0: optional zero-order gate, -inf when
+  // absent, so that its sigmoid is 0)
+  struct Ahead {
+    float4 sc;
+    float M, x1, xh, x0;
   };
-  float g1, gh, g0;
-  load_gates(rank, g1, gh, g0);
-  put_phi(rank, 0);
+  auto load_ahead = [&](int cc) {
+    Ahead o{make_float4(0.f, 0.f, 0.f, 0.f), 0.0f, 0.0f, 0.0f, -INFINITY};
+    if (cc < nch) {
+      o.M = chunk_ref(scal, cc, N);
+      const int i = cc * kC + r;
+      if (i < N) {
+        o.sc = __ldg(scal + i);
+        if (hf == 0) {
+          o.x1 = __ldg(a.g1 + row0 + i);
+          o.xh = __ldg(a.gh + row0 + i);
+          if (a.g0) o.x0 = __ldg(a.g0 + row0 + i);
+        }
+      }
+    }
+    return o;
+  };
+  put_phi(0, 0);
+  Ahead cur = load_ahead(0), nxt{};
 
-  for (int c = rank, kk = 0; c < nch; c += CL, ++kk) {
+  for (int c = 0; c < nch; ++c) {
     const int st = c % CF::NSQ;
     const int i = c * kC + r;
     const bool valid = i < N;
-    Xch* xc = xch(smem, CF::XCH_OFF, st);
     mbar_arrive(&ms->pobar);
-    if (!mbar_wait_warp(&ms->pobar, kk & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
+    if (!mbar_wait_warp(&ms->pobar, c & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
       return;
     }
-    if (!mbar_wait_warp(&ms->tma_full[tf_index<D, CL>(c)], tf_phase<D, CL>(c), &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
+    if (!mbar_wait_warp(&ms->tma_full[st], (uint32_t)(c / CF::NSQ) & 1u, &ms->abort)) {
+      fail_wait(ms, a.status);
       return;
     }
     uint8_t* qt = smem + CF::Q_OFF + st * CF::KA * kTile;
     uint8_t* kt = smem + CF::K_OFF + st * CF::KA * kTile;
     uint8_t* vt = smem + CF::V_OFF + (c % CF::NSV) * 2 * kTile;
-    float g1n, ghn, g0n;
-    load_gates(c + CL, g1n, ghn, g0n);
-    float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
+    nxt = load_ahead(c + 1);
+    // ---- rotate this half's pair groups of q and k in place (TMA tiles), half norms ----
+    const bool rot = a.rope != 0 && valid;
+    float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
     {
-      // ---- rotate q, k in place (TMA tiles), norms ----
-      const bool rot = a.rope != 0 && valid;
-      float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
-      const float* ph = phi + (kk & 1) * (D / 2);
+      const float* ph = phi + (c & 1) * (D / 2);
       const float rf = (float)r;
-#pragma unroll 1
-      for (int g = 0; g < D / 16; ++g) {
+      constexpr int GH = D / 32;  // pair groups per half
+#pragma unroll
+      for (int gg = 0; gg < GH; ++gg) {
+        const int g = hf * GH + gg;
         float2 cs[8];
         if (rot) {
 #pragma unroll
@@ -763,114 +353,92 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
         rotate_group<D>(qt, r, g, rot, cs, qq2);
         rotate_group<D>(kt, r, g, rot, cs, kk2);
       }
-      const float qq = __fadd_rn(qq2.x, qq2.y), kq = __fadd_rn(kk2.x, kk2.y);
-      // ---- scalars of this token from the scalar warps ----
-      const int slot = kk % CF::SCALS;
-      if (!mbar_wait_warp(&ms->scal_full[slot], (kk / CF::SCALS) & 1, &ms->abort)) {
-        fail_wait<CL>(ms, a.status);
-        return;
-      }
-      const float4 sc = scal[slot * kC + r];
-      const float M = ms->Mslot[slot];
-      mbar_arrive(&ms->scal_empty[slot]);
-      const float s = sc.x, m = sc.y, Et = sc.z, P = sc.w;
-      // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
-      // contract: fast exp, reciprocal square root and division are accurate enough here)
-      const float kap = rsqrtf(fmaxf(kq, 1e-24f));
-      const float rho = rsqrtf(fmaxf(qq, 1e-24f));
-      float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid) {
-        ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
-        cs1 = __fmul_rn(s, kap);
-        ck = kap;
-        const float sig1 = __fdividef(1.0f, 1.0f + __expf(-g1));
-        const float sigh = __fdividef(1.0f, 1.0f + __expf(-gh));
+    }
+    nrm[hf * kC + r] = make_float2(__fadd_rn(qq2.x, qq2.y), __fadd_rn(kk2.x, kk2.y));
+    mbar_arrive(&ms->nbar);
+    if (!mbar_wait_warp(&ms->nbar, c & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    const float2 n0 = nrm[r], n1 = nrm[kC + r];
+    const float qq = __fadd_rn(n0.x, n1.x), kq = __fadd_rn(n0.y, n1.y);
+    // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
+    // contract: fast exp, reciprocal square root and division are accurate enough here)
+    const float s = cur.sc.x, m = cur.sc.y, Et = cur.sc.z, P = cur.sc.w, M = cur.M;
+    const float kap = rsqrtf(fmaxf(kq, 1e-24f));
+    float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
+    float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {
+      ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
+      cs1 = __fmul_rn(s, kap);
+      ck = kap;
+      if (hf == 0) {
+        const float rho = rsqrtf(fmaxf(qq, 1e-24f));
+        const float sig1 = __fdividef(1.0f, 1.0f + __expf(-cur.x1));
+        const float sigh = __fdividef(1.0f, 1.0f + __expf(-cur.xh));
         const float rt = __fdividef(1.0f, (float)(i + 1));
         const float b0c = (sig1 - sigh) * rt;
         const float ahat = __fdividef(sigh, Et) * __expf(M - m);
         cf.x = rho * ahat;
         cf.y = rho * b0c;
         cf.z = -rho * (b0c * P * rt + sigh * rt);
-        if (a.g0) cf.z += rho * __fdividef(1.0f, 1.0f + __expf(-g0)) * rt;  // zero-order term
-        if (!isfinite(cf.x) || !isfinite(ce)) report(a.status, kErrRange);
-      }
-      xc->coef[r] = cf;
-      xc->cols[0][r] = ce;
-      xc->cols[1][r] = cs1;
-      xc->cols[2][r] = ck;
-      if (r == 0) xc->M = M;
-      // Weight operands: W_{t,i} = a_t e_i + b_t s'_i + g_t k_i is formed by one K = 16 MMA of
-      // the row vector [a a' a a' b b' b b' g g' g g' 0 0 0 0] (hi and lo bf16 parts,
-      // x = x + x') and the column vector [e e' e e' s s' s s' k k' k k' 0 0 0 0] paired as
-      // (hi hi, hi lo, lo hi, lo lo): every product is exact in fp32, the representation error
-      // is about 2^-17 of each term, so the nearly cancelling sum keeps fp32-level accuracy.
-      // The buffer is single: both CTAs' weight MMAs of the previous chunk must have completed
-      // (without a cluster these warps wait for every phase of w_done in order; with one, the
-      // observer thread's count says how many phases completed).
-      bool wok = true;
-      if (c >= 1) {
-        wok = CL > 1 ? counter_wait(&ms->w_seen, c, &ms->abort)
-                     : mbar_wait(&ms->w_done, (c - 1) & 1, &ms->abort);
-      }
-      if (!__all_sync(0xffffffffu, wok)) {
-        fail_wait<CL>(ms, a.status);
-        return;
-      }
-      {
-        float xh[6], xl[6];
-        const float xs[6] = {cf.x, cf.y, cf.z, ce, cs1, ck};
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          xh[k] = __bfloat162float(__float2bfloat16_rn(xs[k]));
-          xl[k] = __fsub_rn(xs[k], xh[k]);
-        }
-        uint8_t* rw = smem + CF::RW_OFF;
-        uint8_t* cw = smem + CF::CW_OFF;
-        *reinterpret_cast<uint4*>(rw + sw32_off(r, 0)) =
-            make_uint4(pack_bf16x2(xh[0], xh[0]), pack_bf16x2(xl[0], xl[0]),
-                       pack_bf16x2(xh[1], xh[1]), pack_bf16x2(xl[1], xl[1]));
-        *reinterpret_cast<uint4*>(rw + sw32_off(r, 1)) =
-            make_uint4(pack_bf16x2(xh[2], xh[2]), pack_bf16x2(xl[2], xl[2]), 0u, 0u);
-        *reinterpret_cast<uint4*>(cw + sw32_off(r, 0)) =
-            make_uint4(pack_bf16x2(xh[3], xl[3]), pack_bf16x2(xh[3], xl[3]),
-                       pack_bf16x2(xh[4], xl[4]), pack_bf16x2(xh[4], xl[4]));
-        *reinterpret_cast<uint4*>(cw + sw32_off(r, 1)) =
-            make_uint4(pack_bf16x2(xh[5], xl[5]), pack_bf16x2(xh[5], xl[5]), 0u, 0u);
-      }
-      // Q, K, R, C and Xch are complete: the MMA may start, and with a cluster one thread
-      // bulk-copies them to the other CTA once every operand thread's writes are visible to the
-      // copy engine
-      fence_proxy_async_smem();
-      mbar_arrive(&ms->po_sync);
-      if (CL > 1 && r == 0) {
-        if (!mbar_wait(&ms->po_sync, kk & 1, &ms->abort)) {
-          fail_wait<CL>(ms, a.status);
-          return;
-        }
-        const uint32_t bar = mapa(smem_u32(&ms->peer_full), peer);
-        const uint32_t lq = smem_u32(qt), lk = smem_u32(kt);
-        const uint32_t lw = smem_u32(smem + CF::RW_OFF), lx = smem_u32(xc);
-        bulk_copy_to_cta(mapa(lq, peer), lq, CF::KA * kTile, bar);
-        bulk_copy_to_cta(mapa(lk, peer), lk, CF::KA * kTile, bar);
-        bulk_copy_to_cta(mapa(lw, peer), lw, 2 * kC * 32, bar);
-        bulk_copy_to_cta(mapa(lx, peer), lx, (uint32_t)sizeof(Xch), bar);
+        if (a.g0) cf.z += rho * __fdividef(1.0f, 1.0f + __expf(-cur.x0)) * rt;  // zero-order
+        if (!isfinite(cf.x)) report(a.status, kErrRange);
+      } else if (!isfinite(ce)) {
+        report(a.status, kErrRange);
       }
     }
-    // value slice of this token: raw bf16 words copied to columns 0..31 of the Vsc tile (once the
-    // stage's previous Vsc was consumed), the staging buffer handed back, then the scaled parts
-    if (!vsc_wait<D, CL>(ms, c)) {
-      fail_wait<CL>(ms, a.status);
+    if (hf == 0) {
+      coef_block(smem, CF::COEF_OFF, st)->coef[r] = cf;
+      mbar_arrive(&ms->cf_full[st]);
+    }
+    // Weight operands: W_{t,i} = a_t e_i + b_t s'_i + g_t k_i is formed by one K = 16 MMA of
+    // the row vector [a a' a a' b b' b b' g g' g g' 0 0 0 0] (hi and lo bf16 parts,
+    // x = x + x') and the column vector [e e' e e' s s' s s' k k' k k' 0 0 0 0] paired as
+    // (hi hi, hi lo, lo hi, lo lo): every product is exact in fp32, the representation error
+    // is about 2^-17 of each term, so the nearly cancelling sum keeps fp32-level accuracy.
+    // The buffer is single: the previous chunk's weight MMA must have completed.
+    if (c >= 1 && !mbar_wait_warp(&ms->w_done, (c - 1) & 1, &ms->abort)) {
+      fail_wait(ms, a.status);
       return;
     }
-    copy_v_row(vt, smem + CF::VST_OFF, r);
+    {
+      const float x0 = hf == 0 ? cf.x : ce, x1 = hf == 0 ? cf.y : cs1, x2 = hf == 0 ? cf.z : ck;
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      const float h2 = __bfloat162float(__float2bfloat16_rn(x2));
+      const float l0 = __fsub_rn(x0, h0), l1 = __fsub_rn(x1, h1), l2 = __fsub_rn(x2, h2);
+      if (hf == 0) {
+        uint8_t* rw = smem + CF::RW_OFF;
+        *reinterpret_cast<uint4*>(rw + sw32_off(r, 0)) =
+            make_uint4(pack_bf16x2(h0, h0), pack_bf16x2(l0, l0), pack_bf16x2(h1, h1),
+                       pack_bf16x2(l1, l1));
+        *reinterpret_cast<uint4*>(rw + sw32_off(r, 1)) =
+            make_uint4(pack_bf16x2(h2, h2), pack_bf16x2(l2, l2), 0u, 0u);
+      } else {
+        uint8_t* cw = smem + CF::CW_OFF;
+        *reinterpret_cast<uint4*>(cw + sw32_off(r, 0)) =
+            make_uint4(pack_bf16x2(h0, l0), pack_bf16x2(h0, l0), pack_bf16x2(h1, l1),
+                       pack_bf16x2(h1, l1));
+        *reinterpret_cast<uint4*>(cw + sw32_off(r, 1)) =
+            make_uint4(pack_bf16x2(h2, l2), pack_bf16x2(h2, l2), 0u, 0u);
+      }
+    }
+    // Q, K, R, C and the coefficients are complete: the MMA may start
+    fence_proxy_async_smem();
+    mbar_arrive(&ms->po_sync);
+    // half of the value row: raw bf16 words to the Vsc tile (once the stage's previous Vsc was
+    // consumed), the staging buffer handed back, then the scaled parts
+    if (!vsc_wait<D>(ms, c)) {
+      fail_wait(ms, a.status);
+      return;
+    }
+    build_vsc_half(vt, smem + CF::VST_OFF, r, 2 * hf, ce, cs1, ck);
     mbar_arrive(&ms->vst_empty);
-    build_vsc_row(vt, r, ce, cs1, ck);
     fence_proxy_async_smem();
     mbar_arrive(&ms->op_full);
-    if (c + CL < nch) put_phi(c + CL, (kk + 1) & 1);
-    g1 = g1n;
-    gh = ghn;
-    g0 = g0n;
+    if (c + 1 < nch) put_phi(c + 1, (c + 1) & 1);
+    cur = nxt;
   }
 }
 
@@ -882,14 +450,12 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, int h, 
 //   X[:, 0:96] = Q [F~ | G | H] (c >= 1)    (previous outputs read from X)
 //                                                                      -> sst_free, qk_empty
 //   X[:, 96:128] = S V                      (this chunk's S tile formed)   -> x_full, vsc_free
-// qk_empty follows the Q [F|G|H] product (the S V product for the first chunk).  w_done and
-// qk_empty are delivered to both CTAs of a cluster (the owner of a later chunk writes into the
-// other CTA's buffers).  The epilogue reads a chunk's Xch block before it frees X of the
-// previous chunk, which the Q [F|G|H] product waits for.
-template <int D, int CL>
+// qk_empty follows the Q [F|G|H] product (the S V product for the first chunk).  The epilogue
+// reads a chunk's coefficients before it frees X of the previous chunk, which the Q [F|G|H]
+// product waits for.
+template <int D>
 __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
-  constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1u);  // every CTA of the cluster
-  using CF = Cfg<D, CL>;
+  using CF = Cfg<D>;
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const uint32_t tA = tm + CF::TM_A, tW = tm + CF::TM_W, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
@@ -899,90 +465,79 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
   constexpr uint32_t id_st = idesc_bf16_f32(128, D, true, true);       // Vsc^T K
   const uint64_t d_rw = sw32_desc(base + CF::RW_OFF), d_cw = sw32_desc(base + CF::CW_OFF);
   bool ok = true;
-  const int rank = CL > 1 ? (int)cluster_rank() : 0;
+  // descriptors: the start address field is (address >> 4), and every tile lies below 256 KB,
+  // so the descriptor of base + off is the base's descriptor + off / 16
+  const uint64_t dq0 = sw128_desc(base + CF::Q_OFF, 16, 1024);
+  const uint64_t dk0 = sw128_desc(base + CF::K_OFF, 16, 1024);
+  const uint64_t dkm0 = sw128_desc(base + CF::K_OFF, kTile, 1024);   // K as MN-major B
+  const uint64_t dv0 = sw128_desc(base + CF::V_OFF, kTile, 1024);
+  const uint64_t dsst = sw128_desc(base + CF::SST_OFF + 32 * 128, 16, 1024);
   for (int c = 0; c < nch && ok; ++c) {
     const int st = c % CF::NSQ;
-    const bool owned = (c % CL) == rank;
-    const uint32_t ph = (uint32_t)(c / CL) & 1u;  // phase of the owned / other-owned barriers
-    const uint32_t qt = base + CF::Q_OFF + st * CF::KA * kTile;
-    const uint32_t kt = base + CF::K_OFF + st * CF::KA * kTile;
-    const uint32_t vt = base + CF::V_OFF + (c % CF::NSV) * 2 * kTile;
-    ok = owned ? mbar_wait(&ms->po_sync, ph, &ms->abort)
-               : mbar_wait_cl(&ms->peer_full, ph, &ms->abort);
+    const uint32_t ph = (uint32_t)c & 1u;
+    const uint64_t sq = (uint64_t)((st * CF::KA * kTile) >> 4);
+    const uint64_t sv = (uint64_t)(((c % CF::NSV) * 2 * kTile) >> 4);
+    ok = mbar_wait(&ms->po_sync, ph, &ms->abort);
     if (ok && c >= 1) ok = mbar_wait(&ms->a_free, (c - 1) & 1, &ms->abort);
     // the S tile shares the Q K^T columns: the previous S V product must have read it
     if (CF::TM_S == CF::TM_A && ok && c >= 1) ok = mbar_wait(&ms->x_full, (c - 1) & 1, &ms->abort);
-    // every phase of w_done is observed in order (the end-of-kernel wait relies on it)
-    if (ok && c >= 1) ok = mbar_wait_cl(&ms->w_done, (c - 1) & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
     // ---- A = Q K^T (K = d); W = R C^T (K = 16) ----
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
-      mma_bf16(tA, sw128_desc(qt + off, 16, 1024), sw128_desc(kt + off, 16, 1024), id_qk,
-               kk > 0);
+      const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
+      mma_bf16(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
     }
     mma_bf16(tW, d_rw, d_cw, id_qk, 0u);
     mma_commit(&ms->a_full);
-    if (CL > 1) mma_commit_mc(&ms->w_done, kAll);
-    else mma_commit(&ms->w_done);
+    mma_commit(&ms->w_done);
     // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
     if (c >= 1 && !mbar_wait(&ms->sst_full, (c - 1) & 1, &ms->abort)) { ok = false; break; }
-    ok = owned ? mbar_wait(&ms->op_full, ph, &ms->abort) : mbar_wait(&ms->vsc_full, ph, &ms->abort);
-    if (!ok) break;
+    if (!mbar_wait(&ms->op_full, ph, &ms->abort)) { ok = false; break; }
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint32_t off = kk * 2048;
-      mma_bf16(tS, sw128_desc(vt + off, kTile, 1024), sw128_desc(kt + off, kTile, 1024), id_st,
-               (c > 0 || kk > 0) ? 1u : 0u);
+      const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+      mma_bf16(tS, dv0 + sv + off, dkm0 + sq + off, id_st, (c > 0 || kk > 0) ? 1u : 0u);
     }
     mma_commit(&ms->st_done);
     // ---- X[:, 0:96] = Q [F~ | G | H] (state of the previous chunks, B tile rows 32..127) ----
     if (c >= 1) {
       if (!mbar_wait(&ms->x_free, (c - 1) & 1, &ms->abort)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sst = base + CF::SST_OFF + 32 * 128;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * kTile + (kk % 4) * 32;
-        mma_bf16(tX, sw128_desc(qt + off, 16, 1024), sw128_desc(sst + off, 16, 1024), id_qs,
-                 kk > 0);
+        const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
+        mma_bf16(tX, dq0 + sq + off, dsst + off, id_qs, kk > 0);
       }
       mma_commit(&ms->sst_free);
-      // Q, K (and, through the epilogue's order, Xch) of this chunk are no longer read
-      if (CL > 1) mma_commit_mc(&ms->qk_empty[st], kAll);
-      else mma_commit(&ms->qk_empty[st]);
+      mma_commit(&ms->qk_empty[st]);  // Q, K and the coefficients of this chunk are not read again
     }
     // ---- X[:, 96:128] = S V ----
     if (!mbar_wait(&ms->am_full, c & 1, &ms->abort)) { ok = false; break; }
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint32_t boff = kk * 2048;  // MN-major B, 16 token rows per step
-      mma_bf16_ts(tX + 96, tm + CF::TM_S + kk * 8, sw128_desc(vt + boff, kTile, 1024), id_sv,
-                  kk > 0);
+      const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows per step
+      mma_bf16_ts(tX + 96, tm + CF::TM_S + kk * 8, dv0 + sv + boff, id_sv, kk > 0);
     }
     mma_commit(&ms->x_full);
-    if (c == 0) {  // the first chunk has no Q [F|G|H] product: release after the S tile was read
-      if (CL > 1) mma_commit_mc(&ms->qk_empty[st], kAll);
-      else mma_commit(&ms->qk_empty[st]);
-    }
+    if (c == 0) mma_commit(&ms->qk_empty[st]);  // no Q [F|G|H] product: after the S tile was read
     mma_commit(&ms->vsc_free[c & 1]);
   }
-  if (!ok) fail_wait<CL>(ms, a.status);
+  if (!ok) fail_wait(ms, a.status);
   mma_commit(&ms->fin);
 }
 
 // ============================================================================ E: epilogue
-// Per chunk c: the S tile (A o W, masked, bf16), the scaled value tile of chunk c+1 when the
-// other CTA of the cluster owns it, the state after chunk c as the bf16 B tile of chunk c+1 (F~
-// rescaled to M_{c+1}), then the output rows of chunk c.
-template <int D, int CL, bool LN>
+// Per chunk c: the S tile (A o W, masked, bf16), the state after chunk c as the bf16 B tile of
+// chunk c+1 (F~ rescaled to M_{c+1}), then the output rows of chunk c.  The chunk references
+// come from the scalar pass, so the state copy waits only for the state update.
+template <int D, bool LN>
 __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh, size_t row0,
                               int nch) {
-  using CF = Cfg<D, CL>;
+  using CF = Cfg<D>;
   const int wq = (threadIdx.x >> 5) & 3;          // TMEM lane quadrant of this warp
   const int t = wq * 32 + (threadIdx.x & 31);     // TMEM lane = token row / state row
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -990,45 +545,21 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   const uint32_t base = smem_u32(smem);
   const int j0 = blockIdx.y * kDV;
   const int N = a.N;
+  const float4* __restrict__ scal = a.scal + row0;
   __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(a.out) + row0 * D;
-  const int rank = CL > 1 ? (int)cluster_rank() : 0;
-  auto owned = [&](int cc) { return (cc % CL) == rank; };
-  // coefficients and M of chunk cc are in this CTA's Xch block
-  auto wait_xch = [&](int cc) -> bool {
-    const uint32_t ph = (uint32_t)(cc / CL) & 1u;
-    return owned(cc) ? mbar_wait_warp(&ms->po_sync, ph, &ms->abort)
-                     : mbar_wait_cl_warp(&ms->peer_full, ph, &ms->abort);
-  };
-  // value tile of a chunk owned by the other CTA (row t)
-  auto vsc_other = [&](int cc) -> bool {
-    const int sv = cc % CF::NSV;
-    if (!mbar_wait_warp(&ms->tma_full[tf_index<D, CL>(cc)], tf_phase<D, CL>(cc), &ms->abort))
-      return false;
-    if (!vsc_wait<D, CL>(ms, cc)) return false;
-    uint8_t* vt = smem + CF::V_OFF + sv * 2 * kTile;
-    copy_v_row(vt, smem + CF::VST_OFF, t);
-    mbar_arrive(&ms->vst_empty);
-    if (!mbar_wait_cl_warp(&ms->peer_full, (uint32_t)(cc / CL) & 1u, &ms->abort)) return false;
-    const Xch* xv = xch(smem, CF::XCH_OFF, cc % CF::NSQ);
-    build_vsc_row(vt, t, xv->cols[0][t], xv->cols[1][t], xv->cols[2][t]);
-    fence_proxy_async_smem();
-    mbar_arrive(&ms->vsc_full);
-    return true;
-  };
   bool ok = true;
-  if (CL > 1 && nch > 0 && !owned(0)) ok = vsc_other(0);
-  // (a, b, g) of row t and M of the current chunk: read while the previous chunk is in flight
-  // (before X of that chunk is freed), since the chunk's Xch block is released with its Q, K
+  // (a, b, g) of row t of the current chunk: read while the previous chunk is in flight (before
+  // X of that chunk is freed), since the coefficient block is released with the chunk's Q, K
   float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
   float M_cur = 0.0f;
-  if (ok && nch > 0) {
-    ok = wait_xch(0);
-    cf = xch(smem, CF::XCH_OFF, 0)->coef[t];
-    M_cur = xch(smem, CF::XCH_OFF, 0)->M;
+  if (nch > 0) {
+    M_cur = chunk_ref(scal, 0, N);
+    ok = mbar_wait_warp(&ms->cf_full[0], 0, &ms->abort);
+    if (ok) cf = coef_block(smem, CF::COEF_OFF, 0)->coef[t];
   }
   for (int c = 0; c < nch && ok; ++c) {
     float4 cf_next = make_float4(0.f, 0.f, 0.f, 0.f);
-    float M_next = 0.0f;
+    const float M_next = c + 1 < nch ? chunk_ref(scal, c + 1, N) : 0.0f;
     // ---- S = [i <= t] (Q K^T) o W, fp32 product then bf16 (rows t, K = token i) ----
     ok = mbar_wait_warp(&ms->a_full, c & 1, &ms->abort);
     if (!ok) break;
@@ -1086,20 +617,11 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     tc_fence_before();
     mbar_arrive(&ms->a_free);
     mbar_arrive(&ms->am_full);
-    if (CL > 1 && c + 1 < nch && !owned(c + 1)) {
-      ok = vsc_other(c + 1);
-      if (!ok) break;
-    }
     // ---- state after chunk c -> bf16 B operand rows 32..127 of chunk c+1, F~ rescaled ----
     if (c + 1 < nch) {
-      const int st1 = (c + 1) % CF::NSQ;
-      ok = wait_xch(c + 1);
-      if (ok) ok = mbar_wait_warp(&ms->st_done, c & 1, &ms->abort);
+      ok = mbar_wait_warp(&ms->st_done, c & 1, &ms->abort);
       if (ok && c >= 1) ok = mbar_wait_warp(&ms->sst_free, (c - 1) & 1, &ms->abort);
       if (!ok) break;
-      const Xch* xn = xch(smem, CF::XCH_OFF, st1);
-      cf_next = xn->coef[t];
-      M_next = xn->M;
       tc_fence_after();
       if (wq >= 1) {
         const bool rescale = (wq == 1) && (M_next > M_cur);
@@ -1237,6 +759,13 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       for (int j = 0; j < 8; ++j)
         ob[j] = pack_bf16x2(__uint_as_float(rsv[2 * j]), __uint_as_float(rsv[2 * j + 1]));
       if (hf == 1) {
+        // the next chunk's coefficients, before its coefficient block can be released
+        if (c + 1 < nch) {
+          const int sn = (c + 1) % CF::NSQ;
+          ok = mbar_wait_warp(&ms->cf_full[sn], (uint32_t)((c + 1) / CF::NSQ) & 1u, &ms->abort);
+          if (!ok) break;
+          cf_next = coef_block(smem, CF::COEF_OFF, sn)->coef[t];
+        }
         tc_fence_before();
         mbar_arrive(&ms->x_free);
       }
@@ -1245,17 +774,18 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         dst[2 * hf + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
       }
     }
+    if (!ok) break;
     cf = cf_next;
     M_cur = M_next;
   }
   if (!ok) {
-    fail_wait<CL>(ms, a.status);
+    fail_wait(ms, a.status);
     return;
   }
   // ---- final state (prefill): columns j0.. of F~, G, H (state rows 32..127) ----
   if (a.final_state && nch > 0) {
     if (!mbar_wait_warp(&ms->st_done, (nch - 1) & 1, &ms->abort)) {
-      fail_wait<CL>(ms, a.status);
+      fail_wait(ms, a.status);
       return;
     }
     tc_fence_after();
@@ -1275,9 +805,9 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
 }
 
 // ============================================================================ kernel
-template <int D, int CL, bool LN>
+template <int D, bool LN>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ ChunkParams p) {
-  using CF = Cfg<D, CL>;
+  using CF = Cfg<D>;
   const FwdArgs& a = p.a;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -1287,19 +817,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   }
   Misc* ms = reinterpret_cast<Misc*>(smem + CF::MISC_OFF);
   const int warp = threadIdx.x >> 5;
-  const int bh = blockIdx.x, h = bh % a.H;
+  const int bh = blockIdx.x;
   const size_t row0 = (size_t)bh * a.N;
   const int nch = (a.N + kC - 1) / kC;
-  const int rank = CL > 1 ? (int)cluster_rank() : 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2; ++i) mbar_init(&ms->vsc_free[i], 1);
+    for (int i = 0; i < kMaxNSQ; ++i) {
       mbar_init(&ms->tma_full[i], 1);
-      mbar_init(&ms->vsc_free[i], 1);
+      mbar_init(&ms->qk_empty[i], 1);
+      mbar_init(&ms->cf_full[i], 128);
     }
-    for (int i = 0; i < 3; ++i) mbar_init(&ms->qk_empty[i], CL);
-    mbar_init(&ms->op_full, 128);
-    mbar_init(&ms->vsc_full, 128);
+    mbar_init(&ms->op_full, 256);
     mbar_init(&ms->a_full, 1);
     mbar_init(&ms->a_free, 128);
     mbar_init(&ms->am_full, 128);
@@ -1309,29 +838,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     mbar_init(&ms->x_free, 128);
     mbar_init(&ms->st_done, 1);
     mbar_init(&ms->fin, 1);
-    mbar_init(&ms->w_done, CL);
-    mbar_init(&ms->pbar, 128);
-    mbar_init(&ms->pobar, 128);
-    mbar_init(&ms->po_sync, 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->scal_full[i], 128);
-      mbar_init(&ms->scal_empty[i], 128);
-    }
-    mbar_init(&ms->u_full, 1);
-    mbar_init(&ms->u_empty, 128);
-    mbar_init(&ms->vst_empty, 128);
-    mbar_init(&ms->peer_full, 1);
-    mbar_init(&ms->ccar_full, 32);
-    mbar_init(&ms->kcar_full, 1);
+    mbar_init(&ms->w_done, 1);
+    mbar_init(&ms->pobar, 256);
+    mbar_init(&ms->nbar, 256);
+    mbar_init(&ms->po_sync, 256);
+    mbar_init(&ms->vst_empty, 256);
     // LayerNorm statistics: one arrival per epilogue warp of every other value slice
     for (int i = 0; i < 2; ++i) mbar_init(&ms->ln_full[i], 4 * (D / kDV - 1));
     ms->abort = 0;
     ms->never = 0;
-    ms->w_seen = 0;
-    if (CL > 1 || LN) fence_mbarrier_init_cluster();
+    if (LN) fence_mbarrier_init_cluster();
   }
   if (LN && threadIdx.x < 64) {  // this slice's LayerNorm gain (1 when absent) and bias (0)
-    const int j = threadIdx.x & 31;
+    const int h = bh % a.H, j = threadIdx.x & 31;
     const float* src = threadIdx.x < 32 ? a.ln_w : a.ln_b;
     reinterpret_cast<float*>(smem + CF::LNW_OFF)[threadIdx.x] =
         src ? src[(size_t)h * D + blockIdx.y * kDV + j] : (threadIdx.x < 32 ? 1.0f : 0.0f);
@@ -1343,22 +862,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL > 1 || LN) cluster_sync_all();  // the other CTAs' barriers exist before any remote access
+  if (LN) cluster_sync_all();  // the other CTAs' barriers exist before any remote access
 
-  if (warp < 8 && (warp & 2) == 0) {
-    role_scalars<D, CL>(a, smem, ms, bh, h, row0, nch, rank);
-  } else if (warp < 8) {
-    role_operands<D, CL>(a, smem, ms, h, row0, nch, rank);
+  if (warp < 8) {
+    role_operands<D>(a, smem, ms, row0, nch);
   } else if (warp < 12) {
-    role_epilogue<D, CL, LN>(a, smem, ms, bh, row0, nch);
+    role_epilogue<D, LN>(a, smem, ms, bh, row0, nch);
   } else if (warp == 12) {
-    if ((threadIdx.x & 31) == 0) role_mma<D, CL>(a, smem, ms, nch);
+    if ((threadIdx.x & 31) == 0) role_mma<D>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
-    role_tma<D, CL>(p, smem, ms, bh, nch, rank);
-  } else if ((threadIdx.x & 31) == 1) {
-    role_tma_u<D, CL>(p, smem, ms, bh, nch, rank);
-  } else if (CL > 1 && (threadIdx.x & 31) == 2) {
-    role_wdone_observer<CL>(a, ms, nch);
+    role_tma<D>(p, smem, ms, bh, nch);
   }
 
   tc_fence_before();
@@ -1368,17 +881,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
     tc_fence_after();
     tmem_dealloc(ms->tmem, 512);
-  }
-  if (CL > 1 && threadIdx.x == 0 && nch > 0) {
-    // The other CTA's last stage and weight releases land in this CTA's barriers: wait for
-    // them (bounded) so that no arrival targets this CTA after it exits.  Every earlier phase
-    // of these barriers was waited for in order, so the parity identifies the phase.
-    for (int st = 0; st < CF::NSQ && st < nch; ++st) {
-      const int c_last = st + ((nch - 1 - st) / CF::NSQ) * CF::NSQ;
-      if (!mbar_wait_cl(&ms->qk_empty[st], (c_last / CF::NSQ) & 1, &ms->never, 1ll << 31))
-        report(a.status, kErrTimeout);
-    }
-    // (every phase of w_done was waited for by the observer thread before the final barrier)
   }
   // LayerNorm: the other slices write statistics into this CTA's shared memory until their
   // last chunk; no CTA of the cluster exits before all have finished (every wait is bounded,
@@ -1425,16 +927,15 @@ bool make_map(CUtensorMap* m, const void* ptr, int d, int N, int BH, int box_x,
 template <int D, bool LN>
 cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   // with the output LayerNorm the D / 32 value slices of a head form one cluster
-  constexpr int kClY = LN ? D / kDV : kCL;
-  static_assert(!LN || kCL == 1, "the LayerNorm cluster spans the value slices");
+  constexpr int kClY = LN ? D / kDV : 1;
   static std::atomic<uint64_t> attr_set{0};  // bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(chunk_kernel<D, kCL, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Cfg<D, kCL>::SMEM);
+    e = cudaFuncSetAttribute(chunk_kernel<D, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
@@ -1443,14 +944,12 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   if (!make_map(&p.tq, a.q, D, a.N, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&p.tk, a.k, D, a.N, BH, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&p.tv, a.v, D, a.N, BH, kDV, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&p.tu, a.u, D, a.N, BH, D, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_map(&p.tv, a.v, D, a.N, BH, kDV, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorNotSupported;
-  static_assert((D / kDV) % kCL == 0, "value slices pair up into clusters");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(BH, D / kDV, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<D, kCL>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1459,7 +958,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = kClY > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, chunk_kernel<D, kCL, LN>, p);
+  e = cudaLaunchKernelEx(&cfg, chunk_kernel<D, LN>, p);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1472,6 +971,7 @@ bool chunk_supported(int d, int dtype, int causal) {
 }
 
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream) {
+  if (!a.scal) return cudaErrorInvalidValue;
   if (a.d == 64) return a.ln ? launch_d<64, true>(a, stream) : launch_d<64, false>(a, stream);
   if (a.d == 128) return a.ln ? launch_d<128, true>(a, stream) : launch_d<128, false>(a, stream);
   return cudaErrorInvalidValue;

@@ -23,6 +23,9 @@ struct FwdArgs {
   int ln;                    // output LayerNorm over each head's d columns
   const float *ln_w, *ln_b;  // nullable [H,d] gain and bias
   float ln_eps;
+  // chunked path: per-token (s, m, Et, P) of the blocked contract, [B*H, N], written by
+  // launch_fwd_scalars before the chunk kernel reads it
+  float4* scal;
 };
 
 struct DecodeArgs {
@@ -79,9 +82,14 @@ constexpr size_t kNoAllocRopeEntries = size_t(1) << 17;
 // Device address of that scratch on the current device (looked up once per device).
 cudaError_t noalloc_rope_table(float2** table);
 
-// zs_chunk.cu
+// zs_chunk.cu: the chunked forward (d in {64, 128}, bf16, causal).  a.scal must hold the
+// per-token scalars (launch_fwd_scalars on the same stream first).
 bool chunk_supported(int d, int dtype, int causal);
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);
+
+// zs_scalars.cu: per-token (s, m, Et, P) of every sequence into scal ([B*H, N] float4), the
+// debug scalars and the scalar part of the final state when asked for (d in {64, 128}).
+cudaError_t launch_fwd_scalars(const FwdArgs& a, float4* scal, cudaStream_t stream);
 
 // zs_backward.cu
 size_t bwd_scratch_bytes(int B, int H, int N, int d);

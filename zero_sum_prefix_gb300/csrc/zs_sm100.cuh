@@ -167,6 +167,11 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t caddr, float x, float 
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(x), "f"(y)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t caddr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void st_cluster_s32(uint32_t caddr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
 }
