@@ -49,7 +49,7 @@ L2_FLUSH_BYTES = 256 << 20
 # change.
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
                  "zero_sum_prefix_gb300/csrc/zs_sm100.cuh", "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"a39f27938042fa78": 34121984 + 3072 + 107020800 + 16308224}
 
 
 def kernel_fingerprint() -> str:
