@@ -34,7 +34,10 @@
  * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *
  * Memory.  The library allocates nothing per call once warm: it keeps one lazily created,
- * per-device workspace (rotary tables) that only grows; it is released at process exit.
+ * per-device workspace that only grows (growing it waits for the device) and is released at
+ * process exit: rotary tables; for the chunked causal path 16*B*H*N bytes of per-token
+ * scalars; the backward and ZeroS-SM scratches described at those calls.  Code that captures
+ * calls into a CUDA graph makes one call of the same or larger size before the capture.
  */
 #ifndef ZEROS_H
 #define ZEROS_H
@@ -61,7 +64,8 @@ typedef enum { ZEROS_BF16 = 0, ZEROS_F32 = 1 } zeros_dtype;
 typedef enum {
   ZEROS_PATH_AUTO = 0,  /* chunked tensor-core scan where available, else the SIMT scan      */
   ZEROS_PATH_SIMT = 1,  /* token-sequential CUDA-core scan (fp32 and bf16 inputs)            */
-  ZEROS_PATH_CHUNK = 2  /* chunked tcgen05/TMEM scan (bf16 inputs, causal)                   */
+  ZEROS_PATH_CHUNK = 2  /* chunked tcgen05/TMEM scan (bf16 inputs, causal): a scalar pass
+                           (per-token logits and prefix scalars), then the chunk kernel         */
 } zeros_path;
 
 /*
