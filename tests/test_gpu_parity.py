@@ -278,3 +278,24 @@ def test_chunk_final_state_matches_simt(zs, d, N):
     for key in ("F", "G", "H"):
         err = (vc[key] - vs[key]).abs().max() / vs[key].abs().max()
         assert err < 2e-2, (key, float(err))
+
+
+@pytest.mark.parametrize("d,N", [(64, 4096 + 300), (128, 2 * 2048 + 37)])
+def test_chunk_scalars_across_segments_bitexact(zs, d, N):
+    """The scalar pass walks a sequence in segments (4096 tokens at d = 64, 2048 at d = 128)
+    and carries the column sums and the scalar folds from one segment to the next: the per-token
+    logits and prefix scalars, and the scalar part of the prefill state, equal the
+    token-sequential path's bit for bit past the segment boundaries (ragged last block)."""
+    B, H = 1, 2
+    w = zi.Workload("segments", B, H, N, d, rope=True, seed=5151 + d)
+    inp = zi.make(w, "cuda")
+    st_c = torch.empty(zs.state_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+    st_s = torch.empty_like(st_c)
+    _, dbg_c = run(zs, inp, w, path="chunk", debug=True, final_state=st_c)
+    _, dbg_s = run(zs, inp, w, path="simt", debug=True, final_state=st_s)
+    assert zs.get_status() == 0
+    for key in ("s", "E", "P", "m"):
+        assert torch.equal(dbg_c[key].view(torch.int32), dbg_s[key].view(torch.int32)), key
+    vc, vs = zs.state_view(st_c, B, H, d), zs.state_view(st_s, B, H, d)
+    for key in ("t", "mC", "EC", "CP", "etau", "ml", "El", "LP", "C", "L", "mu"):
+        assert torch.equal(vc[key], vs[key]), key
