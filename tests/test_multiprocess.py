@@ -87,3 +87,14 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert len(lines[0]) == 1 and lines[1] == []
     line = json.loads(lines[0][0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the line keeps the contract's keys: the same metric and unit as the kernel arm, the
+    # oracle described as its CPU baseline, and an end-to-end figure with no device copies
+    for key in ("metric", "unit", "higher_is_better", "ms_per_step", "config", "dtype", "data"):
+        assert key in line, key
+    assert line["higher_is_better"] is True and line["unit"] == "tokens/s"
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert cpu["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
