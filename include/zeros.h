@@ -37,7 +37,9 @@
  * per-device workspace that only grows (growing it waits for the device) and is released at
  * process exit: rotary tables; for the chunked causal path 16*B*H*N bytes of per-token
  * scalars; the backward and ZeroS-SM scratches described at those calls.  Code that captures
- * calls into a CUDA graph makes one call of the same or larger size before the capture.
+ * calls into a CUDA graph makes one call of the same or larger size before the capture.  The
+ * workspace is shared by every stream of the device: calls on different streams must not
+ * overlap on the GPU (order them with events), or they overwrite each other's scratch.
  */
 #ifndef ZEROS_H
 #define ZEROS_H
