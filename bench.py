@@ -44,9 +44,8 @@ WORKLOADS = {
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) of one forward call (the scalar pass and the chunk kernel), from the
-# ncu captures summarised in profiles/chunk_kernel_causal_rope_b8h8n4096d64.md, keyed by a
-# fingerprint of the kernel sources they were measured on; reported as null once the sources
-# change.
+# committed ncu summaries of this workload, keyed by a fingerprint of the kernel sources they
+# were measured on; reported as null once the sources change.
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
                  "zero_sum_prefix_gb300/csrc/zs_sm100.cuh", "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
 MEASURED_TRAFFIC = {"a39f27938042fa78": 34121984 + 3072 + 107020800 + 16308224}

@@ -152,8 +152,10 @@ int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, c
  *     (cos, sin) table, lives in a fixed 1 MiB device array compiled into the library, which every
  *     device that loads the library holds until the process exits; with rope = 1 it needs
  *     N * d / 2 <= 131072 and returns ZEROS_ERR_UNSUPPORTED beyond that.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress), so a context that was reset and created again is served its new
+ *     address.  The first call on a device may load the library's device code for that
+ *     device: make that first call before any stream capture.
  *   - Every call rewrites the shared table, so calls that overlap on the GPU (different streams
  *     at the same time) race; serialise them.
  *   - status: nullable device int, caller-owned.  It is zeroed on `stream` at the start of the

@@ -3,9 +3,10 @@
 Tolerance metric (the same everywhere): for every compared (b, h) sequence,
     err = max_t,j |o - o_ref| / max_t,j |o_ref|
 and the test asserts the worst sequence is within 1e-5 for fp32 inputs and 1e-2 for bf16
-inputs (fp32 accumulation).  The denominator has a floor of 0.1 (the scale of the outputs for
-N(0, 1) values): a sequence whose exact output is identically zero (N = 1: w_{1,1} = 0) is then
-held to an absolute error of 0.1 x tolerance instead of a meaningless relative one.  The logit s, the prefix sum P, the running maximum m and the
+inputs (fp32 accumulation).  The one sequence shape whose exact output is identically zero is
+a single token (w_{1,1} = 0, so o_1 = 0; the fp64 oracle returns rounding noise there): it has
+no relative error and is held to max|o - o_ref| <= tolerance in absolute terms, the outputs
+being built from N(0, 1) values.  The logit s, the prefix sum P, the running maximum m and the
 scaled prefix sum Et = E e^{-m} must be bit-identical between the forward pass and the
 token-by-token decode step.
 """
@@ -19,7 +20,6 @@ import zeros_inputs as zi
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-5, "bf16": 1e-2}
-DEN_FLOOR = 0.1
 
 
 @pytest.fixture(scope="module")
@@ -32,14 +32,23 @@ def zs():
 
 
 def seq_err(o, ref):
-    """Worst per-sequence max-abs error over max-abs reference (o, ref: [S, N, d])."""
+    """Worst per-sequence max|o - o_ref| / max|o_ref| (o, ref: [S, N, d]).
+
+    Sequences of one token (exact output 0) contribute their absolute error instead.  The
+    worst ratio is printed (visible with pytest -s or on failure)."""
     o = np.asarray(o, np.float64)
     ref = np.asarray(ref, np.float64)
     worst = 0.0
     for i in range(ref.shape[0]):
-        den = max(np.abs(ref[i]).max(), DEN_FLOOR)
-        num = np.abs(o[i] - ref[i]).max()
-        worst = max(worst, num / den)
+        num = np.abs(o[i] - ref[i]).max() if ref[i].size else 0.0
+        if ref.shape[1] == 1:  # a single token: o_1 = 0 exactly
+            err = num
+        else:
+            den = np.abs(ref[i]).max()
+            assert den > 0.0, "a sequence of two or more tokens with an all-zero reference"
+            err = num / den
+        worst = max(worst, err)
+    print(f"worst per-sequence error {worst:.3e}")
     return worst
 
 

@@ -79,7 +79,7 @@ cudaError_t launch_rope_table(float2* table, int N, int d, double base, cudaStre
 
 // Fixed scratch of the allocation-free forward: (cos, sin) entries for N * d/2 <= this bound.
 constexpr size_t kNoAllocRopeEntries = size_t(1) << 17;
-// Device address of that scratch on the current device (looked up once per device).
+// Device address of that scratch on the current device (looked up on every call).
 cudaError_t noalloc_rope_table(float2** table);
 
 // zs_chunk.cu: the chunked forward (d in {64, 128}, bf16, causal).  a.scal must hold the

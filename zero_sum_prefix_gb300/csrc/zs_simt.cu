@@ -14,7 +14,6 @@
 // normalise / rotate q_t and k_t and stage v_t in shared memory.
 #include <math.h>
 
-#include <mutex>
 
 #include "zs_common.cuh"
 #include "zs_internal.h"
@@ -430,22 +429,14 @@ __global__ void rope_table_kernel(float2* table, int N, int d, double base) {
 static __device__ __align__(256) float2 g_noalloc_rope[kNoAllocRopeEntries];
 
 cudaError_t noalloc_rope_table(float2** table) {
-  // Host code cannot use the array's name as a device address: ask the runtime for it (once
-  // per device, with that device current).
-  static std::mutex mtx;
-  static float2* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // Host code cannot use the array's name as a device address: ask the runtime for it, with the
+  // calling device current.  The lookup is repeated on every call (it is a host-side query, not
+  // stream work), so a context that was torn down and created again (cudaDeviceReset), which
+  // may place the array elsewhere, is never served a stale address.
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_rope);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(mtx);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_rope);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<float2*>(p);
-  }
-  *table = addr[dev];
+  *table = static_cast<float2*>(p);
   return cudaSuccess;
 }
 
