@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -36,6 +37,10 @@ struct DeviceWorkspace {
   size_t sm_bytes = 0;
   void* fwd = nullptr;    // chunked forward scratch (per-token scalars)
   size_t fwd_bytes = 0;
+  float* wang = nullptr;  // rotary angles of the d = 64 walk (frequencies, chunk base angles)
+  size_t wang_floats = 0;
+  int wang_N = 0;
+  float wang_base = 0.0f;
   float2* rope = nullptr;
   size_t rope_entries = 0;  // capacity in float2
   int rope_N = 0, rope_d = 0;
@@ -103,6 +108,44 @@ int rope_table(DeviceWorkspace* ws, int N, int d, float base, cudaStream_t strea
   ws->rope_base = base;
   *table = ws->rope;
   return ZEROS_OK;
+}
+
+// Rotary angle table of the d = 64 walk for N tokens and the given base, built on `stream`.
+int walk_angles(DeviceWorkspace* ws, int N, float base, cudaStream_t stream, const float** tab) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (ws->wang && ws->wang_base == base && ws->wang_N >= N) {
+    *tab = ws->wang;
+    return ZEROS_OK;
+  }
+  const size_t need = walk_angle_floats(N);
+  if (ws->wang) {
+    // Work already queued (on any stream) may still read the current table.
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  }
+  if (need > ws->wang_floats) {
+    if (ws->wang) cudaFree(ws->wang);
+    ws->wang = nullptr;
+    ws->wang_floats = 0;
+    cudaError_t e = cudaMalloc(&ws->wang, need * sizeof(float));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(walk angle table)");
+    ws->wang_floats = need;
+  }
+  cudaError_t e = launch_walk_angles(ws->wang, N, (double)base, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "walk angle table launch");
+  ws->wang_N = N;
+  ws->wang_base = base;
+  *tab = ws->wang;
+  return ZEROS_OK;
+}
+
+// Upper bound on the segments per sequence of the d = 64 walk: ZEROS_MAX_SEGMENTS (1 to 4)
+// when set, else 4.
+int walk_max_segments() {
+  const char* env = getenv("ZEROS_MAX_SEGMENTS");
+  if (!env) return 4;
+  const int v = atoi(env);
+  return v < 1 ? 1 : (v > 4 ? 4 : v);
 }
 
 // Backward scratch of at least `bytes`, grown on demand (after the device has drained: queued
@@ -323,16 +366,21 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
   a.ln_w = ln_w;
   a.ln_b = ln_b;
   a.ln_eps = ln_eps;
-  if (rope && !use_chunk) {  // the chunked kernel computes its rotary factors itself
+  if (rope && !use_chunk) {  // the chunked kernels compute their rotary factors themselves
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
-  if (use_chunk) {  // the scalar pass, then the chunk kernel
+  if (use_chunk) {  // the scalar pass, then the chunked kernel
+    const bool walk = walk_supported(d, dtype, causal);
+    const float* ang = nullptr;
+    if (walk && rope) {
+      if (int rc = walk_angles(ws, N, rope_base, st, &ang)) return rc;
+    }
     void* buf = nullptr;
     if (int rc = fwd_scratch(ws, (size_t)B * H * N * sizeof(float4), &buf)) return rc;
     a.scal = static_cast<float4*>(buf);
     cudaError_t e = launch_fwd_scalars(a, a.scal, st);
     if (e != cudaSuccess) return cuda_fail(e, "forward scalar launch");
-    e = launch_fwd_chunk(a, st);
+    e = walk ? launch_fwd_walk(a, ang, walk_max_segments(), st) : launch_fwd_chunk(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return ZEROS_OK;
   }

@@ -87,6 +87,16 @@ cudaError_t noalloc_rope_table(float2** table);
 bool chunk_supported(int d, int dtype, int causal);
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);
 
+// zs_walk.cu: the causal forward for d = 64 (bf16): one CTA per (sequence, segment), all 64
+// value columns of a head in one CTA.  a.scal must hold the per-token scalars; with rope, `ang`
+// holds walk_angle_floats(N) floats written by launch_walk_angles.  nseg_max bounds the number
+// of segments per sequence.
+bool walk_supported(int d, int dtype, int causal);
+size_t walk_angle_floats(int N);
+cudaError_t launch_walk_angles(float* tab, int N, double base, cudaStream_t stream);
+cudaError_t launch_fwd_walk(const FwdArgs& a, const float* ang, int nseg_max,
+                            cudaStream_t stream);
+
 // zs_scalars.cu: per-token (s, m, Et, P) of every sequence into scal ([B*H, N] float4), the
 // debug scalars and the scalar part of the final state when asked for (d in {64, 128}).
 cudaError_t launch_fwd_scalars(const FwdArgs& a, float4* scal, cudaStream_t stream);
