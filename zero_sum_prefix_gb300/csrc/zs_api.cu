@@ -376,8 +376,11 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
       if (int rc = walk_angles(ws, N, rope_base, st, &ang)) return rc;
     }
     void* buf = nullptr;
-    if (int rc = fwd_scratch(ws, (size_t)B * H * N * sizeof(float4), &buf)) return rc;
+    const size_t scal_bytes = (size_t)B * H * N * sizeof(float4);
+    const size_t smax_bytes = (size_t)B * H * kScalarCtas * sizeof(float);
+    if (int rc = fwd_scratch(ws, scal_bytes + smax_bytes, &buf)) return rc;
     a.scal = static_cast<float4*>(buf);
+    a.smax = reinterpret_cast<float*>(static_cast<char*>(buf) + scal_bytes);
     cudaError_t e = launch_fwd_scalars(a, a.scal, st);
     if (e != cudaSuccess) return cuda_fail(e, "forward scalar launch");
     e = walk ? launch_fwd_walk(a, ang, walk_max_segments(), st) : launch_fwd_chunk(a, st);

@@ -487,9 +487,9 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
-      mma_bf16(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
+      mma_f16kind(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
     }
-    mma_bf16(tW, d_rw, d_cw, id_qk, 0u);
+    mma_f16kind(tW, d_rw, d_cw, id_qk, 0u);
     mma_commit(&ms->a_full);
     mma_commit(&ms->w_done);
     // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
@@ -499,7 +499,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       const uint64_t off = (uint64_t)((kk * 2048) >> 4);
-      mma_bf16(tS, dv0 + sv + off, dkm0 + sq + off, id_st, (c > 0 || kk > 0) ? 1u : 0u);
+      mma_f16kind(tS, dv0 + sv + off, dkm0 + sq + off, id_st, (c > 0 || kk > 0) ? 1u : 0u);
     }
     mma_commit(&ms->st_done);
     // ---- X[:, 0:96] = Q [F~ | G | H] (state of the previous chunks, B tile rows 32..127) ----
@@ -509,7 +509,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
-        mma_bf16(tX, dq0 + sq + off, dsst + off, id_qs, kk > 0);
+        mma_f16kind(tX, dq0 + sq + off, dsst + off, id_qs, kk > 0);
       }
       mma_commit(&ms->sst_free);
       mma_commit(&ms->qk_empty[st]);  // Q, K and the coefficients of this chunk are not read again
@@ -520,7 +520,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
 #pragma unroll
     for (int kk = 0; kk < kC / 16; ++kk) {
       const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows per step
-      mma_bf16_ts(tX + 96, tm + CF::TM_S + kk * 8, dv0 + sv + boff, id_sv, kk > 0);
+      mma_f16kind_ts(tX + 96, tm + CF::TM_S + kk * 8, dv0 + sv + boff, id_sv, kk > 0);
     }
     mma_commit(&ms->x_full);
     if (c == 0) mma_commit(&ms->qk_empty[st]);  // no Q [F|G|H] product: after the S tile was read

@@ -516,9 +516,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
         const uint32_t off = kk * 2048;  // 16 token rows per step
         const uint32_t acc = (tt > 0 || kk > 0) ? 1u : 0u;
         const uint64_t bk = sw128_desc(base + SM::KQ + off, kAtom, 1024);
-        mma_bf16(tm, sw128_desc(base + SM::EVH + off, kAtom, 1024), bk, id_st, acc);
-        mma_bf16(tm, sw128_desc(base + SM::EVL + off, kAtom, 1024), bk, id_st, 1u);
-        mma_bf16(tm + 64, sw128_desc(base + SM::AV + off, kAtom, 1024), bk, id_st, acc);
+        mma_f16kind(tm, sw128_desc(base + SM::EVH + off, kAtom, 1024), bk, id_st, acc);
+        mma_f16kind(tm, sw128_desc(base + SM::EVL + off, kAtom, 1024), bk, id_st, 1u);
+        mma_f16kind(tm + 64, sw128_desc(base + SM::AV + off, kAtom, 1024), bk, id_st, acc);
       }
       mma_commit(bar);
     }
@@ -571,8 +571,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = kk * 32;  // 16 K values = 32 bytes inside the swizzled row
         const uint64_t aq = sw128_desc(base + SM::KQ + off, 16, 1024);
-        mma_bf16(tm, aq, sw128_desc(base + SM::BHI + off, 16, 1024), id_out, kk > 0 ? 1u : 0u);
-        mma_bf16(tm, aq, sw128_desc(base + SM::BLO + off, 16, 1024), id_out, 1u);
+        mma_f16kind(tm, aq, sw128_desc(base + SM::BHI + off, 16, 1024), id_out, kk > 0 ? 1u : 0u);
+        mma_f16kind(tm, aq, sw128_desc(base + SM::BLO + off, 16, 1024), id_out, 1u);
       }
       mma_commit(bar);
     }

@@ -26,6 +26,8 @@ struct FwdArgs {
   // chunked path: per-token (s, m, Et, P) of the blocked contract, [B*H, N], written by
   // launch_fwd_scalars before the chunk kernel reads it
   float4* scal;
+  // nullable: per sequence and scalar-pass CTA, the largest |s| of its tokens, [B*H, 8]
+  float* smax;
 };
 
 struct DecodeArgs {
@@ -98,7 +100,9 @@ cudaError_t launch_fwd_walk(const FwdArgs& a, const float* ang, int nseg_max,
                             cudaStream_t stream);
 
 // zs_scalars.cu: per-token (s, m, Et, P) of every sequence into scal ([B*H, N] float4), the
-// debug scalars and the scalar part of the final state when asked for (d in {64, 128}).
+// largest |s| per sequence and CTA into a.smax when given ([B*H, kScalarCtas]), the debug
+// scalars and the scalar part of the final state when asked for (d in {64, 128}).
+constexpr int kScalarCtas = 8;
 cudaError_t launch_fwd_scalars(const FwdArgs& a, float4* scal, cudaStream_t stream);
 
 // zs_backward.cu

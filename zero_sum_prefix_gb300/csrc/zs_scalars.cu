@@ -41,7 +41,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kScCN = 8;  // CTAs per sequence (one cluster)
+constexpr int kScCN = kScalarCtas;  // CTAs per sequence (one cluster)
 constexpr int kScW = 8;   // warps per CTA
 
 // Blocks per warp and per segment: two at d = 64 (a 4096-token sequence is one segment).
@@ -76,6 +76,7 @@ struct ScSmem {
   float4 fold[SH::SEG];      // per block: the fold's two exponential terms, LP and mC before it
   float4 chain[kScW][32];    // per warp: (s, e^{ml_{j-1} - ml_j}, e^{s - ml_j}, -) of token j
   float4 loc[SH::CB][32];    // per token of this CTA's blocks: (s, ml, El, LP), block-local
+  int smax_bits;             // largest |s| of this CTA's tokens (bits of a non-negative float)
 };
 
 // Lane's R = D / 32 columns of token row j (bf16 pairs as float2), zero past the sequence.
@@ -123,6 +124,8 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
 #pragma unroll
   for (int x = 0; x < RP; ++x) Cseg[x] = make_float2(0.0f, 0.0f);
   BlockCarry kseg{-INFINITY, 0.0f, 0.0f};
+  float amax = 0.0f;  // largest |s| of this thread's tokens
+  if (threadIdx.x == 0) sm.smax_bits = 0;
 
   for (int sg = 0; sg < nseg; ++sg) {
     // this warp's blocks: segment blocks gi0 .. gi0 + BW - 1
@@ -238,6 +241,7 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
       const float den = __fmul_rn(__fadd_rn(etau, (float)(i + 1)), sqrtd);
       const float s = -__fdiv_rn(pp[0], den);
       if (valid && !isfinite(s)) report(a.status, kErrRange);
+      if (valid) amax = fmaxf(amax, fabsf(s));
       float ml = valid ? s : -INFINITY;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -359,6 +363,14 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
         }
       }
     }
+  }
+  // the CTA's largest |s| (non-negative floats order like their bit patterns)
+  if (a.smax) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) atomicMax(&sm.smax_bits, __float_as_int(amax));
+    __syncthreads();
+    if (threadIdx.x == 0) a.smax[(size_t)bh * kScCN + rank] = __int_as_float(sm.smax_bits);
   }
   // (no remote access follows the last cluster barrier)
 }

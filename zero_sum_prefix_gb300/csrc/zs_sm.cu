@@ -140,7 +140,7 @@ __device__ void sm_mma(const SmArgs& a, uint8_t* smem, SmMisc* ms, int J) {
     const uint32_t tw = tm + (b ? CF::TM_W1 : CF::TM_W0);
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-      mma_bf16_ts(tm + CF::TM_O, tw + kk * 8, sw128_desc(vt + kk * 2048, kAtom, 1024), id_ov,
+      mma_f16kind_ts(tm + CF::TM_O, tw + kk * 8, sw128_desc(vt + kk * 2048, kAtom, 1024), id_ov,
                   (j > 0 || kk > 0) ? 1u : 0u);
     mma_commit(&ms->w_free[b]);
     mma_commit(&ms->kv_empty[g % CF::NS]);
@@ -158,7 +158,7 @@ __device__ void sm_mma(const SmArgs& a, uint8_t* smem, SmMisc* ms, int J) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk / 4) * kAtom + (kk % 4) * 32;
-      mma_bf16(ts, sw128_desc(qs + off, 16, 1024), sw128_desc(ks + off, 16, 1024), id_qk,
+      mma_f16kind(ts, sw128_desc(qs + off, 16, 1024), sw128_desc(ks + off, 16, 1024), id_qk,
                kk > 0 ? 1u : 0u);
     }
     mma_commit(&ms->s_full[b]);

@@ -263,8 +263,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] = (accumulate ? D : 0) + A * B, A and B bf16 from shared memory, D fp32.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] = (accumulate ? D : 0) + A * B, A and B 16-bit from shared memory (both bf16 or both
+// fp16, as the instruction descriptor says), D fp32.
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -273,10 +274,10 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// D[tmem] = (accumulate ? D : 0) + A * B with A (bf16, K-major) in tensor memory: lane m holds
+// D[tmem] = (accumulate ? D : 0) + A * B with A (16-bit, K-major) in tensor memory: lane m holds
 // row m, each 32-bit column two consecutive K elements (the lower K index in the low half);
-// B bf16 from shared memory, D fp32.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// B from shared memory, of A's type; D fp32.
+__device__ __forceinline__ void mma_f16kind_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -476,6 +477,14 @@ __device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
   return smem_desc(saddr, 16, 256, 6u);
 }
 
+// Instruction descriptor of kind::f16 with fp16 A/B (A and B share one type) and fp32
+// accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
+                                                    bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                      bool b_mn_major) {
@@ -504,6 +513,12 @@ __device__ __forceinline__ uint32_t sw32_off(int r, int c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
@@ -586,6 +601,21 @@ __device__ __forceinline__ void sts128f(uint32_t saddr, float4 v) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "f"(v.x), "f"(v.y),
                "f"(v.z), "f"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void sts32f(uint32_t saddr, float x) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(x) : "memory");
+}
+
+// Issue a load of 8 consecutive 32-bit columns of this thread's TMEM lane without waiting
+// (same rule as tmem_ld16_nowait).
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
 }
 
 // Programmatic dependent launch: a grid launched with the programmatic-serialization attribute

@@ -7,17 +7,27 @@
 // (E, P, F, G, H) give o_t = q_hat_t (alpha_t F_t + beta_t G_t + gamma_t H_t).
 //
 // Chunked form (chunks of C = 128 tokens).  With the chunk reference M_c (the running maximum of
-// s at the chunk's last token), Q = unit(rot(q)) and K = unit(rot(k)) in bf16, the row
-// coefficients (a, b, g)_t = (sigh_t e^{M_c - m_t} / Et_t, beta_t, gamma_t) and the column
-// scalars (e_i, s_i) = (e^{s_i - M_c}, s_i):
+// s at the chunk's last token), Q = unit(rot(q)) and K = unit(rot(k)), the row coefficients
+// (a, b, g)_t = (sigh_t e^{M_c - m_t} / Et_t, beta_t, gamma_t) and the column scalars
+// (e_i, s_i) = (e^{s_i - M_c}, s_i):
 //     W_{t,i} = a_t e_i + b_t s_i + g_t                (fp32 on the CUDA cores)
-//     S_{t,i} = [i <= t] (Q_t . K_i) W_{t,i}           (fp32 product, rounded once to bf16)
-//     X = Q [F~ | G | H]  (state before the chunk, bf16 copy),   X_SV = S V
+//     S_{t,i} = [i <= t] (Q_t . K_i) W_{t,i}           (fp32 product, rounded once to fp16)
+//     X = Q [F~ | G | H]  (state before the chunk, fp16 copy),   X_SV = S V
 //     o_t = X_SV + a_t X_F + b_t X_G + g_t X_H
 //     state^T += [e v | s v]^T K  and  [v | e v]^T K    (F~ rescaled by e^{M_{c-1} - M_c} first)
 // The weight is formed in fp32 before the product is rounded: its three terms nearly cancel
 // (the weights of a query sum to zero).  The scalars s, m, Et = E e^{-m}, P of every token come
 // from the scalar pass (zs_scalars.cu, the canonical blocked fp32 order), which runs first.
+//
+// Operand precision.  Every tensor-core operand is fp16 (fp32 accumulation): the unit vectors,
+// S and the value-side tiles have 11 significant bits instead of bf16's 8, which is what the
+// error of short sequences is made of.  The range is kept by exact powers of two folded into
+// the fp32 coefficients: row t of S carries 2^kr_t (|S| < 1), the state copy feeding chunk c
+// carries 2^-kb_c (2^kb_c > 128 c, the number of tokens it sums), and G is carried with
+// s 2^-ks (|s 2^-ks| < 1 over the sequence, from the scalar pass).  The copy's F~ is kept at the
+// running maximum before the chunk (its largest factor e^{s - m} is then 1, away from fp16's
+// subnormals), the output coefficient of X_F taking the chunk's e^{m - M_c}.  Values must lie
+// within the fp16 range (|v| <= 65504, reported otherwise).
 //
 // Split along the sequence.  When the sequences are fewer than the SMs, each is cut into
 // segments; the CTA of a later segment first replays the state side of the chunks before its
@@ -26,19 +36,19 @@
 // waits for another, and the replay costs a fraction of a full chunk (no queries, no intra-chunk
 // products, no outputs), so the segment lengths are chosen geometric to equalise the CTAs.
 //
-// Warp roles (576 threads, one CTA per SM):
+// Warp roles (576 threads, one CTA per SM; 448 with the fused LayerNorm):
 //   warps 0-7   (O) : operands; token row r = 16 w + lane / 2, half hf = lane & 1 of the row's
 //                     rotary pairs: norms (halves exchanged by a shuffle), rotation and unit
 //                     scaling of q and k in place (TMA-landed tiles), column scalars (hf = 0),
-//                     row coefficients (hf = 1), half of the row's scaled value tiles.
-//   warps 8-11  (E) : TMEM lane quadrant w & 3: S tile from Q K^T; output rows from X (staged in
-//                     shared memory, one TMA store per chunk); fused LayerNorm when asked for.
-//   warps 12-15 (S) : state copy: after each state update, the state in TMEM -> bf16 B tile of
-//                     the next chunk's Q [F~|G|H] product (and the F~ rescale in TMEM); the
-//                     final state (prefill).
-//   warp 16     (M) : TMEM allocation; one thread issues every tcgen05.mma.
-//   warp 17     (T) : TMA producer of q, k, v (two stages), with L2 prefetch ahead.
-// TMEM (512 columns): [0,128) Q K^T (the bf16 S tile overlays [0,64)), [128,320) X = Q[F~|G|H],
+//                     row coefficients (hf = 1), half of the row's value-side tiles.
+//   warps 8-15  (E) : two per TMEM lane quadrant (one with the LayerNorm, which needs whole
+//                     rows): S tile from Q K^T, the state copy after each update (TMEM -> fp16
+//                     B tile of the next chunk's Q [F~|G|H] product, and the F~ rescale in
+//                     TMEM), output rows from X (staged in shared memory, one TMA store per
+//                     chunk), the final state (prefill).
+//   next warp   (M) : TMEM allocation; one thread issues every tcgen05.mma.
+//   last warp   (T) : TMA producer of q, k, v (three stages), with L2 prefetch ahead.
+// TMEM (512 columns): [0,128) Q K^T (the fp16 S tile overlays it: K step h in [16 h, 16 h + 8)), [128,320) X = Q[F~|G|H],
 // [320,384) X_SV, [384,448) state A = [F~^T ; G^T], [448,512) state B = [H^T ; F~^T].
 // The state B accumulator repeats F~^T in its upper lanes so that every copy warp reads 96
 // columns: quadrants 0/1 take F~ columns 0-31 from A and H from B, quadrants 2/3 G from A and
@@ -61,7 +71,7 @@ using namespace sm100;
 
 constexpr int kC = 128;                 // tokens per chunk
 constexpr int kD = 64;                  // head dimension
-constexpr uint32_t kTile = 128 * 128;   // one bf16 [128 x 64] atom tile (128 rows of 128 bytes)
+constexpr uint32_t kTile = 128 * 128;   // one 16-bit [128 x 64] atom tile (128 rows of 128 bytes)
 constexpr int kNST = 3;                 // q/k/v stages
 constexpr int kOpWarps = 8;
 constexpr int kEpWarp0 = 8;             // from warp 8: S tiles, state copies, outputs
@@ -80,7 +90,8 @@ struct WLay {
   static constexpr uint32_t SB = VSC + 2 * kTile;         // state B tile: 192 rows x 128 bytes
   static constexpr uint32_t OUTS = SB + 192 * 128;        // output staging, [128 x 64] bf16
   static constexpr uint32_t COL = OUTS + kTile;           // float2 [stage][128]: (e_i, s_i)
-  static constexpr uint32_t COEF = COL + kNST * kC * 8;   // float4 [stage][128]: (a, b, g, -)
+  static constexpr uint32_t COEF = COL + kNST * kC * 8;   // float4 [stage][128], the row scales:
+                                                          // (a, b 2^(kb+ks), g 2^kb, 2^kr)
   static constexpr uint32_t LNW = COEF + kNST * kC * 16;  // float [2][64]: LayerNorm gain, bias
   static constexpr uint32_t THETA = LNW + 2 * kD * 4;     // float [32]: rotary frequencies
   static constexpr uint32_t PHI = THETA + 128;            // float [stage][32]: chunk base angles
@@ -138,6 +149,30 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Running maximum at the last token of chunk c (the chunk reference M_c).
 __device__ __forceinline__ float chunk_ref(const float4* scal, int c, int N) {
   return scal[min(N, (c + 1) * kC) - 1].y;
+}
+
+// The fp16 operands are kept in range by exact powers of two, folded into the fp32
+// coefficients: 2^k for |k| < 127.
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
+// The exponent e with x < 2^e (x > 0), 0 for x <= 0.
+__device__ __forceinline__ int exp_above(float x) {
+  int e = 0;
+  if (x > 0.0f) frexpf(x, &e);
+  return e;
+}
+// Scale exponent of the state copy that feeds chunk c's Q [F~|G|H] product: the state holds
+// the c * 128 tokens before the chunk, each entry at most that many times max|v| (the unit
+// keys and the factors e^{s - M} are at most 1; G is carried with s scaled to |s| < 1).
+__device__ __forceinline__ int state_exp(int c) { return c > 0 ? exp_above((float)(c * kC)) : 0; }
+// Scale exponent of s in the G products: s 2^-ks has |s 2^-ks| < 1 (from the scalar pass's
+// largest |s| of each of its CTAs).
+__device__ __forceinline__ int s_exp(const FwdArgs& a, int bh) {
+  float m = 0.0f;
+  if (a.smax) {
+#pragma unroll
+    for (int r = 0; r < kScalarCtas; ++r) m = fmaxf(m, a.smax[(size_t)bh * kScalarCtas + r]);
+  }
+  return max(0, exp_above(m));
 }
 
 // ============================================================================ T: TMA producer
@@ -201,8 +236,9 @@ struct RowIn {  // per-token inputs of a row, loaded one chunk ahead
   float x1, xh, x0;
 };
 
-// Rotate (RoPE) and scale one group of 8 rotary pairs: pair (xa, xb) ->
-// f (xa cos - xb sin, xa sin + xb cos); cs[k] = (cos, sin) of the pair's angle.
+// Rotate (RoPE) and scale one group of 8 rotary pairs of bf16 inputs: pair (xa, xb) ->
+// f (xa cos - xb sin, xa sin + xb cos), written as fp16 (unit vectors: in range, and eight times
+// finer than bf16); cs[k] = (cos, sin) of the pair's angle.
 __device__ __forceinline__ void rot_group(uint4& wa, uint4& wb, const float2 (&cs)[8], float f,
                                           bool rope) {
   const uint32_t ia[4] = {wa.x, wa.y, wa.z, wa.w}, ib[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -223,8 +259,8 @@ __device__ __forceinline__ void rot_group(uint4& wa, uint4& wb, const float2 (&c
       na = __fmul2_rn(xa, f2);
       nb = __fmul2_rn(xb, f2);
     }
-    oa[k] = pack_bf16x2(na.x, na.y);
-    ob[k] = pack_bf16x2(nb.x, nb.y);
+    oa[k] = pack_f16x2(na.x, na.y);
+    ob[k] = pack_f16x2(nb.x, nb.y);
   }
   wa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
   wb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
@@ -259,6 +295,14 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
   // rotary frequencies of this half's 16 pairs (pairs 16 hf .. 16 hf + 15), in shared memory
   const uint32_t th_s = base + WLay::THETA + 64 * hf;
   const float M_ref = c0 > 0 ? scal[c0 * kC - 1].y : 0.0f;  // replay reference
+  const int ks = min(100, s_exp(a, bh));
+  const float sinv = pow2f(-ks);
+  float smax_seq = 0.0f;  // the sequence's largest |s| (bounds the weights of a row)
+  if (a.smax) {
+#pragma unroll
+    for (int rr = 0; rr < kScalarCtas; ++rr)
+      smax_seq = fmaxf(smax_seq, a.smax[(size_t)bh * kScalarCtas + rr]);
+  }
 
   auto load_in = [&](int cc) {
     RowIn o{make_float4(0.f, 0.f, 0.f, 0.f), 0.0f, 0.0f, 0.0f, -INFINITY};
@@ -357,18 +401,25 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
       if (hf == 0) {
         sts64f(base + WLay::COL + (st * kC + r) * 8, ce, cs1);
       } else {
-        float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+        // a as the S tile uses it (reference M_c), (b, g) scaled by 2^kb (the state copy's
+        // scale) and b also by 2^ks (G is carried with s 2^-ks), and the row's S scale 2^kr with
+        // |S| 2^kr < 1: |W| <= |a| + |b| max|s| + |g|
+        float4 cf = make_float4(0.f, 0.f, 0.f, 1.f);
         if (valid) {
           const float m = cur.sc.y, Et = cur.sc.z, P = cur.sc.w;
           const float sig1 = __fdividef(1.0f, 1.0f + __expf(-cur.x1));
           const float sigh = __fdividef(1.0f, 1.0f + __expf(-cur.xh));
           const float rt = __fdividef(1.0f, (float)(i + 1));
           const float bc = (sig1 - sigh) * rt;
-          cf.x = __fdividef(sigh, Et) * __expf(M - m);
-          cf.y = bc;
-          cf.z = -(bc * P * rt + sigh * rt);
-          if (a.g0) cf.z += __fdividef(1.0f, 1.0f + __expf(-cur.x0)) * rt;  // zero-order gate
-          if (!isfinite(cf.x)) report(a.status, kErrRange);
+          float ca = __fdividef(sigh, Et) * __expf(M - m);
+          float cg = -(bc * P * rt + sigh * rt);
+          if (a.g0) cg += __fdividef(1.0f, 1.0f + __expf(-cur.x0)) * rt;  // zero-order gate
+          if (!isfinite(ca)) report(a.status, kErrRange);
+          // a e_i over the row's keys i <= t is at most sigma^h / E~ (e^{s_i - m_t} <= 1)
+          const int kb = state_exp(c);
+          const int kr = min(60, max(-60, -exp_above(__fdividef(sigh, Et) + fabsf(bc) * smax_seq +
+                                                       fabsf(cg))));
+          cf = make_float4(ca, bc * pow2f(kb + ks), cg * pow2f(kb), pow2f(kr));
         }
         sts128f(base + WLay::COEF + (st * kC + r) * 16, cf);
       }
@@ -380,24 +431,31 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
       return;
     }
     {
-      const float2 e2 = make_float2(ce, ce), s2 = make_float2(cs1, cs1);
+      // the value tile becomes fp16 in place (exact for bf16 values within the fp16 range;
+      // larger ones are reported), with e v and (s 2^-ks) v beside it
+      const float2 e2 = make_float2(ce, ce), s2 = make_float2(cs1 * sinv, cs1 * sinv);
+      float vmax = 0.0f;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = sw128_off(r, 4 * hf + s);
         const uint4 wv = lds128(vt + off);
         const uint32_t pv[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t pe[4], ps[4];
+        uint32_t ph[4], pe[4], ps[4];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
           float2 v2;
           unpack_bf16x2(pv[y], v2.x, v2.y);
+          vmax = fmaxf(vmax, fmaxf(fabsf(v2.x), fabsf(v2.y)));
           const float2 ev = __fmul2_rn(e2, v2), sv = __fmul2_rn(s2, v2);
-          pe[y] = pack_bf16x2(ev.x, ev.y);
-          ps[y] = pack_bf16x2(sv.x, sv.y);
+          ph[y] = pack_f16x2(v2.x, v2.y);
+          pe[y] = pack_f16x2(ev.x, ev.y);
+          ps[y] = pack_f16x2(sv.x, sv.y);
         }
+        sts128(vt + off, make_uint4(ph[0], ph[1], ph[2], ph[3]));
         sts128(vs + off, make_uint4(pe[0], pe[1], pe[2], pe[3]));
         sts128(vs + kTile + off, make_uint4(ps[0], ps[1], ps[2], ps[3]));
       }
+      if (!(vmax <= 65504.0f)) report(a.status, kErrRange);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -420,10 +478,10 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const long long lim = p.wait_limit;
-  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-  constexpr uint32_t id_x = idesc_bf16_f32(128, 192, false, false);
-  constexpr uint32_t id_u = idesc_bf16_f32(128, kD, true, true);
-  constexpr uint32_t id_sv = idesc_bf16_f32(128, kD, false, true);
+  constexpr uint32_t id_qk = idesc_f16_f32(128, 128, false, false);
+  constexpr uint32_t id_x = idesc_f16_f32(128, 192, false, false);
+  constexpr uint32_t id_u = idesc_f16_f32(128, kD, true, true);
+  constexpr uint32_t id_sv = idesc_f16_f32(128, kD, false, true);
   // descriptors: the start address field is address / 16, and every tile lies below 256 KB,
   // so the descriptor of base + off is the base's descriptor + off / 16
   const uint64_t dq = sw128_desc(base + WLay::Q, 16, 1024);
@@ -445,7 +503,7 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint64_t off = (uint64_t)((kk * 32) >> 4);
-        mma_bf16(tm + TM_A, dq + so + off, dk + so + off, id_qk, kk > 0);
+        mma_f16kind(tm + TM_A, dq + so + off, dk + so + off, id_qk, kk > 0);
       }
       mma_commit(&ms->a_full);
     }
@@ -465,8 +523,8 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
       for (int kk = 0; kk < kC / 16; ++kk) {
         const uint64_t off = (uint64_t)((kk * 2048) >> 4);
         const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-        mma_bf16(tm + TM_SA, dvsc + off, dkm + so + off, id_u, acc);
-        mma_bf16(tm + TM_SBS, dva + off, dkm + so + off, id_u, acc);
+        mma_f16kind(tm + TM_SA, dvsc + off, dkm + so + off, id_u, acc);
+        mma_f16kind(tm + TM_SBS, dva + off, dkm + so + off, id_u, acc);
       }
       mma_commit(&ms->vsc_free);
       if (c >= cfirst && c <= c1 - 2) mma_commit(&ms->u_done);
@@ -483,7 +541,7 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk * 32) >> 4);
-          mma_bf16(tm + TM_X, dq + so + off, dsb + off, id_x, kk > 0);
+          mma_f16kind(tm + TM_X, dq + so + off, dsb + off, id_x, kk > 0);
         }
         mma_commit(&ms->sb_free);
       } else if (wi >= 1 && !mbar_wait(&ms->x_free, (uint32_t)(wi - 1) & 1u, &ms->abort, lim)) {
@@ -496,7 +554,7 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
 #pragma unroll
       for (int kk = 0; kk < kC / 16; ++kk) {
         const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows per step
-        mma_bf16_ts(tm + TM_SV, tm + TM_A + kk * 8, dvb + so + boff, id_sv, kk > 0);
+        mma_f16kind_ts(tm + TM_SV, tm + TM_A + kk * 16, dvb + so + boff, id_sv, kk > 0);
       }
       mma_commit(&ms->x_full);
     }
@@ -515,7 +573,7 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
 // State copy: lane L of quadrant wq reads 96 state columns (three 32-column pieces):
 //   wq 0/1 (j = L):      A[0:32] = F~ row j cols 0-31,  B[0:32], B[32:64] = H row j
 //   wq 2/3 (j = L - 64): A[0:32], A[32:64] = G row j,   B[32:64] = F~ row j cols 32-63
-// and writes them as bf16 into the B tile rows (F~: j, G: 64 + j, H: 128 + j).
+// and writes them as fp16 into the B tile rows (F~: j, G: 64 + j, H: 128 + j).
 struct Piece {
   uint32_t col;  // TMEM column offset
   int row;       // B tile row
@@ -536,8 +594,10 @@ __device__ __forceinline__ Piece st_piece(int wq, int L, int k) {
   return Piece{TM_SBS + 32u, j, 4, true, 0, 32};
 }
 
-// The copy after the update of chunk c (copy index k = c - cfirst): F~ rescaled from its
-// reference M_cur to the next chunk's M_next (in TMEM too), bf16 B tile.  It first waits until
+// The copy after the update of chunk c (copy index k = c - cfirst): the fp16 B tile (times
+// 2^-kb) keeps F~ at its reference M_cur, the running maximum at the state's last token (so that
+// the largest of its factors e^{s - M_cur} is 1 and fp16 keeps its digits), while F~ in TMEM is
+// rescaled to the next chunk's reference M_next for the next update.  It first waits until
 // the Q [F~|G|H] product of chunk c has read the B tile; that product was issued right after
 // the update and the next update queues behind it on the tensor pipe, so the wait costs no
 // tensor time.  Returns false when a wait gave up.
@@ -547,6 +607,7 @@ __device__ __forceinline__ bool state_copy(WMisc* ms, uint32_t tm, uint32_t base
                                            float M_next, long long lim) {
   const bool resc = M_next > M_cur;
   const float fac = resc ? expf(M_cur - M_next) : 1.0f;
+  const float sc = pow2f(-state_exp(c + 1));  // fp16 range of the next chunk's B tile
   if (!mbar_wait_warp_lim(&ms->u_done, (uint32_t)k & 1u, &ms->abort, lim)) return false;
   if (c >= xfirst &&
       !mbar_wait_warp_lim(&ms->sb_free, (uint32_t)(c - xfirst) & 1u, &ms->abort, lim))
@@ -555,20 +616,20 @@ __device__ __forceinline__ bool state_copy(WMisc* ms, uint32_t tm, uint32_t base
   // each of the EPQ warps of the quadrant copies 32 / EPQ columns of every piece
   constexpr int W = 32 / EPQ;
   auto put = [&](const Piece& pc, uint32_t (&v)[W]) {
+#pragma unroll
+    for (int x = 0; x < W / 8; ++x) {
+      const uint32_t* w8 = v + 8 * x;
+      sts128(base + WLay::SB + sw128_off(pc.row, pc.ch0 + (W / 8) * hb + x),
+             make_uint4(pack_f16x2(__uint_as_float(w8[0]) * sc, __uint_as_float(w8[1]) * sc),
+                        pack_f16x2(__uint_as_float(w8[2]) * sc, __uint_as_float(w8[3]) * sc),
+                        pack_f16x2(__uint_as_float(w8[4]) * sc, __uint_as_float(w8[5]) * sc),
+                        pack_f16x2(__uint_as_float(w8[6]) * sc, __uint_as_float(w8[7]) * sc)));
+    }
     if (pc.f && resc) {
 #pragma unroll
       for (int y = 0; y < W; ++y) v[y] = __float_as_uint(__fmul_rn(__uint_as_float(v[y]), fac));
       if constexpr (EPQ == 1) tmem_st32_nowait(tm + pc.col, v);
       else tmem_st16_nowait(tm + pc.col + W * hb, v);
-    }
-#pragma unroll
-    for (int x = 0; x < W / 8; ++x) {
-      const uint32_t* w8 = v + 8 * x;
-      sts128(base + WLay::SB + sw128_off(pc.row, pc.ch0 + (W / 8) * hb + x),
-             make_uint4(pack_bf16x2(__uint_as_float(w8[0]), __uint_as_float(w8[1])),
-                        pack_bf16x2(__uint_as_float(w8[2]), __uint_as_float(w8[3])),
-                        pack_bf16x2(__uint_as_float(w8[4]), __uint_as_float(w8[5])),
-                        pack_bf16x2(__uint_as_float(w8[6]), __uint_as_float(w8[7]))));
     }
   };
   auto ld = [&](const Piece& pc, uint32_t (&v)[W]) {
@@ -616,6 +677,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
   const uint32_t lnw_s = base + WLay::LNW;
   const int N = a.N;
   const float4* scal = a.scal + (size_t)bh * N;
+  const float sinv = pow2f(-min(100, s_exp(a, bh)));  // G is carried with s 2^-ks
   const int cfirst = c0 > 0 ? c0 - 1 : 0;  // first update followed by a state copy
   const int xfirst = max(c0, 1);           // first chunk with a Q [F~|G|H] product
   // chunk references of the current and the next chunk, loaded one chunk ahead
@@ -641,12 +703,17 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     }
     tc_fence_after();
     // ---- S = [i <= t] (Q K^T) o W: 16-column pieces up to this warp's diagonal block, the
-    //      load of piece h + 1 in flight while piece h is formed; piece h goes to the packed
-    //      bf16 columns 8 h .. 8 h + 7 (already read as fp32 columns) ----
+    //      load of the next piece in flight while one is formed.  Piece h (tokens 16 h ..
+    //      16 h + 15, one K step of S V) is written packed to columns 16 h .. 16 h + 7, inside
+    //      the fp32 columns that the same thread has just read: the quadrant's E warps share
+    //      no column, so neither overwrites what the other still has to read ----
     {
       const int npiece = 2 * (wq + 1);
-      const float2 a2 = make_float2(cf.x, cf.x), b2 = make_float2(cf.y, cf.y);
-      const float2 g2 = make_float2(cf.z, cf.z);
+      // W 2^kr from the coefficients (which carry 2^kb, and b also 2^ks)
+      const float sw = cf.w * pow2f(-state_exp(c));
+      const float wa = cf.x * cf.w, wb = cf.y * sw * sinv, wg = cf.z * sw;
+      const float2 a2 = make_float2(wa, wa), b2 = make_float2(wb, wb);
+      const float2 g2 = make_float2(wg, wg);
       uint32_t ra[2][16];
       auto piece = [&](int h, const uint32_t (&rv)[16]) {
         uint32_t pw[8];
@@ -662,9 +729,9 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
             if (i0 > t) val.x = 0.0f;
             if (i0 + 1 > t) val.y = 0.0f;
           }
-          pw[y] = pack_bf16x2(val.x, val.y);
+          pw[y] = pack_f16x2(val.x, val.y);
         }
-        tmem_st8_nowait(tm + TM_A + 8 * h, pw);
+        tmem_st8_nowait(tm + TM_A + 16 * h, pw);
       };
       // this warp's pieces: h = hb, hb + EPQ, ... (the quadrant's E warps alternate)
       tmem_ld16_nowait(tm + TM_A + 16 * hb, ra[0]);
@@ -682,11 +749,11 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
           piece(h + EPQ, ra[1]);
         }
       }
-      uint32_t zw[16];
+      uint32_t zw[8];
 #pragma unroll
-      for (int y = 0; y < 16; ++y) zw[y] = 0u;
+      for (int y = 0; y < 8; ++y) zw[y] = 0u;
 #pragma unroll 1
-      for (int cb = wq + 1 + hb; cb < 4; cb += EPQ) tmem_st16_nowait(tm + TM_A + 16 * cb, zw);
+      for (int h = npiece + hb; h < kC / 16; h += EPQ) tmem_st8_nowait(tm + TM_A + 16 * h, zw);
       tmem_wait_st();
     }
     tc_fence_before();
@@ -704,6 +771,9 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     }
     tc_fence_after();
     const bool has_state = c > 0;
+    const float rinv = __frcp_rn(cf.w);  // S V carries the row's 2^kr
+    // the B tile's F~ is referenced to the running maximum before the chunk, and scaled by 2^-kb
+    const float xa = has_state ? cf.x * (expf(scal[c * kC - 1].y - Mc) * pow2f(state_exp(c))) : 0.0f;
     // outputs of columns 16 pc .. 16 pc + 15: two TMEM round trips of two matrices each
     auto out_piece = [&](int pc, float (&o)[16]) {
       uint32_t r0[16], r1[16];
@@ -715,7 +785,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
         reg_fence(r1);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          o[j] = __fmaf_rn(cf.x, __uint_as_float(r1[j]), __uint_as_float(r0[j]));
+          o[j] = __fmaf_rn(xa, __uint_as_float(r1[j]), __uint_as_float(r0[j]) * rinv);
         tmem_ld16_nowait(tm + TM_X + 64 + 16 * pc, r0);
         tmem_ld16_nowait(tm + TM_X + 128 + 16 * pc, r1);
         tmem_wait_ld();
@@ -727,7 +797,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
                            __fmaf_rn(cf.y, __uint_as_float(r0[j]), o[j]));
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r0[j]);
+        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r0[j]) * rinv;
       }
     };
     float ln_mean = 0.0f, ln_rstd = 1.0f;
@@ -820,6 +890,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     tc_fence_after();
     float* rec = record_ptr(a.final_state, bh, kD);
     const int j = wq < 2 ? t : t - 64;
+    const float gs = pow2f(min(100, s_exp(a, bh)));  // G was carried with s 2^-ks
     constexpr int W = 32 / EPQ;
 #pragma unroll 1
     for (int q = 0; q < 3; ++q) {
@@ -831,7 +902,8 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
       reg_fence(v);
       const int off = pc.rec == 0 ? rec_F(kD) : pc.rec == 1 ? rec_G(kD) : rec_H(kD);
 #pragma unroll
-      for (int y = 0; y < W; ++y) rec[off + (pc.a0 + W * hb + y) * kD + j] = __uint_as_float(v[y]);
+      for (int y = 0; y < W; ++y)
+        rec[off + (pc.a0 + W * hb + y) * kD + j] = __uint_as_float(v[y]) * (pc.rec == 1 ? gs : 1.0f);
     }
   }
 }
@@ -1041,7 +1113,7 @@ cudaError_t launch_walk_angles(float* tab, int N, double base, cudaStream_t stre
 
 cudaError_t launch_fwd_walk(const FwdArgs& a, const float* ang, int nseg_max,
                             cudaStream_t stream) {
-  if (!a.scal || (a.rope && !ang)) return cudaErrorInvalidValue;
+  if (!a.scal || !a.smax || (a.rope && !ang)) return cudaErrorInvalidValue;
   return a.ln ? launch_walk_t<true>(a, ang, nseg_max, stream)
               : launch_walk_t<false>(a, ang, nseg_max, stream);
 }
