@@ -522,6 +522,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// Running maximum of |x| over pairs of bf16 values (NaN propagates): acc' = max(acc, |w|) per
+// half.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(w & 0x7fff7fffu));
+  return r;
+}
+
 __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& lo, float& hi) {
   lo = __uint_as_float(w << 16);
   hi = __uint_as_float(w & 0xffff0000u);

@@ -154,11 +154,10 @@ __device__ __forceinline__ float chunk_ref(const float4* scal, int c, int N) {
 // The fp16 operands are kept in range by exact powers of two, folded into the fp32
 // coefficients: 2^k for |k| < 127.
 __device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
-// The exponent e with x < 2^e (x > 0), 0 for x <= 0.
+// An exponent e with x < 2^e for x > 0 (the binary exponent of x plus one: 2^(e-1) <= x for
+// normal x), 0 for x <= 0.
 __device__ __forceinline__ int exp_above(float x) {
-  int e = 0;
-  if (x > 0.0f) frexpf(x, &e);
-  return e;
+  return x > 0.0f ? (int)((__float_as_uint(x) >> 23) & 0xffu) - 126 : 0;
 }
 // Scale exponent of the state copy that feeds chunk c's Q [F~|G|H] product: the state holds
 // the c * 128 tokens before the chunk, each entry at most that many times max|v| (the unit
@@ -434,7 +433,7 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
       // the value tile becomes fp16 in place (exact for bf16 values within the fp16 range;
       // larger ones are reported), with e v and (s 2^-ks) v beside it
       const float2 e2 = make_float2(ce, ce), s2 = make_float2(cs1 * sinv, cs1 * sinv);
-      float vmax = 0.0f;
+      uint32_t vmax = 0u;  // largest |v| of the row's half, as bf16 pairs
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = sw128_off(r, 4 * hf + s);
@@ -445,7 +444,7 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
         for (int y = 0; y < 4; ++y) {
           float2 v2;
           unpack_bf16x2(pv[y], v2.x, v2.y);
-          vmax = fmaxf(vmax, fmaxf(fabsf(v2.x), fabsf(v2.y)));
+          vmax = bf16x2_absmax(vmax, pv[y]);
           const float2 ev = __fmul2_rn(e2, v2), sv = __fmul2_rn(s2, v2);
           ph[y] = pack_f16x2(v2.x, v2.y);
           pe[y] = pack_f16x2(ev.x, ev.y);
@@ -455,7 +454,8 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
         sts128(vs + off, make_uint4(pe[0], pe[1], pe[2], pe[3]));
         sts128(vs + kTile + off, make_uint4(ps[0], ps[1], ps[2], ps[3]));
       }
-      if (!(vmax <= 65504.0f)) report(a.status, kErrRange);
+      // bf16 values from 65536 up (and inf, NaN) are beyond the fp16 range
+      if ((vmax & 0xffffu) >= 0x4780u || (vmax >> 16) >= 0x4780u) report(a.status, kErrRange);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -573,7 +573,9 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
 // State copy: lane L of quadrant wq reads 96 state columns (three 32-column pieces):
 //   wq 0/1 (j = L):      A[0:32] = F~ row j cols 0-31,  B[0:32], B[32:64] = H row j
 //   wq 2/3 (j = L - 64): A[0:32], A[32:64] = G row j,   B[32:64] = F~ row j cols 32-63
-// and writes them as fp16 into the B tile rows (F~: j, G: 64 + j, H: 128 + j).
+// and writes them as fp16 into the B tile rows (F~: j, G: 64 + j, H: 128 + j).  (Giving
+// quadrants 2/3, whose S tiles are the largest, a smaller share of the copy measured slower:
+// the update after the copy waits for the slowest warp.)
 struct Piece {
   uint32_t col;  // TMEM column offset
   int row;       // B tile row
@@ -583,6 +585,7 @@ struct Piece {
   int a0;        // first key column
 };
 
+constexpr int kStPieces = 3;  // 32-column pieces of the state copied per lane
 __device__ __forceinline__ Piece st_piece(int wq, int L, int k) {
   const bool lo = wq < 2;
   const int j = lo ? L : L - 64;
@@ -616,18 +619,28 @@ __device__ __forceinline__ bool state_copy(WMisc* ms, uint32_t tm, uint32_t base
   // each of the EPQ warps of the quadrant copies 32 / EPQ columns of every piece
   constexpr int W = 32 / EPQ;
   auto put = [&](const Piece& pc, uint32_t (&v)[W]) {
+    const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
     for (int x = 0; x < W / 8; ++x) {
       const uint32_t* w8 = v + 8 * x;
+      uint32_t pk[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const float2 f = __fmul2_rn(make_float2(__uint_as_float(w8[2 * y]),
+                                                __uint_as_float(w8[2 * y + 1])), sc2);
+        pk[y] = pack_f16x2(f.x, f.y);
+      }
       sts128(base + WLay::SB + sw128_off(pc.row, pc.ch0 + (W / 8) * hb + x),
-             make_uint4(pack_f16x2(__uint_as_float(w8[0]) * sc, __uint_as_float(w8[1]) * sc),
-                        pack_f16x2(__uint_as_float(w8[2]) * sc, __uint_as_float(w8[3]) * sc),
-                        pack_f16x2(__uint_as_float(w8[4]) * sc, __uint_as_float(w8[5]) * sc),
-                        pack_f16x2(__uint_as_float(w8[6]) * sc, __uint_as_float(w8[7]) * sc)));
+             make_uint4(pk[0], pk[1], pk[2], pk[3]));
     }
     if (pc.f && resc) {
+      const float2 f2 = make_float2(fac, fac);
 #pragma unroll
-      for (int y = 0; y < W; ++y) v[y] = __float_as_uint(__fmul_rn(__uint_as_float(v[y]), fac));
+      for (int y = 0; y < W; y += 2) {
+        const float2 f = __fmul2_rn(make_float2(__uint_as_float(v[y]), __uint_as_float(v[y + 1])), f2);
+        v[y] = __float_as_uint(f.x);
+        v[y + 1] = __float_as_uint(f.y);
+      }
       if constexpr (EPQ == 1) tmem_st32_nowait(tm + pc.col, v);
       else tmem_st16_nowait(tm + pc.col + W * hb, v);
     }
@@ -683,10 +696,12 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
   // chunk references of the current and the next chunk, loaded one chunk ahead
   float Mc = chunk_ref(scal, c0, N);
   float Mn = c0 + 1 < c1 ? chunk_ref(scal, c0 + 1, N) : 0.0f;
+  // the running maximum at the token before the current chunk (the B tile's F~ reference)
+  float Mp = c0 > 0 ? scal[c0 * kC - 1].y : 0.0f;
   bool ok = true;
   // the copy after the last replayed update (reference: the running maximum before c0)
   if (c0 > 0)
-    ok = state_copy<EPQ>(ms, tm, base, wq, hb, t, c0 - 1, 0, xfirst, scal[c0 * kC - 1].y, Mc, lim);
+    ok = state_copy<EPQ>(ms, tm, base, wq, hb, t, c0 - 1, 0, xfirst, Mp, Mc, lim);
   for (int c = c0; c < c1 && ok; ++c) {
     const int st = c % kNST;
     const int wi = c - c0;
@@ -773,7 +788,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     const bool has_state = c > 0;
     const float rinv = __frcp_rn(cf.w);  // S V carries the row's 2^kr
     // the B tile's F~ is referenced to the running maximum before the chunk, and scaled by 2^-kb
-    const float xa = has_state ? cf.x * (expf(scal[c * kC - 1].y - Mc) * pow2f(state_exp(c))) : 0.0f;
+    const float xa = has_state ? cf.x * (expf(Mp - Mc) * pow2f(state_exp(c))) : 0.0f;
     // outputs of columns 16 pc .. 16 pc + 15: two TMEM round trips of two matrices each
     auto out_piece = [&](int pc, float (&o)[16]) {
       uint32_t r0[16], r1[16];
@@ -781,23 +796,39 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
       if (has_state) tmem_ld16_nowait(tm + TM_X + 16 * pc, r1);
       tmem_wait_ld();
       reg_fence(r0);
+      const float2 ri2 = make_float2(rinv, rinv);
+      auto f2 = [](const uint32_t (&r)[16], int j) {
+        return make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+      };
       if (has_state) {
         reg_fence(r1);
+        const float2 xa2 = make_float2(xa, xa);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          o[j] = __fmaf_rn(xa, __uint_as_float(r1[j]), __uint_as_float(r0[j]) * rinv);
+        for (int j = 0; j < 16; j += 2) {
+          const float2 y = __ffma2_rn(xa2, f2(r1, j), __fmul2_rn(f2(r0, j), ri2));
+          o[j] = y.x;
+          o[j + 1] = y.y;
+        }
         tmem_ld16_nowait(tm + TM_X + 64 + 16 * pc, r0);
         tmem_ld16_nowait(tm + TM_X + 128 + 16 * pc, r1);
         tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
+        const float2 yb2 = make_float2(cf.y, cf.y), yg2 = make_float2(cf.z, cf.z);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          o[j] = __fmaf_rn(cf.z, __uint_as_float(r1[j]),
-                           __fmaf_rn(cf.y, __uint_as_float(r0[j]), o[j]));
+        for (int j = 0; j < 16; j += 2) {
+          const float2 y = __ffma2_rn(yg2, f2(r1, j),
+                                      __ffma2_rn(yb2, f2(r0, j), make_float2(o[j], o[j + 1])));
+          o[j] = y.x;
+          o[j + 1] = y.y;
+        }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r0[j]) * rinv;
+        for (int j = 0; j < 16; j += 2) {
+          const float2 y = __fmul2_rn(f2(r0, j), ri2);
+          o[j] = y.x;
+          o[j + 1] = y.y;
+        }
       }
     };
     float ln_mean = 0.0f, ln_rstd = 1.0f;
@@ -872,6 +903,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
       }
     }
     ok = __all_sync(0xffffffffu, ok);
+    Mp = Mc;
     Mc = Mn;
     Mn = Mnn;
   }
@@ -893,7 +925,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     const float gs = pow2f(min(100, s_exp(a, bh)));  // G was carried with s 2^-ks
     constexpr int W = 32 / EPQ;
 #pragma unroll 1
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < kStPieces; ++q) {
       const Piece pc = st_piece(wq, t, q);
       uint32_t v[W];
       if constexpr (EPQ == 1) tmem_ld32_nowait(tm + pc.col, v);
@@ -1068,13 +1100,15 @@ cudaError_t launch_walk_t(const FwdArgs& a, const float* ang, int nseg_max, cuda
     return cudaErrorNotSupported;
   // segments per sequence: as many as the SMs allow (one CTA each), at most kMaxSeg and one
   // per chunk; segment j gets a share proportional to (1 - rho)^j, rho the cost of replaying
-  // a chunk's state side relative to walking it, so that every CTA does about the same work
+  // a chunk's state side relative to walking it (0.55 timed best at 64 sequences of 32 chunks,
+  // between 0.4 and 0.85: the replay is bound by the operand warps, which still rotate and scale
+  // every key), so that every CTA does about the same work
   const int nch = (a.N + kC - 1) / kC;
   const int nsm = sm_count(dev);
   int S = BH >= nsm ? 1 : nsm / BH;
   S = std::min(S, std::min(kMaxSeg, nseg_max));
   S = std::max(1, std::min(S, nch));
-  constexpr double rho = 0.4;
+  constexpr double rho = 0.55;
   double wsum = 0.0, wj = 1.0;
   for (int j = 0; j < S; ++j, wj *= 1.0 - rho) wsum += wj;
   p.nseg = S;
