@@ -1,8 +1,9 @@
 """ZeroS-SM (the zero-sum reweighting of standard softmax attention) on the tensor-core kernel
 vs the fp64 oracle (GPU only).
 
-Tolerance: the per-sequence metric of tests/test_gpu_parity.py (max error over max|o_ref|; a
-single-token sequence, whose exact output is 0, in absolute terms) at the bf16 bound 1e-2.  The
+Tolerance: the metric of tests/test_gpu_parity.py (max error over max|o_ref| of the compared
+outputs; single-token sequences, whose exact output is 0, in absolute terms) at the bf16 bound
+1e-2.  The
 kernel's error sources are the bf16 rounding of the weight tile W (once per weight, 2^-9
 relative, after the three nearly cancelling terms were summed in fp32), of the rotated q and k
 (rope), and of the output; products and sums are fp32.

@@ -1,5 +1,5 @@
 """Optional zero-order gate of a first layer (w_{t,i} gains sigmoid(g0_t)/t, encoder /N) on
-every CUDA path vs the fp64 oracle (GPU only).  Same per-sequence tolerance metric as
+every CUDA path vs the fp64 oracle (GPU only).  Same tolerance metric as
 tests/test_gpu_parity.py."""
 import numpy as np
 import pytest

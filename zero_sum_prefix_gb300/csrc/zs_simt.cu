@@ -145,8 +145,26 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
 #pragma unroll
       for (int r = 0; r < R; ++r) nfix[r] = __fmaf_rn(etau, mu[r], Su[r]);
       den_fix = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)D));
+      // the full-sequence scalars first: m_N, Et_N = E_N e^{-m_N}, P_N
+      for (int i = 0; i < N; ++i) {
+        float uu[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) uu[r] = ld(u, (size_t)i * D + R * lane + r);
+        const float si = fixed_logit<R>(uu, nfix, den_fix);
+        const float m_new = fmaxf(m_run, si);
+        Et_run = __fmaf_rn(Et_run, expf(__fsub_rn(m_run, m_new)), expf(__fsub_rn(si, m_new)));
+        P_run = __fadd_rn(P_run, si);
+        m_run = m_new;
+      }
     }
   }
+  // Encoder sums, centred: with t = N for every query the weight is
+  //   w_i = (sig1 - sigh) / N (s_i - P_N / N) + sigh (e^{s_i - m} - Et_N / N) / Et_N,
+  // so F and G are accumulated with the centred factors (e^{s_i - m_N} - Et_N / N) and
+  // (s_i - P_N / N).  The readout then adds two sums that do not cancel each other, instead of
+  // three full sums whose large parts cancel (which costs fp32 digits in proportion).
+  const float ebar = warp == 0 && !a.causal ? __fdiv_rn(Et_run, (float)N) : 0.0f;
+  const float sbar = warp == 0 && !a.causal ? __fdiv_rn(P_run, (float)N) : 0.0f;
 
   auto load_unit_row = [&](const T* src, int t, float* dst) {
     float x[R];
@@ -176,29 +194,27 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
       float uu[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) uu[r] = ld(u, (size_t)t * D + R * lane + r);
-      float f, g, s, Et, P, m;
+      float f, g, s, Et, P, m, s_raw;
       if (a.causal) {
         const TokenOut o = token_update<R>(uu, C, L, mu, etau, t + 1, sc);
         s = o.s;
+        s_raw = s;
         Et = o.Et;
         P = o.P;
         m = o.m;
         f = expf(__fsub_rn(o.m_prev, m));
         g = expf(__fsub_rn(s, m));
       } else {
-        s = fixed_logit<R>(uu, nfix, den_fix);
-        const float m_new = fmaxf(m_run, s);
-        f = expf(__fsub_rn(m_run, m_new));
-        g = expf(__fsub_rn(s, m_new));
-        Et_run = __fmaf_rn(Et_run, f, g);
-        P_run = __fadd_rn(P_run, s);
-        m_run = m_new;
+        s_raw = fixed_logit<R>(uu, nfix, den_fix);  // as in the pre-pass
+        s = __fsub_rn(s_raw, sbar);
+        f = 1.0f;
+        g = __fsub_rn(expf(__fsub_rn(s_raw, m_run)), ebar);
         Et = Et_run;
         P = P_run;
         m = m_run;
       }
       if (lane == 0) {
-        if (!isfinite(s)) report(a.status, kErrRange);
+        if (!isfinite(s_raw)) report(a.status, kErrRange);
         tc.s = s;
         tc.f = f;
         tc.g = g;
@@ -218,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
             if (a.dbg_m) a.dbg_m[row0 + t] = m;
           }
         } else if (blockIdx.y == 0 && a.dbg_s) {
-          a.dbg_s[row0 + t] = s;
+          a.dbg_s[row0 + t] = s_raw;
         }
       }
     } else if (warp == 1) {
@@ -304,11 +320,10 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdArgs a) {
     if (warp == 1) load_unit_row(q, t, qs);
     if (warp == 0 && lane == 0) {
       const float sig1 = sigmoid(g1[t]), sigh = sigmoid(gh[t]);
-      const float beta = __fmul_rn(__fsub_rn(sig1, sigh), rN);
       tc.alpha = __fdiv_rn(sigh, fullsc[0]);
-      tc.beta = beta;
-      tc.gamma = -__fadd_rn(__fmul_rn(__fmul_rn(beta, fullsc[1]), rN), __fmul_rn(sigh, rN));
-      if (a.g0) tc.gamma = __fadd_rn(tc.gamma, __fmul_rn(sigmoid(a.g0[row0 + t]), rN));
+      tc.beta = __fmul_rn(__fsub_rn(sig1, sigh), rN);
+      // the centred sums carry the -beta P / N and -sigh / N parts of gamma
+      tc.gamma = a.g0 ? __fmul_rn(sigmoid(a.g0[row0 + t]), rN) : 0.0f;
       if (blockIdx.y == 0) {
         if (a.dbg_E) a.dbg_E[row0 + t] = fullsc[0];
         if (a.dbg_P) a.dbg_P[row0 + t] = fullsc[1];
