@@ -20,10 +20,11 @@
 //   C. each warp forms its tokens' logits (same lane/tree order as the decode step), the
 //      block-local running max, scaled exp-sum and logit sum, and stores the block's end values
 //      into every CTA of the cluster;
-//   D. warp 0 folds the end values in block order (the same fold as the decode step), recording
-//      the scalar carry at the start of its own blocks: the maximum chain first (one max per
-//      block), then the exponentials of every block at once (one lane each), then the
-//      multiply-add and add chains, so that only one operation per block is sequential;
+//   D. the end values are folded in block order (the same fold as the decode step), recording
+//      the scalar carries at the start of every block: the maximum chain first (a prefix
+//      maximum across the lanes of warp 0), then the exponentials of every block at once, then
+//      the multiply-add and add chains (warps 0 and 1), so that only one operation per block
+//      is sequential;
 //   E. each token combines its block's carries with its local values: (s, m, Et, P).
 // Output: float4 (s, m, Et, P) per token, [B*H, N] (16 bytes per token); optionally the debug
 // scalars and the scalar part of the recurrent state after the last token (C, L, mu and the
@@ -72,8 +73,15 @@ struct ScSmem {
   float lend[SH::SEG][D];    // local column sums of every block of the segment (all CTAs write)
   float4 bend[SH::SEG];      // end values (LP, ml, El, -) of every block (all CTAs write)
   float cw[SH::CB][D];       // column carry at the start of each of this CTA's blocks
-  float4 kw[SH::CB];         // scalar carries (mC, EC, CP, -) at each of its blocks' start
-  float4 fold[SH::SEG];      // per block: the fold's two exponential terms, LP and mC before it
+  // per block of the segment: the fold's two exponential terms fx, fy and its LP (fz), and the
+  // carries (mC, EC, CP) at the block's start
+  __align__(16) float fx[SH::SEG];
+  __align__(16) float fy[SH::SEG];
+  __align__(16) float fz[SH::SEG];
+  __align__(16) float cm[SH::SEG];
+  __align__(16) float cEC[SH::SEG];
+  __align__(16) float cCP[SH::SEG];
+  float kseg[3];             // carries (mC, EC, CP) at the current segment's start
   float4 chain[kScW][32];    // per warp: (s, e^{ml_{j-1} - ml_j}, e^{s - ml_j}, -) of token j
   float4 loc[SH::CB][32];    // per token of this CTA's blocks: (s, ml, El, LP), block-local
   int smax_bits;             // largest |s| of this CTA's tokens (bits of a non-negative float)
@@ -123,9 +131,13 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
   float2 Cseg[RP];
 #pragma unroll
   for (int x = 0; x < RP; ++x) Cseg[x] = make_float2(0.0f, 0.0f);
-  BlockCarry kseg{-INFINITY, 0.0f, 0.0f};
   float amax = 0.0f;  // largest |s| of this thread's tokens
-  if (threadIdx.x == 0) sm.smax_bits = 0;
+  if (threadIdx.x == 0) {
+    sm.smax_bits = 0;
+    sm.kseg[0] = -INFINITY;  // scalar carries (mC, EC, CP) at the segment's start
+    sm.kseg[1] = 0.0f;
+    sm.kseg[2] = 0.0f;
+  }
 
   for (int sg = 0; sg < nseg; ++sg) {
     // this warp's blocks: segment blocks gi0 .. gi0 + BW - 1
@@ -272,51 +284,79 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
       sm.loc[w * BW + bb][lane] = make_float4(s, ml, El, LP);
     }
     cluster_sync_all();
-    // ---- D: scalar carries at the start of every block of the segment (block order): the
-    //      maximum chain, the exponentials of every block at once (one lane each), then the
-    //      multiply-add and add chains ----
+    // ---- D: scalar carries at the start of every block of the segment (block order).  The
+    //      maximum chain is an exact prefix maximum (lane l of warp 0 takes blocks Q l ..
+    //      Q l + Q - 1; a maximum is exact, so any grouping gives the chain's values), and the
+    //      exponentials of every block are formed at once.  The two remaining chains then run
+    //      in block order on two warps (two schedulers), each one FMA per block with its
+    //      operands read four blocks at a time ahead of the chain: EC = fma(EC, x, y) on warp 0,
+    //      CP + z on warp 1 ----
     if (w == 0) {
       constexpr int Q = SEG / 32;
-      float mb[Q], ma[Q];
-      float mrun = kseg.mC;
+      float pre[Q];
 #pragma unroll
-      for (int gb = 0; gb < SEG; ++gb) {
-        const float mn = fmaxf(mrun, sm.bend[gb].y);
-        if ((gb & 31) == lane) {
-          mb[gb >> 5] = mrun;
-          ma[gb >> 5] = mn;
-        }
-        mrun = mn;
+      for (int i = 0; i < Q; ++i) {
+        const float x = sm.bend[Q * lane + i].y;
+        pre[i] = i == 0 ? x : fmaxf(pre[i - 1], x);
       }
+      float incl = pre[Q - 1];
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
-        const int gb = 32 * q + lane;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = fmaxf(incl, y);
+      }
+      const float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      const float mC = sm.kseg[0];
+      const float base = lane == 0 ? mC : fmaxf(mC, excl);
+#pragma unroll
+      for (int i = 0; i < Q; ++i) {
+        const int gb = Q * lane + i;
+        const float mb = i == 0 ? base : fmaxf(base, pre[i - 1]);
+        const float ma = fmaxf(base, pre[i]);
         const float4 be = sm.bend[gb];
-        sm.fold[gb] = make_float4(expf(__fsub_rn(mb[q], ma[q])),
-                                  __fmul_rn(be.z, expf(__fsub_rn(be.y, ma[q]))), be.x, mb[q]);
+        sm.fx[gb] = expf(__fsub_rn(mb, ma));
+        sm.fy[gb] = __fmul_rn(be.z, expf(__fsub_rn(be.y, ma)));
+        sm.fz[gb] = be.x;
+        sm.cm[gb] = mb;
+      }
+      const float mrun = __shfl_sync(0xffffffffu, fmaxf(base, pre[Q - 1]), 31);
+      __syncwarp();
+      if (lane == 0) sm.kseg[0] = mrun;
+    }
+    __syncthreads();
+    if (w < 2) {
+      // every lane alike: broadcast loads, stores of one value
+      float acc = sm.kseg[1 + w];
+      const float* mul = sm.fx;
+      const float* add = w == 0 ? sm.fy : sm.fz;
+      float* out = w == 0 ? sm.cEC : sm.cCP;
+#pragma unroll
+      for (int g = 0; g < SEG; g += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(add + g);
+        float4 c;
+        if (w == 0) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mul + g);
+          c.x = acc; acc = __fmaf_rn(acc, m4.x, a4.x);
+          c.y = acc; acc = __fmaf_rn(acc, m4.y, a4.y);
+          c.z = acc; acc = __fmaf_rn(acc, m4.z, a4.z);
+          c.w = acc; acc = __fmaf_rn(acc, m4.w, a4.w);
+        } else {
+          c.x = acc; acc = __fadd_rn(acc, a4.x);
+          c.y = acc; acc = __fadd_rn(acc, a4.y);
+          c.z = acc; acc = __fadd_rn(acc, a4.z);
+          c.w = acc; acc = __fadd_rn(acc, a4.w);
+        }
+        *reinterpret_cast<float4*>(out + g) = c;
       }
       __syncwarp();
-      float EC = kseg.EC, CP = kseg.CP;
-#pragma unroll 1
-      for (int g0 = 0; g0 < SEG; g0 += 8) {
-        float4 f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = sm.fold[g0 + i];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int gb = g0 + i;
-          if (gb / CB == (int)rank && lane == 0) sm.kw[gb % CB] = make_float4(f[i].w, EC, CP, 0.0f);
-          EC = __fmaf_rn(EC, f[i].x, f[i].y);
-          CP = __fadd_rn(CP, f[i].z);
-        }
-      }
-      kseg = BlockCarry{mrun, EC, CP};
+      if (lane == 0) sm.kseg[1 + w] = acc;
     }
     __syncthreads();
     // ---- E: each token's scalars ----
 #pragma unroll 1
     for (int bb = 0; bb < BW; ++bb) {
-      const float4 kc = sm.kw[w * BW + bb];
+      // the block's carries (mC, EC, CP) at its start
+      const float4 kc = make_float4(sm.cm[gi0 + bb], sm.cEC[gi0 + bb], sm.cCP[gi0 + bb], 0.0f);
       const float4 lv = sm.loc[w * BW + bb][lane];
       const float s = lv.x, ml = lv.y, El = lv.z, LP = lv.w;
       const int i = b0[bb] + lane;
