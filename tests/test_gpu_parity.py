@@ -189,6 +189,37 @@ def test_decode_matches_forward_bitexact(zs, d, rope, dtype):
     assert (view["t"] == N0 + steps).all()
 
 
+def test_decode_after_long_prefill_d128(zs):
+    """The recurrent-decode workload's per-sequence shape: an 8192-token RoPE prefill at d = 128
+    on the chunked tensor-core path, then 64 decode steps.  Logits and prefix scalars of every
+    step equal those of a forward pass over all 8256 tokens bit for bit (every sequence); the
+    decode outputs of four seeded (b, h) sequences match the fp64 oracle over the whole
+    sequence."""
+    base = zi.DECODE_B256H32D128
+    steps = 64
+    w = base.with_(B=2, H=4)
+    N0 = w.N
+    pre = zi.make(w, "cuda")
+    st, outs, dbgs, toks = _decode_run(zs, w, pre, steps)
+    assert zs.get_status() == 0
+    full = {n: torch.cat([pre[n]] + [t[n].unsqueeze(2) for t in toks], dim=2)
+            for n in ("q", "k", "v", "u", "g1", "gh")}
+    full["mu"], full["tau"] = pre["mu"], pre["tau"]
+    wf = w.with_(N=N0 + steps)
+    _, dbg_full = run(zs, full, wf, debug=True)
+    assert zs.get_status() == 0
+    for key in ("s", "E", "P", "m"):
+        dec = torch.stack([dg[key] for dg in dbgs], dim=2)
+        fwd = dbg_full[key][:, :, N0:]
+        assert torch.equal(dec.view(torch.int32), fwd.contiguous().view(torch.int32)), key
+    heads = zi.sample_heads(w, 4)
+    ref = oracle_subset(full, wf, heads)[:, N0:]
+    dec_o = torch.stack(outs, dim=2)
+    assert seq_err(gpu_subset(dec_o, heads), ref) <= TOL["bf16"]
+    view = zs.state_view(st, w.B, w.H, w.d)
+    assert (view["t"] == N0 + steps).all()
+
+
 def test_decode_from_empty_state(zs):
     B, H, d, steps = 3, 2, 64, 24
     w = zi.Workload("dec0", B, H, steps, d, rope=True, seed=91)

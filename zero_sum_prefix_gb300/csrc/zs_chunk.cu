@@ -1,4 +1,5 @@
-// Chunked tensor-core causal forward of the ZeroS layer (bf16 inputs, fp32 accumulation).
+// Chunked tensor-core causal forward of the ZeroS layer (bf16 inputs, fp16 operands, fp32
+// accumulation).
 //
 // Method: Paper-Notes "ZeroS: Zero-Sum Linear Attention for Efficient Transformers", method
 // details: deviation logits, zero-sum weights w_{t,i} = sig1_t delta_{t,i}/t + sigh_t eps_{t,i},
@@ -7,21 +8,25 @@
 //
 // Chunked form used here (chunks of C = 128 tokens, value columns in slices of DV = 32):
 //   w_{t,i} = alpha_t e^{s_i} + beta_t s_i + gamma_t, so with the chunk reference M_c (the
-//   running maximum of s at the chunk's last token), Q = rot(q), K = rot(k) (bf16, unnormalised)
-//   and rho_t = 1/|q_t|, kappa_i = 1/|k_i|, row coefficients (a, b, g)_t = rho_t (alphâ_t,
-//   beta_t, gamma_t) with alphâ_t = sigh_t e^{M_c - m_t} / Et_t and column scalars
-//   (e, s', k)_i = (e^{s_i - M_c} kappa_i, s_i kappa_i, kappa_i):
+//   running maximum of s at the chunk's last token), Q = rot(q), K = rot(k) (fp16,
+//   unnormalised) and rho_t = 1/|q_t|, kappa_i = 1/|k_i|, row coefficients (a, b, g)_t =
+//   rho_t (alphâ_t, beta_t, gamma_t) with alphâ_t = sigh_t e^{M_c - m_t} / Et_t and column
+//   scalars (e, s', k)_i = (e^{s_i - M_c} kappa_i, s_i kappa_i, kappa_i):
 //     W_{t,i} = a_t e_i + b_t s'_i + g_t k_i        (tensor core, hi/lo bf16 split, fp32 sum)
-//     intra  S_{t,i} = [i <= t] (Q_t . K_i) W_{t,i} (fp32 product, rounded once to bf16)
-//     Vsc_i = [ v_i | e_i v_i | s'_i v_i | k_i v_i ]                          (C x 128, bf16)
-//     X[:, 0:96]   = Q [F~ | G | H]   (state of the previous chunks)
+//     intra  S_{t,i} = [i <= t] (Q_t . K_i) W_{t,i} (fp32 product, times 2^kr_t, then fp16)
+//     Vsc_i = [ v_i | e_i v_i | s'_i 2^-ks v_i | k_i v_i ]                    (C x 128, fp16)
+//     X[:, 0:96]   = Q [F~ | G | H]   (state of the previous chunks, fp16 copy times 2^-kb)
 //     X[:, 96:128] = S V
-//     o_t = a_t X_F + b_t X_G + g_t X_H + X_SV
+//     o_t = a'_t X_F + b'_t X_G + g'_t X_H + 2^-kr_t X_SV
 //     state^T (128 x d; rows [unused | F~ | G | H]) += Vsc^T K, F~ rescaled by
 //     e^{M_{c-1} - M_c} before each chunk's update.
+//   The output coefficients a', b', g' carry the copy's 2^kb (and b' G's 2^ks); the copy keeps
+//   F~ at the running maximum before the chunk, and a' takes e^{M_{c-1} - m_t} (power-of-two
+//   range scales: zs_range.cuh).  q, k and v must lie within the fp16 range once rotated
+//   (|x| < 45056 for q and k, |v| <= 65504), which is reported otherwise.
 //   The weight is formed to fp32 accuracy before the product is rounded: the three terms of w
-//   nearly cancel (the weights sum to zero), so rounding them separately would amplify bf16
-//   rounding errors.  The scalars s, m, Et = E e^{-m}, P of every token come from the scalar
+//   nearly cancel (the weights sum to zero), so rounding them separately would amplify the
+//   operand rounding.  The scalars s, m, Et = E e^{-m}, P of every token come from the scalar
 //   pass (zs_scalars.cu, the canonical blocked fp32 order of zs_common.cuh), which runs first;
 //   the chunk reference M_c is the m of the chunk's last token.
 //
@@ -32,7 +37,7 @@
 //                     shared memory; hf = 0 forms the row coefficients and the row weight
 //                     operand, hf = 1 the column weight operand; each half builds half of the
 //                     row's scaled value tile Vsc.
-//   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> bf16 tile; state -> bf16
+//   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> fp16 tile; state -> fp16
 //                     tile (and the F~ rescale); X -> output rows.
 //   warp 12     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
 //   warp 13     (T) : TMA producer: q and k chunks 128B-swizzled directly into the operand
@@ -48,6 +53,7 @@
 
 #include "zs_common.cuh"
 #include "zs_internal.h"
+#include "zs_range.cuh"
 #include "zs_sm100.cuh"
 
 namespace zs {
@@ -58,7 +64,7 @@ using namespace sm100;
 constexpr int kC = 128;       // tokens per chunk
 constexpr int kDV = 32;       // value columns per CTA
 constexpr int kThreads = 448;
-constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] bf16 atom tile
+constexpr uint32_t kTile = 128 * 128;  // one [128 x 64] 16-bit atom tile
 
 // Row coefficients (a, b, g) of a chunk, one block per operand stage.
 struct Coef {
@@ -89,7 +95,7 @@ struct Cfg {
   static constexpr uint32_t BYTES = LNW_OFF + 2 * 32 * 4;
   static constexpr uint32_t SMEM = BYTES;  // the base is 1024-byte aligned (checked at entry)
   static constexpr uint32_t TM_A = 0, TM_W = 128, TM_X = 256, TM_ST = 384;
-  // S tile (bf16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
+  // S tile (fp16 pairs, A operand of S V): its own 64 columns when d = 64, else the consumed
   // Q K^T columns (then the next Q K^T waits for the S V product)
   static constexpr uint32_t TM_S = (D == 64) ? 448 : 0;
   static_assert(SMEM <= 232448, "shared memory budget of one CTA");
@@ -150,32 +156,45 @@ __device__ __forceinline__ bool vsc_wait(Misc* ms, int c) {
   return mbar_wait_warp(&ms->vsc_free[(c - NS) & 1], (uint32_t)((c - NS) >> 1) & 1u, &ms->abort);
 }
 
-// Vsc row r, 16-byte pieces x0, x0 + 1 of the value row: the raw bf16 words are copied from
-// the 64B-swizzled staging tile to columns 8 x .. 8 x + 7 of atom 0, then the scaled parts:
-// atom 0 = [v | e v], atom 1 = [s' v | k v], from the row's column scalars (e, s', k).
-__device__ __forceinline__ void build_vsc_half(uint8_t* vt, const uint8_t* vst, int r, int x0,
-                                               float ce, float cs1, float ck) {
+// Vsc row r, 16-byte pieces x0, x0 + 1 of the value row, fp16: the value itself (exact for bf16
+// values in the fp16 range) to columns 8 x .. 8 x + 7 of atom 0, then the scaled parts:
+// atom 0 = [v | e v], atom 1 = [s' v | k v], from the row's column scalars (e, s', k) (s'
+// already carries G's 2^-ks).  Returns the largest |v| as bf16 pairs.
+__device__ __forceinline__ uint32_t build_vsc_half(uint8_t* vt, const uint8_t* vst, int r,
+                                                   int x0, float ce, float cs1, float ck) {
   const float2 ce2 = make_float2(ce, ce), cs2 = make_float2(cs1, cs1), ck2 = make_float2(ck, ck);
+  uint32_t vmax = 0u;
 #pragma unroll
   for (int x = x0; x < x0 + 2; ++x) {
     const uint4 wv = *reinterpret_cast<const uint4*>(vst + sw64_off(r, x));
-    *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = wv;
     const uint32_t pv[4] = {wv.x, wv.y, wv.z, wv.w};
-    uint32_t pe[4], ps[4], pk[4];
+    uint32_t ph[4], pe[4], ps[4], pk[4];
 #pragma unroll
     for (int y = 0; y < 4; ++y) {
       float2 v2;
       unpack_bf16x2(pv[y], v2.x, v2.y);
+      vmax = bf16x2_absmax(vmax, pv[y]);
       const float2 e2 = __fmul2_rn(ce2, v2), s2 = __fmul2_rn(cs2, v2), k2 = __fmul2_rn(ck2, v2);
-      pe[y] = pack_bf16x2(e2.x, e2.y);
-      ps[y] = pack_bf16x2(s2.x, s2.y);
-      pk[y] = pack_bf16x2(k2.x, k2.y);
+      ph[y] = pack_f16x2(v2.x, v2.y);
+      pe[y] = pack_f16x2(e2.x, e2.y);
+      ps[y] = pack_f16x2(s2.x, s2.y);
+      pk[y] = pack_f16x2(k2.x, k2.y);
     }
+    *reinterpret_cast<uint4*>(vt + sw128_off(r, x)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
     *reinterpret_cast<uint4*>(vt + sw128_off(r, 4 + x)) = make_uint4(pe[0], pe[1], pe[2], pe[3]);
     *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, x)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
     *reinterpret_cast<uint4*>(vt + kTile + sw128_off(r, 4 + x)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
+  return vmax;
 }
+
+// bf16 values from 45056 up (and inf, NaN) are beyond what the fp16 operands hold once rotated
+// (a rotation grows an element by up to sqrt 2; fp16 ends at 65504).
+__device__ __forceinline__ bool beyond_f16(uint32_t bf16x2_max, uint32_t limit) {
+  return (bf16x2_max & 0xffffu) >= limit || (bf16x2_max >> 16) >= limit;
+}
+constexpr uint32_t kBf16RotLimit = 0x4730u;  // 45056
+constexpr uint32_t kBf16Limit = 0x4780u;     // 65536
 
 // ============================================================================ T: TMA producer
 template <int D>
@@ -222,11 +241,12 @@ __device__ void role_tma(const ChunkParams& p, uint8_t* smem, Misc* ms, int bh, 
 
 // ============================================================================ O: operands
 // Rotates (RoPE) pair group g (pairs 8g .. 8g+7 with partners + D/2) of row r of a
-// 128B-swizzled bf16 tile in place and accumulates the row's squared norm into ss (two
-// partial sums).  cs[k] = (cos, sin) of pair 8g + k.
+// 128B-swizzled bf16 tile in place, as fp16 (converted without rotation when rope is off),
+// accumulates the row's squared norm into ss (two partial sums) and the largest |x| (bf16
+// pairs) into amax.  cs[k] = (cos, sin) of pair 8g + k.
 template <int D>
 __device__ __forceinline__ void rotate_group(uint8_t* tile, int r, int g, bool rope,
-                                             const float2 (&cs)[8], float2& ss) {
+                                             const float2 (&cs)[8], float2& ss, uint32_t& amax) {
   constexpr int HALF = D / 2;
   const int ca = 8 * g, cb = 8 * g + HALF;
   uint4* pa = reinterpret_cast<uint4*>(tile + (ca / 64) * kTile + sw128_off(r, (ca % 64) / 8));
@@ -239,6 +259,7 @@ __device__ __forceinline__ void rotate_group(uint8_t* tile, int r, int g, bool r
     float2 xa, xb;  // elements (2k, 2k+1) of the two halves
     unpack_bf16x2(wl[k], xa.x, xa.y);
     unpack_bf16x2(wh[k], xb.x, xb.y);
+    amax = bf16x2_absmax(bf16x2_absmax(amax, wl[k]), wh[k]);
     ss = __ffma2_rn(xa, xa, ss);
     ss = __ffma2_rn(xb, xb, ss);
     if (rope) {
@@ -247,14 +268,15 @@ __device__ __forceinline__ void rotate_group(uint8_t* tile, int r, int g, bool r
       const float2 s2 = make_float2(cs[2 * k].y, cs[2 * k + 1].y);
       const float2 na = __ffma2_rn(xa, c2, __fmul2_rn(make_float2(-xb.x, -xb.y), s2));
       const float2 nb = __ffma2_rn(xa, s2, __fmul2_rn(xb, c2));
-      oa[k] = pack_bf16x2(na.x, na.y);
-      ob[k] = pack_bf16x2(nb.x, nb.y);
+      oa[k] = pack_f16x2(na.x, na.y);
+      ob[k] = pack_f16x2(nb.x, nb.y);
+    } else {
+      oa[k] = pack_f16x2(xa.x, xa.y);
+      ob[k] = pack_f16x2(xb.x, xb.y);
     }
   }
-  if (rope) {
-    *pa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-    *pb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-  }
+  *pa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  *pb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
 }
 
 // Per chunk: rotation of this half's rotary pairs of q and k, the row's norms (halves summed
@@ -268,6 +290,9 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
   const int r = 32 * (warp & 3) + lane;  // token row inside the chunk, 0..127
   const int N = a.N;
   const float4* __restrict__ scal = a.scal + row0;
+  const int ks = s_exp(a, blockIdx.x);          // G is carried with s 2^-ks
+  const float sinv = pow2f(-ks);
+  const float smax = seq_smax(a, blockIdx.x);   // the sequence's largest |s|
   float* phi = reinterpret_cast<float*>(smem + CF::PHI_OFF);      // [2][D/2]
   float* theta = reinterpret_cast<float*>(smem + CF::THETA_OFF);  // [D/2]
   float2* nrm = reinterpret_cast<float2*>(smem + CF::NRM_OFF);    // [2][128] (|q|^2, |k|^2)
@@ -293,12 +318,13 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
   // absent, so that its sigmoid is 0)
   struct Ahead {
     float4 sc;
-    float M, x1, xh, x0;
+    float M, Mp, x1, xh, x0;  // Mp: the running maximum at the token before the chunk
   };
   auto load_ahead = [&](int cc) {
-    Ahead o{make_float4(0.f, 0.f, 0.f, 0.f), 0.0f, 0.0f, 0.0f, -INFINITY};
+    Ahead o{make_float4(0.f, 0.f, 0.f, 0.f), 0.0f, 0.0f, 0.0f, 0.0f, -INFINITY};
     if (cc < nch) {
       o.M = chunk_ref(scal, cc, N);
+      if (cc > 0) o.Mp = __ldg(&scal[cc * kC - 1].y);
       const int i = cc * kC + r;
       if (i < N) {
         o.sc = __ldg(scal + i);
@@ -334,6 +360,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
     // ---- rotate this half's pair groups of q and k in place (TMA tiles), half norms ----
     const bool rot = a.rope != 0 && valid;
     float2 qq2 = make_float2(0.0f, 0.0f), kk2 = make_float2(0.0f, 0.0f);
+    uint32_t amax = 0u;  // the row's largest |q|, |k| elements (bf16 pairs)
     {
       const float* ph = phi + (c & 1) * (D / 2);
       const float rf = (float)r;
@@ -350,10 +377,11 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
             cs[k] = make_float2(cn, sn);
           }
         }
-        rotate_group<D>(qt, r, g, rot, cs, qq2);
-        rotate_group<D>(kt, r, g, rot, cs, kk2);
+        rotate_group<D>(qt, r, g, rot, cs, qq2, amax);
+        rotate_group<D>(kt, r, g, rot, cs, kk2, amax);
       }
     }
+    if (beyond_f16(amax, kBf16RotLimit)) report(a.status, kErrRange);
     nrm[hf * kC + r] = make_float2(__fadd_rn(qq2.x, qq2.y), __fadd_rn(kk2.x, kk2.y));
     mbar_arrive(&ms->nbar);
     if (!mbar_wait_warp(&ms->nbar, c & 1, &ms->abort)) {
@@ -362,12 +390,16 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
     }
     const float2 n0 = nrm[r], n1 = nrm[kC + r];
     const float qq = __fadd_rn(n0.x, n1.x), kq = __fadd_rn(n0.y, n1.y);
-    // column scalars and row coefficients (these feed bf16 / fp32 products, not the scalar
+    // column scalars and row coefficients (these feed 16-bit / fp32 products, not the scalar
     // contract: fast exp, reciprocal square root and division are accurate enough here)
     const float s = cur.sc.x, m = cur.sc.y, Et = cur.sc.z, P = cur.sc.w, M = cur.M;
     const float kap = rsqrtf(fmaxf(kq, 1e-24f));
     float ce = 0.0f, cs1 = 0.0f, ck = 0.0f;
-    float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);  // (a, b, g) of the weight operand
+    // the output's coefficients of X_F, X_G, X_H (scaled for the fp16 state copy: 2^kb, and
+    // 2^ks for G; X_F's copy is referenced to the running maximum before the chunk) and the
+    // row's S scale 2^kr
+    float4 co = make_float4(0.f, 0.f, 0.f, 1.f);
     if (valid) {
       ce = __fmul_rn(__expf(__fsub_rn(s, M)), kap);
       cs1 = __fmul_rn(s, kap);
@@ -379,17 +411,24 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
         const float rt = __fdividef(1.0f, (float)(i + 1));
         const float b0c = (sig1 - sigh) * rt;
         const float ahat = __fdividef(sigh, Et) * __expf(M - m);
+        float g0c = -(b0c * P * rt + sigh * rt);
+        if (a.g0) g0c += __fdividef(1.0f, 1.0f + __expf(-cur.x0)) * rt;  // zero-order
         cf.x = rho * ahat;
         cf.y = rho * b0c;
-        cf.z = -rho * (b0c * P * rt + sigh * rt);
-        if (a.g0) cf.z += rho * __fdividef(1.0f, 1.0f + __expf(-cur.x0)) * rt;  // zero-order
+        cf.z = rho * g0c;
         if (!isfinite(cf.x)) report(a.status, kErrRange);
+        const float kb2 = pow2f(state_exp(c, kC));
+        co.x = c > 0 ? rho * __fdividef(sigh, Et) * __expf(cur.Mp - m) * kb2 : 0.0f;
+        co.y = cf.y * kb2 * pow2f(ks);
+        co.z = cf.z * kb2;
+        // a e_i over the row's keys i <= t is at most sigma^h / E~ (e^{s_i - m_t} <= 1)
+        co.w = pow2f(row_exp(__fdividef(sigh, Et) + fabsf(b0c) * smax + fabsf(g0c)));
       } else if (!isfinite(ce)) {
         report(a.status, kErrRange);
       }
     }
     if (hf == 0) {
-      coef_block(smem, CF::COEF_OFF, st)->coef[r] = cf;
+      coef_block(smem, CF::COEF_OFF, st)->coef[r] = co;
       mbar_arrive(&ms->cf_full[st]);
     }
     // Weight operands: W_{t,i} = a_t e_i + b_t s'_i + g_t k_i is formed by one K = 16 MMA of
@@ -433,7 +472,8 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
       fail_wait(ms, a.status);
       return;
     }
-    build_vsc_half(vt, smem + CF::VST_OFF, r, 2 * hf, ce, cs1, ck);
+    const uint32_t vmax = build_vsc_half(vt, smem + CF::VST_OFF, r, 2 * hf, ce, cs1 * sinv, ck);
+    if (beyond_f16(vmax, kBf16Limit)) report(a.status, kErrRange);
     mbar_arrive(&ms->vst_empty);
     fence_proxy_async_smem();
     mbar_arrive(&ms->op_full);
@@ -459,10 +499,11 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const uint32_t tA = tm + CF::TM_A, tW = tm + CF::TM_W, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
-  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);   // Q K^T, R C^T
-  constexpr uint32_t id_qs = idesc_bf16_f32(128, 96, false, false);    // Q [F|G|H]
-  constexpr uint32_t id_sv = idesc_bf16_f32(128, 32, false, true);     // S V
-  constexpr uint32_t id_st = idesc_bf16_f32(128, D, true, true);       // Vsc^T K
+  constexpr uint32_t id_qk = idesc_f16_f32(128, 128, false, false);    // Q K^T
+  constexpr uint32_t id_w = idesc_bf16_f32(128, 128, false, false);    // R C^T (hi/lo bf16)
+  constexpr uint32_t id_qs = idesc_f16_f32(128, 96, false, false);     // Q [F|G|H]
+  constexpr uint32_t id_sv = idesc_f16_f32(128, 32, false, true);      // S V
+  constexpr uint32_t id_st = idesc_f16_f32(128, D, true, true);        // Vsc^T K
   const uint64_t d_rw = sw32_desc(base + CF::RW_OFF), d_cw = sw32_desc(base + CF::CW_OFF);
   bool ok = true;
   // descriptors: the start address field is (address >> 4), and every tile lies below 256 KB,
@@ -489,7 +530,7 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
       const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
       mma_f16kind(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
     }
-    mma_f16kind(tW, d_rw, d_cw, id_qk, 0u);
+    mma_f16kind(tW, d_rw, d_cw, id_w, 0u);
     mma_commit(&ms->a_full);
     mma_commit(&ms->w_done);
     // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
@@ -560,7 +601,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
   for (int c = 0; c < nch && ok; ++c) {
     float4 cf_next = make_float4(0.f, 0.f, 0.f, 0.f);
     const float M_next = c + 1 < nch ? chunk_ref(scal, c + 1, N) : 0.0f;
-    // ---- S = [i <= t] (Q K^T) o W, fp32 product then bf16 (rows t, K = token i) ----
+    // ---- S = [i <= t] (Q K^T) o W 2^kr_t, fp32 product then fp16 (rows t, K = token i) ----
     ok = mbar_wait_warp(&ms->a_full, c & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
@@ -576,12 +617,13 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
         for (int y = 0; y < 8; ++y) {
           float2 val = __fmul2_rn(make_float2(__uint_as_float(ra[2 * y]), __uint_as_float(ra[2 * y + 1])),
                                   make_float2(__uint_as_float(rw[2 * y]), __uint_as_float(rw[2 * y + 1])));
+          val = __fmul2_rn(val, make_float2(cf.w, cf.w));  // the row's 2^kr
           const int col = 16 * h + 2 * y;
           if ((h >> 1) == wq) {  // diagonal block: keep i <= t only
             if (col > t) val.x = 0.0f;
             if (col + 1 > t) val.y = 0.0f;
           }
-          pw[y] = pack_bf16x2(val.x, val.y);
+          pw[y] = pack_f16x2(val.x, val.y);
         }
         tmem_st8_nowait(tm + CF::TM_S + 8 * h, pw);
       };
@@ -617,7 +659,8 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
     tc_fence_before();
     mbar_arrive(&ms->a_free);
     mbar_arrive(&ms->am_full);
-    // ---- state after chunk c -> bf16 B operand rows 32..127 of chunk c+1, F~ rescaled ----
+    // ---- state after chunk c -> fp16 B operand rows 32..127 of chunk c+1 (times 2^-kb, F~ at
+    //      its reference M_cur), F~ in TMEM rescaled to M_next for the next update ----
     if (c + 1 < nch) {
       ok = mbar_wait_warp(&ms->st_done, c & 1, &ms->abort);
       if (ok && c >= 1) ok = mbar_wait_warp(&ms->sst_free, (c - 1) & 1, &ms->abort);
@@ -626,6 +669,7 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       if (wq >= 1) {
         const bool rescale = (wq == 1) && (M_next > M_cur);
         const float fac = rescale ? expf(__fsub_rn(M_cur, M_next)) : 1.0f;
+        const float2 sc2 = make_float2(pow2f(-state_exp(c + 1, kC)), pow2f(-state_exp(c + 1, kC)));
         const uint32_t sst = base + CF::SST_OFF;
         // 32 state columns per round: two 16-column loads, one wait
 #pragma unroll 1
@@ -636,6 +680,23 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 2; ++q) reg_fence(rr[q]);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              const uint32_t* w8 = rr[q] + 8 * x;
+              uint32_t pk[4];
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                const float2 f = __fmul2_rn(make_float2(__uint_as_float(w8[2 * y]),
+                                                        __uint_as_float(w8[2 * y + 1])), sc2);
+                pk[y] = pack_f16x2(f.x, f.y);
+              }
+              const int col0 = c0 + 16 * q + 8 * x;
+              sts128(sst + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8),
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            }
+          }
           if (rescale) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -645,20 +706,6 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
               tmem_st16_nowait(tm + CF::TM_ST + c0 + 16 * q, rr[q]);
             }
             tmem_wait_st();
-          }
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              const uint32_t* w8 = rr[q] + 8 * x;
-              uint4 p;
-              p.x = pack_bf16x2(__uint_as_float(w8[0]), __uint_as_float(w8[1]));
-              p.y = pack_bf16x2(__uint_as_float(w8[2]), __uint_as_float(w8[3]));
-              p.z = pack_bf16x2(__uint_as_float(w8[4]), __uint_as_float(w8[5]));
-              p.w = pack_bf16x2(__uint_as_float(w8[6]), __uint_as_float(w8[7]));
-              const int col0 = c0 + 16 * q + 8 * x;
-              sts128(sst + (col0 / 64) * kTile + sw128_off(t, (col0 % 64) / 8), p);
-            }
           }
         }
       }
@@ -680,6 +727,9 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       if (c >= 1) tmem_ld16_nowait(tx + 0, rx);
       tmem_wait_ld();
       reg_fence(rsv);
+      const float rinv = __frcp_rn(cf.w);  // S V carries the row's 2^kr
+#pragma unroll
+      for (int j = 0; j < 16; ++j) rsv[j] = __float_as_uint(__uint_as_float(rsv[j]) * rinv);
       if (c >= 1) {
         reg_fence(rx);
 #pragma unroll
@@ -793,12 +843,13 @@ __device__ void role_epilogue(const FwdArgs& a, uint8_t* smem, Misc* ms, int bh,
       float* rec = record_ptr(a.final_state, bh, D);
       const int j = t % 32;
       const int off = wq == 1 ? rec_F(D) : wq == 2 ? rec_G(D) : rec_H(D);
+      const float gs = wq == 2 ? pow2f(s_exp(a, bh)) : 1.0f;  // G was carried with s 2^-ks
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         float v[32];
         tmem_ld32(tm + CF::TM_ST + cb * 32, v);
 #pragma unroll
-        for (int y = 0; y < 32; ++y) rec[off + (cb * 32 + y) * D + j0 + j] = v[y];
+        for (int y = 0; y < 32; ++y) rec[off + (cb * 32 + y) * D + j0 + j] = v[y] * gs;
       }
     }
   }

@@ -62,6 +62,7 @@
 
 #include "zs_common.cuh"
 #include "zs_internal.h"
+#include "zs_range.cuh"
 #include "zs_sm100.cuh"
 
 namespace zs {
@@ -128,6 +129,7 @@ struct WalkParams {
   int nseg;                    // segments per sequence
   int seg_start[kMaxSeg + 1];  // segment j covers chunks [seg_start[j], seg_start[j + 1])
   long long wait_limit;        // bound of every wait, SM clock cycles
+  int dbg_skip;                // testing hook: one warp withholds its first S-tile arrival
 };
 
 __device__ __forceinline__ void fail_wait(WMisc* ms, int* status) {
@@ -151,28 +153,8 @@ __device__ __forceinline__ float chunk_ref(const float4* scal, int c, int N) {
   return scal[min(N, (c + 1) * kC) - 1].y;
 }
 
-// The fp16 operands are kept in range by exact powers of two, folded into the fp32
-// coefficients: 2^k for |k| < 127.
-__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
-// An exponent e with x < 2^e for x > 0 (the binary exponent of x plus one: 2^(e-1) <= x for
-// normal x), 0 for x <= 0.
-__device__ __forceinline__ int exp_above(float x) {
-  return x > 0.0f ? (int)((__float_as_uint(x) >> 23) & 0xffu) - 126 : 0;
-}
-// Scale exponent of the state copy that feeds chunk c's Q [F~|G|H] product: the state holds
-// the c * 128 tokens before the chunk, each entry at most that many times max|v| (the unit
-// keys and the factors e^{s - M} are at most 1; G is carried with s scaled to |s| < 1).
-__device__ __forceinline__ int state_exp(int c) { return c > 0 ? exp_above((float)(c * kC)) : 0; }
-// Scale exponent of s in the G products: s 2^-ks has |s 2^-ks| < 1 (from the scalar pass's
-// largest |s| of each of its CTAs).
-__device__ __forceinline__ int s_exp(const FwdArgs& a, int bh) {
-  float m = 0.0f;
-  if (a.smax) {
-#pragma unroll
-    for (int r = 0; r < kScalarCtas; ++r) m = fmaxf(m, a.smax[(size_t)bh * kScalarCtas + r]);
-  }
-  return max(0, exp_above(m));
-}
+// Scale exponent of the state copy that feeds chunk c's Q [F~|G|H] product.
+__device__ __forceinline__ int state_exp(int c) { return zs::state_exp(c, kC); }
 
 // ============================================================================ T: TMA producer
 // Per chunk: q (walk chunks), k, v into the chunk's stage, and the chunk's rotary base angles
@@ -294,14 +276,9 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
   // rotary frequencies of this half's 16 pairs (pairs 16 hf .. 16 hf + 15), in shared memory
   const uint32_t th_s = base + WLay::THETA + 64 * hf;
   const float M_ref = c0 > 0 ? scal[c0 * kC - 1].y : 0.0f;  // replay reference
-  const int ks = min(100, s_exp(a, bh));
+  const int ks = s_exp(a, bh);
   const float sinv = pow2f(-ks);
-  float smax_seq = 0.0f;  // the sequence's largest |s| (bounds the weights of a row)
-  if (a.smax) {
-#pragma unroll
-    for (int rr = 0; rr < kScalarCtas; ++rr)
-      smax_seq = fmaxf(smax_seq, a.smax[(size_t)bh * kScalarCtas + rr]);
-  }
+  const float smax_seq = seq_smax(a, bh);  // the sequence's largest |s| (bounds a row's weights)
 
   auto load_in = [&](int cc) {
     RowIn o{make_float4(0.f, 0.f, 0.f, 0.f), 0.0f, 0.0f, 0.0f, -INFINITY};
@@ -416,8 +393,7 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
           if (!isfinite(ca)) report(a.status, kErrRange);
           // a e_i over the row's keys i <= t is at most sigma^h / E~ (e^{s_i - m_t} <= 1)
           const int kb = state_exp(c);
-          const int kr = min(60, max(-60, -exp_above(__fdividef(sigh, Et) + fabsf(bc) * smax_seq +
-                                                       fabsf(cg))));
+          const int kr = row_exp(__fdividef(sigh, Et) + fabsf(bc) * smax_seq + fabsf(cg));
           cf = make_float4(ca, bc * pow2f(kb + ks), cg * pow2f(kb), pow2f(kr));
         }
         sts128f(base + WLay::COEF + (st * kC + r) * 16, cf);
@@ -690,7 +666,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
   const uint32_t lnw_s = base + WLay::LNW;
   const int N = a.N;
   const float4* scal = a.scal + (size_t)bh * N;
-  const float sinv = pow2f(-min(100, s_exp(a, bh)));  // G is carried with s 2^-ks
+  const float sinv = pow2f(-s_exp(a, bh));  // G is carried with s 2^-ks
   const int cfirst = c0 > 0 ? c0 - 1 : 0;  // first update followed by a state copy
   const int xfirst = max(c0, 1);           // first chunk with a Q [F~|G|H] product
   // chunk references of the current and the next chunk, loaded one chunk ahead
@@ -773,7 +749,10 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     }
     tc_fence_before();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->s_full);
+    // (the testing hook withholds the first arrival of warp kEpWarp0: the S V product's wait
+    // then runs out and the CTA abandons its work)
+    if ((threadIdx.x & 31) == 0 && !(p.dbg_skip && wi == 0 && (threadIdx.x >> 5) == kEpWarp0))
+      mbar_arrive(&ms->s_full);
     // ---- the state after this chunk -> B tile of the next one ----
     if (c <= c1 - 2) {
       ok = state_copy<EPQ>(ms, tm, base, wq, hb, t, c, c - cfirst, xfirst, Mc, Mn, lim);
@@ -922,7 +901,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     tc_fence_after();
     float* rec = record_ptr(a.final_state, bh, kD);
     const int j = wq < 2 ? t : t - 64;
-    const float gs = pow2f(min(100, s_exp(a, bh)));  // G was carried with s 2^-ks
+    const float gs = pow2f(s_exp(a, bh));  // G was carried with s 2^-ks
     constexpr int W = 32 / EPQ;
 #pragma unroll 1
     for (int q = 0; q < kStPieces; ++q) {
@@ -1030,6 +1009,9 @@ __global__ void walk_angle_kernel(float* tab, int nch, double base) {
   }
 }
 
+std::atomic<long long> g_dbg_wait_limit{0};  // zeros_debug_walk settings (off by default)
+std::atomic<int> g_dbg_skip{0};
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1093,7 +1075,9 @@ cudaError_t launch_walk_t(const FwdArgs& a, const float* ang, int nseg_max, cuda
   WalkParams p;
   p.a = a;
   p.ang = ang;
-  p.wait_limit = 4294967296ll;
+  const long long lim = g_dbg_wait_limit.load();
+  p.wait_limit = lim > 0 ? lim : 4294967296ll;
+  p.dbg_skip = g_dbg_skip.load();
   const int BH = a.B * a.H;
   if (!make_map(&p.tq, a.q, a.N, BH) || !make_map(&p.tk, a.k, a.N, BH) ||
       !make_map(&p.tv, a.v, a.N, BH) || !make_map(&p.to, a.out, a.N, BH))
@@ -1133,6 +1117,11 @@ cudaError_t launch_walk_t(const FwdArgs& a, const float* ang, int nseg_max, cuda
 }  // namespace
 
 bool walk_supported(int d, int dtype, int causal) { return d == kD && dtype == 0 && causal == 1; }
+
+void set_walk_debug(long long wait_limit_cycles, int skip_one_arrive) {
+  g_dbg_wait_limit.store(wait_limit_cycles);
+  g_dbg_skip.store(skip_one_arrive ? 1 : 0);
+}
 
 size_t walk_angle_floats(int N) { return (size_t)((N + kC - 1) / kC + 1) * 32; }
 
