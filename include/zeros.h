@@ -261,6 +261,20 @@ int zeros_version(void);
  * all entry points).  Used by benchmarks to count device work; never reset. */
 unsigned long long zeros_kernel_launches(void);
 
+/* Testing hook for the failure path of the d = 64 tensor-core forward (the bf16 causal
+ * forward at d = 64 on the chunked path).  Every wait of that kernel on another warp's
+ * progress is bounded; when one gives up the kernel records ZEROS_ERR_TIMEOUT, its other warps
+ * leave their loops, it waits for its own copies and tensor-core work still in flight, frees
+ * its tensor memory and returns, so that the context stays usable.
+ *   wait_limit_cycles  > 0: bound of each such wait in SM clock cycles for later launches;
+ *                      0: the default (2^32 cycles, about two seconds).
+ *   skip_one_arrive    nonzero: in later launches one warp of every CTA withholds its arrival
+ *                      on the barrier that releases the first S V product, so that the wait
+ *                      for it runs out (and everything after it is abandoned).
+ * Both are process-wide settings, off by default; set them only while no forward runs on any
+ * thread.  Returns ZEROS_OK, or ZEROS_ERR_INVALID for a negative limit. */
+int zeros_debug_walk(long long wait_limit_cycles, int skip_one_arrive);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ EXPORTS = ["zeros_fwd", "zeros_fwd_ex", "zeros_state_bytes", "zeros_state_record
            "zeros_state_init", "zeros_decode_step", "zeros_decode_step_ex", "zeros_get_status",
            "zeros_status_string", "zeros_last_error_message", "zeros_version",
            "zeros_kernel_launches", "zeros_fwd_noalloc", "zeros_bwd", "zeros_fwd_ln",
-           "zeros_decode_step_ln", "zeros_sm_fwd", "zeros_bwd_ex"]
+           "zeros_decode_step_ln", "zeros_sm_fwd", "zeros_bwd_ex", "zeros_debug_walk"]
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,8 @@ def load():
         lib.zeros_last_error_message.restype = ctypes.c_char_p
         lib.zeros_version.restype = i
         lib.zeros_kernel_launches.restype = ctypes.c_ulonglong
+        lib.zeros_debug_walk.argtypes = [ctypes.c_longlong, i]
+        lib.zeros_debug_walk.restype = i
         lib.zeros_fwd_noalloc.argtypes = [vp] * 9 + [i] * 7 + [f, vp, vp]
         lib.zeros_bwd.argtypes = [vp] * 19 + [i] * 6 + [f, vp]
         lib.zeros_bwd.restype = i
@@ -95,6 +97,15 @@ def load():
 def kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(load().zeros_kernel_launches())
+
+
+def debug_walk(wait_limit_cycles: int = 0, skip_one_arrive: bool = False):
+    """Testing hook of the d = 64 tensor-core forward's failure path (zeros_debug_walk): the
+    bound of its waits in SM cycles (0 = default) and whether one warp per CTA withholds an
+    arrival so that a wait runs out.  Process-wide; set only while no forward runs."""
+    rc = load().zeros_debug_walk(int(wait_limit_cycles), int(bool(skip_one_arrive)))
+    if rc != ZEROS_OK:
+        raise ZerosError(rc, "zeros_debug_walk")
 
 
 def status_string(code: int) -> str:

@@ -252,6 +252,12 @@ int zeros_version(void) { return 100; }
 
 unsigned long long zeros_kernel_launches(void) { return g_launches.load(); }
 
+int zeros_debug_walk(long long wait_limit_cycles, int skip_one_arrive) {
+  if (wait_limit_cycles < 0) return fail(ZEROS_ERR_INVALID, "negative wait limit");
+  set_walk_debug(wait_limit_cycles, skip_one_arrive);
+  return ZEROS_OK;
+}
+
 const char* zeros_status_string(int status) {
   switch (status) {
     case ZEROS_OK: return "ok";

@@ -98,6 +98,9 @@ size_t walk_angle_floats(int N);
 cudaError_t launch_walk_angles(float* tab, int N, double base, cudaStream_t stream);
 cudaError_t launch_fwd_walk(const FwdArgs& a, const float* ang, int nseg_max,
                             cudaStream_t stream);
+// Testing hook of zeros_debug_walk: the wait bound of later walk launches (0 = default) and
+// whether one warp per CTA withholds its first arrival on the S-tile barrier.
+void set_walk_debug(long long wait_limit_cycles, int skip_one_arrive);
 
 // zs_scalars.cu: per-token (s, m, Et, P) of every sequence into scal ([B*H, N] float4), the
 // largest |s| per sequence and CTA into a.smax when given ([B*H, kScalarCtas]), the debug
