@@ -43,12 +43,13 @@ WORKLOADS = {
 }
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) of one forward call (the scalar pass and the chunk kernel), from the
-# committed ncu summaries of this workload, keyed by a fingerprint of the kernel sources they
-# were measured on; reported as null once the sources change.
-CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_chunk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
-                 "zero_sum_prefix_gb300/csrc/zs_sm100.cuh", "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"a39f27938042fa78": 34121984 + 3072 + 107020800 + 16308224}
+# DRAM bytes (read + write) of one forward call (the scalar pass and the d = 64 forward kernel),
+# from the committed ncu summaries of this workload, keyed by a fingerprint of the kernel
+# sources they were measured on; reported as null once the sources change.
+CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_walk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
+                 "zero_sum_prefix_gb300/csrc/zs_range.cuh", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
+                 "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
+MEASURED_TRAFFIC = {"d273b4b55c6aed51": 33602816 + 0 + 109883392 + 9741824}
 
 
 def kernel_fingerprint() -> str:
@@ -107,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -404,7 +405,7 @@ def ours_forward(args, w: zi.Workload):
                                      and not args.ln else None),
                          "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": alg,
-                         "timed": ("the whole zeros_fwd call: scalar pass + chunk kernel"
+                         "timed": ("the whole zeros_fwd call: scalar pass + forward kernel"
                                    if args.path != "simt" else "the whole zeros_fwd call")},
             "cpu_baseline": cpu,
             "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
@@ -726,7 +727,10 @@ def ours_decode(args, w: zi.Workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    # default: 1500 steps (the default workload's timed region is then about a quarter of a
+    # second, so the clock samples, every 50 ms, come from a sustained run); 30 for the
+    # reference arm, whose steps run the CPU oracle
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal", choices=sorted(WORKLOADS))
@@ -735,6 +739,8 @@ def main():
     ap.add_argument("--ln", action="store_true", help="fuse the output LayerNorm (forward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 30 if args.impl == "reference" else 1500
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         reference_arm(args, w)

@@ -189,15 +189,16 @@ def test_decode_matches_forward_bitexact(zs, d, rope, dtype):
     assert (view["t"] == N0 + steps).all()
 
 
-def test_decode_after_long_prefill_d128(zs):
-    """The recurrent-decode workload's per-sequence shape: an 8192-token RoPE prefill at d = 128
-    on the chunked tensor-core path, then 64 decode steps.  Logits and prefix scalars of every
-    step equal those of a forward pass over all 8256 tokens bit for bit (every sequence); the
-    decode outputs of four seeded (b, h) sequences match the fp64 oracle over the whole
-    sequence."""
+@pytest.mark.parametrize("rope", [False, True])
+def test_decode_after_long_prefill_d128(zs, rope):
+    """The recurrent-decode workload's per-sequence shape: an 8192-token prefill at d = 128 on
+    the chunked tensor-core path (as the workload, without RoPE, and with it), then 64 decode
+    steps.  Logits and prefix scalars of every step equal those of a forward pass over all 8256
+    tokens bit for bit (every sequence); the decode outputs of four seeded (b, h) sequences
+    match the fp64 oracle over the whole sequence."""
     base = zi.DECODE_B256H32D128
     steps = 64
-    w = base.with_(B=2, H=4)
+    w = base.with_(B=2, H=4, rope=rope)
     N0 = w.N
     pre = zi.make(w, "cuda")
     st, outs, dbgs, toks = _decode_run(zs, w, pre, steps)

@@ -376,7 +376,7 @@ static int fwd_impl(const void* q, const void* k, const void* v, const void* u, 
     if (int rc = rope_table(ws, N, d, rope_base, st, &a.rope_table)) return rc;
   }
   if (use_chunk) {  // the scalar pass, then the chunked kernel
-    const bool walk = walk_supported(d, dtype, causal);
+    const bool walk = walk_supported(d, dtype, causal) && !ln;
     const float* ang = nullptr;
     if (walk && rope) {
       if (int rc = walk_angles(ws, N, rope_base, st, &ang)) return rc;

@@ -36,19 +36,23 @@
 // waits for another, and the replay costs a fraction of a full chunk (no queries, no intra-chunk
 // products, no outputs), so the segment lengths are chosen geometric to equalise the CTAs.
 //
-// Warp roles (576 threads, one CTA per SM; 448 with the fused LayerNorm):
+// Warp roles (576 threads, one CTA per SM):
 //   warps 0-7   (O) : operands; token row r = 16 w + lane / 2, half hf = lane & 1 of the row's
 //                     rotary pairs: norms (halves exchanged by a shuffle), rotation and unit
 //                     scaling of q and k in place (TMA-landed tiles), column scalars (hf = 0),
 //                     row coefficients (hf = 1), half of the row's value-side tiles.
-//   warps 8-15  (E) : two per TMEM lane quadrant (one with the LayerNorm, which needs whole
-//                     rows): S tile from Q K^T, the state copy after each update (TMEM -> fp16
-//                     B tile of the next chunk's Q [F~|G|H] product, and the F~ rescale in
-//                     TMEM), output rows from X (staged in shared memory, one TMA store per
-//                     chunk), the final state (prefill).
-//   next warp   (M) : TMEM allocation; one thread issues every tcgen05.mma.
-//   last warp   (T) : TMA producer of q, k, v (three stages), with L2 prefetch ahead.
-// TMEM (512 columns): [0,128) Q K^T (the fp16 S tile overlays it: K step h in [16 h, 16 h + 8)), [128,320) X = Q[F~|G|H],
+//   warps 8-15  (E) : two per TMEM lane quadrant: S tile from Q K^T, the state copy after each
+//                     update (TMEM -> fp16 B tile of the next chunk's Q [F~|G|H] product, and the
+//                     F~ rescale in TMEM), output rows from X (staged in shared memory, one TMA
+//                     store per chunk), the final state (prefill).
+//   warp 16     (M) : TMEM allocation; one thread issues every tcgen05.mma.
+//   warp 17     (T) : TMA producer of q, k, v (three stages), with L2 prefetch ahead.
+// The fused output LayerNorm is not done here: it runs on the chunked kernel of zs_chunk.cu,
+// whose value slices exchange row statistics in a cluster (measured faster than whole rows
+// per thread with one E warp per quadrant here: 0.155 against 0.169 ms per call at
+// B8 H8 N4096).
+// TMEM (512 columns): [0,128) Q K^T (the fp16 S tile overlays it: K step h in [16 h, 16 h + 8)),
+// [128,320) X = Q[F~|G|H],
 // [320,384) X_SV, [384,448) state A = [F~^T ; G^T], [448,512) state B = [H^T ; F~^T].
 // The state B accumulator repeats F~^T in its upper lanes so that every copy warp reads 96
 // columns: quadrants 0/1 take F~ columns 0-31 from A and H from B, quadrants 2/3 G from A and
@@ -76,11 +80,9 @@ constexpr uint32_t kTile = 128 * 128;   // one 16-bit [128 x 64] atom tile (128 
 constexpr int kNST = 3;                 // q/k/v stages
 constexpr int kOpWarps = 8;
 constexpr int kEpWarp0 = 8;             // from warp 8: S tiles, state copies, outputs
-// E warps per TMEM lane quadrant: two without the output LayerNorm (they split every E task),
-// one with it (the LayerNorm needs whole rows in one thread)
-template <bool LN> constexpr int kEpq = LN ? 1 : 2;
-template <bool LN> constexpr int kMmaWarp = kEpWarp0 + 4 * kEpq<LN>;
-template <bool LN> constexpr int kThreads = (kMmaWarp<LN> + 2) * 32;
+constexpr int kEpq = 2;                 // E warps per TMEM lane quadrant (they split every E task)
+constexpr int kMmaWarp = kEpWarp0 + 4 * kEpq;
+constexpr int kThreads = (kMmaWarp + 2) * 32;
 constexpr int kMaxSeg = 4;
 
 struct WLay {
@@ -93,8 +95,7 @@ struct WLay {
   static constexpr uint32_t COL = OUTS + kTile;           // float2 [stage][128]: (e_i, s_i)
   static constexpr uint32_t COEF = COL + kNST * kC * 8;   // float4 [stage][128], the row scales:
                                                           // (a, b 2^(kb+ks), g 2^kb, 2^kr)
-  static constexpr uint32_t LNW = COEF + kNST * kC * 16;  // float [2][64]: LayerNorm gain, bias
-  static constexpr uint32_t THETA = LNW + 2 * kD * 4;     // float [32]: rotary frequencies
+  static constexpr uint32_t THETA = COEF + kNST * kC * 16;  // float [32]: rotary frequencies
   static constexpr uint32_t PHI = THETA + 128;            // float [stage][32]: chunk base angles
   static constexpr uint32_t MISC = PHI + kNST * 128;
   static constexpr uint32_t BYTES = MISC + 512;
@@ -652,9 +653,8 @@ __device__ __forceinline__ bool state_copy(WMisc* ms, uint32_t tm, uint32_t base
   return true;
 }
 
-template <bool LN>
 __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, int c0, int c1) {
-  constexpr int EPQ = kEpq<LN>;
+  constexpr int EPQ = kEpq;
   const FwdArgs& a = p.a;
   const long long lim = p.wait_limit;
   const int wq = (threadIdx.x >> 5) & 3;       // TMEM lane quadrant of this warp
@@ -663,7 +663,6 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
   const uint32_t tm = ms->tmem + ((uint32_t)(wq * 32) << 16);
   const uint32_t base = smem_u32(smem);
   const bool leader = threadIdx.x == kEpWarp0 * 32;
-  const uint32_t lnw_s = base + WLay::LNW;
   const int N = a.N;
   const float4* scal = a.scal + (size_t)bh * N;
   const float sinv = pow2f(-s_exp(a, bh));  // G is carried with s 2^-ks
@@ -810,26 +809,6 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
         }
       }
     };
-    float ln_mean = 0.0f, ln_rstd = 1.0f;
-    if constexpr (LN) {
-      // the whole row is in this thread: moments of its 64 outputs (sums shifted by the first)
-      float sh = 0.0f, s1 = 0.0f, s2 = 0.0f;
-#pragma unroll 1
-      for (int pc = 0; pc < 4; ++pc) {
-        float o[16];
-        out_piece(pc, o);
-        if (pc == 0) sh = o[0];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float dv = o[j] - sh;
-          s1 += dv;
-          s2 = __fmaf_rn(dv, dv, s2);
-        }
-      }
-      ln_mean = sh + s1 * (1.0f / kD);
-      const float m2 = fmaxf(s2 - s1 * s1 * (1.0f / kD), 0.0f);
-      ln_rstd = rsqrtf(m2 * (1.0f / kD) + a.ln_eps);
-    }
     // the staging tile is free once the previous chunk's store has read it
     if (wi >= 1) {
       if (leader) {
@@ -845,17 +824,6 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     for (int pc = hb * (4 / EPQ); pc < (hb + 1) * (4 / EPQ); ++pc) {
       float o[16];
       out_piece(pc, o);
-      if constexpr (LN) {
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const float4 w4 = lds128f(lnw_s + (16 * pc + 4 * j4) * 4);
-          const float4 b4 = lds128f(lnw_s + (kD + 16 * pc + 4 * j4) * 4);
-          const float wv[4] = {w4.x, w4.y, w4.z, w4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            o[4 * j4 + j] = __fmaf_rn((o[4 * j4 + j] - ln_mean) * ln_rstd, wv[j], bv[j]);
-        }
-      }
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const float* o8 = o + 8 * x;
@@ -903,12 +871,12 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
     const int j = wq < 2 ? t : t - 64;
     const float gs = pow2f(s_exp(a, bh));  // G was carried with s 2^-ks
     constexpr int W = 32 / EPQ;
+    static_assert(W == 16, "two E warps per quadrant");
 #pragma unroll 1
     for (int q = 0; q < kStPieces; ++q) {
       const Piece pc = st_piece(wq, t, q);
       uint32_t v[W];
-      if constexpr (EPQ == 1) tmem_ld32_nowait(tm + pc.col, v);
-      else tmem_ld16_nowait(tm + pc.col + W * hb, v);
+      tmem_ld16_nowait(tm + pc.col + W * hb, v);
       tmem_wait_ld();
       reg_fence(v);
       const int off = pc.rec == 0 ? rec_F(kD) : pc.rec == 1 ? rec_G(kD) : rec_H(kD);
@@ -920,9 +888,8 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
 }
 
 // ============================================================================ kernel
-template <bool LN>
-__global__ void __launch_bounds__(kThreads<LN>, 1) walk_kernel(const __grid_constant__ WalkParams p) {
-  constexpr int kEw = 4 * kEpq<LN>;  // E warps
+__global__ void __launch_bounds__(kThreads, 1) walk_kernel(const __grid_constant__ WalkParams p) {
+  constexpr int kEw = 4 * kEpq;  // E warps
   const FwdArgs& a = p.a;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -955,15 +922,9 @@ __global__ void __launch_bounds__(kThreads<LN>, 1) walk_kernel(const __grid_cons
     ms->abort = 0;
     ms->never = 0;
   }
-  if (LN && threadIdx.x < 2 * kD) {  // the head's LayerNorm gain (1 when absent) and bias (0)
-    const int h = bh % a.H, j = threadIdx.x % kD;
-    const float* src = threadIdx.x < kD ? a.ln_w : a.ln_b;
-    reinterpret_cast<float*>(smem + WLay::LNW)[threadIdx.x] =
-        src ? src[(size_t)h * kD + j] : (threadIdx.x < kD ? 1.0f : 0.0f);
-  }
   if (a.rope && threadIdx.x < 32)  // rotary frequencies
     reinterpret_cast<float*>(smem + WLay::THETA)[threadIdx.x] = p.ang[threadIdx.x];
-  if (warp == kMmaWarp<LN>) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ms->tmem, 512);
     tmem_relinquish();
   }
@@ -973,9 +934,9 @@ __global__ void __launch_bounds__(kThreads<LN>, 1) walk_kernel(const __grid_cons
 
   if (warp < kOpWarps) {
     role_op(p, smem, ms, bh, c0, c1);
-  } else if (warp < kMmaWarp<LN>) {
-    role_e<LN>(p, smem, ms, bh, c0, c1);
-  } else if (warp == kMmaWarp<LN>) {
+  } else if (warp < kMmaWarp) {
+    role_e(p, smem, ms, bh, c0, c1);
+  } else if (warp == kMmaWarp) {
     if ((threadIdx.x & 31) == 0) role_mma(p, smem, ms, c0, c1);
   } else if ((threadIdx.x & 31) == 0) {
     role_tma(p, smem, ms, bh, c0, c1);
@@ -983,7 +944,7 @@ __global__ void __launch_bounds__(kThreads<LN>, 1) walk_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp<LN>) {
+  if (warp == kMmaWarp) {
     // every MMA has completed once `fin` fires (it is committed after the last one)
     if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ll)) report(a.status, kErrTimeout);
     tc_fence_after();
@@ -1059,15 +1020,14 @@ int sm_count(int dev) {
   return v;
 }
 
-template <bool LN>
-cudaError_t launch_walk_t(const FwdArgs& a, const float* ang, int nseg_max, cudaStream_t stream) {
+cudaError_t launch_walk(const FwdArgs& a, const float* ang, int nseg_max, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_set{0};  // bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(walk_kernel<LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)WLay::BYTES);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
@@ -1109,7 +1069,7 @@ cudaError_t launch_walk_t(const FwdArgs& a, const float* ang, int nseg_max, cuda
   for (int j = S + 1; j <= kMaxSeg; ++j) p.seg_start[j] = nch;
   const long long ctas = (long long)BH * S;
   if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
-  walk_kernel<LN><<<(unsigned)ctas, kThreads<LN>, WLay::BYTES, stream>>>(p);
+  walk_kernel<<<(unsigned)ctas, kThreads, WLay::BYTES, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -1136,9 +1096,9 @@ cudaError_t launch_walk_angles(float* tab, int N, double base, cudaStream_t stre
 
 cudaError_t launch_fwd_walk(const FwdArgs& a, const float* ang, int nseg_max,
                             cudaStream_t stream) {
-  if (!a.scal || !a.smax || (a.rope && !ang)) return cudaErrorInvalidValue;
-  return a.ln ? launch_walk_t<true>(a, ang, nseg_max, stream)
-              : launch_walk_t<false>(a, ang, nseg_max, stream);
+  // (the fused output LayerNorm runs on the chunked kernel of zs_chunk.cu)
+  if (!a.scal || !a.smax || (a.rope && !ang) || a.ln) return cudaErrorInvalidValue;
+  return launch_walk(a, ang, nseg_max, stream);
 }
 
 }  // namespace zs
