@@ -326,7 +326,9 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
 // The three terms nearly cancel (the weights sum to zero), so e o v, s o v and the states are
 // each split into bf16 hi and lo parts (two products accumulated into one TMEM tile): only
 // k_hat, q_hat and v, which the three terms share, are rounded to bf16 once.
-// Each token's logit is recomputed where it is needed (three light passes over u).
+// Each token's logit is computed in one pass over u (the maximum, P and E~ together) and kept
+// in shared memory for the state tiles when the sequence has at most 4096 tokens (recomputed
+// otherwise).
 constexpr int kTcThreads = 128, kTcT = 128, kTcNMax = 1 << 20;
 constexpr uint32_t kAtom = 128 * 128;  // [128 rows x 64 bf16], 128-byte swizzle
 
@@ -341,8 +343,11 @@ struct EncTcSmem {
   static constexpr uint32_t BLO = BHI + 192 * 128;
   static_assert(BLO + 192 * 128 <= KQ, "the state tiles overlay the value atoms only");
   static constexpr uint32_t RED = 6 * kAtom;              // float [2][kD] + misc
-  static constexpr uint32_t BAR = RED + (2 * kD + 8) * 4; // mbarrier, TMEM address
-  static constexpr uint32_t BYTES = BAR + 64;
+  static constexpr uint32_t BAR = RED + (2 * kD + 12) * 4; // mbarrier, TMEM address
+  // the logits of the first pass, kept for the state tiles when the sequence fits
+  static constexpr int kSlogMax = 4096;
+  static constexpr uint32_t SLOG = BAR + 64;
+  static constexpr uint32_t BYTES = SLOG + kSlogMax * 4;
   static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
@@ -435,19 +440,59 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
-  // ---- prior numerator: column j summed by threads j and j + 64 over alternate tokens ----
+  // ---- prior numerator: thread (p, g) sums columns 8 g .. 8 g + 7 over the tokens p, p + 16,
+  //      ... with 16-byte loads (four rows in flight); the 16 partial sums of a column are then
+  //      added by one thread (the q_hat atom, not used yet, holds them) ----
   {
-    const int j = tid & (kD - 1), g = tid >> 6;
-    float su = 0.0f;
-    for (int t = g; t < N; t += 2) su += __bfloat162float(u[(size_t)t * kD + j]);
-    red[g * kD + j] = su;
+    const int g = tid & 7, p = tid >> 3;
+    float su[8];
+#pragma unroll
+    for (int y = 0; y < 8; ++y) su[y] = 0.0f;
+    const uint4* ur = reinterpret_cast<const uint4*>(u) + g;
+    int t = p;
+    for (; t + 48 < N; t += 64) {
+      uint4 w[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) w[r] = ur[(size_t)(t + 16 * r) * (kD / 8)];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t wv[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          float lo, hi;
+          unpack_bf16x2(wv[y], lo, hi);
+          su[2 * y] += lo;
+          su[2 * y + 1] += hi;
+        }
+      }
+    }
+    for (; t < N; t += 16) {
+      const uint4 w = ur[(size_t)t * (kD / 8)];
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        float lo, hi;
+        unpack_bf16x2(wv[y], lo, hi);
+        su[2 * y] += lo;
+        su[2 * y + 1] += hi;
+      }
+    }
+    float* part = reinterpret_cast<float*>(smem + SM::KQ);  // [16][kD]
+#pragma unroll
+    for (int y = 0; y < 8; ++y) part[p * kD + 8 * g + y] = su[y];
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
   const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lane quadrant
-  if (tid < kD) red[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], red[tid] + red[kD + tid]);
+  if (tid < kD) {
+    const float* part = reinterpret_cast<const float*>(smem + SM::KQ);
+    float su = 0.0f;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) su += part[p * kD + tid];
+    red[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], su);
+  }
   __syncthreads();
   const float den = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)kD));
   // logit of token t: s = -(u_t . n) / ((e^tau + N) sqrt d)
@@ -459,34 +504,42 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     for (int i = 0; i < 64; ++i) dot = __fmaf_rn(x[i], red[i], dot);
     return -__fdiv_rn(dot, den);
   };
-  // ---- maximum logit and P (thread per token), then E~ ----
-  float lmax = -INFINITY, lsum = 0.0f;
+  // ---- maximum logit m, P and E~ = sum e^{s - m} in one pass (thread per token): each thread
+  //      keeps its exponential sum relative to its own running maximum, and the partial sums
+  //      are rescaled to the common maximum when they are combined ----
+  float lmax = -INFINITY, lsum = 0.0f, lexp = 0.0f;
+  float* slog = reinterpret_cast<float*>(smem + SM::SLOG);
+  const bool keep = N <= SM::kSlogMax;  // (each thread reads back only its own tokens)
   for (int t = tid; t < N; t += kTcThreads) {
     const float s = logit(t);
-    lmax = fmaxf(lmax, s);
+    if (keep) slog[t] = s;
+    const float mn = fmaxf(lmax, s);
+    lexp = __fmaf_rn(lexp, expf(__fsub_rn(lmax, mn)), expf(__fsub_rn(s, mn)));
+    lmax = mn;
     lsum += s;
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
-    lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    const float om = __shfl_xor_sync(0xffffffffu, lmax, o);
+    const float oe = __shfl_xor_sync(0xffffffffu, lexp, o);
+    const float mn = fmaxf(lmax, om);
+    lexp = mn == -INFINITY ? 0.0f
+                           : __fmaf_rn(lexp, expf(__fsub_rn(lmax, mn)), oe * expf(__fsub_rn(om, mn)));
+    lmax = mn;
     lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
   }
   if ((tid & 31) == 0) {
     red[2 * kD + warp] = lmax;
     red[2 * kD + 4 + warp] = lsum;
+    red[2 * kD + 8 + warp] = lexp;
   }
   __syncthreads();
   const float m = fmaxf(fmaxf(red[2 * kD], red[2 * kD + 1]), fmaxf(red[2 * kD + 2], red[2 * kD + 3]));
   const float P = (red[2 * kD + 4] + red[2 * kD + 5]) + (red[2 * kD + 6] + red[2 * kD + 7]);
   if (!isfinite(m)) report(a.status, kErrRange);
-  float esum = 0.0f;
-  for (int t = tid; t < N; t += kTcThreads) esum += expf(__fsub_rn(logit(t), m));
+  float Et = 0.0f;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) esum += __shfl_xor_sync(0xffffffffu, esum, o);
-  __syncthreads();  // everyone has read the maxima and sums above
-  if ((tid & 31) == 0) red[2 * kD + warp] = esum;
-  __syncthreads();
-  const float Et = (red[2 * kD] + red[2 * kD + 1]) + (red[2 * kD + 2] + red[2 * kD + 3]);
+  for (int w = 0; w < 4; ++w) Et += red[2 * kD + 8 + w] * expf(__fsub_rn(red[2 * kD + w], m));
 
   // ---- states over the token tiles ----
   constexpr uint32_t id_st = idesc_bf16_f32(128, kD, true, true);
@@ -503,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     put_row_bf16(smem + SM::KQ, tid, x);
     get_row_bf16(v + (size_t)t * kD, valid, x);
     put_row_bf16(smem + SM::AV, tid, x);
-    const float s = valid ? logit(t) : 0.0f;
+    const float s = valid ? (keep ? slog[t] : logit(t)) : 0.0f;
     const float e = valid ? expf(__fsub_rn(s, m)) : 0.0f;
     put_row_split(smem + SM::EVH, smem + SM::EVL, tid, e, x);
     put_row_split(smem + SM::SVH, smem + SM::SVL, tid, s, x);
