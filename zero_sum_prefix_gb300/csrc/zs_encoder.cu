@@ -316,7 +316,9 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
 
 // ============================================================== tensor-core encoder (bf16)
 // The same computation with both contractions on tcgen05 (bf16 operands, fp32 accumulation in
-// TMEM), one CTA of 128 threads per sequence, thread = token row of a 128-token tile:
+// TMEM), one CTA of 256 threads per sequence.  Tiles of 128 tokens; token row r of a tile is
+// TMEM lane r, handled by two threads (warps w and w + 4 share lane quadrant w & 3), each
+// holding half of the row's columns:
 //   states:  D1 = [e o v | s o v]^T K_hat  (M = 128: rows 0..63 = F~^T, 64..127 = G^T),
 //            D2 = [v | e o v]^T K_hat       (rows 0..63 = H^T; the rest unused),
 //            accumulated over the token tiles (A operands MN-major from the swizzled value
@@ -326,10 +328,14 @@ __global__ void __launch_bounds__(kNT, 2) enc_kernel(FwdArgs a) {
 // The three terms nearly cancel (the weights sum to zero), so e o v, s o v and the states are
 // each split into bf16 hi and lo parts (two products accumulated into one TMEM tile): only
 // k_hat, q_hat and v, which the three terms share, are rounded to bf16 once.
+// For q and k a thread takes the rotary pairs 16 hf .. 16 hf + 15 of its row (columns
+// 16 hf + i and 32 + 16 hf + i), so that each rotation stays in one thread; the row's squared
+// norm is the sum of the two halves (exchanged through shared memory).  For the states and the
+// outputs it takes the contiguous columns 32 hf .. 32 hf + 31.
 // Each token's logit is computed in one pass over u (the maximum, P and E~ together) and kept
-// in shared memory for the state tiles when the sequence has at most 4096 tokens (recomputed
+// in shared memory for the state tiles when the sequence has at most 2048 tokens (recomputed
 // otherwise).
-constexpr int kTcThreads = 128, kTcT = 128, kTcNMax = 1 << 20;
+constexpr int kTcThreads = 256, kTcT = 128, kTcNMax = 1 << 20;
 constexpr uint32_t kAtom = 128 * 128;  // [128 rows x 64 bf16], 128-byte swizzle
 
 struct EncTcSmem {
@@ -342,29 +348,56 @@ struct EncTcSmem {
   static constexpr uint32_t BHI = 0;
   static constexpr uint32_t BLO = BHI + 192 * 128;
   static_assert(BLO + 192 * 128 <= KQ, "the state tiles overlay the value atoms only");
-  static constexpr uint32_t RED = 6 * kAtom;              // float [2][kD] + misc
-  static constexpr uint32_t BAR = RED + (2 * kD + 12) * 4; // mbarrier, TMEM address
+  // float [kD] prior numerator, then per warp: maximum, logit sum, exponential sum ([8] each)
+  static constexpr uint32_t RED = 6 * kAtom;
+  static constexpr uint32_t NRM = RED + (kD + 24) * 4;   // float [2][128]: half squared norms
+  static constexpr uint32_t LNX = NRM + 2 * kTcT * 4;     // float2 [2][128]: half (mean, M2)
+  static constexpr uint32_t BAR = LNX + 2 * kTcT * 8;     // mbarrier, TMEM address, abort flag
   // the logits of the first pass, kept for the state tiles when the sequence fits
-  static constexpr int kSlogMax = 4096;
+  static constexpr int kSlogMax = 2048;
   static constexpr uint32_t SLOG = BAR + 64;
   static constexpr uint32_t BYTES = SLOG + kSlogMax * 4;
   static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
+  static_assert(BAR % 8 == 0, "mbarrier alignment");
 };
 
-__device__ __forceinline__ void put_row_bf16(uint8_t* atom, int r, const float (&x)[64]) {
+// The 16-byte chunk of the x-th eighth (0..3) of a thread's rotary-pair columns: chunks 2 hf,
+// 2 hf + 1 (columns 16 hf ..) and 4 + 2 hf, 5 + 2 hf (their partners, + 32).
+__device__ __forceinline__ int pair_chunk(int hf, int x) { return (x < 2 ? 2 * hf : 2 + 2 * hf) + x; }
+
+// The raw bf16 words of this thread's rotary-pair columns of row t (loaded ahead of their use),
+// and their values.
+__device__ __forceinline__ void load_half_pairs(const __nv_bfloat16* row, bool valid, int hf,
+                                                uint4 (&w)[4]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(atom + sw128_off(r, c)) =
+  for (int c = 0; c < 4; ++c)
+    w[c] = valid ? reinterpret_cast<const uint4*>(row)[pair_chunk(hf, c)] : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void unpack_half(const uint4 (&w)[4], float (&x)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    unpack_bf16x2(w[c].x, x[8 * c], x[8 * c + 1]);
+    unpack_bf16x2(w[c].y, x[8 * c + 2], x[8 * c + 3]);
+    unpack_bf16x2(w[c].z, x[8 * c + 4], x[8 * c + 5]);
+    unpack_bf16x2(w[c].w, x[8 * c + 6], x[8 * c + 7]);
+  }
+}
+
+__device__ __forceinline__ void put_half_pairs(uint8_t* atom, int r, int hf, const float (&x)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(atom + sw128_off(r, pair_chunk(hf, c))) =
         make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
                    pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
 }
 
-// Row r of scale * x as the bf16 pair (hi, lo) with hi + lo = scale * x to about 2^-17: the
-// three state terms nearly cancel (the weights sum to zero), so each is kept to fp32 accuracy.
-__device__ __forceinline__ void put_row_split(uint8_t* hi_atom, uint8_t* lo_atom, int r,
-                                              float scale, const float (&x)[64]) {
+// scale * x as the bf16 pair (hi, lo) with hi + lo = scale * x to about 2^-17 (the three state
+// terms nearly cancel, so each is kept to fp32 accuracy), into the chunks chunk(c) of row r.
+template <typename ChunkOf>
+__device__ __forceinline__ void put_split(uint8_t* hi_atom, uint8_t* lo_atom, int r, float scale,
+                                          const float (&x)[32], ChunkOf chunk) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < 4; ++c) {
     uint32_t ph[4], pl[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -374,40 +407,27 @@ __device__ __forceinline__ void put_row_split(uint8_t* hi_atom, uint8_t* lo_atom
       ph[e] = pack_bf16x2(h0, h1);
       pl[e] = pack_bf16x2(y0 - h0, y1 - h1);
     }
-    *reinterpret_cast<uint4*>(hi_atom + sw128_off(r, c)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-    *reinterpret_cast<uint4*>(lo_atom + sw128_off(r, c)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+    *reinterpret_cast<uint4*>(hi_atom + sw128_off(r, chunk(c))) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4*>(lo_atom + sw128_off(r, chunk(c))) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
 }
 
-// Row t of a bf16 tensor (64 values) into x; zero when t is past the sequence.
-__device__ __forceinline__ void get_row_bf16(const __nv_bfloat16* src, bool valid, float (&x)[64]) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) w = reinterpret_cast<const uint4*>(src)[c];
-    unpack_bf16x2(w.x, x[8 * c], x[8 * c + 1]);
-    unpack_bf16x2(w.y, x[8 * c + 2], x[8 * c + 3]);
-    unpack_bf16x2(w.z, x[8 * c + 4], x[8 * c + 5]);
-    unpack_bf16x2(w.w, x[8 * c + 6], x[8 * c + 7]);
-  }
-}
-
-// Unit row (rotated to position t with rope; pairs (a, a + 32) are both in this thread).
-__device__ __forceinline__ void unit_rot_row(const FwdArgs& a, int t, bool valid, float (&x)[64]) {
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 64; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+// Unit rotated half row: x scaled by 1 / max(|row|, 1e-12) (ss = the row's squared norm), then
+// each of the thread's rotary pairs (x[i], x[16 + i]) = columns (16 hf + i, 32 + 16 hf + i)
+// rotated to position t with rope.
+__device__ __forceinline__ void unit_rot_half(const FwdArgs& a, int t, bool valid, int hf,
+                                              float ss, float (&x)[32]) {
   const float inv = __fdiv_rn(1.0f, fmaxf(__fsqrt_rn(ss), 1e-12f));
 #pragma unroll
-  for (int i = 0; i < 64; ++i) x[i] *= inv;
+  for (int i = 0; i < 32; ++i) x[i] *= inv;
   if (a.rope && valid) {
-    const float2* tab = a.rope_table + (size_t)t * (kD / 2);
+    const float2* tab = a.rope_table + (size_t)t * (kD / 2) + 16 * hf;
 #pragma unroll
-    for (int p = 0; p < 32; ++p) {
-      const float2 cs = tab[p];
-      const float x0 = x[p], x1 = x[p + 32];
-      x[p] = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-      x[p + 32] = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+    for (int i = 0; i < 16; ++i) {
+      const float2 cs = tab[i];
+      const float x0 = x[i], x1 = x[16 + i];
+      x[i] = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+      x[16 + i] = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
     }
   }
 }
@@ -420,11 +440,16 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     return;
   }
   float* red = reinterpret_cast<float*>(smem + SM::RED);
+  float* nrm = reinterpret_cast<float*>(smem + SM::NRM);
+  float2* lnx = reinterpret_cast<float2*>(smem + SM::LNX);
+  float* slog = reinterpret_cast<float*>(smem + SM::SLOG);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + SM::BAR + 8);
   int* abort_flag = reinterpret_cast<int*>(smem + SM::BAR + 12);
   const int bh = blockIdx.x, h = bh % a.H;
   const int N = a.N, tid = threadIdx.x, warp = tid >> 5;
+  const int r = 32 * (warp & 3) + (tid & 31);  // token row of a tile = TMEM lane
+  const int hf = warp >> 2;                    // which half of the row this thread holds
   const size_t row0 = (size_t)bh * N;
   const __nv_bfloat16* __restrict__ q = static_cast<const __nv_bfloat16*>(a.q) + row0 * kD;
   const __nv_bfloat16* __restrict__ k = static_cast<const __nv_bfloat16*>(a.k) + row0 * kD;
@@ -440,8 +465,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
-  // ---- prior numerator: thread (p, g) sums columns 8 g .. 8 g + 7 over the tokens p, p + 16,
-  //      ... with 16-byte loads (four rows in flight); the 16 partial sums of a column are then
+  // the first state tile's k and v words, loaded now: their latency passes under the two
+  // passes over u; every later tile's are loaded while the previous tile's products run
+  uint4 kw[4], vw[4];
+  load_half_pairs(k + (size_t)r * kD, r < N, hf, kw);
+  load_half_pairs(v + (size_t)r * kD, r < N, hf, vw);
+  // ---- prior numerator: thread (p, g) sums columns 8 g .. 8 g + 7 over the tokens p, p + 32,
+  //      ... with 16-byte loads (four rows in flight); the 32 partial sums of a column are then
   //      added by one thread (the q_hat atom, not used yet, holds them) ----
   {
     const int g = tid & 7, p = tid >> 3;
@@ -449,25 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
 #pragma unroll
     for (int y = 0; y < 8; ++y) su[y] = 0.0f;
     const uint4* ur = reinterpret_cast<const uint4*>(u) + g;
-    int t = p;
-    for (; t + 48 < N; t += 64) {
-      uint4 w[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) w[r] = ur[(size_t)(t + 16 * r) * (kD / 8)];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t wv[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          float lo, hi;
-          unpack_bf16x2(wv[y], lo, hi);
-          su[2 * y] += lo;
-          su[2 * y + 1] += hi;
-        }
-      }
-    }
-    for (; t < N; t += 16) {
-      const uint4 w = ur[(size_t)t * (kD / 8)];
+    auto add_row = [&](const uint4& w) {
       const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int y = 0; y < 4; ++y) {
@@ -476,8 +488,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
         su[2 * y] += lo;
         su[2 * y + 1] += hi;
       }
+    };
+    int t = p;
+    for (; t + 96 < N; t += 128) {
+      uint4 w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = ur[(size_t)(t + 32 * i) * (kD / 8)];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) add_row(w[i]);
     }
-    float* part = reinterpret_cast<float*>(smem + SM::KQ);  // [16][kD]
+    for (; t < N; t += 32) add_row(ur[(size_t)t * (kD / 8)]);
+    float* part = reinterpret_cast<float*>(smem + SM::KQ);  // [32][kD]
 #pragma unroll
     for (int y = 0; y < 8; ++y) part[p * kD + 8 * g + y] = su[y];
   }
@@ -485,31 +506,39 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lane quadrant
+  const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quadrant
   if (tid < kD) {
     const float* part = reinterpret_cast<const float*>(smem + SM::KQ);
     float su = 0.0f;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) su += part[p * kD + tid];
+#pragma unroll 8
+    for (int p = 0; p < kTcThreads / 8; ++p) su += part[p * kD + tid];
     red[tid] = __fmaf_rn(etau, a.mu[(size_t)h * kD + tid], su);
   }
   __syncthreads();
   const float den = __fmul_rn(__fadd_rn(etau, (float)N), __fsqrt_rn((float)kD));
   // logit of token t: s = -(u_t . n) / ((e^tau + N) sqrt d)
   auto logit = [&](int t) -> float {
-    float x[64];
-    get_row_bf16(u + (size_t)t * kD, true, x);
+    const uint4* row = reinterpret_cast<const uint4*>(u + (size_t)t * kD);
     float dot = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) dot = __fmaf_rn(x[i], red[i], dot);
+    for (int c = 0; c < 8; ++c) {
+      const uint4 w = row[c];
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        float lo, hi;
+        unpack_bf16x2(wv[y], lo, hi);
+        dot = __fmaf_rn(lo, red[8 * c + 2 * y], dot);
+        dot = __fmaf_rn(hi, red[8 * c + 2 * y + 1], dot);
+      }
+    }
     return -__fdiv_rn(dot, den);
   };
   // ---- maximum logit m, P and E~ = sum e^{s - m} in one pass (thread per token): each thread
   //      keeps its exponential sum relative to its own running maximum, and the partial sums
   //      are rescaled to the common maximum when they are combined ----
+  const bool keep = N <= SM::kSlogMax;
   float lmax = -INFINITY, lsum = 0.0f, lexp = 0.0f;
-  float* slog = reinterpret_cast<float*>(smem + SM::SLOG);
-  const bool keep = N <= SM::kSlogMax;  // (each thread reads back only its own tokens)
   for (int t = tid; t < N; t += kTcThreads) {
     const float s = logit(t);
     if (keep) slog[t] = s;
@@ -529,39 +558,58 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
   }
   if ((tid & 31) == 0) {
-    red[2 * kD + warp] = lmax;
-    red[2 * kD + 4 + warp] = lsum;
-    red[2 * kD + 8 + warp] = lexp;
+    red[kD + warp] = lmax;
+    red[kD + 8 + warp] = lsum;
+    red[kD + 16 + warp] = lexp;
   }
   __syncthreads();
-  const float m = fmaxf(fmaxf(red[2 * kD], red[2 * kD + 1]), fmaxf(red[2 * kD + 2], red[2 * kD + 3]));
-  const float P = (red[2 * kD + 4] + red[2 * kD + 5]) + (red[2 * kD + 6] + red[2 * kD + 7]);
+  float m = -INFINITY, P = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    m = fmaxf(m, red[kD + w]);
+    P += red[kD + 8 + w];
+  }
   if (!isfinite(m)) report(a.status, kErrRange);
   float Et = 0.0f;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) Et += red[2 * kD + 8 + w] * expf(__fsub_rn(red[2 * kD + w], m));
+  for (int w = 0; w < 8; ++w) Et += red[kD + 16 + w] * expf(__fsub_rn(red[kD + w], m));
 
   // ---- states over the token tiles ----
   constexpr uint32_t id_st = idesc_bf16_f32(128, kD, true, true);
   const uint32_t base = smem_u32(smem);
   const int NT = (N + kTcT - 1) / kTcT;
+  auto pc = [hf](int c) { return pair_chunk(hf, c); };
   uint32_t phase = 0;
   bool ok = true;
   for (int tt = 0; tt < NT && ok; ++tt) {
-    const int t = tt * kTcT + tid;
+    const int t = tt * kTcT + r;
     const bool valid = t < N;
-    float x[64];
-    get_row_bf16(k + (size_t)t * kD, valid, x);
-    unit_rot_row(a, t, valid, x);
-    put_row_bf16(smem + SM::KQ, tid, x);
-    get_row_bf16(v + (size_t)t * kD, valid, x);
-    put_row_bf16(smem + SM::AV, tid, x);
+    float x[32];
+    unpack_half(kw, x);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+    nrm[hf * kTcT + r] = ss;
+    __syncthreads();
+    unit_rot_half(a, t, valid, hf, nrm[r] + nrm[kTcT + r], x);
+    put_half_pairs(smem + SM::KQ, r, hf, x);
+    unpack_half(vw, x);
+    put_half_pairs(smem + SM::AV, r, hf, x);
     const float s = valid ? (keep ? slog[t] : logit(t)) : 0.0f;
     const float e = valid ? expf(__fsub_rn(s, m)) : 0.0f;
-    put_row_split(smem + SM::EVH, smem + SM::EVL, tid, e, x);
-    put_row_split(smem + SM::SVH, smem + SM::SVL, tid, s, x);
+    put_split(smem + SM::EVH, smem + SM::EVL, r, e, x, pc);
+    put_split(smem + SM::SVH, smem + SM::SVL, r, s, x, pc);
     fence_proxy_async_smem();
     __syncthreads();
+    {  // the next tile's k and v (or the first q tile's words, after the last state tile)
+      const int tn = t + kTcT;
+      if (tt + 1 < NT) {
+        load_half_pairs(k + (size_t)tn * kD, tn < N, hf, kw);
+        load_half_pairs(v + (size_t)tn * kD, tn < N, hf, vw);
+      } else {
+        load_half_pairs(q + (size_t)r * kD, r < N, hf, kw);
+      }
+    }
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -582,31 +630,39 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
   }
   if (!ok) report(a.status, kErrTimeout);
 
-  // ---- states -> K-major bf16 hi/lo tiles: rows 0..63 F~, 64..127 G (D1), 128..191 H (D2) ----
+  // ---- states -> K-major bf16 hi/lo tiles: rows 0..63 F~, 64..127 G (D1), 128..191 H (D2);
+  //      this thread copies key columns 32 hf .. 32 hf + 31 of its lane's rows ----
   if (ok) {
-    float x[64];
-    tmem_ld32(tl + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-    tmem_ld32(tl + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-    put_row_split(smem + SM::BHI, smem + SM::BLO, tid, 1.0f, x);
-    tmem_ld32(tl + 64, *reinterpret_cast<float(*)[32]>(&x[0]));
-    tmem_ld32(tl + 96, *reinterpret_cast<float(*)[32]>(&x[32]));
-    if (tid < kD) put_row_split(smem + SM::BHI, smem + SM::BLO, 128 + tid, 1.0f, x);
+    auto cc = [hf](int c) { return 4 * hf + c; };
+    float x[32];
+    tmem_ld32(tl + 32 * hf, x);
+    put_split(smem + SM::BHI, smem + SM::BLO, r, 1.0f, x, cc);
+    if ((warp & 3) < 2) {  // lanes 0..63 of D2 (warp-uniform)
+      tmem_ld32(tl + 64 + 32 * hf, x);
+      put_split(smem + SM::BHI, smem + SM::BLO, 128 + r, 1.0f, x, cc);
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- outputs per token tile: D3 = Q_hat [F~|G|H], combined with the row coefficients ----
+  // ---- outputs per token tile: D3 = Q_hat [F~|G|H], combined with the row coefficients; this
+  //      thread writes output columns 32 hf .. 32 hf + 31 of its row ----
   constexpr uint32_t id_out = idesc_bf16_f32(128, 3 * kD, false, false);
   const float rN = __fdiv_rn(1.0f, (float)N);
   for (int tt = 0; tt < NT && ok; ++tt) {
-    const int t = tt * kTcT + tid;
+    const int t = tt * kTcT + r;
     const bool valid = t < N;
-    float x[64];
-    get_row_bf16(q + (size_t)t * kD, valid, x);
-    unit_rot_row(a, t, valid, x);
-    put_row_bf16(smem + SM::KQ, tid, x);
+    float x[32];
+    unpack_half(kw, x);  // this tile's q words
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss = __fmaf_rn(x[i], x[i], ss);
+    nrm[hf * kTcT + r] = ss;
+    __syncthreads();
+    unit_rot_half(a, t, valid, hf, nrm[r] + nrm[kTcT + r], x);
+    put_half_pairs(smem + SM::KQ, r, hf, x);
     float al = 0.0f, be = 0.0f, ga = 0.0f;
     if (valid) {
       const size_t row = row0 + t;
@@ -618,6 +674,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     }
     fence_proxy_async_smem();
     __syncthreads();
+    if (tt + 1 < NT) {  // the next tile's q words, while this tile's product runs
+      const int tn = t + kTcT;
+      load_half_pairs(q + (size_t)tn * kD, tn < N, hf, kw);
+    }
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -634,37 +694,45 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
     tc_fence_after();
     ok = __syncthreads_and(ok) != 0;  // uniform before the aligned TMEM loads
     if (!ok) break;
-    float o[64];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    float o[32];
+    {
       float f[32], g2[32], hh[32];
-      tmem_ld32(tl + 32 * half, f);
-      tmem_ld32(tl + 64 + 32 * half, g2);
-      tmem_ld32(tl + 128 + 32 * half, hh);
+      tmem_ld32(tl + 32 * hf, f);
+      tmem_ld32(tl + 64 + 32 * hf, g2);
+      tmem_ld32(tl + 128 + 32 * hf, hh);
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        o[32 * half + j] = __fmaf_rn(al, f[j], __fmaf_rn(be, g2[j], __fmul_rn(ga, hh[j])));
+        o[j] = __fmaf_rn(al, f[j], __fmaf_rn(be, g2[j], __fmul_rn(ga, hh[j])));
     }
-    if (a.ln) {  // output LayerNorm over the row (the whole row is in this thread)
+    if (a.ln) {
+      // output LayerNorm over the row: each half's mean and M2 over its 32 columns, merged
+      // with the other half's (pairwise update for equal counts, half 0 first)
       float mean = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) mean += o[j];
-      mean *= (1.0f / kD);
-      float var = 0.0f;
+      for (int j = 0; j < 32; ++j) mean += o[j];
+      mean *= (1.0f / 32.0f);
+      float m2 = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) var = __fmaf_rn(o[j] - mean, o[j] - mean, var);
-      const float rstd = rsqrtf(var * (1.0f / kD) + a.ln_eps);
+      for (int j = 0; j < 32; ++j) m2 = __fmaf_rn(o[j] - mean, o[j] - mean, m2);
+      lnx[hf * kTcT + r] = make_float2(mean, m2);
+      __syncthreads();
+      const float2 h0 = lnx[r], h1 = lnx[kTcT + r];
+      const float dlt = h1.x - h0.x;
+      const float mu_r = 0.5f * (h0.x + h1.x);
+      const float var = (h0.y + h1.y + dlt * dlt * 16.0f) * (1.0f / kD);
+      const float rstd = rsqrtf(var + a.ln_eps);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float w = a.ln_w ? a.ln_w[(size_t)h * kD + j] : 1.0f;
-        const float b = a.ln_b ? a.ln_b[(size_t)h * kD + j] : 0.0f;
-        o[j] = __fmaf_rn((o[j] - mean) * rstd, w, b);
+      for (int j = 0; j < 32; ++j) {
+        const int col = 32 * hf + j;
+        const float w = a.ln_w ? a.ln_w[(size_t)h * kD + col] : 1.0f;
+        const float b = a.ln_b ? a.ln_b[(size_t)h * kD + col] : 0.0f;
+        o[j] = __fmaf_rn((o[j] - mu_r) * rstd, w, b);
       }
     }
     if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)t * kD);
+      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)t * kD) + 4 * hf;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
+      for (int c = 0; c < 4; ++c)
         dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
                             pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
                             pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
