@@ -1023,7 +1023,8 @@ bool chunk_supported(int d, int dtype, int causal) {
 
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream) {
   if (!a.scal) return cudaErrorInvalidValue;
-  if (a.d == 64) return a.ln ? launch_d<64, true>(a, stream) : launch_d<64, false>(a, stream);
+  // at d = 64 only the fused-LayerNorm forward runs here (the plain one is the walk kernel's)
+  if (a.d == 64) return a.ln ? launch_d<64, true>(a, stream) : cudaErrorInvalidValue;
   if (a.d == 128) return a.ln ? launch_d<128, true>(a, stream) : launch_d<128, false>(a, stream);
   return cudaErrorInvalidValue;
 }

@@ -84,8 +84,9 @@ constexpr size_t kNoAllocRopeEntries = size_t(1) << 17;
 // Device address of that scratch on the current device (looked up on every call).
 cudaError_t noalloc_rope_table(float2** table);
 
-// zs_chunk.cu: the chunked forward (d in {64, 128}, bf16, causal).  a.scal must hold the
-// per-token scalars (launch_fwd_scalars on the same stream first).
+// zs_chunk.cu: the chunked forward (bf16, causal; d = 128, and d = 64 with the fused output
+// LayerNorm).  a.scal must hold the per-token scalars (launch_fwd_scalars on the same stream
+// first).  chunk_supported tells whether the chunked path (this kernel or zs_walk.cu) exists.
 bool chunk_supported(int d, int dtype, int causal);
 cudaError_t launch_fwd_chunk(const FwdArgs& a, cudaStream_t stream);
 
