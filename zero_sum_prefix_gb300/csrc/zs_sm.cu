@@ -480,6 +480,502 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
   }
 }
 
+// ============================================================================ one-pass, d = 64
+// Expanding the weights per query row, o_t = alpha_t A_t + beta_t B_t + gamma_t C_t with
+//   A_t = sum_i 2^{c2 x_{t,i} - m_t} v_i,   B_t = sum_i x_{t,i} v_i / sqrt d,   C_t = sum_i v_i
+// (i over the row's keys, x the raw logit q k^T, c2 = log2(e) / sqrt d, m_t a reference in
+// base-2 units), and alpha_t = sigh_t / l_t with l_t = sum_i 2^{c2 x - m}, beta_t and gamma_t as
+// above with P_t = sum_i x_{t,i} / sqrt d.  So one pass over the key tiles suffices: S = Q K^T
+// once per tile; P = 2^{c2 x - m} and x itself rounded to bf16 and written over S's own fp32
+// columns (piece h of 16 keys: P in columns 16 h .. 16 h + 7, x in 16 h + 8 .. 16 h + 15); then
+// A += P V and [B | P_t] += X [V | 1].  The second product runs with N = 80 over V and a
+// constant tile whose first column is 1, so the logit sum P_t is the sum of the very bf16 values
+// that B sums: the weights alpha P + beta x / sqrt d + gamma of a row then sum to sig0 up to the
+// fp32 rounding of the sums (exactly zero output for a single visible key), and the roundings
+// only perturb each weight.  C does not depend on the query: the column sums of the key tiles
+// before the diagonal one are added up on the CUDA cores by two otherwise idle warps, and the
+// diagonal tile's prefix comes from one product with a lower-triangular ones tile at the end.
+// The two epilogue warpgroups take the even and odd key tiles, each with its own A accumulator
+// and its own reference m; m is raised only when a 32-key chunk would give P > 2^32 (the first
+// chunk of a warpgroup sets it), in which case the warpgroup's A rows, its exp-sum and the P
+// already written for the tile are rescaled (the previous P V product of the warpgroup has
+// completed by then: the commit that signalled this tile's S covers it).  At the end the two
+// halves are merged with their reference maxima.
+// TMEM (512 columns): S0, S1 (128 each), A0, A1 (64 each), [B | P_t] (80).
+struct Sm1Cfg {
+  static constexpr int NS = 4;                             // K/V stages
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t STAGE_OFF = Q_OFF + kAtom;
+  static constexpr uint32_t STAGE = 2 * kAtom;             // K then V
+  static constexpr uint32_t TRI_OFF = STAGE_OFF + NS * STAGE;  // [128 x 128] lower-triangular ones
+  static constexpr uint32_t ONE_OFF = TRI_OFF + 2 * kAtom;     // V's 65th column (1) and zeros
+  static constexpr uint32_t STAT_OFF = ONE_OFF + kAtom;        // float2 [2][128]
+  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 8;  // float [8][64] partial sums
+  static constexpr uint32_t CBASE_OFF = CSUM_OFF + 8 * 64 * 4; // float [64]
+  static constexpr uint32_t MISC_OFF = CBASE_OFF + 64 * 4;
+  static constexpr uint32_t BYTES = MISC_OFF + 256;
+  static_assert(BYTES <= 232448, "shared memory budget of one CTA");
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_A0 = 256, TM_A1 = 320, TM_B = 384;
+  static constexpr int kGuard = 32;  // P stays below 2^kGuard
+};
+
+struct Sm1Misc {
+  uint64_t q_full;
+  uint64_t kv_full[4], kv_empty[4];
+  uint64_t s_full[2], w_full[2];
+  uint64_t o_full, fin, cb_full;
+  uint32_t tmem;
+  int abort;
+  int never;
+};
+static_assert(sizeof(Sm1Misc) <= 256, "Sm1Misc fits its slot");
+
+__device__ void sm1_producer(const SmParams& p, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J) {
+  using CF = Sm1Cfg;
+  const uint32_t base = smem_u32(smem);
+  mbar_arrive_expect_tx(&ms->q_full, kAtom);
+  tma_load_3d(base + CF::Q_OFF, &p.tq, 0, qt * kT, bh, &ms->q_full);
+  for (int g = 0; g < J; ++g) {
+    const int st = g % CF::NS;
+    if (g >= CF::NS && !mbar_wait(&ms->kv_empty[st], ((g / CF::NS) - 1) & 1, &ms->abort)) {
+      report(p.a.status, kErrTimeout);
+      ms->abort = 1;
+      return;
+    }
+    const uint32_t kt = base + CF::STAGE_OFF + st * CF::STAGE;
+    mbar_arrive_expect_tx(&ms->kv_full[st], 2 * kAtom);
+    tma_load_3d(kt, &p.tk, 0, g * kT, bh, &ms->kv_full[st]);
+    tma_load_3d(kt + kAtom, &p.tv, 0, g * kT, bh, &ms->kv_full[st]);
+  }
+}
+
+// Per key tile g, in issue order: S_g = Q K_g^T (into S_{g & 1}); then the products of tile
+// g - 1 once its P and x are written: A_{(g-1) & 1} += P V, [B | P_t] += X [V | 1].  The
+// tensor-core operations of one thread run in order, so S_{g+2} overwrites S_g only after tile
+// g's products have read it.  Descriptors advance by plain additions (16 key rows of an
+// MN-major tile = 2048 bytes = 128 descriptor units), keeping the issue loop short.
+__device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
+  using CF = Sm1Cfg;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t tm = ms->tmem;
+  constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
+  constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);    // A += P V, C = T V
+  constexpr uint32_t id_xv = idesc_bf16_f32(128, 80, false, true);    // [B | P_t] += X [V | 1]
+  const uint64_t qd = sw128_desc(base + CF::Q_OFF, 16, 1024);
+  auto products = [&](int g) -> bool {
+    const int b = g & 1, st = g % CF::NS;
+    if (!mbar_wait(&ms->w_full[b], (g >> 1) & 1, &ms->abort)) return false;
+    tc_fence_after();
+    const uint32_t vt = base + CF::STAGE_OFF + st * CF::STAGE + kAtom;
+    // one descriptor for both products: the second 64-column atom (N = 64 .. 79) is the
+    // constant tile, at a fixed distance from this stage's V
+    const uint64_t vd = sw128_desc(vt, base + CF::ONE_OFF - vt, 1024);
+    const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
+    const uint32_t ta = tm + (b ? CF::TM_A1 : CF::TM_A0);
+    const uint32_t acc_a = g >= 2 ? 1u : 0u, acc_b = g >= 1 ? 1u : 0u;
+    mma_f16kind_ts(ta, ts, vd, id_pv, acc_a);
+    mma_f16kind_ts(tm + CF::TM_B, ts + 8, vd, id_xv, acc_b);
+#pragma unroll
+    for (int kk = 1; kk < kT / 16; ++kk) {
+      mma_f16kind_ts(ta, ts + 16 * kk, vd + 128 * kk, id_pv, 1u);
+      mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_xv, 1u);
+    }
+    if (a.causal && g == J - 1) {
+      // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V,
+      // into the other S buffer (its last tile's products were issued before these)
+      const uint32_t tc = tm + (b ? CF::TM_S0 : CF::TM_S1);
+      const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        mma_f16kind(tc, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4), vd + 128 * kk,
+                    id_pv, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&ms->kv_empty[st]);
+    return true;
+  };
+  bool ok = mbar_wait(&ms->q_full, 0, &ms->abort);
+  for (int g = 0; g < J && ok; ++g) {
+    const int st = g % CF::NS, b = g & 1;
+    ok = mbar_wait(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const uint64_t kd = sw128_desc(base + CF::STAGE_OFF + st * CF::STAGE, 16, 1024);
+    const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
+    mma_f16kind(ts, qd, kd, id_qk, 0u);
+#pragma unroll
+    for (int kk = 1; kk < 4; ++kk) mma_f16kind(ts, qd + 2 * kk, kd + 2 * kk, id_qk, 1u);
+    mma_commit(&ms->s_full[b]);
+    if (g >= 1) ok = products(g - 1);
+  }
+  if (ok && J > 0) ok = products(J - 1);
+  if (ok) mma_commit(&ms->o_full);
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+  }
+  mma_commit(&ms->fin);
+}
+
+// Warps 2 and 3: the column sums of V over the key tiles before the diagonal one (all tiles in
+// encoder mode), C's part that is the same for every row.  Thread (rg, cg) adds rows
+// 16 rg .. 16 rg + 15, columns 8 cg .. 8 cg + 7 of each tile; each stage is released once both
+// warps and the tensor cores are done with it.
+__device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
+  using CF = Sm1Cfg;
+  const int t = threadIdx.x - 64, cg = t & 7, rg = t >> 3;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  bool ok = true;
+  for (int g = 0; g < J && ok; ++g) {
+    const int st = g % CF::NS;
+    ok = mbar_wait_warp(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort);
+    if (!ok) break;
+    if (!a.causal || g < J - 1) {
+      const uint32_t vt = smem_u32(smem) + CF::STAGE_OFF + st * CF::STAGE + kAtom;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * rg + i;
+        const uint4 w = lds128(vt + sw128_off(r, cg));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          float lo, hi;
+          unpack_bf16x2(wv[y], lo, hi);
+          acc[2 * y] += lo;
+          acc[2 * y + 1] += hi;
+        }
+      }
+    }
+    __syncwarp();
+    if ((t & 31) == 0) mbar_arrive(&ms->kv_empty[st]);
+  }
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+  }
+  float* part = reinterpret_cast<float*>(smem + CF::CSUM_OFF);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[rg * 64 + 8 * cg + j] = acc[j];
+  named_bar_sync(2, 64);
+  float s = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) s += part[q * 64 + t];
+  reinterpret_cast<float*>(smem + CF::CBASE_OFF)[t] = s;
+  named_bar_sync(2, 64);
+  if (t == 0) mbar_arrive(&ms->cb_full);
+}
+
+// Warpgroup w (0 or 1) handles the key tiles of parity w; thread = query row of the tile.
+__device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J,
+                             int w) {
+  using CF = Sm1Cfg;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int r = wq * 32 + (threadIdx.x & 31);
+  const uint32_t tl = ms->tmem + ((uint32_t)(wq * 32) << 16);
+  const uint32_t ts = tl + (w ? CF::TM_S1 : CF::TM_S0);
+  const uint32_t ta = tl + (w ? CF::TM_A1 : CF::TM_A0);
+  const int t = qt * kT + r;                      // query index (0-based)
+  const bool row_ok = t < a.N;
+  const size_t row = (size_t)bh * a.N + t;
+  const int lim = a.causal ? t : a.N - 1;         // last key of this query
+  // last key visible to every row of this warp (uniform, as the aligned TMEM accesses require)
+  const int lim_warp = a.causal ? qt * kT + wq * 32 : a.N - 1;
+  const float tc = a.causal ? (float)(t + 1) : (float)a.N;
+  constexpr float inv_sqrt_d = 0.125f;                      // d = 64
+  constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
+  float m2 = -INFINITY, l = 0.0f;  // reference (base-2 units) and exp-sum of this warpgroup
+  bool ok = true;
+  int n = 0;                       // this warpgroup's tile count
+  for (int g = w; g < J && ok; g += 2, ++n) {
+    ok = mbar_wait_warp(&ms->s_full[w], n & 1, &ms->abort);
+    if (!ok) break;
+    tc_fence_after();
+    const int k0 = g * kT;
+    const bool full = k0 + kT - 1 <= lim_warp;
+    // one 32-key chunk, first half: its maximum decides whether the reference must rise before
+    // the chunk's P is formed (no TMEM load is in flight here)
+    auto chunk_max = [&](const uint32_t (&rv)[32], const int ch) {
+      float cm = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) cm = fmaxf(cm, __uint_as_float(rv[x]));
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x)
+          if (k0 + 32 * ch + x <= lim) cm = fmaxf(cm, __uint_as_float(rv[x]));
+      }
+      const bool raise = cm * c2 > m2 + (float)CF::kGuard;
+      if (__any_sync(0xffffffffu, raise)) {
+        const float mn = raise ? cm * c2 : m2;
+        const float f = (raise && m2 != -INFINITY) ? ex2(m2 - mn) : 1.0f;
+        tmem_wait_st();  // this tile's earlier P must have landed before it is read back
+#pragma unroll 1
+        for (int pc = 0; pc < 2 * ch; ++pc) {  // 16-key pieces written so far: P columns
+          uint32_t pw[8];
+          tmem_ld8_nowait(ts + 16 * pc, pw);
+          tmem_wait_ld();
+          reg_fence(pw);
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            float lo, hi;
+            unpack_bf16x2(pw[y], lo, hi);
+            pw[y] = pack_bf16x2(lo * f, hi * f);
+          }
+          tmem_st8_nowait(ts + 16 * pc, pw);
+        }
+        if (n >= 1) {  // the warpgroup's earlier tiles: their products completed before S_g
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            uint32_t av[16];
+            tmem_ld16_nowait(ta + 16 * q, av);
+            tmem_wait_ld();
+            reg_fence(av);
+#pragma unroll
+            for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
+            tmem_st16_nowait(ta + 16 * q, av);
+          }
+        }
+        tmem_wait_st();
+        l *= f;
+        m2 = mn;
+      }
+    };
+    // second half: P = 2^{c2 x - m} and x as bf16 pairs over the chunk's own columns
+    auto chunk_px = [&](const uint32_t (&rv)[32], const int ch) {
+      float2 ls = make_float2(0.0f, 0.0f);
+      if (full) {
+        const float2 c2v = make_float2(c2, c2), nm = make_float2(-m2, -m2);
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          uint32_t pp[8], xp[8];
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            const float2 xv = make_float2(__uint_as_float(rv[16 * hp + 2 * y]),
+                                          __uint_as_float(rv[16 * hp + 2 * y + 1]));
+            const float2 e = __ffma2_rn(xv, c2v, nm);
+            const float2 pe = make_float2(ex2(e.x), ex2(e.y));
+            ls = __fadd2_rn(ls, pe);
+            pp[y] = pack_bf16x2(pe.x, pe.y);
+            xp[y] = pack_bf16x2(xv.x, xv.y);
+          }
+          tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
+          tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
+        }
+      } else {
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          uint32_t pp[8], xp[8];
+#pragma unroll
+          for (int y = 0; y < 8; ++y) {
+            float pe[2], xe[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int x = 16 * hp + 2 * y + e;
+              const float xv = __uint_as_float(rv[x]);
+              const bool valid = k0 + 32 * ch + x <= lim;
+              pe[e] = valid ? ex2(fmaf(xv, c2, -m2)) : 0.0f;
+              xe[e] = valid ? xv : 0.0f;
+            }
+            ls.x += pe[0];
+            ls.y += pe[1];
+            pp[y] = pack_bf16x2(pe[0], pe[1]);
+            xp[y] = pack_bf16x2(xe[0], xe[1]);
+          }
+          tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
+          tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
+        }
+      }
+      l += ls.x + ls.y;
+    };
+    // chunk loads double-buffered (the next chunk's load overlaps this chunk's P; its columns
+    // are not written by this chunk)
+    uint32_t ra[32], rb[32];
+    tmem_ld32_nowait(ts, ra);
+    tmem_wait_ld();
+    reg_fence(ra);
+    chunk_max(ra, 0);
+    tmem_ld32_nowait(ts + 32, rb);
+    chunk_px(ra, 0);
+    tmem_wait_ld();
+    reg_fence(rb);
+    chunk_max(rb, 1);
+    tmem_ld32_nowait(ts + 64, ra);
+    chunk_px(rb, 1);
+    tmem_wait_ld();
+    reg_fence(ra);
+    chunk_max(ra, 2);
+    tmem_ld32_nowait(ts + 96, rb);
+    chunk_px(ra, 2);
+    tmem_wait_ld();
+    reg_fence(rb);
+    chunk_max(rb, 3);
+    chunk_px(rb, 3);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&ms->w_full[w]);
+  }
+  if (!ok) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+  }
+  // ---- the two halves' references and exp-sums (both warpgroups reach the barrier) ----
+  float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
+  stat[w * kT + r] = make_float2(m2, l);
+  named_bar_sync(1, 256);
+  const float2 h0 = stat[r], h1 = stat[kT + r];
+  if (ms->abort) return;
+  const bool has1 = J > 1;  // warpgroup 1 saw a tile (A1 written)
+  const float m = has1 ? fmaxf(h0.x, h1.x) : h0.x;
+  const float f0 = h0.x == -INFINITY ? 0.0f : ex2(h0.x - m);
+  const float f1 = (has1 && h1.x != -INFINITY) ? ex2(h1.x - m) : 0.0f;
+  const float lt = f0 * h0.y + f1 * h1.y;
+  // ---- output: O = alpha (f0 A0 + f1 A1) + beta B + gamma C; warpgroup w writes columns
+  //      32 w .. 32 w + 31 of its rows ----
+  if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort) || !mbar_wait_warp(&ms->cb_full, 0, &ms->abort)) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+    return;
+  }
+  tc_fence_after();
+  float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
+  if (row_ok) {
+    sig1 = sigmoid(a.g1[row]);
+    sigh = sigmoid(a.gh[row]);
+    if (a.g0) sig0 = sigmoid(a.g0[row]);
+  }
+  const float rt = 1.0f / tc;
+  const float alpha = lt > 0.0f ? sigh / lt : 0.0f;
+  const float beta = (sig1 - sigh) * rt;
+  uint32_t pt[16];
+  tmem_ld16_nowait(tl + CF::TM_B + 64, pt);  // column 64: the sum of the row's bf16 logits
+  tmem_wait_ld();
+  reg_fence(pt);
+  const float Pt = __uint_as_float(pt[0]) * inv_sqrt_d;
+  const float bs = beta * inv_sqrt_d;
+  const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
+  const float fa0 = alpha * f0, fa1 = alpha * f1;
+  const int c0 = 32 * w;
+  const float* cbase = reinterpret_cast<const float*>(smem + CF::CBASE_OFF) + c0;
+  const uint32_t tcd = tl + ((J & 1) ? CF::TM_S1 : CF::TM_S0);  // the diagonal tile's C
+  float o[32];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {  // two 16-column rounds
+    uint32_t a0[16], a1[16], bv[16], cv[16];
+    tmem_ld16_nowait(tl + CF::TM_A0 + c0 + 16 * hh, a0);
+    if (has1) tmem_ld16_nowait(tl + CF::TM_A1 + c0 + 16 * hh, a1);
+    tmem_ld16_nowait(tl + CF::TM_B + c0 + 16 * hh, bv);
+    if (a.causal) tmem_ld16_nowait(tcd + c0 + 16 * hh, cv);
+    tmem_wait_ld();
+    reg_fence(a0);
+    reg_fence(a1);
+    reg_fence(bv);
+    reg_fence(cv);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float c = cbase[16 * hh + j];
+      if (a.causal) c += __uint_as_float(cv[j]);
+      float x = fmaf(bs, __uint_as_float(bv[j]), gamma * c);
+      x = fmaf(fa0, __uint_as_float(a0[j]), x);
+      if (has1) x = fmaf(fa1, __uint_as_float(a1[j]), x);
+      o[16 * hh + j] = x;
+    }
+  }
+  if (row_ok) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * 64 + c0);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+      dst[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]),
+                           pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                           pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]),
+                           pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+  }
+}
+
+__global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constant__ SmParams p) {
+  using CF = Sm1Cfg;
+  const SmArgs& a = p.a;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report(a.status, kErrUnsupported);
+    return;
+  }
+  Sm1Misc* ms = reinterpret_cast<Sm1Misc*>(smem + CF::MISC_OFF);
+  const int warp = threadIdx.x >> 5;
+  const int nqt = (a.N + kT - 1) / kT;
+  // every sequence's heaviest (last) causal query tile first, then the next lighter ones
+  const int qt = a.causal ? nqt - 1 - (int)blockIdx.y : (int)blockIdx.y;
+  const int bh = blockIdx.x;
+  const int J = key_tiles(a, qt);
+  if (threadIdx.x == 0) {
+    mbar_init(&ms->q_full, 1);
+    for (int i = 0; i < CF::NS; ++i) {
+      mbar_init(&ms->kv_full[i], 1);
+      mbar_init(&ms->kv_empty[i], 3);  // the tensor cores and the two column-sum warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->w_full[i], 128);
+    }
+    mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->fin, 1);
+    mbar_init(&ms->cb_full, 1);
+    ms->abort = 0;
+    ms->never = 0;
+  }
+  // constant operand tiles: the lower-triangular ones [query row][key] (K-major, two atoms of
+  // 64 keys: 1 where key <= row) and V's extension [key][64 columns] (MN-major: column 0 is 1,
+  // the rest 0), both 128-byte swizzled
+  for (int idx = threadIdx.x; idx < 3 * kT * 8; idx += kSmThreads) {
+    const int part = idx / (kT * 8), rr = (idx / 8) % kT, c = idx % 8;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t off;
+    if (part < 2) {
+      uint32_t wv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key0 = 64 * part + 8 * c + 2 * e;
+        wv[e] = pack_bf16x2(key0 <= rr ? 1.0f : 0.0f, key0 + 1 <= rr ? 1.0f : 0.0f);
+      }
+      val = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      off = CF::TRI_OFF + part * kAtom + sw128_off(rr, c);
+    } else {
+      if (c == 0) val.x = pack_bf16x2(1.0f, 0.0f);
+      off = CF::ONE_OFF + sw128_off(rr, c);
+    }
+    *reinterpret_cast<uint4*>(smem + off) = val;
+  }
+  fence_proxy_async_smem();  // written by the threads, read by the tensor cores
+  if (warp == 1) {
+    tmem_alloc(&ms->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 0) {
+    if ((threadIdx.x & 31) == 0) sm1_producer(p, smem, ms, bh, qt, J);
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) sm1_mma(a, smem, ms, J);
+  } else if (warp < 4) {
+    sm1_colsum(a, smem, ms, J);
+  } else {
+    sm1_epilogue(a, smem, ms, bh, qt, J, (warp - 4) >> 2);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    // every MMA has completed once `fin` fires (it is committed after the last one)
+    if (!mbar_wait(&ms->fin, 0, &ms->never, 4000000000ull)) report(a.status, kErrTimeout);
+    tc_fence_after();
+    tmem_dealloc(ms->tmem, 512);
+  }
+}
+
 // Rotary map of the bf16 rows [BH, N, d] of q and of k (half-split pairs, token n at position
 // n) into yq and yk, with the fp64-built (cos, sin) table [N][d/2]; the rotated values are
 // rounded to bf16 once.  A thread takes 8 consecutive pairs of one row (16-byte loads and
@@ -578,6 +1074,30 @@ cudaError_t launch_sm_d(const SmArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_sm1(const SmArgs& a, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_set{0};  // bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(sm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Sm1Cfg::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  SmParams p;
+  p.a = a;
+  const int BH = a.B * a.H;
+  if (!sm_map(&p.tq, a.q, 64, a.N, BH) || !sm_map(&p.tk, a.k, 64, a.N, BH) ||
+      !sm_map(&p.tv, a.v, 64, a.N, BH))
+    return cudaErrorNotSupported;
+  const dim3 grid(BH, (a.N + kT - 1) / kT, 1);
+  sm1_kernel<<<grid, kSmThreads, Sm1Cfg::BYTES, stream>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool sm_supported(int d, int dtype) { return dtype == 0 && (d == 64 || d == 128); }
@@ -596,7 +1116,7 @@ cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
 }
 
 cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return launch_sm_d<64>(a, stream);
+  if (a.d == 64) return launch_sm1(a, stream);
   if (a.d == 128) return launch_sm_d<128>(a, stream);
   return cudaErrorInvalidValue;
 }
