@@ -495,13 +495,13 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
 // only perturb each weight.  C does not depend on the query: the column sums of the key tiles
 // before the diagonal one are added up on the CUDA cores by two otherwise idle warps, and the
 // diagonal tile's prefix comes from one product with a lower-triangular ones tile at the end.
-// The two epilogue warpgroups take the even and odd key tiles, each with its own A accumulator
-// and its own reference m; m is raised only when a 32-key chunk would give P > 2^32 (the first
-// chunk of a warpgroup sets it), in which case the warpgroup's A rows, its exp-sum and the P
-// already written for the tile are rescaled (the previous P V product of the warpgroup has
-// completed by then: the commit that signalled this tile's S covers it).  At the end the two
-// halves are merged with their reference maxima.
-// TMEM (512 columns): S0, S1 (128 each), A0, A1 (64 each), [B | P_t] (80).
+// Both epilogue warpgroups work on every key tile, warpgroup w on its keys 64 w .. 64 w + 63,
+// so that S_{g+1} is formed while tile g is turned into P and x and the products of tile g run
+// while tile g+1 is.  The row's tile maximum is exchanged through shared memory; the reference
+// m rises (lazily: only when the tile maximum exceeds it by more than 8, so P <= 2^8) before the
+// tile's P is formed, and A and the exp-sums are then rescaled (warpgroup 0 rescales A, after
+// the previous tile's products have completed).
+// TMEM (512 columns): S0, S1 (128 each), A (64), [B | P_t] (80), the diagonal tile's C (64).
 struct Sm1Cfg {
   static constexpr int NS = 4;                             // K/V stages
   static constexpr uint32_t Q_OFF = 0;
@@ -509,21 +509,22 @@ struct Sm1Cfg {
   static constexpr uint32_t STAGE = 2 * kAtom;             // K then V
   static constexpr uint32_t TRI_OFF = STAGE_OFF + NS * STAGE;  // [128 x 128] lower-triangular ones
   static constexpr uint32_t ONE_OFF = TRI_OFF + 2 * kAtom;     // V's 65th column (1) and zeros
-  static constexpr uint32_t STAT_OFF = ONE_OFF + kAtom;        // float2 [2][128]
-  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 8;  // float [8][64] partial sums
+  static constexpr uint32_t XMAX_OFF = ONE_OFF + kAtom;        // float [2 bufs][2 halves][128]
+  static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float [2][128] exp-sums
+  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 4;  // float [8][64] partial sums
   static constexpr uint32_t CBASE_OFF = CSUM_OFF + 8 * 64 * 4; // float [64]
   static constexpr uint32_t MISC_OFF = CBASE_OFF + 64 * 4;
   static constexpr uint32_t BYTES = MISC_OFF + 256;
   static_assert(BYTES <= 232448, "shared memory budget of one CTA");
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_A0 = 256, TM_A1 = 320, TM_B = 384;
-  static constexpr int kGuard = 32;  // P stays below 2^kGuard
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_A = 256, TM_B = 320, TM_C = 448;
+  static constexpr float kRaise = 8.0f;  // base-2 units
 };
 
 struct Sm1Misc {
   uint64_t q_full;
   uint64_t kv_full[4], kv_empty[4];
-  uint64_t s_full[2], w_full[2];
-  uint64_t o_full, fin, cb_full;
+  uint64_t s_full[2], w_full[2][2];  // [S buffer][warpgroup]
+  uint64_t a_done, o_full, fin, cb_full;
   uint32_t tmem;
   int abort;
   int never;
@@ -549,71 +550,87 @@ __device__ void sm1_producer(const SmParams& p, uint8_t* smem, Sm1Misc* ms, int 
   }
 }
 
-// Per key tile g, in issue order: S_g = Q K_g^T (into S_{g & 1}); then the products of tile
-// g - 1 once its P and x are written: A_{(g-1) & 1} += P V, [B | P_t] += X [V | 1].  The
-// tensor-core operations of one thread run in order, so S_{g+2} overwrites S_g only after tile
-// g's products have read it.  Descriptors advance by plain additions (16 key rows of an
-// MN-major tile = 2048 bytes = 128 descriptor units), keeping the issue loop short.
+// Issue order: S_0, S_1; then per key tile g the products of tile g, half by half as the two
+// warpgroups release their keys (A += P V, [B | P_t] += X [V | 1]), and S_{g+2} into the buffer
+// those products have just read.  The tensor-core operations of one thread run in order, so
+// S_{g+2} overwrites tile g's P and x only after its products have read them.  The whole warp
+// runs this loop (its operands stay warp-uniform, so the issue stays short next to the busy
+// epilogue warps of the same scheduler) and one elected lane issues; descriptors advance by
+// plain additions (16 key rows of an MN-major tile = 2048 bytes = 128 units).
 __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   using CF = Sm1Cfg;
+  const bool leader = elect_one();
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
   constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);    // A += P V, C = T V
   constexpr uint32_t id_xv = idesc_bf16_f32(128, 80, false, true);    // [B | P_t] += X [V | 1]
   const uint64_t qd = sw128_desc(base + CF::Q_OFF, 16, 1024);
-  auto products = [&](int g) -> bool {
-    const int b = g & 1, st = g % CF::NS;
-    if (!mbar_wait(&ms->w_full[b], (g >> 1) & 1, &ms->abort)) return false;
+  auto issue_s = [&](int g) -> bool {
+    const int st = g % CF::NS;
+    if (!mbar_wait_warp(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort)) return false;
     tc_fence_after();
+    const uint64_t kd = sw128_desc(base + CF::STAGE_OFF + st * CF::STAGE, 16, 1024);
+    const uint32_t ts = tm + ((g & 1) ? CF::TM_S1 : CF::TM_S0);
+    if (leader) {
+      mma_f16kind(ts, qd, kd, id_qk, 0u);
+#pragma unroll
+      for (int kk = 1; kk < 4; ++kk) mma_f16kind(ts, qd + 2 * kk, kd + 2 * kk, id_qk, 1u);
+      mma_commit(&ms->s_full[g & 1]);
+    }
+    __syncwarp();
+    return true;
+  };
+  bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
+  if (ok) ok = issue_s(0);
+  if (ok && J > 1) ok = issue_s(1);
+  for (int g = 0; g < J && ok; ++g) {
+    const int b = g & 1, st = g % CF::NS;
     const uint32_t vt = base + CF::STAGE_OFF + st * CF::STAGE + kAtom;
     // one descriptor for both products: the second 64-column atom (N = 64 .. 79) is the
     // constant tile, at a fixed distance from this stage's V
     const uint64_t vd = sw128_desc(vt, base + CF::ONE_OFF - vt, 1024);
     const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
-    const uint32_t ta = tm + (b ? CF::TM_A1 : CF::TM_A0);
-    const uint32_t acc_a = g >= 2 ? 1u : 0u, acc_b = g >= 1 ? 1u : 0u;
-    mma_f16kind_ts(ta, ts, vd, id_pv, acc_a);
-    mma_f16kind_ts(tm + CF::TM_B, ts + 8, vd, id_xv, acc_b);
 #pragma unroll
-    for (int kk = 1; kk < kT / 16; ++kk) {
-      mma_f16kind_ts(ta, ts + 16 * kk, vd + 128 * kk, id_pv, 1u);
-      mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_xv, 1u);
-    }
-    if (a.causal && g == J - 1) {
-      // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V,
-      // into the other S buffer (its last tile's products were issued before these)
-      const uint32_t tc = tm + (b ? CF::TM_S0 : CF::TM_S1);
-      const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
+    for (int h = 0; h < 2; ++h) {
+      ok = mbar_wait_warp(&ms->w_full[b][h], (g >> 1) & 1, &ms->abort);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
 #pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        mma_f16kind(tc, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4), vd + 128 * kk,
-                    id_pv, kk > 0 ? 1u : 0u);
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
+          const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+          mma_f16kind_ts(tm + CF::TM_A, ts + 16 * kk, vd + 128 * kk, id_pv, acc);
+          mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_xv, acc);
+        }
+      }
+      __syncwarp();
     }
-    mma_commit(&ms->kv_empty[st]);
-    return true;
-  };
-  bool ok = mbar_wait(&ms->q_full, 0, &ms->abort);
-  for (int g = 0; g < J && ok; ++g) {
-    const int st = g % CF::NS, b = g & 1;
-    ok = mbar_wait(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort);
     if (!ok) break;
-    tc_fence_after();
-    const uint64_t kd = sw128_desc(base + CF::STAGE_OFF + st * CF::STAGE, 16, 1024);
-    const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
-    mma_f16kind(ts, qd, kd, id_qk, 0u);
+    if (leader) {
+      if (a.causal && g == J - 1) {
+        // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V
+        const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
 #pragma unroll
-    for (int kk = 1; kk < 4; ++kk) mma_f16kind(ts, qd + 2 * kk, kd + 2 * kk, id_qk, 1u);
-    mma_commit(&ms->s_full[b]);
-    if (g >= 1) ok = products(g - 1);
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_f16kind(tm + CF::TM_C, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4),
+                      vd + 128 * kk, id_pv, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&ms->a_done);
+      mma_commit(&ms->kv_empty[st]);
+    }
+    __syncwarp();
+    if (g + 2 < J) ok = issue_s(g + 2);
   }
-  if (ok && J > 0) ok = products(J - 1);
-  if (ok) mma_commit(&ms->o_full);
-  if (!ok) {
-    report(a.status, kErrTimeout);
-    ms->abort = 1;
+  if (leader) {
+    if (ok) mma_commit(&ms->o_full);
+    if (!ok) {
+      report(a.status, kErrTimeout);
+      ms->abort = 1;
+    }
+    mma_commit(&ms->fin);
   }
-  mma_commit(&ms->fin);
+  __syncwarp();
 }
 
 // Warps 2 and 3: the column sums of V over the key tiles before the diagonal one (all tiles in
@@ -666,15 +683,14 @@ __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   if (t == 0) mbar_arrive(&ms->cb_full);
 }
 
-// Warpgroup w (0 or 1) handles the key tiles of parity w; thread = query row of the tile.
+// Both warpgroups take every key tile; warpgroup w its keys 64 w .. 64 w + 63.  Thread = query
+// row of the tile.
 __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J,
                              int w) {
   using CF = Sm1Cfg;
   const int wq = (threadIdx.x >> 5) & 3;
   const int r = wq * 32 + (threadIdx.x & 31);
   const uint32_t tl = ms->tmem + ((uint32_t)(wq * 32) << 16);
-  const uint32_t ts = tl + (w ? CF::TM_S1 : CF::TM_S0);
-  const uint32_t ta = tl + (w ? CF::TM_A1 : CF::TM_A0);
   const int t = qt * kT + r;                      // query index (0-based)
   const bool row_ok = t < a.N;
   const size_t row = (size_t)bh * a.N + t;
@@ -684,64 +700,77 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   const float tc = a.causal ? (float)(t + 1) : (float)a.N;
   constexpr float inv_sqrt_d = 0.125f;                      // d = 64
   constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
-  float m2 = -INFINITY, l = 0.0f;  // reference (base-2 units) and exp-sum of this warpgroup
+  float* xmax = reinterpret_cast<float*>(smem + CF::XMAX_OFF);
+  float m2 = -INFINITY, l = 0.0f;  // the row's reference (base-2 units), this half's exp-sum
   bool ok = true;
-  int n = 0;                       // this warpgroup's tile count
-  for (int g = w; g < J && ok; g += 2, ++n) {
-    ok = mbar_wait_warp(&ms->s_full[w], n & 1, &ms->abort);
-    if (!ok) break;
-    tc_fence_after();
-    const int k0 = g * kT;
-    const bool full = k0 + kT - 1 <= lim_warp;
-    // one 32-key chunk, first half: its maximum decides whether the reference must rise before
-    // the chunk's P is formed (no TMEM load is in flight here)
-    auto chunk_max = [&](const uint32_t (&rv)[32], const int ch) {
-      float cm = -INFINITY;
-      if (full) {
+  // Every iteration reaches the one named barrier of the tile, also after a failed wait (the
+  // work is then skipped), so that the two warpgroups never wait on it for each other in vain.
+  for (int g = 0; g < J; ++g) {
+    const int b = g & 1;
+    if (ok) {
+      ok = mbar_wait_warp(&ms->s_full[b], (g >> 1) & 1, &ms->abort);
+      if (!ok) ms->abort = 1;
+    }
+    const uint32_t ts = tl + (b ? CF::TM_S1 : CF::TM_S0) + 64 * w;  // this half's columns
+    const int k0 = g * kT + 64 * w;                                 // its first key
+    const bool full = k0 + 63 <= lim_warp;
+    uint32_t ra[32], rb[32];
+    float cm = -INFINITY;
+    if (ok) {
+      tc_fence_after();
+      tmem_ld32_nowait(ts, ra);
+      tmem_ld32_nowait(ts + 32, rb);
+      tmem_wait_ld();
+      reg_fence(ra);
+      reg_fence(rb);
+    }
+    // ---- the row's maximum over this half, then over the tile ----
+    if (!ok) {
+    } else if (full) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) cm = fmaxf(cm, __uint_as_float(rv[x]));
-      } else {
+      for (int x = 0; x < 32; ++x)
+        cm = fmaxf(cm, fmaxf(__uint_as_float(ra[x]), __uint_as_float(rb[x])));
+    } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x)
-          if (k0 + 32 * ch + x <= lim) cm = fmaxf(cm, __uint_as_float(rv[x]));
+      for (int x = 0; x < 32; ++x) {
+        if (k0 + x <= lim) cm = fmaxf(cm, __uint_as_float(ra[x]));
+        if (k0 + 32 + x <= lim) cm = fmaxf(cm, __uint_as_float(rb[x]));
       }
-      const bool raise = cm * c2 > m2 + (float)CF::kGuard;
-      if (__any_sync(0xffffffffu, raise)) {
-        const float mn = raise ? cm * c2 : m2;
-        const float f = (raise && m2 != -INFINITY) ? ex2(m2 - mn) : 1.0f;
-        tmem_wait_st();  // this tile's earlier P must have landed before it is read back
+    }
+    float* xm = xmax + b * 2 * kT;  // double-buffered: the next tile writes the other half
+    xm[w * kT + r] = cm;
+    named_bar_sync(1, 256);
+    if (!ok) continue;
+    const float tmx = fmaxf(xm[r], xm[kT + r]) * c2;
+    // ---- lazy rise of the reference: both warpgroups decide alike for a row ----
+    const bool raise = tmx > m2 + CF::kRaise;  // false for a row without visible keys yet
+    if (__any_sync(0xffffffffu, raise)) {
+      const float f = (raise && m2 != -INFINITY) ? ex2(m2 - tmx) : 1.0f;
+      if (w == 0 && g >= 1) {
+        // A's earlier tiles: wait until their products have completed, then rescale
+        ok = mbar_wait_warp(&ms->a_done, (g - 1) & 1, &ms->abort);
+        if (!ok) {
+          ms->abort = 1;
+          continue;
+        }
+        tc_fence_after();
 #pragma unroll 1
-        for (int pc = 0; pc < 2 * ch; ++pc) {  // 16-key pieces written so far: P columns
-          uint32_t pw[8];
-          tmem_ld8_nowait(ts + 16 * pc, pw);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t av[16];
+          tmem_ld16_nowait(tl + CF::TM_A + 16 * q, av);
           tmem_wait_ld();
-          reg_fence(pw);
+          reg_fence(av);
 #pragma unroll
-          for (int y = 0; y < 8; ++y) {
-            float lo, hi;
-            unpack_bf16x2(pw[y], lo, hi);
-            pw[y] = pack_bf16x2(lo * f, hi * f);
-          }
-          tmem_st8_nowait(ts + 16 * pc, pw);
+          for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
+          tmem_st16_nowait(tl + CF::TM_A + 16 * q, av);
         }
-        if (n >= 1) {  // the warpgroup's earlier tiles: their products completed before S_g
-#pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
-            uint32_t av[16];
-            tmem_ld16_nowait(ta + 16 * q, av);
-            tmem_wait_ld();
-            reg_fence(av);
-#pragma unroll
-            for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
-            tmem_st16_nowait(ta + 16 * q, av);
-          }
-        }
-        tmem_wait_st();
-        l *= f;
-        m2 = mn;
       }
-    };
-    // second half: P = 2^{c2 x - m} and x as bf16 pairs over the chunk's own columns
+      if (raise) {
+        l *= f;
+        m2 = tmx;
+      }
+    }
+    // ---- P = 2^{c2 x - m} and x as bf16 pairs over this half's own columns ----
     auto chunk_px = [&](const uint32_t (&rv)[32], const int ch) {
       float2 ls = make_float2(0.0f, 0.0f);
       if (full) {
@@ -788,50 +817,24 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
       }
       l += ls.x + ls.y;
     };
-    // chunk loads double-buffered (the next chunk's load overlaps this chunk's P; its columns
-    // are not written by this chunk)
-    uint32_t ra[32], rb[32];
-    tmem_ld32_nowait(ts, ra);
-    tmem_wait_ld();
-    reg_fence(ra);
-    chunk_max(ra, 0);
-    tmem_ld32_nowait(ts + 32, rb);
     chunk_px(ra, 0);
-    tmem_wait_ld();
-    reg_fence(rb);
-    chunk_max(rb, 1);
-    tmem_ld32_nowait(ts + 64, ra);
     chunk_px(rb, 1);
-    tmem_wait_ld();
-    reg_fence(ra);
-    chunk_max(ra, 2);
-    tmem_ld32_nowait(ts + 96, rb);
-    chunk_px(ra, 2);
-    tmem_wait_ld();
-    reg_fence(rb);
-    chunk_max(rb, 3);
-    chunk_px(rb, 3);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(&ms->w_full[w]);
+    mbar_arrive(&ms->w_full[b][w]);
   }
   if (!ok) {
     report(a.status, kErrTimeout);
     ms->abort = 1;
   }
-  // ---- the two halves' references and exp-sums (both warpgroups reach the barrier) ----
-  float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
-  stat[w * kT + r] = make_float2(m2, l);
+  // ---- the two halves' exp-sums, both relative to the row's common reference ----
+  float* stat = reinterpret_cast<float*>(smem + CF::STAT_OFF);
+  stat[w * kT + r] = l;
   named_bar_sync(1, 256);
-  const float2 h0 = stat[r], h1 = stat[kT + r];
+  const float lt = stat[r] + stat[kT + r];
   if (ms->abort) return;
-  const bool has1 = J > 1;  // warpgroup 1 saw a tile (A1 written)
-  const float m = has1 ? fmaxf(h0.x, h1.x) : h0.x;
-  const float f0 = h0.x == -INFINITY ? 0.0f : ex2(h0.x - m);
-  const float f1 = (has1 && h1.x != -INFINITY) ? ex2(h1.x - m) : 0.0f;
-  const float lt = f0 * h0.y + f1 * h1.y;
-  // ---- output: O = alpha (f0 A0 + f1 A1) + beta B + gamma C; warpgroup w writes columns
-  //      32 w .. 32 w + 31 of its rows ----
+  // ---- output: O = alpha A + beta B + gamma C; warpgroup w writes columns 32 w .. 32 w + 31
+  //      of its rows ----
   if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort) || !mbar_wait_warp(&ms->cb_full, 0, &ms->abort)) {
     report(a.status, kErrTimeout);
     ms->abort = 1;
@@ -854,31 +857,25 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   const float Pt = __uint_as_float(pt[0]) * inv_sqrt_d;
   const float bs = beta * inv_sqrt_d;
   const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
-  const float fa0 = alpha * f0, fa1 = alpha * f1;
   const int c0 = 32 * w;
   const float* cbase = reinterpret_cast<const float*>(smem + CF::CBASE_OFF) + c0;
-  const uint32_t tcd = tl + ((J & 1) ? CF::TM_S1 : CF::TM_S0);  // the diagonal tile's C
   float o[32];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {  // two 16-column rounds
-    uint32_t a0[16], a1[16], bv[16], cv[16];
-    tmem_ld16_nowait(tl + CF::TM_A0 + c0 + 16 * hh, a0);
-    if (has1) tmem_ld16_nowait(tl + CF::TM_A1 + c0 + 16 * hh, a1);
+    uint32_t av[16], bv[16], cv[16];
+    tmem_ld16_nowait(tl + CF::TM_A + c0 + 16 * hh, av);
     tmem_ld16_nowait(tl + CF::TM_B + c0 + 16 * hh, bv);
-    if (a.causal) tmem_ld16_nowait(tcd + c0 + 16 * hh, cv);
+    if (a.causal) tmem_ld16_nowait(tl + CF::TM_C + c0 + 16 * hh, cv);
     tmem_wait_ld();
-    reg_fence(a0);
-    reg_fence(a1);
+    reg_fence(av);
     reg_fence(bv);
     reg_fence(cv);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       float c = cbase[16 * hh + j];
       if (a.causal) c += __uint_as_float(cv[j]);
-      float x = fmaf(bs, __uint_as_float(bv[j]), gamma * c);
-      x = fmaf(fa0, __uint_as_float(a0[j]), x);
-      if (has1) x = fmaf(fa1, __uint_as_float(a1[j]), x);
-      o[16 * hh + j] = x;
+      o[16 * hh + j] = fmaf(alpha, __uint_as_float(av[j]),
+                            fmaf(bs, __uint_as_float(bv[j]), gamma * c));
     }
   }
   if (row_ok) {
@@ -917,8 +914,10 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->s_full[i], 1);
-      mbar_init(&ms->w_full[i], 128);
+      mbar_init(&ms->w_full[i][0], 128);
+      mbar_init(&ms->w_full[i][1], 128);
     }
+    mbar_init(&ms->a_done, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->fin, 1);
     mbar_init(&ms->cb_full, 1);
@@ -959,7 +958,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
   if (warp == 0) {
     if ((threadIdx.x & 31) == 0) sm1_producer(p, smem, ms, bh, qt, J);
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) sm1_mma(a, smem, ms, J);
+    sm1_mma(a, smem, ms, J);
   } else if (warp < 4) {
     sm1_colsum(a, smem, ms, J);
   } else {
