@@ -802,16 +802,28 @@ int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, c
   a.d = d;
   a.causal = causal;
   a.status = ws->status;
-  if (rope) {  // rotate q and k once into the library's scratch
-    const size_t each = (size_t)B * H * N * d * 2;
-    void* buf = nullptr;
-    if (int rc = sm_scratch(ws, 2 * each, &buf)) return rc;
-    const float2* table = nullptr;
+  // scratch: the rotated q and k (with rope), then (d = 64) the key-tile statistics
+  const size_t each = rope ? (size_t)B * H * N * d * 2 : 0;
+  const size_t ntiles = ((size_t)N + 127) / 128;
+  const size_t stat_bytes = d == 64 ? (size_t)B * H * ntiles * kSmStat * sizeof(float) : 0;
+  void* buf = nullptr;
+  if (2 * each + stat_bytes > 0)
+    if (int rc = sm_scratch(ws, 2 * each + stat_bytes, &buf)) return rc;
+  const float2* table = nullptr;
+  if (rope)
     if (int rc = rope_table(ws, N, d, rope_base, st, &table)) return rc;
-    void* qr = buf;
-    void* kr = static_cast<uint8_t*>(buf) + each;
+  void* qr = buf;
+  void* kr = static_cast<uint8_t*>(buf) + each;
+  if (d == 64) {  // one pass: the statistics, and with rope the rotated q and k
+    float* kstat = reinterpret_cast<float*>(static_cast<uint8_t*>(buf) + 2 * each);
+    cudaError_t e = launch_sm_prep(q, k, qr, kr, rope ? table : nullptr, kstat, B * H, N, st);
+    if (e != cudaSuccess) return cuda_fail(e, "ZeroS-SM key statistics launch");
+    a.kstat = kstat;
+  } else if (rope) {
     cudaError_t e = launch_sm_rotate(q, k, qr, kr, table, B * H, N, d, st);
     if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
+  }
+  if (rope) {
     a.q = qr;
     a.k = kr;
   }

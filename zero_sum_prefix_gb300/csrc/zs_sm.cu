@@ -488,43 +488,54 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
 // above with P_t = sum_i x_{t,i} / sqrt d.  So one pass over the key tiles suffices: S = Q K^T
 // once per tile; P = 2^{c2 x - m} and x itself rounded to bf16 and written over S's own fp32
 // columns (piece h of 16 keys: P in columns 16 h .. 16 h + 7, x in 16 h + 8 .. 16 h + 15); then
-// A += P V and [B | P_t] += X [V | 1].  The second product runs with N = 80 over V and a
-// constant tile whose first column is 1, so the logit sum P_t is the sum of the very bf16 values
-// that B sums: the weights alpha P + beta x / sqrt d + gamma of a row then sum to sig0 up to the
-// fp32 rounding of the sums (exactly zero output for a single visible key), and the roundings
-// only perturb each weight.  C does not depend on the query: the column sums of the key tiles
-// before the diagonal one are added up on the CUDA cores by two otherwise idle warps, and the
-// diagonal tile's prefix comes from one product with a lower-triangular ones tile at the end.
-// Both epilogue warpgroups work on every key tile, warpgroup w on its keys 64 w .. 64 w + 63,
-// so that S_{g+1} is formed while tile g is turned into P and x and the products of tile g run
-// while tile g+1 is.  The row's tile maximum is exchanged through shared memory; the reference
-// m rises (lazily: only when the tile maximum exceeds it by more than 8, so P <= 2^8) before the
-// tile's P is formed, and A and the exp-sums are then rescaled (warpgroup 0 rescales A, after
-// the previous tile's products have completed).
-// TMEM (512 columns): S0, S1 (128 each), A (64), [B | P_t] (80), the diagonal tile's C (64).
+// A += P V and B += X V.  The logit sum P_t is q_t . (sum of the earlier tiles' keys) plus the
+// sum of the last tile's bf16 logits, the very values that B sums there: for the rows of the
+// first query tile (few keys) the weights alpha P + beta x / sqrt d + gamma then sum to sig0 up to
+// the fp32 rounding of the sums (exactly zero output for a single visible key), and elsewhere the
+// roundings only perturb each weight.  C does not depend on the query: the column sums of the key
+// tiles before the diagonal one are added up on the CUDA cores by two otherwise idle warps, and
+// the diagonal tile's prefix comes from one product with a lower-triangular ones tile at the
+// end.  Each tile's largest key norm (with the key column sums, from a pass that also applies
+// the rotary map) bounds its logits: where c2 |q_t| max |k| cannot exceed the reference by more
+// than kRaise, the tile's maximum is not needed at all.
+// Three S buffers: S_{g+3} is formed as soon as tile g's products are issued, so the tensor
+// cores, the exponentials of tile g+1 and the products of tile g overlap.  Both epilogue
+// warpgroups work on every key tile, warpgroup w on its keys 64 w .. 64 w + 63; where the bound
+// does not settle it, the row's tile maximum is exchanged between the two warps that hold the
+// row (a 64-thread barrier), and the reference m rises (lazily: only when the tile maximum
+// exceeds it by more than kRaise = 16, so P <= 2^16) before the tile's P is formed; A and the
+// exp-sums are then rescaled (warpgroup 0 rescales A, once the previous tile's products have
+// completed).
+// TMEM (512 columns): S0, S1, S2 (128 each), A (64), B (64); the diagonal tile's C goes to the S
+// buffer that is free at the end.
 struct Sm1Cfg {
-  static constexpr int NS = 4;                             // K/V stages
+  static constexpr int NS = 5;                             // K/V stages
+  static constexpr int NB = 3;                             // S buffers
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t STAGE_OFF = Q_OFF + kAtom;
   static constexpr uint32_t STAGE = 2 * kAtom;             // K then V
   static constexpr uint32_t TRI_OFF = STAGE_OFF + NS * STAGE;  // [128 x 128] lower-triangular ones
-  static constexpr uint32_t ONE_OFF = TRI_OFF + 2 * kAtom;     // V's 65th column (1) and zeros
-  static constexpr uint32_t XMAX_OFF = ONE_OFF + kAtom;        // float [2 bufs][2 halves][128]
-  static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float [2][128] exp-sums
-  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 4;  // float [8][64] partial sums
+  static constexpr uint32_t XMAX_OFF = TRI_OFF + 2 * kAtom;    // float [2 bufs][2 halves][128]
+  static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float2 [2][128] sums
+  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 8;  // float [8][64] partial sums
   static constexpr uint32_t CBASE_OFF = CSUM_OFF + 8 * 64 * 4; // float [64]
-  static constexpr uint32_t MISC_OFF = CBASE_OFF + 64 * 4;
+  static constexpr uint32_t KBASE_OFF = CBASE_OFF + 64 * 4;    // float [64]
+  static constexpr uint32_t QN_OFF = KBASE_OFF + 64 * 4;       // float [128]
+  static constexpr uint32_t MISC_OFF = QN_OFF + kT * 4;
   static constexpr uint32_t BYTES = MISC_OFF + 256;
   static_assert(BYTES <= 232448, "shared memory budget of one CTA");
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_A = 256, TM_B = 320, TM_C = 448;
-  static constexpr float kRaise = 8.0f;  // base-2 units
+  static constexpr uint32_t TM_A = 384, TM_B = 448;
+  static constexpr float kRaise = 16.0f;  // base-2 units
+  static constexpr float kBoundSlack = 1.001f;  // covers the fp32 rounding of logits and norms
 };
+
+__device__ __forceinline__ uint32_t sm1_sbuf(int i) { return 128u * (uint32_t)i; }
 
 struct Sm1Misc {
   uint64_t q_full;
-  uint64_t kv_full[4], kv_empty[4];
-  uint64_t s_full[2], w_full[2][2];  // [S buffer][warpgroup]
-  uint64_t a_done, o_full, fin, cb_full;
+  uint64_t kv_full[Sm1Cfg::NS], kv_empty[Sm1Cfg::NS];
+  uint64_t s_full[3], w_full[3];
+  uint64_t o_full, fin, cb_full;
   uint32_t tmem;
   int abort;
   int never;
@@ -550,77 +561,67 @@ __device__ void sm1_producer(const SmParams& p, uint8_t* smem, Sm1Misc* ms, int 
   }
 }
 
-// Issue order: S_0, S_1; then per key tile g the products of tile g, half by half as the two
-// warpgroups release their keys (A += P V, [B | P_t] += X [V | 1]), and S_{g+2} into the buffer
-// those products have just read.  The tensor-core operations of one thread run in order, so
-// S_{g+2} overwrites tile g's P and x only after its products have read them.  The whole warp
-// runs this loop (its operands stay warp-uniform, so the issue stays short next to the busy
-// epilogue warps of the same scheduler) and one elected lane issues; descriptors advance by
-// plain additions (16 key rows of an MN-major tile = 2048 bytes = 128 units).
+// Issue order: S_0, S_1, S_2; then per key tile g the products of tile g once both warpgroups
+// have released it (A += P V, B += X V), and S_{g+3} into the buffer those products have just
+// read.  The tensor-core operations of one thread run in order, so S_{g+3} overwrites tile g's
+// P and x only after its products have read them.  The whole warp runs this loop (its operands
+// stay warp-uniform, so the issue stays short next to the busy epilogue warps of the same
+// scheduler) and one elected lane issues; descriptors advance by plain additions (16 key rows of
+// an MN-major tile = 2048 bytes = 128 units).
 __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   using CF = Sm1Cfg;
   const bool leader = elect_one();
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
-  constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);    // A += P V, C = T V
-  constexpr uint32_t id_xv = idesc_bf16_f32(128, 80, false, true);    // [B | P_t] += X [V | 1]
+  constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);    // A += P V, B += X V
   const uint64_t qd = sw128_desc(base + CF::Q_OFF, 16, 1024);
   auto issue_s = [&](int g) -> bool {
     const int st = g % CF::NS;
     if (!mbar_wait_warp(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort)) return false;
     tc_fence_after();
     const uint64_t kd = sw128_desc(base + CF::STAGE_OFF + st * CF::STAGE, 16, 1024);
-    const uint32_t ts = tm + ((g & 1) ? CF::TM_S1 : CF::TM_S0);
+    const uint32_t ts = tm + sm1_sbuf(g % CF::NB);
     if (leader) {
       mma_f16kind(ts, qd, kd, id_qk, 0u);
 #pragma unroll
       for (int kk = 1; kk < 4; ++kk) mma_f16kind(ts, qd + 2 * kk, kd + 2 * kk, id_qk, 1u);
-      mma_commit(&ms->s_full[g & 1]);
+      mma_commit(&ms->s_full[g % CF::NB]);
     }
     __syncwarp();
     return true;
   };
   bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
-  if (ok) ok = issue_s(0);
-  if (ok && J > 1) ok = issue_s(1);
+  for (int g = 0; g < CF::NB && g < J && ok; ++g) ok = issue_s(g);
   for (int g = 0; g < J && ok; ++g) {
-    const int b = g & 1, st = g % CF::NS;
+    const int b = g % CF::NB, st = g % CF::NS;
     const uint32_t vt = base + CF::STAGE_OFF + st * CF::STAGE + kAtom;
-    // one descriptor for both products: the second 64-column atom (N = 64 .. 79) is the
-    // constant tile, at a fixed distance from this stage's V
-    const uint64_t vd = sw128_desc(vt, base + CF::ONE_OFF - vt, 1024);
-    const uint32_t ts = tm + (b ? CF::TM_S1 : CF::TM_S0);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      ok = mbar_wait_warp(&ms->w_full[b][h], (g >> 1) & 1, &ms->abort);
-      if (!ok) break;
-      tc_fence_after();
-      if (leader) {
-#pragma unroll
-        for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
-          const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
-          mma_f16kind_ts(tm + CF::TM_A, ts + 16 * kk, vd + 128 * kk, id_pv, acc);
-          mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_xv, acc);
-        }
-      }
-      __syncwarp();
-    }
+    const uint64_t vd = sw128_desc(vt, kAtom, 1024);
+    const uint32_t ts = tm + sm1_sbuf(b);
+    ok = mbar_wait_warp(&ms->w_full[b], (g / CF::NB) & 1, &ms->abort);
     if (!ok) break;
+    tc_fence_after();
     if (leader) {
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk) {
+        const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+        mma_f16kind_ts(tm + CF::TM_A, ts + 16 * kk, vd + 128 * kk, id_pv, acc);
+        mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_pv, acc);
+      }
       if (a.causal && g == J - 1) {
-        // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V
+        // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V,
+        // into the S buffer no tile uses any more
         const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
+        const uint32_t tcd = tm + sm1_sbuf(J % CF::NB);
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_f16kind(tm + CF::TM_C, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4),
+          mma_f16kind(tcd, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4),
                       vd + 128 * kk, id_pv, kk > 0 ? 1u : 0u);
       }
-      mma_commit(&ms->a_done);
-      mma_commit(&ms->kv_empty[st]);
+      mma_commit(&ms->kv_empty[st]);  // also tells the epilogue that A holds tile g
     }
     __syncwarp();
-    if (g + 2 < J) ok = issue_s(g + 2);
+    if (g + CF::NB < J) ok = issue_s(g + CF::NB);
   }
   if (leader) {
     if (ok) mma_commit(&ms->o_full);
@@ -633,13 +634,21 @@ __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   __syncwarp();
 }
 
-// Warps 2 and 3: the column sums of V over the key tiles before the diagonal one (all tiles in
-// encoder mode), C's part that is the same for every row.  Thread (rg, cg) adds rows
-// 16 rg .. 16 rg + 15, columns 8 cg .. 8 cg + 7 of each tile; each stage is released once both
-// warps and the tensor cores are done with it.
-__device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
+// Warps 2 and 3: the parts of C and P_t that are the same for every row.  First the key column
+// sums of the tiles before the last one (K_base, from the per-tile statistics, tiles in order);
+// then the column sums of V over the key tiles before the diagonal one (all tiles in encoder
+// mode), thread (rg, cg) adding rows 16 rg .. 16 rg + 15, columns 8 cg .. 8 cg + 7 of each tile;
+// each stage is released once both warps and the tensor cores are done with it.
+__device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int J) {
   using CF = Sm1Cfg;
   const int t = threadIdx.x - 64, cg = t & 7, rg = t >> 3;
+  {
+    const int nt = (a.N + kT - 1) / kT;
+    const float* kst = a.kstat + (size_t)bh * nt * kSmStat + t;
+    float s = 0.0f;
+    for (int g = 0; g < J - 1; ++g) s += kst[(size_t)g * kSmStat];
+    reinterpret_cast<float*>(smem + CF::KBASE_OFF)[t] = s;
+  }
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
@@ -684,7 +693,7 @@ __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
 }
 
 // Both warpgroups take every key tile; warpgroup w its keys 64 w .. 64 w + 63.  Thread = query
-// row of the tile.
+// row of the tile; warp wq of warpgroup 0 and warp wq of warpgroup 1 hold the same 32 rows.
 __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J,
                              int w) {
   using CF = Sm1Cfg;
@@ -700,22 +709,51 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   const float tc = a.causal ? (float)(t + 1) : (float)a.N;
   constexpr float inv_sqrt_d = 0.125f;                      // d = 64
   constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
+  const int nt = (a.N + kT - 1) / kT;
+  const float* kn2 = a.kstat + (size_t)bh * nt * kSmStat + 64;  // largest |k|^2 of each tile
   float* xmax = reinterpret_cast<float*>(smem + CF::XMAX_OFF);
+  bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
+  // |q_t| of this row (the bf16 values the tensor cores read), for the bound of its logits;
+  // warpgroup 0 computes it and both warps of the row pair take that one value, so that their
+  // exchange decisions below agree whatever happens
+  float* qnorm = reinterpret_cast<float*>(smem + CF::QN_OFF);
+  if (w == 0) {
+    float qn = 0.0f;
+    const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 u = lds128(qrow + sw128_off(r, c));
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        float lo, hi;
+        unpack_bf16x2(wv[y], lo, hi);
+        qn = __fmaf_rn(lo, lo, __fmaf_rn(hi, hi, qn));
+      }
+    }
+    qnorm[r] = sqrtf(qn) * (c2 * CF::kBoundSlack);
+  }
+  named_bar_sync(3 + wq, 64);
+  const float qn = qnorm[r];
   float m2 = -INFINITY, l = 0.0f;  // the row's reference (base-2 units), this half's exp-sum
-  bool ok = true;
-  // Every iteration reaches the one named barrier of the tile, also after a failed wait (the
-  // work is then skipped), so that the two warpgroups never wait on it for each other in vain.
+  float2 xs = make_float2(0.0f, 0.0f);  // this half's sum of the last tile's bf16 logits
+  int ex = 0;                           // exchanges so far (alternating buffers)
+  float kn_next = kn2[0];
+  // Every iteration takes the same exchange decisions in both warps of a row pair, also after a
+  // failed wait (the work is then skipped), so that neither waits on the pair barrier in vain.
   for (int g = 0; g < J; ++g) {
-    const int b = g & 1;
+    const int b = g % CF::NB;
+    const float kn = kn_next;
+    if (g + 1 < J) kn_next = kn2[(size_t)(g + 1) * kSmStat];
     if (ok) {
-      ok = mbar_wait_warp(&ms->s_full[b], (g >> 1) & 1, &ms->abort);
+      ok = mbar_wait_warp(&ms->s_full[b], (g / CF::NB) & 1, &ms->abort);
       if (!ok) ms->abort = 1;
     }
-    const uint32_t ts = tl + (b ? CF::TM_S1 : CF::TM_S0) + 64 * w;  // this half's columns
-    const int k0 = g * kT + 64 * w;                                 // its first key
+    const uint32_t ts = tl + sm1_sbuf(b) + 64 * w;  // this half's columns
+    const int k0 = g * kT + 64 * w;                 // its first key
     const bool full = k0 + 63 <= lim_warp;
+    const bool last = g == J - 1;
     uint32_t ra[32], rb[32];
-    float cm = -INFINITY;
     if (ok) {
       tc_fence_after();
       tmem_ld32_nowait(ts, ra);
@@ -724,53 +762,60 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
       reg_fence(ra);
       reg_fence(rb);
     }
-    // ---- the row's maximum over this half, then over the tile ----
-    if (!ok) {
-    } else if (full) {
+    // ---- the reference rises only if some logit of the tile may exceed it by more than
+    //      kRaise: c2 x <= c2 |q_t| max |k| (Cauchy-Schwarz) rules that out for most tiles;
+    //      otherwise the two halves' maxima are exchanged (both warps decide alike) ----
+    const bool exch = !__all_sync(0xffffffffu, qn * sqrtf(kn) <= m2 + CF::kRaise);
+    if (exch) {
+      float cm = -INFINITY;
+      if (!ok) {
+      } else if (full) {
 #pragma unroll
-      for (int x = 0; x < 32; ++x)
-        cm = fmaxf(cm, fmaxf(__uint_as_float(ra[x]), __uint_as_float(rb[x])));
-    } else {
+        for (int x = 0; x < 32; ++x)
+          cm = fmaxf(cm, fmaxf(__uint_as_float(ra[x]), __uint_as_float(rb[x])));
+      } else {
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        if (k0 + x <= lim) cm = fmaxf(cm, __uint_as_float(ra[x]));
-        if (k0 + 32 + x <= lim) cm = fmaxf(cm, __uint_as_float(rb[x]));
-      }
-    }
-    float* xm = xmax + b * 2 * kT;  // double-buffered: the next tile writes the other half
-    xm[w * kT + r] = cm;
-    named_bar_sync(1, 256);
-    if (!ok) continue;
-    const float tmx = fmaxf(xm[r], xm[kT + r]) * c2;
-    // ---- lazy rise of the reference: both warpgroups decide alike for a row ----
-    const bool raise = tmx > m2 + CF::kRaise;  // false for a row without visible keys yet
-    if (__any_sync(0xffffffffu, raise)) {
-      const float f = (raise && m2 != -INFINITY) ? ex2(m2 - tmx) : 1.0f;
-      if (w == 0 && g >= 1) {
-        // A's earlier tiles: wait until their products have completed, then rescale
-        ok = mbar_wait_warp(&ms->a_done, (g - 1) & 1, &ms->abort);
-        if (!ok) {
-          ms->abort = 1;
-          continue;
+        for (int x = 0; x < 32; ++x) {
+          if (k0 + x <= lim) cm = fmaxf(cm, __uint_as_float(ra[x]));
+          if (k0 + 32 + x <= lim) cm = fmaxf(cm, __uint_as_float(rb[x]));
         }
-        tc_fence_after();
+      }
+      float* xm = xmax + (ex & 1) * 2 * kT;
+      ++ex;
+      xm[w * kT + r] = cm;
+      named_bar_sync(3 + wq, 64);
+      const float tmx = fmaxf(xm[r], xm[kT + r]) * c2;
+      const bool raise = tmx > m2 + CF::kRaise;  // false for a row without visible keys yet
+      if (__any_sync(0xffffffffu, raise)) {
+        const float f = (raise && m2 != -INFINITY) ? ex2(m2 - tmx) : 1.0f;
+        if (raise) {
+          l *= f;
+          m2 = tmx;
+        }
+        if (ok && w == 0 && g >= 1) {
+          // A's earlier tiles: wait until their products have completed (the commit that frees
+          // tile g-1's stage follows them), then rescale
+          ok = mbar_wait_warp(&ms->kv_empty[(g - 1) % CF::NS], ((g - 1) / CF::NS) & 1, &ms->abort);
+          if (!ok) ms->abort = 1;
+          if (ok) {
+            tc_fence_after();
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          uint32_t av[16];
-          tmem_ld16_nowait(tl + CF::TM_A + 16 * q, av);
-          tmem_wait_ld();
-          reg_fence(av);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t av[16];
+              tmem_ld16_nowait(tl + CF::TM_A + 16 * q, av);
+              tmem_wait_ld();
+              reg_fence(av);
 #pragma unroll
-          for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
-          tmem_st16_nowait(tl + CF::TM_A + 16 * q, av);
+              for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
+              tmem_st16_nowait(tl + CF::TM_A + 16 * q, av);
+            }
+          }
         }
       }
-      if (raise) {
-        l *= f;
-        m2 = tmx;
-      }
     }
-    // ---- P = 2^{c2 x - m} and x as bf16 pairs over this half's own columns ----
+    if (!ok) continue;
+    // ---- P = 2^{c2 x - m} and x as bf16 pairs over this half's own columns; the last tile's
+    //      rounded logits are summed (the earlier tiles' sum comes from K_base) ----
     auto chunk_px = [&](const uint32_t (&rv)[32], const int ch) {
       float2 ls = make_float2(0.0f, 0.0f);
       if (full) {
@@ -787,6 +832,9 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
             ls = __fadd2_rn(ls, pe);
             pp[y] = pack_bf16x2(pe.x, pe.y);
             xp[y] = pack_bf16x2(xv.x, xv.y);
+            if (last)
+              xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
+                                              __uint_as_float(xp[y] & 0xffff0000u)));
           }
           tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
           tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
@@ -810,6 +858,9 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
             ls.y += pe[1];
             pp[y] = pack_bf16x2(pe[0], pe[1]);
             xp[y] = pack_bf16x2(xe[0], xe[1]);
+            if (last)
+              xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
+                                              __uint_as_float(xp[y] & 0xffff0000u)));
           }
           tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
           tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
@@ -821,17 +872,19 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
     chunk_px(rb, 1);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(&ms->w_full[b][w]);
+    mbar_arrive(&ms->w_full[b]);
   }
   if (!ok) {
     report(a.status, kErrTimeout);
     ms->abort = 1;
   }
-  // ---- the two halves' exp-sums, both relative to the row's common reference ----
-  float* stat = reinterpret_cast<float*>(smem + CF::STAT_OFF);
-  stat[w * kT + r] = l;
+  // ---- the two halves' exp-sums (both relative to the row's common reference) and last-tile
+  //      logit sums ----
+  float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
+  stat[w * kT + r] = make_float2(l, xs.x + xs.y);
   named_bar_sync(1, 256);
-  const float lt = stat[r] + stat[kT + r];
+  const float2 s0 = stat[r], s1 = stat[kT + r];
+  const float lt = s0.x + s1.x;
   if (ms->abort) return;
   // ---- output: O = alpha A + beta B + gamma C; warpgroup w writes columns 32 w .. 32 w + 31
   //      of its rows ----
@@ -847,14 +900,28 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
     sigh = sigmoid(a.gh[row]);
     if (a.g0) sig0 = sigmoid(a.g0[row]);
   }
+  // the logit sum: q_t . K_base over the earlier tiles, plus the last tile's bf16 logits
+  float qk = 0.0f;
+  {
+    const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
+    const float* kb = reinterpret_cast<const float*>(smem + CF::KBASE_OFF);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 u = lds128(qrow + sw128_off(r, c));
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        float lo, hi;
+        unpack_bf16x2(wv[y], lo, hi);
+        qk = __fmaf_rn(lo, kb[8 * c + 2 * y], qk);
+        qk = __fmaf_rn(hi, kb[8 * c + 2 * y + 1], qk);
+      }
+    }
+  }
   const float rt = 1.0f / tc;
   const float alpha = lt > 0.0f ? sigh / lt : 0.0f;
   const float beta = (sig1 - sigh) * rt;
-  uint32_t pt[16];
-  tmem_ld16_nowait(tl + CF::TM_B + 64, pt);  // column 64: the sum of the row's bf16 logits
-  tmem_wait_ld();
-  reg_fence(pt);
-  const float Pt = __uint_as_float(pt[0]) * inv_sqrt_d;
+  const float Pt = (qk + s0.y + s1.y) * inv_sqrt_d;
   const float bs = beta * inv_sqrt_d;
   const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
   const int c0 = 32 * w;
@@ -865,7 +932,7 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
     uint32_t av[16], bv[16], cv[16];
     tmem_ld16_nowait(tl + CF::TM_A + c0 + 16 * hh, av);
     tmem_ld16_nowait(tl + CF::TM_B + c0 + 16 * hh, bv);
-    if (a.causal) tmem_ld16_nowait(tl + CF::TM_C + c0 + 16 * hh, cv);
+    if (a.causal) tmem_ld16_nowait(tl + sm1_sbuf(J % CF::NB) + c0 + 16 * hh, cv);
     tmem_wait_ld();
     reg_fence(av);
     reg_fence(bv);
@@ -912,39 +979,28 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
       mbar_init(&ms->kv_full[i], 1);
       mbar_init(&ms->kv_empty[i], 3);  // the tensor cores and the two column-sum warps
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < CF::NB; ++i) {
       mbar_init(&ms->s_full[i], 1);
-      mbar_init(&ms->w_full[i][0], 128);
-      mbar_init(&ms->w_full[i][1], 128);
+      mbar_init(&ms->w_full[i], 256);  // both epilogue warpgroups
     }
-    mbar_init(&ms->a_done, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->fin, 1);
     mbar_init(&ms->cb_full, 1);
     ms->abort = 0;
     ms->never = 0;
   }
-  // constant operand tiles: the lower-triangular ones [query row][key] (K-major, two atoms of
-  // 64 keys: 1 where key <= row) and V's extension [key][64 columns] (MN-major: column 0 is 1,
-  // the rest 0), both 128-byte swizzled
-  for (int idx = threadIdx.x; idx < 3 * kT * 8; idx += kSmThreads) {
+  // the lower-triangular ones tile [query row][key] (K-major, two atoms of 64 keys: 1 where
+  // key <= row), 128-byte swizzled
+  for (int idx = threadIdx.x; idx < 2 * kT * 8; idx += kSmThreads) {
     const int part = idx / (kT * 8), rr = (idx / 8) % kT, c = idx % 8;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t off;
-    if (part < 2) {
-      uint32_t wv[4];
+    uint32_t wv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key0 = 64 * part + 8 * c + 2 * e;
-        wv[e] = pack_bf16x2(key0 <= rr ? 1.0f : 0.0f, key0 + 1 <= rr ? 1.0f : 0.0f);
-      }
-      val = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      off = CF::TRI_OFF + part * kAtom + sw128_off(rr, c);
-    } else {
-      if (c == 0) val.x = pack_bf16x2(1.0f, 0.0f);
-      off = CF::ONE_OFF + sw128_off(rr, c);
+    for (int e = 0; e < 4; ++e) {
+      const int key0 = 64 * part + 8 * c + 2 * e;
+      wv[e] = pack_bf16x2(key0 <= rr ? 1.0f : 0.0f, key0 + 1 <= rr ? 1.0f : 0.0f);
     }
-    *reinterpret_cast<uint4*>(smem + off) = val;
+    *reinterpret_cast<uint4*>(smem + CF::TRI_OFF + part * kAtom + sw128_off(rr, c)) =
+        make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
   fence_proxy_async_smem();  // written by the threads, read by the tensor cores
   if (warp == 1) {
@@ -960,7 +1016,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
   } else if (warp == 1) {
     sm1_mma(a, smem, ms, J);
   } else if (warp < 4) {
-    sm1_colsum(a, smem, ms, J);
+    sm1_colsum(a, smem, ms, bh, J);
   } else {
     sm1_epilogue(a, smem, ms, bh, qt, J, (warp - 4) >> 2);
   }
@@ -1010,6 +1066,100 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
     }
     *reinterpret_cast<uint4*>(y + o) = make_uint4(ra[0], ra[1], ra[2], ra[3]);
     *reinterpret_cast<uint4*>(y + o + half) = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+  }
+}
+
+// d = 64: one CTA of 512 threads per 128-key tile of one (b, h).  Thread (row r = tid / 4,
+// part p = tid % 4) holds the pairs 8 p .. 8 p + 7 of the tile's row r of k (and of q when
+// rotating): columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.  With a rotary table the row
+// is rotated exactly as sm_rotate_kernel does it and rounded to bf16 once; the statistics are
+// those of the bf16 values the attention kernel reads: the 64 column sums over the tile's keys
+// (fp32; four 32-row partial sums, added in order) and the largest squared row norm.
+__global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __restrict__ xq,
+                                                      const __nv_bfloat16* __restrict__ xk,
+                                                      __nv_bfloat16* __restrict__ yq,
+                                                      __nv_bfloat16* __restrict__ yk,
+                                                      const float2* __restrict__ table,
+                                                      float* __restrict__ kstat, int N, int nt) {
+  __shared__ __align__(16) __nv_bfloat16 sk[kT][64];
+  __shared__ float part[4][64];
+  __shared__ float wmax[16];
+  const int tile = (int)(blockIdx.x % (unsigned)nt);
+  const size_t bh = blockIdx.x / (unsigned)nt;
+  const int tid = threadIdx.x, r = tid >> 2, p = tid & 3;
+  const int n = tile * kT + r;
+  const bool valid = n < N;
+  const size_t off = (bh * N + (size_t)(valid ? n : 0)) * 64 + 8 * p;
+  uint4 ka = make_uint4(0, 0, 0, 0), kb = ka;
+  if (valid) {
+    ka = *reinterpret_cast<const uint4*>(xk + off);
+    kb = *reinterpret_cast<const uint4*>(xk + off + 32);
+  }
+  if (table != nullptr && valid) {
+    const float4* tb = reinterpret_cast<const float4*>(table + (size_t)n * 32 + 8 * p);
+    float4 cs[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cs[e] = tb[e];  // (cos, sin) of pairs 8 p + 2 e, 8 p + 2 e + 1
+    auto rotate = [&](uint4& ua, uint4& ub) {
+      uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float xa0, xa1, xb0, xb1;
+        unpack_bf16x2(wa[e], xa0, xa1);
+        unpack_bf16x2(wb[e], xb0, xb1);
+        wa[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].x, -xb0 * cs[e].y),
+                            __fmaf_rn(xa1, cs[e].z, -xb1 * cs[e].w));
+        wb[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].y, xb0 * cs[e].x),
+                            __fmaf_rn(xa1, cs[e].w, xb1 * cs[e].z));
+      }
+      ua = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      ub = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    };
+    rotate(ka, kb);
+    uint4 qa = *reinterpret_cast<const uint4*>(xq + off);
+    uint4 qb = *reinterpret_cast<const uint4*>(xq + off + 32);
+    rotate(qa, qb);
+    *reinterpret_cast<uint4*>(yq + off) = qa;
+    *reinterpret_cast<uint4*>(yq + off + 32) = qb;
+    *reinterpret_cast<uint4*>(yk + off) = ka;
+    *reinterpret_cast<uint4*>(yk + off + 32) = kb;
+  }
+  // squared row norm (this thread's 16 values, then the row), the tile's largest
+  float n2 = 0.0f;
+  {
+    const uint32_t w8[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float x0, x1;
+      unpack_bf16x2(w8[e], x0, x1);
+      n2 = __fmaf_rn(x0, x0, n2);
+      n2 = __fmaf_rn(x1, x1, n2);
+    }
+  }
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+  if ((tid & 31) == 0) wmax[tid >> 5] = n2;
+  *reinterpret_cast<uint4*>(&sk[r][8 * p]) = ka;
+  *reinterpret_cast<uint4*>(&sk[r][32 + 8 * p]) = kb;
+  __syncthreads();
+  if (tid < 256) {
+    const int c = tid & 63, qq = tid >> 6;
+    float sum = 0.0f;
+#pragma unroll 8
+    for (int rr = 32 * qq; rr < 32 * qq + 32; ++rr) sum += __bfloat162float(sk[rr][c]);
+    part[qq][c] = sum;
+  }
+  __syncthreads();
+  float* st = kstat + (bh * nt + tile) * kSmStat;
+  if (tid < 64) {
+    st[tid] = ((part[0][tid] + part[1][tid]) + part[2][tid]) + part[3][tid];
+  } else if (tid == 64) {
+    float m = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 16; ++w) m = fmaxf(m, wmax[w]);
+    st[64] = m;
   }
 }
 
@@ -1110,6 +1260,19 @@ cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
   sm_rotate_kernel<<<blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<__nv_bfloat16*>(yq), static_cast<__nv_bfloat16*>(yk), table, N, d, groups);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sm_prep(const void* q, const void* k, void* yq, void* yk, const float2* table,
+                           float* kstat, int BH, int N, cudaStream_t stream) {
+  const int nt = (N + kT - 1) / kT;
+  const size_t ctas = (size_t)BH * nt;
+  if (ctas == 0) return cudaSuccess;
+  if (ctas > 0x7fffffffu) return cudaErrorInvalidValue;
+  sm_prep_kernel<<<(unsigned)ctas, 512, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<__nv_bfloat16*>(yq), static_cast<__nv_bfloat16*>(yk), table, kstat, N, nt);
   count_launches(1);
   return cudaGetLastError();
 }
