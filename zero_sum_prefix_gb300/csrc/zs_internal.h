@@ -66,11 +66,12 @@ struct SmArgs {
   void* out;
   int B, H, N, d, causal;
   int* status;
-  // d = 64: per 128-key tile of k (as the kernel reads it), [B*H][tiles][kSmStat] fp32: the
-  // column sums (64) and the largest squared row norm; written by launch_sm_prep
+  // d = 64: per 128-key tile, [B*H][tiles][kSmStat] fp32: the column sums of k as the kernel
+  // reads it (0..63), the largest squared row norm of k (64), the column sums of v (68..131);
+  // written by launch_sm_prep
   const float* kstat;
 };
-constexpr int kSmStat = 68;
+constexpr int kSmStat = 132;
 
 // Counts every kernel launch the library issues (zs_api.cu).
 void count_launches(unsigned n);
@@ -138,7 +139,7 @@ cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
                              const float2* table, int BH, int N, int d, cudaStream_t stream);
 // d = 64: the key-tile statistics of SmArgs::kstat, and with a rotary table also the rotated q
 // and k (into yq, yk; as launch_sm_rotate writes them), in one pass.
-cudaError_t launch_sm_prep(const void* q, const void* k, void* yq, void* yk, const float2* table,
-                           float* kstat, int BH, int N, cudaStream_t stream);
+cudaError_t launch_sm_prep(const void* q, const void* k, const void* v, void* yq, void* yk,
+                           const float2* table, float* kstat, int BH, int N, cudaStream_t stream);
 
 }  // namespace zs

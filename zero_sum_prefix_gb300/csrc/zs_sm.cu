@@ -492,12 +492,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
 // sum of the last tile's bf16 logits, the very values that B sums there: for the rows of the
 // first query tile (few keys) the weights alpha P + beta x / sqrt d + gamma then sum to sig0 up to
 // the fp32 rounding of the sums (exactly zero output for a single visible key), and elsewhere the
-// roundings only perturb each weight.  C does not depend on the query: the column sums of the key
-// tiles before the diagonal one are added up on the CUDA cores by two otherwise idle warps, and
-// the diagonal tile's prefix comes from one product with a lower-triangular ones tile at the
-// end.  Each tile's largest key norm (with the key column sums, from a pass that also applies
-// the rotary map) bounds its logits: where c2 |q_t| max |k| cannot exceed the reference by more
-// than kRaise, the tile's maximum is not needed at all.
+// roundings only perturb each weight.  C does not depend on the query: it is the sum of the value
+// column sums of the key tiles before the diagonal one, and the diagonal tile's prefix comes from
+// one product with a lower-triangular ones tile at the end.  The per-tile column sums of k and v
+// and each tile's largest key norm come from a pass that also applies the rotary map; the norm
+// bounds the tile's logits: where c2 |q_t| max |k| cannot exceed the reference by more than
+// kRaise, the tile's maximum is not needed at all.
 // Three S buffers: S_{g+3} is formed as soon as tile g's products are issued, so the tensor
 // cores, the exponentials of tile g+1 and the products of tile g overlap.  Both epilogue
 // warpgroups work on every key tile, warpgroup w on its keys 64 w .. 64 w + 63; where the bound
@@ -517,8 +517,7 @@ struct Sm1Cfg {
   static constexpr uint32_t TRI_OFF = STAGE_OFF + NS * STAGE;  // [128 x 128] lower-triangular ones
   static constexpr uint32_t XMAX_OFF = TRI_OFF + 2 * kAtom;    // float [2 bufs][2 halves][128]
   static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float2 [2][128] sums
-  static constexpr uint32_t CSUM_OFF = STAT_OFF + 2 * kT * 8;  // float [8][64] partial sums
-  static constexpr uint32_t CBASE_OFF = CSUM_OFF + 8 * 64 * 4; // float [64]
+  static constexpr uint32_t CBASE_OFF = STAT_OFF + 2 * kT * 8;  // float [64]
   static constexpr uint32_t KBASE_OFF = CBASE_OFF + 64 * 4;    // float [64]
   static constexpr uint32_t QN_OFF = KBASE_OFF + 64 * 4;       // float [128]
   static constexpr uint32_t MISC_OFF = QN_OFF + kT * 4;
@@ -634,60 +633,21 @@ __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   __syncwarp();
 }
 
-// Warps 2 and 3: the parts of C and P_t that are the same for every row.  First the key column
-// sums of the tiles before the last one (K_base, from the per-tile statistics, tiles in order);
-// then the column sums of V over the key tiles before the diagonal one (all tiles in encoder
-// mode), thread (rg, cg) adding rows 16 rg .. 16 rg + 15, columns 8 cg .. 8 cg + 7 of each tile;
-// each stage is released once both warps and the tensor cores are done with it.
+// Warps 2 and 3: the parts of C and P_t that are the same for every row, from the per-tile
+// statistics (tiles in order): K_base = the key column sums of the tiles before the last one,
+// C_base = the value column sums of the tiles before the diagonal one (all tiles in encoder
+// mode).
 __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int J) {
   using CF = Sm1Cfg;
-  const int t = threadIdx.x - 64, cg = t & 7, rg = t >> 3;
-  {
-    const int nt = (a.N + kT - 1) / kT;
-    const float* kst = a.kstat + (size_t)bh * nt * kSmStat + t;
-    float s = 0.0f;
-    for (int g = 0; g < J - 1; ++g) s += kst[(size_t)g * kSmStat];
-    reinterpret_cast<float*>(smem + CF::KBASE_OFF)[t] = s;
-  }
-  float acc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  bool ok = true;
-  for (int g = 0; g < J && ok; ++g) {
-    const int st = g % CF::NS;
-    ok = mbar_wait_warp(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort);
-    if (!ok) break;
-    if (!a.causal || g < J - 1) {
-      const uint32_t vt = smem_u32(smem) + CF::STAGE_OFF + st * CF::STAGE + kAtom;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int r = 16 * rg + i;
-        const uint4 w = lds128(vt + sw128_off(r, cg));
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          float lo, hi;
-          unpack_bf16x2(wv[y], lo, hi);
-          acc[2 * y] += lo;
-          acc[2 * y + 1] += hi;
-        }
-      }
-    }
-    __syncwarp();
-    if ((t & 31) == 0) mbar_arrive(&ms->kv_empty[st]);
-  }
-  if (!ok) {
-    report(a.status, kErrTimeout);
-    ms->abort = 1;
-  }
-  float* part = reinterpret_cast<float*>(smem + CF::CSUM_OFF);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) part[rg * 64 + 8 * cg + j] = acc[j];
-  named_bar_sync(2, 64);
-  float s = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) s += part[q * 64 + t];
-  reinterpret_cast<float*>(smem + CF::CBASE_OFF)[t] = s;
+  const int t = threadIdx.x - 64;  // column
+  const int nt = (a.N + kT - 1) / kT;
+  const float* st = a.kstat + (size_t)bh * nt * kSmStat;
+  float sk = 0.0f, sv = 0.0f;
+  const int nv = a.causal ? J - 1 : J;
+  for (int g = 0; g < J - 1; ++g) sk += st[(size_t)g * kSmStat + t];
+  for (int g = 0; g < nv; ++g) sv += st[(size_t)g * kSmStat + 68 + t];
+  reinterpret_cast<float*>(smem + CF::KBASE_OFF)[t] = sk;
+  reinterpret_cast<float*>(smem + CF::CBASE_OFF)[t] = sv;
   named_bar_sync(2, 64);
   if (t == 0) mbar_arrive(&ms->cb_full);
 }
@@ -977,7 +937,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
     mbar_init(&ms->q_full, 1);
     for (int i = 0; i < CF::NS; ++i) {
       mbar_init(&ms->kv_full[i], 1);
-      mbar_init(&ms->kv_empty[i], 3);  // the tensor cores and the two column-sum warps
+      mbar_init(&ms->kv_empty[i], 1);
     }
     for (int i = 0; i < CF::NB; ++i) {
       mbar_init(&ms->s_full[i], 1);
@@ -1071,18 +1031,20 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
 
 // d = 64: one CTA of 512 threads per 128-key tile of one (b, h).  Thread (row r = tid / 4,
 // part p = tid % 4) holds the pairs 8 p .. 8 p + 7 of the tile's row r of k (and of q when
-// rotating): columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.  With a rotary table the row
-// is rotated exactly as sm_rotate_kernel does it and rounded to bf16 once; the statistics are
-// those of the bf16 values the attention kernel reads: the 64 column sums over the tile's keys
-// (fp32; four 32-row partial sums, added in order) and the largest squared row norm.
+// rotating), and the same columns of v: columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.
+// With a rotary table the row is rotated exactly as sm_rotate_kernel does it and rounded to bf16
+// once; the statistics are those of the bf16 values the attention kernel reads: the 64 column
+// sums of k and of v over the tile's keys (fp32; four 32-row partial sums, added in order) and
+// the largest squared row norm of k.
 __global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __restrict__ xq,
                                                       const __nv_bfloat16* __restrict__ xk,
+                                                      const __nv_bfloat16* __restrict__ xv,
                                                       __nv_bfloat16* __restrict__ yq,
                                                       __nv_bfloat16* __restrict__ yk,
                                                       const float2* __restrict__ table,
                                                       float* __restrict__ kstat, int N, int nt) {
-  __shared__ __align__(16) __nv_bfloat16 sk[kT][64];
-  __shared__ float part[4][64];
+  __shared__ __align__(16) __nv_bfloat16 sk[2][kT][64];  // k, v
+  __shared__ float part[4][128];
   __shared__ float wmax[16];
   const int tile = (int)(blockIdx.x % (unsigned)nt);
   const size_t bh = blockIdx.x / (unsigned)nt;
@@ -1090,10 +1052,12 @@ __global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __res
   const int n = tile * kT + r;
   const bool valid = n < N;
   const size_t off = (bh * N + (size_t)(valid ? n : 0)) * 64 + 8 * p;
-  uint4 ka = make_uint4(0, 0, 0, 0), kb = ka;
+  uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
   if (valid) {
     ka = *reinterpret_cast<const uint4*>(xk + off);
     kb = *reinterpret_cast<const uint4*>(xk + off + 32);
+    va = *reinterpret_cast<const uint4*>(xv + off);
+    vb = *reinterpret_cast<const uint4*>(xv + off + 32);
   }
   if (table != nullptr && valid) {
     const float4* tb = reinterpret_cast<const float4*>(table + (size_t)n * 32 + 8 * p);
@@ -1141,21 +1105,24 @@ __global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __res
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
   if ((tid & 31) == 0) wmax[tid >> 5] = n2;
-  *reinterpret_cast<uint4*>(&sk[r][8 * p]) = ka;
-  *reinterpret_cast<uint4*>(&sk[r][32 + 8 * p]) = kb;
+  *reinterpret_cast<uint4*>(&sk[0][r][8 * p]) = ka;
+  *reinterpret_cast<uint4*>(&sk[0][r][32 + 8 * p]) = kb;
+  *reinterpret_cast<uint4*>(&sk[1][r][8 * p]) = va;
+  *reinterpret_cast<uint4*>(&sk[1][r][32 + 8 * p]) = vb;
   __syncthreads();
-  if (tid < 256) {
-    const int c = tid & 63, qq = tid >> 6;
+  {
+    const int c = tid & 127, qq = tid >> 7;  // column c of k (c < 64) or of v
+    const __nv_bfloat16* col = &sk[c >> 6][0][c & 63];
     float sum = 0.0f;
 #pragma unroll 8
-    for (int rr = 32 * qq; rr < 32 * qq + 32; ++rr) sum += __bfloat162float(sk[rr][c]);
+    for (int rr = 32 * qq; rr < 32 * qq + 32; ++rr) sum += __bfloat162float(col[rr * 64]);
     part[qq][c] = sum;
   }
   __syncthreads();
   float* st = kstat + (bh * nt + tile) * kSmStat;
-  if (tid < 64) {
-    st[tid] = ((part[0][tid] + part[1][tid]) + part[2][tid]) + part[3][tid];
-  } else if (tid == 64) {
+  if (tid < 128) {
+    st[tid < 64 ? tid : tid + 4] = ((part[0][tid] + part[1][tid]) + part[2][tid]) + part[3][tid];
+  } else if (tid == 128) {
     float m = wmax[0];
 #pragma unroll
     for (int w = 1; w < 16; ++w) m = fmaxf(m, wmax[w]);
@@ -1264,15 +1231,16 @@ cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
   return cudaGetLastError();
 }
 
-cudaError_t launch_sm_prep(const void* q, const void* k, void* yq, void* yk, const float2* table,
-                           float* kstat, int BH, int N, cudaStream_t stream) {
+cudaError_t launch_sm_prep(const void* q, const void* k, const void* v, void* yq, void* yk,
+                           const float2* table, float* kstat, int BH, int N, cudaStream_t stream) {
   const int nt = (N + kT - 1) / kT;
   const size_t ctas = (size_t)BH * nt;
   if (ctas == 0) return cudaSuccess;
   if (ctas > 0x7fffffffu) return cudaErrorInvalidValue;
   sm_prep_kernel<<<(unsigned)ctas, 512, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<__nv_bfloat16*>(yq), static_cast<__nv_bfloat16*>(yk), table, kstat, N, nt);
+      static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(yq),
+      static_cast<__nv_bfloat16*>(yk), table, kstat, N, nt);
   count_launches(1);
   return cudaGetLastError();
 }
