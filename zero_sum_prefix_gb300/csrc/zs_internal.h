@@ -67,7 +67,7 @@ struct SmArgs {
   int B, H, N, d, causal;
   int* status;
   // d = 64: per 128-key tile, [B*H][tiles][kSmStat] fp32: the column sums of k as the kernel
-  // reads it (0..63), the largest squared row norm of k (64), the column sums of v (68..131);
+  // reads it (0..63), the largest row norm of k (64), the column sums of v (68..131);
   // written by launch_sm_prep
   const float* kstat;
 };

@@ -634,18 +634,26 @@ __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
 }
 
 // Warps 2 and 3: the parts of C and P_t that are the same for every row, from the per-tile
-// statistics (tiles in order): K_base = the key column sums of the tiles before the last one,
-// C_base = the value column sums of the tiles before the diagonal one (all tiles in encoder
-// mode).
+// statistics: K_base = the key column sums of the tiles before the last one, C_base = the value
+// column sums of the tiles before the diagonal one (all tiles in encoder mode); eight partial
+// sums over the tiles (g = 8 j + u), added in a fixed order, so that the loads overlap.
 __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int J) {
   using CF = Sm1Cfg;
   const int t = threadIdx.x - 64;  // column
   const int nt = (a.N + kT - 1) / kT;
-  const float* st = a.kstat + (size_t)bh * nt * kSmStat;
-  float sk = 0.0f, sv = 0.0f;
-  const int nv = a.causal ? J - 1 : J;
-  for (int g = 0; g < J - 1; ++g) sk += st[(size_t)g * kSmStat + t];
-  for (int g = 0; g < nv; ++g) sv += st[(size_t)g * kSmStat + 68 + t];
+  const float* st = a.kstat + (size_t)bh * nt * kSmStat + t;
+  float pk[8] = {}, pv[8] = {};
+  const int nk = J - 1, nv = a.causal ? J - 1 : J;
+  for (int g0 = 0; g0 < nv; g0 += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int g = g0 + u;
+      if (g < nk) pk[u] += st[(size_t)g * kSmStat];
+      if (g < nv) pv[u] += st[(size_t)g * kSmStat + 68];
+    }
+  }
+  const float sk = ((pk[0] + pk[1]) + (pk[2] + pk[3])) + ((pk[4] + pk[5]) + (pk[6] + pk[7]));
+  const float sv = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
   reinterpret_cast<float*>(smem + CF::KBASE_OFF)[t] = sk;
   reinterpret_cast<float*>(smem + CF::CBASE_OFF)[t] = sv;
   named_bar_sync(2, 64);
@@ -670,7 +678,14 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   constexpr float inv_sqrt_d = 0.125f;                      // d = 64
   constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
   const int nt = (a.N + kT - 1) / kT;
-  const float* kn2 = a.kstat + (size_t)bh * nt * kSmStat + 64;  // largest |k|^2 of each tile
+  // the row's gate logits, loaded now and used at the end
+  float gl1 = 0.0f, glh = 0.0f, gl0 = 0.0f;
+  if (row_ok) {
+    gl1 = a.g1[row];
+    glh = a.gh[row];
+    if (a.g0) gl0 = a.g0[row];
+  }
+  const float* kn2 = a.kstat + (size_t)bh * nt * kSmStat + 64;  // largest |k| of each tile
   float* xmax = reinterpret_cast<float*>(smem + CF::XMAX_OFF);
   bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
   // |q_t| of this row (the bf16 values the tensor cores read), for the bound of its logits;
@@ -725,7 +740,7 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
     // ---- the reference rises only if some logit of the tile may exceed it by more than
     //      kRaise: c2 x <= c2 |q_t| max |k| (Cauchy-Schwarz) rules that out for most tiles;
     //      otherwise the two halves' maxima are exchanged (both warps decide alike) ----
-    const bool exch = !__all_sync(0xffffffffu, qn * sqrtf(kn) <= m2 + CF::kRaise);
+    const bool exch = !__all_sync(0xffffffffu, qn * kn <= m2 + CF::kRaise);
     if (exch) {
       float cm = -INFINITY;
       if (!ok) {
@@ -832,7 +847,8 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
     chunk_px(rb, 1);
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(&ms->w_full[b]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->w_full[b]);
   }
   if (!ok) {
     report(a.status, kErrTimeout);
@@ -856,9 +872,9 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   tc_fence_after();
   float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
   if (row_ok) {
-    sig1 = sigmoid(a.g1[row]);
-    sigh = sigmoid(a.gh[row]);
-    if (a.g0) sig0 = sigmoid(a.g0[row]);
+    sig1 = sigmoid(gl1);
+    sigh = sigmoid(glh);
+    if (a.g0) sig0 = sigmoid(gl0);
   }
   // the logit sum: q_t . K_base over the earlier tiles, plus the last tile's bf16 logits
   float qk = 0.0f;
@@ -941,7 +957,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
     }
     for (int i = 0; i < CF::NB; ++i) {
       mbar_init(&ms->s_full[i], 1);
-      mbar_init(&ms->w_full[i], 256);  // both epilogue warpgroups
+      mbar_init(&ms->w_full[i], 8);  // the 8 epilogue warps
     }
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->fin, 1);
@@ -1035,7 +1051,7 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
 // With a rotary table the row is rotated exactly as sm_rotate_kernel does it and rounded to bf16
 // once; the statistics are those of the bf16 values the attention kernel reads: the 64 column
 // sums of k and of v over the tile's keys (fp32; four 32-row partial sums, added in order) and
-// the largest squared row norm of k.
+// the largest row norm of k.
 __global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __restrict__ xq,
                                                       const __nv_bfloat16* __restrict__ xk,
                                                       const __nv_bfloat16* __restrict__ xv,
@@ -1126,7 +1142,7 @@ __global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __res
     float m = wmax[0];
 #pragma unroll
     for (int w = 1; w < 16; ++w) m = fmaxf(m, wmax[w]);
-    st[64] = m;
+    st[64] = sqrtf(m);
   }
 }
 
