@@ -862,14 +862,13 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   const float2 s0 = stat[r], s1 = stat[kT + r];
   const float lt = s0.x + s1.x;
   if (ms->abort) return;
-  // ---- output: O = alpha A + beta B + gamma C; warpgroup w writes columns 32 w .. 32 w + 31
-  //      of its rows ----
-  if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort) || !mbar_wait_warp(&ms->cb_full, 0, &ms->abort)) {
+  // ---- the row's coefficients, while the last products complete; then the output:
+  //      O = alpha A + beta B + gamma C, warpgroup w writing columns 32 w .. 32 w + 31 ----
+  if (!mbar_wait_warp(&ms->cb_full, 0, &ms->abort)) {
     report(a.status, kErrTimeout);
     ms->abort = 1;
     return;
   }
-  tc_fence_after();
   float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
   if (row_ok) {
     sig1 = sigmoid(gl1);
@@ -900,6 +899,12 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh
   const float Pt = (qk + s0.y + s1.y) * inv_sqrt_d;
   const float bs = beta * inv_sqrt_d;
   const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
+  if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort)) {
+    report(a.status, kErrTimeout);
+    ms->abort = 1;
+    return;
+  }
+  tc_fence_after();
   const int c0 = 32 * w;
   const float* cbase = reinterpret_cast<const float*>(smem + CF::CBASE_OFF) + c0;
   float o[32];
