@@ -49,13 +49,17 @@ L2_FLUSH_BYTES = 256 << 20
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_walk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
                  "zero_sum_prefix_gb300/csrc/zs_range.cuh", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
                  "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"d273b4b55c6aed51": 33602816 + 0 + 109883392 + 9741824}
+MEASURED_TRAFFIC = {"50aaf296b3681530": 33606656 + 0 + 109523712 + 9813504}
+# the ZeroS-SM workload's dominant kernel (sm1_kernel): DRAM bytes read + written per launch
+SM_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_sm.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
+              "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
+MEASURED_SM_TRAFFIC = {"57337719dfee95a5": 166423552 + 15833600}
 
 
-def kernel_fingerprint() -> str:
+def kernel_fingerprint(sources=None) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in CHUNK_SOURCES:
+    for f in (sources or CHUNK_SOURCES):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -622,8 +626,12 @@ def ours_sm(args, w: zi.Workload):
                        "causal": w.causal, "rope": w.rope, "variant": "ZeroS-SM",
                        "l2": "flushed before every step (256 MB write, outside the events)"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                         "peak_source": kind, "algorithmic_flops_per_launch": sm_flops(w)},
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": (MEASURED_SM_TRAFFIC.get(kernel_fingerprint(SM_SOURCES))
+                                     if w is zi.CAUSAL_ROPE_B8H8N4096D64 else None),
+                         "peak_source": kind, "algorithmic_flops_per_launch": sm_flops(w),
+                         "timed": "the whole zeros_sm_fwd call: statistics and rotary pass + "
+                                  "attention kernel"},
             "cpu_baseline": cpu,
             "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
