@@ -450,8 +450,11 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
 //   X_SV = S V                         (walk chunks; S tile formed)                 -> x_full
 //   stage released                                                                  -> empty
 // MMAs issued by this thread execute in order, so A of a chunk may overwrite the S tile that
-// the previous chunk's S V product reads.
+// the previous chunk's S V product reads.  The whole warp runs this loop (its operands stay
+// warp-uniform, so the issue stays short next to the busy warps of the same scheduler) and one
+// elected lane issues.
 __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, int c1) {
+  const bool leader = elect_one();
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const long long lim = p.wait_limit;
@@ -474,9 +477,12 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
     const bool walk = c >= c0;
     const int wi = c - c0;
     const uint64_t so = (uint64_t)((st * kTile) >> 4);
-    if (!mbar_wait(&ms->opd[st], (uint32_t)(c / kNST) & 1u, &ms->abort, lim)) { ok = false; break; }
+    if (!mbar_wait_warp_lim(&ms->opd[st], (uint32_t)(c / kNST) & 1u, &ms->abort, lim)) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
-    if (walk) {
+    if (walk && leader) {
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint64_t off = (uint64_t)((kk * 32) >> 4);
@@ -484,15 +490,16 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
       }
       mma_commit(&ms->a_full);
     }
+    __syncwarp();
     // ---- state update (M = 128 value rows, N = 64 key columns, K = the chunk's tokens) ----
     if (c >= 1 && c - 1 >= cfirst) {
-      if (!mbar_wait(&ms->st_done, (uint32_t)(c - 1 - cfirst) & 1u, &ms->abort, lim)) {
+      if (!mbar_wait_warp_lim(&ms->st_done, (uint32_t)(c - 1 - cfirst) & 1u, &ms->abort, lim)) {
         ok = false;
         break;
       }
       tc_fence_after();
     }
-    {
+    if (leader) {
       const uint32_t va = base + WLay::V + st * kTile;
       const uint32_t lbo = (base + WLay::VSC) - va;  // [v | e v]: the second atom is e v
       const uint64_t dva = sw128_desc(va, lbo, 1024);
@@ -506,39 +513,55 @@ __device__ void role_mma(const WalkParams& p, uint8_t* smem, WMisc* ms, int c0, 
       mma_commit(&ms->vsc_free);
       if (c >= cfirst && c <= c1 - 2) mma_commit(&ms->u_done);
     }
+    __syncwarp();
     if (walk) {
       if (c > 0) {
         // ---- X = Q [F~ | G | H] with the state before this chunk (its copy was waited for
         //      before the state update) ----
-        if (wi >= 1 && !mbar_wait(&ms->x_free, (uint32_t)(wi - 1) & 1u, &ms->abort, lim)) {
+        if (wi >= 1 &&
+            !mbar_wait_warp_lim(&ms->x_free, (uint32_t)(wi - 1) & 1u, &ms->abort, lim)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t off = (uint64_t)((kk * 32) >> 4);
-          mma_f16kind(tm + TM_X, dq + so + off, dsb + off, id_x, kk > 0);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)((kk * 32) >> 4);
+            mma_f16kind(tm + TM_X, dq + so + off, dsb + off, id_x, kk > 0);
+          }
+          mma_commit(&ms->sb_free);
         }
-        mma_commit(&ms->sb_free);
-      } else if (wi >= 1 && !mbar_wait(&ms->x_free, (uint32_t)(wi - 1) & 1u, &ms->abort, lim)) {
+        __syncwarp();
+      } else if (wi >= 1 &&
+                 !mbar_wait_warp_lim(&ms->x_free, (uint32_t)(wi - 1) & 1u, &ms->abort, lim)) {
         ok = false;
         break;
       }
       // ---- X_SV = S V (S from TMEM) ----
-      if (!mbar_wait(&ms->s_full, (uint32_t)wi & 1u, &ms->abort, lim)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kC / 16; ++kk) {
-        const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows per step
-        mma_f16kind_ts(tm + TM_SV, tm + TM_A + kk * 16, dvb + so + boff, id_sv, kk > 0);
+      if (!mbar_wait_warp_lim(&ms->s_full, (uint32_t)wi & 1u, &ms->abort, lim)) {
+        ok = false;
+        break;
       }
-      mma_commit(&ms->x_full);
+      tc_fence_after();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows/step
+          mma_f16kind_ts(tm + TM_SV, tm + TM_A + kk * 16, dvb + so + boff, id_sv, kk > 0);
+        }
+        mma_commit(&ms->x_full);
+      }
+      __syncwarp();
     }
-    mma_commit(&ms->empty[st]);
+    if (leader) mma_commit(&ms->empty[st]);
+    __syncwarp();
   }
-  if (!ok) fail_wait(ms, p.a.status);
-  mma_commit(&ms->fin);
+  if (leader) {
+    if (!ok) fail_wait(ms, p.a.status);
+    mma_commit(&ms->fin);
+  }
+  __syncwarp();
 }
 
 // ============================================================================ E: S tiles,
@@ -937,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const __grid_constant
   } else if (warp < kMmaWarp) {
     role_e(p, smem, ms, bh, c0, c1);
   } else if (warp == kMmaWarp) {
-    if ((threadIdx.x & 31) == 0) role_mma(p, smem, ms, c0, c1);
+    role_mma(p, smem, ms, c0, c1);
   } else if ((threadIdx.x & 31) == 0) {
     role_tma(p, smem, ms, bh, c0, c1);
   }
