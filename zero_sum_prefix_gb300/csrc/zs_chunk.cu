@@ -39,7 +39,8 @@
 //                     row's scaled value tile Vsc.
 //   warps 8-11  (E) : TMEM -> registers: S = masked (Q K^T) o W -> fp16 tile; state -> fp16
 //                     tile (and the F~ rescale); X -> output rows.
-//   warp 12     (M) : TMEM allocation; one elected thread issues every tcgen05.mma.
+//   warp 12     (M) : TMEM allocation; the whole warp runs the issue loop (warp-uniform
+//                     operands) and one elected lane issues every tcgen05.mma.
 //   warp 13     (T) : TMA producer: q and k chunks 128B-swizzled directly into the operand
 //                     tiles (two stages at d = 64) and the value slice into a 64B-swizzled
 //                     staging tile, with an L2 prefetch of each chunk issued before its stage
@@ -496,6 +497,7 @@ __device__ void role_operands(const FwdArgs& a, uint8_t* smem, Misc* ms, size_t 
 template <int D>
 __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
   using CF = Cfg<D>;
+  const bool leader = elect_one();
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
   const uint32_t tA = tm + CF::TM_A, tW = tm + CF::TM_W, tX = tm + CF::TM_X, tS = tm + CF::TM_ST;
@@ -518,57 +520,73 @@ __device__ void role_mma(const FwdArgs& a, uint8_t* smem, Misc* ms, int nch) {
     const uint32_t ph = (uint32_t)c & 1u;
     const uint64_t sq = (uint64_t)((st * CF::KA * kTile) >> 4);
     const uint64_t sv = (uint64_t)(((c % CF::NSV) * 2 * kTile) >> 4);
-    ok = mbar_wait(&ms->po_sync, ph, &ms->abort);
-    if (ok && c >= 1) ok = mbar_wait(&ms->a_free, (c - 1) & 1, &ms->abort);
+    ok = mbar_wait_warp(&ms->po_sync, ph, &ms->abort);
+    if (ok && c >= 1) ok = mbar_wait_warp(&ms->a_free, (c - 1) & 1, &ms->abort);
     // the S tile shares the Q K^T columns: the previous S V product must have read it
-    if (CF::TM_S == CF::TM_A && ok && c >= 1) ok = mbar_wait(&ms->x_full, (c - 1) & 1, &ms->abort);
+    if (CF::TM_S == CF::TM_A && ok && c >= 1)
+      ok = mbar_wait_warp(&ms->x_full, (c - 1) & 1, &ms->abort);
     if (!ok) break;
     tc_fence_after();
     // ---- A = Q K^T (K = d); W = R C^T (K = 16) ----
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
-      mma_f16kind(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
-    }
-    mma_f16kind(tW, d_rw, d_cw, id_w, 0u);
-    mma_commit(&ms->a_full);
-    mma_commit(&ms->w_done);
-    // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
-    if (c >= 1 && !mbar_wait(&ms->sst_full, (c - 1) & 1, &ms->abort)) { ok = false; break; }
-    if (!mbar_wait(&ms->op_full, ph, &ms->abort)) { ok = false; break; }
-    tc_fence_after();
-#pragma unroll
-    for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint64_t off = (uint64_t)((kk * 2048) >> 4);
-      mma_f16kind(tS, dv0 + sv + off, dkm0 + sq + off, id_st, (c > 0 || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(&ms->st_done);
-    // ---- X[:, 0:96] = Q [F~ | G | H] (state of the previous chunks, B tile rows 32..127) ----
-    if (c >= 1) {
-      if (!mbar_wait(&ms->x_free, (c - 1) & 1, &ms->abort)) { ok = false; break; }
-      tc_fence_after();
+    if (leader) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
-        mma_f16kind(tX, dq0 + sq + off, dsst + off, id_qs, kk > 0);
+        mma_f16kind(tA, dq0 + sq + off, dk0 + sq + off, id_qk, kk > 0);
       }
-      mma_commit(&ms->sst_free);
-      mma_commit(&ms->qk_empty[st]);  // Q, K and the coefficients of this chunk are not read again
+      mma_f16kind(tW, d_rw, d_cw, id_w, 0u);
+      mma_commit(&ms->a_full);
+      mma_commit(&ms->w_done);
+    }
+    __syncwarp();
+    // ---- state^T += Vsc^T K (M = 128 value rows, N = d, K = chunk tokens) ----
+    if (c >= 1 && !mbar_wait_warp(&ms->sst_full, (c - 1) & 1, &ms->abort)) { ok = false; break; }
+    if (!mbar_wait_warp(&ms->op_full, ph, &ms->abort)) { ok = false; break; }
+    tc_fence_after();
+    if (leader) {
+#pragma unroll
+      for (int kk = 0; kk < kC / 16; ++kk) {
+        const uint64_t off = (uint64_t)((kk * 2048) >> 4);
+        mma_f16kind(tS, dv0 + sv + off, dkm0 + sq + off, id_st, (c > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&ms->st_done);
+    }
+    __syncwarp();
+    // ---- X[:, 0:96] = Q [F~ | G | H] (state of the previous chunks, B tile rows 32..127) ----
+    if (c >= 1) {
+      if (!mbar_wait_warp(&ms->x_free, (c - 1) & 1, &ms->abort)) { ok = false; break; }
+      tc_fence_after();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = (uint64_t)(((kk / 4) * kTile + (kk % 4) * 32) >> 4);
+          mma_f16kind(tX, dq0 + sq + off, dsst + off, id_qs, kk > 0);
+        }
+        mma_commit(&ms->sst_free);
+        mma_commit(&ms->qk_empty[st]);  // Q, K and the coefficients of this chunk: not read again
+      }
+      __syncwarp();
     }
     // ---- X[:, 96:128] = S V ----
-    if (!mbar_wait(&ms->am_full, c & 1, &ms->abort)) { ok = false; break; }
+    if (!mbar_wait_warp(&ms->am_full, c & 1, &ms->abort)) { ok = false; break; }
     tc_fence_after();
+    if (leader) {
 #pragma unroll
-    for (int kk = 0; kk < kC / 16; ++kk) {
-      const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows per step
-      mma_f16kind_ts(tX + 96, tm + CF::TM_S + kk * 8, dv0 + sv + boff, id_sv, kk > 0);
+      for (int kk = 0; kk < kC / 16; ++kk) {
+        const uint64_t boff = (uint64_t)((kk * 2048) >> 4);  // MN-major B, 16 token rows/step
+        mma_f16kind_ts(tX + 96, tm + CF::TM_S + kk * 8, dv0 + sv + boff, id_sv, kk > 0);
+      }
+      mma_commit(&ms->x_full);
+      if (c == 0) mma_commit(&ms->qk_empty[st]);  // no Q [F|G|H] product: after S was read
+      mma_commit(&ms->vsc_free[c & 1]);
     }
-    mma_commit(&ms->x_full);
-    if (c == 0) mma_commit(&ms->qk_empty[st]);  // no Q [F|G|H] product: after the S tile was read
-    mma_commit(&ms->vsc_free[c & 1]);
+    __syncwarp();
   }
-  if (!ok) fail_wait(ms, a.status);
-  mma_commit(&ms->fin);
+  if (leader) {
+    if (!ok) fail_wait(ms, a.status);
+    mma_commit(&ms->fin);
+  }
+  __syncwarp();
 }
 
 // ============================================================================ E: epilogue
@@ -920,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
   } else if (warp < 12) {
     role_epilogue<D, LN>(a, smem, ms, bh, row0, nch);
   } else if (warp == 12) {
-    if ((threadIdx.x & 31) == 0) role_mma<D>(a, smem, ms, nch);
+    role_mma<D>(a, smem, ms, nch);
   } else if ((threadIdx.x & 31) == 0) {
     role_tma<D>(p, smem, ms, bh, nch);
   }
