@@ -45,7 +45,8 @@
 //                     update (TMEM -> fp16 B tile of the next chunk's Q [F~|G|H] product, and the
 //                     F~ rescale in TMEM), output rows from X (staged in shared memory, one TMA
 //                     store per chunk), the final state (prefill).
-//   warp 16     (M) : TMEM allocation; one thread issues every tcgen05.mma.
+//   warp 16     (M) : TMEM allocation; the whole warp runs the issue loop (warp-uniform
+//                     operands) and one elected lane issues every tcgen05.mma.
 //   warp 17     (T) : TMA producer of q, k, v (three stages), with L2 prefetch ahead.
 // The fused output LayerNorm is not done here: it runs on the chunked kernel of zs_chunk.cu,
 // whose value slices exchange row statistics in a cluster (measured faster than whole rows
