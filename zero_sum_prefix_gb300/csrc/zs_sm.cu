@@ -498,16 +498,22 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm_kernel(const __grid_constant
 // and each tile's largest key norm come from a pass that also applies the rotary map; the norm
 // bounds the tile's logits: where c2 |q_t| max |k| cannot exceed the reference by more than
 // kRaise, the tile's maximum is not needed at all.
-// Three S buffers: S_{g+3} is formed as soon as tile g's products are issued, so the tensor
-// cores, the exponentials of tile g+1 and the products of tile g overlap.  Both epilogue
+// Three S buffers: S_{n+3} is formed as soon as tile n's products are issued, so the tensor
+// cores, the exponentials of tile n+1 and the products of tile n overlap.  Both epilogue
 // warpgroups work on every key tile, warpgroup w on its keys 64 w .. 64 w + 63; where the bound
 // does not settle it, the row's tile maximum is exchanged between the two warps that hold the
 // row (a 64-thread barrier), and the reference m rises (lazily: only when the tile maximum
 // exceeds it by more than kRaise = 16, so P <= 2^16) before the tile's P is formed; A and the
 // exp-sums are then rescaled (warpgroup 0 rescales A, once the previous tile's products have
 // completed).
-// TMEM (512 columns): S0, S1, S2 (128 each), A (64), B (64); the diagonal tile's C goes to the S
-// buffer that is free at the end.
+// Persistent: one CTA per SM takes the query tiles ("items", heaviest first) c, c + G, c + 2G, ...
+// (G CTAs), and every role runs through one sequence of key tiles n counted over its items, so
+// the next item's Q and K/V loads and its first S products overlap the current item's last
+// products and output (the per-CTA start and drain are paid once per SM instead of once per
+// query tile).  An item's C goes into its diagonal tile's own S buffer (the products of that tile
+// have read it by then: the tensor-core operations of one thread run in order); the next item's
+// third S product, which uses that buffer, waits until the output has read C, A and B.
+// TMEM (512 columns): S0, S1, S2 (128 each), A (64), B (64).
 struct Sm1Cfg {
   static constexpr int NS = 5;                             // K/V stages
   static constexpr int NB = 3;                             // S buffers
@@ -517,10 +523,12 @@ struct Sm1Cfg {
   static constexpr uint32_t TRI_OFF = STAGE_OFF + NS * STAGE;  // [128 x 128] lower-triangular ones
   static constexpr uint32_t XMAX_OFF = TRI_OFF + 2 * kAtom;    // float [2 bufs][2 halves][128]
   static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float2 [2][128] sums
-  static constexpr uint32_t CBASE_OFF = STAT_OFF + 2 * kT * 8;  // float [64]
-  static constexpr uint32_t KBASE_OFF = CBASE_OFF + 64 * 4;    // float [64]
-  static constexpr uint32_t QN_OFF = KBASE_OFF + 64 * 4;       // float [128]
-  static constexpr uint32_t MISC_OFF = QN_OFF + kT * 4;
+  static constexpr uint32_t CBASE_OFF = STAT_OFF + 2 * kT * 8;  // float [2 items][64]
+  static constexpr uint32_t KBASE_OFF = CBASE_OFF + 2 * 64 * 4;  // float [2 items][64]
+  static constexpr uint32_t QN_OFF = KBASE_OFF + 2 * 64 * 4;     // float [128]
+  // per row, by item parity: the gate logits (g1, gh, g0) and q_t . K_base
+  static constexpr uint32_t ROWV_OFF = QN_OFF + kT * 4;         // float [2 items][4][128]
+  static constexpr uint32_t MISC_OFF = ROWV_OFF + 2 * 4 * kT * 4;
   static constexpr uint32_t BYTES = MISC_OFF + 256;
   static_assert(BYTES <= 232448, "shared memory budget of one CTA");
   static constexpr uint32_t TM_A = 384, TM_B = 448;
@@ -531,99 +539,164 @@ struct Sm1Cfg {
 __device__ __forceinline__ uint32_t sm1_sbuf(int i) { return 128u * (uint32_t)i; }
 
 struct Sm1Misc {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t kv_full[Sm1Cfg::NS], kv_empty[Sm1Cfg::NS];
   uint64_t s_full[3], w_full[3];
-  uint64_t o_full, fin, cb_full;
+  uint64_t o_full, acc_free, fin;
+  uint64_t cb_full[2], cb_empty[2];
   uint32_t tmem;
   int abort;
   int never;
 };
 static_assert(sizeof(Sm1Misc) <= 256, "Sm1Misc fits its slot");
 
-__device__ void sm1_producer(const SmParams& p, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J) {
-  using CF = Sm1Cfg;
-  const uint32_t base = smem_u32(smem);
-  mbar_arrive_expect_tx(&ms->q_full, kAtom);
-  tma_load_3d(base + CF::Q_OFF, &p.tq, 0, qt * kT, bh, &ms->q_full);
-  for (int g = 0; g < J; ++g) {
-    const int st = g % CF::NS;
-    if (g >= CF::NS && !mbar_wait(&ms->kv_empty[st], ((g / CF::NS) - 1) & 1, &ms->abort)) {
-      report(p.a.status, kErrTimeout);
-      ms->abort = 1;
-      return;
-    }
-    const uint32_t kt = base + CF::STAGE_OFF + st * CF::STAGE;
-    mbar_arrive_expect_tx(&ms->kv_full[st], 2 * kAtom);
-    tma_load_3d(kt, &p.tk, 0, g * kT, bh, &ms->kv_full[st]);
-    tma_load_3d(kt + kAtom, &p.tv, 0, g * kT, bh, &ms->kv_full[st]);
-  }
+// The query tile of work item i: every sequence's last causal query tile first, then the next
+// lighter ones (in encoder mode all items have the same number of key tiles).
+struct Sm1Item {
+  int bh, qt, J;
+};
+__device__ __forceinline__ Sm1Item sm1_item(const SmArgs& a, int i) {
+  const int BH = a.B * a.H, nqt = (a.N + kT - 1) / kT;
+  const int y = i / BH;
+  Sm1Item it;
+  it.bh = i - y * BH;
+  it.qt = a.causal ? nqt - 1 - y : y;
+  it.J = key_tiles(a, it.qt);
+  return it;
+}
+__device__ __forceinline__ int sm1_items(const SmArgs& a) {
+  return a.B * a.H * ((a.N + kT - 1) / kT);
+}
+// The it-th item of this CTA: rounds of gridDim.x items, taken in alternating directions, so
+// that every CTA's total of key tiles is about the same (items >= sm1_items when none is left).
+__device__ __forceinline__ int sm1_mine(int it) {
+  const int c = (it & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+  return it * (int)gridDim.x + c;
 }
 
-// Issue order: S_0, S_1, S_2; then per key tile g the products of tile g once both warpgroups
-// have released it (A += P V, B += X V), and S_{g+3} into the buffer those products have just
-// read.  The tensor-core operations of one thread run in order, so S_{g+3} overwrites tile g's
-// P and x only after its products have read them.  The whole warp runs this loop (its operands
-// stay warp-uniform, so the issue stays short next to the busy epilogue warps of the same
-// scheduler) and one elected lane issues; descriptors advance by plain additions (16 key rows of
-// an MN-major tile = 2048 bytes = 128 units).
-__device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
+
+// Named barrier over nthreads threads that also returns whether any of them passed pred = true.
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0u;
+}
+
+// One lane: per item Q (once the previous item's Q has been read by its last S product and by
+// the epilogue), then the item's K and V tiles through the stage ring.
+__device__ void sm1_producer(const SmParams& p, uint8_t* smem, Sm1Misc* ms) {
+  using CF = Sm1Cfg;
+  const SmArgs& a = p.a;
+  const uint32_t base = smem_u32(smem);
+  const int nitems = sm1_items(a);
+  int n = 0;  // key tiles loaded so far, over all items
+  for (int it = 0, item = sm1_mine(0); item < nitems; item = sm1_mine(++it)) {
+    const Sm1Item w = sm1_item(a, item);
+    if (it >= 1 && !mbar_wait(&ms->q_empty, (it - 1) & 1, &ms->abort)) goto fail;
+    mbar_arrive_expect_tx(&ms->q_full, kAtom);
+    tma_load_3d(base + CF::Q_OFF, &p.tq, 0, w.qt * kT, w.bh, &ms->q_full);
+    for (int g = 0; g < w.J; ++g, ++n) {
+      const int st = n % CF::NS;
+      if (n >= CF::NS && !mbar_wait(&ms->kv_empty[st], ((n / CF::NS) - 1) & 1, &ms->abort))
+        goto fail;
+      const uint32_t kt = base + CF::STAGE_OFF + st * CF::STAGE;
+      mbar_arrive_expect_tx(&ms->kv_full[st], 2 * kAtom);
+      tma_load_3d(kt, &p.tk, 0, g * kT, w.bh, &ms->kv_full[st]);
+      tma_load_3d(kt + kAtom, &p.tv, 0, g * kT, w.bh, &ms->kv_full[st]);
+    }
+  }
+  return;
+fail:
+  report(a.status, kErrTimeout);
+  ms->abort = 1;
+}
+
+// Issue order per item: S of its first three key tiles (the third only once the previous item's
+// output has read C, A and B: it uses the buffer that held C); then per key tile the products
+// once both warpgroups have released it (A += P V, B += X V; the item's first products also wait
+// until the previous item's A and B have been read), and S_{n+3} into the buffer those products
+// have just read.  The tensor-core operations of one thread run in order, so S_{n+3} overwrites
+// tile n's P and x only after its products have read them.  The whole warp runs this loop (its
+// operands stay warp-uniform, so the issue stays short next to the busy epilogue warps of the
+// same scheduler) and one elected lane issues; descriptors advance by plain additions (16 key
+// rows of an MN-major tile = 2048 bytes = 128 units).
+__device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
   using CF = Sm1Cfg;
   const bool leader = elect_one();
   const uint32_t base = smem_u32(smem);
   const uint32_t tm = ms->tmem;
+  const int nitems = sm1_items(a);
   constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
   constexpr uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);    // A += P V, B += X V
   const uint64_t qd = sw128_desc(base + CF::Q_OFF, 16, 1024);
-  auto issue_s = [&](int g) -> bool {
-    const int st = g % CF::NS;
-    if (!mbar_wait_warp(&ms->kv_full[st], (g / CF::NS) & 1, &ms->abort)) return false;
+  // S_n for key tile n (counted over all items) into buffer n % 3; after the item's last one, Q
+  // is released (to the producer, once the epilogue has read it too)
+  auto issue_s = [&](int n, bool last) -> bool {
+    const int st = n % CF::NS;
+    if (!mbar_wait_warp(&ms->kv_full[st], (n / CF::NS) & 1, &ms->abort)) return false;
     tc_fence_after();
     const uint64_t kd = sw128_desc(base + CF::STAGE_OFF + st * CF::STAGE, 16, 1024);
-    const uint32_t ts = tm + sm1_sbuf(g % CF::NB);
+    const uint32_t ts = tm + sm1_sbuf(n % CF::NB);
     if (leader) {
       mma_f16kind(ts, qd, kd, id_qk, 0u);
 #pragma unroll
       for (int kk = 1; kk < 4; ++kk) mma_f16kind(ts, qd + 2 * kk, kd + 2 * kk, id_qk, 1u);
-      mma_commit(&ms->s_full[g % CF::NB]);
+      mma_commit(&ms->s_full[n % CF::NB]);
+      if (last) mma_commit(&ms->q_empty);
     }
     __syncwarp();
     return true;
   };
-  bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
-  for (int g = 0; g < CF::NB && g < J && ok; ++g) ok = issue_s(g);
-  for (int g = 0; g < J && ok; ++g) {
-    const int b = g % CF::NB, st = g % CF::NS;
-    const uint32_t vt = base + CF::STAGE_OFF + st * CF::STAGE + kAtom;
-    const uint64_t vd = sw128_desc(vt, kAtom, 1024);
-    const uint32_t ts = tm + sm1_sbuf(b);
-    ok = mbar_wait_warp(&ms->w_full[b], (g / CF::NB) & 1, &ms->abort);
-    if (!ok) break;
-    tc_fence_after();
-    if (leader) {
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk) {
-        const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
-        mma_f16kind_ts(tm + CF::TM_A, ts + 16 * kk, vd + 128 * kk, id_pv, acc);
-        mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_pv, acc);
-      }
-      if (a.causal && g == J - 1) {
-        // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times V,
-        // into the S buffer no tile uses any more
-        const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
-        const uint32_t tcd = tm + sm1_sbuf(J % CF::NB);
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_f16kind(tcd, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4),
-                      vd + 128 * kk, id_pv, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(&ms->kv_empty[st]);  // also tells the epilogue that A holds tile g
+  bool ok = true;
+  int n0 = 0;  // the item's first key tile, counted over all items
+  for (int it = 0, item = sm1_mine(0); ok && item < nitems; item = sm1_mine(++it)) {
+    const int J = sm1_item(a, item).J;
+    ok = mbar_wait_warp(&ms->q_full, it & 1, &ms->abort);
+    for (int g = 0; g < CF::NB && g < J && ok; ++g) {
+      if (g == CF::NB - 1 && it >= 1 && a.causal)
+        ok = mbar_wait_warp(&ms->acc_free, (it - 1) & 1, &ms->abort);
+      if (ok) ok = issue_s(n0 + g, g == J - 1);
     }
-    __syncwarp();
-    if (g + CF::NB < J) ok = issue_s(g + CF::NB);
+    for (int g = 0; g < J && ok; ++g) {
+      const int n = n0 + g;
+      const int b = n % CF::NB, st = n % CF::NS;
+      const uint32_t vt = base + CF::STAGE_OFF + st * CF::STAGE + kAtom;
+      const uint64_t vd = sw128_desc(vt, kAtom, 1024);
+      const uint32_t ts = tm + sm1_sbuf(b);
+      ok = mbar_wait_warp(&ms->w_full[b], (n / CF::NB) & 1, &ms->abort);
+      if (ok && g == 0 && it >= 1) ok = mbar_wait_warp(&ms->acc_free, (it - 1) & 1, &ms->abort);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
+          mma_f16kind_ts(tm + CF::TM_A, ts + 16 * kk, vd + 128 * kk, id_pv, acc);
+          mma_f16kind_ts(tm + CF::TM_B, ts + 16 * kk + 8, vd + 128 * kk, id_pv, acc);
+        }
+        if (a.causal && g == J - 1) {
+          // C of the diagonal tile: lower-triangular ones (K-major, two atoms of 64 keys) times
+          // V, into this tile's own S buffer, after the products above have read it
+          const uint64_t td = sw128_desc(base + CF::TRI_OFF, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_f16kind(ts, td + (uint64_t)(((kk / 4) * kAtom + (kk % 4) * 32) >> 4),
+                        vd + 128 * kk, id_pv, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&ms->kv_empty[st]);  // also tells the epilogue that A holds tile n
+        if (g == J - 1) mma_commit(&ms->o_full);
+      }
+      __syncwarp();
+      if (g + CF::NB < J) ok = issue_s(n + CF::NB, g + CF::NB == J - 1);
+    }
+    n0 += J;
   }
   if (leader) {
-    if (ok) mma_commit(&ms->o_full);
     if (!ok) {
       report(a.status, kErrTimeout);
       ms->abort = 1;
@@ -633,309 +706,352 @@ __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int J) {
   __syncwarp();
 }
 
-// Warps 2 and 3: the parts of C and P_t that are the same for every row, from the per-tile
-// statistics: K_base = the key column sums of the tiles before the last one, C_base = the value
-// column sums of the tiles before the diagonal one (all tiles in encoder mode); eight partial
-// sums over the tiles (g = 8 j + u), added in a fixed order, so that the loads overlap.
-__device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int J) {
+// Warps 2 and 3 (thread = column t, warp 2 columns 0..31, warp 3 columns 32..63): per item the
+// parts of C and P_t that are the same for every row, from the per-tile statistics: K_base = the
+// key column sums of the tiles before the last one, C_base = the value column sums of the tiles
+// before the diagonal one (all tiles in encoder mode); eight partial sums over the tiles
+// (g = 8 j + u), added in a fixed order, so that the loads overlap; and the gate logits of the
+// item's rows.  Two buffers (by item parity): an item's values are written once the epilogue
+// has used those of two items before, so their loads run ahead of the epilogue.
+__device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
   using CF = Sm1Cfg;
   const int t = threadIdx.x - 64;  // column
   const int nt = (a.N + kT - 1) / kT;
-  const float* st = a.kstat + (size_t)bh * nt * kSmStat + t;
-  float pk[8] = {}, pv[8] = {};
-  const int nk = J - 1, nv = a.causal ? J - 1 : J;
-  for (int g0 = 0; g0 < nv; g0 += 8) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int g = g0 + u;
-      if (g < nk) pk[u] += st[(size_t)g * kSmStat];
-      if (g < nv) pv[u] += st[(size_t)g * kSmStat + 68];
+  const int nitems = sm1_items(a);
+  for (int it = 0, item = sm1_mine(0); item < nitems; item = sm1_mine(++it)) {
+    const Sm1Item w = sm1_item(a, item);
+    const int par = it & 1;
+    if (it >= 2 && !mbar_wait_warp(&ms->cb_empty[par], ((it >> 1) - 1) & 1, &ms->abort)) {
+      report(a.status, kErrTimeout);
+      ms->abort = 1;
+      return;
     }
+    const float* st = a.kstat + (size_t)w.bh * nt * kSmStat + t;
+    float pk[8] = {}, pv[8] = {};
+    const int nk = w.J - 1, nv = a.causal ? w.J - 1 : w.J;
+    for (int g0 = 0; g0 < nv; g0 += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int g = g0 + u;
+        if (g < nk) pk[u] += st[(size_t)g * kSmStat];
+        if (g < nv) pv[u] += st[(size_t)g * kSmStat + 68];
+      }
+    }
+    const float sk = ((pk[0] + pk[1]) + (pk[2] + pk[3])) + ((pk[4] + pk[5]) + (pk[6] + pk[7]));
+    const float sv = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
+    reinterpret_cast<float*>(smem + CF::KBASE_OFF)[par * 64 + t] = sk;
+    reinterpret_cast<float*>(smem + CF::CBASE_OFF)[par * 64 + t] = sv;
+    // the gate logits of the item's rows t and t + 64
+    float* rowv = reinterpret_cast<float*>(smem + CF::ROWV_OFF) + par * 4 * kT;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = t + 64 * h, tq = w.qt * kT + rr;
+      const bool valid = tq < a.N;
+      const size_t row = (size_t)w.bh * a.N + tq;
+      rowv[rr] = valid ? a.g1[row] : 0.0f;
+      rowv[kT + rr] = valid ? a.gh[row] : 0.0f;
+      rowv[2 * kT + rr] = (valid && a.g0) ? a.g0[row] : 0.0f;
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->cb_full[par]);  // count 2: both warps
   }
-  const float sk = ((pk[0] + pk[1]) + (pk[2] + pk[3])) + ((pk[4] + pk[5]) + (pk[6] + pk[7]));
-  const float sv = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-  reinterpret_cast<float*>(smem + CF::KBASE_OFF)[t] = sk;
-  reinterpret_cast<float*>(smem + CF::CBASE_OFF)[t] = sv;
-  named_bar_sync(2, 64);
-  if (t == 0) mbar_arrive(&ms->cb_full);
 }
 
 // Both warpgroups take every key tile; warpgroup w its keys 64 w .. 64 w + 63.  Thread = query
 // row of the tile; warp wq of warpgroup 0 and warp wq of warpgroup 1 hold the same 32 rows.
-__device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int bh, int qt, int J,
-                             int w) {
+// Per item: |q_t| and q_t . K_base while Q is resident (then Q is released), the key tiles, and
+// the output once the item's products have completed (then A, B, C and the item's sums are
+// released).  Every named barrier is taken alike by all its warps, also after a failed wait (the
+// work is then skipped); after a failure anywhere, the barrier at the end of the item's tiles
+// tells every epilogue warp to stop.
+__device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w) {
   using CF = Sm1Cfg;
   const int wq = (threadIdx.x >> 5) & 3;
   const int r = wq * 32 + (threadIdx.x & 31);
   const uint32_t tl = ms->tmem + ((uint32_t)(wq * 32) << 16);
-  const int t = qt * kT + r;                      // query index (0-based)
-  const bool row_ok = t < a.N;
-  const size_t row = (size_t)bh * a.N + t;
-  const int lim = a.causal ? t : a.N - 1;         // last key of this query
-  // last key visible to every row of this warp (uniform, as the aligned TMEM accesses require)
-  const int lim_warp = a.causal ? qt * kT + wq * 32 : a.N - 1;
-  const float tc = a.causal ? (float)(t + 1) : (float)a.N;
   constexpr float inv_sqrt_d = 0.125f;                      // d = 64
   constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
   const int nt = (a.N + kT - 1) / kT;
-  // the row's gate logits, loaded now and used at the end
-  float gl1 = 0.0f, glh = 0.0f, gl0 = 0.0f;
-  if (row_ok) {
-    gl1 = a.g1[row];
-    glh = a.gh[row];
-    if (a.g0) gl0 = a.g0[row];
-  }
-  const float* kn2 = a.kstat + (size_t)bh * nt * kSmStat + 64;  // largest |k| of each tile
   float* xmax = reinterpret_cast<float*>(smem + CF::XMAX_OFF);
-  bool ok = mbar_wait_warp(&ms->q_full, 0, &ms->abort);
-  // |q_t| of this row (the bf16 values the tensor cores read), for the bound of its logits;
-  // warpgroup 0 computes it and both warps of the row pair take that one value, so that their
-  // exchange decisions below agree whatever happens
   float* qnorm = reinterpret_cast<float*>(smem + CF::QN_OFF);
-  if (w == 0) {
-    float qn = 0.0f;
-    const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
+  float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
+  const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
+  bool ok = true;
+  int ex = 0;  // exchanges so far (alternating buffers), over all items
+  int n0 = 0;  // the item's first key tile, counted over all items
+  for (int it = 0; sm1_mine(it) < sm1_items(a); ++it) {
+    const Sm1Item wi = sm1_item(a, sm1_mine(it));
+    const int J = wi.J, par = it & 1;
+    const int lim = a.causal ? wi.qt * kT + r : a.N - 1;  // last key of this query
+    // last key visible to every row of this warp (uniform, as the aligned TMEM accesses require)
+    const int lim_warp = a.causal ? wi.qt * kT + wq * 32 : a.N - 1;
+    const int kn0 = wi.bh * nt;  // this sequence's first tile statistics record
+    if (ok) ok = mbar_wait_warp(&ms->q_full, par, &ms->abort);
+    // |q_t| of this row (the bf16 values the tensor cores read), for the bound of its logits;
+    // warpgroup 0 computes it and both warps of the row pair take that one value, so that their
+    // exchange decisions below agree whatever happens
+    if (w == 0) {
+      float qn = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 u = lds128(qrow + sw128_off(r, c));
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      for (int c = 0; c < 8; ++c) {
+        const uint4 u = lds128(qrow + sw128_off(r, c));
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        float lo, hi;
-        unpack_bf16x2(wv[y], lo, hi);
-        qn = __fmaf_rn(lo, lo, __fmaf_rn(hi, hi, qn));
+        for (int y = 0; y < 4; ++y) {
+          float lo, hi;
+          unpack_bf16x2(wv[y], lo, hi);
+          qn = __fmaf_rn(lo, lo, __fmaf_rn(hi, hi, qn));
+        }
       }
+      qnorm[r] = sqrtf(qn) * (c2 * CF::kBoundSlack);
     }
-    qnorm[r] = sqrtf(qn) * (c2 * CF::kBoundSlack);
-  }
-  named_bar_sync(3 + wq, 64);
-  const float qn = qnorm[r];
-  float m2 = -INFINITY, l = 0.0f;  // the row's reference (base-2 units), this half's exp-sum
-  float2 xs = make_float2(0.0f, 0.0f);  // this half's sum of the last tile's bf16 logits
-  int ex = 0;                           // exchanges so far (alternating buffers)
-  float kn_next = kn2[0];
-  // Every iteration takes the same exchange decisions in both warps of a row pair, also after a
-  // failed wait (the work is then skipped), so that neither waits on the pair barrier in vain.
-  for (int g = 0; g < J; ++g) {
-    const int b = g % CF::NB;
-    const float kn = kn_next;
-    if (g + 1 < J) kn_next = kn2[(size_t)(g + 1) * kSmStat];
-    if (ok) {
-      ok = mbar_wait_warp(&ms->s_full[b], (g / CF::NB) & 1, &ms->abort);
-      if (!ok) ms->abort = 1;
+    named_bar_sync(3 + wq, 64);
+    const float qn = qnorm[r];
+    // the earlier tiles' part of the logit sum, q_t . K_base (warpgroup 0); then Q is not read
+    // again
+    if (ok) ok = mbar_wait_warp(&ms->cb_full[par], (it >> 1) & 1, &ms->abort);
+    if (w == 0) {
+      float qk = 0.0f;
+      const float* kb = reinterpret_cast<const float*>(smem + CF::KBASE_OFF) + par * 64;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 u = lds128(qrow + sw128_off(r, c));
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          float lo, hi;
+          unpack_bf16x2(wv[y], lo, hi);
+          qk = __fmaf_rn(lo, kb[8 * c + 2 * y], qk);
+          qk = __fmaf_rn(hi, kb[8 * c + 2 * y + 1], qk);
+        }
+      }
+      reinterpret_cast<float*>(smem + CF::ROWV_OFF)[(par * 4 + 3) * kT + r] = qk;
     }
-    const uint32_t ts = tl + sm1_sbuf(b) + 64 * w;  // this half's columns
-    const int k0 = g * kT + 64 * w;                 // its first key
-    const bool full = k0 + 63 <= lim_warp;
-    const bool last = g == J - 1;
-    uint32_t ra[32], rb[32];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->q_empty);  // count 9: the last S, 8 warps
+    if (!ok) ms->abort = 1;
+    float m2 = -INFINITY, l = 0.0f;  // the row's reference (base-2 units), this half's exp-sum
+    float2 xs = make_float2(0.0f, 0.0f);  // this half's sum of the last tile's bf16 logits
+    // largest |k| of each tile (not needed for the first one: with the reference at -inf the
+    // bound never holds there)
+    float kn_next = 0.0f;
+    // Every iteration takes the same exchange decisions in both warps of a row pair, also after
+    // a failed wait (the work is then skipped), so that neither waits on the pair barrier in
+    // vain.
+    for (int g = 0; g < J; ++g) {
+      const int n = n0 + g;
+      const int b = n % CF::NB;
+      const float kn = kn_next;
+      if (g + 1 < J) kn_next = a.kstat[(size_t)(kn0 + g + 1) * kSmStat + 64];
+      if (ok) {
+        ok = mbar_wait_warp(&ms->s_full[b], (n / CF::NB) & 1, &ms->abort);
+        if (!ok) ms->abort = 1;
+      }
+      const uint32_t ts = tl + sm1_sbuf(b) + 64 * w;  // this half's columns
+      const int k0 = g * kT + 64 * w;                 // its first key
+      const bool full = k0 + 63 <= lim_warp;
+      const bool last = g == J - 1;
+      uint32_t ra[32], rb[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32_nowait(ts, ra);
+        tmem_ld32_nowait(ts + 32, rb);
+        tmem_wait_ld();
+        reg_fence(ra);
+        reg_fence(rb);
+      }
+      // ---- the reference rises only if some logit of the tile may exceed it by more than
+      //      kRaise: c2 x <= c2 |q_t| max |k| (Cauchy-Schwarz) rules that out for most tiles;
+      //      otherwise the two halves' maxima are exchanged (both warps decide alike) ----
+      const bool exch = !__all_sync(0xffffffffu, qn * kn <= m2 + CF::kRaise);
+      if (exch) {
+        float cm = -INFINITY;
+        if (!ok) {
+        } else if (full) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            cm = fmaxf(cm, fmaxf(__uint_as_float(ra[x]), __uint_as_float(rb[x])));
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            if (k0 + x <= lim) cm = fmaxf(cm, __uint_as_float(ra[x]));
+            if (k0 + 32 + x <= lim) cm = fmaxf(cm, __uint_as_float(rb[x]));
+          }
+        }
+        float* xm = xmax + (ex & 1) * 2 * kT;
+        ++ex;
+        xm[w * kT + r] = cm;
+        named_bar_sync(3 + wq, 64);
+        const float tmx = fmaxf(xm[r], xm[kT + r]) * c2;
+        const bool raise = tmx > m2 + CF::kRaise;  // false for a row without visible keys yet
+        if (__any_sync(0xffffffffu, raise)) {
+          const float f = (raise && m2 != -INFINITY) ? ex2(m2 - tmx) : 1.0f;
+          if (raise) {
+            l *= f;
+            m2 = tmx;
+          }
+          if (ok && w == 0 && g >= 1) {
+            // A's earlier tiles: wait until their products have completed (the commit that
+            // frees tile n-1's stage follows them), then rescale
+            ok = mbar_wait_warp(&ms->kv_empty[(n - 1) % CF::NS], ((n - 1) / CF::NS) & 1,
+                                &ms->abort);
+            if (!ok) ms->abort = 1;
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int q = 0; q < 4; ++q) {
+                uint32_t av[16];
+                tmem_ld16_nowait(tl + CF::TM_A + 16 * q, av);
+                tmem_wait_ld();
+                reg_fence(av);
+#pragma unroll
+                for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
+                tmem_st16_nowait(tl + CF::TM_A + 16 * q, av);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) continue;
+      // ---- P = 2^{c2 x - m} and x as bf16 pairs over this half's own columns; the last tile's
+      //      rounded logits are summed (the earlier tiles' sum comes from K_base) ----
+      auto chunk_px = [&](const uint32_t (&rv)[32], const int ch) {
+        float2 ls = make_float2(0.0f, 0.0f);
+        if (full) {
+          const float2 c2v = make_float2(c2, c2), nm = make_float2(-m2, -m2);
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp) {
+            uint32_t pp[8], xp[8];
+#pragma unroll
+            for (int y = 0; y < 8; ++y) {
+              const float2 xv = make_float2(__uint_as_float(rv[16 * hp + 2 * y]),
+                                            __uint_as_float(rv[16 * hp + 2 * y + 1]));
+              const float2 e = __ffma2_rn(xv, c2v, nm);
+              const float2 pe = make_float2(ex2(e.x), ex2(e.y));
+              ls = __fadd2_rn(ls, pe);
+              pp[y] = pack_bf16x2(pe.x, pe.y);
+              xp[y] = pack_bf16x2(xv.x, xv.y);
+              if (last)
+                xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
+                                                __uint_as_float(xp[y] & 0xffff0000u)));
+            }
+            tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
+            tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
+          }
+        } else {
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp) {
+            uint32_t pp[8], xp[8];
+#pragma unroll
+            for (int y = 0; y < 8; ++y) {
+              float pe[2], xe[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int x = 16 * hp + 2 * y + e;
+                const float xv = __uint_as_float(rv[x]);
+                const bool valid = k0 + 32 * ch + x <= lim;
+                pe[e] = valid ? ex2(fmaf(xv, c2, -m2)) : 0.0f;
+                xe[e] = valid ? xv : 0.0f;
+              }
+              ls.x += pe[0];
+              ls.y += pe[1];
+              pp[y] = pack_bf16x2(pe[0], pe[1]);
+              xp[y] = pack_bf16x2(xe[0], xe[1]);
+              if (last)
+                xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
+                                                __uint_as_float(xp[y] & 0xffff0000u)));
+            }
+            tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
+            tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
+          }
+        }
+        l += ls.x + ls.y;
+      };
+      chunk_px(ra, 0);
+      chunk_px(rb, 1);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->w_full[b]);
+    }
+    // ---- the two halves' exp-sums (both relative to the row's common reference) and last-tile
+    //      logit sums; every epilogue warp learns here whether any role has failed ----
+    stat[w * kT + r] = make_float2(l, xs.x + xs.y);
+    if (named_bar_any(1, 256, !ok || ms->abort != 0)) {
+      ok = false;
+      break;
+    }
+    const float2 s0 = stat[r], s1 = stat[kT + r];
+    const float lt = s0.x + s1.x;
+    // ---- the row's coefficients, while the last products complete; then the output:
+    //      O = alpha A + beta B + gamma C, warpgroup w writing columns 32 w .. 32 w + 31 ----
+    const Sm1Item wd = sm1_item(a, sm1_mine(it));
+    const int t = wd.qt * kT + r;  // query index (0-based)
+    const bool row_ok = t < a.N;
+    const float tc = a.causal ? (float)(t + 1) : (float)a.N;
+    const float* rowv = reinterpret_cast<const float*>(smem + CF::ROWV_OFF) + par * 4 * kT + r;
+    float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
+    if (row_ok) {
+      sig1 = sigmoid(rowv[0]);
+      sigh = sigmoid(rowv[kT]);
+      if (a.g0) sig0 = sigmoid(rowv[2 * kT]);
+    }
+    const float qk = rowv[3 * kT];
+    const float rt = 1.0f / tc;
+    const float alpha = lt > 0.0f ? sigh / lt : 0.0f;
+    const float beta = (sig1 - sigh) * rt;
+    const float Pt = (qk + s0.y + s1.y) * inv_sqrt_d;
+    const float bs = beta * inv_sqrt_d;
+    const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
+    ok = mbar_wait_warp(&ms->o_full, par, &ms->abort);
     if (ok) {
       tc_fence_after();
-      tmem_ld32_nowait(ts, ra);
-      tmem_ld32_nowait(ts + 32, rb);
-      tmem_wait_ld();
-      reg_fence(ra);
-      reg_fence(rb);
+      const int c0 = 32 * w;
+      const float* cbase = reinterpret_cast<const float*>(smem + CF::CBASE_OFF) + par * 64 + c0;
+      const uint32_t tcd = tl + sm1_sbuf((n0 + J - 1) % CF::NB);  // the diagonal tile's C
+      float o[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // two 16-column rounds
+        uint32_t av[16], bv[16], cv[16];
+        tmem_ld16_nowait(tl + CF::TM_A + c0 + 16 * hh, av);
+        tmem_ld16_nowait(tl + CF::TM_B + c0 + 16 * hh, bv);
+        if (a.causal) tmem_ld16_nowait(tcd + c0 + 16 * hh, cv);
+        tmem_wait_ld();
+        reg_fence(av);
+        reg_fence(bv);
+        reg_fence(cv);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float c = cbase[16 * hh + j];
+          if (a.causal) c += __uint_as_float(cv[j]);
+          o[16 * hh + j] = fmaf(alpha, __uint_as_float(av[j]),
+                                fmaf(bs, __uint_as_float(bv[j]), gamma * c));
+        }
+      }
+      if (row_ok) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)wd.bh * a.N + t) * 64 + c0);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]),
+                               pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                               pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]),
+                               pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+      }
+    } else {
+      ms->abort = 1;
     }
-    // ---- the reference rises only if some logit of the tile may exceed it by more than
-    //      kRaise: c2 x <= c2 |q_t| max |k| (Cauchy-Schwarz) rules that out for most tiles;
-    //      otherwise the two halves' maxima are exchanged (both warps decide alike) ----
-    const bool exch = !__all_sync(0xffffffffu, qn * kn <= m2 + CF::kRaise);
-    if (exch) {
-      float cm = -INFINITY;
-      if (!ok) {
-      } else if (full) {
-#pragma unroll
-        for (int x = 0; x < 32; ++x)
-          cm = fmaxf(cm, fmaxf(__uint_as_float(ra[x]), __uint_as_float(rb[x])));
-      } else {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          if (k0 + x <= lim) cm = fmaxf(cm, __uint_as_float(ra[x]));
-          if (k0 + 32 + x <= lim) cm = fmaxf(cm, __uint_as_float(rb[x]));
-        }
-      }
-      float* xm = xmax + (ex & 1) * 2 * kT;
-      ++ex;
-      xm[w * kT + r] = cm;
-      named_bar_sync(3 + wq, 64);
-      const float tmx = fmaxf(xm[r], xm[kT + r]) * c2;
-      const bool raise = tmx > m2 + CF::kRaise;  // false for a row without visible keys yet
-      if (__any_sync(0xffffffffu, raise)) {
-        const float f = (raise && m2 != -INFINITY) ? ex2(m2 - tmx) : 1.0f;
-        if (raise) {
-          l *= f;
-          m2 = tmx;
-        }
-        if (ok && w == 0 && g >= 1) {
-          // A's earlier tiles: wait until their products have completed (the commit that frees
-          // tile g-1's stage follows them), then rescale
-          ok = mbar_wait_warp(&ms->kv_empty[(g - 1) % CF::NS], ((g - 1) / CF::NS) & 1, &ms->abort);
-          if (!ok) ms->abort = 1;
-          if (ok) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              uint32_t av[16];
-              tmem_ld16_nowait(tl + CF::TM_A + 16 * q, av);
-              tmem_wait_ld();
-              reg_fence(av);
-#pragma unroll
-              for (int y = 0; y < 16; ++y) av[y] = __float_as_uint(__uint_as_float(av[y]) * f);
-              tmem_st16_nowait(tl + CF::TM_A + 16 * q, av);
-            }
-          }
-        }
-      }
-    }
-    if (!ok) continue;
-    // ---- P = 2^{c2 x - m} and x as bf16 pairs over this half's own columns; the last tile's
-    //      rounded logits are summed (the earlier tiles' sum comes from K_base) ----
-    auto chunk_px = [&](const uint32_t (&rv)[32], const int ch) {
-      float2 ls = make_float2(0.0f, 0.0f);
-      if (full) {
-        const float2 c2v = make_float2(c2, c2), nm = make_float2(-m2, -m2);
-#pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {
-          uint32_t pp[8], xp[8];
-#pragma unroll
-          for (int y = 0; y < 8; ++y) {
-            const float2 xv = make_float2(__uint_as_float(rv[16 * hp + 2 * y]),
-                                          __uint_as_float(rv[16 * hp + 2 * y + 1]));
-            const float2 e = __ffma2_rn(xv, c2v, nm);
-            const float2 pe = make_float2(ex2(e.x), ex2(e.y));
-            ls = __fadd2_rn(ls, pe);
-            pp[y] = pack_bf16x2(pe.x, pe.y);
-            xp[y] = pack_bf16x2(xv.x, xv.y);
-            if (last)
-              xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
-                                              __uint_as_float(xp[y] & 0xffff0000u)));
-          }
-          tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
-          tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
-        }
-      } else {
-#pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {
-          uint32_t pp[8], xp[8];
-#pragma unroll
-          for (int y = 0; y < 8; ++y) {
-            float pe[2], xe[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int x = 16 * hp + 2 * y + e;
-              const float xv = __uint_as_float(rv[x]);
-              const bool valid = k0 + 32 * ch + x <= lim;
-              pe[e] = valid ? ex2(fmaf(xv, c2, -m2)) : 0.0f;
-              xe[e] = valid ? xv : 0.0f;
-            }
-            ls.x += pe[0];
-            ls.y += pe[1];
-            pp[y] = pack_bf16x2(pe[0], pe[1]);
-            xp[y] = pack_bf16x2(xe[0], xe[1]);
-            if (last)
-              xs = __fadd2_rn(xs, make_float2(__uint_as_float(xp[y] << 16),
-                                              __uint_as_float(xp[y] & 0xffff0000u)));
-          }
-          tmem_st8_nowait(ts + 32 * ch + 16 * hp, pp);
-          tmem_st8_nowait(ts + 32 * ch + 16 * hp + 8, xp);
-        }
-      }
-      l += ls.x + ls.y;
-    };
-    chunk_px(ra, 0);
-    chunk_px(rb, 1);
-    tmem_wait_st();
+    // A, B and C have been read (the next item's products and third S product may write them),
+    // and so have the item's column sums
     tc_fence_before();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->w_full[b]);
-  }
-  if (!ok) {
-    report(a.status, kErrTimeout);
-    ms->abort = 1;
-  }
-  // ---- the two halves' exp-sums (both relative to the row's common reference) and last-tile
-  //      logit sums ----
-  float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
-  stat[w * kT + r] = make_float2(l, xs.x + xs.y);
-  named_bar_sync(1, 256);
-  const float2 s0 = stat[r], s1 = stat[kT + r];
-  const float lt = s0.x + s1.x;
-  if (ms->abort) return;
-  // ---- the row's coefficients, while the last products complete; then the output:
-  //      O = alpha A + beta B + gamma C, warpgroup w writing columns 32 w .. 32 w + 31 ----
-  if (!mbar_wait_warp(&ms->cb_full, 0, &ms->abort)) {
-    report(a.status, kErrTimeout);
-    ms->abort = 1;
-    return;
-  }
-  float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
-  if (row_ok) {
-    sig1 = sigmoid(gl1);
-    sigh = sigmoid(glh);
-    if (a.g0) sig0 = sigmoid(gl0);
-  }
-  // the logit sum: q_t . K_base over the earlier tiles, plus the last tile's bf16 logits
-  float qk = 0.0f;
-  {
-    const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
-    const float* kb = reinterpret_cast<const float*>(smem + CF::KBASE_OFF);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 u = lds128(qrow + sw128_off(r, c));
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        float lo, hi;
-        unpack_bf16x2(wv[y], lo, hi);
-        qk = __fmaf_rn(lo, kb[8 * c + 2 * y], qk);
-        qk = __fmaf_rn(hi, kb[8 * c + 2 * y + 1], qk);
-      }
+    if ((threadIdx.x & 31) == 0) {
+      mbar_arrive(&ms->acc_free);
+      mbar_arrive(&ms->cb_empty[par]);
     }
+    n0 += J;
   }
-  const float rt = 1.0f / tc;
-  const float alpha = lt > 0.0f ? sigh / lt : 0.0f;
-  const float beta = (sig1 - sigh) * rt;
-  const float Pt = (qk + s0.y + s1.y) * inv_sqrt_d;
-  const float bs = beta * inv_sqrt_d;
-  const float gamma = fmaf(-beta * Pt, rt, (sig0 - sigh) * rt);
-  if (!mbar_wait_warp(&ms->o_full, 0, &ms->abort)) {
-    report(a.status, kErrTimeout);
-    ms->abort = 1;
-    return;
-  }
-  tc_fence_after();
-  const int c0 = 32 * w;
-  const float* cbase = reinterpret_cast<const float*>(smem + CF::CBASE_OFF) + c0;
-  float o[32];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {  // two 16-column rounds
-    uint32_t av[16], bv[16], cv[16];
-    tmem_ld16_nowait(tl + CF::TM_A + c0 + 16 * hh, av);
-    tmem_ld16_nowait(tl + CF::TM_B + c0 + 16 * hh, bv);
-    if (a.causal) tmem_ld16_nowait(tl + sm1_sbuf(J % CF::NB) + c0 + 16 * hh, cv);
-    tmem_wait_ld();
-    reg_fence(av);
-    reg_fence(bv);
-    reg_fence(cv);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      float c = cbase[16 * hh + j];
-      if (a.causal) c += __uint_as_float(cv[j]);
-      o[16 * hh + j] = fmaf(alpha, __uint_as_float(av[j]),
-                            fmaf(bs, __uint_as_float(bv[j]), gamma * c));
-    }
-  }
-  if (row_ok) {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    uint4* dst = reinterpret_cast<uint4*>(out + row * 64 + c0);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-      dst[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]),
-                           pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
-                           pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]),
-                           pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
-  }
+  if (!ok) report(a.status, kErrTimeout);
 }
 
 __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constant__ SmParams p) {
@@ -949,13 +1065,9 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
   }
   Sm1Misc* ms = reinterpret_cast<Sm1Misc*>(smem + CF::MISC_OFF);
   const int warp = threadIdx.x >> 5;
-  const int nqt = (a.N + kT - 1) / kT;
-  // every sequence's heaviest (last) causal query tile first, then the next lighter ones
-  const int qt = a.causal ? nqt - 1 - (int)blockIdx.y : (int)blockIdx.y;
-  const int bh = blockIdx.x;
-  const int J = key_tiles(a, qt);
   if (threadIdx.x == 0) {
     mbar_init(&ms->q_full, 1);
+    mbar_init(&ms->q_empty, 9);  // the item's last S product and the 8 epilogue warps
     for (int i = 0; i < CF::NS; ++i) {
       mbar_init(&ms->kv_full[i], 1);
       mbar_init(&ms->kv_empty[i], 1);
@@ -965,8 +1077,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
       mbar_init(&ms->w_full[i], 8);  // the 8 epilogue warps
     }
     mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->acc_free, 8);
     mbar_init(&ms->fin, 1);
-    mbar_init(&ms->cb_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->cb_full[i], 2);   // warps 2 and 3
+      mbar_init(&ms->cb_empty[i], 8);  // the 8 epilogue warps
+    }
     ms->abort = 0;
     ms->never = 0;
   }
@@ -993,13 +1109,13 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
   tc_fence_after();
 
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) sm1_producer(p, smem, ms, bh, qt, J);
+    if ((threadIdx.x & 31) == 0) sm1_producer(p, smem, ms);
   } else if (warp == 1) {
-    sm1_mma(a, smem, ms, J);
+    sm1_mma(a, smem, ms);
   } else if (warp < 4) {
-    sm1_colsum(a, smem, ms, bh, J);
+    sm1_colsum(a, smem, ms);
   } else {
-    sm1_epilogue(a, smem, ms, bh, qt, J, (warp - 4) >> 2);
+    sm1_epilogue(a, smem, ms, (warp - 4) >> 2);
   }
 
   tc_fence_before();
@@ -1229,7 +1345,14 @@ cudaError_t launch_sm1(const SmArgs& a, cudaStream_t stream) {
   if (!sm_map(&p.tq, a.q, 64, a.N, BH) || !sm_map(&p.tk, a.k, 64, a.N, BH) ||
       !sm_map(&p.tv, a.v, 64, a.N, BH))
     return cudaErrorNotSupported;
-  const dim3 grid(BH, (a.N + kT - 1) / kT, 1);
+  // persistent: one CTA per SM (at most one per item)
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)BH * ((a.N + kT - 1) / kT);
+  if (items > 0x7fffffffll) return cudaErrorInvalidValue;
+  const int grid = (int)(items < sms ? items : sms);
+  if (grid == 0) return cudaSuccess;
   sm1_kernel<<<grid, kSmThreads, Sm1Cfg::BYTES, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
