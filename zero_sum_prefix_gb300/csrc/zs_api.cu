@@ -816,7 +816,8 @@ int zeros_sm_fwd(const void* q, const void* k, const void* v, const float* g1, c
   void* kr = static_cast<uint8_t*>(buf) + each;
   if (d == 64) {  // one pass: the statistics, and with rope the rotated q and k
     float* kstat = reinterpret_cast<float*>(static_cast<uint8_t*>(buf) + 2 * each);
-    cudaError_t e = launch_sm_prep(q, k, v, qr, kr, rope ? table : nullptr, kstat, B * H, N, st);
+    cudaError_t e = launch_sm_prep(q, k, v, qr, kr, rope ? table : nullptr, kstat, ws->status,
+                                   B * H, N, st);
     if (e != cudaSuccess) return cuda_fail(e, "ZeroS-SM key statistics launch");
     a.kstat = kstat;
   } else if (rope) {

@@ -138,8 +138,10 @@ cudaError_t launch_sm(const SmArgs& a, cudaStream_t stream);
 cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
                              const float2* table, int BH, int N, int d, cudaStream_t stream);
 // d = 64: the key-tile statistics of SmArgs::kstat, and with a rotary table also the rotated q
-// and k (into yq, yk; as launch_sm_rotate writes them), in one pass.
+// and k (into yq, yk; as launch_sm_rotate writes them), in one pass; a wait that gives up is
+// reported in *status.
 cudaError_t launch_sm_prep(const void* q, const void* k, const void* v, void* yq, void* yk,
-                           const float2* table, float* kstat, int BH, int N, cudaStream_t stream);
+                           const float2* table, float* kstat, int* status, int BH, int N,
+                           cudaStream_t stream);
 
 }  // namespace zs

@@ -1166,104 +1166,151 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
   }
 }
 
-// d = 64: one CTA of 512 threads per 128-key tile of one (b, h).  Thread (row r = tid / 4,
-// part p = tid % 4) holds the pairs 8 p .. 8 p + 7 of the tile's row r of k (and of q when
-// rotating), and the same columns of v: columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.
+// d = 64: CTAs of 512 threads walk the 128-key tiles of all (b, h) (tile i, i + G, ...; G CTAs,
+// two per SM), each tile's q, k and v brought in by TMA (128-byte swizzled, zero past the
+// sequence) two tiles ahead, so that the loads of the next tiles run while this one is worked
+// on.  Thread (row r = tid / 4, part p = tid % 4) takes the pairs 8 p .. 8 p + 7 of the tile's
+// row r of k (and of q when rotating): columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.
 // With a rotary table the row is rotated exactly as sm_rotate_kernel does it and rounded to bf16
 // once; the statistics are those of the bf16 values the attention kernel reads: the 64 column
 // sums of k and of v over the tile's keys (fp32; four 32-row partial sums, added in order) and
 // the largest row norm of k.
-__global__ void __launch_bounds__(512) sm_prep_kernel(const __nv_bfloat16* __restrict__ xq,
-                                                      const __nv_bfloat16* __restrict__ xk,
-                                                      const __nv_bfloat16* __restrict__ xv,
-                                                      __nv_bfloat16* __restrict__ yq,
-                                                      __nv_bfloat16* __restrict__ yk,
-                                                      const float2* __restrict__ table,
-                                                      float* __restrict__ kstat, int N, int nt) {
-  __shared__ __align__(16) __nv_bfloat16 sk[2][kT][64];  // k, v
-  __shared__ float part[4][128];
-  __shared__ float wmax[16];
-  const int tile = (int)(blockIdx.x % (unsigned)nt);
-  const size_t bh = blockIdx.x / (unsigned)nt;
-  const int tid = threadIdx.x, r = tid >> 2, p = tid & 3;
-  const int n = tile * kT + r;
-  const bool valid = n < N;
-  const size_t off = (bh * N + (size_t)(valid ? n : 0)) * 64 + 8 * p;
-  uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
-  if (valid) {
-    ka = *reinterpret_cast<const uint4*>(xk + off);
-    kb = *reinterpret_cast<const uint4*>(xk + off + 32);
-    va = *reinterpret_cast<const uint4*>(xv + off);
-    vb = *reinterpret_cast<const uint4*>(xv + off + 32);
+struct PrepParams {
+  CUtensorMap tq, tk, tv;  // q, k, v [B*H, N, 64] bf16, box {64, 128, 1}, 128-byte swizzle
+  __nv_bfloat16* yq;
+  __nv_bfloat16* yk;
+  const float2* table;     // (cos, sin) [N][32], or null: no rotation (q not read)
+  float* kstat;
+  int* status;
+  int N, nt, ntiles;       // key tiles per sequence, over all sequences
+};
+struct PrepSmem {
+  static constexpr uint32_t TILES = 0;                       // [2 buffers][q, k, v] atoms
+  static constexpr uint32_t PART = 2 * 3 * kAtom;            // float [2][4][128] partial sums
+  static constexpr uint32_t WMAX = PART + 2 * 4 * 128 * 4;   // float [2][16] warp maxima
+  static constexpr uint32_t BAR = WMAX + 2 * 16 * 4;         // two mbarriers
+  static constexpr uint32_t BYTES = BAR + 16;
+};
+constexpr int kPrepThreads = 512;
+
+__global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_constant__ PrepParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report(p.status, kErrUnsupported);
+    return;
   }
-  if (table != nullptr && valid) {
-    const float4* tb = reinterpret_cast<const float4*>(table + (size_t)n * 32 + 8 * p);
-    float4 cs[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) cs[e] = tb[e];  // (cos, sin) of pairs 8 p + 2 e, 8 p + 2 e + 1
-    auto rotate = [&](uint4& ua, uint4& ub) {
-      uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float xa0, xa1, xb0, xb1;
-        unpack_bf16x2(wa[e], xa0, xa1);
-        unpack_bf16x2(wb[e], xb0, xb1);
-        wa[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].x, -xb0 * cs[e].y),
-                            __fmaf_rn(xa1, cs[e].z, -xb1 * cs[e].w));
-        wb[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].y, xb0 * cs[e].x),
-                            __fmaf_rn(xa1, cs[e].w, xb1 * cs[e].z));
-      }
-      ua = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-      ub = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-    };
-    rotate(ka, kb);
-    uint4 qa = *reinterpret_cast<const uint4*>(xq + off);
-    uint4 qb = *reinterpret_cast<const uint4*>(xq + off + 32);
-    rotate(qa, qb);
-    *reinterpret_cast<uint4*>(yq + off) = qa;
-    *reinterpret_cast<uint4*>(yq + off + 32) = qb;
-    *reinterpret_cast<uint4*>(yk + off) = ka;
-    *reinterpret_cast<uint4*>(yk + off + 32) = kb;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + PrepSmem::BAR);
+  const int tid = threadIdx.x, r = tid >> 2, pp = tid & 3;
+  const bool rot = p.table != nullptr;
+  const uint32_t base = smem_u32(smem) + PrepSmem::TILES;
+  // thread 0: the q (when rotating), k and v tiles of work tile i into buffer b
+  auto issue = [&](int i, int b) {
+    const int tile = i % p.nt, bh = i / p.nt;
+    const uint32_t dst = base + (uint32_t)b * 3 * kAtom;
+    mbar_arrive_expect_tx(&bar[b], (rot ? 3 : 2) * kAtom);
+    if (rot) tma_load_3d(dst, &p.tq, 0, tile * kT, bh, &bar[b]);
+    tma_load_3d(dst + kAtom, &p.tk, 0, tile * kT, bh, &bar[b]);
+    tma_load_3d(dst + 2 * kAtom, &p.tv, 0, tile * kT, bh, &bar[b]);
+  };
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
   }
-  // squared row norm (this thread's 16 values, then the row), the tile's largest
-  float n2 = 0.0f;
-  {
-    const uint32_t w8[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+  __syncthreads();
+  const int G = (int)gridDim.x;
+  if (tid == 0) {
+    issue(blockIdx.x, 0);
+    if ((int)blockIdx.x + G < p.ntiles) issue(blockIdx.x + G, 1);
+  }
+  int never = 0;
+  for (int j = 0, i = blockIdx.x; i < p.ntiles; ++j, i += G) {
+    const int b = j & 1;
+    const int tile = i % p.nt, bh = i / p.nt;
+    const int n = tile * kT + r;
+    const bool valid = n < p.N;
+    const uint32_t qt = base + (uint32_t)b * 3 * kAtom, kt = qt + kAtom, vt = kt + kAtom;
+    if (!mbar_wait(&bar[b], (j >> 1) & 1, &never)) report(p.status, kErrTimeout);
+    uint4 ka = lds128(kt + sw128_off(r, pp)), kb = lds128(kt + sw128_off(r, 4 + pp));
+    if (rot && valid) {
+      const float4* tb = reinterpret_cast<const float4*>(p.table + (size_t)n * 32 + 8 * pp);
+      float4 cs[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float x0, x1;
-      unpack_bf16x2(w8[e], x0, x1);
-      n2 = __fmaf_rn(x0, x0, n2);
-      n2 = __fmaf_rn(x1, x1, n2);
+      for (int e = 0; e < 4; ++e) cs[e] = tb[e];  // (cos, sin) of pairs 8 p + 2 e, 8 p + 2 e + 1
+      auto rotate = [&](uint4& ua, uint4& ub) {
+        uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float xa0, xa1, xb0, xb1;
+          unpack_bf16x2(wa[e], xa0, xa1);
+          unpack_bf16x2(wb[e], xb0, xb1);
+          wa[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].x, -xb0 * cs[e].y),
+                              __fmaf_rn(xa1, cs[e].z, -xb1 * cs[e].w));
+          wb[e] = pack_bf16x2(__fmaf_rn(xa0, cs[e].y, xb0 * cs[e].x),
+                              __fmaf_rn(xa1, cs[e].w, xb1 * cs[e].z));
+        }
+        ua = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        ub = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+      };
+      rotate(ka, kb);
+      uint4 qa = lds128(qt + sw128_off(r, pp)), qb = lds128(qt + sw128_off(r, 4 + pp));
+      rotate(qa, qb);
+      const size_t off = ((size_t)bh * p.N + n) * 64 + 8 * pp;
+      *reinterpret_cast<uint4*>(p.yq + off) = qa;
+      *reinterpret_cast<uint4*>(p.yq + off + 32) = qb;
+      *reinterpret_cast<uint4*>(p.yk + off) = ka;
+      *reinterpret_cast<uint4*>(p.yk + off + 32) = kb;
+      // the rotated row, for the column sums
+      sts128(kt + sw128_off(r, pp), ka);
+      sts128(kt + sw128_off(r, 4 + pp), kb);
     }
-  }
-  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
-  n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+    // squared row norm (this thread's 16 values, then the row), the tile's largest
+    float n2 = 0.0f;
+    {
+      const uint32_t w8[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
-  if ((tid & 31) == 0) wmax[tid >> 5] = n2;
-  *reinterpret_cast<uint4*>(&sk[0][r][8 * p]) = ka;
-  *reinterpret_cast<uint4*>(&sk[0][r][32 + 8 * p]) = kb;
-  *reinterpret_cast<uint4*>(&sk[1][r][8 * p]) = va;
-  *reinterpret_cast<uint4*>(&sk[1][r][32 + 8 * p]) = vb;
-  __syncthreads();
-  {
-    const int c = tid & 127, qq = tid >> 7;  // column c of k (c < 64) or of v
-    const __nv_bfloat16* col = &sk[c >> 6][0][c & 63];
-    float sum = 0.0f;
+      for (int e = 0; e < 8; ++e) {
+        float x0, x1;
+        unpack_bf16x2(w8[e], x0, x1);
+        n2 = __fmaf_rn(x0, x0, n2);
+        n2 = __fmaf_rn(x1, x1, n2);
+      }
+    }
+    n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+    n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+    float* wmax = reinterpret_cast<float*>(smem + PrepSmem::WMAX) + b * 16;
+    float* part = reinterpret_cast<float*>(smem + PrepSmem::PART) + b * 4 * 128;
+    if ((tid & 31) == 0) wmax[tid >> 5] = n2;
+    __syncthreads();
+    {
+      const int c = tid & 127, qq = tid >> 7;  // column c of k (c < 64) or of v
+      const uint32_t tt = c < 64 ? kt : vt;
+      const int cc = c & 63;
+      float sum = 0.0f;
 #pragma unroll 8
-    for (int rr = 32 * qq; rr < 32 * qq + 32; ++rr) sum += __bfloat162float(col[rr * 64]);
-    part[qq][c] = sum;
-  }
-  __syncthreads();
-  float* st = kstat + (bh * nt + tile) * kSmStat;
-  if (tid < 128) {
-    st[tid < 64 ? tid : tid + 4] = ((part[0][tid] + part[1][tid]) + part[2][tid]) + part[3][tid];
-  } else if (tid == 128) {
-    float m = wmax[0];
+      for (int rr = 32 * qq; rr < 32 * qq + 32; ++rr) {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(tt + sw128_off(rr, cc >> 3) + 2 * (cc & 7)));
+        sum += __uint_as_float((uint32_t)h << 16);
+      }
+      part[qq * 128 + c] = sum;
+    }
+    __syncthreads();  // every read of buffer b is done: it takes the tile after next
+    if (tid == 0 && i + 2 * G < p.ntiles) {
+      fence_proxy_async_smem();
+      issue(i + 2 * G, b);
+    }
+    float* st = p.kstat + ((size_t)bh * p.nt + tile) * kSmStat;
+    if (tid < 128) {
+      st[tid < 64 ? tid : tid + 4] =
+          ((part[tid] + part[128 + tid]) + part[256 + tid]) + part[384 + tid];
+    } else if (tid == 128) {
+      float m = wmax[0];
 #pragma unroll
-    for (int w = 1; w < 16; ++w) m = fmaxf(m, wmax[w]);
-    st[64] = sqrtf(m);
+      for (int w = 1; w < 16; ++w) m = fmaxf(m, wmax[w]);
+      st[64] = sqrtf(m);
+    }
   }
 }
 
@@ -1376,15 +1423,39 @@ cudaError_t launch_sm_rotate(const void* q, const void* k, void* yq, void* yk,
 }
 
 cudaError_t launch_sm_prep(const void* q, const void* k, const void* v, void* yq, void* yk,
-                           const float2* table, float* kstat, int BH, int N, cudaStream_t stream) {
+                           const float2* table, float* kstat, int* status, int BH, int N,
+                           cudaStream_t stream) {
   const int nt = (N + kT - 1) / kT;
-  const size_t ctas = (size_t)BH * nt;
-  if (ctas == 0) return cudaSuccess;
-  if (ctas > 0x7fffffffu) return cudaErrorInvalidValue;
-  sm_prep_kernel<<<(unsigned)ctas, 512, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(yq),
-      static_cast<__nv_bfloat16*>(yk), table, kstat, N, nt);
+  const long long ntiles = (long long)BH * nt;
+  if (ntiles == 0) return cudaSuccess;
+  if (ntiles > 0x7fffffffll) return cudaErrorInvalidValue;
+  static std::atomic<uint64_t> attr_set{0};  // bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(sm_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PrepSmem::BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  PrepParams p;
+  if (!sm_map(&p.tq, q, 64, N, BH) || !sm_map(&p.tk, k, 64, N, BH) || !sm_map(&p.tv, v, 64, N, BH))
+    return cudaErrorNotSupported;
+  p.yq = static_cast<__nv_bfloat16*>(yq);
+  p.yk = static_cast<__nv_bfloat16*>(yk);
+  p.table = table;
+  p.kstat = kstat;
+  p.status = status;
+  p.N = N;
+  p.nt = nt;
+  p.ntiles = (int)ntiles;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)(ntiles < 2ll * sms ? ntiles : 2ll * sms);  // two CTAs per SM
+  sm_prep_kernel<<<grid, kPrepThreads, PrepSmem::BYTES, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }
