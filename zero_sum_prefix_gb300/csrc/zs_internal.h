@@ -66,12 +66,12 @@ struct SmArgs {
   void* out;
   int B, H, N, d, causal;
   int* status;
-  // d = 64: per 128-key tile, [B*H][tiles][kSmStat] fp32: the column sums of k as the kernel
-  // reads it (0..63), the largest row norm of k (64), the column sums of v (68..131);
-  // written by launch_sm_prep
+  // d = 64: per 128-token tile, [B*H][tiles][kSmStat] fp32: the column sums of k as the kernel
+  // reads it (0..63), the largest row norm of k (64), the column sums of v (68..131), the norm
+  // of each row of q as the kernel reads it (132..259); written by launch_sm_prep
   const float* kstat;
 };
-constexpr int kSmStat = 132;
+constexpr int kSmStat = 260;
 
 // Counts every kernel launch the library issues (zs_api.cu).
 void count_launches(unsigned n);

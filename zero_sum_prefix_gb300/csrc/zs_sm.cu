@@ -524,11 +524,12 @@ struct Sm1Cfg {
   static constexpr uint32_t XMAX_OFF = TRI_OFF + 2 * kAtom;    // float [2 bufs][2 halves][128]
   static constexpr uint32_t STAT_OFF = XMAX_OFF + 4 * kT * 4;  // float2 [2][128] sums
   static constexpr uint32_t CBASE_OFF = STAT_OFF + 2 * kT * 8;  // float [2 items][64]
-  static constexpr uint32_t KBASE_OFF = CBASE_OFF + 2 * 64 * 4;  // float [2 items][64]
-  static constexpr uint32_t QN_OFF = KBASE_OFF + 2 * 64 * 4;     // float [128]
-  // per row, by item parity: the gate logits (g1, gh, g0) and q_t . K_base
-  static constexpr uint32_t ROWV_OFF = QN_OFF + kT * 4;         // float [2 items][4][128]
-  static constexpr uint32_t MISC_OFF = ROWV_OFF + 2 * 4 * kT * 4;
+  // K_base, one copy per column-sum warp
+  static constexpr uint32_t KBASE_OFF = CBASE_OFF + 2 * 64 * 4;  // float [2 items][2][64]
+  // per row, by item parity: the gate logits (g1, gh, g0), q_t . K_base and the bound factor
+  // c2 |q_t| (1 + slack)
+  static constexpr uint32_t ROWV_OFF = KBASE_OFF + 2 * 2 * 64 * 4;  // float [2 items][5][128]
+  static constexpr uint32_t MISC_OFF = ROWV_OFF + 2 * 5 * kT * 4;
   static constexpr uint32_t BYTES = MISC_OFF + 256;
   static_assert(BYTES <= 232448, "shared memory budget of one CTA");
   static constexpr uint32_t TM_A = 384, TM_B = 448;
@@ -706,18 +707,23 @@ __device__ void sm1_mma(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
   __syncwarp();
 }
 
-// Warps 2 and 3 (thread = column t, warp 2 columns 0..31, warp 3 columns 32..63): per item the
+// Warps 2 and 3 (thread t = 0..63: C_base column t, query rows t and t + 64): per item the
 // parts of C and P_t that are the same for every row, from the per-tile statistics: K_base = the
 // key column sums of the tiles before the last one, C_base = the value column sums of the tiles
 // before the diagonal one (all tiles in encoder mode); eight partial sums over the tiles
 // (g = 8 j + u), added in a fixed order, so that the loads overlap; and the gate logits of the
-// item's rows.  Two buffers (by item parity): an item's values are written once the epilogue
-// has used those of two items before, so their loads run ahead of the epilogue.
+// item's rows with the bound factor of their logits; once the query tile has landed, each row's
+// q_t . K_base (each warp keeps its own copy of K_base).  Two buffers (by item parity): an
+// item's values are written once the epilogue has used those of two items before, so their
+// loads run ahead of the epilogue.
 __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
   using CF = Sm1Cfg;
-  const int t = threadIdx.x - 64;  // column
+  constexpr float c2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(d), d = 64
+  const int t = threadIdx.x - 64;     // C_base column, and the rows t and t + 64
+  const int c = t >> 5, l = t & 31;   // this warp (0, 1) and lane
   const int nt = (a.N + kT - 1) / kT;
   const int nitems = sm1_items(a);
+  const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
   for (int it = 0, item = sm1_mine(0); item < nitems; item = sm1_mine(++it)) {
     const Sm1Item w = sm1_item(a, item);
     const int par = it & 1;
@@ -726,23 +732,31 @@ __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
       ms->abort = 1;
       return;
     }
-    const float* st = a.kstat + (size_t)w.bh * nt * kSmStat + t;
-    float pk[8] = {}, pv[8] = {};
+    // K_base over all 64 columns (this lane: columns l and l + 32), C_base over the column t
+    const float* st = a.kstat + (size_t)w.bh * nt * kSmStat;
+    float pk0[8] = {}, pk1[8] = {}, pv[8] = {};
     const int nk = w.J - 1, nv = a.causal ? w.J - 1 : w.J;
     for (int g0 = 0; g0 < nv; g0 += 8) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int g = g0 + u;
-        if (g < nk) pk[u] += st[(size_t)g * kSmStat];
-        if (g < nv) pv[u] += st[(size_t)g * kSmStat + 68];
+        if (g < nk) {
+          pk0[u] += st[(size_t)g * kSmStat + l];
+          pk1[u] += st[(size_t)g * kSmStat + 32 + l];
+        }
+        if (g < nv) pv[u] += st[(size_t)g * kSmStat + 68 + t];
       }
     }
-    const float sk = ((pk[0] + pk[1]) + (pk[2] + pk[3])) + ((pk[4] + pk[5]) + (pk[6] + pk[7]));
-    const float sv = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-    reinterpret_cast<float*>(smem + CF::KBASE_OFF)[par * 64 + t] = sk;
-    reinterpret_cast<float*>(smem + CF::CBASE_OFF)[par * 64 + t] = sv;
-    // the gate logits of the item's rows t and t + 64
-    float* rowv = reinterpret_cast<float*>(smem + CF::ROWV_OFF) + par * 4 * kT;
+    auto sum8 = [](const float (&x)[8]) {
+      return ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+    };
+    float* kb = reinterpret_cast<float*>(smem + CF::KBASE_OFF) + (par * 2 + c) * 64;
+    kb[l] = sum8(pk0);
+    kb[32 + l] = sum8(pk1);
+    reinterpret_cast<float*>(smem + CF::CBASE_OFF)[par * 64 + t] = sum8(pv);
+    // per row rr (t and t + 64): the gate logits and the bound factor of its logits
+    float* rowv = reinterpret_cast<float*>(smem + CF::ROWV_OFF) + par * 5 * kT;
+    const float* qn = st + (size_t)w.qt * kSmStat + 132;  // the norms of the tile's q rows
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int rr = t + 64 * h, tq = w.qt * kT + rr;
@@ -751,17 +765,45 @@ __device__ void sm1_colsum(const SmArgs& a, uint8_t* smem, Sm1Misc* ms) {
       rowv[rr] = valid ? a.g1[row] : 0.0f;
       rowv[kT + rr] = valid ? a.gh[row] : 0.0f;
       rowv[2 * kT + rr] = (valid && a.g0) ? a.g0[row] : 0.0f;
+      rowv[4 * kT + rr] = qn[rr] * (c2 * CF::kBoundSlack);
     }
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->cb_full[par]);  // count 2: both warps
+    // the earlier tiles' part of the logit sum of the rows t and t + 64, q_t . K_base (four
+    // partial sums), once the query tile has landed; then Q is not read again here
+    if (!mbar_wait_warp(&ms->q_full, par, &ms->abort)) {
+      report(a.status, kErrTimeout);
+      ms->abort = 1;
+      return;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = t + 64 * h;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 u = lds128(qrow + sw128_off(rr, cc));
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          float lo, hi;
+          unpack_bf16x2(wv[y], lo, hi);
+          acc[y] = __fmaf_rn(hi, kb[8 * cc + 2 * y + 1], __fmaf_rn(lo, kb[8 * cc + 2 * y], acc[y]));
+        }
+      }
+      rowv[3 * kT + rr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    __syncwarp();
+    if (l == 0) {
+      mbar_arrive(&ms->cb_full[par]);  // count 2: both warps
+      mbar_arrive(&ms->q_empty);       // count 3: the item's last S and both warps
+    }
   }
 }
 
 // Both warpgroups take every key tile; warpgroup w its keys 64 w .. 64 w + 63.  Thread = query
 // row of the tile; warp wq of warpgroup 0 and warp wq of warpgroup 1 hold the same 32 rows.
-// Per item: |q_t| and q_t . K_base while Q is resident (then Q is released), the key tiles, and
-// the output once the item's products have completed (then A, B, C and the item's sums are
-// released).  Every named barrier is taken alike by all its warps, also after a failed wait (the
+// Per item: the key tiles (the per-row values come from warps 2 and 3), and the output once the
+// item's products have completed (then A, B, C and the item's sums are released).  Every named barrier is taken alike by all its warps, also after a failed wait (the
 // work is then skipped); after a failure anywhere, the barrier at the end of the item's tiles
 // tells every epilogue warp to stop.
 __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w) {
@@ -773,9 +815,7 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w)
   constexpr float c2 = 1.4426950408889634f * inv_sqrt_d;   // log2(e) / sqrt(d)
   const int nt = (a.N + kT - 1) / kT;
   float* xmax = reinterpret_cast<float*>(smem + CF::XMAX_OFF);
-  float* qnorm = reinterpret_cast<float*>(smem + CF::QN_OFF);
   float2* stat = reinterpret_cast<float2*>(smem + CF::STAT_OFF);
-  const uint32_t qrow = smem_u32(smem) + CF::Q_OFF;
   bool ok = true;
   int ex = 0;  // exchanges so far (alternating buffers), over all items
   int n0 = 0;  // the item's first key tile, counted over all items
@@ -786,49 +826,10 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w)
     // last key visible to every row of this warp (uniform, as the aligned TMEM accesses require)
     const int lim_warp = a.causal ? wi.qt * kT + wq * 32 : a.N - 1;
     const int kn0 = wi.bh * nt;  // this sequence's first tile statistics record
-    if (ok) ok = mbar_wait_warp(&ms->q_full, par, &ms->abort);
-    // |q_t| of this row (the bf16 values the tensor cores read), for the bound of its logits;
-    // warpgroup 0 computes it and both warps of the row pair take that one value, so that their
-    // exchange decisions below agree whatever happens
-    if (w == 0) {
-      float qn = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 u = lds128(qrow + sw128_off(r, c));
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          float lo, hi;
-          unpack_bf16x2(wv[y], lo, hi);
-          qn = __fmaf_rn(lo, lo, __fmaf_rn(hi, hi, qn));
-        }
-      }
-      qnorm[r] = sqrtf(qn) * (c2 * CF::kBoundSlack);
-    }
-    named_bar_sync(3 + wq, 64);
-    const float qn = qnorm[r];
-    // the earlier tiles' part of the logit sum, q_t . K_base (warpgroup 0); then Q is not read
-    // again
+    // the item's per-row values (gates, q_t . K_base, the bound factor of the logits: both warps
+    // of a row pair read the one value, so that their exchange decisions below agree)
     if (ok) ok = mbar_wait_warp(&ms->cb_full[par], (it >> 1) & 1, &ms->abort);
-    if (w == 0) {
-      float qk = 0.0f;
-      const float* kb = reinterpret_cast<const float*>(smem + CF::KBASE_OFF) + par * 64;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 u = lds128(qrow + sw128_off(r, c));
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          float lo, hi;
-          unpack_bf16x2(wv[y], lo, hi);
-          qk = __fmaf_rn(lo, kb[8 * c + 2 * y], qk);
-          qk = __fmaf_rn(hi, kb[8 * c + 2 * y + 1], qk);
-        }
-      }
-      reinterpret_cast<float*>(smem + CF::ROWV_OFF)[(par * 4 + 3) * kT + r] = qk;
-    }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms->q_empty);  // count 9: the last S, 8 warps
+    const float qn = reinterpret_cast<const float*>(smem + CF::ROWV_OFF)[(par * 5 + 4) * kT + r];
     if (!ok) ms->abort = 1;
     float m2 = -INFINITY, l = 0.0f;  // the row's reference (base-2 units), this half's exp-sum
     float2 xs = make_float2(0.0f, 0.0f);  // this half's sum of the last tile's bf16 logits
@@ -989,7 +990,7 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w)
     const int t = wd.qt * kT + r;  // query index (0-based)
     const bool row_ok = t < a.N;
     const float tc = a.causal ? (float)(t + 1) : (float)a.N;
-    const float* rowv = reinterpret_cast<const float*>(smem + CF::ROWV_OFF) + par * 4 * kT + r;
+    const float* rowv = reinterpret_cast<const float*>(smem + CF::ROWV_OFF) + par * 5 * kT + r;
     float sig1 = 0.0f, sigh = 0.0f, sig0 = 0.0f;
     if (row_ok) {
       sig1 = sigmoid(rowv[0]);
@@ -1067,7 +1068,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) sm1_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(&ms->q_full, 1);
-    mbar_init(&ms->q_empty, 9);  // the item's last S product and the 8 epilogue warps
+    mbar_init(&ms->q_empty, 3);  // the item's last S product and warps 2, 3
     for (int i = 0; i < CF::NS; ++i) {
       mbar_init(&ms->kv_full[i], 1);
       mbar_init(&ms->kv_empty[i], 1);
@@ -1166,20 +1167,20 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
   }
 }
 
-// d = 64: CTAs of 512 threads walk the 128-key tiles of all (b, h) (tile i, i + G, ...; G CTAs,
+// d = 64: CTAs of 512 threads walk the 128-token tiles of all (b, h) (tile i, i + G, ...; G CTAs,
 // two per SM), each tile's q, k and v brought in by TMA (128-byte swizzled, zero past the
 // sequence) two tiles ahead, so that the loads of the next tiles run while this one is worked
 // on.  Thread (row r = tid / 4, part p = tid % 4) takes the pairs 8 p .. 8 p + 7 of the tile's
 // row r of k (and of q when rotating): columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.
 // With a rotary table the row is rotated exactly as sm_rotate_kernel does it and rounded to bf16
 // once; the statistics are those of the bf16 values the attention kernel reads: the 64 column
-// sums of k and of v over the tile's keys (fp32; four 32-row partial sums, added in order) and
-// the largest row norm of k.
+// sums of k and of v over the tile's keys (fp32; four 32-row partial sums, added in order), the
+// largest row norm of k and the norm of every row of q.
 struct PrepParams {
   CUtensorMap tq, tk, tv;  // q, k, v [B*H, N, 64] bf16, box {64, 128, 1}, 128-byte swizzle
   __nv_bfloat16* yq;
   __nv_bfloat16* yk;
-  const float2* table;     // (cos, sin) [N][32], or null: no rotation (q not read)
+  const float2* table;     // (cos, sin) [N][32], or null: no rotation
   float* kstat;
   int* status;
   int N, nt, ntiles;       // key tiles per sequence, over all sequences
@@ -1203,12 +1204,12 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
   const int tid = threadIdx.x, r = tid >> 2, pp = tid & 3;
   const bool rot = p.table != nullptr;
   const uint32_t base = smem_u32(smem) + PrepSmem::TILES;
-  // thread 0: the q (when rotating), k and v tiles of work tile i into buffer b
+  // thread 0: the q, k and v tiles of work tile i into buffer b
   auto issue = [&](int i, int b) {
     const int tile = i % p.nt, bh = i / p.nt;
     const uint32_t dst = base + (uint32_t)b * 3 * kAtom;
-    mbar_arrive_expect_tx(&bar[b], (rot ? 3 : 2) * kAtom);
-    if (rot) tma_load_3d(dst, &p.tq, 0, tile * kT, bh, &bar[b]);
+    mbar_arrive_expect_tx(&bar[b], 3 * kAtom);
+    tma_load_3d(dst, &p.tq, 0, tile * kT, bh, &bar[b]);
     tma_load_3d(dst + kAtom, &p.tk, 0, tile * kT, bh, &bar[b]);
     tma_load_3d(dst + 2 * kAtom, &p.tv, 0, tile * kT, bh, &bar[b]);
   };
@@ -1231,6 +1232,7 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
     const uint32_t qt = base + (uint32_t)b * 3 * kAtom, kt = qt + kAtom, vt = kt + kAtom;
     if (!mbar_wait(&bar[b], (j >> 1) & 1, &never)) report(p.status, kErrTimeout);
     uint4 ka = lds128(kt + sw128_off(r, pp)), kb = lds128(kt + sw128_off(r, 4 + pp));
+    uint4 qa = lds128(qt + sw128_off(r, pp)), qb = lds128(qt + sw128_off(r, 4 + pp));
     if (rot && valid) {
       const float4* tb = reinterpret_cast<const float4*>(p.table + (size_t)n * 32 + 8 * pp);
       float4 cs[4];
@@ -1252,7 +1254,6 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
         ub = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       };
       rotate(ka, kb);
-      uint4 qa = lds128(qt + sw128_off(r, pp)), qb = lds128(qt + sw128_off(r, 4 + pp));
       rotate(qa, qb);
       const size_t off = ((size_t)bh * p.N + n) * 64 + 8 * pp;
       *reinterpret_cast<uint4*>(p.yq + off) = qa;
@@ -1263,20 +1264,28 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
       sts128(kt + sw128_off(r, pp), ka);
       sts128(kt + sw128_off(r, 4 + pp), kb);
     }
-    // squared row norm (this thread's 16 values, then the row), the tile's largest
-    float n2 = 0.0f;
+    // squared row norms of k and of q (this thread's 16 values, then the row); the norm of each
+    // q row, and the tile's largest of k
+    float n2 = 0.0f, q2 = 0.0f;
     {
       const uint32_t w8[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+      const uint32_t v8[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float x0, x1;
+        float x0, x1, y0, y1;
         unpack_bf16x2(w8[e], x0, x1);
         n2 = __fmaf_rn(x0, x0, n2);
         n2 = __fmaf_rn(x1, x1, n2);
+        unpack_bf16x2(v8[e], y0, y1);
+        q2 = __fmaf_rn(y0, y0, q2);
+        q2 = __fmaf_rn(y1, y1, q2);
       }
     }
     n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
     n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+    q2 += __shfl_xor_sync(0xffffffffu, q2, 1);
+    q2 += __shfl_xor_sync(0xffffffffu, q2, 2);
+    if (pp == 0) p.kstat[((size_t)bh * p.nt + tile) * kSmStat + 132 + r] = sqrtf(q2);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) n2 = fmaxf(n2, __shfl_xor_sync(0xffffffffu, n2, o));
     float* wmax = reinterpret_cast<float*>(smem + PrepSmem::WMAX) + b * 16;
