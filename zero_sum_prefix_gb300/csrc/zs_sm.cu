@@ -1029,16 +1029,42 @@ __device__ void sm1_epilogue(const SmArgs& a, uint8_t* smem, Sm1Misc* ms, int w)
                                 fmaf(bs, __uint_as_float(bv[j]), gamma * c));
         }
       }
-      if (row_ok) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)wd.bh * a.N + t) * 64 + c0);
+      // the row's 64 output bytes as four 16-byte chunks, transposed within each group of four
+      // lanes (rows 4g .. 4g + 3 of the warp) so that each store instruction writes whole 64-byte
+      // row segments of eight rows rather than 16 bytes of 32 rows: afterwards lane 4g + j holds
+      // chunk j of the row 4g + k in x[k]
+      uint4 x[4];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          dst[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]),
-                               pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
-                               pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]),
-                               pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+      for (int q4 = 0; q4 < 4; ++q4)
+        x[q4] = make_uint4(pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]),
+                           pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                           pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]),
+                           pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]));
+      const int lane = (int)(threadIdx.x & 31), j = lane & 3;
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        const bool up = (j & m) != 0;
+#pragma unroll
+        for (int s0 = 0; s0 < 4; ++s0) {
+          if (s0 & m) continue;  // the pair (s0, s0 | m)
+          const uint4 send = up ? x[s0] : x[s0 | m];
+          uint4 recv;
+          recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+          recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+          recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+          recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+          if (up)
+            x[s0] = recv;
+          else
+            x[s0 | m] = recv;
+        }
       }
+      const int t4 = wd.qt * kT + wq * 32 + (lane & ~3);  // query index of the group's first row
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (t4 + k < a.N)
+          *reinterpret_cast<uint4*>(out + ((size_t)wd.bh * a.N + t4 + k) * 64 + c0 + 8 * j) = x[k];
     } else {
       ms->abort = 1;
     }
