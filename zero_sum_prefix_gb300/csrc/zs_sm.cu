@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "zs_common.cuh"
@@ -1193,10 +1194,11 @@ __global__ void sm_rotate_kernel(const __nv_bfloat16* __restrict__ xq,
   }
 }
 
-// d = 64: CTAs of 512 threads walk the 128-token tiles of all (b, h) (tile i, i + G, ...; G CTAs,
-// two per SM), each tile's q, k and v brought in by TMA (128-byte swizzled, zero past the
-// sequence) two tiles ahead, so that the loads of the next tiles run while this one is worked
-// on.  Thread (row r = tid / 4, part p = tid % 4) takes the pairs 8 p .. 8 p + 7 of the tile's
+// d = 64: CTAs of 512 threads walk the 128-token tiles of all (b, h): CTA c takes the tile
+// position c % nt of the sequences c / nt, c / nt + S, ... (S CTAs per position, about two CTAs
+// per SM in all), so that the rotary table entries of its rows are loaded once; each tile's q, k
+// and v are brought in by TMA (128-byte swizzled, zero past the sequence) two tiles ahead, so
+// that the loads of the next tiles run while this one is worked on.  Thread (row r = tid / 4, part p = tid % 4) takes the pairs 8 p .. 8 p + 7 of the tile's
 // row r of k (and of q when rotating): columns 8 p .. 8 p + 7 and 32 + 8 p .. 32 + 8 p + 7.
 // With a rotary table the row is rotated exactly as sm_rotate_kernel does it and rounded to bf16
 // once; the statistics are those of the bf16 values the attention kernel reads: the 64 column
@@ -1209,7 +1211,7 @@ struct PrepParams {
   const float2* table;     // (cos, sin) [N][32], or null: no rotation
   float* kstat;
   int* status;
-  int N, nt, ntiles;       // key tiles per sequence, over all sequences
+  int N, nt, BH, S;        // tiles per sequence, sequences, CTAs per tile position
 };
 struct PrepSmem {
   static constexpr uint32_t TILES = 0;                       // [2 buffers][q, k, v] atoms
@@ -1230,9 +1232,9 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
   const int tid = threadIdx.x, r = tid >> 2, pp = tid & 3;
   const bool rot = p.table != nullptr;
   const uint32_t base = smem_u32(smem) + PrepSmem::TILES;
-  // thread 0: the q, k and v tiles of work tile i into buffer b
-  auto issue = [&](int i, int b) {
-    const int tile = i % p.nt, bh = i / p.nt;
+  const int tile = (int)blockIdx.x % p.nt, bh0 = (int)blockIdx.x / p.nt;
+  // thread 0: the q, k and v tiles of sequence bh into buffer b
+  auto issue = [&](int bh, int b) {
     const uint32_t dst = base + (uint32_t)b * 3 * kAtom;
     mbar_arrive_expect_tx(&bar[b], 3 * kAtom);
     tma_load_3d(dst, &p.tq, 0, tile * kT, bh, &bar[b]);
@@ -1244,26 +1246,26 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
     mbar_init(&bar[1], 1);
   }
   __syncthreads();
-  const int G = (int)gridDim.x;
   if (tid == 0) {
-    issue(blockIdx.x, 0);
-    if ((int)blockIdx.x + G < p.ntiles) issue(blockIdx.x + G, 1);
+    if (bh0 < p.BH) issue(bh0, 0);
+    if (bh0 + p.S < p.BH) issue(bh0 + p.S, 1);
   }
+  const int n = tile * kT + r;
+  const bool valid = n < p.N;
+  // (cos, sin) of this thread's pairs 8 p + 2 e, 8 p + 2 e + 1, the same for every sequence
+  float4 cs[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    cs[e] = (rot && valid) ? reinterpret_cast<const float4*>(p.table + (size_t)n * 32 + 8 * pp)[e]
+                           : make_float4(1.0f, 0.0f, 1.0f, 0.0f);
   int never = 0;
-  for (int j = 0, i = blockIdx.x; i < p.ntiles; ++j, i += G) {
+  for (int j = 0, bh = bh0; bh < p.BH; ++j, bh += p.S) {
     const int b = j & 1;
-    const int tile = i % p.nt, bh = i / p.nt;
-    const int n = tile * kT + r;
-    const bool valid = n < p.N;
     const uint32_t qt = base + (uint32_t)b * 3 * kAtom, kt = qt + kAtom, vt = kt + kAtom;
     if (!mbar_wait(&bar[b], (j >> 1) & 1, &never)) report(p.status, kErrTimeout);
     uint4 ka = lds128(kt + sw128_off(r, pp)), kb = lds128(kt + sw128_off(r, 4 + pp));
     uint4 qa = lds128(qt + sw128_off(r, pp)), qb = lds128(qt + sw128_off(r, 4 + pp));
     if (rot && valid) {
-      const float4* tb = reinterpret_cast<const float4*>(p.table + (size_t)n * 32 + 8 * pp);
-      float4 cs[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cs[e] = tb[e];  // (cos, sin) of pairs 8 p + 2 e, 8 p + 2 e + 1
       auto rotate = [&](uint4& ua, uint4& ub) {
         uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
@@ -1332,9 +1334,9 @@ __global__ void __launch_bounds__(kPrepThreads) sm_prep_kernel(const __grid_cons
       part[qq * 128 + c] = sum;
     }
     __syncthreads();  // every read of buffer b is done: it takes the tile after next
-    if (tid == 0 && i + 2 * G < p.ntiles) {
+    if (tid == 0 && bh + 2 * p.S < p.BH) {
       fence_proxy_async_smem();
-      issue(i + 2 * G, b);
+      issue(bh + 2 * p.S, b);
     }
     float* st = p.kstat + ((size_t)bh * p.nt + tile) * kSmStat;
     if (tid < 128) {
@@ -1485,12 +1487,16 @@ cudaError_t launch_sm_prep(const void* q, const void* k, const void* v, void* yq
   p.status = status;
   p.N = N;
   p.nt = nt;
-  p.ntiles = (int)ntiles;
+  p.BH = BH;
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int grid = (int)(ntiles < 2ll * sms ? ntiles : 2ll * sms);  // two CTAs per SM
-  sm_prep_kernel<<<grid, kPrepThreads, PrepSmem::BYTES, stream>>>(p);
+  // S CTAs per tile position, about two CTAs per SM in all (at least one per position)
+  const int S = std::max(1, std::min(BH, 2 * sms / nt));
+  p.S = S;
+  const long long grid = (long long)nt * S;
+  if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+  sm_prep_kernel<<<(unsigned)grid, kPrepThreads, PrepSmem::BYTES, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }
