@@ -53,7 +53,7 @@ MEASURED_TRAFFIC = {"1f36bff999f6dfd8": 33603072 + 0 + 111619840 + 9410304}
 # the ZeroS-SM workload's dominant kernel (sm1_kernel): DRAM bytes read + written per launch
 SM_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_sm.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
               "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_SM_TRAFFIC = {"57337719dfee95a5": 166423552 + 15833600}
+MEASURED_SM_TRAFFIC = {"72bcbcc9246ff7f2": 180504064 + 17020416}
 
 
 def kernel_fingerprint(sources=None) -> str:
