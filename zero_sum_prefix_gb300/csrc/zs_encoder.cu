@@ -729,13 +729,40 @@ __global__ void __launch_bounds__(kTcThreads, 2) enc_tc_kernel(FwdArgs a) {
         o[j] = __fmaf_rn((o[j] - mu_r) * rstd, w, b);
       }
     }
-    if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(out + (size_t)t * kD) + 4 * hf;
+    {
+      // the row's 64 output bytes as four 16-byte chunks, transposed within each group of four
+      // lanes (rows 4g .. 4g + 3 of the warp) so that each store instruction writes whole 64-byte
+      // row segments of eight rows: afterwards lane 4g + j holds chunk j of the row 4g + k in x[k]
+      uint4 x[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        dst[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
-                            pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
-                            pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+        x[c] = make_uint4(pack_bf16x2(o[8 * c], o[8 * c + 1]), pack_bf16x2(o[8 * c + 2], o[8 * c + 3]),
+                          pack_bf16x2(o[8 * c + 4], o[8 * c + 5]),
+                          pack_bf16x2(o[8 * c + 6], o[8 * c + 7]));
+      const int lane = tid & 31, j = lane & 3;
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        const bool up = (j & m) != 0;
+#pragma unroll
+        for (int s0 = 0; s0 < 4; ++s0) {
+          if (s0 & m) continue;  // the pair (s0, s0 | m)
+          const uint4 send = up ? x[s0] : x[s0 | m];
+          uint4 recv;
+          recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+          recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+          recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+          recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+          if (up)
+            x[s0] = recv;
+          else
+            x[s0 | m] = recv;
+        }
+      }
+      const int t4 = t - (lane & 3);  // token of the group's first row
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (t4 + k < N)
+          reinterpret_cast<uint4*>(out + (size_t)(t4 + k) * kD)[4 * hf + j] = x[k];
     }
     tc_fence_before();
     __syncthreads();  // D3 read and the q tile consumed before the next tile
