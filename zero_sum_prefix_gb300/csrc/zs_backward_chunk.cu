@@ -18,7 +18,7 @@
 //           D^G_c, D^H_c): Y = V D^T, Z = K D;  dk_hat += e Y_F + s Y_G + Y_H,
 //           dv += e Z_F + s Z_G + Z_H, ds += e v.Z_F + v.Z_G.
 // The chunk-start and suffix states come from bwd_states_kernel (one pass over the chunks in
-// each direction, the value columns split over four CTAs); the E and P terms of ds, the gate
+// each direction, all value columns in one CTA); the E and P terms of ds, the gate
 // gradients' companions and du, d mu, d tau from bwd_ds_kernel and bwd_du_kernel (scans over
 // the tokens).
 // The per-token s, E e^{-m}, P and m are those of the forward kernels (their debug outputs).
@@ -43,8 +43,6 @@ constexpr int kD = 64;        // head dimension of the chunked path
 constexpr int kCk = 64;       // tokens per chunk
 constexpr int kNT = 256;      // threads per CTA
 constexpr int kLD = tiles::kLD;  // padded row stride of the fp32 tiles
-constexpr int kSlices = 4;    // value-column slices of the state kernel
-constexpr int kSW = kD / kSlices;
 
 // Scratch layout (fp32), shared with the host: per-token forward scalars, the two state sets,
 // per-token backward scalars, the prior means.
@@ -118,43 +116,56 @@ __global__ void __launch_bounds__(kNT) bwd_rows_kernel(BwdArgs a, BwdChunkScratc
 }
 
 // ================================================================== chunk states
-// grid (BH, slices, 2): z = 0 stores the chunk-start forward states F~_c, G_c, H_c (F~ relative
-// to M_{c-1}) going forward; z = 1 stores the suffix states D~F_c (relative to M_c), D^G_c, D^H_c
-// going backward.  Columns j0 .. j0 + 15 of each d x d state; thread (a = tid / 4, 4 columns).
-// The next chunk's rows, value slice and scalars are loaded into registers while the current
-// chunk is accumulated.
+// grid (BH, 1, 2): z = 0 stores the chunk-start forward states F~_c, G_c, H_c (F~ relative to
+// M_{c-1}) going forward; z = 1 stores the suffix states D~F_c (relative to M_c), D^G_c, D^H_c
+// going backward.  Thread (ar = tid / 16, cj = tid % 16) holds rows 4 ar .. 4 ar + 3 and columns
+// 4 cj .. 4 cj + 3 of each d x d state (48 accumulators: per token 16 products and 48
+// multiply-adds against three 16-byte shared-memory loads).  The next chunk's rows, values and
+// scalars are loaded into registers while the current chunk is accumulated.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  float4 r;
+  r.x = __uint_as_float(w.x << 16);
+  r.y = __uint_as_float(w.x & 0xffff0000u);
+  r.z = __uint_as_float(w.y << 16);
+  r.w = __uint_as_float(w.y & 0xffff0000u);
+  return r;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScratch sc) {
   __shared__ __align__(16) float rows[kCk][kD];  // k_hat (z = 0) or q_hat (z = 1) of the chunk
-  __shared__ __align__(16) float cols[kCk][kSW];  // v or do slice
-  __shared__ float cf[kCk][3];                    // per-token weights of the three states
-  __shared__ float fac;                           // rescale of the F~ state
-  const int bh = blockIdx.x, j0 = blockIdx.y * kSW, dir = blockIdx.z;
+  __shared__ __align__(16) float cols[kCk][kD];  // v or do of the chunk
+  __shared__ __align__(16) float cf[kCk][4];     // per-token weights of the three states
+  __shared__ float fac;                          // rescale of the F~ state
+  const int bh = blockIdx.x, dir = blockIdx.z;
   const int N = a.N, NC = (N + kCk - 1) / kCk;
   const int tid = threadIdx.x;
-  const int ar = tid >> 2, cj = (tid & 3) * 4;
+  const int ar = tid >> 4, cj = tid & 15;
   const size_t row0 = (size_t)bh * N;
   const float* __restrict__ hat = (dir == 0 ? sc.khat : sc.qhat) + row0 * kD;
   const T* __restrict__ val = static_cast<const T*>(dir == 0 ? a.v : a.dout) + row0 * kD;
-  float st[3][4];
+  float st[3][4][4];
 #pragma unroll
   for (int m = 0; m < 3; ++m)
 #pragma unroll
-    for (int x = 0; x < 4; ++x) st[m][x] = 0.0f;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st[m][i][j] = 0.0f;
   float* out = dir == 0 ? sc.fs : sc.ds;
-  // prefetch registers: 16 row values, 4 values of the slice, the token's weights, M_c, M_{c-1}
-  float4 pr[4];
-  float pv[4], pw[3], pMc = 0.0f, pMp = 0.0f;
+  // prefetch registers: 16 row values, 16 values, the token's weights, M_c, M_{c-1}
+  float4 pr[4], pv[4];
+  float pw[3], pMc = 0.0f, pMp = 0.0f;
   auto fetch = [&](int c) {
     const int t0 = c * kCk, tn = min(N, t0 + kCk) - t0;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int e = tid + kNT * x, r = e / (kD / 4);
-      pr[x] = r < tn ? reinterpret_cast<const float4*>(hat + (size_t)t0 * kD)[e]
-                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      pr[x] = r < tn ? reinterpret_cast<const float4*>(hat + (size_t)t0 * kD)[e] : z;
+      pv[x] = r < tn ? ld4(val + (size_t)t0 * kD + 4 * (size_t)e) : z;
     }
-#pragma unroll
-    for (int y = 0; y < 4; ++y) pv[y] = ar < tn ? ld(val, (size_t)(t0 + ar) * kD + j0 + cj + y) : 0.0f;
     pMc = sc.m[row0 + t0 + tn - 1];
     pMp = c > 0 ? sc.m[row0 + t0 - 1] : 0.0f;
     pw[0] = pw[1] = pw[2] = 0.0f;
@@ -180,37 +191,52 @@ __global__ void __launch_bounds__(kNT) bwd_states_kernel(BwdArgs a, BwdChunkScra
     float* dst = out + (((size_t)bh * NC + c) * 3) * kD * kD;
 #pragma unroll
     for (int m = 0; m < 3; ++m)
-      *reinterpret_cast<float4*>(dst + (size_t)m * kD * kD + ar * kD + j0 + cj) =
-          make_float4(st[m][0], st[m][1], st[m][2], st[m][3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(dst + (size_t)m * kD * kD + (4 * ar + i) * kD + 4 * cj) =
+            make_float4(st[m][i][0], st[m][i][1], st[m][i][2], st[m][i][3]);
     if (c == last) break;
     const int tn = min(N, c * kCk + kCk) - c * kCk;
 #pragma unroll
-    for (int x = 0; x < 4; ++x) reinterpret_cast<float4*>(&rows[0][0])[tid + kNT * x] = pr[x];
-    *reinterpret_cast<float4*>(&cols[ar][cj]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
-    if (tid < kCk) {
-      cf[tid][0] = pw[0];
-      cf[tid][1] = pw[1];
-      cf[tid][2] = pw[2];
+    for (int x = 0; x < 4; ++x) {
+      reinterpret_cast<float4*>(&rows[0][0])[tid + kNT * x] = pr[x];
+      reinterpret_cast<float4*>(&cols[0][0])[tid + kNT * x] = pv[x];
     }
+    if (tid < kCk) *reinterpret_cast<float4*>(&cf[tid][0]) = make_float4(pw[0], pw[1], pw[2], 0.0f);
     if (tid == 0) fac = (dir == 0 && c == 0) ? 0.0f : expf(__fsub_rn(pMp, pMc));
     __syncthreads();
     const int nxt = dir == 0 ? c + 1 : c - 1;
     if (nxt != last) fetch(nxt);  // in flight while this chunk is accumulated
     const float f = fac;
 #pragma unroll
-    for (int x = 0; x < 4; ++x) st[0][x] = __fmul_rn(st[0][x], f);
-#pragma unroll 4
-    for (int r = 0; r < tn; ++r) {
-      const float ka = rows[r][ar];
-      const float4 vv = *reinterpret_cast<const float4*>(&cols[r][cj]);
-      const float kv[4] = {__fmul_rn(ka, vv.x), __fmul_rn(ka, vv.y), __fmul_rn(ka, vv.z),
-                           __fmul_rn(ka, vv.w)};
-      const float w0 = cf[r][0], w1 = cf[r][1], w2 = cf[r][2];
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        st[0][x] = __fmaf_rn(w0, kv[x], st[0][x]);
-        st[1][x] = __fmaf_rn(w1, kv[x], st[1][x]);
-        st[2][x] = __fmaf_rn(w2, kv[x], st[2][x]);
+      for (int j = 0; j < 4; ++j) st[0][i][j] = __fmul_rn(st[0][i][j], f);
+#pragma unroll 2
+    for (int r = 0; r < tn; ++r) {
+      // packed fp32 pairs (columns j, j + 1): the same roundings as scalar products and fmas
+      const float4 k4 = *reinterpret_cast<const float4*>(&rows[r][4 * ar]);
+      const float4 v4 = *reinterpret_cast<const float4*>(&cols[r][4 * cj]);
+      const float4 w = *reinterpret_cast<const float4*>(&cf[r][0]);
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      const float2 v01 = make_float2(v4.x, v4.y), v23 = make_float2(v4.z, v4.w);
+      const float2 w0 = make_float2(w.x, w.x), w1 = make_float2(w.y, w.y), w2 = make_float2(w.z, w.z);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 ki = make_float2(kk[i], kk[i]);
+        const float2 kv[2] = {__fmul2_rn(ki, v01), __fmul2_rn(ki, v23)};
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          float2 a0 = make_float2(st[0][i][2 * jp], st[0][i][2 * jp + 1]);
+          float2 a1 = make_float2(st[1][i][2 * jp], st[1][i][2 * jp + 1]);
+          float2 a2 = make_float2(st[2][i][2 * jp], st[2][i][2 * jp + 1]);
+          a0 = __ffma2_rn(w0, kv[jp], a0);
+          a1 = __ffma2_rn(w1, kv[jp], a1);
+          a2 = __ffma2_rn(w2, kv[jp], a2);
+          st[0][i][2 * jp] = a0.x; st[0][i][2 * jp + 1] = a0.y;
+          st[1][i][2 * jp] = a1.x; st[1][i][2 * jp + 1] = a1.y;
+          st[2][i][2 * jp] = a2.x; st[2][i][2 * jp + 1] = a2.y;
+        }
       }
     }
     __syncthreads();
@@ -660,7 +686,7 @@ cudaError_t launch_chunk_t(const BwdArgs& a, const BwdChunkScratch& sc, cudaStre
   const size_t warps = 2 * (size_t)BH * a.N;
   const size_t rb = (warps * 32 + kNT - 1) / kNT;
   bwd_rows_kernel<T><<<(unsigned)(rb < 152 * 32 ? rb : 152 * 32), kNT, 0, stream>>>(a, sc);
-  bwd_states_kernel<T><<<dim3(BH, kSlices, 2), kNT, 0, stream>>>(a, sc);
+  bwd_states_kernel<T><<<dim3(BH, 1, 2), kNT, 0, stream>>>(a, sc);
   bwd_chunk_kernel<T><<<(unsigned)(BH * NC), kNT, ChunkSmem::BYTES, stream>>>(a, sc);
   bwd_ds_kernel<<<BH, kNT, 0, stream>>>(a, sc);
   bwd_du_kernel<T><<<dim3(BH, kD / kCols), kSeg * kCols, 0, stream>>>(a, sc);
