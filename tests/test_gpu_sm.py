@@ -79,6 +79,25 @@ def test_sm_full_size(zs):
     assert oc.float().abs().max().item() < 2e-2
 
 
+@pytest.mark.parametrize("causal,rope,gate0,N", [
+    (True, True, False, 300), (True, False, True, 257), (False, True, True, 300),
+    (False, False, False, 129)])
+def test_sm_many_query_tiles_per_cta(zs, causal, rope, gate0, N):
+    """d = 64 with more query tiles than CTAs (B8 H16: 256 to 384 tiles of 128 queries), so that
+    each CTA of the d = 64 kernel takes several of them, of different key-tile counts, in a row:
+    every sequence against the oracle."""
+    B, H, d = 8, 16, 64
+    x = _inputs(B, H, N, d, 3100 + N)
+    g0 = _g0((B, H, N), 31) if gate0 else None
+    o = zs.sm_fwd(x["q"], x["k"], x["v"], x["g1"], x["gh"], causal=causal, rope=rope,
+                  rope_base=10000.0, g0=g0)
+    assert zs.get_status() == 0
+    ref = oracle.sm(*(x[n].cpu() for n in ("q", "k", "v", "g1", "gh")), causal=causal,
+                    rope=rope, rope_base=10000.0, g0=None if g0 is None else g0.cpu())
+    err = seq_err(o.float().cpu().numpy().reshape(B * H, N, d), ref.reshape(B * H, N, d))
+    assert err <= TOL["bf16"], err
+
+
 def test_sm_zero_order_gate_constant_values(zs):
     """With the zero-order gate the weights of query t sum to sig0_t: constant values c give
     o_t = sig0_t c."""
