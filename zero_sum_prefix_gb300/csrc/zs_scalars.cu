@@ -169,30 +169,42 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
       }
     }
     cluster_sync_all();
-    // ---- B: column carry at the start of every block of the segment (block order) ----
+    // ---- B: column carry at the start of every block of the segment (block order); the sums
+    //      of the next 8 blocks are loaded while the chain runs over the current 8 ----
     if (w == 0) {
+      constexpr int G = 8;
+      static_assert(SEG % (2 * G) == 0, "whole pairs of groups per segment");
       float2 Cc[RP];
 #pragma unroll
       for (int x = 0; x < RP; ++x) Cc[x] = Cseg[x];
-#pragma unroll 1
-      for (int g0 = 0; g0 < SEG; g0 += 8) {
-        float2 le[8][RP];  // the next 8 blocks' sums, loaded before the chain uses them
+      float2 la[G][RP], lb[G][RP];
+      auto load_group = [&](float2 (&le)[G][RP], int g0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < G; ++i)
 #pragma unroll
           for (int x = 0; x < RP; ++x)
             le[i][x] = *reinterpret_cast<const float2*>(&sm.lend[g0 + i][R * lane + 2 * x]);
+      };
+      auto chain_group = [&](const float2 (&le)[G][RP], int g0) {
+        const bool own = g0 / CB == (int)rank;  // a group of 8 lies within one CTA's blocks
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int gb = g0 + i;
-          if (gb / CB == (int)rank) {
+        for (int i = 0; i < G; ++i) {
+          if (own) {
 #pragma unroll
             for (int x = 0; x < RP; ++x)
-              *reinterpret_cast<float2*>(&sm.cw[gb % CB][R * lane + 2 * x]) = Cc[x];
+              *reinterpret_cast<float2*>(&sm.cw[(g0 + i) % CB][R * lane + 2 * x]) = Cc[x];
           }
 #pragma unroll
           for (int x = 0; x < RP; ++x) Cc[x] = __fadd2_rn(Cc[x], le[i][x]);
         }
+      };
+      load_group(la, 0);
+#pragma unroll 1
+      for (int g0 = 0; g0 < SEG; g0 += 2 * G) {
+        load_group(lb, g0 + G);
+        chain_group(la, g0);
+        if (g0 + 2 * G < SEG) load_group(la, g0 + 2 * G);
+        chain_group(lb, g0 + G);
       }
 #pragma unroll
       for (int x = 0; x < RP; ++x) Cseg[x] = Cc[x];
