@@ -49,7 +49,7 @@ L2_FLUSH_BYTES = 256 << 20
 CHUNK_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_walk.cu", "zero_sum_prefix_gb300/csrc/zs_scalars.cu",
                  "zero_sum_prefix_gb300/csrc/zs_range.cuh", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
                  "zero_sum_prefix_gb300/csrc/zs_common.cuh"]
-MEASURED_TRAFFIC = {"93e532c27061c927": 33602560 + 0 + 111803904 + 9587456}
+MEASURED_TRAFFIC = {"2990ea0b17be6957": 33602816 + 0 + 111005952 + 9714944}
 # the ZeroS-SM workload's dominant kernel (sm1_kernel): DRAM bytes read + written per launch
 SM_SOURCES = ["zero_sum_prefix_gb300/csrc/zs_sm.cu", "zero_sum_prefix_gb300/csrc/zs_sm100.cuh",
               "zero_sum_prefix_gb300/csrc/zs_common.cuh"]

@@ -35,7 +35,7 @@ __device__ __forceinline__ float seq_smax(const FwdArgs& a, int bh) {
   float m = 0.0f;
   if (a.smax) {
 #pragma unroll
-    for (int r = 0; r < kScalarCtas; ++r) m = fmaxf(m, a.smax[(size_t)bh * kScalarCtas + r]);
+    for (int r = 0; r < kScalarCtas; ++r) m = fmaxf(m, __ldcg(a.smax + (size_t)bh * kScalarCtas + r));
   }
   return m;
 }

@@ -425,6 +425,7 @@ __global__ void __cluster_dims__(kScCN, 1, 1) __launch_bounds__(kScW * 32, D == 
     if (threadIdx.x == 0) a.smax[(size_t)bh * kScCN + rank] = __int_as_float(sm.smax_bits);
   }
   // (no remote access follows the last cluster barrier)
+  grid_dep_launch();  // the forward kernel may be scheduled; it waits for this grid's completion
 }
 
 

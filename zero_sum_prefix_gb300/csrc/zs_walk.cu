@@ -17,7 +17,9 @@
 //     state^T += [e v | s v]^T K  and  [v | e v]^T K    (F~ rescaled by e^{M_{c-1} - M_c} first)
 // The weight is formed in fp32 before the product is rounded: its three terms nearly cancel
 // (the weights of a query sum to zero).  The scalars s, m, Et = E e^{-m}, P of every token come
-// from the scalar pass (zs_scalars.cu, the canonical blocked fp32 order), which runs first.
+// from the scalar pass (zs_scalars.cu, the canonical blocked fp32 order), which runs first; this
+// kernel is launched as its programmatic dependent, so it sets up its barriers and tensor memory
+// while the pass ends and waits for the pass (grid_dep_wait) before any role starts.
 //
 // Operand precision.  Every tensor-core operand is fp16 (fp32 accumulation): the unit vectors,
 // S and the value-side tiles have 11 significant bits instead of bf16's 8, which is what the
@@ -150,9 +152,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// The scalar pass's output is read through L2 only (ld.global.cg): this kernel is launched as a
+// programmatic dependent of that pass and may start while it still writes the buffer, so no read
+// may be served from a line cached before its grid_dep_wait().
+__device__ __forceinline__ float4 scal_at(const float4* scal, int i) { return __ldcg(scal + i); }
+
 // Running maximum at the last token of chunk c (the chunk reference M_c).
 __device__ __forceinline__ float chunk_ref(const float4* scal, int c, int N) {
-  return scal[min(N, (c + 1) * kC) - 1].y;
+  return scal_at(scal, min(N, (c + 1) * kC) - 1).y;
 }
 
 // Scale exponent of the state copy that feeds chunk c's Q [F~|G|H] product.
@@ -277,7 +284,7 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
   const bool rope = a.rope != 0;
   // rotary frequencies of this half's 16 pairs (pairs 16 hf .. 16 hf + 15), in shared memory
   const uint32_t th_s = base + WLay::THETA + 64 * hf;
-  const float M_ref = c0 > 0 ? scal[c0 * kC - 1].y : 0.0f;  // replay reference
+  const float M_ref = c0 > 0 ? scal_at(scal, c0 * kC - 1).y : 0.0f;  // replay reference
   const int ks = s_exp(a, bh);
   const float sinv = pow2f(-ks);
   const float smax_seq = seq_smax(a, bh);  // the sequence's largest |s| (bounds a row's weights)
@@ -288,7 +295,7 @@ __device__ void role_op(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, i
       o.M = cc >= c0 ? chunk_ref(scal, cc, N) : M_ref;
       const int i = cc * kC + r;
       if (i < N) {
-        o.sc = scal[i];
+        o.sc = scal_at(scal, i);
         if (cc >= c0 && hf == 1) {
           o.x1 = a.g1[row0 + i];
           o.xh = a.gh[row0 + i];
@@ -696,7 +703,7 @@ __device__ void role_e(const WalkParams& p, uint8_t* smem, WMisc* ms, int bh, in
   float Mc = chunk_ref(scal, c0, N);
   float Mn = c0 + 1 < c1 ? chunk_ref(scal, c0 + 1, N) : 0.0f;
   // the running maximum at the token before the current chunk (the B tile's F~ reference)
-  float Mp = c0 > 0 ? scal[c0 * kC - 1].y : 0.0f;
+  float Mp = c0 > 0 ? scal_at(scal, c0 * kC - 1).y : 0.0f;
   bool ok = true;
   // the copy after the last replayed update (reference: the running maximum before c0)
   if (c0 > 0)
@@ -955,6 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the scalar pass: every read of its output follows
+  grid_dep_wait();
 
   if (warp < kOpWarps) {
     role_op(p, smem, ms, bh, c0, c1);
@@ -1093,8 +1102,19 @@ cudaError_t launch_walk(const FwdArgs& a, const float* ang, int nseg_max, cudaSt
   for (int j = S + 1; j <= kMaxSeg; ++j) p.seg_start[j] = nch;
   const long long ctas = (long long)BH * S;
   if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
-  walk_kernel<<<(unsigned)ctas, kThreads, WLay::BYTES, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = WLay::BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, walk_kernel, p);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
